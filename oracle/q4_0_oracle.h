@@ -1,0 +1,72 @@
+/*
+ * CPU oracle for Q4_0 dequantisation and MUL_MAT -- TEST INFRASTRUCTURE ONLY.
+ *
+ * Only the tests, the smoke check and the benchmark's CPU-baseline leg may
+ * load this code.  It shares nothing with the CUDA library: no headers, no
+ * helpers, no tables.
+ *
+ * What it computes, and where that is defined:
+ *  - block_q4_0 is an fp16 scale d followed by uint8_t qs[16] holding 32
+ *    four-bit codes, two per byte ("Binding GGUF weights to the compute
+ *    graph", section 2.3, the block_q4_0 struct).  A block is 18 bytes; a row of K weights is K/32
+ *    blocks, so a quantised tensor takes M*K/32*18 bytes, not M*K*bits/8
+ *    (same section, the ggml_nbytes note).
+ *  - Each code q maps back to w = s*(q - z) ("Architecture and module
+ *    overview", weight-loading section, the block-quantisation formula); for
+ *    Q4_0, s = d and z = 8, the low nibble of qs[j] is element j and the high
+ *    nibble is element j+16 (the fixed Q4_0 convention of the method).
+ *  - MUL_MAT takes the quantised weight W with ne = [K, M] and activations b
+ *    with ne = [K, N], and dequantises inside the operator ("GGUF loading,
+ *    mmap and tensor placement", step six, the MUL_MAT probe; section 2.3
+ *    above).  The result Y has ne = [M, N]: Y[n][m] = sum_k w[m][k]*x[n][k].
+ *
+ * Precision: the scale is decoded exactly from its IEEE-754 binary16 fields;
+ * w = d*(q-8) is formed in fp32 (exact: 11 significant bits times at most
+ * 4 bits); products and sums of MUL_MAT are taken in fp64 in plain k order.
+ *
+ * Every function here is pinned by the CPU tests (hand-derived block
+ * fixtures, all 65536 binary16 patterns against numpy, one-hot columns,
+ * exact special cases, brute force against a dense fp64 matmul).
+ */
+#ifndef Q4_0_ORACLE_H
+#define Q4_0_ORACLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Bytes of a Q4_0 matrix of M rows and K columns (K a multiple of 32). */
+size_t oracle_q4_0_nbytes(int64_t M, int64_t K);
+
+/* Exact value of an IEEE-754 binary16 bit pattern (subnormals, inf, NaN). */
+double oracle_half_to_double(uint16_t h);
+
+/* n patterns -> n fp32 values (binary16 values are all exact in fp32). */
+void oracle_half_to_float_n(const uint16_t *h, size_t n, float *out);
+
+/* Dequantise M rows of K/32 blocks each into out[M][K] (fp32). */
+void oracle_dequant_q4_0(const uint8_t *W, int64_t M, int64_t K, float *out);
+
+/*
+ * MUL_MAT against Q4_0 weights:
+ *   Y[n][m] = sum_k w[m][k] * X[n][k]       (fp64, k ascending)
+ *   S[n][m] = sum_k |w[m][k] * X[n][k]|     (fp64; the tolerance scale)
+ * W: M rows of K/32 blocks; X: [N][K] fp32; Y, S: [N][M] fp64.
+ * nthreads > 1 splits the rows m over OpenMP threads; each output is still
+ * one sequential sum, so the results do not depend on nthreads.
+ */
+void oracle_mul_mat_q4_0(const uint8_t *W, int64_t M, int64_t K,
+                         const float *X, int64_t N,
+                         double *Y, double *S, int nthreads);
+
+/* Number of threads OpenMP would use by default (1 without OpenMP). */
+int oracle_max_threads(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif

@@ -1,0 +1,94 @@
+"""Seeded synthetic inputs shared by the oracle-side tests and the CUDA path.
+
+This module only draws random numbers and lays them out as raw bytes; it holds
+none of the Q4_0 arithmetic (no decoding, no products).  Both sides of every
+parity check read the arrays it returns.
+
+Workload shapes follow the 7B-like model on the pages ("Binding GGUF weights to the
+compute graph", section 2.4: per-layer q/k/v/o, gate/up/down projections) and the
+capability probe batch of 512 tokens ("GGUF loading, mmap and tensor placement",
+step six).  Value distributions:
+
+* ``qs``: uniform random bytes (all 256 values, so every 4-bit code appears);
+* ``d``: fp16 (round-to-nearest-even) of U[0.005, 0.02] drawn in fp64;
+* activations: fp32 N(0, 1).
+
+Random bits come from numpy's SFC64 generator (``random_raw``), whose output
+stream is fixed by its published definition, so the same seed yields the same
+bytes on x86-64 and aarch64.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+QK4_0 = 32           # weights per block_q4_0
+BLOCK_BYTES = 18     # ggml_half d (2 bytes) + uint8_t qs[16]
+
+# Matrix ids inside one 7B-like layer, in graph order.
+LAYER_MATRICES = (
+    ("attn_q", 4096, 4096),
+    ("attn_k", 4096, 4096),
+    ("attn_v", 4096, 4096),
+    ("attn_output", 4096, 4096),
+    ("ffn_gate", 11008, 4096),
+    ("ffn_up", 11008, 4096),
+    ("ffn_down", 4096, 11008),
+)
+N_LAYERS = 32
+
+
+def seed_for(workload: int, matrix: int, layer: int = 0) -> int:
+    """Seed of one matrix of one workload (stable across runs)."""
+    return 0x51A00000 + 16 * workload + matrix + 1000 * layer
+
+
+def _raw_u64(seed: int, n_words: int) -> np.ndarray:
+    return np.random.SFC64(seed).random_raw(n_words)
+
+
+def random_bytes(seed: int, n: int) -> np.ndarray:
+    words = _raw_u64(seed, (n + 7) // 8)
+    return words.view(np.uint8)[:n]
+
+
+def random_scales(seed: int, n: int, lo: float = 0.005, hi: float = 0.02) -> np.ndarray:
+    """n fp16 scales: round-to-nearest-even of U[lo, hi] drawn in fp64."""
+    rng = np.random.Generator(np.random.SFC64(seed ^ 0x5CA1E))
+    u = rng.random(n, dtype=np.float64) * (hi - lo) + lo
+    return u.astype("<f2")
+
+
+def q4_0_weights(M: int, K: int, seed: int) -> np.ndarray:
+    """A Q4_0 weight matrix with M rows of K weights, as raw bytes.
+
+    Shape ``[M, K/32*18]`` uint8: row m is K/32 consecutive 18-byte blocks, each
+    the little-endian fp16 scale followed by 16 bytes of packed codes.
+    """
+    if K % QK4_0:
+        raise ValueError("K must be a multiple of 32")
+    nb = K // QK4_0
+    out = np.empty((M, nb, BLOCK_BYTES), dtype=np.uint8)
+    out[:, :, 2:] = random_bytes(seed, M * nb * 16).reshape(M, nb, 16)
+    out[:, :, 0:2] = random_scales(seed, M * nb).view(np.uint8).reshape(M, nb, 2)
+    return out.reshape(M, nb * BLOCK_BYTES)
+
+
+def activations(N: int, K: int, seed: int) -> np.ndarray:
+    """fp32 N(0,1) activations, shape [N, K] (K innermost, as ggml ne[0])."""
+    rng = np.random.Generator(np.random.SFC64(seed ^ 0xAC7))
+    return rng.standard_normal((N, K), dtype=np.float32)
+
+
+def blocks_from_parts(d_bits: np.ndarray, qs: np.ndarray) -> np.ndarray:
+    """Assemble blocks from explicit fp16 bit patterns and code bytes.
+
+    ``d_bits``: uint16 ``[M, nb]``; ``qs``: uint8 ``[M, nb, 16]``.  Returns the
+    ``[M, nb*18]`` byte matrix.  Used for hand-built edge cases.
+    """
+    d_bits = np.asarray(d_bits, dtype="<u2")
+    qs = np.asarray(qs, dtype=np.uint8)
+    M, nb = d_bits.shape
+    out = np.empty((M, nb, BLOCK_BYTES), dtype=np.uint8)
+    out[:, :, 0:2] = d_bits.view(np.uint8).reshape(M, nb, 2)
+    out[:, :, 2:] = qs
+    return out.reshape(M, nb * BLOCK_BYTES)
