@@ -1,0 +1,110 @@
+/*
+ * gq -- MUL_MAT against block-quantised Q4_0 weights on NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("GGUF loading, mmap and tensor placement", step six, the
+ * MUL_MAT probe; "ggml compute graph and memory allocator", the ggml_tensor
+ * section on ne/nb):
+ *   W  quantised weight, ggml ne = [K, M]: M rows, each K/32 block_q4_0.
+ *   X  activations, F32, ne = [K, N]: N rows of K floats (K innermost).
+ *   Y  result, F32, ne = [M, N]: Y[n][m] = sum_k w[m][k] * X[n][k].
+ * block_q4_0 ("Binding GGUF weights to the compute graph", section 2.3): an
+ * IEEE binary16 scale d (little-endian) followed by uint8_t qs[16]; 18 bytes
+ * per 32 weights.  The low nibble of qs[j] is code q of element j, the high
+ * nibble that of element j+16, and w = d*(q - 8) ("Architecture and module
+ * overview", weight-loading section: w = s*(q - z)).  Dequantisation happens
+ * inside the operator (section 2.3 above); W is never expanded in memory.
+ *
+ * Conventions for every entry point:
+ *  - Pointers to tensors are DEVICE pointers owned by the caller; the library
+ *    never frees or retains them.  Rows are contiguous: W row stride is
+ *    K/32*18 bytes, X row stride K floats, Y row stride M floats.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
+ *    enqueued asynchronously on it; the call returns after enqueueing.
+ *  - The return value reports argument errors and launch errors found while
+ *    enqueueing.  A device-side fault detected later (a bounded wait inside a
+ *    kernel that gave up) is reported by gq_sync_status().
+ *  - M or N equal to 0 is a no-op that returns GQ_OK; K equal to 0 (an empty
+ *    sum) writes zeros to Y.
+ *  - Non-finite scales or activations propagate as IEEE arithmetic does; they
+ *    are not validated.
+ *  - No C++ exception crosses this interface.  Thread-safe for calls on
+ *    different streams; gq_last_error() is per thread.
+ */
+#ifndef GQ_H
+#define GQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GQ_OK = 0,
+  GQ_ERR_NULL = -1,            /* a required pointer is NULL */
+  GQ_ERR_SHAPE = -2,           /* negative size, K % 32 != 0, or a size overflows */
+  GQ_ERR_ALIGN = -3,           /* pointer alignment the entry point requires is missing */
+  GQ_ERR_CUDA = -4,            /* a CUDA runtime call or kernel launch failed */
+  GQ_ERR_ALLOC = -5,           /* stream-ordered scratch allocation failed */
+  GQ_ERR_DEVICE_TIMEOUT = -6,  /* a kernel's bounded wait gave up (see gq_sync_status) */
+  GQ_ERR_UNSUPPORTED = -7      /* current device is not compute capability 10.3 */
+} gq_status;
+
+/* Bytes of a Q4_0 matrix of M rows and K columns: M*(K/32)*18
+ * ("Binding GGUF weights to the compute graph", section 2.3, ggml_nbytes note).
+ * Returns 0 for K % 32 != 0 or negative sizes. */
+size_t gq_q4_0_nbytes(int64_t M, int64_t K);
+
+/* Dequantise W (M x K, Q4_0) into out[M][K] fp32.  Bit-exact: every output is
+ * the fp32 value d*(q-8), including the sign of zero.  No alignment needed
+ * (16-byte aligned W and out take the vectorised kernel). */
+gq_status gq_dequant_q4_0(const void *W, int64_t M, int64_t K, float *out, void *stream);
+
+/* Y[N][M] = X[N][K] * W^T with W in Q4_0, fp32 in and out (see header).
+ * Dispatch by N: N < 64 streams W through the decode kernel (fp16 x, exact
+ * integer codes, fp32 block scales and accumulation); N >= 64 converts X to
+ * bf16 once and runs the tcgen05 tensor-core kernel on bf16 tiles of the
+ * dequantised W with fp32 accumulation.  Fast paths need K % 256 == 0 and W,
+ * X, Y 16-byte aligned; other shapes take a slower generic kernel.  The N >= 64
+ * path allocates N*K*2 bytes of stream-ordered scratch (cudaMallocAsync) and
+ * frees it on the same stream.  Accuracy: |y - y_ref| <= 1e-3*sum_k|w_k x_k|
+ * + 1e-5 on the synthetic workloads (random-sign data). */
+gq_status gq_mul_mat_q4_0(const void *W, int64_t M, int64_t K, const float *X, int64_t N, float *Y,
+                          void *stream);
+
+/* MUL_MAT with activations the caller already holds in bf16: X_bf16[N][K]
+ * (raw bfloat16 bits).  Runs the tensor-core kernel for every N >= 1 and
+ * allocates nothing.  Needs K % 256 == 0, W and X_bf16 16-byte aligned. */
+gq_status gq_mul_mat_q4_0_bf16x(const void *W, int64_t M, int64_t K, const uint16_t *X_bf16, int64_t N,
+                                float *Y, void *stream);
+
+/* y[i] = bf16(x[i]), round to nearest even (NaN stays NaN), for n elements. */
+gq_status gq_f32_to_bf16(const float *x, uint16_t *y, int64_t n, void *stream);
+
+/* Synchronise `stream`, then read and clear the device error word.  Returns
+ * GQ_ERR_DEVICE_TIMEOUT if a kernel's bounded wait gave up since the last
+ * call, GQ_ERR_CUDA if the synchronisation failed, else GQ_OK. */
+gq_status gq_sync_status(void *stream);
+
+/* Tuning / test options (process-wide). */
+typedef enum {
+  GQ_OPT_PREFILL_MIN_N = 0,  /* N at which mul_mat switches to the tensor-core path (default 64) */
+  GQ_OPT_FORCE_GENERIC = 1,  /* 1: every mul_mat takes the generic kernel (test aid) */
+  GQ_OPT_WAIT_LIMIT_NS = 2   /* bound on any in-kernel wait, nanoseconds (default 2e9) */
+} gq_option;
+gq_status gq_set_option(gq_option opt, int64_t value);
+int64_t gq_get_option(gq_option opt);
+
+/* Human-readable text of the last error on this thread ("" if none). */
+const char *gq_last_error(void);
+const char *gq_status_string(gq_status s);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int gq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQ_H */

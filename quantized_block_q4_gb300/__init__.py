@@ -1,0 +1,174 @@
+"""Python binding of the gq C ABI (``include/gq.h``): Q4_0 MUL_MAT on GB300.
+
+Argument marshalling only: every step of dequantisation and MUL_MAT runs in the
+CUDA kernels of ``libgq.so``.  PyTorch is used for device memory and streams.
+The functions named ``gq_*`` mirror the C entry points one to one and take
+torch CUDA tensors (or raw device addresses as ints); ``dequant_q4_0`` and
+``mul_mat_q4_0`` are conveniences that allocate their outputs with torch.
+
+If ``libgq.so`` is missing this module refuses to import: there is no CPU or
+PyTorch fallback.  Build it with ``python quantized_block_q4_gb300/build.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgq.so")
+
+GQ_OK = 0
+GQ_ERR_NULL = -1
+GQ_ERR_SHAPE = -2
+GQ_ERR_ALIGN = -3
+GQ_ERR_CUDA = -4
+GQ_ERR_ALLOC = -5
+GQ_ERR_DEVICE_TIMEOUT = -6
+GQ_ERR_UNSUPPORTED = -7
+
+GQ_OPT_PREFILL_MIN_N = 0
+GQ_OPT_FORCE_GENERIC = 1
+GQ_OPT_WAIT_LIMIT_NS = 2
+
+# Every symbol include/gq.h declares, with (restype, argtypes).
+_i64, _sz, _vp, _i32 = ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int
+SIGNATURES = {
+    "gq_q4_0_nbytes": (_sz, [_i64, _i64]),
+    "gq_dequant_q4_0": (_i32, [_vp, _i64, _i64, _vp, _vp]),
+    "gq_mul_mat_q4_0": (_i32, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
+    "gq_mul_mat_q4_0_bf16x": (_i32, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
+    "gq_f32_to_bf16": (_i32, [_vp, _vp, _i64, _vp]),
+    "gq_sync_status": (_i32, [_vp]),
+    "gq_set_option": (_i32, [_i32, _i64]),
+    "gq_get_option": (_i64, [_i32]),
+    "gq_last_error": (ctypes.c_char_p, []),
+    "gq_status_string": (ctypes.c_char_p, [_i32]),
+    "gq_version": (_i32, []),
+}
+
+
+class GQError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built; run `python quantized_block_q4_gb300/build.py` "
+                          "(there is no fallback implementation)")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def _check(status: int) -> None:
+    if status != GQ_OK:
+        name = _lib.gq_status_string(status).decode()
+        raise GQError(status, f"{name}: {_lib.gq_last_error().decode()}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch tensor or a device address")
+    if not t.is_cuda:
+        raise ValueError("tensor must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+# ---------------------------------------------------------------- C mirrors
+def gq_q4_0_nbytes(M: int, K: int) -> int:
+    return int(_lib.gq_q4_0_nbytes(M, K))
+
+
+def gq_dequant_q4_0(W, M: int, K: int, out, stream=None) -> None:
+    _check(_lib.gq_dequant_q4_0(_ptr(W), M, K, _ptr(out), _stream(stream)))
+
+
+def gq_mul_mat_q4_0(W, M: int, K: int, X, N: int, Y, stream=None) -> None:
+    _check(_lib.gq_mul_mat_q4_0(_ptr(W), M, K, _ptr(X), N, _ptr(Y), _stream(stream)))
+
+
+def gq_mul_mat_q4_0_bf16x(W, M: int, K: int, X_bf16, N: int, Y, stream=None) -> None:
+    _check(_lib.gq_mul_mat_q4_0_bf16x(_ptr(W), M, K, _ptr(X_bf16), N, _ptr(Y), _stream(stream)))
+
+
+def gq_f32_to_bf16(x, y, n: int, stream=None) -> None:
+    _check(_lib.gq_f32_to_bf16(_ptr(x), _ptr(y), n, _stream(stream)))
+
+
+def gq_sync_status(stream=None) -> None:
+    _check(_lib.gq_sync_status(_stream(stream)))
+
+
+def gq_set_option(opt: int, value: int) -> None:
+    _check(_lib.gq_set_option(opt, value))
+
+
+def gq_get_option(opt: int) -> int:
+    return int(_lib.gq_get_option(opt))
+
+
+def gq_last_error() -> str:
+    return _lib.gq_last_error().decode()
+
+
+def gq_status_string(status: int) -> str:
+    return _lib.gq_status_string(status).decode()
+
+
+def gq_version() -> int:
+    return int(_lib.gq_version())
+
+
+# ---------------------------------------------------------------- conveniences
+def _check_w(W: torch.Tensor, K: int) -> int:
+    if W.dtype != torch.uint8:
+        raise TypeError("W must be uint8 (raw block_q4_0 bytes)")
+    if K % 32 or K <= 0:
+        raise ValueError("K must be a positive multiple of 32")
+    row = K // 32 * 18
+    if W.numel() % row:
+        raise ValueError("W size is not a whole number of rows")
+    return W.numel() // row
+
+
+def dequant_q4_0(W: torch.Tensor, K: int, stream=None) -> torch.Tensor:
+    """W: uint8 [M, K/32*18] -> float32 [M, K] (bit-exact d*(q-8))."""
+    M = _check_w(W, K)
+    out = torch.empty((M, K), dtype=torch.float32, device=W.device)
+    gq_dequant_q4_0(W, M, K, out, stream)
+    return out
+
+
+def mul_mat_q4_0(W: torch.Tensor, X: torch.Tensor, stream=None, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Y[N, M] = X[N, K] @ dequant(W)^T with W uint8 [M, K/32*18], X float32 [N, K]."""
+    if X.dtype != torch.float32 or X.dim() != 2:
+        raise TypeError("X must be float32 [N, K]")
+    N, K = X.shape
+    M = _check_w(W, K)
+    Y = out if out is not None else torch.empty((N, M), dtype=torch.float32, device=X.device)
+    gq_mul_mat_q4_0(W, M, K, X, N, Y, stream)
+    return Y

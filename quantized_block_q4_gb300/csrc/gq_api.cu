@@ -1,0 +1,336 @@
+// The C ABI of include/gq.h: argument checks, dispatch, tensor maps, errors.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "gq.h"
+#include "gq_internal.h"
+
+namespace gq {
+
+__device__ uint32_t g_dev_error = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+thread_local std::string t_last_error;
+
+std::atomic<int64_t> g_prefill_min_n{64};
+std::atomic<int64_t> g_force_generic{0};
+std::atomic<int64_t> g_wait_limit_ns{2000000000LL};
+
+gq_status fail(gq_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+gq_status fail(gq_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return st;
+}
+
+gq_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(GQ_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// 2-D tiled tensor map: dim0 innermost (elements), dim1 rows, row stride in bytes.
+gq_status make_tmap(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, uint64_t dim0, uint64_t dim1,
+                    uint64_t row_stride, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swz) {
+  auto fn = encode_fn();
+  if (!fn) return fail(GQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {dim0, dim1};
+  cuuint64_t strides[1] = {row_stride};
+  cuuint32_t box[2] = {box0, box1};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(tm, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(GQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d, dims %llu x %llu, box %u x %u)",
+                static_cast<int>(r), static_cast<unsigned long long>(dim0), static_cast<unsigned long long>(dim1),
+                box0, box1);
+  return GQ_OK;
+}
+
+gq_status check_device() {
+  const DeviceInfo& di = device_info();
+  if (di.device < 0) return fail(GQ_ERR_CUDA, "no current CUDA device");
+  if (!(di.cc_major == 10 && di.cc_minor == 3))
+    return fail(GQ_ERR_UNSUPPORTED, "device %d is compute capability %d.%d; this library is built for sm_103a",
+                di.device, di.cc_major, di.cc_minor);
+  return GQ_OK;
+}
+
+// Shapes shared by the mul_mat entry points.  Kernels index with 32-bit ints.
+gq_status check_mm_shape(int64_t M, int64_t K, int64_t N) {
+  if (M < 0 || K < 0 || N < 0)
+    return fail(GQ_ERR_SHAPE, "negative size (M=%lld K=%lld N=%lld)", (long long)M, (long long)K, (long long)N);
+  if (K % kQK) return fail(GQ_ERR_SHAPE, "K=%lld is not a multiple of 32", (long long)K);
+  const int64_t lim = (int64_t(1) << 31) - 1;
+  if (M > lim || K > lim || N > lim)
+    return fail(GQ_ERR_SHAPE, "a size exceeds 2^31-1 (M=%lld K=%lld N=%lld)", (long long)M, (long long)K,
+                (long long)N);
+  // products must fit comfortably in 63 bits of bytes
+  const unsigned __int128 wb = (unsigned __int128)M * (K / kQK) * kBlockBytes;
+  const unsigned __int128 xb = (unsigned __int128)N * K * 4, yb = (unsigned __int128)N * M * 4;
+  const unsigned __int128 cap = (unsigned __int128)1 << 62;
+  if (wb > cap || xb > cap || yb > cap) return fail(GQ_ERR_SHAPE, "tensor size overflows");
+  return GQ_OK;
+}
+
+}  // namespace
+
+uint32_t* device_error_word() {
+  static uint32_t* ptrs[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dev_error) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<uint32_t*>(p);
+  }
+  return ptrs[dev];
+}
+
+const DeviceInfo& device_info() {
+  static DeviceInfo infos[kMaxDevices];
+  static std::mutex mu;
+  static DeviceInfo none;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return none;
+  DeviceInfo& di = infos[dev];
+  if (di.device < 0) {
+    std::lock_guard<std::mutex> lk(mu);
+    if (di.device < 0) {
+      DeviceInfo d;
+      int v = 0;
+      cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+      d.sm_count = v;
+      cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+      cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+      cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+      d.smem_optin = static_cast<size_t>(v);
+      d.device = dev;
+      di = d;
+    }
+  }
+  return di;
+}
+
+}  // namespace gq
+
+using namespace gq;
+
+static gq_status mul_mat_decode(const void* W, int64_t M, int64_t K, const float* X, int64_t N, float* Y,
+                                cudaStream_t s) {
+  CUtensorMap tm;
+  uint32_t bx = 0, by = 0;
+  decode_w_box(N, &bx, &by);
+  const uint64_t row_bytes = static_cast<uint64_t>(K / kQK) * kBlockBytes;
+  gq_status st = make_tmap(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, row_bytes, static_cast<uint64_t>(M), row_bytes,
+                           bx, by, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st != GQ_OK) return st;
+  cudaError_t e = launch_decode(&tm, X, N, M, K, Y, static_cast<uint64_t>(g_wait_limit_ns.load()), s);
+  return e == cudaSuccess ? GQ_OK : cuda_fail(e, "decode launch");
+}
+
+static gq_status mul_mat_prefill_bf16(const void* W, int64_t M, int64_t K, const uint16_t* Xb, int64_t N, float* Y,
+                                      cudaStream_t s) {
+  CUtensorMap tmW, tmX;
+  uint32_t wbx, wby, xbk, xbr;
+  prefill_boxes(&wbx, &wby, &xbk, &xbr);
+  const uint64_t row_bytes = static_cast<uint64_t>(K / kQK) * kBlockBytes;
+  gq_status st = make_tmap(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, row_bytes, static_cast<uint64_t>(M), row_bytes,
+                           wbx, wby, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st != GQ_OK) return st;
+  st = make_tmap(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Xb, static_cast<uint64_t>(K), static_cast<uint64_t>(N),
+                 static_cast<uint64_t>(K) * 2, xbk, xbr, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != GQ_OK) return st;
+  cudaError_t e = launch_prefill(&tmW, &tmX, N, M, K, Y, static_cast<uint64_t>(g_wait_limit_ns.load()), s);
+  return e == cudaSuccess ? GQ_OK : cuda_fail(e, "prefill launch");
+}
+
+extern "C" {
+
+size_t gq_q4_0_nbytes(int64_t M, int64_t K) {
+  if (M < 0 || K < 0 || K % kQK) return 0;
+  return static_cast<size_t>(M) * static_cast<size_t>(K / kQK) * kBlockBytes;
+}
+
+gq_status gq_dequant_q4_0(const void* W, int64_t M, int64_t K, float* out, void* stream) {
+  t_last_error.clear();
+  if (M < 0 || K < 0) return fail(GQ_ERR_SHAPE, "negative size");
+  if (K % kQK) return fail(GQ_ERR_SHAPE, "K=%lld is not a multiple of 32", (long long)K);
+  if (M == 0 || K == 0) return GQ_OK;
+  if (!W || !out) return fail(GQ_ERR_NULL, "W and out must not be NULL");
+  if ((unsigned __int128)M * K * 4 > ((unsigned __int128)1 << 62)) return fail(GQ_ERR_SHAPE, "size overflows");
+  gq_status st = check_device();
+  if (st != GQ_OK) return st;
+  const int64_t nblocks = M * (K / kQK);
+  auto s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = (aligned(W, 16) && aligned(out, 16))
+                      ? launch_dequant_vec(static_cast<const uint8_t*>(W), nblocks, out, s)
+                      : launch_dequant_bytes(static_cast<const uint8_t*>(W), nblocks, out, s);
+  return e == cudaSuccess ? GQ_OK : cuda_fail(e, "dequant launch");
+}
+
+gq_status gq_mul_mat_q4_0(const void* W, int64_t M, int64_t K, const float* X, int64_t N, float* Y, void* stream) {
+  t_last_error.clear();
+  gq_status st = check_mm_shape(M, K, N);
+  if (st != GQ_OK) return st;
+  if (M == 0 || N == 0) return GQ_OK;
+  if (!Y) return fail(GQ_ERR_NULL, "Y must not be NULL");
+  st = check_device();
+  if (st != GQ_OK) return st;
+  auto s = static_cast<cudaStream_t>(stream);
+  if (K == 0) {  // empty sum
+    cudaError_t e = cudaMemsetAsync(Y, 0, static_cast<size_t>(N) * M * sizeof(float), s);
+    return e == cudaSuccess ? GQ_OK : cuda_fail(e, "memset");
+  }
+  if (!W || !X) return fail(GQ_ERR_NULL, "W and X must not be NULL");
+  if (!aligned(X, 4) || !aligned(Y, 4)) return fail(GQ_ERR_ALIGN, "X and Y must be 4-byte aligned");
+
+  const bool fast = (K % 256 == 0) && aligned(W, 16) && aligned(X, 16) && aligned(Y, 16);
+  if (!fast || g_force_generic.load()) {
+    cudaError_t e = launch_generic(static_cast<const uint8_t*>(W), M, K, X, N, Y, s);
+    return e == cudaSuccess ? GQ_OK : cuda_fail(e, "generic launch");
+  }
+  if (N < g_prefill_min_n.load() && N <= 64) return mul_mat_decode(W, M, K, X, N, Y, s);
+  if (N <= 64) return mul_mat_decode(W, M, K, X, N, Y, s);  // TEMP until the tensor-core path lands
+  {
+    cudaError_t e = launch_generic(static_cast<const uint8_t*>(W), M, K, X, N, Y, s);  // TEMP
+    return e == cudaSuccess ? GQ_OK : cuda_fail(e, "generic launch");
+  }
+
+  // Prefill: X -> bf16 scratch (stream-ordered), then the tensor-core kernel.
+  const size_t xbytes = static_cast<size_t>(N) * K * sizeof(uint16_t);
+  void* xb = nullptr;
+  cudaError_t e = cudaMallocAsync(&xb, xbytes, s);
+  if (e != cudaSuccess) return fail(GQ_ERR_ALLOC, "cudaMallocAsync(%zu): %s", xbytes, cudaGetErrorString(e));
+  e = launch_f32_to_bf16(X, static_cast<uint16_t*>(xb), N * K, s);
+  if (e != cudaSuccess) {
+    cudaFreeAsync(xb, s);
+    return cuda_fail(e, "f32->bf16 launch");
+  }
+  st = mul_mat_prefill_bf16(W, M, K, static_cast<const uint16_t*>(xb), N, Y, s);
+  e = cudaFreeAsync(xb, s);
+  if (st != GQ_OK) return st;
+  return e == cudaSuccess ? GQ_OK : cuda_fail(e, "cudaFreeAsync");
+}
+
+gq_status gq_mul_mat_q4_0_bf16x(const void* W, int64_t M, int64_t K, const uint16_t* X_bf16, int64_t N, float* Y,
+                                void* stream) {
+  t_last_error.clear();
+  gq_status st = check_mm_shape(M, K, N);
+  if (st != GQ_OK) return st;
+  if (M == 0 || N == 0) return GQ_OK;
+  if (!Y) return fail(GQ_ERR_NULL, "Y must not be NULL");
+  st = check_device();
+  if (st != GQ_OK) return st;
+  auto s = static_cast<cudaStream_t>(stream);
+  if (K == 0) {
+    cudaError_t e = cudaMemsetAsync(Y, 0, static_cast<size_t>(N) * M * sizeof(float), s);
+    return e == cudaSuccess ? GQ_OK : cuda_fail(e, "memset");
+  }
+  if (!W || !X_bf16) return fail(GQ_ERR_NULL, "W and X_bf16 must not be NULL");
+  if (K % 256) return fail(GQ_ERR_SHAPE, "the bf16-activation path needs K %% 256 == 0 (K=%lld)", (long long)K);
+  if (!aligned(W, 16) || !aligned(X_bf16, 16) || !aligned(Y, 16))
+    return fail(GQ_ERR_ALIGN, "W, X_bf16 and Y must be 16-byte aligned");
+  return mul_mat_prefill_bf16(W, M, K, X_bf16, N, Y, s);
+}
+
+gq_status gq_f32_to_bf16(const float* x, uint16_t* y, int64_t n, void* stream) {
+  t_last_error.clear();
+  if (n < 0) return fail(GQ_ERR_SHAPE, "negative size");
+  if (n == 0) return GQ_OK;
+  if (!x || !y) return fail(GQ_ERR_NULL, "x and y must not be NULL");
+  if (!aligned(x, 4) || !aligned(y, 2)) return fail(GQ_ERR_ALIGN, "x must be 4-byte and y 2-byte aligned");
+  gq_status st = check_device();
+  if (st != GQ_OK) return st;
+  cudaError_t e = launch_f32_to_bf16(x, y, n, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GQ_OK : cuda_fail(e, "f32->bf16 launch");
+}
+
+gq_status gq_sync_status(void* stream) {
+  t_last_error.clear();
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  uint32_t* w = device_error_word();
+  if (!w) return fail(GQ_ERR_CUDA, "device error word unavailable");
+  uint32_t v = 0;
+  e = cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read error word");
+  if (v) {
+    const uint32_t zero = 0;
+    cudaMemcpy(w, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    return fail(GQ_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait gave up (device error bits 0x%x)", v);
+  }
+  return GQ_OK;
+}
+
+gq_status gq_set_option(gq_option opt, int64_t value) {
+  t_last_error.clear();
+  switch (opt) {
+    case GQ_OPT_PREFILL_MIN_N:
+      if (value < 1) return fail(GQ_ERR_SHAPE, "prefill threshold must be >= 1");
+      g_prefill_min_n = value;
+      return GQ_OK;
+    case GQ_OPT_FORCE_GENERIC:
+      g_force_generic = value ? 1 : 0;
+      return GQ_OK;
+    case GQ_OPT_WAIT_LIMIT_NS:
+      if (value < 1000) return fail(GQ_ERR_SHAPE, "wait limit must be >= 1000 ns");
+      g_wait_limit_ns = value;
+      return GQ_OK;
+  }
+  return fail(GQ_ERR_SHAPE, "unknown option %d", static_cast<int>(opt));
+}
+
+int64_t gq_get_option(gq_option opt) {
+  switch (opt) {
+    case GQ_OPT_PREFILL_MIN_N: return g_prefill_min_n.load();
+    case GQ_OPT_FORCE_GENERIC: return g_force_generic.load();
+    case GQ_OPT_WAIT_LIMIT_NS: return g_wait_limit_ns.load();
+  }
+  return -1;
+}
+
+const char* gq_last_error(void) { return t_last_error.c_str(); }
+
+const char* gq_status_string(gq_status s) {
+  switch (s) {
+    case GQ_OK: return "GQ_OK";
+    case GQ_ERR_NULL: return "GQ_ERR_NULL";
+    case GQ_ERR_SHAPE: return "GQ_ERR_SHAPE";
+    case GQ_ERR_ALIGN: return "GQ_ERR_ALIGN";
+    case GQ_ERR_CUDA: return "GQ_ERR_CUDA";
+    case GQ_ERR_ALLOC: return "GQ_ERR_ALLOC";
+    case GQ_ERR_DEVICE_TIMEOUT: return "GQ_ERR_DEVICE_TIMEOUT";
+    case GQ_ERR_UNSUPPORTED: return "GQ_ERR_UNSUPPORTED";
+  }
+  return "unknown gq_status";
+}
+
+int gq_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,369 @@
+// K2: decode / small-N MUL_MAT against Q4_0 weights, plus the generic
+// fallback kernel.
+//
+// Y[n][m] = sum_k w[m][k] * X[n][k],  w = d*(q-8)  ("Binding GGUF weights to
+// the compute graph", section 2.3: blocks are dequantised inside MUL_MAT;
+// "GGUF loading, mmap and tensor placement", step six: W ne=[K,M], b ne=[K,N]).
+//
+// Design (decode is HBM-bound: 0.5625 bytes of W per weight, N <= 64 tokens):
+//  * A producer warp streams W with 2-D TMA boxes of 16 rows x 144 bytes (256
+//    weights, 8 blocks per row) into a ring of shared-memory stages; each
+//    stage holds KW such boxes, one per consumer warp (split-K inside the CTA).
+//  * Consumer warps run mma.sync m16n8k16 (fp16 in, fp32 accumulate) with the
+//    16 W rows as the A operand and up to 8 tokens per n8 tile as B.  A holds
+//    the integer codes (q - 8) in fp16, which is exact; the block scale d is
+//    applied in fp32 to the per-block partial product, so W is never rounded.
+//    Only x is rounded (to fp16, relative error <= 2^-11 per element).
+//  * The four bytes of codes a lane needs are read straight from the raw
+//    18-byte blocks: two blocks (36 bytes) form nine aligned 32-bit words, and
+//    one PRMT rebuilds the word that straddles the scale of the even block.
+//    Which 8 codes a lane owns therefore depends on the block's parity; the
+//    x fragments staged in shared memory follow the same permutation of k
+//    (a contraction does not care how k is ordered, only that A and B agree).
+//  * The k-warps' partial sums of a 16-row tile are reduced through shared
+//    memory; CTAs loop over tiles persistently.
+#include <algorithm>
+#include <cuda_fp16.h>
+
+#include "gq_internal.h"
+#include "gq_ptx.cuh"
+
+namespace gq {
+namespace {
+
+constexpr int kBM = 16;                        // rows per tile (one m16 MMA tile)
+constexpr int kSubK = 256;                     // weights per row per TMA box
+constexpr int kSubBytesRow = 144;              // 8 blocks x 18 bytes
+constexpr int kSubBytes = kBM * kSubBytesRow;  // 2304 bytes per box
+
+template <int NT, int KW, int STAGES>
+struct DecodeCfg {
+  static constexpr int kThreads = 32 * (KW + 1);
+  static constexpr int kStageK = kSubK * KW;
+  static constexpr int kStageBytes = kSubBytes * KW;
+  static constexpr int kRingBytes = kStageBytes * STAGES;
+  static constexpr int kRedFloats = 2 * KW * 4 * NT * 32;
+  static size_t smem_bytes(int N, int KX) {
+    return kRingBytes + static_cast<size_t>(2) * KX * N + kRedFloats * sizeof(float) + 2 * STAGES * 8 + 16 + 128;
+  }
+};
+
+// Bytes of the two 16-bit halves -> fp32 scale.
+__device__ __forceinline__ float half_lo(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<uint16_t>(w & 0xFFFFu)));
+}
+__device__ __forceinline__ float half_hi(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<uint16_t>(w >> 16)));
+}
+
+// The 4 code bytes (qs indices) lane t owns in an even / odd block of a pair.
+__device__ __forceinline__ void lane_bytes(int parity, int t, int (&c)[4]) {
+  if (parity) {
+    c[0] = 4 * t; c[1] = 4 * t + 1; c[2] = 4 * t + 2; c[3] = 4 * t + 3;
+  } else if (t < 3) {
+    c[0] = 4 * t + 2; c[1] = 4 * t + 3; c[2] = 4 * t + 4; c[3] = 4 * t + 5;
+  } else {
+    c[0] = 0; c[1] = 1; c[2] = 14; c[3] = 15;
+  }
+}
+
+// Word of 8 codes (bytes c0..c3) -> four f16x2 registers holding q - 8 exactly.
+// lo: (c0,c2) and (c1,c3) low nibbles; hi: the same bytes' high nibbles.
+__device__ __forceinline__ void codes_to_f16(uint32_t v, uint32_t& lo02, uint32_t& lo13, uint32_t& hi02,
+                                             uint32_t& hi13) {
+  const uint32_t kMagic = 0x64006400u;      // fp16 1024 in both halves
+  const uint32_t kSub = 0x64086408u;        // fp16 1032
+  const uint32_t kSixteenth = 0x2C002C00u;  // fp16 1/16
+  const uint32_t kMinus72 = 0xD480D480u;    // fp16 -72
+  const uint32_t v8 = v >> 8;
+  lo02 = hsub2_u32(lop3_and_or(v, 0x000F000Fu, kMagic), kSub);  // (1024+q) - 1032
+  lo13 = hsub2_u32(lop3_and_or(v8, 0x000F000Fu, kMagic), kSub);
+  hi02 = hfma2_u32(lop3_and_or(v, 0x00F000F0u, kMagic), kSixteenth, kMinus72);  // (1024+16q)/16 - 72
+  hi13 = hfma2_u32(lop3_and_or(v8, 0x00F000F0u, kMagic), kSixteenth, kMinus72);
+}
+
+template <int NT, int KW, int STAGES>
+__global__ void __launch_bounds__(32 * (KW + 1), 1)
+    k_decode_q4_0(const __grid_constant__ CUtensorMap tmW, const float* __restrict__ X, int N, int M, int K,
+                  int KX, float* __restrict__ Y, uint64_t limit_ns, uint32_t* err) {
+  using Cfg = DecodeCfg<NT, KW, STAGES>;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  uint8_t* ring = smem;
+  uint4* xs = reinterpret_cast<uint4*>(smem + Cfg::kRingBytes);
+  float* red = reinterpret_cast<float*>(smem + Cfg::kRingBytes + static_cast<size_t>(2) * KX * N);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(red + Cfg::kRedFloats);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ntiles = (M + kBM - 1) / kBM;
+  const int nchunks = (K + KX - 1) / KX;
+  const int stages_per_chunk = KX / Cfg::kStageK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&bars[s]), 1);            // full: producer's expect_tx arrive + tx bytes
+      mbar_init(smem_u32(&bars[STAGES + s]), KW);  // empty: one arrive per consumer warp
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == KW) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmW);
+      uint32_t q = 0;
+      bool ok = true;
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const int kc0 = c * KX;
+        const int kend = min(K, kc0 + KX);
+        const int nst = min(stages_per_chunk, (kend - kc0 + Cfg::kStageK - 1) / Cfg::kStageK);
+        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+          for (int st = 0; st < nst; ++st, ++q) {
+            const int slot = q % STAGES;
+            const uint32_t ph = (q / STAGES) & 1;
+            if (!mbar_wait_bounded(smem_u32(&bars[STAGES + slot]), ph ^ 1, limit_ns, abort_flag, err)) {
+              ok = false;
+              break;
+            }
+            const int k0 = kc0 + st * Cfg::kStageK;
+            const int nvalid = min(KW, (kend - k0 + kSubK - 1) / kSubK);
+            const uint32_t full = smem_u32(&bars[slot]);
+            mbar_arrive_expect_tx(full, nvalid * kSubBytes);
+            for (int j = 0; j < nvalid; ++j) {
+              const int xb = ((k0 + j * kSubK) / kSubK) * kSubBytesRow;  // byte column in the row
+              tma_load_2d(smem_u32(ring + slot * Cfg::kStageBytes + j * kSubBytes), &tmW, xb, tile * kBM, full);
+            }
+          }
+        }
+      }
+      if (!ok) {
+        // Let copies already issued land before the CTA can exit.
+        for (uint32_t i = 0; i < STAGES && i < q; ++i) {
+          const uint32_t qq = q - 1 - i;
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(smem_u32(&bars[qq % STAGES]), (qq / STAGES) & 1) &&
+                 globaltimer_ns() - t0 < limit_ns) {
+          }
+        }
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int kw = warp;
+  const int g = lane >> 2, t = lane & 3;
+  const uint32_t sel = (t == 3) ? 0x5432u : 0x7654u;  // even-block word: U, or Z.hi | U.lo for t == 3
+  uint32_t q = 0;
+  int tile_iter = 0;
+  bool live = true;  // false once a bounded wait gave up; the loops still run to keep barriers matched
+
+  for (int c = 0; c < nchunks; ++c) {
+    const int kc0 = c * KX;
+    const int kend = min(K, kc0 + KX);
+    const int nst = min(stages_per_chunk, (kend - kc0 + Cfg::kStageK - 1) / Cfg::kStageK);
+    const int nbl = nst * Cfg::kStageK / kQK;  // local blocks covered by this chunk's stages
+
+    // Stage this chunk of x into shared memory as fp16 fragments, permuted
+    // like the codes: entry (block b, token n, lane-slot t) = 8 halves
+    // [x[c0], x[c2], x[c1], x[c3], x[16+c0], x[16+c2], x[16+c1], x[16+c3]].
+    named_bar_sync(1, 32 * KW);  // previous chunk's x fragments are no longer read
+    for (int e = threadIdx.x; e < nbl * N * 4; e += 32 * KW) {
+      const int tt = e & 3;
+      const int n = (e >> 2) % N;
+      const int bl = (e >> 2) / N;
+      const int bg = kc0 / kQK + bl;
+      int cb[4];
+      lane_bytes(bg & 1, tt, cb);
+      const float* xr = X + static_cast<size_t>(n) * K + static_cast<size_t>(bg) * kQK;
+      const bool in = bg * kQK < K;
+      float v[8];
+      const int order[4] = {cb[0], cb[2], cb[1], cb[3]};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[i] = in ? xr[order[i]] : 0.f;
+        v[4 + i] = in ? xr[16 + order[i]] : 0.f;
+      }
+      uint4 pk;
+      __half2 h;
+      h = __floats2half2_rn(v[0], v[1]); pk.x = *reinterpret_cast<uint32_t*>(&h);
+      h = __floats2half2_rn(v[2], v[3]); pk.y = *reinterpret_cast<uint32_t*>(&h);
+      h = __floats2half2_rn(v[4], v[5]); pk.z = *reinterpret_cast<uint32_t*>(&h);
+      h = __floats2half2_rn(v[6], v[7]); pk.w = *reinterpret_cast<uint32_t*>(&h);
+      xs[e] = pk;
+    }
+    named_bar_sync(1, 32 * KW);
+
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tile_iter) {
+      float acc[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
+
+      for (int st = 0; st < nst; ++st, ++q) {
+        const int slot = q % STAGES;
+        if (live) live = mbar_wait_bounded(smem_u32(&bars[slot]), (q / STAGES) & 1, limit_ns, abort_flag, err);
+        const int k0 = kc0 + st * Cfg::kStageK + kw * kSubK;
+        if (live && k0 < kend) {
+          const uint8_t* sub = ring + slot * Cfg::kStageBytes + kw * kSubBytes;
+          const int bl0 = (k0 - kc0) / kQK;
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            uint32_t wd[2][2];  // [row g / g+8][even / odd block] code words
+            float dd[2][2];     // scales
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const uint8_t* rb = sub + (g + 8 * r) * kSubBytesRow + 36 * p;
+              const uint32_t Z = *reinterpret_cast<const uint32_t*>(rb);
+              const uint32_t U = *reinterpret_cast<const uint32_t*>(rb + 4 + 4 * t);
+              const uint32_t W4 = *reinterpret_cast<const uint32_t*>(rb + 16);
+              const uint32_t Y1 = *reinterpret_cast<const uint32_t*>(rb + 20 + 4 * t);
+              wd[r][0] = prmt(Z, U, sel);
+              wd[r][1] = Y1;
+              dd[r][0] = half_lo(Z);
+              dd[r][1] = half_hi(W4);
+            }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              uint32_t a_lo[4], a_hi[4];
+              codes_to_f16(wd[0][e], a_lo[0], a_lo[2], a_hi[0], a_hi[2]);
+              codes_to_f16(wd[1][e], a_lo[1], a_lo[3], a_hi[1], a_hi[3]);
+              const int bl = bl0 + 2 * p + e;
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                const int n = nt * 8 + g;
+                uint4 xf = make_uint4(0u, 0u, 0u, 0u);
+                if (n < N) xf = xs[(bl * N + n) * 4 + t];
+                float tsum[4];
+                const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_m16n8k16_f16(tsum, a_lo, xf.x, xf.y, zero);
+                mma_m16n8k16_f16(tsum, a_hi, xf.z, xf.w, tsum);
+                acc[nt][0] = fmaf(dd[0][e], tsum[0], acc[nt][0]);
+                acc[nt][1] = fmaf(dd[0][e], tsum[1], acc[nt][1]);
+                acc[nt][2] = fmaf(dd[1][e], tsum[2], acc[nt][2]);
+                acc[nt][3] = fmaf(dd[1][e], tsum[3], acc[nt][3]);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (live && lane == 0) mbar_arrive(smem_u32(&bars[STAGES + slot]));
+      }
+
+      // Reduce the KW partial sums of this tile; warp kw finishes values i = kw, kw+KW, ...
+      const int slotr = tile_iter & 1;
+      float* rs = red + static_cast<size_t>(slotr) * KW * 4 * NT * 32;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rs[((kw * NT + nt) * 4 + i) * 32 + lane] = acc[nt][i];
+      named_bar_sync(1, 32 * KW);
+      for (int iv = kw; iv < 4 * NT; iv += KW) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < KW; ++w) s += rs[((w * NT) * 4 + iv) * 32 + lane];
+        const int nt = iv >> 2, i = iv & 3;
+        const int row = tile * kBM + g + 8 * (i >> 1);
+        const int n = nt * 8 + 2 * t + (i & 1);
+        if (live && row < M && n < N) {
+          float* yp = Y + static_cast<size_t>(n) * M + row;
+          *yp = (c == 0) ? s : (*yp + s);
+        }
+      }
+    }
+  }
+}
+
+template <int NT, int KW, int STAGES>
+cudaError_t launch_cfg(const CUtensorMap* tmW, const float* X, int N, int M, int K, float* Y, uint64_t limit_ns,
+                       int xs_budget, cudaStream_t s) {
+  using Cfg = DecodeCfg<NT, KW, STAGES>;
+  // x chunk: a multiple of the stage width, as long as the budget allows
+  int KX = (xs_budget / (2 * N)) / Cfg::kStageK * Cfg::kStageK;
+  if (KX < Cfg::kStageK) KX = Cfg::kStageK;
+  const int Kpad = (K + Cfg::kStageK - 1) / Cfg::kStageK * Cfg::kStageK;
+  if (KX > Kpad) KX = Kpad;
+  const size_t smem = Cfg::smem_bytes(N, KX);
+  auto kern = k_decode_q4_0<NT, KW, STAGES>;
+  static int configured_smem = 0;
+  static int occ_cache_smem = -1, occ_cache = 1;
+  if (static_cast<int>(smem) > configured_smem) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured_smem = static_cast<int>(smem);
+  }
+  if (occ_cache_smem != static_cast<int>(smem)) {
+    int occ = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, Cfg::kThreads, smem);
+    if (e != cudaSuccess) return e;
+    occ_cache = occ > 0 ? occ : 1;
+    occ_cache_smem = static_cast<int>(smem);
+  }
+  const int ntiles = (M + kBM - 1) / kBM;
+  const int grid = std::min(ntiles, device_info().sm_count * occ_cache);
+  kern<<<grid, Cfg::kThreads, smem, s>>>(*tmW, X, N, M, K, KX, Y, limit_ns, device_error_word());
+  return cudaGetLastError();
+}
+
+// -------------------------------------------------------------------------
+// Generic fallback: any K % 32 == 0, any alignment, any N.  One warp per row;
+// W bytes are re-read per token (from cache).  Used for shapes the fast paths
+// do not take (K % 256 != 0, unaligned pointers).
+__global__ void k_generic_q4_0(const uint8_t* __restrict__ W, int64_t M, int64_t K, const float* __restrict__ X,
+                               int64_t N, float* __restrict__ Y) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nb = K / kQK;
+  const int64_t row_bytes = nb * kBlockBytes;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t m = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); m < M; m += warps) {
+    const uint8_t* row = W + m * row_bytes;
+    for (int64_t n = 0; n < N; ++n) {
+      const float* x = X + n * K;
+      float acc = 0.f;
+      for (int64_t b = lane; b < nb; b += 32) {
+        const uint8_t* blk = row + b * kBlockBytes;
+        const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(blk[0] | (blk[1] << 8))));
+        float part = 0.f;
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t byte = blk[2 + j];
+          part = fmaf(static_cast<float>(static_cast<int>(byte & 0xF) - 8), x[b * kQK + j], part);
+          part = fmaf(static_cast<float>(static_cast<int>(byte >> 4) - 8), x[b * kQK + j + 16], part);
+        }
+        acc = fmaf(d, part, acc);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+      if (lane == 0) Y[n * M + m] = acc;
+    }
+  }
+}
+
+}  // namespace
+
+void decode_w_box(int64_t /*N*/, uint32_t* box_x_bytes, uint32_t* box_rows) {
+  *box_x_bytes = kSubBytesRow;
+  *box_rows = kBM;
+}
+
+cudaError_t launch_decode(const CUtensorMap* tmW, const float* X, int64_t N, int64_t M, int64_t K, float* Y,
+                          uint64_t wait_limit_ns, cudaStream_t s) {
+  const int n = static_cast<int>(N), m = static_cast<int>(M), k = static_cast<int>(K);
+  if (N <= 8) return launch_cfg<1, 8, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, s);
+  if (N <= 16) return launch_cfg<2, 8, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, s);
+  if (N <= 32) return launch_cfg<4, 4, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 128 << 10, s);
+  return launch_cfg<8, 4, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 128 << 10, s);
+}
+
+cudaError_t launch_generic(const uint8_t* W, int64_t M, int64_t K, const float* X, int64_t N, float* Y,
+                           cudaStream_t s) {
+  const int64_t blocks = (M + 7) / 8;
+  const int grid = static_cast<int>(std::min<int64_t>(blocks, static_cast<int64_t>(device_info().sm_count) * 16));
+  k_generic_q4_0<<<grid, 256, 0, s>>>(W, M, K, X, N, Y);
+  return cudaGetLastError();
+}
+
+}  // namespace gq

@@ -1,0 +1,49 @@
+// Internal interface between the C ABI (gq_api.cu) and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace gq {
+
+constexpr int kQK = 32;          // weights per block_q4_0
+constexpr int kBlockBytes = 18;  // fp16 d + 16 bytes of codes
+
+// Device-side error word (defined in gq_api.cu).
+uint32_t* device_error_word();
+
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+  int cc_major = 0, cc_minor = 0;
+  size_t smem_optin = 0;
+};
+const DeviceInfo& device_info();  // current device, cached
+
+// ---- K1: Q4_0 blocks -> fp32, bit-exact (gq_dequant.cu)
+cudaError_t launch_dequant_vec(const uint8_t* W, int64_t nblocks, float* out, cudaStream_t s);
+cudaError_t launch_dequant_bytes(const uint8_t* W, int64_t nblocks, float* out, cudaStream_t s);
+
+// ---- K2: decode / small-N mul_mat (gq_decode.cu).  Needs K % 256 == 0,
+// W 16-byte aligned, N <= 64.
+cudaError_t launch_decode(const CUtensorMap* tmW, const float* X, int64_t N, int64_t M, int64_t K,
+                          float* Y, uint64_t wait_limit_ns, cudaStream_t s);
+// TMA box the decode kernel expects for W (rows of raw blocks viewed as bytes).
+void decode_w_box(int64_t N, uint32_t* box_x_bytes, uint32_t* box_rows);
+
+// ---- generic fallback mul_mat: any K % 32 == 0, any alignment, any N.
+cudaError_t launch_generic(const uint8_t* W, int64_t M, int64_t K, const float* X, int64_t N, float* Y,
+                           cudaStream_t s);
+
+// ---- K0: fp32 -> bf16 (round to nearest even) (gq_prefill.cu)
+cudaError_t launch_f32_to_bf16(const float* x, uint16_t* y, int64_t n, cudaStream_t s);
+
+// ---- K3: prefill mul_mat on tcgen05 (gq_prefill.cu).  Needs K % 256 == 0.
+cudaError_t launch_prefill(const CUtensorMap* tmW, const CUtensorMap* tmX, int64_t N, int64_t M,
+                           int64_t K, float* Y, uint64_t wait_limit_ns, cudaStream_t s);
+void prefill_boxes(uint32_t* w_box_x_bytes, uint32_t* w_box_rows, uint32_t* x_box_k,
+                   uint32_t* x_box_rows);
+
+}  // namespace gq

@@ -1,0 +1,224 @@
+"""CUDA path against the CPU oracle, element by element, through the C ABI.
+
+Dequantisation must be bit-exact (NaN == NaN); MUL_MAT must satisfy
+|y - y_ref| <= 1e-3 * sum_k |w_k x_k| + 1e-5 for every element, with y_ref and
+the sum from the fp64 oracle.  Inputs come from synth.py (seeded).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from golden_io import read_blocks, same_f32_bits
+from gpu_util import assert_mul_mat_close, oracle_mul_mat
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import quantized_block_q4_gb300 as gq
+else:  # collected on CPU machines, never run there (marked gpu)
+    gq = None
+
+
+def dev(a: np.ndarray):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+# ------------------------------------------------------------------ dequant
+DEQUANT_SHAPES = [(256, 1024), (11008, 4096), (4096, 11008), (4096, 4096), (32000, 4096), (14336, 4096),
+                  (1, 32), (3, 64), (7, 288), (129, 256), (5, 8192)]
+
+
+@pytest.mark.parametrize("M,K", DEQUANT_SHAPES)
+def test_dequant_bit_exact(M, K):
+    W = synth.q4_0_weights(M, K, seed=synth.seed_for(1, 0) + M + K)
+    ref = oracle.get().dequant(W, M, K)
+    out = gq.dequant_q4_0(dev(W), K)
+    torch.cuda.synchronize()
+    assert same_f32_bits(out.cpu().numpy(), ref).all()
+
+
+def test_dequant_golden_blocks_and_signs():
+    recs = read_blocks()
+    W = np.concatenate([raw for _, raw, _ in recs])          # one row of len(recs) blocks
+    K = 32 * len(recs)
+    out = gq.dequant_q4_0(dev(W), K).cpu().numpy()[0]
+    expect = np.concatenate([v for _, _, v in recs])
+    assert same_f32_bits(out, expect).all()
+    assert same_f32_bits(out, oracle.get().dequant(W, 1, K)[0]).all()
+
+
+@pytest.mark.parametrize("offset", [1, 2, 6])
+def test_dequant_unaligned(offset):
+    M, K = 37, 288
+    W = synth.q4_0_weights(M, K, seed=77)
+    buf = torch.zeros(W.size + 64, dtype=torch.uint8, device="cuda")
+    buf[offset:offset + W.size] = dev(W.reshape(-1))
+    out = torch.full((M * K + 1,), float("nan"), dtype=torch.float32, device="cuda")
+    gq.gq_dequant_q4_0(buf.data_ptr() + offset, M, K, out.data_ptr() + 4, None)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    assert np.isnan(got[0])
+    assert same_f32_bits(got[1:].reshape(M, K), oracle.get().dequant(W, M, K)).all()
+
+
+def test_dequant_scale_specials():
+    # every scale class: +-0, subnormal, normal, max, +-inf, NaN; all codes 0..15
+    d_bits = np.array([0x0000, 0x8000, 0x0001, 0x83FF, 0x3C00, 0xB555, 0x7BFF, 0x7C00, 0xFC00, 0x7E01],
+                      dtype=np.uint16)
+    nb = d_bits.size
+    ramp = np.array([j | ((15 - j) << 4) for j in range(16)], dtype=np.uint8)  # every code, both nibbles
+    qs = np.tile(ramp, (1, nb, 1))
+    W = synth.blocks_from_parts(d_bits.reshape(1, nb), qs)
+    out = gq.dequant_q4_0(dev(W), 32 * nb).cpu().numpy()
+    assert same_f32_bits(out, oracle.get().dequant(W, 1, 32 * nb)).all()
+
+
+def test_dequant_empty_and_errors():
+    out = torch.empty(0, dtype=torch.float32, device="cuda")
+    gq.gq_dequant_q4_0(torch.empty(0, dtype=torch.uint8, device="cuda"), 0, 64, out)
+    with pytest.raises(gq.GQError) as e:
+        gq.gq_dequant_q4_0(torch.empty(18, dtype=torch.uint8, device="cuda"), 1, 33, out)
+    assert e.value.status == gq.GQ_ERR_SHAPE
+
+
+# ------------------------------------------------------------------ mul_mat
+def run_mm(W, X, M, K):
+    Wd, Xd = dev(W), dev(X)
+    Y = gq.mul_mat_q4_0(Wd, Xd)
+    torch.cuda.synchronize()
+    gq.gq_sync_status()
+    return Y.cpu().numpy()
+
+
+def check_mm(M, K, N, seed, label=""):
+    W = synth.q4_0_weights(M, K, seed=seed)
+    X = synth.activations(N, K, seed=seed + 1)
+    y = run_mm(W, X, M, K)
+    y_ref, s_ref = oracle_mul_mat(W, M, K, X)
+    return assert_mul_mat_close(y, y_ref, s_ref, label or f"M={M} K={K} N={N}")
+
+
+def test_tiny_matvec():  # 256 x 1024, N = 1
+    check_mm(256, 1024, 1, synth.seed_for(1, 0))
+
+
+@pytest.mark.parametrize("M,K", [(11008, 4096), (4096, 11008)])
+def test_ffn_decode(M, K):
+    check_mm(M, K, 1, synth.seed_for(2, 0) + M)
+
+
+@pytest.mark.parametrize("N", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("M", [4096, 32000])
+def test_small_batch_decode(M, N):
+    check_mm(M, 4096, N, synth.seed_for(3, N) + M)
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 7, 8, 9, 15, 16, 17, 31, 32, 33, 48, 63, 64, 65, 127, 128, 129, 200])
+def test_n_edges(N):
+    check_mm(129, 512, N, 900 + N)
+
+
+@pytest.mark.parametrize("M", [1, 3, 15, 16, 17, 100, 255, 257])
+@pytest.mark.parametrize("N", [1, 5, 64, 130])
+def test_m_edges(M, N):
+    check_mm(M, 768, N, 1000 + M * 7 + N)
+
+
+@pytest.mark.parametrize("K", [32, 64, 96, 288, 1000 // 32 * 32, 2048 + 32])
+@pytest.mark.parametrize("N", [1, 3, 70])
+def test_k_not_multiple_of_256(K, N):
+    check_mm(33, K, N, 2000 + K + N)
+
+
+@pytest.mark.parametrize("K", [256, 512, 2304, 8448, 12288, 16384])
+@pytest.mark.parametrize("N", [1, 16, 40, 64, 256])
+def test_k_sweep(K, N):
+    check_mm(80, K, N, 3000 + K + N)
+
+
+def test_zero_k_writes_zeros():
+    Y = torch.full((3, 5), 7.0, device="cuda")
+    gq.gq_mul_mat_q4_0(torch.empty(0, dtype=torch.uint8, device="cuda"), 5, 0,
+                       torch.empty(3, 0, device="cuda"), 3, Y)
+    torch.cuda.synchronize()
+    assert (Y.cpu().numpy() == 0).all()
+
+
+def test_generic_path_matches():
+    gq.gq_set_option(gq.GQ_OPT_FORCE_GENERIC, 1)
+    try:
+        check_mm(70, 1024, 5, 4001, "forced generic")
+        check_mm(70, 1024, 80, 4002, "forced generic")
+    finally:
+        gq.gq_set_option(gq.GQ_OPT_FORCE_GENERIC, 0)
+
+
+def test_unaligned_pointers_take_generic_path():
+    M, K, N = 40, 512, 3
+    W = synth.q4_0_weights(M, K, seed=4100)
+    X = synth.activations(N, K, seed=4101)
+    wbuf = torch.zeros(W.size + 32, dtype=torch.uint8, device="cuda")
+    wbuf[3:3 + W.size] = dev(W.reshape(-1))
+    xbuf = torch.zeros(N * K + 1, dtype=torch.float32, device="cuda")
+    xbuf[1:] = dev(X.reshape(-1))
+    Y = torch.zeros(N * M + 1, dtype=torch.float32, device="cuda")
+    gq.gq_mul_mat_q4_0(wbuf.data_ptr() + 3, M, K, xbuf.data_ptr() + 4, N, Y.data_ptr() + 4)
+    torch.cuda.synchronize()
+    y_ref, s_ref = oracle_mul_mat(W, M, K, X)
+    assert_mul_mat_close(Y.cpu().numpy()[1:].reshape(N, M), y_ref, s_ref, "unaligned")
+
+
+def test_output_guard_bytes_untouched():
+    M, K = 100, 1024
+    for N in (1, 8, 64, 100):
+        W = synth.q4_0_weights(M, K, seed=4200 + N)
+        X = synth.activations(N, K, seed=4300 + N)
+        guard = 1024
+        buf = torch.full((guard + N * M + guard,), -12345.0, dtype=torch.float32, device="cuda")
+        Y = buf[guard:guard + N * M]
+        gq.gq_mul_mat_q4_0(dev(W), M, K, dev(X), N, Y)
+        torch.cuda.synchronize()
+        b = buf.cpu().numpy()
+        assert (b[:guard] == -12345.0).all() and (b[-guard:] == -12345.0).all()
+        y_ref, s_ref = oracle_mul_mat(W, M, K, X)
+        assert_mul_mat_close(b[guard:guard + N * M].reshape(N, M), y_ref, s_ref, f"guard N={N}")
+
+
+def test_repeated_calls_are_deterministic():
+    M, K, N = 300, 4096, 4
+    W, X = dev(synth.q4_0_weights(M, K, seed=5)), dev(synth.activations(N, K, seed=6))
+    a = gq.mul_mat_q4_0(W, X)
+    b = gq.mul_mat_q4_0(W, X)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_shape_errors():
+    W = torch.zeros(18, dtype=torch.uint8, device="cuda")
+    X = torch.zeros(1, 32, device="cuda")
+    Y = torch.zeros(1, 1, device="cuda")
+    with pytest.raises(gq.GQError) as e:
+        gq.gq_mul_mat_q4_0(W, 1, 33, X, 1, Y)
+    assert e.value.status == gq.GQ_ERR_SHAPE
+    with pytest.raises(gq.GQError) as e:
+        gq.gq_mul_mat_q4_0(W, -1, 32, X, 1, Y)
+    assert e.value.status == gq.GQ_ERR_SHAPE
+    with pytest.raises(gq.GQError) as e:
+        gq.gq_mul_mat_q4_0(0, 1, 32, X, 1, Y)
+    assert e.value.status == gq.GQ_ERR_NULL
+
+
+def test_nonfinite_scale_propagates():
+    M, K, N = 16, 256, 2
+    W = synth.q4_0_weights(M, K, seed=8)
+    Wv = W.reshape(M, K // 32, 18)
+    Wv[3, 2, 0:2] = np.frombuffer(np.uint16(0x7C00).tobytes(), np.uint8)  # +inf scale
+    X = synth.activations(N, K, seed=9)
+    y = run_mm(W, X, M, K)
+    y_ref, s_ref = oracle_mul_mat(W, M, K, X)
+    assert (np.isnan(y_ref[:, 3]) | np.isinf(y_ref[:, 3])).all()
+    assert (np.isnan(y[:, 3]) | np.isinf(y[:, 3])).all()
+    rest = [m for m in range(M) if m != 3]
+    assert_mul_mat_close(y[:, rest], y_ref[:, rest], s_ref[:, rest], "finite rows")
