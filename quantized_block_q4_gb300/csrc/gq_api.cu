@@ -158,7 +158,7 @@ static gq_status mul_mat_prefill_bf16(const void* W, int64_t M, int64_t K, const
                                       cudaStream_t s) {
   CUtensorMap tmW, tmX;
   uint32_t wbx, wby, xbk, xbr;
-  prefill_boxes(&wbx, &wby, &xbk, &xbr);
+  prefill_boxes(N, &wbx, &wby, &xbk, &xbr);
   const uint64_t row_bytes = static_cast<uint64_t>(K / kQK) * kBlockBytes;
   gq_status st = make_tmap(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, row_bytes, static_cast<uint64_t>(M), row_bytes,
                            wbx, wby, CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -216,11 +216,6 @@ gq_status gq_mul_mat_q4_0(const void* W, int64_t M, int64_t K, const float* X, i
     return e == cudaSuccess ? GQ_OK : cuda_fail(e, "generic launch");
   }
   if (N < g_prefill_min_n.load() && N <= 64) return mul_mat_decode(W, M, K, X, N, Y, s);
-  if (N <= 64) return mul_mat_decode(W, M, K, X, N, Y, s);  // TEMP until the tensor-core path lands
-  {
-    cudaError_t e = launch_generic(static_cast<const uint8_t*>(W), M, K, X, N, Y, s);  // TEMP
-    return e == cudaSuccess ? GQ_OK : cuda_fail(e, "generic launch");
-  }
 
   // Prefill: X -> bf16 scratch (stream-ordered), then the tensor-core kernel.
   const size_t xbytes = static_cast<size_t>(N) * K * sizeof(uint16_t);

@@ -222,3 +222,70 @@ def test_nonfinite_scale_propagates():
     assert (np.isnan(y[:, 3]) | np.isinf(y[:, 3])).all()
     rest = [m for m in range(M) if m != 3]
     assert_mul_mat_close(y[:, rest], y_ref[:, rest], s_ref[:, rest], "finite rows")
+
+
+# ------------------------------------------------------------------ prefill (tensor cores)
+def sampled_rows(M, count, seed):
+    rng = np.random.Generator(np.random.SFC64(seed))
+    rows = np.concatenate([np.arange(min(128, M)), np.arange(max(0, M - 128), M),
+                           rng.integers(0, M, count)])
+    return np.unique(rows)
+
+
+def test_prefill_full_size_sampled_rows():
+    """14336 x 4096 weights, 512 tokens (the prefill workload): every column of
+    a seeded sample of rows (first and last tile included) against the oracle."""
+    M, K, N = 14336, 4096, 512
+    W = synth.q4_0_weights(M, K, seed=synth.seed_for(4, 0))
+    X = synth.activations(N, K, seed=synth.seed_for(4, 1))
+    y = run_mm(W, X, M, K)
+    rows = sampled_rows(M, 256, 41)
+    y_ref, s_ref = oracle_mul_mat(W.reshape(M, -1)[rows], len(rows), K, X)
+    assert_mul_mat_close(y[:, rows], y_ref, s_ref, "prefill sampled rows")
+
+
+@pytest.mark.parametrize("N", [64, 96, 128, 129, 256, 300, 512, 513])
+def test_prefill_n_tiles(N):
+    check_mm(384, 1024, N, 5000 + N)
+
+
+def test_f32_to_bf16_matches_torch_rounding():
+    x = torch.from_numpy(synth.activations(7, 1000, seed=12)).cuda().reshape(-1)
+    x[:6] = torch.tensor([float("nan"), float("inf"), -float("inf"), 0.0, -0.0, 1e-40], device="cuda")
+    y = torch.empty(x.numel(), dtype=torch.int16, device="cuda")
+    gq.gq_f32_to_bf16(x, y, x.numel())
+    ref = x.to(torch.bfloat16).view(torch.int16)
+    torch.cuda.synchronize()
+    nan = torch.isnan(x)
+    assert torch.equal(y[~nan], ref[~nan])
+    assert torch.isnan(y.view(torch.bfloat16)[nan].float()).all()
+
+
+@pytest.mark.parametrize("N", [1, 7, 16, 64, 200])
+def test_bf16_activation_entry(N):
+    M, K = 257, 2048
+    W = synth.q4_0_weights(M, K, seed=6000 + N)
+    X = synth.activations(N, K, seed=6100 + N)
+    xb = torch.from_numpy(X).cuda().to(torch.bfloat16)
+    Y = torch.empty(N, M, device="cuda")
+    gq.gq_mul_mat_q4_0_bf16x(dev(W), M, K, xb.view(torch.int16), N, Y)
+    torch.cuda.synchronize()
+    gq.gq_sync_status()
+    y_ref, s_ref = oracle_mul_mat(W, M, K, xb.float().cpu().numpy())
+    assert_mul_mat_close(Y.cpu().numpy(), y_ref, s_ref, f"bf16x N={N}")
+
+
+def test_prefill_threshold_option_switches_kernels():
+    M, K, N = 200, 1024, 20
+    W = synth.q4_0_weights(M, K, seed=7000)
+    X = synth.activations(N, K, seed=7001)
+    y_ref, s_ref = oracle_mul_mat(W, M, K, X)
+    old = gq.gq_get_option(gq.GQ_OPT_PREFILL_MIN_N)
+    try:
+        gq.gq_set_option(gq.GQ_OPT_PREFILL_MIN_N, 1)           # tensor-core path for N = 20
+        a = run_mm(W, X, M, K)
+    finally:
+        gq.gq_set_option(gq.GQ_OPT_PREFILL_MIN_N, old)
+    b = run_mm(W, X, M, K)                                      # decode path
+    assert_mul_mat_close(a, y_ref, s_ref, "tensor-core path")
+    assert_mul_mat_close(b, y_ref, s_ref, "decode path")
