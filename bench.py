@@ -1,0 +1,419 @@
+"""Benchmark: Q4_0 MUL_MAT over a 7B-like 32-layer weight sweep on GB300.
+
+One step = one pass of the whole hot path over the sweep:
+  decode   224 MUL_MATs at N = 1 through gq_mul_mat_q4_0 (decode kernel),
+           replayed as one CUDA graph;
+  prefill  224 MUL_MATs at N = 512: gq_f32_to_bf16 (activation conversion)
+           then gq_mul_mat_q4_0_bf16x (tensor-core kernel), CUDA events
+           around the tensor-core launches.
+Per layer: q, k, v, o 4096 x 4096, gate and up 11008 x 4096, down 4096 x 11008
+("Binding GGUF weights to the compute graph", section 2.4), 3.64 GB of Q4_0
+weights in total, all resident in HBM and larger than L2, so every pass
+streams them from DRAM.  Weights and activations are seeded synthetic data
+(synth.py).
+
+Prints ONE JSON line.  `value` is decode weight throughput (weight bytes of the
+sweep / decode time); prefill TFLOP/s, the roofline of the dominant kernel
+(tensor-core prefill), the decode roofline, the end-to-end number through
+host buffers, clocks and the CPU-oracle baseline are extra keys.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gq|reference]
+Under torchrun (N > 1) every rank runs its own replica of the sweep (weak
+scaling); rank 0 prints.  `--impl reference` times the CPU oracle on the host
+cores for the same metric (bounded sample per step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "Q4_0 mul_mat weight GB/s (decode N=1) and TFLOP/s (prefill N=512) vs roofline"
+DECODE_N, PREFILL_N = 1, 512
+WORKLOAD = ("7B-like 32-layer Q4_0 weight sweep: per layer q/k/v/o 4096x4096, gate/up 11008x4096, "
+            "down 4096x11008 (3.64 GB of weights); decode N=1 then prefill N=512")
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def layer_inputs():
+    """Per layer: which activation feeds which matrix (q/k/v share one input, gate/up another)."""
+    # input ids: 0 attn input (K=4096), 1 attn-output input (4096), 2 ffn input (4096), 3 down input (11008)
+    return [0, 0, 0, 1, 2, 2, 3], [4096, 4096, 4096, 11008]
+
+
+def make_weights(n_layers, rank):
+    host = []
+    for layer in range(n_layers):
+        for j, (_, M, K) in enumerate(synth.LAYER_MATRICES):
+            seed = synth.seed_for(5, j, layer) + 7919 * rank
+            host.append((M, K, synth.q4_0_weights(M, K, seed)))
+    return host
+
+
+def make_acts(n_layers, N, rank, tag):
+    _, ks = layer_inputs()
+    return [[synth.activations(N, K, synth.seed_for(5, 8 + i, layer) + 104729 * rank + tag)
+             for i, K in enumerate(ks)] for layer in range(n_layers)]
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index=0):
+        self.rows, self.proc, self.dev = [], None, device_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 7:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "", 1).isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+def oracle_decode_rate(weights, acts, budget_s, nthreads):
+    """Oracle MUL_MAT at N=1 over matrices of the sweep until budget_s elapses.
+    Returns (weight GB/s, matrices done, weight bytes done)."""
+    import oracle
+    orc = oracle.get()
+    order, _ = layer_inputs()
+    done_bytes, done, t0 = 0, 0, time.perf_counter()
+    for idx, (M, K, W) in enumerate(weights):
+        layer, j = divmod(idx, len(order))
+        orc.mul_mat(W, M, K, acts[layer][order[j]], nthreads=nthreads)
+        done_bytes += W.nbytes
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return done_bytes / dt / 1e9, done, done_bytes, dt
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import oracle
+    nthreads = os.cpu_count() or 1
+    oracle.get()
+    layers = 2
+    weights = make_weights(layers, 0)
+    acts = make_acts(layers, DECODE_N, 0, 0)
+    for _ in range(args.warmup):
+        oracle_decode_rate(weights[:1], acts, 1e9, nthreads)
+    total_bytes, total_t, mats = 0, 0.0, 0
+    for _ in range(args.steps):
+        _, n, b, dt = oracle_decode_rate(weights, acts, args.ref_budget, nthreads)
+        total_bytes += b
+        total_t += dt
+        mats += n
+    value = total_bytes / total_t / 1e9
+    sample = (f"oracle MUL_MAT at N=1 over the first {layers} layers of the sweep "
+              f"({sum(w.nbytes for _, _, w in weights) / 1e6:.0f} MB of Q4_0 weights), "
+              f"{mats} matrix calls over {args.steps} steps, fp64 sums, {nthreads} OpenMP threads")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_t / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sampled": True},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU leg
+def run_gpu(args, rank, world, dist):
+    import torch
+    import quantized_block_q4_gb300 as gq
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = load_peaks()
+    order, ks = layer_inputs()
+    L = args.layers
+
+    t_gen = time.perf_counter()
+    host_w = make_weights(L, rank)
+    W = [torch.from_numpy(w).to(dev) for _, _, w in host_w]
+    shapes = [(M, K) for M, K, _ in host_w]
+    acts1 = make_acts(L, DECODE_N, rank, 0)
+    actsP = make_acts(L, PREFILL_N, rank, 1)
+    X1 = [[torch.from_numpy(a).to(dev) for a in la] for la in acts1]
+    XP = [[torch.from_numpy(a).to(dev) for a in la] for la in actsP]
+    XPb = [[torch.empty(x.shape, dtype=torch.int16, device=dev) for x in la] for la in XP]
+    Y1 = [torch.empty(DECODE_N, M, device=dev) for M, _ in shapes]
+    YP = [torch.empty(PREFILL_N, M, device=dev) for M, _ in shapes]
+    gen_s = time.perf_counter() - t_gen
+    wbytes = sum(w.numel() for w in W)
+    flops_p = sum(2.0 * M * K * PREFILL_N for M, K in shapes)
+    dec_alg_bytes = sum(M * K * 18 // 32 + 4 * DECODE_N * K + 4 * DECODE_N * M for M, K in shapes)
+
+    s = torch.cuda.Stream(device=dev)
+
+    def decode_pass():
+        for i, (M, K) in enumerate(shapes):
+            layer, j = divmod(i, len(order))
+            gq.gq_mul_mat_q4_0(W[i], M, K, X1[layer][order[j]], DECODE_N, Y1[i], stream=s)
+
+    ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in shapes]
+
+    def prefill_pass(record):
+        # activation conversion for each layer's inputs, then the tensor-core MUL_MATs
+        for layer in range(L):
+            for i, x in enumerate(XP[layer]):
+                gq.gq_f32_to_bf16(x, XPb[layer][i], x.numel(), stream=s)
+            for j in range(len(order)):
+                i = layer * len(order) + j
+                M, K = shapes[i]
+                if record:
+                    ev_pairs[i][0].record(s)
+                gq.gq_mul_mat_q4_0_bf16x(W[i], M, K, XPb[layer][order[j]], PREFILL_N, YP[i], stream=s)
+                if record:
+                    ev_pairs[i][1].record(s)
+
+    # decode sweep as one CUDA graph (224 short launches)
+    with torch.cuda.stream(s):
+        decode_pass()
+        prefill_pass(False)
+    torch.cuda.synchronize(dev)
+    gq.gq_sync_status(s)
+    g_dec = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g_dec, stream=s):
+            decode_pass()
+    torch.cuda.synchronize(dev)
+
+    def step(record):
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        with torch.cuda.stream(s):
+            e0.record(s)
+            g_dec.replay()
+            e1.record(s)
+            prefill_pass(record)
+            e2.record(s)
+        return e0, e1, e2
+
+    for _ in range(max(args.warmup, 3)):
+        step(False)
+    torch.cuda.synchronize(dev)
+    gq.gq_sync_status(s)
+
+    clk = ClockSampler(local)
+    clk.start()
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.perf_counter()
+    marks = []
+    k3_ms = 0.0
+    for _ in range(args.steps):
+        marks.append(step(True))
+        torch.cuda.synchronize(dev)  # per-step, so the K3 events of this step can be read
+        k3_ms += sum(a.elapsed_time(b) for a, b in ev_pairs)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t_wall0
+    if dist is not None:
+        dist.barrier()
+    clocks = clk.stop()
+    gq.gq_sync_status(s)
+
+    dec_ms = sum(a.elapsed_time(b) for a, b, _ in marks)
+    pre_ms = sum(b.elapsed_time(c) for _, b, c in marks)
+    step_ms = sum(a.elapsed_time(c) for a, _, c in marks)
+    if dist is not None:
+        t = torch.tensor([dec_ms, pre_ms, step_ms, k3_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dec_ms, pre_ms, step_ms, k3_ms = t.tolist()
+
+    K_ = args.steps
+    value = world * wbytes * K_ / (dec_ms * 1e-3) / 1e9
+    prefill_tflops = world * flops_p * K_ / (pre_ms * 1e-3) / 1e12
+    k3_avg_us = k3_ms / (K_ * len(shapes)) * 1e3
+    k3_tflops = flops_p * K_ / (k3_ms * 1e-3) / 1e12
+    dec_avg_us = dec_ms / (K_ * len(shapes)) * 1e3
+    dec_gbs_alg = dec_alg_bytes * K_ / (dec_ms * 1e-3) / 1e9
+
+    # ---- end to end through the public API with host buffers (decode, N = 1)
+    e2e = run_e2e(gq, torch, dev, s, W, shapes, acts1, order, L, args)
+    if dist is not None:
+        t = torch.tensor([e2e["ms"]], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e["ms"] = t.item()
+    e2e_value = world * wbytes / (e2e["ms"] * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        nthreads = os.cpu_count() or 1
+        gbs, n, b, dt = oracle_decode_rate(host_w, acts1, args.cpu_budget, nthreads)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+               "sample": f"oracle MUL_MAT at N=1 on the first {n} matrices of the same sweep "
+                         f"({b / 1e6:.0f} MB of weights, {dt:.1f} s), fp64 sums"}
+
+    if rank != 0:
+        return 0
+    sust = peaks["bf16_tflops_sustained"]
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K_,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(step_ms / K_, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16 x f16 -> f32 (decode), bf16 x bf16 -> f32 (prefill)", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "layers": L, "matrices": len(shapes), "decode_n": DECODE_N,
+                   "prefill_n": PREFILL_N, "weight_bytes": wbytes,
+                   "l2": "inputs larger than L2 (3.64 GB of weights streamed per pass)",
+                   "parallelism": f"replicas x{world}"},
+        "decode": {"value": round(value, 2), "unit": "GB/s", "ms": round(dec_ms / K_, 4),
+                   "avg_launch_us": round(dec_avg_us, 3)},
+        "prefill": {"value": round(prefill_tflops, 2), "unit": "TFLOP/s", "ms": round(pre_ms / K_, 4),
+                    "includes": "fp32->bf16 activation conversion + tensor-core MUL_MAT"},
+        "roofline": {"kernel": "k_prefill_q4_0 (tcgen05 prefill)", "bound": "tensor",
+                     "achieved": round(k3_tflops, 2), "peak": sust, "unit": "TFLOP/s",
+                     "frac": round(k3_tflops / sust, 4), "traffic": None,
+                     "peak_kind": f"bf16 sustained ({peaks['source']})", "avg_launch_us": round(k3_avg_us, 3),
+                     "per_launch": "2*M*K*512 flops of the launch's matrix"},
+        "roofline_decode": {"kernel": "k_decode_q4_0 (decode)", "bound": "hbm", "achieved": round(dec_gbs_alg, 1),
+                            "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": round(dec_gbs_alg / peaks["hbm_gbs"], 4), "traffic": None,
+                            "peak_kind": f"HBM copy ({peaks['source']})",
+                            "per_launch": "M*K*18/32 + 4*N*K + 4*N*M bytes; graph-replay time incl. launch gaps"},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
+                "d2h_bytes_per_step": e2e["d2h"],
+                "path": "pinned host X -> device, gq_mul_mat_q4_0, Y -> pinned host, per matrix (decode sweep)"},
+        "gpu_launches": K_ * (len(shapes) + len(shapes) + L * len(ks)),
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "wall_s": round(wall, 3), "setup_s": round(gen_s, 1),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_e2e(gq, torch, dev, s, W, shapes, acts1, order, L, args):
+    """Decode sweep through gq_mul_mat_q4_0 with host buffers: every step copies
+    each layer's activations from pinned host memory and every result back."""
+    hx = [[torch.from_numpy(a).pin_memory() for a in la] for la in acts1]
+    dx = [[torch.empty(a.shape, dtype=torch.float32, device=dev) for a in la] for la in acts1]
+    dy = [torch.empty(DECODE_N, M, device=dev) for M, _ in shapes]
+    hy = [torch.empty(DECODE_N, M).pin_memory() for M, _ in shapes]
+
+    def one():
+        for layer in range(L):
+            for i in range(len(hx[layer])):
+                dx[layer][i].copy_(hx[layer][i], non_blocking=True)
+            for j in range(len(order)):
+                i = layer * len(order) + j
+                M, K = shapes[i]
+                gq.gq_mul_mat_q4_0(W[i], M, K, dx[layer][order[j]], DECODE_N, dy[i], stream=s)
+                hy[i].copy_(dy[i], non_blocking=True)
+
+    with torch.cuda.stream(s):
+        one()
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            one()
+    torch.cuda.synchronize(dev)
+    for _ in range(3):
+        with torch.cuda.stream(s):
+            g.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(args.steps):
+            g.replay()
+        e1.record(s)
+    e1.synchronize()
+    h2d = sum(t.numel() * 4 for la in hx for t in la)
+    d2h = sum(t.numel() * 4 for t in hy)
+    return {"ms": e0.elapsed_time(e1) / args.steps, "h2d": h2d, "d2h": d2h}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gq", "reference"], default="gq")
+    ap.add_argument("--layers", type=int, default=synth.N_LAYERS)
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=5.0, help="seconds of oracle work per reference step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group(backend=backend)
+        dist = tdist
+    try:
+        if args.impl == "reference":
+            return run_reference(args, rank, world)
+        return run_gpu(args, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())
