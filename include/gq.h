@@ -79,6 +79,22 @@ gq_status gq_mul_mat_q4_0(const void *W, int64_t M, int64_t K, const float *X, i
 gq_status gq_mul_mat_q4_0_bf16x(const void *W, int64_t M, int64_t K, const uint16_t *X_bf16, int64_t N,
                                 float *Y, void *stream);
 
+/* Same result as the N >= 64 path of gq_mul_mat_q4_0 (bf16 activations,
+ * tensor-core kernel), for any N >= 1, but with no device allocation: the
+ * bf16 copy of X goes to a fixed 12 MiB array inside the library instead of
+ * cudaMallocAsync scratch.  The pages have no counterpart; it exists for
+ * callers that cannot let a library allocate device memory (memory pools that
+ * own the whole device, fixed arenas, allocation-free hot loops).
+ *  - Needs K % 256 == 0 and N*K <= 6291456 (GQ_ERR_SHAPE otherwise), W 16-byte
+ *    aligned, X and Y 4-byte aligned.
+ *  - Every GPU that loads the library holds the 12 MiB array until the
+ *    process exits.  The first call on a device looks up the array's device
+ *    address (cudaGetSymbolAddress) with that device current; make that first
+ *    call before any stream capture.
+ *  - All calls share the array: calls whose GPU work overlaps race on it. */
+gq_status gq_mul_mat_q4_0_noalloc(const void *W, int64_t M, int64_t K, const float *X, int64_t N, float *Y,
+                                  void *stream);
+
 /* y[i] = bf16(x[i]), round to nearest even (NaN stays NaN), for n elements. */
 gq_status gq_f32_to_bf16(const float *x, uint16_t *y, int64_t n, void *stream);
 

@@ -39,6 +39,7 @@ SIGNATURES = {
     "gq_dequant_q4_0": (_i32, [_vp, _i64, _i64, _vp, _vp]),
     "gq_mul_mat_q4_0": (_i32, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "gq_mul_mat_q4_0_bf16x": (_i32, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
+    "gq_mul_mat_q4_0_noalloc": (_i32, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "gq_f32_to_bf16": (_i32, [_vp, _vp, _i64, _vp]),
     "gq_sync_status": (_i32, [_vp]),
     "gq_set_option": (_i32, [_i32, _i64]),
@@ -113,6 +114,12 @@ def gq_mul_mat_q4_0(W, M: int, K: int, X, N: int, Y, stream=None) -> None:
 
 def gq_mul_mat_q4_0_bf16x(W, M: int, K: int, X_bf16, N: int, Y, stream=None) -> None:
     _check(_lib.gq_mul_mat_q4_0_bf16x(_ptr(W), M, K, _ptr(X_bf16), N, _ptr(Y), _stream(stream)))
+
+
+def gq_mul_mat_q4_0_noalloc(W, M: int, K: int, X, N: int, Y, stream=None) -> None:
+    """Tensor-core MUL_MAT that allocates no device memory (fixed in-library
+    scratch); for callers whose memory must come only from their own pool."""
+    _check(_lib.gq_mul_mat_q4_0_noalloc(_ptr(W), M, K, _ptr(X), N, _ptr(Y), _stream(stream)))
 
 
 def gq_f32_to_bf16(x, y, n: int, stream=None) -> None:

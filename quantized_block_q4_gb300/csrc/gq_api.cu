@@ -170,6 +170,16 @@ static gq_status mul_mat_prefill_bf16(const void* W, int64_t M, int64_t K, const
   return e == cudaSuccess ? GQ_OK : cuda_fail(e, "prefill launch");
 }
 
+namespace gq {
+gq_status api_fail(gq_status st, const char* msg) { return fail(st, "%s", msg); }
+gq_status api_check_device() { return check_device(); }
+gq_status api_check_mm_shape(int64_t M, int64_t K, int64_t N) { return check_mm_shape(M, K, N); }
+gq_status api_prefill_bf16(const void* W, int64_t M, int64_t K, const uint16_t* X_bf16, int64_t N, float* Y,
+                           cudaStream_t s) {
+  return mul_mat_prefill_bf16(W, M, K, X_bf16, N, Y, s);
+}
+}  // namespace gq
+
 extern "C" {
 
 size_t gq_q4_0_nbytes(int64_t M, int64_t K) {

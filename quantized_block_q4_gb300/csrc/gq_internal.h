@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "gq.h"
+
 namespace gq {
 
 constexpr int kQK = 32;          // weights per block_q4_0
@@ -45,5 +47,12 @@ cudaError_t launch_prefill(const CUtensorMap* tmW, const CUtensorMap* tmX, int64
                            int64_t K, float* Y, uint64_t wait_limit_ns, cudaStream_t s);
 void prefill_boxes(int64_t N, uint32_t* w_box_x_bytes, uint32_t* w_box_rows, uint32_t* x_box_k,
                    uint32_t* x_box_rows);
+
+// ---- helpers of the C ABI (gq_api.cu) for entry points defined in other files
+gq_status api_fail(gq_status st, const char* msg);  // records the per-thread error text
+gq_status api_check_device();
+gq_status api_check_mm_shape(int64_t M, int64_t K, int64_t N);
+gq_status api_prefill_bf16(const void* W, int64_t M, int64_t K, const uint16_t* X_bf16, int64_t N, float* Y,
+                           cudaStream_t s);
 
 }  // namespace gq
