@@ -5,17 +5,26 @@
 // per CTA ("GGUF loading, mmap and tensor placement", step six: the MUL_MAT
 // probe with a 512-token batch; "Binding GGUF weights to the compute graph",
 // section 2.3: the kernel reads the blocks and dequantises them itself).
-// Roles (192 threads):
+// Roles (320 threads):
 //   warp 0  TMA producer: raw W rows (128 x 144 bytes = 256 weights each) and
 //           bf16 x tiles (BN x 64, 128-byte swizzle) into shared-memory rings.
-//   warp 1  allocates BN TMEM columns; one thread issues tcgen05.mma
-//           (M=128, N=BN, K=16, bf16 x bf16 -> fp32 in TMEM) and commits to
-//           the rings' "empty" barriers.
-//   warps 2-5  dequantise: thread i owns W row i of the tile, expands its two
-//           blocks per 64-k step to w = d*(q-8) in fp32 (exact), rounds once to
-//           bf16 and writes the 128-byte-swizzled K-major A tile; then read the
-//           accumulator with tcgen05.ld (warp w reads TMEM lanes 32*(w%4)..)
-//           and store fp32 Y, consecutive lanes writing consecutive m.
+//   warp 1  allocates 512 TMEM columns: the fp32 accumulator (BN columns) and
+//           a ring of A stages (32 columns = 64 bf16 k each).  One thread
+//           issues tcgen05.mma with A read from tensor memory and B (x) from
+//           shared memory (M=128, N=BN, K=16, bf16 x bf16 -> fp32) and
+//           commits to the rings' "empty" barriers.
+//   warps 2-9  dequantise: warps 2-5 take the even 64-k steps, warps 6-9 the
+//           odd ones; a thread owns one W row of the tile, i.e. one TMEM lane,
+//           and stores RN_bf16(d*(q-8)) for the step's 64 weights into its
+//           lane with one tcgen05.st.  Then they read the accumulator with
+//           tcgen05.ld (warp w reads TMEM lanes 32*(w%4)..; the two groups
+//           split the columns) and store fp32 Y, consecutive lanes writing
+//           consecutive m.
+// Dequantisation to bf16 with a single rounding, in bf16x2 arithmetic: the
+// fp16 scale is split exactly as d = d_hi + d_lo (both bf16; d_lo holds the
+// last 3 bits), q - 8 is formed exactly as (128 + q) - 136 from the bit
+// pattern 0x4300 | q, q'*d_lo is exact in bf16, and one fused
+// fma.rn.bf16x2(q', d_hi, q'*d_lo) rounds d*(q-8) once.
 // Every wait is bounded; a timeout sets the device error word, the roles
 // drain what they issued, TMEM is released and the CTA exits.
 #include <algorithm>
@@ -76,37 +85,60 @@ struct PrefillCfg {
   static constexpr int kBK = 64;        // k per MMA stage: one 128-byte row of bf16
   static constexpr int kRawK = 256;     // k per raw W stage
   static constexpr int kRawRow = 144;   // bytes of 8 blocks
-  static constexpr int RS = 2, AS = 4, BS = (BN == 256 ? 3 : 4);
+  static constexpr int RS = 3, BS = (BN == 256 ? 5 : 8);
+  static constexpr int kACols = kBK / 2;               // TMEM columns per A stage
+  static constexpr int AS = (512 - BN) / kACols;       // A stages in the rest of TMEM
+  static constexpr int kTmemCols = 512;
   static constexpr int kRawBytes = kBM * kRawRow;  // 18432
-  static constexpr int kABytes = kBM * 128;        // 16384
   static constexpr int kBBytes = BN * 128;
   static constexpr int kOffB = 0;
-  static constexpr int kOffA = kOffB + BS * kBBytes;
-  static constexpr int kOffRaw = kOffA + AS * kABytes;
+  static constexpr int kOffRaw = kOffB + BS * kBBytes;
   static constexpr int kOffBar = kOffRaw + RS * kRawBytes;
   static constexpr int kNBar = 2 * RS + 2 * AS + 2 * BS + 1;
   static constexpr int kOffTmem = kOffBar + kNBar * 8;
   static constexpr int kOffAbort = kOffTmem + 8;
   static constexpr int kSmem = kOffAbort + 8 + 1024;  // + slack to align the base to 1024
-  static constexpr int kThreads = 192;
+  static constexpr int kDeqWarps = 8;
+  static constexpr int kThreads = 32 * (2 + kDeqWarps);
 };
 
-// Two 4-bit codes -> bf16x2 of d*(q-8): exact in fp32, one rounding to bf16.
-__device__ __forceinline__ uint32_t deq_pair(uint32_t q0, uint32_t q1, float d) {
-  const float f0 = __uint_as_float(0x4B000000u | q0) - 8388616.0f;  // 2^23 + q - (2^23 + 8) = q - 8
-  const float f1 = __uint_as_float(0x4B000000u | q1) - 8388616.0f;
-  __nv_bfloat162 h = __floats2bfloat162_rn(f0 * d, f1 * d);
-  return *reinterpret_cast<uint32_t*>(&h);
+__device__ __forceinline__ uint32_t scale_pair(uint32_t qp, uint32_t dhi2, uint32_t dlo2) {
+  return bfma2_u32(qp, dhi2, bmul2_u32(qp, dlo2));
 }
 
-// 8 codes from two words of code bytes (low or high nibbles) -> 8 bf16.
-__device__ __forceinline__ uint4 deq_chunk(uint32_t qa, uint32_t qb, int sh, float d) {
-  uint4 o;
-  o.x = deq_pair((qa >> sh) & 0xF, (qa >> (sh + 8)) & 0xF, d);
-  o.y = deq_pair((qa >> (sh + 16)) & 0xF, (qa >> (sh + 24)) & 0xF, d);
-  o.z = deq_pair((qb >> sh) & 0xF, (qb >> (sh + 8)) & 0xF, d);
-  o.w = deq_pair((qb >> (sh + 16)) & 0xF, (qb >> (sh + 24)) & 0xF, d);
-  return o;
+// Four consecutive code bytes c0..c3 -> bf16x2 pairs of RN(d*(q-8)):
+// lo01 = (c0.lo, c1.lo), lo23 = (c2.lo, c3.lo), hi01 = (c0.hi, c1.hi), hi23 = (c2.hi, c3.hi).
+__device__ __forceinline__ void word_to_bf16(uint32_t q, uint32_t dhi2, uint32_t dlo2, uint32_t& lo01,
+                                             uint32_t& lo23, uint32_t& hi01, uint32_t& hi23) {
+  const uint32_t kMagic = 0x43004300u;  // bf16 128 in both halves
+  const uint32_t kSub = 0x43084308u;    // bf16 136
+  const uint32_t p = prmt(q, 0u, 0x3120u);  // bytes c0 c2 c1 c3
+  lo01 = scale_pair(bsub2_u32(lop3_and_or(p, 0x000F000Fu, kMagic), kSub), dhi2, dlo2);
+  lo23 = scale_pair(bsub2_u32(lop3_and_or(p >> 8, 0x000F000Fu, kMagic), kSub), dhi2, dlo2);
+  hi01 = scale_pair(bsub2_u32(lop3_and_or(p >> 4, 0x000F000Fu, kMagic), kSub), dhi2, dlo2);
+  hi23 = scale_pair(bsub2_u32(lop3_and_or(p >> 12, 0x000F000Fu, kMagic), kSub), dhi2, dlo2);
+}
+
+// Exact split of an fp16 scale into bf16 d_hi + d_lo, each broadcast to both halves.
+__device__ __forceinline__ void split_scale(uint32_t d_bits, uint32_t& dhi2, uint32_t& dlo2) {
+  const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(d_bits)));
+  const __nv_bfloat16 hi = __float2bfloat16_rn(d);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(d - __bfloat162float(hi));  // exact: at most 3 bits remain
+  const uint32_t h = *reinterpret_cast<const uint16_t*>(&hi), l = *reinterpret_cast<const uint16_t*>(&lo);
+  dhi2 = h | (h << 16);
+  dlo2 = l | (l << 16);
+}
+
+// One block's 16 code bytes (4 words, k-consecutive) -> 16 bf16x2 words
+// holding k = 0..31 of the block in order (o[i] = k 2i, 2i+1).
+__device__ __forceinline__ void block_words(const uint32_t (&q)[4], uint32_t d_bits, uint32_t* o) {
+  uint32_t dhi2, dlo2;
+  split_scale(d_bits, dhi2, dlo2);
+  // low nibbles of bytes 0..15 are k 0..15, high nibbles are k 16..31
+  word_to_bf16(q[0], dhi2, dlo2, o[0], o[1], o[8], o[9]);
+  word_to_bf16(q[1], dhi2, dlo2, o[2], o[3], o[10], o[11]);
+  word_to_bf16(q[2], dhi2, dlo2, o[4], o[5], o[12], o[13]);
+  word_to_bf16(q[3], dhi2, dlo2, o[6], o[7], o[14], o[15]);
 }
 
 // Bounded wait on the last phase issued into each slot of a ring (drain path).
@@ -121,7 +153,7 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int slots, uint32_t i
 }
 
 template <int BN>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(PrefillCfg<BN>::kThreads, 1)
     k_prefill_q4_0(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int N, int M,
                    int K, float* __restrict__ Y, uint64_t limit_ns, uint32_t* err) {
   using C = PrefillCfg<BN>;
@@ -149,10 +181,10 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::RS; ++i) {
       mbar_init(smem_u32(&raw_full[i]), 1);
-      mbar_init(smem_u32(&raw_empty[i]), 4);
+      mbar_init(smem_u32(&raw_empty[i]), C::kDeqWarps);
     }
     for (int i = 0; i < C::AS; ++i) {
-      mbar_init(smem_u32(&a_full[i]), 4);
+      mbar_init(smem_u32(&a_full[i]), 4);  // the 4 warps of the group that owns this k step
       mbar_init(smem_u32(&a_empty[i]), 1);
     }
     for (int i = 0; i < C::BS; ++i) {
@@ -164,7 +196,7 @@ __global__ void __launch_bounds__(192, 1)
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), BN);
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -213,12 +245,11 @@ __global__ void __launch_bounds__(192, 1)
         if (!mbar_wait_bounded(smem_u32(&a_full[as]), (ks / C::AS) & 1, limit_ns, abort_flag, err)) break;
         if (!mbar_wait_bounded(smem_u32(&b_full[bs]), (ks / C::BS) & 1, limit_ns, abort_flag, err)) break;
         tc_fence_after();
-        const uint32_t a_addr = sbase + C::kOffA + as * C::kABytes;
+        const uint32_t a_tmem = tmem_base + BN + as * C::kACols;
         const uint32_t b_addr = sbase + C::kOffB + bs * C::kBBytes;
 #pragma unroll
         for (int kk = 0; kk < C::kBK / 16; ++kk)
-          umma_bf16_ss(tmem_base, umma_desc_sw128(a_addr + kk * 32), umma_desc_sw128(b_addr + kk * 32), idesc,
-                       (ks | kk) != 0);
+          umma_bf16_ts(tmem_base, a_tmem + kk * 8, umma_desc_sw128(b_addr + kk * 32), idesc, (ks | kk) != 0);
         umma_commit(smem_u32(&a_empty[as]));
         umma_commit(smem_u32(&b_empty[bs]));
       }
@@ -231,13 +262,15 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     // ------------------------------------------------------------ dequant + epilogue
     const int quad = warp & 3;
+    const int grp = (warp - 2) >> 2;   // 0: even 64-k steps, 1: odd 64-k steps
     const int row = quad * 32 + lane;  // W row within the tile == TMEM lane
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
     bool live = true;
     for (int r = 0; r < nr; ++r) {
       const int rslot = r % C::RS;
       if (live) live = mbar_wait_bounded(smem_u32(&raw_full[rslot]), (r / C::RS) & 1, limit_ns, abort_flag, err);
       live = __all_sync(0xFFFFFFFFu, live);
-      uint32_t w[36];
+      uint32_t w[36];  // the whole raw row: 8 blocks
       if (live) {
         const uint4* src = reinterpret_cast<const uint4*>(smem + C::kOffRaw + rslot * C::kRawBytes + row * C::kRawRow);
 #pragma unroll
@@ -249,43 +282,36 @@ __global__ void __launch_bounds__(192, 1)
       __syncwarp();
       if (live && lane == 0) mbar_arrive(smem_u32(&raw_empty[rslot]));
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 4; ++j) {  // pair j of the raw row = 64-k step 4r + j
+        if ((j & 1) != grp) continue;  // warp-uniform: the groups alternate steps
         const int ks = r * 4 + j, as = ks % C::AS;
         if (live) live = mbar_wait_bounded(smem_u32(&a_empty[as]), ((ks / C::AS) & 1) ^ 1, limit_ns, abort_flag, err);
         live = __all_sync(0xFFFFFFFFu, live);
         if (live) {
-          // blocks 2j (even) and 2j+1 (odd) of the raw row = words 9j .. 9j+8
+          // blocks 2j (even) and 2j+1 (odd) of the row = words 9j .. 9j+8
           const uint32_t W0 = w[9 * j], W1 = w[9 * j + 1], W2 = w[9 * j + 2], W3 = w[9 * j + 3], W4 = w[9 * j + 4];
-          const float d0 = __half2float(__ushort_as_half(static_cast<uint16_t>(W0 & 0xFFFFu)));
-          const float d1 = __half2float(__ushort_as_half(static_cast<uint16_t>(W4 >> 16)));
           const uint32_t q0[4] = {prmt(W0, W1, 0x5432u), prmt(W1, W2, 0x5432u), prmt(W2, W3, 0x5432u),
                                   prmt(W3, W4, 0x5432u)};
           const uint32_t q1[4] = {w[9 * j + 5], w[9 * j + 6], w[9 * j + 7], w[9 * j + 8]};
-          uint8_t* arow = smem + C::kOffA + as * C::kABytes + row * 128;
-          const int sw = row & 7;
-          // chunk c holds k = 8c .. 8c+7 of this 64-k step
-          *reinterpret_cast<uint4*>(arow + ((0 ^ sw) << 4)) = deq_chunk(q0[0], q0[1], 0, d0);
-          *reinterpret_cast<uint4*>(arow + ((1 ^ sw) << 4)) = deq_chunk(q0[2], q0[3], 0, d0);
-          *reinterpret_cast<uint4*>(arow + ((2 ^ sw) << 4)) = deq_chunk(q0[0], q0[1], 4, d0);
-          *reinterpret_cast<uint4*>(arow + ((3 ^ sw) << 4)) = deq_chunk(q0[2], q0[3], 4, d0);
-          *reinterpret_cast<uint4*>(arow + ((4 ^ sw) << 4)) = deq_chunk(q1[0], q1[1], 0, d1);
-          *reinterpret_cast<uint4*>(arow + ((5 ^ sw) << 4)) = deq_chunk(q1[2], q1[3], 0, d1);
-          *reinterpret_cast<uint4*>(arow + ((6 ^ sw) << 4)) = deq_chunk(q1[0], q1[1], 4, d1);
-          *reinterpret_cast<uint4*>(arow + ((7 ^ sw) << 4)) = deq_chunk(q1[2], q1[3], 4, d1);
+          uint32_t o[32];
+          block_words(q0, W0 & 0xFFFFu, o);
+          block_words(q1, W4 >> 16, o + 16);
+          tmem_st_32x32b_x32(lane_addr + BN + as * C::kACols, o);
+          tmem_st_wait();
         }
-        fence_proxy_async_smem();
+        tc_fence_before();
         __syncwarp();
         if (live && lane == 0) mbar_arrive(smem_u32(&a_full[as]));
       }
     }
-    // epilogue
+    // epilogue: this group's half of the accumulator columns
     if (live) live = mbar_wait_bounded(smem_u32(acc_full), 0, limit_ns, abort_flag, err);
     live = __all_sync(0xFFFFFFFFu, live);
     tc_fence_after();
     if (live) {
       const int m = m0 + row;
 #pragma unroll 1
-      for (int cb = 0; cb < BN / 32; ++cb) {
+      for (int cb = grp * (BN / 64); cb < (grp + 1) * (BN / 64); ++cb) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + cb * 32, v);
         tmem_ld_wait();
@@ -304,7 +330,7 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, BN);
+    tmem_dealloc(tmem_base, C::kTmemCols);
   }
 }
 

@@ -289,3 +289,21 @@ def test_prefill_threshold_option_switches_kernels():
     b = run_mm(W, X, M, K)                                      # decode path
     assert_mul_mat_close(a, y_ref, s_ref, "tensor-core path")
     assert_mul_mat_close(b, y_ref, s_ref, "decode path")
+
+
+def test_prefill_dequant_is_single_rounded_bf16():
+    """One-hot activation rows: every output is one weight times 1, so the
+    tensor-core path must return exactly RN_bf16(d*(q-8)) (torch's bf16
+    rounding of the oracle's fp32 dequant)."""
+    M, K, N = 300, 1024, 96
+    W = synth.q4_0_weights(M, K, seed=7100)
+    ks = np.random.Generator(np.random.SFC64(7101)).integers(0, K, N)
+    X = np.zeros((N, K), dtype=np.float32)
+    X[np.arange(N), ks] = 1.0
+    xb = torch.from_numpy(X).cuda().to(torch.bfloat16)
+    Y = torch.empty(N, M, device="cuda")
+    gq.gq_mul_mat_q4_0_bf16x(dev(W), M, K, xb.view(torch.int16), N, Y)
+    torch.cuda.synchronize()
+    w_bf16 = torch.from_numpy(oracle.get().dequant(W, M, K)).to(torch.bfloat16).float().numpy()
+    expect = w_bf16[:, ks].T                                  # [N, M]
+    assert same_f32_bits(np.abs(Y.cpu().numpy()), np.abs(expect)).all()
