@@ -23,6 +23,7 @@ thread_local std::string t_last_error;
 std::atomic<int64_t> g_prefill_min_n{64};
 std::atomic<int64_t> g_force_generic{0};
 std::atomic<int64_t> g_wait_limit_ns{2000000000LL};
+std::atomic<int64_t> g_early_w{0};
 
 gq_status fail(gq_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 gq_status fail(gq_status st, const char* fmt, ...) {
@@ -150,7 +151,8 @@ static gq_status mul_mat_decode(const void* W, int64_t M, int64_t K, const float
   gq_status st = make_tmap(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, row_bytes, static_cast<uint64_t>(M), row_bytes,
                            bx, by, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (st != GQ_OK) return st;
-  cudaError_t e = launch_decode(&tm, X, N, M, K, Y, static_cast<uint64_t>(g_wait_limit_ns.load()), s);
+  cudaError_t e = launch_decode(&tm, X, N, M, K, Y, static_cast<uint64_t>(g_wait_limit_ns.load()),
+                                static_cast<int>(g_early_w.load()), s);
   return e == cudaSuccess ? GQ_OK : cuda_fail(e, "decode launch");
 }
 
@@ -307,6 +309,9 @@ gq_status gq_set_option(gq_option opt, int64_t value) {
       if (value < 1000) return fail(GQ_ERR_SHAPE, "wait limit must be >= 1000 ns");
       g_wait_limit_ns = value;
       return GQ_OK;
+    case GQ_OPT_WEIGHTS_STATIC:
+      g_early_w = value ? 1 : 0;
+      return GQ_OK;
   }
   return fail(GQ_ERR_SHAPE, "unknown option %d", static_cast<int>(opt));
 }
@@ -316,6 +321,7 @@ int64_t gq_get_option(gq_option opt) {
     case GQ_OPT_PREFILL_MIN_N: return g_prefill_min_n.load();
     case GQ_OPT_FORCE_GENERIC: return g_force_generic.load();
     case GQ_OPT_WAIT_LIMIT_NS: return g_wait_limit_ns.load();
+    case GQ_OPT_WEIGHTS_STATIC: return g_early_w.load();
   }
   return -1;
 }

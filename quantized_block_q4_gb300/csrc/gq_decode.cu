@@ -11,9 +11,13 @@
 //    stage holds KW such boxes, one per consumer warp (split-K inside the CTA).
 //  * Consumer warps run mma.sync m16n8k16 (fp16 in, fp32 accumulate) with the
 //    16 W rows as the A operand and up to 8 tokens per n8 tile as B.  A holds
-//    the integer codes (q - 8) in fp16, which is exact; the block scale d is
-//    applied in fp32 to the per-block partial product, so W is never rounded.
-//    Only x is rounded (to fp16, relative error <= 2^-11 per element).
+//    codes straight from one LOP3 per pair: the fp16 bit pattern 0x6400 | q is
+//    exactly 1024 + q (low nibbles) and 0x6400 | (q << 4) is 1024 + 16q (high
+//    nibbles, met by x/16 in B).  The exact bias this adds, 1032*x + 1152*(x/16)
+//    summed over the block, is precomputed per block and token and enters as
+//    the MMA's C input with a minus sign, so each block's MMA pair yields
+//    sum (q-8)*x directly.  The block scale d is then applied in fp32 to that
+//    partial, so W is never rounded; only x is (fp16, relative <= 2^-11).
 //  * The four bytes of codes a lane needs are read straight from the raw
 //    18-byte blocks: two blocks (36 bytes) form nine aligned 32-bit words, and
 //    one PRMT rebuilds the word that straddles the scale of the even block.
@@ -22,6 +26,11 @@
 //    (a contraction does not care how k is ordered, only that A and B agree).
 //  * The k-warps' partial sums of a 16-row tile are reduced through shared
 //    memory; CTAs loop over tiles persistently.
+//  * Launched with programmatic dependent launch: the grid may start while
+//    the previous kernel on the stream drains; X is read and Y written only
+//    after griddepcontrol.wait.  With `early_w` set, the producer also starts
+//    streaming W before that wait (valid when the previous kernel does not
+//    write W, as in weight-stationary inference).
 #include <algorithm>
 #include <cuda_fp16.h>
 
@@ -43,8 +52,11 @@ struct DecodeCfg {
   static constexpr int kStageBytes = kSubBytes * KW;
   static constexpr int kRingBytes = kStageBytes * STAGES;
   static constexpr int kRedFloats = 2 * KW * 4 * NT * 32;
+  // x fragments (2*KX*N bytes) + bias table (KX/32 blocks x 8*NT tokens floats)
+  __host__ __device__ static size_t xs_bytes(int N, int KX) { return static_cast<size_t>(2) * KX * N; }
+  __host__ __device__ static size_t cs_bytes(int KX) { return static_cast<size_t>(KX / 32) * 8 * NT * sizeof(float); }
   static size_t smem_bytes(int N, int KX) {
-    return kRingBytes + static_cast<size_t>(2) * KX * N + kRedFloats * sizeof(float) + 2 * STAGES * 8 + 16 + 128;
+    return kRingBytes + xs_bytes(N, KX) + cs_bytes(KX) + kRedFloats * sizeof(float) + 2 * STAGES * 8 + 16 + 128;
   }
 };
 
@@ -56,42 +68,67 @@ __device__ __forceinline__ float half_hi(uint32_t w) {
   return __half2float(__ushort_as_half(static_cast<uint16_t>(w >> 16)));
 }
 
-// The 4 code bytes (qs indices) lane t owns in an even / odd block of a pair.
-__device__ __forceinline__ void lane_bytes(int parity, int t, int (&c)[4]) {
-  if (parity) {
-    c[0] = 4 * t; c[1] = 4 * t + 1; c[2] = 4 * t + 2; c[3] = 4 * t + 3;
-  } else if (t < 3) {
-    c[0] = 4 * t + 2; c[1] = 4 * t + 3; c[2] = 4 * t + 4; c[3] = 4 * t + 5;
-  } else {
-    c[0] = 0; c[1] = 1; c[2] = 14; c[3] = 15;
-  }
-}
-
-// Word of 8 codes (bytes c0..c3) -> four f16x2 registers holding q - 8 exactly.
-// lo: (c0,c2) and (c1,c3) low nibbles; hi: the same bytes' high nibbles.
+// Word of 8 codes (bytes c0..c3) -> four f16x2 registers of biased codes:
+// lo02 = (1024+q) of c0, c2 low nibbles, lo13 = c1, c3 low nibbles,
+// hi02 / hi13 = (1024+16q) of the high nibbles.  One LOP3 each, all exact.
 __device__ __forceinline__ void codes_to_f16(uint32_t v, uint32_t& lo02, uint32_t& lo13, uint32_t& hi02,
                                              uint32_t& hi13) {
-  const uint32_t kMagic = 0x64006400u;      // fp16 1024 in both halves
-  const uint32_t kSub = 0x64086408u;        // fp16 1032
-  const uint32_t kSixteenth = 0x2C002C00u;  // fp16 1/16
-  const uint32_t kMinus72 = 0xD480D480u;    // fp16 -72
+  const uint32_t kMagic = 0x64006400u;  // fp16 1024 in both halves
   const uint32_t v8 = v >> 8;
-  lo02 = hsub2_u32(lop3_and_or(v, 0x000F000Fu, kMagic), kSub);  // (1024+q) - 1032
-  lo13 = hsub2_u32(lop3_and_or(v8, 0x000F000Fu, kMagic), kSub);
-  hi02 = hfma2_u32(lop3_and_or(v, 0x00F000F0u, kMagic), kSixteenth, kMinus72);  // (1024+16q)/16 - 72
-  hi13 = hfma2_u32(lop3_and_or(v8, 0x00F000F0u, kMagic), kSixteenth, kMinus72);
+  lo02 = lop3_and_or(v, 0x000F000Fu, kMagic);
+  lo13 = lop3_and_or(v8, 0x000F000Fu, kMagic);
+  hi02 = lop3_and_or(v, 0x00F000F0u, kMagic);
+  hi13 = lop3_and_or(v8, 0x00F000F0u, kMagic);
+}
+
+// Stage x for one (block, token): four lane-slot fragments and the negated bias.
+// Slot t of an even block holds code bytes c = {4t+2, 4t+3, 4t+4, 4t+5} (t < 3)
+// or {0, 1, 14, 15} (t = 3); of an odd block c = {4t, .., 4t+3}.  The slot is
+// [x[c0], x[c2], x[c1], x[c3]] (fp16) and [x[16+c0], x[16+c2], x[16+c1],
+// x[16+c3]] / 16 (fp16), matching the A fragments built from those bytes.
+template <int PARITY>
+__device__ __forceinline__ float stage_block(const float (&x)[32], uint4* dst) {
+  float bias = 0.f;
+  __half xh[32];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    xh[j] = __float2half_rn(x[j]);
+    xh[16 + j] = __float2half_rn(x[16 + j] * 0.0625f);
+    bias = fmaf(1032.f, __half2float(xh[j]), bias);
+    bias = fmaf(1152.f, __half2float(xh[16 + j]), bias);
+  }
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    int c0, c1, c2, c3;
+    if (PARITY) {
+      c0 = 4 * t; c1 = 4 * t + 1; c2 = 4 * t + 2; c3 = 4 * t + 3;
+    } else if (t < 3) {
+      c0 = 4 * t + 2; c1 = 4 * t + 3; c2 = 4 * t + 4; c3 = 4 * t + 5;
+    } else {
+      c0 = 0; c1 = 1; c2 = 14; c3 = 15;
+    }
+    __half2 h;
+    uint4 pk;
+    h = __halves2half2(xh[c0], xh[c2]); pk.x = *reinterpret_cast<uint32_t*>(&h);
+    h = __halves2half2(xh[c1], xh[c3]); pk.y = *reinterpret_cast<uint32_t*>(&h);
+    h = __halves2half2(xh[16 + c0], xh[16 + c2]); pk.z = *reinterpret_cast<uint32_t*>(&h);
+    h = __halves2half2(xh[16 + c1], xh[16 + c3]); pk.w = *reinterpret_cast<uint32_t*>(&h);
+    dst[t] = pk;
+  }
+  return -bias;
 }
 
 template <int NT, int KW, int STAGES>
-__global__ void __launch_bounds__(32 * (KW + 1), 1)
+__global__ void __launch_bounds__(32 * (KW + 1), (NT <= 2 ? 2 : 1))
     k_decode_q4_0(const __grid_constant__ CUtensorMap tmW, const float* __restrict__ X, int N, int M, int K,
-                  int KX, float* __restrict__ Y, uint64_t limit_ns, uint32_t* err) {
+                  int KX, float* __restrict__ Y, uint64_t limit_ns, uint32_t* err, int early_w) {
   using Cfg = DecodeCfg<NT, KW, STAGES>;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   uint8_t* ring = smem;
   uint4* xs = reinterpret_cast<uint4*>(smem + Cfg::kRingBytes);
-  float* red = reinterpret_cast<float*>(smem + Cfg::kRingBytes + static_cast<size_t>(2) * KX * N);
+  float* cs = reinterpret_cast<float*>(smem + Cfg::kRingBytes + Cfg::xs_bytes(N, KX));
+  float* red = reinterpret_cast<float*>(smem + Cfg::kRingBytes + Cfg::xs_bytes(N, KX) + Cfg::cs_bytes(KX));
   uint64_t* bars = reinterpret_cast<uint64_t*>(red + Cfg::kRedFloats);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES);
 
@@ -108,12 +145,14 @@ __global__ void __launch_bounds__(32 * (KW + 1), 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
+  pdl_launch_dependents();
   __syncthreads();
 
   if (warp == KW) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tmW);
+      if (!early_w) pdl_wait();
       uint32_t q = 0;
       bool ok = true;
       for (int c = 0; c < nchunks && ok; ++c) {
@@ -160,6 +199,7 @@ __global__ void __launch_bounds__(32 * (KW + 1), 1)
   uint32_t q = 0;
   int tile_iter = 0;
   bool live = true;  // false once a bounded wait gave up; the loops still run to keep barriers matched
+  pdl_wait();        // X may come from the previous kernel; Y may still be read by it
 
   for (int c = 0; c < nchunks; ++c) {
     const int kc0 = c * KX;
@@ -167,33 +207,31 @@ __global__ void __launch_bounds__(32 * (KW + 1), 1)
     const int nst = min(stages_per_chunk, (kend - kc0 + Cfg::kStageK - 1) / Cfg::kStageK);
     const int nbl = nst * Cfg::kStageK / kQK;  // local blocks covered by this chunk's stages
 
-    // Stage this chunk of x into shared memory as fp16 fragments, permuted
-    // like the codes: entry (block b, token n, lane-slot t) = 8 halves
-    // [x[c0], x[c2], x[c1], x[c3], x[16+c0], x[16+c2], x[16+c1], x[16+c3]].
-    named_bar_sync(1, 32 * KW);  // previous chunk's x fragments are no longer read
-    for (int e = threadIdx.x; e < nbl * N * 4; e += 32 * KW) {
-      const int tt = e & 3;
-      const int n = (e >> 2) % N;
-      const int bl = (e >> 2) / N;
+    // Stage this chunk of x: per (block, token) four fp16 lane-slot fragments
+    // (k permuted like the codes) and the negated bias of the biased codes.
+    named_bar_sync(1, 32 * KW);  // previous chunk's fragments are no longer read
+    for (int e = threadIdx.x; e < nbl * N; e += 32 * KW) {
+      const int n = e % N;
+      const int bl = e / N;
       const int bg = kc0 / kQK + bl;
-      int cb[4];
-      lane_bytes(bg & 1, tt, cb);
-      const float* xr = X + static_cast<size_t>(n) * K + static_cast<size_t>(bg) * kQK;
-      const bool in = bg * kQK < K;
-      float v[8];
-      const int order[4] = {cb[0], cb[2], cb[1], cb[3]};
+      float x[32];
+      if (bg * kQK < K) {
+        const float4* xr = reinterpret_cast<const float4*>(X + static_cast<size_t>(n) * K + static_cast<size_t>(bg) * kQK);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        v[i] = in ? xr[order[i]] : 0.f;
-        v[4 + i] = in ? xr[16 + order[i]] : 0.f;
+        for (int i = 0; i < 8; ++i) {
+          const float4 v = __ldg(xr + i);
+          x[4 * i] = v.x; x[4 * i + 1] = v.y; x[4 * i + 2] = v.z; x[4 * i + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = 0.f;
       }
-      uint4 pk;
-      __half2 h;
-      h = __floats2half2_rn(v[0], v[1]); pk.x = *reinterpret_cast<uint32_t*>(&h);
-      h = __floats2half2_rn(v[2], v[3]); pk.y = *reinterpret_cast<uint32_t*>(&h);
-      h = __floats2half2_rn(v[4], v[5]); pk.z = *reinterpret_cast<uint32_t*>(&h);
-      h = __floats2half2_rn(v[6], v[7]); pk.w = *reinterpret_cast<uint32_t*>(&h);
-      xs[e] = pk;
+      uint4* dst = xs + (bl * N + n) * 4;
+      cs[bl * 8 * NT + n] = (bg & 1) ? stage_block<1>(x, dst) : stage_block<0>(x, dst);
+    }
+    for (int e = threadIdx.x; e < nbl * (8 * NT - N); e += 32 * KW) {  // padding tokens: no bias
+      const int pad = 8 * NT - N;
+      cs[(e / pad) * 8 * NT + N + e % pad] = 0.f;
     }
     named_bar_sync(1, 32 * KW);
 
@@ -238,9 +276,10 @@ __global__ void __launch_bounds__(32 * (KW + 1), 1)
                 const int n = nt * 8 + g;
                 uint4 xf = make_uint4(0u, 0u, 0u, 0u);
                 if (n < N) xf = xs[(bl * N + n) * 4 + t];
+                const float2 nb = *reinterpret_cast<const float2*>(cs + bl * 8 * NT + nt * 8 + 2 * t);
                 float tsum[4];
-                const float zero[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_m16n8k16_f16(tsum, a_lo, xf.x, xf.y, zero);
+                const float init[4] = {nb.x, nb.y, nb.x, nb.y};
+                mma_m16n8k16_f16(tsum, a_lo, xf.x, xf.y, init);
                 mma_m16n8k16_f16(tsum, a_hi, xf.z, xf.w, tsum);
                 acc[nt][0] = fmaf(dd[0][e], tsum[0], acc[nt][0]);
                 acc[nt][1] = fmaf(dd[0][e], tsum[1], acc[nt][1]);
@@ -280,7 +319,7 @@ __global__ void __launch_bounds__(32 * (KW + 1), 1)
 
 template <int NT, int KW, int STAGES>
 cudaError_t launch_cfg(const CUtensorMap* tmW, const float* X, int N, int M, int K, float* Y, uint64_t limit_ns,
-                       int xs_budget, cudaStream_t s) {
+                       int xs_budget, int early_w, cudaStream_t s) {
   using Cfg = DecodeCfg<NT, KW, STAGES>;
   // x chunk: a multiple of the stage width, as long as the budget allows
   int KX = (xs_budget / (2 * N)) / Cfg::kStageK * Cfg::kStageK;
@@ -294,6 +333,8 @@ cudaError_t launch_cfg(const CUtensorMap* tmW, const float* X, int N, int M, int
   if (static_cast<int>(smem) > configured_smem) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     configured_smem = static_cast<int>(smem);
   }
   if (occ_cache_smem != static_cast<int>(smem)) {
@@ -305,8 +346,17 @@ cudaError_t launch_cfg(const CUtensorMap* tmW, const float* X, int N, int M, int
   }
   const int ntiles = (M + kBM - 1) / kBM;
   const int grid = std::min(ntiles, device_info().sm_count * occ_cache);
-  kern<<<grid, Cfg::kThreads, smem, s>>>(*tmW, X, N, M, K, KX, Y, limit_ns, device_error_word());
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(Cfg::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, *tmW, X, N, M, K, KX, Y, limit_ns, device_error_word(), early_w);
 }
 
 // -------------------------------------------------------------------------
@@ -350,12 +400,12 @@ void decode_w_box(int64_t /*N*/, uint32_t* box_x_bytes, uint32_t* box_rows) {
 }
 
 cudaError_t launch_decode(const CUtensorMap* tmW, const float* X, int64_t N, int64_t M, int64_t K, float* Y,
-                          uint64_t wait_limit_ns, cudaStream_t s) {
+                          uint64_t wait_limit_ns, int early_w, cudaStream_t s) {
   const int n = static_cast<int>(N), m = static_cast<int>(M), k = static_cast<int>(K);
-  if (N <= 8) return launch_cfg<1, 8, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, s);
-  if (N <= 16) return launch_cfg<2, 8, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, s);
-  if (N <= 32) return launch_cfg<4, 4, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 128 << 10, s);
-  return launch_cfg<8, 4, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 128 << 10, s);
+  if (N <= 8) return launch_cfg<1, 8, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, s);
+  if (N <= 16) return launch_cfg<2, 8, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, s);
+  if (N <= 32) return launch_cfg<4, 4, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 128 << 10, early_w, s);
+  return launch_cfg<8, 4, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 128 << 10, early_w, s);
 }
 
 cudaError_t launch_generic(const uint8_t* W, int64_t M, int64_t K, const float* X, int64_t N, float* Y,

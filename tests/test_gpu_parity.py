@@ -307,3 +307,36 @@ def test_prefill_dequant_is_single_rounded_bf16():
     w_bf16 = torch.from_numpy(oracle.get().dequant(W, M, K)).to(torch.bfloat16).float().numpy()
     expect = w_bf16[:, ks].T                                  # [N, M]
     assert same_f32_bits(np.abs(Y.cpu().numpy()), np.abs(expect)).all()
+
+
+def test_weights_static_option_gives_identical_results():
+    M, K, N = 2000, 4096, 3
+    W = dev(synth.q4_0_weights(M, K, seed=7200))
+    X = dev(synth.activations(N, K, seed=7201))
+    a = gq.mul_mat_q4_0(W, X)
+    gq.gq_set_option(gq.GQ_OPT_WEIGHTS_STATIC, 1)
+    try:
+        b = gq.mul_mat_q4_0(W, X)
+        c = gq.mul_mat_q4_0(W, X)
+    finally:
+        gq.gq_set_option(gq.GQ_OPT_WEIGHTS_STATIC, 0)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b) and torch.equal(b, c)
+
+
+def test_back_to_back_dependent_calls():
+    """Each call's X is the previous call's Y: programmatic dependent launch
+    must still order the reads after the producer kernel."""
+    K = 4096
+    Ws = [synth.q4_0_weights(K, K, seed=7300 + i) for i in range(4)]
+    x0 = synth.activations(2, K, seed=7310)
+    xs = [dev(x0)]
+    for W in Ws:
+        xs.append(gq.mul_mat_q4_0(dev(W), xs[-1]))
+    torch.cuda.synchronize()
+    x = x0
+    for i, W in enumerate(Ws):
+        y_ref, s_ref = oracle_mul_mat(W, K, K, x)
+        got = xs[i + 1].cpu().numpy()
+        assert_mul_mat_close(got, y_ref, s_ref, f"chain step {i}")
+        x = got.astype(np.float32)      # continue from what the GPU produced
