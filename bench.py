@@ -387,8 +387,41 @@ def run_e2e(gq, torch, dev, s, W, shapes, acts1, order, L, args):
     return {"ms": e0.elapsed_time(e1) / args.steps, "h2d": h2d, "d2h": d2h}
 
 
+PROFILE_CASES = {
+    # name: (M, K, N, entry point)
+    "decode": (11008, 4096, 1, "f32"),
+    "decode_down": (4096, 11008, 1, "f32"),
+    "decode_small": (4096, 4096, 1, "f32"),
+    "decode_big": (32000, 4096, 1, "f32"),
+    "prefill": (14336, 4096, 512, "bf16"),
+    "prefill_small": (4096, 4096, 512, "bf16"),
+}
+
+
+def run_profile_case(name):
+    """One small invocation for an ncu capture: two launches of one MUL_MAT."""
+    import torch
+    import quantized_block_q4_gb300 as gq
+    M, K, N, mode = PROFILE_CASES[name]
+    gq.gq_set_option(gq.GQ_OPT_WEIGHTS_STATIC, 1)
+    W = torch.from_numpy(synth.q4_0_weights(M, K, seed=1)).cuda()
+    X = torch.from_numpy(synth.activations(N, K, seed=2)).cuda()
+    Y = torch.empty(N, M, device="cuda")
+    for _ in range(2):
+        if mode == "bf16":
+            gq.gq_mul_mat_q4_0_bf16x(W, M, K, X.to(torch.bfloat16).view(torch.int16), N, Y)
+        else:
+            gq.gq_mul_mat_q4_0(W, M, K, X, N, Y)
+    torch.cuda.synchronize()
+    gq.gq_sync_status()
+    print(f"profile case {name}: M={M} K={K} N={N} ok")
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
+                    help="run one MUL_MAT twice (for an ncu capture) and exit")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
@@ -398,6 +431,8 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=5.0, help="seconds of oracle work per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.profile_case:
+        return run_profile_case(args.profile_case)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
