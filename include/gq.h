@@ -108,9 +108,11 @@ typedef enum {
   GQ_OPT_PREFILL_MIN_N = 0,  /* N at which mul_mat switches to the tensor-core path (default 64) */
   GQ_OPT_FORCE_GENERIC = 1,  /* 1: every mul_mat takes the generic kernel (test aid) */
   GQ_OPT_WAIT_LIMIT_NS = 2,  /* bound on any in-kernel wait, nanoseconds (default 2e9) */
-  GQ_OPT_WEIGHTS_STATIC = 3  /* 1: promise that no kernel launched right before a mul_mat on the same
+  GQ_OPT_WEIGHTS_STATIC = 3, /* 1: promise that no kernel launched right before a mul_mat on the same
                                 stream writes its W, so the decode kernel may start streaming W
                                 while that kernel finishes (weight-stationary inference); default 0 */
+  GQ_OPT_DECODE_VARIANT = 4  /* tuning: tile/warp layout of the N <= 8 decode kernel, 0..3 (default 0);
+                                every variant computes the same result */
 } gq_option;
 gq_status gq_set_option(gq_option opt, int64_t value);
 int64_t gq_get_option(gq_option opt);

@@ -40,23 +40,28 @@
 namespace gq {
 namespace {
 
-constexpr int kBM = 16;                        // rows per tile (one m16 MMA tile)
-constexpr int kSubK = 256;                     // weights per row per TMA box
-constexpr int kSubBytesRow = 144;              // 8 blocks x 18 bytes
-constexpr int kSubBytes = kBM * kSubBytesRow;  // 2304 bytes per box
+constexpr int kSubK = 256;         // weights per row per TMA box
+constexpr int kSubBytesRow = 144;  // 8 blocks x 18 bytes
 
-template <int NT, int KW, int STAGES>
+// NT: n8 token tiles (N <= 8*NT); MT: m16 row tiles per warp (tile = 16*MT
+// rows); KW: consumer warps, each taking one 256-k box of every stage.
+template <int NT, int MT, int KW, int STAGES>
 struct DecodeCfg {
+  static constexpr int kBM = 16 * MT;
+  static constexpr int kSubBytes = kBM * kSubBytesRow;
   static constexpr int kThreads = 32 * (KW + 1);
   static constexpr int kStageK = kSubK * KW;
   static constexpr int kStageBytes = kSubBytes * KW;
   static constexpr int kRingBytes = kStageBytes * STAGES;
-  static constexpr int kRedFloats = 2 * KW * 4 * NT * 32;
+  static constexpr int kSlots = STAGES + 1;  // tile accumulators in flight (see the reduction below)
+  // one partial per k-warp: [KW][kBM][N] floats per slot
+  __host__ __device__ static size_t slot_floats(int N) { return static_cast<size_t>(KW) * kBM * N; }
   // x fragments (2*KX*N bytes) + bias table (KX/32 blocks x 8*NT tokens floats)
   __host__ __device__ static size_t xs_bytes(int N, int KX) { return static_cast<size_t>(2) * KX * N; }
   __host__ __device__ static size_t cs_bytes(int KX) { return static_cast<size_t>(KX / 32) * 8 * NT * sizeof(float); }
   static size_t smem_bytes(int N, int KX) {
-    return kRingBytes + xs_bytes(N, KX) + cs_bytes(KX) + kRedFloats * sizeof(float) + 2 * STAGES * 8 + 16 + 128;
+    return kRingBytes + xs_bytes(N, KX) + cs_bytes(KX) + (kSlots * slot_floats(N) + kSlots) * sizeof(float) +
+           2 * STAGES * 8 + 16 + 128;
   }
 };
 
@@ -118,18 +123,22 @@ __device__ __forceinline__ float stage_block(const float (&x)[32], uint4* dst) {
   return -bias;
 }
 
-template <int NT, int KW, int STAGES>
+template <int NT, int MT, int KW, int STAGES>
 __global__ void __launch_bounds__(32 * (KW + 1), (NT <= 2 ? 2 : 1))
     k_decode_q4_0(const __grid_constant__ CUtensorMap tmW, const float* __restrict__ X, int N, int M, int K,
                   int KX, float* __restrict__ Y, uint64_t limit_ns, uint32_t* err, int early_w) {
-  using Cfg = DecodeCfg<NT, KW, STAGES>;
+  using Cfg = DecodeCfg<NT, MT, KW, STAGES>;
+  constexpr int kBM = Cfg::kBM;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   uint8_t* ring = smem;
   uint4* xs = reinterpret_cast<uint4*>(smem + Cfg::kRingBytes);
   float* cs = reinterpret_cast<float*>(smem + Cfg::kRingBytes + Cfg::xs_bytes(N, KX));
-  float* red = reinterpret_cast<float*>(smem + Cfg::kRingBytes + Cfg::xs_bytes(N, KX) + Cfg::cs_bytes(KX));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(red + Cfg::kRedFloats);
+  float* acc_slots = cs + Cfg::cs_bytes(KX) / sizeof(float);  // [kSlots][KW][kBM][N]
+  const int slot_floats = static_cast<int>(Cfg::slot_floats(N));
+  int* slot_count = reinterpret_cast<int*>(acc_slots + Cfg::kSlots * slot_floats);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(
+      (reinterpret_cast<uintptr_t>(slot_count + Cfg::kSlots) + 7) & ~uintptr_t(7));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -137,6 +146,7 @@ __global__ void __launch_bounds__(32 * (KW + 1), (NT <= 2 ? 2 : 1))
   const int nchunks = (K + KX - 1) / KX;
   const int stages_per_chunk = KX / Cfg::kStageK;
 
+  if (threadIdx.x < Cfg::kSlots) slot_count[threadIdx.x] = 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&bars[s]), 1);            // full: producer's expect_tx arrive + tx bytes
@@ -170,10 +180,11 @@ __global__ void __launch_bounds__(32 * (KW + 1), (NT <= 2 ? 2 : 1))
             const int k0 = kc0 + st * Cfg::kStageK;
             const int nvalid = min(KW, (kend - k0 + kSubK - 1) / kSubK);
             const uint32_t full = smem_u32(&bars[slot]);
-            mbar_arrive_expect_tx(full, nvalid * kSubBytes);
+            mbar_arrive_expect_tx(full, nvalid * Cfg::kSubBytes);
             for (int j = 0; j < nvalid; ++j) {
               const int xb = ((k0 + j * kSubK) / kSubK) * kSubBytesRow;  // byte column in the row
-              tma_load_2d(smem_u32(ring + slot * Cfg::kStageBytes + j * kSubBytes), &tmW, xb, tile * kBM, full);
+              tma_load_2d(smem_u32(ring + slot * Cfg::kStageBytes + j * Cfg::kSubBytes), &tmW, xb, tile * kBM,
+                          full);
             }
           }
         }
@@ -216,7 +227,8 @@ __global__ void __launch_bounds__(32 * (KW + 1), (NT <= 2 ? 2 : 1))
       const int bg = kc0 / kQK + bl;
       float x[32];
       if (bg * kQK < K) {
-        const float4* xr = reinterpret_cast<const float4*>(X + static_cast<size_t>(n) * K + static_cast<size_t>(bg) * kQK);
+        const float4* xr =
+            reinterpret_cast<const float4*>(X + static_cast<size_t>(n) * K + static_cast<size_t>(bg) * kQK);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float4 v = __ldg(xr + i);
@@ -236,55 +248,67 @@ __global__ void __launch_bounds__(32 * (KW + 1), (NT <= 2 ? 2 : 1))
     named_bar_sync(1, 32 * KW);
 
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tile_iter) {
-      float acc[NT][4];
+      float acc[MT][NT][4];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+      for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[mt][nt][i] = 0.f;
 
       for (int st = 0; st < nst; ++st, ++q) {
         const int slot = q % STAGES;
         if (live) live = mbar_wait_bounded(smem_u32(&bars[slot]), (q / STAGES) & 1, limit_ns, abort_flag, err);
         const int k0 = kc0 + st * Cfg::kStageK + kw * kSubK;
         if (live && k0 < kend) {
-          const uint8_t* sub = ring + slot * Cfg::kStageBytes + kw * kSubBytes;
+          const uint8_t* sub = ring + slot * Cfg::kStageBytes + kw * Cfg::kSubBytes + g * kSubBytesRow;
           const int bl0 = (k0 - kc0) / kQK;
+          const uint4* xsp = xs + (bl0 * N + g) * 4 + t;     // + block * 4N + nt * 32
+          const float* csp = cs + bl0 * 8 * NT + 2 * t;      // + block * 8NT + nt * 8
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
-            uint32_t wd[2][2];  // [row g / g+8][even / odd block] code words
-            float dd[2][2];     // scales
+            uint32_t wd[MT][2][2];  // [m-tile][row g / g+8][even / odd block] code words
+            float dd[MT][2][2];     // scales
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              const uint8_t* rb = sub + (g + 8 * r) * kSubBytesRow + 36 * p;
-              const uint32_t Z = *reinterpret_cast<const uint32_t*>(rb);
-              const uint32_t U = *reinterpret_cast<const uint32_t*>(rb + 4 + 4 * t);
-              const uint32_t W4 = *reinterpret_cast<const uint32_t*>(rb + 16);
-              const uint32_t Y1 = *reinterpret_cast<const uint32_t*>(rb + 20 + 4 * t);
-              wd[r][0] = prmt(Z, U, sel);
-              wd[r][1] = Y1;
-              dd[r][0] = half_lo(Z);
-              dd[r][1] = half_hi(W4);
-            }
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+              for (int r = 0; r < 2; ++r) {
+                const uint8_t* rb = sub + (mt * 16 + 8 * r) * kSubBytesRow + 36 * p;
+                const uint32_t Z = *reinterpret_cast<const uint32_t*>(rb);
+                const uint32_t U = *reinterpret_cast<const uint32_t*>(rb + 4 + 4 * t);
+                const uint32_t W4 = *reinterpret_cast<const uint32_t*>(rb + 16);
+                const uint32_t Y1 = *reinterpret_cast<const uint32_t*>(rb + 20 + 4 * t);
+                wd[mt][r][0] = prmt(Z, U, sel);
+                wd[mt][r][1] = Y1;
+                dd[mt][r][0] = half_lo(Z);
+                dd[mt][r][1] = half_hi(W4);
+              }
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              uint32_t a_lo[4], a_hi[4];
-              codes_to_f16(wd[0][e], a_lo[0], a_lo[2], a_hi[0], a_hi[2]);
-              codes_to_f16(wd[1][e], a_lo[1], a_lo[3], a_hi[1], a_hi[3]);
-              const int bl = bl0 + 2 * p + e;
+              const int b = 2 * p + e;
+              uint4 xf[NT];
+              float2 nb[NT];
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt) {
-                const int n = nt * 8 + g;
-                uint4 xf = make_uint4(0u, 0u, 0u, 0u);
-                if (n < N) xf = xs[(bl * N + n) * 4 + t];
-                const float2 nb = *reinterpret_cast<const float2*>(cs + bl * 8 * NT + nt * 8 + 2 * t);
-                float tsum[4];
-                const float init[4] = {nb.x, nb.y, nb.x, nb.y};
-                mma_m16n8k16_f16(tsum, a_lo, xf.x, xf.y, init);
-                mma_m16n8k16_f16(tsum, a_hi, xf.z, xf.w, tsum);
-                acc[nt][0] = fmaf(dd[0][e], tsum[0], acc[nt][0]);
-                acc[nt][1] = fmaf(dd[0][e], tsum[1], acc[nt][1]);
-                acc[nt][2] = fmaf(dd[1][e], tsum[2], acc[nt][2]);
-                acc[nt][3] = fmaf(dd[1][e], tsum[3], acc[nt][3]);
+                xf[nt] = (nt * 8 + g < N) ? xsp[b * 4 * N + nt * 32] : make_uint4(0u, 0u, 0u, 0u);
+                nb[nt] = *reinterpret_cast<const float2*>(csp + b * 8 * NT + nt * 8);
+              }
+#pragma unroll
+              for (int mt = 0; mt < MT; ++mt) {
+                uint32_t a_lo[4], a_hi[4];
+                codes_to_f16(wd[mt][0][e], a_lo[0], a_lo[2], a_hi[0], a_hi[2]);
+                codes_to_f16(wd[mt][1][e], a_lo[1], a_lo[3], a_hi[1], a_hi[3]);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                  float tsum[4];
+                  const float init[4] = {nb[nt].x, nb[nt].y, nb[nt].x, nb[nt].y};
+                  mma_m16n8k16_f16(tsum, a_lo, xf[nt].x, xf[nt].y, init);
+                  mma_m16n8k16_f16(tsum, a_hi, xf[nt].z, xf[nt].w, tsum);
+                  acc[mt][nt][0] = fmaf(dd[mt][0][e], tsum[0], acc[mt][nt][0]);
+                  acc[mt][nt][1] = fmaf(dd[mt][0][e], tsum[1], acc[mt][nt][1]);
+                  acc[mt][nt][2] = fmaf(dd[mt][1][e], tsum[2], acc[mt][nt][2]);
+                  acc[mt][nt][3] = fmaf(dd[mt][1][e], tsum[3], acc[mt][nt][3]);
+                }
               }
             }
           }
@@ -293,41 +317,65 @@ __global__ void __launch_bounds__(32 * (KW + 1), (NT <= 2 ? 2 : 1))
         if (live && lane == 0) mbar_arrive(smem_u32(&bars[STAGES + slot]));
       }
 
-      // Reduce the KW partial sums of this tile; warp kw finishes values i = kw, kw+KW, ...
-      const int slotr = tile_iter & 1;
-      float* rs = red + static_cast<size_t>(slotr) * KW * 4 * NT * 32;
+      // Hand this warp's partial sums to the tile's shared slot; the last of
+      // the KW warps to arrive adds the KW partials in a fixed order (so the
+      // result does not depend on timing), writes Y and releases the slot.  A
+      // warp cannot run more than STAGES tiles ahead of the slowest one (it
+      // needs the stages that warp still has to release), so kSlots =
+      // STAGES + 1 slots are never reused while still in use.
+      const int aslot = tile_iter % Cfg::kSlots;
+      float* as = acc_slots + aslot * slot_floats;
+      float* mine = as + kw * kBM * N;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+      for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) rs[((kw * NT + nt) * 4 + i) * 32 + lane] = acc[nt][i];
-      named_bar_sync(1, 32 * KW);
-      for (int iv = kw; iv < 4 * NT; iv += KW) {
-        float s = 0.f;
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int w = 0; w < KW; ++w) s += rs[((w * NT) * 4 + iv) * 32 + lane];
-        const int nt = iv >> 2, i = iv & 3;
-        const int row = tile * kBM + g + 8 * (i >> 1);
-        const int n = nt * 8 + 2 * t + (i & 1);
-        if (live && row < M && n < N) {
-          float* yp = Y + static_cast<size_t>(n) * M + row;
-          *yp = (c == 0) ? s : (*yp + s);
+          for (int i = 0; i < 4; ++i) {
+            const int n = nt * 8 + 2 * t + (i & 1);
+            if (n < N) mine[(mt * 16 + g + 8 * (i >> 1)) * N + n] = acc[mt][nt][i];
+          }
+      __syncwarp();
+      int prev = 0;
+      if (lane == 0) {
+        __threadfence_block();
+        prev = atomicAdd(&slot_count[aslot], 1);
+      }
+      prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
+      if (prev == KW - 1) {
+        __threadfence_block();
+        for (int idx = lane; idx < kBM * N; idx += 32) {
+          const int r = idx / N, n = idx % N;
+          const int row = tile * kBM + r;
+          float v = 0.f;
+#pragma unroll
+          for (int w = 0; w < KW; ++w) v += *reinterpret_cast<volatile float*>(&as[(w * kBM + r) * N + n]);
+          if (live && row < M) {
+            float* yp = Y + static_cast<size_t>(n) * M + row;
+            *yp = (c == 0) ? v : (*yp + v);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence_block();
+          slot_count[aslot] = 0;
         }
       }
     }
   }
 }
 
-template <int NT, int KW, int STAGES>
+template <int NT, int MT, int KW, int STAGES>
 cudaError_t launch_cfg(const CUtensorMap* tmW, const float* X, int N, int M, int K, float* Y, uint64_t limit_ns,
                        int xs_budget, int early_w, cudaStream_t s) {
-  using Cfg = DecodeCfg<NT, KW, STAGES>;
+  using Cfg = DecodeCfg<NT, MT, KW, STAGES>;
   // x chunk: a multiple of the stage width, as long as the budget allows
   int KX = (xs_budget / (2 * N)) / Cfg::kStageK * Cfg::kStageK;
   if (KX < Cfg::kStageK) KX = Cfg::kStageK;
   const int Kpad = (K + Cfg::kStageK - 1) / Cfg::kStageK * Cfg::kStageK;
   if (KX > Kpad) KX = Kpad;
   const size_t smem = Cfg::smem_bytes(N, KX);
-  auto kern = k_decode_q4_0<NT, KW, STAGES>;
+  auto kern = k_decode_q4_0<NT, MT, KW, STAGES>;
   static int configured_smem = 0;
   static int occ_cache_smem = -1, occ_cache = 1;
   if (static_cast<int>(smem) > configured_smem) {
@@ -344,7 +392,7 @@ cudaError_t launch_cfg(const CUtensorMap* tmW, const float* X, int N, int M, int
     occ_cache = occ > 0 ? occ : 1;
     occ_cache_smem = static_cast<int>(smem);
   }
-  const int ntiles = (M + kBM - 1) / kBM;
+  const int ntiles = (M + Cfg::kBM - 1) / Cfg::kBM;
   const int grid = std::min(ntiles, device_info().sm_count * occ_cache);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -394,18 +442,30 @@ __global__ void k_generic_q4_0(const uint8_t* __restrict__ W, int64_t M, int64_t
 
 }  // namespace
 
-void decode_w_box(int64_t /*N*/, uint32_t* box_x_bytes, uint32_t* box_rows) {
+// Decode configuration by N: (NT, MT, KW, STAGES).  The variant index can be
+// overridden for tuning (GQ_OPT_DECODE_VARIANT); 0 = default.
+int decode_rows_per_tile(int64_t N, int variant) {
+  if (N <= 8) return (variant == 2) ? 16 : 32;
+  return 16;
+}
+
+void decode_w_box(int64_t N, int variant, uint32_t* box_x_bytes, uint32_t* box_rows) {
   *box_x_bytes = kSubBytesRow;
-  *box_rows = kBM;
+  *box_rows = static_cast<uint32_t>(decode_rows_per_tile(N, variant));
 }
 
 cudaError_t launch_decode(const CUtensorMap* tmW, const float* X, int64_t N, int64_t M, int64_t K, float* Y,
-                          uint64_t wait_limit_ns, int early_w, cudaStream_t s) {
+                          uint64_t wait_limit_ns, int early_w, int variant, cudaStream_t s) {
   const int n = static_cast<int>(N), m = static_cast<int>(M), k = static_cast<int>(K);
-  if (N <= 8) return launch_cfg<1, 8, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, s);
-  if (N <= 16) return launch_cfg<2, 8, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, s);
-  if (N <= 32) return launch_cfg<4, 4, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 128 << 10, early_w, s);
-  return launch_cfg<8, 4, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 128 << 10, early_w, s);
+  if (N <= 8) {
+    if (variant == 1) return launch_cfg<1, 2, 4, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, s);
+    if (variant == 2) return launch_cfg<1, 1, 8, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, s);
+    if (variant == 3) return launch_cfg<1, 2, 8, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, s);
+    return launch_cfg<1, 2, 8, 2>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, s);
+  }
+  if (N <= 16) return launch_cfg<2, 1, 8, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, s);
+  if (N <= 32) return launch_cfg<4, 1, 4, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 96 << 10, early_w, s);
+  return launch_cfg<8, 1, 4, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 48 << 10, early_w, s);
 }
 
 cudaError_t launch_generic(const uint8_t* W, int64_t M, int64_t K, const float* X, int64_t N, float* Y,

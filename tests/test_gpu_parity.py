@@ -340,3 +340,14 @@ def test_back_to_back_dependent_calls():
         got = xs[i + 1].cpu().numpy()
         assert_mul_mat_close(got, y_ref, s_ref, f"chain step {i}")
         x = got.astype(np.float32)      # continue from what the GPU produced
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+@pytest.mark.parametrize("M,K,N", [(4096, 4096, 1), (300, 11008, 3), (33, 2304, 8)])
+def test_decode_variants(variant, M, K, N):
+    old = gq.gq_get_option(gq.GQ_OPT_DECODE_VARIANT)
+    gq.gq_set_option(gq.GQ_OPT_DECODE_VARIANT, variant)
+    try:
+        check_mm(M, K, N, 7400 + M + N, f"variant {variant}")
+    finally:
+        gq.gq_set_option(gq.GQ_OPT_DECODE_VARIANT, old)
