@@ -25,6 +25,7 @@ std::atomic<int64_t> g_force_generic{0};
 std::atomic<int64_t> g_wait_limit_ns{2000000000LL};
 std::atomic<int64_t> g_early_w{0};
 std::atomic<int64_t> g_decode_variant{0};
+std::atomic<int64_t> g_pdl{1};
 
 gq_status fail(gq_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 gq_status fail(gq_status st, const char* fmt, ...) {
@@ -154,7 +155,7 @@ static gq_status mul_mat_decode(const void* W, int64_t M, int64_t K, const float
                            bx, by, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (st != GQ_OK) return st;
   cudaError_t e = launch_decode(&tm, X, N, M, K, Y, static_cast<uint64_t>(g_wait_limit_ns.load()),
-                                static_cast<int>(g_early_w.load()), variant, s);
+                                static_cast<int>(g_early_w.load()), variant, static_cast<int>(g_pdl.load()), s);
   return e == cudaSuccess ? GQ_OK : cuda_fail(e, "decode launch");
 }
 
@@ -318,6 +319,9 @@ gq_status gq_set_option(gq_option opt, int64_t value) {
       if (value < 0 || value > 3) return fail(GQ_ERR_SHAPE, "decode variant must be 0..3");
       g_decode_variant = value;
       return GQ_OK;
+    case GQ_OPT_PDL:
+      g_pdl = value ? 1 : 0;
+      return GQ_OK;
   }
   return fail(GQ_ERR_SHAPE, "unknown option %d", static_cast<int>(opt));
 }
@@ -329,6 +333,7 @@ int64_t gq_get_option(gq_option opt) {
     case GQ_OPT_WAIT_LIMIT_NS: return g_wait_limit_ns.load();
     case GQ_OPT_WEIGHTS_STATIC: return g_early_w.load();
     case GQ_OPT_DECODE_VARIANT: return g_decode_variant.load();
+    case GQ_OPT_PDL: return g_pdl.load();
   }
   return -1;
 }

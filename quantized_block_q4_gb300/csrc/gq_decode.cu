@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(32 * (KW + 1), (NT <= 2 ? 2 : 1))
 
 template <int NT, int MT, int KW, int STAGES>
 cudaError_t launch_cfg(const CUtensorMap* tmW, const float* X, int N, int M, int K, float* Y, uint64_t limit_ns,
-                       int xs_budget, int early_w, cudaStream_t s) {
+                       int xs_budget, int early_w, int pdl, cudaStream_t s) {
   using Cfg = DecodeCfg<NT, MT, KW, STAGES>;
   // x chunk: a multiple of the stage width, as long as the budget allows
   int KX = (xs_budget / (2 * N)) / Cfg::kStageK * Cfg::kStageK;
@@ -403,7 +403,7 @@ cudaError_t launch_cfg(const CUtensorMap* tmW, const float* X, int N, int M, int
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, *tmW, X, N, M, K, KX, Y, limit_ns, device_error_word(), early_w);
 }
 
@@ -455,17 +455,17 @@ void decode_w_box(int64_t N, int variant, uint32_t* box_x_bytes, uint32_t* box_r
 }
 
 cudaError_t launch_decode(const CUtensorMap* tmW, const float* X, int64_t N, int64_t M, int64_t K, float* Y,
-                          uint64_t wait_limit_ns, int early_w, int variant, cudaStream_t s) {
+                          uint64_t wait_limit_ns, int early_w, int variant, int pdl, cudaStream_t s) {
   const int n = static_cast<int>(N), m = static_cast<int>(M), k = static_cast<int>(K);
   if (N <= 8) {
-    if (variant == 1) return launch_cfg<1, 2, 4, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, s);
-    if (variant == 2) return launch_cfg<1, 1, 8, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, s);
-    if (variant == 3) return launch_cfg<1, 2, 8, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, s);
-    return launch_cfg<1, 2, 8, 2>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, s);
+    if (variant == 1) return launch_cfg<1, 2, 4, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    if (variant == 2) return launch_cfg<1, 1, 8, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    if (variant == 3) return launch_cfg<1, 2, 8, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    return launch_cfg<1, 2, 8, 2>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
   }
-  if (N <= 16) return launch_cfg<2, 1, 8, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, s);
-  if (N <= 32) return launch_cfg<4, 1, 4, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 96 << 10, early_w, s);
-  return launch_cfg<8, 1, 4, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 48 << 10, early_w, s);
+  if (N <= 16) return launch_cfg<2, 1, 8, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+  if (N <= 32) return launch_cfg<4, 1, 4, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 96 << 10, early_w, pdl, s);
+  return launch_cfg<8, 1, 4, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 48 << 10, early_w, pdl, s);
 }
 
 cudaError_t launch_generic(const uint8_t* W, int64_t M, int64_t K, const float* X, int64_t N, float* Y,

@@ -31,7 +31,7 @@ cudaError_t launch_dequant_bytes(const uint8_t* W, int64_t nblocks, float* out, 
 // ---- K2: decode / small-N mul_mat (gq_decode.cu).  Needs K % 256 == 0,
 // W 16-byte aligned, N <= 64.
 cudaError_t launch_decode(const CUtensorMap* tmW, const float* X, int64_t N, int64_t M, int64_t K,
-                          float* Y, uint64_t wait_limit_ns, int early_w, int variant, cudaStream_t s);
+                          float* Y, uint64_t wait_limit_ns, int early_w, int variant, int pdl, cudaStream_t s);
 // TMA box the decode kernel expects for W (rows of raw blocks viewed as bytes).
 void decode_w_box(int64_t N, int variant, uint32_t* box_x_bytes, uint32_t* box_rows);
 
