@@ -80,6 +80,17 @@ def make_acts(n_layers, N, rank, tag):
              for i, K in enumerate(ks)] for layer in range(n_layers)]
 
 
+def max_over_ranks(values, dist=None, device=None):
+    """Element-wise max of a list of floats over all ranks (the slowest rank
+    sets the time); the identity when there is no process group."""
+    if dist is None:
+        return list(values)
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
@@ -277,10 +288,7 @@ def run_gpu(args, rank, world, dist):
     dec_ms = sum(a.elapsed_time(b) for a, b, _ in marks)
     pre_ms = sum(b.elapsed_time(c) for _, b, c in marks)
     step_ms = sum(a.elapsed_time(c) for a, _, c in marks)
-    if dist is not None:
-        t = torch.tensor([dec_ms, pre_ms, step_ms, k3_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dec_ms, pre_ms, step_ms, k3_ms = t.tolist()
+    dec_ms, pre_ms, step_ms, k3_ms = max_over_ranks([dec_ms, pre_ms, step_ms, k3_ms], dist, dev)
 
     K_ = args.steps
     value = world * wbytes * K_ / (dec_ms * 1e-3) / 1e9
@@ -292,10 +300,7 @@ def run_gpu(args, rank, world, dist):
 
     # ---- end to end through the public API with host buffers (decode, N = 1)
     e2e = run_e2e(gq, torch, dev, s, W, shapes, acts1, order, L, args)
-    if dist is not None:
-        t = torch.tensor([e2e["ms"]], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e["ms"] = t.item()
+    e2e["ms"] = max_over_ranks([e2e["ms"]], dist, dev)[0]
     e2e_value = world * wbytes / (e2e["ms"] * 1e-3) / 1e9
 
     cpu = None
