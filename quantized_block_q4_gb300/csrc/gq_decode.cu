@@ -460,8 +460,8 @@ cudaError_t launch_decode(const CUtensorMap* tmW, const float* X, int64_t N, int
   if (N <= 8) {
     if (variant == 1) return launch_cfg<1, 2, 4, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
     if (variant == 2) return launch_cfg<1, 1, 8, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
-    if (variant == 3) return launch_cfg<1, 2, 8, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
-    return launch_cfg<1, 2, 8, 2>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    if (variant == 3) return launch_cfg<1, 2, 8, 2>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    return launch_cfg<1, 2, 8, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
   }
   if (N <= 16) return launch_cfg<2, 1, 8, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
   if (N <= 32) return launch_cfg<4, 1, 4, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 96 << 10, early_w, pdl, s);
