@@ -56,11 +56,14 @@ struct DecodeCfg {
   static constexpr int kSlots = STAGES + 1;  // tile accumulators in flight (see the reduction below)
   // one partial per k-warp: [KW][kBM][N] floats per slot
   __host__ __device__ static size_t slot_floats(int N) { return static_cast<size_t>(KW) * kBM * N; }
-  // x fragments (2*KX*N bytes) + bias table (KX/32 blocks x 8*NT tokens floats)
+  // x fragments (2*KX*N bytes) + bias table (KX/32 blocks x N tokens, N rounded up to even)
   __host__ __device__ static size_t xs_bytes(int N, int KX) { return static_cast<size_t>(2) * KX * N; }
-  __host__ __device__ static size_t cs_bytes(int KX) { return static_cast<size_t>(KX / 32) * 8 * NT * sizeof(float); }
+  __host__ __device__ static int cs_stride(int N) { return N + (N & 1); }
+  __host__ __device__ static size_t cs_bytes(int N, int KX) {
+    return static_cast<size_t>(KX / 32) * cs_stride(N) * sizeof(float);
+  }
   static size_t smem_bytes(int N, int KX) {
-    return kRingBytes + xs_bytes(N, KX) + cs_bytes(KX) + (kSlots * slot_floats(N) + kSlots) * sizeof(float) +
+    return kRingBytes + xs_bytes(N, KX) + cs_bytes(N, KX) + (kSlots * slot_floats(N) + kSlots) * sizeof(float) +
            2 * STAGES * 8 + 16 + 128;
   }
 };
@@ -123,8 +126,15 @@ __device__ __forceinline__ float stage_block(const float (&x)[32], uint4* dst) {
   return -bias;
 }
 
+// Two CTAs per SM only where the ring leaves room for a second one; otherwise
+// let the kernel use the registers of a single CTA.
 template <int NT, int MT, int KW, int STAGES>
-__global__ void __launch_bounds__(32 * (KW + 1), (NT <= 2 ? 2 : 1))
+constexpr int decode_min_blocks() {
+  return (NT <= 2 && STAGES * KW * 16 * MT * 144 <= 80 * 1024) ? 2 : 1;
+}
+
+template <int NT, int MT, int KW, int STAGES, bool ONE>
+__global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, STAGES>()))
     k_decode_q4_0(const __grid_constant__ CUtensorMap tmW, const float* __restrict__ X, int N, int M, int K,
                   int KX, float* __restrict__ Y, uint64_t limit_ns, uint32_t* err, int early_w) {
   using Cfg = DecodeCfg<NT, MT, KW, STAGES>;
@@ -134,7 +144,8 @@ __global__ void __launch_bounds__(32 * (KW + 1), (NT <= 2 ? 2 : 1))
   uint8_t* ring = smem;
   uint4* xs = reinterpret_cast<uint4*>(smem + Cfg::kRingBytes);
   float* cs = reinterpret_cast<float*>(smem + Cfg::kRingBytes + Cfg::xs_bytes(N, KX));
-  float* acc_slots = cs + Cfg::cs_bytes(KX) / sizeof(float);  // [kSlots][KW][kBM][N]
+  float* acc_slots = cs + Cfg::cs_bytes(N, KX) / sizeof(float);  // [kSlots][KW][kBM][N]
+  const int csn = Cfg::cs_stride(N);
   const int slot_floats = static_cast<int>(Cfg::slot_floats(N));
   int* slot_count = reinterpret_cast<int*>(acc_slots + Cfg::kSlots * slot_floats);
   uint64_t* bars = reinterpret_cast<uint64_t*>(
@@ -221,30 +232,38 @@ __global__ void __launch_bounds__(32 * (KW + 1), (NT <= 2 ? 2 : 1))
     // Stage this chunk of x: per (block, token) four fp16 lane-slot fragments
     // (k permuted like the codes) and the negated bias of the biased codes.
     named_bar_sync(1, 32 * KW);  // previous chunk's fragments are no longer read
-    for (int e = threadIdx.x; e < nbl * N; e += 32 * KW) {
-      const int n = e % N;
-      const int bl = e / N;
-      const int bg = kc0 / kQK + bl;
-      float x[32];
-      if (bg * kQK < K) {
-        const float4* xr =
-            reinterpret_cast<const float4*>(X + static_cast<size_t>(n) * K + static_cast<size_t>(bg) * kQK);
+    // Two (block, token) entries per thread per round, loads issued first.
+    for (int e0 = threadIdx.x; e0 < nbl * N; e0 += 64 * KW) {
+      float xv[2][32];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 v = __ldg(xr + i);
-          x[4 * i] = v.x; x[4 * i + 1] = v.y; x[4 * i + 2] = v.z; x[4 * i + 3] = v.w;
+      for (int h = 0; h < 2; ++h) {
+        const int e = e0 + h * 32 * KW;
+        const int bg = kc0 / kQK + e / N;
+        if (e < nbl * N && bg * kQK < K) {
+          const float4* xr = reinterpret_cast<const float4*>(X + static_cast<size_t>(e % N) * K +
+                                                             static_cast<size_t>(bg) * kQK);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 v = __ldg(xr + i);
+            xv[h][4 * i] = v.x; xv[h][4 * i + 1] = v.y; xv[h][4 * i + 2] = v.z; xv[h][4 * i + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) xv[h][i] = 0.f;
         }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = 0.f;
       }
-      uint4* dst = xs + (bl * N + n) * 4;
-      cs[bl * 8 * NT + n] = (bg & 1) ? stage_block<1>(x, dst) : stage_block<0>(x, dst);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int e = e0 + h * 32 * KW;
+        if (e < nbl * N) {
+          const int n = e % N, bl = e / N;
+          uint4* dst = xs + (bl * N + n) * 4;
+          cs[bl * csn + n] = ((kc0 / kQK + bl) & 1) ? stage_block<1>(xv[h], dst) : stage_block<0>(xv[h], dst);
+        }
+      }
     }
-    for (int e = threadIdx.x; e < nbl * (8 * NT - N); e += 32 * KW) {  // padding tokens: no bias
-      const int pad = 8 * NT - N;
-      cs[(e / pad) * 8 * NT + N + e % pad] = 0.f;
-    }
+    if (N & 1)  // the padding column read by the lane pair of the last token
+      for (int bl = threadIdx.x; bl < nbl; bl += 32 * KW) cs[bl * csn + N] = 0.f;
     named_bar_sync(1, 32 * KW);
 
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tile_iter) {
@@ -264,7 +283,9 @@ __global__ void __launch_bounds__(32 * (KW + 1), (NT <= 2 ? 2 : 1))
           const uint8_t* sub = ring + slot * Cfg::kStageBytes + kw * Cfg::kSubBytes + g * kSubBytesRow;
           const int bl0 = (k0 - kc0) / kQK;
           const uint4* xsp = xs + (bl0 * N + g) * 4 + t;     // + block * 4N + nt * 32
-          const float* csp = cs + bl0 * 8 * NT + 2 * t;      // + block * 8NT + nt * 8
+          const float* csp = cs + bl0 * csn + 2 * t;         // + block * csn + nt * 8
+          const uint4* xs1 = xs + bl0 * 4 + t;               // N = 1: token 0, slot t
+          const float* cs1 = cs + bl0 * csn;                 // N = 1: token 0's bias
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
             uint32_t wd[MT][2][2];  // [m-tile][row g / g+8][even / odd block] code words
@@ -288,10 +309,19 @@ __global__ void __launch_bounds__(32 * (KW + 1), (NT <= 2 ? 2 : 1))
               const int b = 2 * p + e;
               uint4 xf[NT];
               float2 nb[NT];
+              if (ONE) {
+                // N = 1: every lane takes token 0's fragment (columns 1..7 then
+                // repeat column 0 and are never stored) and its bias.
+                xf[0] = xs1[b * 4];
+                const float bias = cs1[b * 2];  // stride of the bias table for N = 1
+                nb[0] = make_float2(bias, 0.f);
+              } else {
 #pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                xf[nt] = (nt * 8 + g < N) ? xsp[b * 4 * N + nt * 32] : make_uint4(0u, 0u, 0u, 0u);
-                nb[nt] = *reinterpret_cast<const float2*>(csp + b * 8 * NT + nt * 8);
+                for (int nt = 0; nt < NT; ++nt) {
+                  xf[nt] = (nt * 8 + g < N) ? xsp[b * 4 * N + nt * 32] : make_uint4(0u, 0u, 0u, 0u);
+                  nb[nt] = (nt * 8 + 2 * t < N) ? *reinterpret_cast<const float2*>(csp + b * csn + nt * 8)
+                                                : make_float2(0.f, 0.f);
+                }
               }
 #pragma unroll
               for (int mt = 0; mt < MT; ++mt) {
@@ -305,9 +335,11 @@ __global__ void __launch_bounds__(32 * (KW + 1), (NT <= 2 ? 2 : 1))
                   mma_m16n8k16_f16(tsum, a_lo, xf[nt].x, xf[nt].y, init);
                   mma_m16n8k16_f16(tsum, a_hi, xf[nt].z, xf[nt].w, tsum);
                   acc[mt][nt][0] = fmaf(dd[mt][0][e], tsum[0], acc[mt][nt][0]);
-                  acc[mt][nt][1] = fmaf(dd[mt][0][e], tsum[1], acc[mt][nt][1]);
                   acc[mt][nt][2] = fmaf(dd[mt][1][e], tsum[2], acc[mt][nt][2]);
-                  acc[mt][nt][3] = fmaf(dd[mt][1][e], tsum[3], acc[mt][nt][3]);
+                  if (!ONE) {  // with N = 1 only column 0 (c0, c2) is ever stored
+                    acc[mt][nt][1] = fmaf(dd[mt][0][e], tsum[1], acc[mt][nt][1]);
+                    acc[mt][nt][3] = fmaf(dd[mt][1][e], tsum[3], acc[mt][nt][3]);
+                  }
                 }
               }
             }
@@ -365,7 +397,7 @@ __global__ void __launch_bounds__(32 * (KW + 1), (NT <= 2 ? 2 : 1))
   }
 }
 
-template <int NT, int MT, int KW, int STAGES>
+template <int NT, int MT, int KW, int STAGES, bool ONE = false>
 cudaError_t launch_cfg(const CUtensorMap* tmW, const float* X, int N, int M, int K, float* Y, uint64_t limit_ns,
                        int xs_budget, int early_w, int pdl, cudaStream_t s) {
   using Cfg = DecodeCfg<NT, MT, KW, STAGES>;
@@ -375,7 +407,7 @@ cudaError_t launch_cfg(const CUtensorMap* tmW, const float* X, int N, int M, int
   const int Kpad = (K + Cfg::kStageK - 1) / Cfg::kStageK * Cfg::kStageK;
   if (KX > Kpad) KX = Kpad;
   const size_t smem = Cfg::smem_bytes(N, KX);
-  auto kern = k_decode_q4_0<NT, MT, KW, STAGES>;
+  auto kern = k_decode_q4_0<NT, MT, KW, STAGES, ONE>;
   static int configured_smem = 0;
   static int occ_cache_smem = -1, occ_cache = 1;
   if (static_cast<int>(smem) > configured_smem) {
@@ -457,10 +489,14 @@ void decode_w_box(int64_t N, int variant, uint32_t* box_x_bytes, uint32_t* box_r
 cudaError_t launch_decode(const CUtensorMap* tmW, const float* X, int64_t N, int64_t M, int64_t K, float* Y,
                           uint64_t wait_limit_ns, int early_w, int variant, int pdl, cudaStream_t s) {
   const int n = static_cast<int>(N), m = static_cast<int>(M), k = static_cast<int>(K);
+  if (N == 1) {
+    if (variant == 1) return launch_cfg<1, 2, 4, 3, true>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    if (variant == 2) return launch_cfg<1, 1, 8, 4, true>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    if (variant == 3) return launch_cfg<1, 2, 8, 2, true>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    return launch_cfg<1, 2, 8, 3, true>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+  }
   if (N <= 8) {
-    if (variant == 1) return launch_cfg<1, 2, 4, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
     if (variant == 2) return launch_cfg<1, 1, 8, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
-    if (variant == 3) return launch_cfg<1, 2, 8, 2>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
     return launch_cfg<1, 2, 8, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
   }
   if (N <= 16) return launch_cfg<2, 1, 8, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);

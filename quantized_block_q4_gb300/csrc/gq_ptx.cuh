@@ -63,8 +63,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int* abort, uint32_t* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  while (true) {
+  for (uint32_t spin = 1;; ++spin) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (spin & 63) continue;  // look at the clock and the abort flag now and then
     if (*abort) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       *abort = 1;
