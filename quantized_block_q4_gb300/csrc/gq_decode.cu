@@ -477,6 +477,7 @@ __global__ void k_generic_q4_0(const uint8_t* __restrict__ W, int64_t M, int64_t
 // Decode configuration by N: (NT, MT, KW, STAGES).  The variant index can be
 // overridden for tuning (GQ_OPT_DECODE_VARIANT); 0 = default.
 int decode_rows_per_tile(int64_t N, int variant) {
+  if (N == 1) return variant == 1 ? 16 : (variant == 2 ? 64 : 32);
   if (N <= 8) return (variant == 2) ? 16 : 32;
   return 16;
 }
@@ -490,8 +491,8 @@ cudaError_t launch_decode(const CUtensorMap* tmW, const float* X, int64_t N, int
                           uint64_t wait_limit_ns, int early_w, int variant, int pdl, cudaStream_t s) {
   const int n = static_cast<int>(N), m = static_cast<int>(M), k = static_cast<int>(K);
   if (N == 1) {
-    if (variant == 1) return launch_cfg<1, 2, 4, 3, true>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
-    if (variant == 2) return launch_cfg<1, 1, 8, 4, true>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    if (variant == 1) return launch_cfg<1, 1, 16, 4, true>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    if (variant == 2) return launch_cfg<1, 4, 8, 2, true>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
     if (variant == 3) return launch_cfg<1, 2, 8, 2, true>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
     return launch_cfg<1, 2, 8, 3, true>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
   }
