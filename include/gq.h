@@ -113,9 +113,11 @@ typedef enum {
                                 while that kernel finishes (weight-stationary inference); default 0 */
   GQ_OPT_DECODE_VARIANT = 4, /* tuning: tile/warp layout of the N <= 8 decode kernel, 0..3 (default 0);
                                 every variant computes the same result */
-  GQ_OPT_PDL = 5             /* 1 (default): launch kernels with programmatic dependent launch, so a
+  GQ_OPT_PDL = 5,            /* 1 (default): launch kernels with programmatic dependent launch, so a
                                 kernel may start while the previous one on the stream drains; every
                                 read of X and write of Y still waits for that previous kernel */
+  GQ_OPT_PREFILL_TILE_N = 6  /* tuning: token-tile width of the tensor-core kernel, 0 = by shape
+                                (default), 128 or 256 */
 } gq_option;
 gq_status gq_set_option(gq_option opt, int64_t value);
 int64_t gq_get_option(gq_option opt);

@@ -349,9 +349,17 @@ cudaError_t launch_prefill_bn(const CUtensorMap* tmW, const CUtensorMap* tmX, in
   return cudaGetLastError();
 }
 
-int prefill_bn(int64_t N) { return N <= 128 ? 128 : 256; }
+int g_bn_override = 0;  // 0: choose by shape; 128 or 256: force the tile width (tuning)
+
+int prefill_bn(int64_t N) {
+  if (g_bn_override) return g_bn_override;
+  return N <= 128 ? 128 : 256;
+}
 
 }  // namespace
+
+void set_prefill_bn_override(int bn) { g_bn_override = bn; }
+int get_prefill_bn_override() { return g_bn_override; }
 
 void prefill_boxes(int64_t N, uint32_t* w_box_x_bytes, uint32_t* w_box_rows, uint32_t* x_box_k,
                    uint32_t* x_box_rows) {
