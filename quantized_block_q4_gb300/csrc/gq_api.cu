@@ -326,6 +326,9 @@ gq_status gq_set_option(gq_option opt, int64_t value) {
       if (value != 0 && value != 128 && value != 256) return fail(GQ_ERR_SHAPE, "tile width must be 0, 128 or 256");
       set_prefill_bn_override(static_cast<int>(value));
       return GQ_OK;
+    case GQ_OPT_PREFILL_PAIR:
+      set_prefill_pair_mode(static_cast<int>(value));
+      return GQ_OK;
   }
   return fail(GQ_ERR_SHAPE, "unknown option %d", static_cast<int>(opt));
 }
@@ -339,6 +342,7 @@ int64_t gq_get_option(gq_option opt) {
     case GQ_OPT_DECODE_VARIANT: return g_decode_variant.load();
     case GQ_OPT_PDL: return g_pdl.load();
     case GQ_OPT_PREFILL_TILE_N: return get_prefill_bn_override();
+    case GQ_OPT_PREFILL_PAIR: return get_prefill_pair_mode();
   }
   return -1;
 }
