@@ -403,12 +403,13 @@ PROFILE_CASES = {
 }
 
 
-def run_profile_case(name):
+def run_profile_case(name, pair=False):
     """One small invocation for an ncu capture: two launches of one MUL_MAT."""
     import torch
     import quantized_block_q4_gb300 as gq
     M, K, N, mode = PROFILE_CASES[name]
     gq.gq_set_option(gq.GQ_OPT_WEIGHTS_STATIC, 1)
+    gq.gq_set_option(gq.GQ_OPT_PREFILL_PAIR, 1 if pair else 0)
     W = torch.from_numpy(synth.q4_0_weights(M, K, seed=1)).cuda()
     X = torch.from_numpy(synth.activations(N, K, seed=2)).cuda()
     Y = torch.empty(N, M, device="cuda")
@@ -427,6 +428,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
                     help="run one MUL_MAT twice (for an ncu capture) and exit")
+    ap.add_argument("--pair", action="store_true", help="with --profile-case: use the 2-SM prefill kernel")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
@@ -437,7 +439,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.profile_case:
-        return run_profile_case(args.profile_case)
+        return run_profile_case(args.profile_case, args.pair)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

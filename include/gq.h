@@ -118,8 +118,8 @@ typedef enum {
                                 read of X and write of Y still waits for that previous kernel */
   GQ_OPT_PREFILL_TILE_N = 6, /* tuning: token-tile width of the 1-CTA tensor-core kernel, 0 = by shape
                                 (default), 128 or 256; a non-zero value also selects the 1-CTA kernel */
-  GQ_OPT_PREFILL_PAIR = 7    /* 1 (default): N > 128 runs the 2-SM kernel (CTA pairs, 256 x 256 tiles);
-                                0: the 1-CTA kernel */
+  GQ_OPT_PREFILL_PAIR = 7    /* 1: N > 128 runs the 2-SM kernel (CTA pairs, 256 x 256 tiles);
+                                0 (default): the 1-CTA kernel */
 } gq_option;
 gq_status gq_set_option(gq_option opt, int64_t value);
 int64_t gq_get_option(gq_option opt);

@@ -46,7 +46,7 @@ cudaError_t launch_f32_to_bf16(const float* x, uint16_t* y, int64_t n, cudaStrea
 cudaError_t launch_prefill(const CUtensorMap* tmW, const CUtensorMap* tmX, int64_t N, int64_t M,
                            int64_t K, float* Y, uint64_t wait_limit_ns, cudaStream_t s);
 void set_prefill_bn_override(int bn);  // 0 = by shape, else 128 or 256
-void set_prefill_pair_mode(int on);    // 1 (default): 2-SM pair kernel for N > 128
+void set_prefill_pair_mode(int on);    // 1: 2-SM pair kernel for N > 128 (default 0)
 int get_prefill_pair_mode();
 int get_prefill_bn_override();
 void prefill_boxes(int64_t N, uint32_t* w_box_x_bytes, uint32_t* w_box_rows, uint32_t* x_box_k,

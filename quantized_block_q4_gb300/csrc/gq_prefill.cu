@@ -597,8 +597,8 @@ int prefill_bn(int64_t N) {
   return N <= 128 ? 128 : 256;
 }
 
-// 0: 1-CTA kernel with 128 x prefill_bn tiles; 1: 2-SM pair kernel (256 x 256 tiles).
-int g_pair_mode = 1;
+// 0 (default): 1-CTA kernel with 128 x prefill_bn tiles; 1: 2-SM pair kernel (256 x 256 tiles).
+int g_pair_mode = 0;
 bool use_pair(int64_t N) { return g_pair_mode && g_bn_override == 0 && N > 128; }
 
 }  // namespace
