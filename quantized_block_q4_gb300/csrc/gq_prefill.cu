@@ -517,7 +517,7 @@ __global__ void __launch_bounds__(Prefill2Cfg::kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (live && lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&a_full[as]), 0));
+        if (live && lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&a_full[as]), 0));
       }
     }
     if (live) live = mbar_wait_bounded(smem_u32(acc_full), 0, limit_ns, abort_flag, err);

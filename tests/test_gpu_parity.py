@@ -249,6 +249,19 @@ def test_prefill_n_tiles(N):
     check_mm(384, 1024, N, 5000 + N)
 
 
+@pytest.mark.parametrize("opt,val", [("GQ_OPT_PREFILL_PAIR", 1), ("GQ_OPT_PREFILL_TILE_N", 128)])
+@pytest.mark.parametrize("M,N", [(384, 129), (384, 300), (640, 513), (130, 257)])
+def test_prefill_kernel_options(opt, val, M, N):
+    """The 2-SM (CTA pair) kernel and the 128-wide tile variant, each against the oracle."""
+    code = getattr(gq, opt)
+    old = gq.gq_get_option(code)
+    gq.gq_set_option(code, val)
+    try:
+        check_mm(M, 1024, N, 5100 + M + N)
+    finally:
+        gq.gq_set_option(code, old)
+
+
 def test_f32_to_bf16_matches_torch_rounding():
     x = torch.from_numpy(synth.activations(7, 1000, seed=12)).cuda().reshape(-1)
     x[:6] = torch.tensor([float("nan"), float("inf"), -float("inf"), 0.0, -0.0, 1e-40], device="cuda")
