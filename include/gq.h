@@ -67,22 +67,27 @@ gq_status gq_dequant_q4_0(const void *W, int64_t M, int64_t K, float *out, void 
  * bf16 once and runs the tcgen05 tensor-core kernel on bf16 tiles of the
  * dequantised W with fp32 accumulation.  Fast paths need K % 256 == 0 and W,
  * X, Y 16-byte aligned; other shapes take a slower generic kernel.  The N >= 64
- * path allocates N*K*2 bytes of stream-ordered scratch (cudaMallocAsync) and
- * frees it on the same stream.  Accuracy: |y - y_ref| <= 1e-3*sum_k|w_k x_k|
+ * path allocates N*K*2 bytes of stream-ordered scratch (cudaMallocAsync) for
+ * bf16 X, plus, when the tensor-core kernel splits tiles across CTAs
+ * (GQ_OPT_PREFILL_STREAMK), 2 x 128 KiB per CTA and 4 bytes per output tile
+ * for partial sums; it frees them on the same stream.  Accuracy: |y - y_ref| <= 1e-3*sum_k|w_k x_k|
  * + 1e-5 on the synthetic workloads (random-sign data). */
 gq_status gq_mul_mat_q4_0(const void *W, int64_t M, int64_t K, const float *X, int64_t N, float *Y,
                           void *stream);
 
 /* MUL_MAT with activations the caller already holds in bf16: X_bf16[N][K]
- * (raw bfloat16 bits).  Runs the tensor-core kernel for every N >= 1 and
- * allocates nothing.  Needs K % 256 == 0, W and X_bf16 16-byte aligned. */
+ * (raw bfloat16 bits).  Runs the tensor-core kernel for every N >= 1.  Its
+ * only allocation is the stream-ordered partial-sum scratch of split tiles
+ * (see gq_mul_mat_q4_0); if that allocation fails it runs one CTA per tile
+ * instead.  Needs K % 256 == 0, W and X_bf16 16-byte aligned. */
 gq_status gq_mul_mat_q4_0_bf16x(const void *W, int64_t M, int64_t K, const uint16_t *X_bf16, int64_t N,
                                 float *Y, void *stream);
 
 /* Same result as the N >= 64 path of gq_mul_mat_q4_0 (bf16 activations,
  * tensor-core kernel), for any N >= 1, but with no device allocation: the
  * bf16 copy of X goes to a fixed 12 MiB array inside the library instead of
- * cudaMallocAsync scratch.  The pages have no counterpart; it exists for
+ * cudaMallocAsync scratch, and the tensor-core kernel runs one CTA per tile
+ * (no stream-K partial sums).  The pages have no counterpart; it exists for
  * callers that cannot let a library allocate device memory (memory pools that
  * own the whole device, fixed arenas, allocation-free hot loops).
  *  - Needs K % 256 == 0 and N*K <= 6291456 (GQ_ERR_SHAPE otherwise), W 16-byte
@@ -118,8 +123,13 @@ typedef enum {
                                 read of X and write of Y still waits for that previous kernel */
   GQ_OPT_PREFILL_TILE_N = 6, /* tuning: token-tile width of the 1-CTA tensor-core kernel, 0 = by shape
                                 (default), 128 or 256; a non-zero value also selects the 1-CTA kernel */
-  GQ_OPT_PREFILL_PAIR = 7    /* 1: N > 128 runs the 2-SM kernel (CTA pairs, 256 x 256 tiles);
+  GQ_OPT_PREFILL_PAIR = 7,   /* 1: N > 128 runs the 2-SM kernel (CTA pairs, 256 x 256 tiles);
                                 0 (default): the 1-CTA kernel */
+  GQ_OPT_PREFILL_STREAMK = 8 /* work split of the 1-CTA tensor-core kernel: 1 (default) = by shape:
+                                when the output tiles fill the SMs unevenly, the tiles' k ranges
+                                are spread evenly over one CTA per SM and split tiles are summed
+                                in a fixed order (results do not depend on timing); 0 = one CTA
+                                per tile; n >= 2 = exactly n CTAs (test aid) */
 } gq_option;
 gq_status gq_set_option(gq_option opt, int64_t value);
 int64_t gq_get_option(gq_option opt);

@@ -140,6 +140,40 @@ const DeviceInfo& device_info() {
   return di;
 }
 
+// Stream-ordered scratch from a pool the library owns (one per device), which
+// keeps freed memory for the next call instead of returning it to the driver
+// at every synchronisation; the caller's own default pool is left alone.
+static cudaMemPool_t scratch_pool() {
+  static cudaMemPool_t pools[kMaxDevices];
+  static std::mutex mu;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!pools[dev]) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t p = nullptr;
+    if (cudaMemPoolCreate(&p, &props) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    uint64_t keep = ~0ull;
+    cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep);
+    pools[dev] = p;
+  }
+  return pools[dev];
+}
+
+cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t s) {
+  cudaMemPool_t pool = scratch_pool();
+  return pool ? cudaMallocFromPoolAsync(p, bytes, pool, s) : cudaMallocAsync(p, bytes, s);
+}
+
+cudaError_t scratch_free(void* p, cudaStream_t s) { return cudaFreeAsync(p, s); }
+
 }  // namespace gq
 
 using namespace gq;
@@ -160,7 +194,7 @@ static gq_status mul_mat_decode(const void* W, int64_t M, int64_t K, const float
 }
 
 static gq_status mul_mat_prefill_bf16(const void* W, int64_t M, int64_t K, const uint16_t* Xb, int64_t N, float* Y,
-                                      cudaStream_t s) {
+                                      bool allow_scratch, cudaStream_t s) {
   CUtensorMap tmW, tmX;
   uint32_t wbx, wby, xbk, xbr;
   prefill_boxes(N, &wbx, &wby, &xbk, &xbr);
@@ -171,7 +205,8 @@ static gq_status mul_mat_prefill_bf16(const void* W, int64_t M, int64_t K, const
   st = make_tmap(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Xb, static_cast<uint64_t>(K), static_cast<uint64_t>(N),
                  static_cast<uint64_t>(K) * 2, xbk, xbr, CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != GQ_OK) return st;
-  cudaError_t e = launch_prefill(&tmW, &tmX, N, M, K, Y, static_cast<uint64_t>(g_wait_limit_ns.load()), s);
+  cudaError_t e =
+      launch_prefill(&tmW, &tmX, N, M, K, Y, static_cast<uint64_t>(g_wait_limit_ns.load()), allow_scratch, s);
   return e == cudaSuccess ? GQ_OK : cuda_fail(e, "prefill launch");
 }
 
@@ -180,8 +215,8 @@ gq_status api_fail(gq_status st, const char* msg) { return fail(st, "%s", msg); 
 gq_status api_check_device() { return check_device(); }
 gq_status api_check_mm_shape(int64_t M, int64_t K, int64_t N) { return check_mm_shape(M, K, N); }
 gq_status api_prefill_bf16(const void* W, int64_t M, int64_t K, const uint16_t* X_bf16, int64_t N, float* Y,
-                           cudaStream_t s) {
-  return mul_mat_prefill_bf16(W, M, K, X_bf16, N, Y, s);
+                           bool allow_scratch, cudaStream_t s) {
+  return mul_mat_prefill_bf16(W, M, K, X_bf16, N, Y, allow_scratch, s);
 }
 }  // namespace gq
 
@@ -235,17 +270,17 @@ gq_status gq_mul_mat_q4_0(const void* W, int64_t M, int64_t K, const float* X, i
   // Prefill: X -> bf16 scratch (stream-ordered), then the tensor-core kernel.
   const size_t xbytes = static_cast<size_t>(N) * K * sizeof(uint16_t);
   void* xb = nullptr;
-  cudaError_t e = cudaMallocAsync(&xb, xbytes, s);
-  if (e != cudaSuccess) return fail(GQ_ERR_ALLOC, "cudaMallocAsync(%zu): %s", xbytes, cudaGetErrorString(e));
+  cudaError_t e = scratch_alloc(&xb, xbytes, s);
+  if (e != cudaSuccess) return fail(GQ_ERR_ALLOC, "scratch allocation (%zu bytes): %s", xbytes, cudaGetErrorString(e));
   e = launch_f32_to_bf16(X, static_cast<uint16_t*>(xb), N * K, s);
   if (e != cudaSuccess) {
-    cudaFreeAsync(xb, s);
+    scratch_free(xb, s);
     return cuda_fail(e, "f32->bf16 launch");
   }
-  st = mul_mat_prefill_bf16(W, M, K, static_cast<const uint16_t*>(xb), N, Y, s);
-  e = cudaFreeAsync(xb, s);
+  st = mul_mat_prefill_bf16(W, M, K, static_cast<const uint16_t*>(xb), N, Y, true, s);
+  e = scratch_free(xb, s);
   if (st != GQ_OK) return st;
-  return e == cudaSuccess ? GQ_OK : cuda_fail(e, "cudaFreeAsync");
+  return e == cudaSuccess ? GQ_OK : cuda_fail(e, "scratch free");
 }
 
 gq_status gq_mul_mat_q4_0_bf16x(const void* W, int64_t M, int64_t K, const uint16_t* X_bf16, int64_t N, float* Y,
@@ -266,7 +301,7 @@ gq_status gq_mul_mat_q4_0_bf16x(const void* W, int64_t M, int64_t K, const uint1
   if (K % 256) return fail(GQ_ERR_SHAPE, "the bf16-activation path needs K %% 256 == 0 (K=%lld)", (long long)K);
   if (!aligned(W, 16) || !aligned(X_bf16, 16) || !aligned(Y, 16))
     return fail(GQ_ERR_ALIGN, "W, X_bf16 and Y must be 16-byte aligned");
-  return mul_mat_prefill_bf16(W, M, K, X_bf16, N, Y, s);
+  return mul_mat_prefill_bf16(W, M, K, X_bf16, N, Y, true, s);
 }
 
 gq_status gq_f32_to_bf16(const float* x, uint16_t* y, int64_t n, void* stream) {
@@ -329,6 +364,10 @@ gq_status gq_set_option(gq_option opt, int64_t value) {
     case GQ_OPT_PREFILL_PAIR:
       set_prefill_pair_mode(static_cast<int>(value));
       return GQ_OK;
+    case GQ_OPT_PREFILL_STREAMK:
+      if (value < 0 || value > 65536) return fail(GQ_ERR_SHAPE, "stream-K setting must be 0..65536");
+      set_prefill_streamk(value);
+      return GQ_OK;
   }
   return fail(GQ_ERR_SHAPE, "unknown option %d", static_cast<int>(opt));
 }
@@ -343,6 +382,7 @@ int64_t gq_get_option(gq_option opt) {
     case GQ_OPT_PDL: return g_pdl.load();
     case GQ_OPT_PREFILL_TILE_N: return get_prefill_bn_override();
     case GQ_OPT_PREFILL_PAIR: return get_prefill_pair_mode();
+    case GQ_OPT_PREFILL_STREAMK: return get_prefill_streamk();
   }
   return -1;
 }

@@ -24,6 +24,10 @@ struct DeviceInfo {
 };
 const DeviceInfo& device_info();  // current device, cached
 
+// Stream-ordered scratch from the library's own per-device pool (gq_api.cu).
+cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t s);
+cudaError_t scratch_free(void* p, cudaStream_t s);
+
 // ---- K1: Q4_0 blocks -> fp32, bit-exact (gq_dequant.cu)
 cudaError_t launch_dequant_vec(const uint8_t* W, int64_t nblocks, float* out, cudaStream_t s);
 cudaError_t launch_dequant_bytes(const uint8_t* W, int64_t nblocks, float* out, cudaStream_t s);
@@ -43,8 +47,12 @@ cudaError_t launch_generic(const uint8_t* W, int64_t M, int64_t K, const float* 
 cudaError_t launch_f32_to_bf16(const float* x, uint16_t* y, int64_t n, cudaStream_t s);
 
 // ---- K3: prefill mul_mat on tcgen05 (gq_prefill.cu).  Needs K % 256 == 0.
+// allow_scratch: the launch may take stream-ordered scratch for stream-K
+// partial tiles (else, or if that allocation fails, one CTA per tile).
 cudaError_t launch_prefill(const CUtensorMap* tmW, const CUtensorMap* tmX, int64_t N, int64_t M,
-                           int64_t K, float* Y, uint64_t wait_limit_ns, cudaStream_t s);
+                           int64_t K, float* Y, uint64_t wait_limit_ns, bool allow_scratch, cudaStream_t s);
+void set_prefill_streamk(int64_t v);   // 0 off, 1 by shape (default), >= 2: force that many CTAs
+int64_t get_prefill_streamk();
 void set_prefill_bn_override(int bn);  // 0 = by shape, else 128 or 256
 void set_prefill_pair_mode(int on);    // 1: 2-SM pair kernel for N > 128 (default 0)
 int get_prefill_pair_mode();
@@ -57,6 +65,6 @@ gq_status api_fail(gq_status st, const char* msg);  // records the per-thread er
 gq_status api_check_device();
 gq_status api_check_mm_shape(int64_t M, int64_t K, int64_t N);
 gq_status api_prefill_bf16(const void* W, int64_t M, int64_t K, const uint16_t* X_bf16, int64_t N, float* Y,
-                           cudaStream_t s);
+                           bool allow_scratch, cudaStream_t s);
 
 }  // namespace gq

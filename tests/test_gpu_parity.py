@@ -262,6 +262,61 @@ def test_prefill_kernel_options(opt, val, M, N):
         gq.gq_set_option(code, old)
 
 
+def _with_option(code, val, fn):
+    old = gq.gq_get_option(code)
+    gq.gq_set_option(code, val)
+    try:
+        return fn()
+    finally:
+        gq.gq_set_option(code, old)
+
+
+# (M, K, N, CTAs): T = ceil(M/128) * ceil(N/BN) tiles of K/256 units each.
+#   384x1024, N=300: T=6, 24 units -> 5 CTAs (splits of 2), 13 (tiles over 3-4 CTAs),
+#   24 (one unit per CTA), 40 (clamped to 24); N=100 takes the 128-wide tile;
+#   640x2048, N=513: T=15, 120 units over 7 or 152 CTAs; 130 rows: ragged last row block.
+@pytest.mark.parametrize("M,K,N,G", [(384, 1024, 300, 5), (384, 1024, 300, 13), (384, 1024, 300, 24),
+                                     (384, 1024, 300, 40), (384, 1024, 100, 5), (640, 2048, 513, 7),
+                                     (640, 2048, 513, 152), (130, 1024, 257, 3)])
+def test_prefill_stream_k_splits(M, K, N, G):
+    """Tiles whose k range is split across CTAs: partial sums through the
+    workspace, summed by whichever CTA arrives last, against the oracle."""
+    code = gq.GQ_OPT_PREFILL_STREAMK
+    _with_option(code, G, lambda: check_mm(M, K, N, 5200 + M + N + G, f"stream-K G={G}"))
+
+
+def test_prefill_stream_k_is_deterministic():
+    """The split tiles are summed in k order, so repeated calls agree bit for bit."""
+    M, K, N = 640, 2048, 513
+    W = dev(synth.q4_0_weights(M, K, seed=5300))
+    X = dev(synth.activations(N, K, seed=5301))
+
+    def run():
+        ys = [gq.mul_mat_q4_0(W, X) for _ in range(4)]
+        torch.cuda.synchronize()
+        return ys
+    ys = _with_option(gq.GQ_OPT_PREFILL_STREAMK, 11, run)
+    for y in ys[1:]:
+        assert torch.equal(ys[0], y)
+
+
+def test_prefill_stream_k_off_matches_oracle():
+    _with_option(gq.GQ_OPT_PREFILL_STREAMK, 0, lambda: check_mm(640, 2048, 513, 5400, "one CTA per tile"))
+
+
+@pytest.mark.parametrize("M,K", [(4096, 4096), (4096, 11008)])
+def test_prefill_full_size_stream_k_sampled_rows(M, K):
+    """Full-size shapes whose 64 tiles leave most SMs idle: the default split
+    spreads their k ranges over all SMs.  Sampled rows against the oracle."""
+    N = 512
+    W = synth.q4_0_weights(M, K, seed=synth.seed_for(5, M + K))
+    X = synth.activations(N, K, seed=synth.seed_for(5, M + K + 1))
+    y = run_mm(W, X, M, K)
+    rows = sampled_rows(M, 128, 43)
+    y_ref, s_ref = oracle_mul_mat(W.reshape(M, -1)[rows], len(rows), K, X)
+    assert_mul_mat_close(y[:, rows], y_ref, s_ref, f"stream-K {M}x{K}")
+
+
 def test_f32_to_bf16_matches_torch_rounding():
     x = torch.from_numpy(synth.activations(7, 1000, seed=12)).cuda().reshape(-1)
     x[:6] = torch.tensor([float("nan"), float("inf"), -float("inf"), 0.0, -0.0, 1e-40], device="cuda")
