@@ -125,11 +125,13 @@ typedef enum {
                                 (default), 128 or 256; a non-zero value also selects the 1-CTA kernel */
   GQ_OPT_PREFILL_PAIR = 7,   /* 1: N > 128 runs the 2-SM kernel (CTA pairs, 256 x 256 tiles);
                                 0 (default): the 1-CTA kernel */
-  GQ_OPT_PREFILL_STREAMK = 8 /* work split of the 1-CTA tensor-core kernel: 1 (default) = by shape:
-                                when the output tiles fill the SMs unevenly, the tiles' k ranges
-                                are spread evenly over one CTA per SM and split tiles are summed
-                                in a fixed order (results do not depend on timing); 0 = one CTA
-                                per tile; n >= 2 = exactly n CTAs (test aid) */
+  GQ_OPT_PREFILL_STREAMK = 8, /* k-splitting of tiles in the tensor-core kernel: 1 (default) = when the
+                                last wave of tiles would leave SMs idle, its tiles are split along k
+                                over the idle SMs and the pieces summed in k order (the result does
+                                not depend on timing); 0 = whole tiles only; n >= 2 = every tile
+                                in n pieces (test aid) */
+  GQ_OPT_PREFILL_SLOTS = 9    /* test aid: run the tensor-core kernel as if the GPU had this many SMs
+                                (CTA pairs: pairs); 0 (default) = the real count */
 } gq_option;
 gq_status gq_set_option(gq_option opt, int64_t value);
 int64_t gq_get_option(gq_option opt);

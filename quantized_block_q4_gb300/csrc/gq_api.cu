@@ -365,8 +365,12 @@ gq_status gq_set_option(gq_option opt, int64_t value) {
       set_prefill_pair_mode(static_cast<int>(value));
       return GQ_OK;
     case GQ_OPT_PREFILL_STREAMK:
-      if (value < 0 || value > 65536) return fail(GQ_ERR_SHAPE, "stream-K setting must be 0..65536");
+      if (value < 0 || value > 4096) return fail(GQ_ERR_SHAPE, "k-split setting must be 0..4096");
       set_prefill_streamk(value);
+      return GQ_OK;
+    case GQ_OPT_PREFILL_SLOTS:
+      if (value < 0 || value > 65536) return fail(GQ_ERR_SHAPE, "slot count must be 0..65536");
+      set_prefill_slots(value);
       return GQ_OK;
   }
   return fail(GQ_ERR_SHAPE, "unknown option %d", static_cast<int>(opt));
@@ -383,6 +387,7 @@ int64_t gq_get_option(gq_option opt) {
     case GQ_OPT_PREFILL_TILE_N: return get_prefill_bn_override();
     case GQ_OPT_PREFILL_PAIR: return get_prefill_pair_mode();
     case GQ_OPT_PREFILL_STREAMK: return get_prefill_streamk();
+    case GQ_OPT_PREFILL_SLOTS: return get_prefill_slots();
   }
   return -1;
 }

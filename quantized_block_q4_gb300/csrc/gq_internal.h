@@ -47,12 +47,14 @@ cudaError_t launch_generic(const uint8_t* W, int64_t M, int64_t K, const float* 
 cudaError_t launch_f32_to_bf16(const float* x, uint16_t* y, int64_t n, cudaStream_t s);
 
 // ---- K3: prefill mul_mat on tcgen05 (gq_prefill.cu).  Needs K % 256 == 0.
-// allow_scratch: the launch may take stream-ordered scratch for stream-K
-// partial tiles (else, or if that allocation fails, one CTA per tile).
+// allow_scratch: the launch may take stream-ordered scratch for the partial
+// sums of tiles split along k (else, or if that allocation fails, whole tiles).
 cudaError_t launch_prefill(const CUtensorMap* tmW, const CUtensorMap* tmX, int64_t N, int64_t M,
                            int64_t K, float* Y, uint64_t wait_limit_ns, bool allow_scratch, cudaStream_t s);
-void set_prefill_streamk(int64_t v);   // 0 off, 1 by shape (default), >= 2: force that many CTAs
+void set_prefill_streamk(int64_t v);   // 0 whole tiles only, 1 by shape (default), n >= 2: every tile in n pieces
 int64_t get_prefill_streamk();
+void set_prefill_slots(int64_t v);     // 0: SM count; n: plan for n SMs (test aid)
+int64_t get_prefill_slots();
 void set_prefill_bn_override(int bn);  // 0 = by shape, else 128 or 256
 void set_prefill_pair_mode(int on);    // 1: 2-SM pair kernel for N > 128 (default 0)
 int get_prefill_pair_mode();

@@ -33,6 +33,8 @@
 // Every wait is bounded; a timeout sets the device error word, the roles
 // drain what they issued, TMEM is released and the CTA exits.
 #include <algorithm>
+#include <atomic>
+#include <random>
 #include <cuda_bf16.h>
 
 #include "gq_internal.h"
@@ -84,22 +86,26 @@ cudaError_t launch_f32_to_bf16(const float* x, uint16_t* y, int64_t n, cudaStrea
 
 namespace {
 
-template <int BN>
+template <int BN, bool PAIR>
 struct PrefillCfg {
-  static constexpr int kBM = 128;
+  static constexpr int kBM = 128;       // W rows per CTA (a CTA pair covers 256)
   static constexpr int kBK = 64;        // k per MMA stage: one 128-byte row of bf16
   static constexpr int kRawK = 256;     // k per raw W stage (one work unit)
   static constexpr int kRawRow = 144;   // bytes of 8 blocks
-  static constexpr int RS = 3, BS = (BN == 256 ? 5 : 8);
+  static constexpr int kCtas = PAIR ? 2 : 1;
+  static constexpr int kXRows = BN / kCtas;            // x rows (tokens) this CTA loads per stage
   static constexpr int kACols = kBK / 2;               // TMEM columns per A stage
-  static constexpr int AS = (512 - BN) / kACols;       // A stages in the rest of TMEM
+  // One ring of S stages, each an A tile in TMEM (64 k of the 128 rows) and
+  // an x tile in shared memory; the accumulator takes the first BN columns.
+  static constexpr int RS = 3, S = PAIR ? 8 : (BN == 256 ? 5 : 8);
+  static_assert(BN + S * kACols <= 512, "TMEM holds the accumulator and the A stages");
   static constexpr int kTmemCols = 512;
   static constexpr int kRawBytes = kBM * kRawRow;  // 18432
-  static constexpr int kBBytes = BN * 128;
+  static constexpr int kBBytes = kXRows * 128;
   static constexpr int kOffB = 0;
-  static constexpr int kOffRaw = kOffB + BS * kBBytes;
+  static constexpr int kOffRaw = kOffB + S * kBBytes;
   static constexpr int kOffBar = kOffRaw + RS * kRawBytes;
-  static constexpr int kNBar = 2 * RS + 2 * AS + 2 * BS + 2;
+  static constexpr int kNBar = 2 * RS + 2 * S + 2;
   static constexpr int kOffTmem = kOffBar + kNBar * 8;
   static constexpr int kOffAbort = kOffTmem + 8;
   static constexpr int kOffFlag = kOffAbort + 8;       // two words: "this CTA reduces the tile"
@@ -107,41 +113,82 @@ struct PrefillCfg {
   static constexpr int kDeqWarps = 16;  // warps 2..17, 4 groups of 4: one 64-k step of each 256-k chunk per group
   static constexpr int kXWarp = 2 + kDeqWarps;  // warp 0 loads W, warp 1 issues MMAs, the last warp loads x
   static constexpr int kThreads = 32 * (3 + kDeqWarps);
-  static constexpr int kSlotFloats = BN * kBM;         // one partial tile, [column][row]
+  static constexpr int kSlotFloats = BN * kBM;         // one CTA's partial tile, [column][row]
 };
 
-// Stream-K split of a launch: the T output tiles x nr chunks of 256 k are
-// U = T*nr work units in tile-major order; CTA g of G takes the contiguous
-// units [g*U/G, (g+1)*U/G).  A CTA thus runs one or more segments (a tile
-// and a range of its chunks); only its first and last segments can cover
-// part of a tile.  With G == T every CTA runs exactly one whole tile.
+// Work schedule of a launch over G work ranges (one CTA, or one CTA pair,
+// each; G <= the SMs or pairs, so every range runs at once):
+//   * tiles [R, T) are whole tiles, dealt round-robin: range g runs tiles
+//     R + g, R + g + G, ... (persistent: the rings and the accumulator
+//     hand-off carry over from one tile to the next);
+//   * tiles [0, R) are each split into s pieces along k (256-k chunks
+//     [p*nr/s, (p+1)*nr/s)); piece p of tile t is the first segment of range
+//     t*s + p.  The pieces' partial sums meet in a workspace and the range that
+//     finds all the others published adds them, in k order.
+// R = 0 is the plain one-tile-per-CTA split when T <= G.
 struct PrefillWork {
-  int64_t units;  // U
-  int nr;         // chunks per tile, K / 256
-  int ntn;        // token tiles per 128-row block; tile t = (t / ntn, t % ntn)
-  float* ws;      // 2 partial-tile slots per CTA (nullptr when no tile is split)
-  int* count;     // per tile: partials published so far; zero at launch
+  int64_t T;      // output tiles; tile t = (row block t / ntn, token block t % ntn)
+  int64_t G;      // work ranges
+  int nr;         // 256-k chunks per tile, K / 256
+  int ntn;        // token tiles per row block
+  int R, s;       // split tiles and pieces per split tile
+  float* ws;      // one partial-tile slot per piece and CTA (nullptr when R == 0)
+  unsigned long long* count;  // per split tile and CTA of a pair: (epoch << 8) | pieces published
+  unsigned long long epoch;   // this launch's tag (< 2^56): a counter with another tag reads as 0
 };
 
-__device__ __forceinline__ int64_t sk_begin(int64_t g, int64_t grid, int64_t units) { return g * units / grid; }
-// The CTA whose range holds unit u.
-__device__ __forceinline__ int sk_owner(int64_t u, int64_t grid, int64_t units) {
-  return static_cast<int>(((u + 1) * grid - 1) / units);
+// Arrival counters need no zeroing between launches: a counter whose tag is
+// not this launch's epoch counts as zero pieces.
+__device__ __forceinline__ int pieces_published(unsigned long long v, unsigned long long epoch) {
+  return (v >> 8) == epoch ? static_cast<int>(v & 0xFF) : 0;
 }
-// Partial slot of CTA g for tile t: 0 for the CTA's first tile, 1 for its last.
-__device__ __forceinline__ int64_t sk_slot(int g, int64_t t, int64_t grid, const PrefillWork& wk) {
-  return 2 * static_cast<int64_t>(g) + (sk_begin(g, grid, wk.units) / wk.nr == t ? 0 : 1);
+
+// Count one more published piece; returns how many were published before it
+// (-1 if the update kept failing, which only heavy contention could cause).
+__device__ __forceinline__ int publish_piece(unsigned long long* count, unsigned long long epoch) {
+  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(count);
+  for (int tries = 0; tries < (1 << 20); ++tries) {
+    const int before = pieces_published(cur, epoch);
+    const unsigned long long want = (epoch << 8) | static_cast<unsigned long long>(before + 1);
+    const unsigned long long seen = atomicCAS(count, cur, want);
+    if (seen == cur) return before;
+    cur = seen;
+  }
+  return -1;
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
 }
 
 struct Seg {
-  int64_t t;  // tile
-  int r0, r1; // chunk range [r0, r1) of the tile
+  int64_t t;   // tile
+  int r0, r1;  // chunk range [r0, r1) of the tile
 };
-__device__ __forceinline__ Seg seg_at(int64_t u, int64_t ue, int nr) {
+
+__device__ __forceinline__ int seg_count(int g, const PrefillWork& wk) {
+  const int64_t full = wk.T - wk.R;
+  const int64_t nfull = full > g ? (full - g + wk.G - 1) / wk.G : 0;
+  return (g < static_cast<int64_t>(wk.R) * wk.s ? 1 : 0) + static_cast<int>(nfull);
+}
+
+__device__ __forceinline__ Seg seg_of(int g, int i, const PrefillWork& wk) {
   Seg sg;
-  sg.t = u / nr;
-  sg.r0 = static_cast<int>(u - sg.t * nr);
-  sg.r1 = static_cast<int>(sg.r0 + ue - u < nr ? sg.r0 + ue - u : nr);
+  if (g < static_cast<int64_t>(wk.R) * wk.s) {
+    if (i == 0) {
+      const int p = g % wk.s;
+      sg.t = g / wk.s;
+      sg.r0 = p * wk.nr / wk.s;
+      sg.r1 = (p + 1) * wk.nr / wk.s;
+      return sg;
+    }
+    --i;
+  }
+  sg.t = wk.R + g + static_cast<int64_t>(i) * wk.G;
+  sg.r0 = 0;
+  sg.r1 = wk.nr;
   return sg;
 }
 
@@ -195,56 +242,69 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int slots, uint32_t i
   }
 }
 
-template <int BN>
-__global__ void __launch_bounds__(PrefillCfg<BN>::kThreads, 1)
+template <int BN, bool PAIR>
+__global__ void __launch_bounds__(PrefillCfg<BN, PAIR>::kThreads, 1)
     k_prefill_q4_0(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int N, int M,
                    float* __restrict__ Y, const PrefillWork wk, uint64_t limit_ns, uint32_t* err) {
-  using C = PrefillCfg<BN>;
+  using C = PrefillCfg<BN, PAIR>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* raw_full = bars;
   uint64_t* raw_empty = raw_full + C::RS;
-  uint64_t* a_full = raw_empty + C::RS;
-  uint64_t* a_empty = a_full + C::AS;
-  uint64_t* b_full = a_empty + C::AS;
-  uint64_t* b_empty = b_full + C::BS;
-  uint64_t* acc_full = b_empty + C::BS;
+  uint64_t* full = raw_empty + C::RS;   // stage holds A (dequant arrivals) and x (TMA bytes)
+  uint64_t* empty = full + C::S;        // stage's MMAs have completed
+  uint64_t* acc_full = empty + C::S;
   uint64_t* acc_empty = acc_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffTmem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
   volatile int* reduce_flag = reinterpret_cast<volatile int*>(smem + C::kOffFlag);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t grid = gridDim.x;
-  const int64_t ub = sk_begin(blockIdx.x, grid, wk.units), ue = sk_begin(blockIdx.x + 1, grid, wk.units);
+  // A pair shares one range of work units; its leader (rank 0) issues the MMAs.
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int gi = static_cast<int>(blockIdx.x / C::kCtas);
+  const int nseg = seg_count(gi, wk);
   const int nr = wk.nr;
+  // Barriers the leader's MMA thread waits on receive the arrivals of both CTAs.
+  auto leader_bar = [&](uint64_t* bar) -> uint32_t { return PAIR ? mapa_shared(smem_u32(bar), 0) : smem_u32(bar); };
+  auto arrive_leader = [&](uint64_t* bar) {
+    if (PAIR)
+      mbar_arrive_remote(leader_bar(bar));
+    else
+      mbar_arrive(smem_u32(bar));
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::RS; ++i) {
       mbar_init(smem_u32(&raw_full[i]), 1);
       mbar_init(smem_u32(&raw_empty[i]), C::kDeqWarps);
     }
-    for (int i = 0; i < C::AS; ++i) {
-      mbar_init(smem_u32(&a_full[i]), 4);  // the 4 warps of the group that owns this k step
-      mbar_init(smem_u32(&a_empty[i]), 1);
-    }
-    for (int i = 0; i < C::BS; ++i) {
-      mbar_init(smem_u32(&b_full[i]), 1);
-      mbar_init(smem_u32(&b_empty[i]), 1);
+    for (int i = 0; i < C::S; ++i) {
+      // the 4 dequant warps of the owning group in each CTA, plus the leader's
+      // x producer (expect_tx); every x half completes its bytes on it
+      mbar_init(smem_u32(&full[i]), 4 * C::kCtas + 1);
+      mbar_init(smem_u32(&empty[i]), 1);
     }
     mbar_init(smem_u32(acc_full), 1);
-    mbar_init(smem_u32(acc_empty), C::kDeqWarps);
+    mbar_init(smem_u32(acc_empty), C::kDeqWarps * C::kCtas);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -254,9 +314,9 @@ __global__ void __launch_bounds__(PrefillCfg<BN>::kThreads, 1)
       tma_prefetch_desc(&tmW);
       uint32_t nraw = 0;
       bool ok = true;
-      for (int64_t u = ub; u < ue && ok;) {
-        const Seg sg = seg_at(u, ue, nr);
-        const int m0 = static_cast<int>(sg.t / wk.ntn) * C::kBM;
+      for (int i = 0; i < nseg && ok; ++i) {
+        const Seg sg = seg_of(gi, i, wk);
+        const int m0 = static_cast<int>(sg.t / wk.ntn) * (C::kBM * C::kCtas) + static_cast<int>(rank) * C::kBM;
         for (int r = sg.r0; r < sg.r1; ++r) {
           const uint32_t slot = nraw % C::RS;
           if (!mbar_wait_bounded(smem_u32(&raw_empty[slot]), ((nraw / C::RS) & 1) ^ 1, limit_ns, abort_flag, err)) {
@@ -267,7 +327,6 @@ __global__ void __launch_bounds__(PrefillCfg<BN>::kThreads, 1)
           tma_load_2d(sbase + C::kOffRaw + slot * C::kRawBytes, &tmW, r * C::kRawRow, m0, smem_u32(&raw_full[slot]));
           ++nraw;
         }
-        u += sg.r1 - sg.r0;
       }
       if (!ok) drain_ring(raw_full, C::RS, nraw, limit_ns);
     }
@@ -277,31 +336,37 @@ __global__ void __launch_bounds__(PrefillCfg<BN>::kThreads, 1)
       tma_prefetch_desc(&tmX);
       uint32_t nb = 0;
       bool ok = true;
-      for (int64_t u = ub; u < ue && ok;) {
-        const Seg sg = seg_at(u, ue, nr);
-        const int n0 = static_cast<int>(sg.t % wk.ntn) * BN;
+      for (int i = 0; i < nseg && ok; ++i) {
+        const Seg sg = seg_of(gi, i, wk);
+        const int n0 = static_cast<int>(sg.t % wk.ntn) * BN + static_cast<int>(rank) * C::kXRows;
         for (int ks = 4 * sg.r0; ks < 4 * sg.r1; ++ks) {
-          const uint32_t bs = nb % C::BS;
-          if (!mbar_wait_bounded(smem_u32(&b_empty[bs]), ((nb / C::BS) & 1) ^ 1, limit_ns, abort_flag, err)) {
+          const uint32_t bs = nb % C::S;
+          if (!mbar_wait_bounded(smem_u32(&empty[bs]), ((nb / C::S) & 1) ^ 1, limit_ns, abort_flag, err)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(smem_u32(&b_full[bs]), C::kBBytes);
-          tma_load_2d(sbase + C::kOffB + bs * C::kBBytes, &tmX, ks * C::kBK, n0, smem_u32(&b_full[bs]));
+          const uint32_t dst = sbase + C::kOffB + bs * C::kBBytes;
+          if (PAIR) {
+            if (leader) mbar_arrive_expect_tx(smem_u32(&full[bs]), C::kCtas * C::kBBytes);
+            tma_load_2d_pair(dst, &tmX, ks * C::kBK, n0, leader_bar(&full[bs]));
+          } else {
+            mbar_arrive_expect_tx(smem_u32(&full[bs]), C::kBBytes);
+            tma_load_2d(dst, &tmX, ks * C::kBK, n0, smem_u32(&full[bs]));
+          }
           ++nb;
         }
-        u += sg.r1 - sg.r0;
       }
-      if (!ok) drain_ring(b_full, C::BS, nb, limit_ns);
+      // (a pair's x copies complete on the leader's barriers: only the leader can drain them)
+      if (!ok && leader) drain_ring(full, C::S, nb, limit_ns);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = umma_idesc_bf16_f32(128, BN);
+    // ------------------------------------------------------------ MMA issuer (the leader of a pair)
+    if (leader && lane == 0) {
+      constexpr uint32_t idesc = umma_idesc_bf16_f32(C::kBM * C::kCtas, BN);
       uint32_t c = 0, seg = 0;
       bool ok = true;
-      for (int64_t u = ub; u < ue && ok;) {
-        const Seg sg = seg_at(u, ue, nr);
+      for (int i = 0; i < nseg && ok; ++i) {
+        const Seg sg = seg_of(gi, i, wk);
         // the previous segment's epilogue must have read the accumulator
         if (seg > 0 && !mbar_wait_bounded(smem_u32(acc_empty), (seg - 1) & 1, limit_ns, abort_flag, err)) {
           ok = false;
@@ -309,25 +374,33 @@ __global__ void __launch_bounds__(PrefillCfg<BN>::kThreads, 1)
         }
         tc_fence_after();
         for (int ks = 4 * sg.r0; ks < 4 * sg.r1; ++ks, ++c) {
-          const uint32_t as = c % C::AS, bs = c % C::BS;
-          if (!mbar_wait_bounded(smem_u32(&a_full[as]), (c / C::AS) & 1, limit_ns, abort_flag, err) ||
-              !mbar_wait_bounded(smem_u32(&b_full[bs]), (c / C::BS) & 1, limit_ns, abort_flag, err)) {
+          const uint32_t st = c % C::S;
+          if (!mbar_wait_bounded(smem_u32(&full[st]), (c / C::S) & 1, limit_ns, abort_flag, err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_tmem = tmem_base + BN + as * C::kACols;
-          const uint32_t b_addr = sbase + C::kOffB + bs * C::kBBytes;
+          const uint32_t a_tmem = tmem_base + BN + st * C::kACols;
+          const uint32_t b_addr = sbase + C::kOffB + st * C::kBBytes;
 #pragma unroll
-          for (int kk = 0; kk < C::kBK / 16; ++kk)
-            umma_bf16_ts(tmem_base, a_tmem + kk * 8, umma_desc_sw128(b_addr + kk * 32), idesc,
-                         ks != 4 * sg.r0 || kk != 0);
-          umma_commit(smem_u32(&a_empty[as]));
-          umma_commit(smem_u32(&b_empty[bs]));
+          for (int kk = 0; kk < C::kBK / 16; ++kk) {
+            const uint32_t acc = ks != 4 * sg.r0 || kk != 0;
+            if (PAIR)
+              umma_bf16_ts_pair(tmem_base, a_tmem + kk * 8, umma_desc_sw128(b_addr + kk * 32), idesc, acc);
+            else
+              umma_bf16_ts(tmem_base, a_tmem + kk * 8, umma_desc_sw128(b_addr + kk * 32), idesc, acc);
+          }
+          if (PAIR)
+            umma_commit_pair(smem_u32(&empty[st]), 3);
+          else
+            umma_commit(smem_u32(&empty[st]));
         }
-        umma_commit(smem_u32(acc_full));  // also on the error path: tracks every MMA issued so far
+        // also on the error path: tracks every MMA issued so far
+        if (PAIR)
+          umma_commit_pair(smem_u32(acc_full), 3);
+        else
+          umma_commit(smem_u32(acc_full));
         ++seg;
-        u += sg.r1 - sg.r0;
       }
       // Do not leave while MMAs issued by this thread may still run: the last
       // commit tracks all of them.
@@ -341,7 +414,7 @@ __global__ void __launch_bounds__(PrefillCfg<BN>::kThreads, 1)
     // ------------------------------------------------------------ dequant + epilogue
     const int quad = warp & 3;           // TMEM lane quadrant this warp may access
     const int grp = (warp - 2) >> 2;     // 64-k step grp of every 256-k chunk; then columns grp/4 of the tile
-    const int row = quad * 32 + lane;    // W row within the tile == TMEM lane
+    const int row = quad * 32 + lane;    // W row within this CTA's 128 == TMEM lane
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
     const bool e0 = warp == 2 && lane == 0;
     constexpr int kCbPerGrp = BN / 128;  // 32-column blocks of the accumulator per group
@@ -351,11 +424,11 @@ __global__ void __launch_bounds__(PrefillCfg<BN>::kThreads, 1)
     const int raw_off = row * C::kRawRow + (36 * grp & ~15);
     bool live = true;
     uint32_t cr = 0, c = 0, seg = 0;
-    for (int64_t u = ub; u < ue;) {
-      const Seg sg = seg_at(u, ue, nr);
+    for (int i = 0; i < nseg; ++i) {
+      const Seg sg = seg_of(gi, i, wk);
       for (int r = sg.r0; r < sg.r1; ++r, ++cr, c += 4) {
         const uint32_t rslot = cr % C::RS;
-        const uint32_t as = (c + grp) % C::AS;
+        const uint32_t as = (c + grp) % C::S;
         if (live) live = mbar_wait_bounded(smem_u32(&raw_full[rslot]), (cr / C::RS) & 1, limit_ns, abort_flag, err);
         live = __all_sync(0xFFFFFFFFu, live);
         uint32_t v[12];
@@ -383,7 +456,7 @@ __global__ void __launch_bounds__(PrefillCfg<BN>::kThreads, 1)
           block_words(q0, w[0] & 0xFFFFu, o);
           block_words(q1, w[4] >> 16, o + 16);
         }
-        if (live) live = mbar_wait_bounded(smem_u32(&a_empty[as]), (((c + grp) / C::AS) & 1) ^ 1, limit_ns, abort_flag, err);
+        if (live) live = mbar_wait_bounded(smem_u32(&empty[as]), (((c + grp) / C::S) & 1) ^ 1, limit_ns, abort_flag, err);
         live = __all_sync(0xFFFFFFFFu, live);
         if (live) {
           tmem_st_32x32b_x32(lane_addr + BN + as * C::kACols, o);
@@ -391,14 +464,14 @@ __global__ void __launch_bounds__(PrefillCfg<BN>::kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (live && lane == 0) mbar_arrive(smem_u32(&a_full[as]));
+        if (live && lane == 0) arrive_leader(&full[as]);
       }
 
       // ---- epilogue of this segment: this group's quarter of the accumulator columns
       if (live) live = mbar_wait_bounded(smem_u32(acc_full), seg & 1, limit_ns, abort_flag, err);
       live = __all_sync(0xFFFFFFFFu, live);
       tc_fence_after();
-      const int m = static_cast<int>(sg.t / wk.ntn) * C::kBM + row;
+      const int m = static_cast<int>(sg.t / wk.ntn) * (C::kBM * C::kCtas) + static_cast<int>(rank) * C::kBM + row;
       const int n0 = static_cast<int>(sg.t % wk.ntn) * BN;
       if (sg.r0 == 0 && sg.r1 == nr) {
         if (live) {
@@ -419,17 +492,18 @@ __global__ void __launch_bounds__(PrefillCfg<BN>::kThreads, 1)
       } else {
         // Part of a split tile.  The CTA that sees every other split published
         // reduces: partial sums are added in the order of their k ranges, so
-        // the result does not depend on which CTA finishes last.
+        // the result does not depend on which CTA finishes last.  Each CTA of
+        // a pair does this for its own 128 rows.
         const int64_t t = sg.t;
-        const int ga = sk_owner(t * nr, grid, wk.units), gb = sk_owner(t * nr + nr - 1, grid, wk.units);
-        const int nsplit = gb - ga + 1;
+        const int ga = static_cast<int>(t) * wk.s, nsplit = wk.s;  // pieces: ranges ga .. ga + s - 1
+        unsigned long long* count = wk.count + t * C::kCtas + rank;
         volatile int* flag = reduce_flag + (seg & 1);
-        if (e0) *flag = live && ld_acquire_gpu(wk.count + t) == nsplit - 1;
+        if (e0) *flag = live && pieces_published(ld_acquire_gpu_u64(count), wk.epoch) == nsplit - 1;
         named_bar_sync(1, 32 * C::kDeqWarps);
         int last = *flag;
         if (!last) {
           if (live) {  // publish this split's partial tile
-            float* p = wk.ws + sk_slot(blockIdx.x, t, grid, wk) * C::kSlotFloats + row;
+            float* p = wk.ws + (static_cast<int64_t>(gi) * C::kCtas + rank) * C::kSlotFloats + row;
 #pragma unroll 1
             for (int cb = cb0; cb < cb1; ++cb) {
               uint32_t v32[32];
@@ -441,7 +515,11 @@ __global__ void __launch_bounds__(PrefillCfg<BN>::kThreads, 1)
           }
           __threadfence();
           named_bar_sync(1, 32 * C::kDeqWarps);
-          if (e0) *flag = live && atomicAdd(wk.count + t, 1) == nsplit - 1;
+          if (e0) {
+            const int before = live ? publish_piece(count, wk.epoch) : -1;
+            if (before < 0 && live) atomicOr(err, 1u);
+            *flag = before == nsplit - 1;
+          }
           named_bar_sync(1, 32 * C::kDeqWarps);
           last = *flag;
         }
@@ -451,13 +529,14 @@ __global__ void __launch_bounds__(PrefillCfg<BN>::kThreads, 1)
           for (int hb = 2 * cb0; hb < 2 * cb1; ++hb) {  // 16-column halves of this group's blocks
             float acc[16];
 #pragma unroll 1
-            for (int g = ga; g <= gb; ++g) {
+            for (int g = ga; g < ga + nsplit; ++g) {
               uint32_t q[16];  // split g's partial sums of these 16 columns
-              if (g == static_cast<int>(blockIdx.x)) {
+              if (g == gi) {
                 tmem_ld_32x32b_x16(lane_addr + hb * 16, q);
                 tmem_ld_wait();
               } else {
-                const float* p = wk.ws + sk_slot(g, t, grid, wk) * C::kSlotFloats + hb * 16 * C::kBM + row;
+                const float* p =
+                    wk.ws + (static_cast<int64_t>(g) * C::kCtas + rank) * C::kSlotFloats + hb * 16 * C::kBM + row;
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) q[jj] = __float_as_uint(__ldcg(p + jj * C::kBM));
               }
@@ -477,316 +556,115 @@ __global__ void __launch_bounds__(PrefillCfg<BN>::kThreads, 1)
               }
             }
           }
-          if (e0) wk.count[t] = 0;  // every split has arrived: leave the counter as found
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(acc_empty));
+      if (lane == 0) arrive_leader(acc_empty);
       ++seg;
-      u += sg.r1 - sg.r0;
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // neither CTA frees TMEM or leaves while the pair's MMAs or arrivals may touch it
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::kTmemCols);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    else
+      tmem_dealloc(tmem_base, C::kTmemCols);
   }
 }
 
-// ---------------------------------------------------------------------------
-// 2-SM variant: a cluster of two CTAs computes a 256 x 256 tile.  CTA r of the
-// pair dequantises W rows m0 + 128r .. +127 into its own TMEM and loads x rows
-// n0 + 128r .. +127 (half of the B tile) into its own shared memory; the
-// leader (r = 0) issues tcgen05.mma.cta_group::2 (M = 256, N = 256), which
-// reads A and B from both CTAs and accumulates each CTA's 128 rows in its own
-// TMEM.  Each SM thus loads half as much x per flop as the 1-CTA kernel, which
-// is bound by that traffic.  Hand-offs:
-//   x half of CTA r  -> TMA completing on the leader's b_full (cta_group::2);
-//   A stage of CTA r -> its dequant warps arrive on the leader's a_full;
-//   MMA completion   -> multicast commit to both CTAs' empty / acc barriers.
-struct Prefill2Cfg {
-  static constexpr int kBM = 128;       // rows per CTA (256 per pair)
-  static constexpr int kBN = 256;       // tokens per pair tile
-  static constexpr int kBK = 64;
-  static constexpr int kRawK = 256;
-  static constexpr int kRawRow = 144;
-  static constexpr int RS = 3, BS = 8;
-  static constexpr int kACols = kBK / 2;
-  static constexpr int AS = (512 - kBN) / kACols;  // 8
-  static constexpr int kTmemCols = 512;
-  static constexpr int kRawBytes = kBM * kRawRow;        // 18432
-  static constexpr int kBBytes = (kBN / 2) * 128;        // 16384: this CTA's half of the x tile
-  static constexpr int kOffB = 0;
-  static constexpr int kOffRaw = kOffB + BS * kBBytes;
-  static constexpr int kOffBar = kOffRaw + RS * kRawBytes;
-  static constexpr int kNBar = 2 * RS + 2 * AS + 2 * BS + 1;
-  static constexpr int kOffTmem = kOffBar + kNBar * 8;
-  static constexpr int kOffAbort = kOffTmem + 8;
-  static constexpr int kSmem = kOffAbort + 8 + 1024;
-  static constexpr int kDeqWarps = 8;
-  static constexpr int kThreads = 32 * (2 + kDeqWarps);
-};
+int64_t g_streamk = 1;  // 0: never split tiles; 1: split the last partial wave when it pays; n >= 2: split every tile in n
+int64_t g_slots = 0;    // 0: work ranges up to the SM count (pairs: half); n > 0: at most n ranges (test aid)
 
-__global__ void __launch_bounds__(Prefill2Cfg::kThreads, 1)
-    k_prefill2_q4_0(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int N, int M,
-                    int K, float* __restrict__ Y, uint64_t limit_ns, uint32_t* err) {
-  using C = Prefill2Cfg;
-  constexpr int BN = C::kBN;
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sbase = smem_u32(smem);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  uint64_t* raw_full = bars;
-  uint64_t* raw_empty = raw_full + C::RS;
-  uint64_t* a_full = raw_empty + C::RS;
-  uint64_t* a_empty = a_full + C::AS;
-  uint64_t* b_full = a_empty + C::AS;
-  uint64_t* b_empty = b_full + C::BS;
-  uint64_t* acc_full = b_empty + C::BS;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffTmem);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
+constexpr int64_t kFixupUnits = 6;
+// Launch tags for the arrival counters: unique per launch in this process; the
+// start is random so that scratch memory left by another process's launches
+// cannot carry a matching tag either.
+std::atomic<unsigned long long> g_epoch{(static_cast<unsigned long long>(std::random_device{}()) << 24) + 1};  // time of a split tile's publish / reduce, in 256-k chunks
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  const bool leader = rank == 0;
-  const int pair = blockIdx.x >> 1;
-  const int ntn = (N + BN - 1) / BN;
-  const int m0 = (pair / ntn) * 2 * C::kBM + static_cast<int>(rank) * C::kBM;
-  const int n0 = (pair % ntn) * BN;
-  const int nk = K / C::kBK;
-  const int nr = K / C::kRawK;
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < C::RS; ++i) {
-      mbar_init(smem_u32(&raw_full[i]), 1);
-      mbar_init(smem_u32(&raw_empty[i]), C::kDeqWarps);
-    }
-    for (int i = 0; i < C::AS; ++i) {
-      mbar_init(smem_u32(&a_full[i]), 8);  // 4 warps of the owning group in each CTA (leader's copy is used)
-      mbar_init(smem_u32(&a_empty[i]), 1);
-    }
-    for (int i = 0; i < C::BS; ++i) {
-      mbar_init(smem_u32(&b_full[i]), 1);  // leader's expect_tx; both halves complete bytes on it
-      mbar_init(smem_u32(&b_empty[i]), 1);
-    }
-    mbar_init(smem_u32(acc_full), 1);
-    *abort_flag = 0;
-    fence_mbar_init();
+// Schedule of T tiles of nr chunks on P ranges (PrefillWork): w = T / P whole
+// tiles per range, and the rem = T % P left over either as one more whole
+// tile for rem ranges or, when it is faster, split s = P / rem ways along k.
+void prefill_plan(int64_t T, int64_t nr, int64_t P, bool allow_split, PrefillWork* wk) {
+  if (g_slots > 0) P = g_slots;
+  P = std::max<int64_t>(P, 1);
+  wk->T = T;
+  wk->R = 0;
+  wk->s = 1;
+  wk->G = std::min(T, P);
+  if (!allow_split || g_streamk == 0 || nr < 2) return;
+  if (g_streamk >= 2) {  // every tile in pieces
+    wk->s = static_cast<int>(std::min(g_streamk, nr));
+    wk->R = static_cast<int>(T);
+    wk->G = T * wk->s;
+    return;
   }
-  if (warp == 1) {
-    tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
-    tmem_relinquish_pair();
-  }
-  tc_fence_before();
-  __syncthreads();
-  cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer (both CTAs)
-    if (lane == 0) {
-      tma_prefetch_desc(&tmW);
-      tma_prefetch_desc(&tmX);
-      uint32_t nraw = 0;
-      bool ok = true;
-      for (int ks = 0; ks < nk && ok; ++ks) {
-        if ((ks & 3) == 0) {
-          const int r = ks >> 2, slot = r % C::RS;
-          if (!mbar_wait_bounded(smem_u32(&raw_empty[slot]), ((r / C::RS) & 1) ^ 1, limit_ns, abort_flag, err)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(smem_u32(&raw_full[slot]), C::kRawBytes);
-          tma_load_2d(sbase + C::kOffRaw + slot * C::kRawBytes, &tmW, r * C::kRawRow, m0, smem_u32(&raw_full[slot]));
-          ++nraw;
-        }
-        const int slot = ks % C::BS;
-        if (!mbar_wait_bounded(smem_u32(&b_empty[slot]), ((ks / C::BS) & 1) ^ 1, limit_ns, abort_flag, err)) {
-          ok = false;
-          break;
-        }
-        const uint32_t leader_full = mapa_shared(smem_u32(&b_full[slot]), 0);
-        if (leader) mbar_arrive_expect_tx(smem_u32(&b_full[slot]), 2 * C::kBBytes);
-        tma_load_2d_pair(sbase + C::kOffB + slot * C::kBBytes, &tmX, ks * C::kBK, n0 + static_cast<int>(rank) * (BN / 2),
-                         leader_full);
-      }
-      if (!ok) drain_ring(raw_full, C::RS, nraw, limit_ns);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (leader CTA)
-    if (leader && lane == 0) {
-      constexpr uint32_t idesc = umma_idesc_bf16_f32(256, BN);
-      for (int ks = 0; ks < nk; ++ks) {
-        const int as = ks % C::AS, bs = ks % C::BS;
-        if (!mbar_wait_bounded(smem_u32(&a_full[as]), (ks / C::AS) & 1, limit_ns, abort_flag, err)) break;
-        if (!mbar_wait_bounded(smem_u32(&b_full[bs]), (ks / C::BS) & 1, limit_ns, abort_flag, err)) break;
-        tc_fence_after();
-        const uint32_t a_tmem = tmem_base + BN + as * C::kACols;
-        const uint32_t b_addr = sbase + C::kOffB + bs * C::kBBytes;
-#pragma unroll
-        for (int kk = 0; kk < C::kBK / 16; ++kk)
-          umma_bf16_ts_pair(tmem_base, a_tmem + kk * 8, umma_desc_sw128(b_addr + kk * 32), idesc, (ks | kk) != 0);
-        umma_commit_pair(smem_u32(&a_empty[as]), 3);
-        umma_commit_pair(smem_u32(&b_empty[bs]), 3);
-      }
-      umma_commit_pair(smem_u32(acc_full), 3);
-      const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(smem_u32(acc_full), 0) && globaltimer_ns() - t0 < limit_ns) {
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ dequant + epilogue (both CTAs)
-    const int quad = warp & 3;
-    const int grp = (warp - 2) >> 2;
-    const int row = quad * 32 + lane;
-    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-    bool live = true;
-    for (int r = 0; r < nr; ++r) {
-      const int rslot = r % C::RS;
-      if (live) live = mbar_wait_bounded(smem_u32(&raw_full[rslot]), (r / C::RS) & 1, limit_ns, abort_flag, err);
-      live = __all_sync(0xFFFFFFFFu, live);
-      uint32_t w[36];
-      if (live) {
-        const uint4* src = reinterpret_cast<const uint4*>(smem + C::kOffRaw + rslot * C::kRawBytes + row * C::kRawRow);
-#pragma unroll
-        for (int i = 0; i < 9; ++i) {
-          const uint4 v = src[i];
-          w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
-        }
-      }
-      __syncwarp();
-      if (live && lane == 0) mbar_arrive(smem_u32(&raw_empty[rslot]));
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if ((j & 1) != grp) continue;
-        const int ks = r * 4 + j, as = ks % C::AS;
-        if (live) live = mbar_wait_bounded(smem_u32(&a_empty[as]), ((ks / C::AS) & 1) ^ 1, limit_ns, abort_flag, err);
-        live = __all_sync(0xFFFFFFFFu, live);
-        if (live) {
-          const uint32_t W0 = w[9 * j], W1 = w[9 * j + 1], W2 = w[9 * j + 2], W3 = w[9 * j + 3], W4 = w[9 * j + 4];
-          const uint32_t q0[4] = {prmt(W0, W1, 0x5432u), prmt(W1, W2, 0x5432u), prmt(W2, W3, 0x5432u),
-                                  prmt(W3, W4, 0x5432u)};
-          const uint32_t q1[4] = {w[9 * j + 5], w[9 * j + 6], w[9 * j + 7], w[9 * j + 8]};
-          uint32_t o[32];
-          block_words(q0, W0 & 0xFFFFu, o);
-          block_words(q1, W4 >> 16, o + 16);
-          tmem_st_32x32b_x32(lane_addr + BN + as * C::kACols, o);
-          tmem_st_wait();
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (live && lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&a_full[as]), 0));
-      }
-    }
-    if (live) live = mbar_wait_bounded(smem_u32(acc_full), 0, limit_ns, abort_flag, err);
-    live = __all_sync(0xFFFFFFFFu, live);
-    tc_fence_after();
-    if (live) {
-      const int m = m0 + row;
-#pragma unroll 1
-      for (int cb = grp * (BN / 64); cb < (grp + 1) * (BN / 64); ++cb) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + cb * 32, v);
-        tmem_ld_wait();
-        if (m < M) {
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            const int n = n0 + cb * 32 + jj;
-            if (n < N) Y[static_cast<size_t>(n) * M + m] = __uint_as_float(v[jj]);
-          }
-        }
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  cluster_sync();  // neither CTA frees TMEM or leaves while the pair's MMAs or remote arrivals may touch it
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc_pair(tmem_base, C::kTmemCols);
-  }
+  const int64_t w = T / P, rem = T - w * P;
+  if (rem == 0) return;
+  const int64_t s = std::min(P / rem, nr / 2);
+  if (s < 2 || w * nr + (nr + s - 1) / s + kFixupUnits >= (w + 1) * nr) return;
+  wk->R = static_cast<int>(rem);
+  wk->s = static_cast<int>(s);
+  wk->G = std::max(std::min(T, P), rem * s);
 }
 
-cudaError_t launch_prefill2(const CUtensorMap* tmW, const CUtensorMap* tmX, int N, int M, int K, float* Y,
-                            uint64_t limit_ns, cudaStream_t s) {
-  using C = Prefill2Cfg;
+template <int BN, bool PAIR>
+cudaError_t launch_prefill_cfg(const CUtensorMap* tmW, const CUtensorMap* tmX, int N, int M, int K, float* Y,
+                               uint64_t limit_ns, bool allow_scratch, cudaStream_t s) {
+  using C = PrefillCfg<BN, PAIR>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_prefill2_q4_0, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  const int pairs = ((M + 2 * C::kBM - 1) / (2 * C::kBM)) * ((N + C::kBN - 1) / C::kBN);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * pairs);
-  cfg.blockDim = dim3(C::kThreads);
-  cfg.dynamicSmemBytes = C::kSmem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_prefill2_q4_0, *tmW, *tmX, N, M, K, Y, limit_ns, device_error_word());
-}
-
-int64_t g_streamk = 1;  // 0: one CTA per tile; 1: stream-K when it balances the SMs better; >= 2: that many CTAs
-
-// CTAs for T tiles of nr chunks each: T (one tile per CTA) unless spreading
-// the T*nr units evenly over the SMs (at least 4 units per CTA, plus about
-// 2 units' worth of time for the split tiles' fix-up) is 10% faster.
-int64_t prefill_grid(int64_t T, int64_t nr, bool allow_scratch) {
-  const int64_t U = T * nr;
-  if (!allow_scratch || g_streamk == 0) return T;
-  if (g_streamk >= 2) return std::min(g_streamk, U);
-  const int64_t P = device_info().sm_count > 0 ? device_info().sm_count : 1;
-  const int64_t g = std::min(P, std::max<int64_t>(1, U / 4));
-  const double t_dp = static_cast<double>((T + P - 1) / P) * static_cast<double>(nr);
-  const double t_sk = static_cast<double>((U + g - 1) / g) + 2.0;
-  return t_sk < 0.9 * t_dp ? g : T;
-}
-
-template <int BN>
-cudaError_t launch_prefill_bn(const CUtensorMap* tmW, const CUtensorMap* tmX, int N, int M, int K, float* Y,
-                              uint64_t limit_ns, bool allow_scratch, cudaStream_t s) {
-  using C = PrefillCfg<BN>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_prefill_q4_0<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    cudaError_t e =
+        cudaFuncSetAttribute(k_prefill_q4_0<BN, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const int64_t ntn = (N + BN - 1) / BN;
-  const int64_t T = ((M + C::kBM - 1) / C::kBM) * ntn;
+  const int64_t rows = C::kBM * C::kCtas;
+  const int64_t T = ((M + rows - 1) / rows) * ntn;
   const int64_t nr = K / C::kRawK;
-  int64_t grid = prefill_grid(T, nr, allow_scratch);
-  PrefillWork wk{T * nr, static_cast<int>(nr), static_cast<int>(ntn), nullptr, nullptr};
+  PrefillWork wk{};
+  wk.nr = static_cast<int>(nr);
+  wk.ntn = static_cast<int>(ntn);
+  prefill_plan(T, nr, device_info().sm_count / C::kCtas, allow_scratch, &wk);
   void* scratch = nullptr;
-  if (T % grid != 0) {  // some tile is split across CTAs: partial-tile slots and arrival counters
-    const size_t ws_bytes = static_cast<size_t>(2 * grid) * C::kSlotFloats * sizeof(float);
-    const size_t bytes = ws_bytes + static_cast<size_t>(T) * sizeof(int);
-    if (scratch_alloc(&scratch, bytes, s) == cudaSuccess &&
-        cudaMemsetAsync(static_cast<uint8_t*>(scratch) + ws_bytes, 0, static_cast<size_t>(T) * sizeof(int), s) ==
-            cudaSuccess) {
+  if (wk.R > 0) {  // split tiles: partial-tile slots and arrival counters
+    const size_t ws_bytes =
+        static_cast<size_t>(wk.R) * wk.s * C::kCtas * static_cast<size_t>(C::kSlotFloats) * sizeof(float);
+    const size_t cnt_bytes = static_cast<size_t>(wk.R) * C::kCtas * sizeof(unsigned long long);
+    if (scratch_alloc(&scratch, ws_bytes + cnt_bytes, s) == cudaSuccess) {
       wk.ws = static_cast<float*>(scratch);
-      wk.count = reinterpret_cast<int*>(static_cast<uint8_t*>(scratch) + ws_bytes);
-    } else {  // no scratch: one tile per CTA
+      wk.count = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(scratch) + ws_bytes);
+      wk.epoch = g_epoch.fetch_add(1) & ((1ull << 56) - 1);
+    } else {  // no scratch: whole tiles only
       cudaGetLastError();
       if (scratch) scratch_free(scratch, s);
       scratch = nullptr;
-      grid = T;
+      wk.R = 0;
+      wk.s = 1;
+      wk.G = std::min<int64_t>(T, std::max<int64_t>(1, g_slots > 0 ? g_slots : device_info().sm_count / C::kCtas));
     }
   }
-  k_prefill_q4_0<BN><<<static_cast<unsigned>(grid), C::kThreads, C::kSmem, s>>>(*tmW, *tmX, N, M, Y, wk, limit_ns,
-                                                                                device_error_word());
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(wk.G * C::kCtas));
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (PAIR) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  cudaError_t e =
+      cudaLaunchKernelEx(&cfg, k_prefill_q4_0<BN, PAIR>, *tmW, *tmX, N, M, Y, wk, limit_ns, device_error_word());
   if (scratch) {
     cudaError_t f = scratch_free(scratch, s);
     if (e == cudaSuccess) e = f;
@@ -821,14 +699,16 @@ void prefill_boxes(int64_t N, uint32_t* w_box_x_bytes, uint32_t* w_box_rows, uin
 void set_prefill_pair_mode(int on) { g_pair_mode = on ? 1 : 0; }
 void set_prefill_streamk(int64_t v) { g_streamk = v; }
 int64_t get_prefill_streamk() { return g_streamk; }
+void set_prefill_slots(int64_t v) { g_slots = v; }
+int64_t get_prefill_slots() { return g_slots; }
 int get_prefill_pair_mode() { return g_pair_mode; }
 
 cudaError_t launch_prefill(const CUtensorMap* tmW, const CUtensorMap* tmX, int64_t N, int64_t M, int64_t K,
                            float* Y, uint64_t wait_limit_ns, bool allow_scratch, cudaStream_t s) {
   const int n = static_cast<int>(N), m = static_cast<int>(M), k = static_cast<int>(K);
-  if (use_pair(N)) return launch_prefill2(tmW, tmX, n, m, k, Y, wait_limit_ns, s);
-  if (prefill_bn(N) == 128) return launch_prefill_bn<128>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, s);
-  return launch_prefill_bn<256>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, s);
+  if (use_pair(N)) return launch_prefill_cfg<256, true>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, s);
+  if (prefill_bn(N) == 128) return launch_prefill_cfg<128, false>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, s);
+  return launch_prefill_cfg<256, false>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, s);
 }
 
 }  // namespace gq

@@ -271,22 +271,51 @@ def _with_option(code, val, fn):
         gq.gq_set_option(code, old)
 
 
-# (M, K, N, CTAs): T = ceil(M/128) * ceil(N/BN) tiles of K/256 units each.
-#   384x1024, N=300: T=6, 24 units -> 5 CTAs (splits of 2), 13 (tiles over 3-4 CTAs),
-#   24 (one unit per CTA), 40 (clamped to 24); N=100 takes the 128-wide tile;
-#   640x2048, N=513: T=15, 120 units over 7 or 152 CTAs; 130 rows: ragged last row block.
-@pytest.mark.parametrize("M,K,N,G", [(384, 1024, 300, 5), (384, 1024, 300, 13), (384, 1024, 300, 24),
-                                     (384, 1024, 300, 40), (384, 1024, 100, 5), (640, 2048, 513, 7),
-                                     (640, 2048, 513, 152), (130, 1024, 257, 3)])
-def test_prefill_stream_k_splits(M, K, N, G):
-    """Tiles whose k range is split across CTAs: partial sums through the
-    workspace, summed by whichever CTA arrives last, against the oracle."""
-    code = gq.GQ_OPT_PREFILL_STREAMK
-    _with_option(code, G, lambda: check_mm(M, K, N, 5200 + M + N + G, f"stream-K G={G}"))
+# Every tile split along k into n pieces (partial sums through the workspace,
+# summed in k order by whichever piece arrives last).  T = ceil(M/128) *
+# ceil(N/BN) tiles of K/256 chunks; n is capped at the chunk count.
+#   384x1024 (4 chunks), N=300: 2, 3, 4 and 7 (-> 4) pieces; N=100: the 128-wide tile;
+#   640x2048 (8 chunks), N=513: 3 and 8 pieces; 130 rows: ragged last row block.
+@pytest.mark.parametrize("M,K,N,n", [(384, 1024, 300, 2), (384, 1024, 300, 3), (384, 1024, 300, 4),
+                                     (384, 1024, 300, 7), (384, 1024, 100, 2), (640, 2048, 513, 3),
+                                     (640, 2048, 513, 8), (130, 1024, 257, 3)])
+def test_prefill_split_every_tile(M, K, N, n):
+    _with_option(gq.GQ_OPT_PREFILL_STREAMK, n, lambda: check_mm(M, K, N, 5200 + M + N + n, f"k-split n={n}"))
 
 
-def test_prefill_stream_k_is_deterministic():
-    """The split tiles are summed in k order, so repeated calls agree bit for bit."""
+# The default planner on a GPU of `slots` SMs: 640x8192, N=513 is 15 tiles of
+# 32 chunks.  4 slots: 3-4 whole tiles per CTA; 6: 2 whole tiles each and the
+# last 3 tiles in 2 pieces; 7: 2 whole tiles each and the last tile in 7
+# pieces; 40: no whole tiles, every tile in 2 pieces; 16: one tile per CTA.
+@pytest.mark.parametrize("slots", [4, 6, 7, 16, 40])
+def test_prefill_schedule(slots):
+    _with_option(gq.GQ_OPT_PREFILL_SLOTS, slots,
+                 lambda: check_mm(640, 8192, 513, 5300 + slots, f"schedule on {slots} SMs"))
+
+
+def _with_option(code, val, fn):
+    old = gq.gq_get_option(code)
+    gq.gq_set_option(code, val)
+    try:
+        return fn()
+    finally:
+        gq.gq_set_option(code, old)
+
+
+# CTA pairs (256-row tiles): 640x2048, N=513 is 3 x 3 pair tiles of 8 chunks;
+# 130 rows: the second CTA of each pair has no rows.
+@pytest.mark.parametrize("M,K,N,n,slots", [(640, 2048, 513, 3, 0), (640, 2048, 513, 8, 0), (384, 1024, 300, 2, 0),
+                                           (130, 1024, 300, 3, 0), (640, 8192, 513, 1, 2), (640, 8192, 513, 1, 4),
+                                           (640, 8192, 513, 0, 4)])
+def test_prefill_pair_split_and_schedule(M, K, N, n, slots):
+    def run():
+        return _with_option(gq.GQ_OPT_PREFILL_STREAMK, n, lambda: _with_option(
+            gq.GQ_OPT_PREFILL_SLOTS, slots, lambda: check_mm(M, K, N, 5500 + M + N + n + slots, "pair")))
+    _with_option(gq.GQ_OPT_PREFILL_PAIR, 1, run)
+
+
+def test_prefill_split_is_deterministic():
+    """Split tiles are summed in k order, so repeated calls agree bit for bit."""
     M, K, N = 640, 2048, 513
     W = dev(synth.q4_0_weights(M, K, seed=5300))
     X = dev(synth.activations(N, K, seed=5301))
@@ -295,26 +324,26 @@ def test_prefill_stream_k_is_deterministic():
         ys = [gq.mul_mat_q4_0(W, X) for _ in range(4)]
         torch.cuda.synchronize()
         return ys
-    ys = _with_option(gq.GQ_OPT_PREFILL_STREAMK, 11, run)
+    ys = _with_option(gq.GQ_OPT_PREFILL_STREAMK, 3, run)
     for y in ys[1:]:
         assert torch.equal(ys[0], y)
 
 
-def test_prefill_stream_k_off_matches_oracle():
-    _with_option(gq.GQ_OPT_PREFILL_STREAMK, 0, lambda: check_mm(640, 2048, 513, 5400, "one CTA per tile"))
+def test_prefill_whole_tiles_only_matches_oracle():
+    _with_option(gq.GQ_OPT_PREFILL_STREAMK, 0, lambda: check_mm(640, 2048, 513, 5400, "whole tiles"))
 
 
-@pytest.mark.parametrize("M,K", [(4096, 4096), (4096, 11008)])
-def test_prefill_full_size_stream_k_sampled_rows(M, K):
-    """Full-size shapes whose 64 tiles leave most SMs idle: the default split
-    spreads their k ranges over all SMs.  Sampled rows against the oracle."""
+@pytest.mark.parametrize("M,K", [(4096, 4096), (4096, 11008), (11008, 4096)])
+def test_prefill_full_size_split_sampled_rows(M, K):
+    """Full-size shapes whose last wave of tiles is split along k by default.
+    Sampled rows against the oracle."""
     N = 512
     W = synth.q4_0_weights(M, K, seed=synth.seed_for(5, M + K))
     X = synth.activations(N, K, seed=synth.seed_for(5, M + K + 1))
     y = run_mm(W, X, M, K)
     rows = sampled_rows(M, 128, 43)
     y_ref, s_ref = oracle_mul_mat(W.reshape(M, -1)[rows], len(rows), K, X)
-    assert_mul_mat_close(y[:, rows], y_ref, s_ref, f"stream-K {M}x{K}")
+    assert_mul_mat_close(y[:, rows], y_ref, s_ref, f"split {M}x{K}")
 
 
 def test_f32_to_bf16_matches_torch_rounding():
