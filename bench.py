@@ -330,12 +330,15 @@ def run_gpu(args, rank, world, dist):
                     "includes": "fp32->bf16 activation conversion + tensor-core MUL_MAT"},
         "roofline": {"kernel": "k_prefill_q4_0 (tcgen05 prefill)", "bound": "tensor",
                      "achieved": round(k3_tflops, 2), "peak": sust, "unit": "TFLOP/s",
-                     "frac": round(k3_tflops / sust, 4), "traffic": None,
+                     "frac": round(k3_tflops / sust, 4), "traffic": sweep_traffic("prefill", shapes),
+                     "traffic_unit": "bytes per launch (ncu, mean over the sweep's shapes)",
                      "peak_kind": f"bf16 sustained ({peaks['source']})", "avg_launch_us": round(k3_avg_us, 3),
                      "per_launch": "2*M*K*512 flops of the launch's matrix"},
         "roofline_decode": {"kernel": "k_decode_q4_0 (decode)", "bound": "hbm", "achieved": round(dec_gbs_alg, 1),
                             "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                            "frac": round(dec_gbs_alg / peaks["hbm_gbs"], 4), "traffic": None,
+                            "frac": round(dec_gbs_alg / peaks["hbm_gbs"], 4),
+                            "traffic": sweep_traffic("decode", shapes),
+                            "traffic_unit": "bytes per launch (ncu, mean over the sweep's shapes)",
                             "peak_kind": f"HBM copy ({peaks['source']})",
                             "per_launch": "M*K*18/32 + 4*N*K + 4*N*M bytes; graph-replay time incl. launch gaps"},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
@@ -392,6 +395,22 @@ def run_e2e(gq, torch, dev, s, W, shapes, acts1, order, L, args):
     return {"ms": e0.elapsed_time(e1) / args.steps, "h2d": h2d, "d2h": d2h}
 
 
+# DRAM bytes (read + write) per launch, from one ncu capture per shape of the
+# sweep (profiles/dram_traffic_sweep_shapes.md); refresh when a kernel changes.
+MEASURED_TRAFFIC = {
+    "decode": {(4096, 4096): 9487360, (11008, 4096): 25412352, (4096, 11008): 25440512},
+    "prefill": {(4096, 4096): 13680384, (11008, 4096): 29956864, (4096, 11008): 36795136},
+}
+
+
+def sweep_traffic(kind, shapes):
+    """Mean measured DRAM bytes per launch over the sweep's launches, or None."""
+    table = MEASURED_TRAFFIC[kind]
+    if not all(sh in table for sh in shapes):
+        return None
+    return round(sum(table[sh] for sh in shapes) / len(shapes))
+
+
 PROFILE_CASES = {
     # name: (M, K, N, entry point)
     "decode": (11008, 4096, 1, "f32"),
@@ -400,6 +419,8 @@ PROFILE_CASES = {
     "decode_big": (32000, 4096, 1, "f32"),
     "prefill": (14336, 4096, 512, "bf16"),
     "prefill_small": (4096, 4096, 512, "bf16"),
+    "prefill_gate": (11008, 4096, 512, "bf16"),
+    "prefill_down": (4096, 11008, 512, "bf16"),
 }
 
 
