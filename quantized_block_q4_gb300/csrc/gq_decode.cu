@@ -231,40 +231,32 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
 
     // Stage this chunk of x: per (block, token) four fp16 lane-slot fragments
     // (k permuted like the codes) and the negated bias of the biased codes.
-    named_bar_sync(1, 32 * KW);  // previous chunk's fragments are no longer read
-    // Two (block, token) entries per thread per round, loads issued first.
-    for (int e0 = threadIdx.x; e0 < nbl * N; e0 += 64 * KW) {
-      float xv[2][32];
+    // Each warp stages only the blocks of its own k boxes (box kw of every
+    // stage), which only it reads: no CTA-wide barrier, so a warp starts on
+    // its W as soon as its own x has arrived.
+    __syncwarp();  // this warp's previous chunk of fragments is no longer read
+    {
+      constexpr int kBoxBlocks = kSubK / kQK;  // 8
+      const int nent = nst * kBoxBlocks * N;   // (stage, block of the box, token) entries of this warp
+      for (int e = lane; e < nent; e += 32) {
+        const int st = e / (kBoxBlocks * N), rem = e % (kBoxBlocks * N);
+        const int bl = st * (Cfg::kStageK / kQK) + kw * kBoxBlocks + rem / N;  // block within the chunk
+        const int n = rem % N;
+        if (kc0 + bl * kQK >= kend) continue;
+        float xv[32];
+        const float4* xr =
+            reinterpret_cast<const float4*>(X + static_cast<size_t>(n) * K + static_cast<size_t>(kc0 + bl * kQK));
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int e = e0 + h * 32 * KW;
-        const int bg = kc0 / kQK + e / N;
-        if (e < nbl * N && bg * kQK < K) {
-          const float4* xr = reinterpret_cast<const float4*>(X + static_cast<size_t>(e % N) * K +
-                                                             static_cast<size_t>(bg) * kQK);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 v = __ldg(xr + i);
-            xv[h][4 * i] = v.x; xv[h][4 * i + 1] = v.y; xv[h][4 * i + 2] = v.z; xv[h][4 * i + 3] = v.w;
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) xv[h][i] = 0.f;
+        for (int i = 0; i < 8; ++i) {
+          const float4 v = __ldg(xr + i);
+          xv[4 * i] = v.x; xv[4 * i + 1] = v.y; xv[4 * i + 2] = v.z; xv[4 * i + 3] = v.w;
         }
-      }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int e = e0 + h * 32 * KW;
-        if (e < nbl * N) {
-          const int n = e % N, bl = e / N;
-          uint4* dst = xs + (bl * N + n) * 4;
-          cs[bl * csn + n] = ((kc0 / kQK + bl) & 1) ? stage_block<1>(xv[h], dst) : stage_block<0>(xv[h], dst);
-        }
+        uint4* dst = xs + (bl * N + n) * 4;
+        cs[bl * csn + n] = ((kc0 / kQK + bl) & 1) ? stage_block<1>(xv, dst) : stage_block<0>(xv, dst);
+        if ((N & 1) && n == N - 1) cs[bl * csn + N] = 0.f;  // the padding column read by the last lane pair
       }
     }
-    if (N & 1)  // the padding column read by the lane pair of the last token
-      for (int bl = threadIdx.x; bl < nbl; bl += 32 * KW) cs[bl * csn + N] = 0.f;
-    named_bar_sync(1, 32 * KW);
+    __syncwarp();
 
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tile_iter) {
       float acc[MT][NT][4];
