@@ -293,15 +293,6 @@ def test_prefill_schedule(slots):
                  lambda: check_mm(640, 8192, 513, 5300 + slots, f"schedule on {slots} SMs"))
 
 
-def _with_option(code, val, fn):
-    old = gq.gq_get_option(code)
-    gq.gq_set_option(code, val)
-    try:
-        return fn()
-    finally:
-        gq.gq_set_option(code, old)
-
-
 # CTA pairs (256-row tiles): 640x2048, N=513 is 3 x 3 pair tiles of 8 chunks;
 # 130 rows: the second CTA of each pair has no rows.
 @pytest.mark.parametrize("M,K,N,n,slots", [(640, 2048, 513, 3, 0), (640, 2048, 513, 8, 0), (384, 1024, 300, 2, 0),
