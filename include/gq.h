@@ -130,8 +130,16 @@ typedef enum {
                                 over the idle SMs and the pieces summed in k order (the result does
                                 not depend on timing); 0 = whole tiles only; n >= 2 = every tile
                                 in n pieces (test aid) */
-  GQ_OPT_PREFILL_SLOTS = 9    /* test aid: run the tensor-core kernel as if the GPU had this many SMs
+  GQ_OPT_PREFILL_SLOTS = 9,   /* test aid: run the tensor-core kernel as if the GPU had this many SMs
                                 (CTA pairs: pairs); 0 (default) = the real count */
+  GQ_OPT_DECODE_EARLY_STAGES = 10, /* with GQ_OPT_WEIGHTS_STATIC: how many ring stages of W the decode
+                                kernel streams before the previous kernel finishes (1..64, capped by the
+                                ring, default 2); later stages wait until x is staged */
+  GQ_OPT_X_STATIC = 11        /* 1: promise that the kernel launched right before a decode mul_mat
+                                (N < 64) on the same stream does not write its X (e.g. several
+                                projections of one activation), so the kernel may read X and compute
+                                before that kernel finishes; Y is still written only after it.
+                                Default 0: X is read after the previous kernel completes */
 } gq_option;
 gq_status gq_set_option(gq_option opt, int64_t value);
 int64_t gq_get_option(gq_option opt);

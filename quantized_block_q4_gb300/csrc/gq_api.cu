@@ -372,6 +372,13 @@ gq_status gq_set_option(gq_option opt, int64_t value) {
       if (value < 0 || value > 65536) return fail(GQ_ERR_SHAPE, "slot count must be 0..65536");
       set_prefill_slots(value);
       return GQ_OK;
+    case GQ_OPT_DECODE_EARLY_STAGES:
+      if (value < 1 || value > 64) return fail(GQ_ERR_SHAPE, "early stage count must be 1..64");
+      set_decode_early_stages(static_cast<int>(value));
+      return GQ_OK;
+    case GQ_OPT_X_STATIC:
+      set_decode_x_static(static_cast<int>(value));
+      return GQ_OK;
   }
   return fail(GQ_ERR_SHAPE, "unknown option %d", static_cast<int>(opt));
 }
@@ -388,6 +395,8 @@ int64_t gq_get_option(gq_option opt) {
     case GQ_OPT_PREFILL_PAIR: return get_prefill_pair_mode();
     case GQ_OPT_PREFILL_STREAMK: return get_prefill_streamk();
     case GQ_OPT_PREFILL_SLOTS: return get_prefill_slots();
+    case GQ_OPT_DECODE_EARLY_STAGES: return get_decode_early_stages();
+    case GQ_OPT_X_STATIC: return get_decode_x_static();
   }
   return -1;
 }

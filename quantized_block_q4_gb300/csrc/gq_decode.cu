@@ -64,7 +64,7 @@ struct DecodeCfg {
   }
   static size_t smem_bytes(int N, int KX) {
     return kRingBytes + xs_bytes(N, KX) + cs_bytes(N, KX) + (kSlots * slot_floats(N) + kSlots) * sizeof(float) +
-           2 * STAGES * 8 + 16 + 128;
+           (2 * STAGES + 1) * 8 + 16 + 128;
   }
 };
 
@@ -136,7 +136,8 @@ constexpr int decode_min_blocks() {
 template <int NT, int MT, int KW, int STAGES, bool ONE>
 __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, STAGES>()))
     k_decode_q4_0(const __grid_constant__ CUtensorMap tmW, const float* __restrict__ X, int N, int M, int K,
-                  int KX, float* __restrict__ Y, uint64_t limit_ns, uint32_t* err, int early_w) {
+                  int KX, float* __restrict__ Y, uint64_t limit_ns, uint32_t* err, int early_stages,
+                  int x_static) {
   using Cfg = DecodeCfg<NT, MT, KW, STAGES>;
   constexpr int kBM = Cfg::kBM;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -150,7 +151,8 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
   int* slot_count = reinterpret_cast<int*>(acc_slots + Cfg::kSlots * slot_floats);
   uint64_t* bars = reinterpret_cast<uint64_t*>(
       (reinterpret_cast<uintptr_t>(slot_count + Cfg::kSlots) + 7) & ~uintptr_t(7));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES);
+  uint64_t* x_ready = bars + 2 * STAGES;  // every consumer warp has staged the first chunk of x
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntiles = (M + kBM - 1) / kBM;
@@ -163,6 +165,7 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
       mbar_init(smem_u32(&bars[s]), 1);            // full: producer's expect_tx arrive + tx bytes
       mbar_init(smem_u32(&bars[STAGES + s]), KW);  // empty: one arrive per consumer warp
     }
+    mbar_init(smem_u32(x_ready), KW);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -173,7 +176,11 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tmW);
-      if (!early_w) pdl_wait();
+      // With early_stages > 0 the first stages of W stream before the previous
+      // kernel finishes; the rest waits until x is staged, so that the x loads
+      // right after the dependency do not queue behind a ring full of W.
+      if (!early_stages) pdl_wait();
+      bool x_waited = early_stages == 0;
       uint32_t q = 0;
       bool ok = true;
       for (int c = 0; c < nchunks && ok; ++c) {
@@ -184,6 +191,13 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
           for (int st = 0; st < nst; ++st, ++q) {
             const int slot = q % STAGES;
             const uint32_t ph = (q / STAGES) & 1;
+            if (!x_waited && q >= static_cast<uint32_t>(early_stages)) {
+              x_waited = true;
+              if (!mbar_wait_bounded(smem_u32(x_ready), 0, limit_ns, abort_flag, err)) {
+                ok = false;
+                break;
+              }
+            }
             if (!mbar_wait_bounded(smem_u32(&bars[STAGES + slot]), ph ^ 1, limit_ns, abort_flag, err)) {
               ok = false;
               break;
@@ -221,7 +235,9 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
   uint32_t q = 0;
   int tile_iter = 0;
   bool live = true;  // false once a bounded wait gave up; the loops still run to keep barriers matched
-  pdl_wait();        // X may come from the previous kernel; Y may still be read by it
+  // X may come from the previous kernel (unless the caller promised it does
+  // not: x_static); Y may still be read by it, so Y is written after the wait.
+  if (!x_static) pdl_wait();
 
   for (int c = 0; c < nchunks; ++c) {
     const int kc0 = c * KX;
@@ -257,6 +273,7 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
       }
     }
     __syncwarp();
+    if (c == 0 && lane == 0) mbar_arrive(smem_u32(x_ready));
 
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tile_iter) {
       float acc[MT][NT][4];
@@ -367,6 +384,7 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
       }
       prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
       if (prev == KW - 1) {
+        if (x_static) pdl_wait();
         __threadfence_block();
         for (int idx = lane; idx < kBM * N; idx += 32) {
           const int r = idx / N, n = idx % N;
@@ -389,9 +407,15 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
   }
 }
 
+int g_early_stages = 2;  // W stages a launch may stream before the dependency (capped by the ring)
+int decode_early_stages() { return g_early_stages; }
+int g_x_static = 0;      // the caller promises X is not written by the kernel right before
+int decode_x_static() { return g_x_static; }
+
 template <int NT, int MT, int KW, int STAGES, bool ONE = false>
 cudaError_t launch_cfg(const CUtensorMap* tmW, const float* X, int N, int M, int K, float* Y, uint64_t limit_ns,
                        int xs_budget, int early_w, int pdl, cudaStream_t s) {
+  const int early_stages = early_w ? std::max(1, std::min(STAGES, decode_early_stages())) : 0;
   using Cfg = DecodeCfg<NT, MT, KW, STAGES>;
   // x chunk: a multiple of the stage width, as long as the budget allows
   int KX = (xs_budget / (2 * N)) / Cfg::kStageK * Cfg::kStageK;
@@ -428,7 +452,8 @@ cudaError_t launch_cfg(const CUtensorMap* tmW, const float* X, int N, int M, int
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, *tmW, X, N, M, K, KX, Y, limit_ns, device_error_word(), early_w);
+  return cudaLaunchKernelEx(&cfg, kern, *tmW, X, N, M, K, KX, Y, limit_ns, device_error_word(), early_stages,
+                            decode_x_static());
 }
 
 // -------------------------------------------------------------------------
@@ -478,6 +503,11 @@ void decode_w_box(int64_t N, int variant, uint32_t* box_x_bytes, uint32_t* box_r
   *box_x_bytes = kSubBytesRow;
   *box_rows = static_cast<uint32_t>(decode_rows_per_tile(N, variant));
 }
+
+void set_decode_early_stages(int n) { g_early_stages = n; }
+void set_decode_x_static(int on) { g_x_static = on ? 1 : 0; }
+int get_decode_x_static() { return g_x_static; }
+int get_decode_early_stages() { return g_early_stages; }
 
 cudaError_t launch_decode(const CUtensorMap* tmW, const float* X, int64_t N, int64_t M, int64_t K, float* Y,
                           uint64_t wait_limit_ns, int early_w, int variant, int pdl, cudaStream_t s) {

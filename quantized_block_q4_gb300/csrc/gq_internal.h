@@ -43,6 +43,11 @@ void decode_w_box(int64_t N, int variant, uint32_t* box_x_bytes, uint32_t* box_r
 cudaError_t launch_generic(const uint8_t* W, int64_t M, int64_t K, const float* X, int64_t N, float* Y,
                            cudaStream_t s);
 
+void set_decode_early_stages(int n);  // W stages streamed before the dependency (with WEIGHTS_STATIC)
+int get_decode_early_stages();
+void set_decode_x_static(int on);      // X is not written by the kernel right before (decode reads it early)
+int get_decode_x_static();
+
 // ---- K0: fp32 -> bf16 (round to nearest even) (gq_prefill.cu)
 cudaError_t launch_f32_to_bf16(const float* x, uint16_t* y, int64_t n, cudaStream_t s);
 

@@ -439,3 +439,32 @@ def test_decode_variants(variant, M, K, N):
         check_mm(M, K, N, 7400 + M + N, f"variant {variant}")
     finally:
         gq.gq_set_option(gq.GQ_OPT_DECODE_VARIANT, old)
+
+
+@pytest.mark.parametrize("M,K", [(4096, 4096), (11008, 4096), (4096, 11008)])
+def test_x_static_back_to_back_independent_calls(M, K):
+    """X_STATIC + WEIGHTS_STATIC: calls whose X no preceding kernel writes may
+    read X and compute before that kernel finishes; Y is written after it.
+    Several calls in a row, each checked against the oracle."""
+    Ws = [synth.q4_0_weights(M, K, seed=7800 + i) for i in range(3)]
+    Xs = [synth.activations(1, K, seed=7810 + i) for i in range(3)]
+    Wd, Xd = [dev(w) for w in Ws], [dev(x) for x in Xs]
+    Ys = [torch.empty(1, M, device="cuda") for _ in range(3)]
+
+    def run():
+        for _ in range(3):  # repeated: the later rounds overwrite Y while earlier calls may still run
+            for w, x, y in zip(Wd, Xd, Ys):
+                gq.gq_mul_mat_q4_0(w, M, K, x, 1, y)
+        torch.cuda.synchronize()
+        gq.gq_sync_status()
+    _with_option(gq.GQ_OPT_X_STATIC, 1, lambda: _with_option(gq.GQ_OPT_WEIGHTS_STATIC, 1, run))
+    for i in range(3):
+        y_ref, s_ref = oracle_mul_mat(Ws[i], M, K, Xs[i])
+        assert_mul_mat_close(Ys[i].cpu().numpy(), y_ref, s_ref, f"x-static call {i}")
+
+
+@pytest.mark.parametrize("stages", [1, 2, 3, 8])
+def test_decode_early_stages_option(stages):
+    def run():
+        return _with_option(gq.GQ_OPT_WEIGHTS_STATIC, 1, lambda: check_mm(4096, 4096, 1, 7900 + stages, "early"))
+    _with_option(gq.GQ_OPT_DECODE_EARLY_STAGES, stages, run)
