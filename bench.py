@@ -194,6 +194,9 @@ def run_gpu(args, rank, world, dist):
     # weights are uploaded once and never written by the kernels that run
     # before each MUL_MAT, so the decode kernel may stream W early
     gq.gq_set_option(gq.GQ_OPT_WEIGHTS_STATIC, 1)
+    # each MUL_MAT's activations are prepared before the sweep, never written by
+    # the MUL_MAT launched before it, so decode launches may read X early
+    gq.gq_set_option(gq.GQ_OPT_X_STATIC, 1)
     dev = torch.device("cuda", local)
     peaks = load_peaks()
     order, ks = layer_inputs()
@@ -322,7 +325,7 @@ def run_gpu(args, rank, world, dist):
         "config": {"workload": WORKLOAD, "layers": L, "matrices": len(shapes), "decode_n": DECODE_N,
                    "prefill_n": PREFILL_N, "weight_bytes": wbytes,
                    "l2": "inputs larger than L2 (3.64 GB of weights streamed per pass)",
-                   "weights_static": True,
+                   "weights_static": True, "x_static": True,
                    "parallelism": f"replicas x{world}"},
         "decode": {"value": round(value, 2), "unit": "GB/s", "ms": round(dec_ms / K_, 4),
                    "avg_launch_us": round(dec_avg_us, 3)},
@@ -430,6 +433,7 @@ def run_profile_case(name, pair=False):
     import quantized_block_q4_gb300 as gq
     M, K, N, mode = PROFILE_CASES[name]
     gq.gq_set_option(gq.GQ_OPT_WEIGHTS_STATIC, 1)
+    gq.gq_set_option(gq.GQ_OPT_X_STATIC, 1)
     gq.gq_set_option(gq.GQ_OPT_PREFILL_PAIR, 1 if pair else 0)
     W = torch.from_numpy(synth.q4_0_weights(M, K, seed=1)).cuda()
     X = torch.from_numpy(synth.activations(N, K, seed=2)).cuda()

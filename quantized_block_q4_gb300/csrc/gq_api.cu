@@ -351,7 +351,7 @@ gq_status gq_set_option(gq_option opt, int64_t value) {
       g_early_w = value ? 1 : 0;
       return GQ_OK;
     case GQ_OPT_DECODE_VARIANT:
-      if (value < 0 || value > 3) return fail(GQ_ERR_SHAPE, "decode variant must be 0..3");
+      if (value < 0 || value > 4) return fail(GQ_ERR_SHAPE, "decode variant must be 0..4");
       g_decode_variant = value;
       return GQ_OK;
     case GQ_OPT_PDL:

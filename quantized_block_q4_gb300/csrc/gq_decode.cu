@@ -441,7 +441,10 @@ cudaError_t launch_cfg(const CUtensorMap* tmW, const float* X, int N, int M, int
     occ_cache_smem = static_cast<int>(smem);
   }
   const int ntiles = (M + Cfg::kBM - 1) / Cfg::kBM;
-  const int grid = std::min(ntiles, device_info().sm_count * occ_cache);
+  // Small CTAs (two fit on an SM) run one per SM, so that the next launch's
+  // CTA can share the SM and overlap this one.
+  const int per_sm = (KW <= 4) ? 1 : occ_cache;
+  const int grid = std::min(ntiles, device_info().sm_count * per_sm);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(Cfg::kThreads);
@@ -516,6 +519,13 @@ cudaError_t launch_decode(const CUtensorMap* tmW, const float* X, int64_t N, int
     if (variant == 1) return launch_cfg<1, 1, 16, 4, true>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
     if (variant == 2) return launch_cfg<1, 4, 8, 2, true>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
     if (variant == 3) return launch_cfg<1, 2, 8, 2, true>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    if (variant == 4) return launch_cfg<1, 2, 4, 3, true>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    // By default, when consecutive launches may overlap (X and W not written by
+    // the previous kernel) and every SM gets at most one 32-row tile, the small
+    // 4-warp CTA lets the next launch's CTA share the SM; with more tiles per
+    // SM the 8-warp CTA computes faster.
+    if (variant == 0 && early_w && decode_x_static() && (m + 31) / 32 <= device_info().sm_count)
+      return launch_cfg<1, 2, 4, 3, true>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
     return launch_cfg<1, 2, 8, 3, true>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
   }
   if (N <= 8) {

@@ -430,7 +430,7 @@ def test_back_to_back_dependent_calls():
         x = got.astype(np.float32)      # continue from what the GPU produced
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4])
 @pytest.mark.parametrize("M,K,N", [(4096, 4096, 1), (300, 11008, 3), (33, 2304, 8)])
 def test_decode_variants(variant, M, K, N):
     old = gq.gq_get_option(gq.GQ_OPT_DECODE_VARIANT)
