@@ -62,15 +62,16 @@ size_t gq_q4_0_nbytes(int64_t M, int64_t K);
 gq_status gq_dequant_q4_0(const void *W, int64_t M, int64_t K, float *out, void *stream);
 
 /* Y[N][M] = X[N][K] * W^T with W in Q4_0, fp32 in and out (see header).
- * Dispatch by N: N < 64 streams W through the decode kernel (fp16 x, exact
- * integer codes, fp32 block scales and accumulation); N >= 64 converts X to
+ * Dispatch by N: N < 16 streams W through the decode kernel (fp16 x, exact
+ * integer codes, fp32 block scales and accumulation); N >= 16 converts X to
  * bf16 once and runs the tcgen05 tensor-core kernel on bf16 tiles of the
- * dequantised W with fp32 accumulation.  Fast paths need K % 256 == 0 and W,
- * X, Y 16-byte aligned; other shapes take a slower generic kernel.  The N >= 64
- * path allocates N*K*2 bytes of stream-ordered scratch (cudaMallocAsync) for
- * bf16 X, plus, when the tensor-core kernel splits tiles across CTAs
- * (GQ_OPT_PREFILL_STREAMK), 2 x 128 KiB per CTA and 4 bytes per output tile
- * for partial sums; it frees them on the same stream.  Accuracy: |y - y_ref| <= 1e-3*sum_k|w_k x_k|
+ * dequantised W with fp32 accumulation (GQ_OPT_PREFILL_MIN_N moves the
+ * threshold).  Fast paths need K % 256 == 0 and W, X, Y 16-byte aligned; other
+ * shapes take a slower generic kernel.  The tensor-core path allocates N*K*2
+ * bytes of stream-ordered scratch for bf16 X, plus, when it splits tiles
+ * along k (GQ_OPT_PREFILL_STREAMK), 128 KiB per split piece and 8 bytes per
+ * split tile for partial sums, from a pool the library keeps per device; it
+ * frees them on the same stream.  Accuracy: |y - y_ref| <= 1e-3*sum_k|w_k x_k|
  * + 1e-5 on the synthetic workloads (random-sign data). */
 gq_status gq_mul_mat_q4_0(const void *W, int64_t M, int64_t K, const float *X, int64_t N, float *Y,
                           void *stream);
@@ -83,7 +84,7 @@ gq_status gq_mul_mat_q4_0(const void *W, int64_t M, int64_t K, const float *X, i
 gq_status gq_mul_mat_q4_0_bf16x(const void *W, int64_t M, int64_t K, const uint16_t *X_bf16, int64_t N,
                                 float *Y, void *stream);
 
-/* Same result as the N >= 64 path of gq_mul_mat_q4_0 (bf16 activations,
+/* Same result as the tensor-core path of gq_mul_mat_q4_0 (bf16 activations,
  * tensor-core kernel), for any N >= 1, but with no device allocation: the
  * bf16 copy of X goes to a fixed 12 MiB array inside the library instead of
  * cudaMallocAsync scratch, and the tensor-core kernel runs one CTA per tile
@@ -110,7 +111,7 @@ gq_status gq_sync_status(void *stream);
 
 /* Tuning / test options (process-wide). */
 typedef enum {
-  GQ_OPT_PREFILL_MIN_N = 0,  /* N at which mul_mat switches to the tensor-core path (default 64) */
+  GQ_OPT_PREFILL_MIN_N = 0,  /* N at which mul_mat switches to the tensor-core path (default 16) */
   GQ_OPT_FORCE_GENERIC = 1,  /* 1: every mul_mat takes the generic kernel (test aid) */
   GQ_OPT_WAIT_LIMIT_NS = 2,  /* bound on any in-kernel wait, nanoseconds (default 2e9) */
   GQ_OPT_WEIGHTS_STATIC = 3, /* 1: promise that no kernel launched right before a mul_mat on the same
@@ -136,7 +137,7 @@ typedef enum {
                                 kernel streams before the previous kernel finishes (1..64, capped by the
                                 ring, default 2); later stages wait until x is staged */
   GQ_OPT_X_STATIC = 11        /* 1: promise that the kernel launched right before a decode mul_mat
-                                (N < 64) on the same stream does not write its X (e.g. several
+                                (N below the tensor-core threshold) on the same stream does not write its X (e.g. several
                                 projections of one activation), so the kernel may read X and compute
                                 before that kernel finishes; Y is still written only after it.
                                 Default 0: X is read after the previous kernel completes */

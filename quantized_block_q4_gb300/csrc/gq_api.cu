@@ -20,7 +20,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 thread_local std::string t_last_error;
 
-std::atomic<int64_t> g_prefill_min_n{64};
+std::atomic<int64_t> g_prefill_min_n{16};  // N >= 16: the tensor-core kernel is faster
 std::atomic<int64_t> g_force_generic{0};
 std::atomic<int64_t> g_wait_limit_ns{2000000000LL};
 std::atomic<int64_t> g_early_w{0};

@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int n = nt * 8 + 2 * t + (i & 1);
-            if (n < N) mine[(mt * 16 + g + 8 * (i >> 1)) * N + n] = acc[mt][nt][i];
+            if (n < N) mine[n * kBM + mt * 16 + g + 8 * (i >> 1)] = acc[mt][nt][i];
           }
       __syncwarp();
       int prev = 0;
@@ -386,16 +386,30 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
       if (prev == KW - 1) {
         if (x_static) pdl_wait();
         __threadfence_block();
-        for (int idx = lane; idx < kBM * N; idx += 32) {
-          const int r = idx / N, n = idx % N;
+        // Partials are [warp][token][row]: lanes walk rows, so the shared
+        // reads are conflict-free and the Y stores coalesce along m.  After
+        // the first x chunk, Y already holds the earlier chunks' sums: load
+        // all of them before any store (independent loads, one latency).
+        constexpr int kPer = (kBM * 8 * NT + 31) / 32;  // outputs per lane at most
+        float yold[kPer];
+        if (c > 0) {
+#pragma unroll
+          for (int j = 0; j < kPer; ++j) {
+            const int idx = lane + 32 * j;
+            const int n = idx / kBM, row = tile * kBM + idx % kBM;
+            yold[j] = (idx < kBM * N && live && row < M) ? Y[static_cast<size_t>(n) * M + row] : 0.f;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+          const int idx = lane + 32 * j;
+          if (idx >= kBM * N) break;
+          const int n = idx / kBM, r = idx % kBM;
           const int row = tile * kBM + r;
           float v = 0.f;
 #pragma unroll
-          for (int w = 0; w < KW; ++w) v += *reinterpret_cast<volatile float*>(&as[(w * kBM + r) * N + n]);
-          if (live && row < M) {
-            float* yp = Y + static_cast<size_t>(n) * M + row;
-            *yp = (c == 0) ? v : (*yp + v);
-          }
+          for (int w = 0; w < KW; ++w) v += *reinterpret_cast<volatile float*>(&as[(w * N + n) * kBM + r]);
+          if (live && row < M) Y[static_cast<size_t>(n) * M + row] = (c == 0) ? v : (yold[j] + v);
         }
         __syncwarp();
         if (lane == 0) {

@@ -364,7 +364,7 @@ def test_bf16_activation_entry(N):
 
 
 def test_prefill_threshold_option_switches_kernels():
-    M, K, N = 200, 1024, 20
+    M, K, N = 200, 1024, 12
     W = synth.q4_0_weights(M, K, seed=7000)
     X = synth.activations(N, K, seed=7001)
     y_ref, s_ref = oracle_mul_mat(W, M, K, X)
