@@ -513,6 +513,7 @@ __global__ void k_generic_q4_0(const uint8_t* __restrict__ W, int64_t M, int64_t
 int decode_rows_per_tile(int64_t N, int variant) {
   if (N == 1) return variant == 1 ? 16 : (variant == 2 ? 64 : 32);
   if (N <= 8) return (variant == 2) ? 16 : 32;
+  if (N <= 16) return 32;
   return 16;
 }
 
@@ -546,7 +547,7 @@ cudaError_t launch_decode(const CUtensorMap* tmW, const float* X, int64_t N, int
     if (variant == 2) return launch_cfg<1, 1, 8, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
     return launch_cfg<1, 2, 8, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
   }
-  if (N <= 16) return launch_cfg<2, 1, 8, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+  if (N <= 16) return launch_cfg<2, 2, 8, 2>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
   if (N <= 32) return launch_cfg<4, 1, 4, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 96 << 10, early_w, pdl, s);
   return launch_cfg<8, 1, 4, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 48 << 10, early_w, pdl, s);
 }
