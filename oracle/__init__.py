@@ -63,6 +63,10 @@ class Oracle:
         lib.oracle_dequant_q4_0.restype = None
         lib.oracle_mul_mat_q4_0.argtypes = [vp, i64, i64, vp, i64, vp, vp, i32]
         lib.oracle_mul_mat_q4_0.restype = None
+        lib.oracle_float_to_half.argtypes = [ctypes.c_float]
+        lib.oracle_float_to_half.restype = ctypes.c_uint16
+        lib.oracle_quantize_q4_0.argtypes = [vp, i64, i64, vp]
+        lib.oracle_quantize_q4_0.restype = None
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = i32
         self.lib = lib
@@ -104,6 +108,19 @@ class Oracle:
         self.lib.oracle_mul_mat_q4_0(W.ctypes.data, M, K, X.ctypes.data, N,
                                      Y.ctypes.data, S.ctypes.data, int(nthreads))
         return Y, S
+
+    def float_to_half(self, f: float) -> int:
+        return int(self.lib.oracle_float_to_half(float(f)))
+
+    def quantize(self, W: np.ndarray) -> np.ndarray:
+        """fp32 W[M][K] -> uint8 [M][K/32*18] Q4_0 blocks."""
+        W = np.ascontiguousarray(W, dtype=np.float32)
+        M, K = W.shape
+        if K % 32:
+            raise ValueError("K must be a multiple of 32")
+        out = np.empty((M, K // 32 * 18), dtype=np.uint8)
+        self.lib.oracle_quantize_q4_0(W.ctypes.data, M, K, out.ctypes.data)
+        return out
 
     def max_threads(self) -> int:
         return int(self.lib.oracle_max_threads())

@@ -111,3 +111,99 @@ int oracle_max_threads(void)
     return 1;
 #endif
 }
+
+/*
+ * binary32 -> binary16, round to nearest, ties to even, from the IEEE-754
+ * fields: finite values too large for binary16 become infinity, values below
+ * its smallest subnormal round to (signed) zero or to the smallest subnormal,
+ * NaN stays NaN (quiet, sign kept).
+ */
+uint16_t oracle_float_to_half(float f)
+{
+    uint32_t x;
+    memcpy(&x, &f, sizeof x);
+    uint16_t sign = (uint16_t)((x >> 16) & 0x8000u);
+    int e = (int)((x >> 23) & 0xFF);          /* biased exponent of binary32 */
+    uint32_t m = x & 0x7FFFFFu;               /* 23 fraction bits */
+    if (e == 255)                              /* inf or NaN */
+        return (uint16_t)(sign | 0x7C00u | (m ? 0x200u : 0u));
+    /* value = 1.m * 2^(e-127) for e > 0, 0.m * 2^-126 for e == 0 */
+    int he = e - 127 + 15;                     /* binary16 biased exponent if normal */
+    if (he >= 31)
+        return (uint16_t)(sign | 0x7C00u);     /* overflow */
+    uint32_t mant;                             /* significand with the implicit bit, 24 bits */
+    int shift;                                 /* right shift down to the 10-bit binary16 fraction */
+    if (he >= 1) {
+        mant = m | 0x800000u;
+        shift = 13;
+    } else {
+        if (e == 0)
+            return sign;                       /* binary32 subnormals are far below binary16's range */
+        mant = m | 0x800000u;
+        shift = 14 - he;                       /* binary16 subnormal: fraction = value / 2^-24 */
+        if (shift > 24)
+            return sign;                       /* rounds to zero: below half the smallest subnormal */
+        he = 0;
+    }
+    uint32_t kept = mant >> shift;
+    uint32_t rest = mant & ((1u << shift) - 1u);
+    uint32_t half = 1u << (shift - 1);
+    if (rest > half || (rest == half && (kept & 1u)))
+        kept += 1u;                            /* may carry into the exponent: still correct */
+    if (he >= 1)
+        return (uint16_t)(sign | (uint16_t)((((uint32_t)he << 10) + (kept - 0x400u))));
+    return (uint16_t)(sign | (uint16_t)kept);  /* kept == 0x400 means the smallest normal */
+}
+
+/*
+ * Quantise one block of 32 weights to Q4_0, following the block-quantisation
+ * formula q(w) = clip(round(w / s) + z, q_min, q_max), w_hat = s * (q - z)
+ * ("Architecture and module overview", weight-loading section) with z = 8,
+ * q in [0, 15].  The pages leave the choice of s open; the reading used here:
+ *   m = the weight of largest magnitude, sign kept (the first on ties),
+ *   s = m / -8 rounded to binary16 (the stored d), so that m maps to q = 0,
+ *   q = clip(rint(w / d) + 8, 0, 15) with the quotient taken in fp32 and the
+ *   rounding to nearest even; an all-zero block stores d = +0 and q = 8 for
+ *   all, and a quotient that is NaN also gives 8.
+ */
+static void quantize_block(const float *w, uint8_t *blk)
+{
+    float amax = 0.0f, m = 0.0f;
+    for (int j = 0; j < QK; ++j) {
+        float a = fabsf(w[j]);
+        if (a > amax) {
+            amax = a;
+            m = w[j];
+        }
+    }
+    uint16_t d_bits = amax > 0.0f ? oracle_float_to_half(m / -8.0f) : 0;   /* all-zero block: d = +0 */
+    float d = (float)oracle_half_to_double(d_bits);
+    int q[QK];
+    for (int j = 0; j < QK; ++j) {
+        if (d == 0.0f) {
+            q[j] = 8;
+            continue;
+        }
+        float t = rintf(w[j] / d) + 8.0f;
+        if (t != t)
+            q[j] = 8;
+        else if (t < 0.0f)
+            q[j] = 0;
+        else if (t > 15.0f)
+            q[j] = 15;
+        else
+            q[j] = (int)t;
+    }
+    blk[0] = (uint8_t)(d_bits & 0xFF);         /* little-endian binary16 */
+    blk[1] = (uint8_t)(d_bits >> 8);
+    for (int j = 0; j < 16; ++j)               /* low nibble: element j, high nibble: element j + 16 */
+        blk[2 + j] = (uint8_t)(q[j] | (q[j + 16] << 4));
+}
+
+void oracle_quantize_q4_0(const float *W, int64_t M, int64_t K, uint8_t *out)
+{
+    int64_t nb = K / QK;
+    for (int64_t r = 0; r < M; ++r)
+        for (int64_t b = 0; b < nb; ++b)
+            quantize_block(W + r * K + b * QK, out + (r * nb + b) * BLOCK_BYTES);
+}

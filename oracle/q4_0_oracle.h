@@ -24,9 +24,15 @@
  * w = d*(q-8) is formed in fp32 (exact: 11 significant bits times at most
  * 4 bits); products and sums of MUL_MAT are taken in fp64 in plain k order.
  *
+ *  - The quantiser follows the block-quantisation formula q(w) = clip(
+ *    round(w/s) + z, q_min, q_max) of the same section; how s is chosen is
+ *    not fixed by the pages (the reading is stated at quantize_block).
+ *
  * Every function here is pinned by the CPU tests (hand-derived block
  * fixtures, all 65536 binary16 patterns against numpy, one-hot columns,
- * exact special cases, brute force against a dense fp64 matmul).
+ * exact special cases, brute force against a dense fp64 matmul; for the
+ * quantiser: binary16 rounding against numpy, exact round trips, the nearest
+ * level by brute force and the error model).
  */
 #ifndef Q4_0_ORACLE_H
 #define Q4_0_ORACLE_H
@@ -61,6 +67,16 @@ void oracle_dequant_q4_0(const uint8_t *W, int64_t M, int64_t K, float *out);
 void oracle_mul_mat_q4_0(const uint8_t *W, int64_t M, int64_t K,
                          const float *X, int64_t N,
                          double *Y, double *S, int nthreads);
+
+/* binary32 -> binary16 bit pattern, round to nearest even (IEEE-754). */
+uint16_t oracle_float_to_half(float f);
+
+/*
+ * fp32 weights W[M][K] -> M rows of K/32 Q4_0 blocks (the quantiser, the step
+ * before MUL_MAT): per block, d = binary16(m / -8) with m the weight of largest
+ * magnitude, q = clip(rint(w / d) + 8, 0, 15) in fp32 (see the .c file).
+ */
+void oracle_quantize_q4_0(const float *W, int64_t M, int64_t K, uint8_t *out);
 
 /* Number of threads OpenMP would use by default (1 without OpenMP). */
 int oracle_max_threads(void);
