@@ -303,6 +303,7 @@ def run_gpu(args, rank, world, dist):
 
     # ---- end to end through the public API with host buffers (decode, N = 1)
     e2e = run_e2e(gq, torch, dev, s, W, shapes, acts1, order, L, args)
+    aux = run_aux(gq, torch, dev, s, peaks["hbm_gbs"]) if rank == 0 else {}
     e2e["ms"] = max_over_ranks([e2e["ms"]], dist, dev)[0]
     e2e_value = world * wbytes / (e2e["ms"] * 1e-3) / 1e9
 
@@ -347,6 +348,8 @@ def run_gpu(args, rank, world, dist):
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
                 "d2h_bytes_per_step": e2e["d2h"],
                 "path": "pinned host X -> device, gq_mul_mat_q4_0, Y -> pinned host, per matrix (decode sweep)"},
+        "dequant": aux.get("dequant"),
+        "quantize": aux.get("quantize"),
         "gpu_launches": K_ * (len(shapes) + len(shapes) + L * len(ks)),
         "clocks": clocks,
         "cpu_baseline": cpu,
@@ -354,6 +357,44 @@ def run_gpu(args, rank, world, dist):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+AUX_M, AUX_K, AUX_REPS = 14336, 4096, 10
+
+
+def run_aux(gq, torch, dev, s, hbm_gbs):
+    """The dequant and quantise kernels on the 14336 x 4096 matrix (fp32 side
+    235 MB, larger than L2), timed with CUDA events on the bench stream, each
+    against the HBM roofline with its algorithmic bytes."""
+    M, K = AUX_M, AUX_K
+    g = torch.Generator(device=dev).manual_seed(0x51A0)
+    Wf = torch.randn(M, K, device=dev, generator=g) * 0.05
+    Q = torch.empty(M, K // 32 * 18, dtype=torch.uint8, device=dev)
+    D = torch.empty(M, K, dtype=torch.float32, device=dev)
+    qbytes, fbytes = M * K // 32 * 18, 4 * M * K
+
+    def timed(fn):
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(AUX_REPS):
+                fn()
+            e1.record(s)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / AUX_REPS * 1e-3
+
+    tq = timed(lambda: gq.gq_quantize_q4_0(Wf, M, K, Q, stream=s))
+    td = timed(lambda: gq.gq_dequant_q4_0(Q, M, K, D, stream=s))
+    gq.gq_sync_status(s)
+    out = {}
+    for name, t, kern in (("quantize", tq, "k_quantize_q4_0"), ("dequant", td, "k_dequant_vec")):
+        gbs = (qbytes + fbytes) / t / 1e9
+        out[name] = {"kernel": kern, "shape": f"{M}x{K}", "us": round(t * 1e6, 2), "achieved": round(gbs, 1),
+                     "unit": "GB/s", "peak": hbm_gbs, "frac": round(gbs / hbm_gbs, 4), "bound": "hbm",
+                     "bytes": qbytes + fbytes, "bytes_note": "4*M*K fp32 + M*K/32*18 Q4_0, one read, one written"}
+    return out
 
 
 def run_e2e(gq, torch, dev, s, W, shapes, acts1, order, L, args):

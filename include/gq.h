@@ -61,6 +61,20 @@ size_t gq_q4_0_nbytes(int64_t M, int64_t K);
  * (16-byte aligned W and out take the vectorised kernel). */
 gq_status gq_dequant_q4_0(const void *W, int64_t M, int64_t K, float *out, void *stream);
 
+/* Quantise fp32 weights W[M][K] into M rows of K/32 Q4_0 blocks (18 bytes
+ * each) at `out` (M*K/32*18 bytes): the step before MUL_MAT.  Follows the
+ * block-quantisation formula q(w) = clip(round(w/s) + z, q_min, q_max),
+ * w_hat = s*(q - z) ("Architecture and module overview", weight-loading
+ * section) with z = 8, q in [0, 15].  The pages do not fix s; this library
+ * takes, per block, m = the weight of largest magnitude (sign kept, the first
+ * on ties), d = binary16(m / -8) rounded to nearest even (so m gets code 0;
+ * an all-zero block stores d = +0), and q = clip(rint(w / d) + 8, 0, 15) with
+ * the quotient an IEEE fp32 division (q = 8 when d == 0 or the quotient is
+ * NaN).  Every element that is not clipped is within d/2 of its weight.
+ * Device pointers; W 4-byte aligned (16 bytes takes the vector path); errors:
+ * K % 32 != 0 or negative sizes -> GQ_ERR_SHAPE, NULL -> GQ_ERR_NULL. */
+gq_status gq_quantize_q4_0(const float *W, int64_t M, int64_t K, void *out, void *stream);
+
 /* Y[N][M] = X[N][K] * W^T with W in Q4_0, fp32 in and out (see header).
  * Dispatch by N: N < 16 streams W through the decode kernel (fp16 x, exact
  * integer codes, fp32 block scales and accumulation); N >= 16 converts X to

@@ -46,6 +46,7 @@ _i64, _sz, _vp, _i32 = ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.
 SIGNATURES = {
     "gq_q4_0_nbytes": (_sz, [_i64, _i64]),
     "gq_dequant_q4_0": (_i32, [_vp, _i64, _i64, _vp, _vp]),
+    "gq_quantize_q4_0": (_i32, [_vp, _i64, _i64, _vp, _vp]),
     "gq_mul_mat_q4_0": (_i32, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "gq_mul_mat_q4_0_bf16x": (_i32, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "gq_mul_mat_q4_0_noalloc": (_i32, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
@@ -117,6 +118,10 @@ def gq_dequant_q4_0(W, M: int, K: int, out, stream=None) -> None:
     _check(_lib.gq_dequant_q4_0(_ptr(W), M, K, _ptr(out), _stream(stream)))
 
 
+def gq_quantize_q4_0(W, M: int, K: int, out, stream=None) -> None:
+    _check(_lib.gq_quantize_q4_0(_ptr(W), M, K, _ptr(out), _stream(stream)))
+
+
 def gq_mul_mat_q4_0(W, M: int, K: int, X, N: int, Y, stream=None) -> None:
     _check(_lib.gq_mul_mat_q4_0(_ptr(W), M, K, _ptr(X), N, _ptr(Y), _stream(stream)))
 
@@ -176,6 +181,18 @@ def dequant_q4_0(W: torch.Tensor, K: int, stream=None) -> torch.Tensor:
     M = _check_w(W, K)
     out = torch.empty((M, K), dtype=torch.float32, device=W.device)
     gq_dequant_q4_0(W, M, K, out, stream)
+    return out
+
+
+def quantize_q4_0(W: torch.Tensor, stream=None) -> torch.Tensor:
+    """W: float32 [M, K] (K % 32 == 0) -> uint8 [M, K/32*18] Q4_0 blocks."""
+    if W.dtype != torch.float32 or W.dim() != 2 or not W.is_contiguous():
+        raise TypeError("W must be a contiguous float32 [M, K] tensor")
+    M, K = W.shape
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    out = torch.empty((M, K // 32 * 18), dtype=torch.uint8, device=W.device)
+    gq_quantize_q4_0(W, M, K, out, stream)
     return out
 
 

@@ -244,6 +244,20 @@ gq_status gq_dequant_q4_0(const void* W, int64_t M, int64_t K, float* out, void*
   return e == cudaSuccess ? GQ_OK : cuda_fail(e, "dequant launch");
 }
 
+gq_status gq_quantize_q4_0(const float* W, int64_t M, int64_t K, void* out, void* stream) {
+  t_last_error.clear();
+  if (M < 0 || K < 0) return fail(GQ_ERR_SHAPE, "negative size");
+  if (K % kQK) return fail(GQ_ERR_SHAPE, "K=%lld is not a multiple of 32", (long long)K);
+  if (M == 0 || K == 0) return GQ_OK;
+  if (!W || !out) return fail(GQ_ERR_NULL, "W and out must not be NULL");
+  if (!aligned(W, 4)) return fail(GQ_ERR_ALIGN, "W must be 4-byte aligned");
+  if ((unsigned __int128)M * K * 4 > ((unsigned __int128)1 << 62)) return fail(GQ_ERR_SHAPE, "size overflows");
+  gq_status st = check_device();
+  if (st != GQ_OK) return st;
+  cudaError_t e = launch_quantize(W, M, K, static_cast<uint8_t*>(out), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GQ_OK : cuda_fail(e, "quantize launch");
+}
+
 gq_status gq_mul_mat_q4_0(const void* W, int64_t M, int64_t K, const float* X, int64_t N, float* Y, void* stream) {
   t_last_error.clear();
   gq_status st = check_mm_shape(M, K, N);

@@ -48,6 +48,9 @@ int get_decode_early_stages();
 void set_decode_x_static(int on);      // X is not written by the kernel right before (decode reads it early)
 int get_decode_x_static();
 
+// ---- KQ: fp32 -> Q4_0 blocks (gq_quantize.cu).  K % 32 == 0, W 4-byte aligned.
+cudaError_t launch_quantize(const float* W, int64_t M, int64_t K, uint8_t* out, cudaStream_t s);
+
 // ---- K0: fp32 -> bf16 (round to nearest even) (gq_prefill.cu)
 cudaError_t launch_f32_to_bf16(const float* x, uint16_t* y, int64_t n, cudaStream_t s);
 
