@@ -35,13 +35,20 @@ __device__ __forceinline__ void quantize_one(const float (&w)[32], uint8_t* dst)
   }
   const uint16_t d_bits = amax > 0.f ? __half_as_ushort(__float2half_rn(m / -8.0f)) : static_cast<uint16_t>(0);
   const float d = __half2float(__ushort_as_half(d_bits));
+  // rint(w / d) with the IEEE quotient: w * RN(1/d) is within 2 ulps of the
+  // rounded quotient (|w / d| <= 8.01), so the two can round to different
+  // integers only next to a half-integer; there the division itself decides.
+  const float r = __frcp_rn(d);
   uint32_t q[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     if (d == 0.f) {
       q[j] = 8;
     } else {
-      const float t = rintf(__fdiv_rn(w[j], d)) + 8.0f;
+      float u = w[j] * r;
+      float h = rintf(u);
+      if (fabsf(u - h) > 0.5f - 1e-4f) h = rintf(__fdiv_rn(w[j], d));
+      const float t = h + 8.0f;
       q[j] = (t != t) ? 8u : (t < 0.f ? 0u : (t > 15.f ? 15u : static_cast<uint32_t>(t)));
     }
   }
