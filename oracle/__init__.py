@@ -67,6 +67,8 @@ class Oracle:
         lib.oracle_float_to_half.restype = ctypes.c_uint16
         lib.oracle_quantize_q4_0.argtypes = [vp, i64, i64, vp]
         lib.oracle_quantize_q4_0.restype = None
+        lib.oracle_mul_mat_id_q4_0.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, vp, i32]
+        lib.oracle_mul_mat_id_q4_0.restype = None
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = i32
         self.lib = lib
@@ -121,6 +123,23 @@ class Oracle:
         out = np.empty((M, K // 32 * 18), dtype=np.uint8)
         self.lib.oracle_quantize_q4_0(W.ctypes.data, M, K, out.ctypes.data)
         return out
+
+    def mul_mat_id(self, W: np.ndarray, n_expert: int, M: int, K: int, X: np.ndarray, ids: np.ndarray,
+                   nthreads: int = 1):
+        """W: n_expert*M rows of blocks; X [T][S][K] fp32; ids [T][S] int32 -> (Y, S) fp64 [T][S][M]."""
+        W = np.ascontiguousarray(W, dtype=np.uint8)
+        X = np.ascontiguousarray(X, dtype=np.float32)
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        if W.size != n_expert * self.nbytes(M, K):
+            raise ValueError("W has the wrong number of bytes")
+        T, S = ids.shape
+        if X.shape != (T, S, K):
+            raise ValueError("X must be [T][S][K]")
+        Y = np.empty((T, S, M), dtype=np.float64)
+        Sa = np.empty((T, S, M), dtype=np.float64)
+        self.lib.oracle_mul_mat_id_q4_0(W.ctypes.data, n_expert, M, K, X.ctypes.data, S, ids.ctypes.data, T,
+                                        Y.ctypes.data, Sa.ctypes.data, int(nthreads))
+        return Y, Sa
 
     def max_threads(self) -> int:
         return int(self.lib.oracle_max_threads())

@@ -207,3 +207,33 @@ void oracle_quantize_q4_0(const float *W, int64_t M, int64_t K, uint8_t *out)
         for (int64_t b = 0; b < nb; ++b)
             quantize_block(W + r * K + b * QK, out + (r * nb + b) * BLOCK_BYTES);
 }
+
+/*
+ * MUL_MAT_ID (expert-routed MUL_MAT; "GGUF loading, mmap and tensor
+ * placement", step six, the MUL_MAT_ID probe: w ne = [K, M, n_expert], b ne =
+ * [K, n_ids, tokens], ids ne = [n_ids, tokens]):
+ *   Y[t][s][m] = sum_k w_e[m][k] * X[t][s][k],  e = ids[t][s]
+ * W holds n_expert matrices of M rows one after the other; X is [T][S][K];
+ * ids is [T][S]; Y and the tolerance scale S_abs are [T][S][M] (fp64, k
+ * ascending, as in oracle_mul_mat_q4_0).  An id outside [0, n_expert) leaves
+ * its Y and S_abs rows NaN.
+ */
+void oracle_mul_mat_id_q4_0(const uint8_t *W, int64_t n_expert, int64_t M, int64_t K,
+                            const float *X, int64_t S, const int32_t *ids, int64_t T,
+                            double *Y, double *S_abs, int nthreads)
+{
+    size_t expert_bytes = (size_t)M * (size_t)(K / QK) * BLOCK_BYTES;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t s = 0; s < S; ++s) {
+            int32_t e = ids[t * S + s];
+            double *y = Y + (size_t)(t * S + s) * (size_t)M;
+            double *sa = S_abs + (size_t)(t * S + s) * (size_t)M;
+            if (e < 0 || e >= n_expert) {
+                for (int64_t m = 0; m < M; ++m)
+                    y[m] = sa[m] = NAN;
+                continue;
+            }
+            oracle_mul_mat_q4_0(W + (size_t)e * expert_bytes, M, K, X + (size_t)(t * S + s) * (size_t)K, 1,
+                                y, sa, nthreads);
+        }
+}

@@ -78,6 +78,16 @@ uint16_t oracle_float_to_half(float f);
  */
 void oracle_quantize_q4_0(const float *W, int64_t M, int64_t K, uint8_t *out);
 
+/*
+ * MUL_MAT_ID: Y[t][s][m] = sum_k w_e[m][k] * X[t][s][k] with e = ids[t][s]
+ * (expert-routed; W = n_expert matrices of M rows each, X [T][S][K], ids
+ * [T][S], Y and S_abs [T][S][M] in fp64).  Ids outside [0, n_expert) give
+ * NaN rows.
+ */
+void oracle_mul_mat_id_q4_0(const uint8_t *W, int64_t n_expert, int64_t M, int64_t K,
+                            const float *X, int64_t S, const int32_t *ids, int64_t T,
+                            double *Y, double *S_abs, int nthreads);
+
 /* Number of threads OpenMP would use by default (1 without OpenMP). */
 int oracle_max_threads(void);
 
