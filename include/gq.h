@@ -48,7 +48,9 @@ typedef enum {
   GQ_ERR_CUDA = -4,            /* a CUDA runtime call or kernel launch failed */
   GQ_ERR_ALLOC = -5,           /* stream-ordered scratch allocation failed */
   GQ_ERR_DEVICE_TIMEOUT = -6,  /* a kernel's bounded wait gave up (see gq_sync_status) */
-  GQ_ERR_UNSUPPORTED = -7      /* current device is not compute capability 10.3 */
+  GQ_ERR_UNSUPPORTED = -7,     /* current device is not compute capability 10.3 */
+  GQ_ERR_BAD_INDEX = -8        /* an expert id outside [0, n_expert) reached gq_mul_mat_id_q4_0
+                                  (reported by gq_sync_status) */
 } gq_status;
 
 /* Bytes of a Q4_0 matrix of M rows and K columns: M*(K/32)*18
@@ -90,6 +92,33 @@ gq_status gq_quantize_q4_0(const float *W, int64_t M, int64_t K, void *out, void
 gq_status gq_mul_mat_q4_0(const void *W, int64_t M, int64_t K, const float *X, int64_t N, float *Y,
                           void *stream);
 
+/* MUL_MAT_ID: the expert-routed MUL_MAT of mixture-of-experts layers
+ * ("GGUF loading, mmap and tensor placement", step six, the MUL_MAT_ID probe:
+ * w ne = [K, M, n_expert], b ne = [K, n_ids, T], ids ne = [n_ids, T] of I32).
+ *   W    n_expert Q4_0 matrices of M rows, one after the other (expert e's row
+ *        m is row e*M + m; n_expert*M*K/32*18 bytes).
+ *   X    F32 [T][n_ids][K]: the activation row of each (token t, slot s).
+ *   ids  I32 [T][n_ids], device memory: the expert of each (t, s).
+ *   Y    F32 [T][n_ids][M]: Y[t][s][m] = sum_k w_e[m][k] * X[t][s][k],
+ *        e = ids[t][s].
+ * The pairs are sorted by expert on the device (a stable counting sort, no
+ * host synchronisation), so each expert's weights stream once for all its
+ * tokens: with fewer than 16 tokens per used expert on average the decode
+ * kernel runs one group of tokens per expert, otherwise the gathered tokens
+ * go to the tcgen05 tensor-core kernel as bf16 (GQ_OPT_MOE_PATH forces either).
+ * Accuracy as gq_mul_mat_q4_0.  Scratch (stream-ordered, library pool): the
+ * routing tables, about (2*n_expert + 4*T*n_ids) * 4 bytes, plus T*n_ids*K*2
+ * bytes of bf16 rows on the tensor-core path.
+ *  - An id outside [0, n_expert) sets that Y row to NaN and makes the next
+ *    gq_sync_status() return GQ_ERR_BAD_INDEX; the other rows are computed.
+ *  - Fast paths need K % 256 == 0, W, X, Y 16-byte aligned, ids 4-byte
+ *    aligned, n_expert <= 16384 and n_expert*M < 2^31; other shapes take a
+ *    slower generic kernel.
+ *  - T or n_ids or M equal to 0 is a no-op; K == 0 writes zeros (NaN for bad
+ *    ids).  n_expert must be >= 1 (GQ_ERR_SHAPE). */
+gq_status gq_mul_mat_id_q4_0(const void *W, int64_t n_expert, int64_t M, int64_t K, const float *X,
+                             int64_t n_ids, const int32_t *ids, int64_t T, float *Y, void *stream);
+
 /* MUL_MAT with activations the caller already holds in bf16: X_bf16[N][K]
  * (raw bfloat16 bits).  Runs the tensor-core kernel for every N >= 1.  Its
  * only allocation is the stream-ordered partial-sum scratch of split tiles
@@ -120,7 +149,8 @@ gq_status gq_f32_to_bf16(const float *x, uint16_t *y, int64_t n, void *stream);
 
 /* Synchronise `stream`, then read and clear the device error word.  Returns
  * GQ_ERR_DEVICE_TIMEOUT if a kernel's bounded wait gave up since the last
- * call, GQ_ERR_CUDA if the synchronisation failed, else GQ_OK. */
+ * call, else GQ_ERR_BAD_INDEX if gq_mul_mat_id_q4_0 met an expert id out of
+ * range, GQ_ERR_CUDA if the synchronisation failed, else GQ_OK. */
 gq_status gq_sync_status(void *stream);
 
 /* Tuning / test options (process-wide). */
@@ -150,11 +180,13 @@ typedef enum {
   GQ_OPT_DECODE_EARLY_STAGES = 10, /* with GQ_OPT_WEIGHTS_STATIC: how many ring stages of W the decode
                                 kernel streams before the previous kernel finishes (1..64, capped by the
                                 ring, default 2); later stages wait until x is staged */
-  GQ_OPT_X_STATIC = 11        /* 1: promise that the kernel launched right before a decode mul_mat
+  GQ_OPT_X_STATIC = 11,       /* 1: promise that the kernel launched right before a decode mul_mat
                                 (N below the tensor-core threshold) on the same stream does not write its X (e.g. several
                                 projections of one activation), so the kernel may read X and compute
                                 before that kernel finishes; Y is still written only after it.
                                 Default 0: X is read after the previous kernel completes */
+  GQ_OPT_MOE_PATH = 12        /* gq_mul_mat_id_q4_0 kernel: 0 (default) by tokens per used expert,
+                                1 decode kernel, 2 tensor-core kernel (fast-path shapes only) */
 } gq_option;
 gq_status gq_set_option(gq_option opt, int64_t value);
 int64_t gq_get_option(gq_option opt);

@@ -4,7 +4,7 @@ Argument marshalling only: every step of dequantisation and MUL_MAT runs in the
 CUDA kernels of ``libgq.so``.  PyTorch is used for device memory and streams.
 The functions named ``gq_*`` mirror the C entry points one to one and take
 torch CUDA tensors (or raw device addresses as ints); ``dequant_q4_0`` and
-``mul_mat_q4_0`` are conveniences that allocate their outputs with torch.
+``mul_mat_q4_0`` / ``mul_mat_id_q4_0`` are conveniences that allocate their outputs with torch.
 
 If ``libgq.so`` is missing this module refuses to import: there is no CPU or
 PyTorch fallback.  Build it with ``python quantized_block_q4_gb300/build.py``.
@@ -27,6 +27,7 @@ GQ_ERR_CUDA = -4
 GQ_ERR_ALLOC = -5
 GQ_ERR_DEVICE_TIMEOUT = -6
 GQ_ERR_UNSUPPORTED = -7
+GQ_ERR_BAD_INDEX = -8
 
 GQ_OPT_PREFILL_MIN_N = 0
 GQ_OPT_FORCE_GENERIC = 1
@@ -40,6 +41,7 @@ GQ_OPT_PREFILL_STREAMK = 8
 GQ_OPT_PREFILL_SLOTS = 9
 GQ_OPT_DECODE_EARLY_STAGES = 10
 GQ_OPT_X_STATIC = 11
+GQ_OPT_MOE_PATH = 12
 
 # Every symbol include/gq.h declares, with (restype, argtypes).
 _i64, _sz, _vp, _i32 = ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int
@@ -48,6 +50,7 @@ SIGNATURES = {
     "gq_dequant_q4_0": (_i32, [_vp, _i64, _i64, _vp, _vp]),
     "gq_quantize_q4_0": (_i32, [_vp, _i64, _i64, _vp, _vp]),
     "gq_mul_mat_q4_0": (_i32, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
+    "gq_mul_mat_id_q4_0": (_i32, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp]),
     "gq_mul_mat_q4_0_bf16x": (_i32, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "gq_mul_mat_q4_0_noalloc": (_i32, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "gq_f32_to_bf16": (_i32, [_vp, _vp, _i64, _vp]),
@@ -124,6 +127,11 @@ def gq_quantize_q4_0(W, M: int, K: int, out, stream=None) -> None:
 
 def gq_mul_mat_q4_0(W, M: int, K: int, X, N: int, Y, stream=None) -> None:
     _check(_lib.gq_mul_mat_q4_0(_ptr(W), M, K, _ptr(X), N, _ptr(Y), _stream(stream)))
+
+
+def gq_mul_mat_id_q4_0(W, n_expert: int, M: int, K: int, X, n_ids: int, ids, T: int, Y, stream=None) -> None:
+    _check(_lib.gq_mul_mat_id_q4_0(_ptr(W), n_expert, M, K, _ptr(X), n_ids, _ptr(ids), T, _ptr(Y),
+                                   _stream(stream)))
 
 
 def gq_mul_mat_q4_0_bf16x(W, M: int, K: int, X_bf16, N: int, Y, stream=None) -> None:
@@ -204,4 +212,23 @@ def mul_mat_q4_0(W: torch.Tensor, X: torch.Tensor, stream=None, out: torch.Tenso
     M = _check_w(W, K)
     Y = out if out is not None else torch.empty((N, M), dtype=torch.float32, device=X.device)
     gq_mul_mat_q4_0(W, M, K, X, N, Y, stream)
+    return Y
+
+
+def mul_mat_id_q4_0(W: torch.Tensor, n_expert: int, X: torch.Tensor, ids: torch.Tensor, stream=None,
+                    out: torch.Tensor | None = None) -> torch.Tensor:
+    """Y[T, S, M]: row (t, s) is X[t, s] @ dequant(W_e)^T with e = ids[t, s].
+    W uint8 [n_expert*M, K/32*18] (experts one after the other), X float32
+    [T, S, K], ids int32 [T, S]."""
+    if X.dtype != torch.float32 or X.dim() != 3:
+        raise TypeError("X must be float32 [T, S, K]")
+    if ids.dtype != torch.int32 or tuple(ids.shape) != tuple(X.shape[:2]):
+        raise TypeError("ids must be int32 [T, S]")
+    T, S, K = X.shape
+    rows = _check_w(W, K)
+    if n_expert < 1 or rows % n_expert:
+        raise ValueError("W rows are not a multiple of n_expert")
+    M = rows // n_expert
+    Y = out if out is not None else torch.empty((T, S, M), dtype=torch.float32, device=X.device)
+    gq_mul_mat_id_q4_0(W, n_expert, M, K, X, S, ids, T, Y, stream)
     return Y

@@ -1,6 +1,7 @@
 // The C ABI of include/gq.h: argument checks, dispatch, tensor maps, errors.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -10,6 +11,7 @@
 
 #include "gq.h"
 #include "gq_internal.h"
+#include "gq_ptx.cuh"
 
 namespace gq {
 
@@ -26,6 +28,7 @@ std::atomic<int64_t> g_wait_limit_ns{2000000000LL};
 std::atomic<int64_t> g_early_w{0};
 std::atomic<int64_t> g_decode_variant{0};
 std::atomic<int64_t> g_pdl{1};
+std::atomic<int64_t> g_moe_path{0};
 
 gq_status fail(gq_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 gq_status fail(gq_status st, const char* fmt, ...) {
@@ -297,6 +300,85 @@ gq_status gq_mul_mat_q4_0(const void* W, int64_t M, int64_t K, const float* X, i
   return e == cudaSuccess ? GQ_OK : cuda_fail(e, "scratch free");
 }
 
+gq_status gq_mul_mat_id_q4_0(const void* W, int64_t n_expert, int64_t M, int64_t K, const float* X, int64_t n_ids,
+                             const int32_t* ids, int64_t T, float* Y, void* stream) {
+  t_last_error.clear();
+  if (n_expert < 1) return fail(GQ_ERR_SHAPE, "n_expert=%lld must be >= 1", (long long)n_expert);
+  if (n_ids < 0 || T < 0) return fail(GQ_ERR_SHAPE, "negative size (n_ids=%lld T=%lld)", (long long)n_ids, (long long)T);
+  const int64_t lim = (int64_t(1) << 31) - 1;
+  if (n_ids > lim || T > lim || (T > 0 && n_ids > lim / T))
+    return fail(GQ_ERR_SHAPE, "T*n_ids exceeds 2^31-1 (n_ids=%lld T=%lld)", (long long)n_ids, (long long)T);
+  const int64_t P = T * n_ids;  // (token, slot) pairs
+  gq_status st = check_mm_shape(M, K, P);
+  if (st != GQ_OK) return st;
+  if (n_expert > lim || (unsigned __int128)n_expert * M * (K / kQK) * kBlockBytes > ((unsigned __int128)1 << 62))
+    return fail(GQ_ERR_SHAPE, "n_expert=%lld: weight size overflows", (long long)n_expert);
+  if (M == 0 || P == 0) return GQ_OK;
+  if (!Y || !ids) return fail(GQ_ERR_NULL, "ids and Y must not be NULL");
+  if (K > 0 && (!W || !X)) return fail(GQ_ERR_NULL, "W and X must not be NULL");
+  if (!aligned(X, 4) || !aligned(Y, 4) || !aligned(ids, 4))
+    return fail(GQ_ERR_ALIGN, "X, Y and ids must be 4-byte aligned");
+  st = check_device();
+  if (st != GQ_OK) return st;
+  auto s = static_cast<cudaStream_t>(stream);
+
+  const bool fast = K > 0 && K % 256 == 0 && aligned(W, 16) && aligned(X, 16) && aligned(Y, 16) &&
+                    moe_route_supported(n_expert) && n_expert * M <= lim;
+  if (!fast || g_force_generic.load()) {
+    cudaError_t e = launch_generic_id(static_cast<const uint8_t*>(W), n_expert, M, K, X, ids, P, Y, s);
+    return e == cudaSuccess ? GQ_OK : cuda_fail(e, "generic MUL_MAT_ID launch");
+  }
+  const int64_t used = std::min(n_expert, P);
+  const int64_t path = g_moe_path.load();
+  const bool tc = path == 2 || (path == 0 && P >= 16 * used);
+  const int cap = decode_moe_cap(P, n_expert);
+  const int64_t n_mtiles = (M + 127) / 128;
+  if (tc && n_mtiles * ((P + kMoeBN - 1) / kMoeBN + used) > lim)
+    return fail(GQ_ERR_SHAPE, "too many tensor-core work items");
+
+  const size_t route_bytes = (moe_route_ints(n_expert, P, cap) * sizeof(int32_t) + 255) / 256 * 256;
+  const size_t xg_bytes = tc ? static_cast<size_t>(P) * K * sizeof(uint16_t) : 0;
+  void* scratch = nullptr;
+  cudaError_t e = scratch_alloc(&scratch, route_bytes + xg_bytes, s);
+  if (e != cudaSuccess)
+    return fail(GQ_ERR_ALLOC, "scratch allocation (%zu bytes): %s", route_bytes + xg_bytes, cudaGetErrorString(e));
+  const MoeRoute rt = moe_route_layout(static_cast<int32_t*>(scratch), n_expert, P, cap);
+  const uint64_t limit = static_cast<uint64_t>(g_wait_limit_ns.load());
+  const int pdl = static_cast<int>(g_pdl.load());
+  const uint64_t row_bytes = static_cast<uint64_t>(K / kQK) * kBlockBytes;
+  const char* what = "MUL_MAT_ID routing launch";
+  e = launch_moe_route(ids, P, n_expert, n_mtiles, kMoeBN, cap, rt, Y, M, s);
+  if (e == cudaSuccess && !tc) {
+    CUtensorMap tm;
+    uint32_t bx = 0, by = 0;
+    decode_moe_w_box(cap, &bx, &by);
+    st = make_tmap(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, row_bytes, static_cast<uint64_t>(n_expert * M), row_bytes,
+                   bx, by, CU_TENSOR_MAP_SWIZZLE_NONE);
+    what = "MUL_MAT_ID decode launch";
+    if (st == GQ_OK) e = launch_decode_moe(&tm, X, cap, n_expert, M, K, P, rt, Y, limit, pdl, s);
+  } else if (e == cudaSuccess) {
+    uint16_t* xg = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(scratch) + route_bytes);
+    CUtensorMap tmW, tmX;
+    st = make_tmap(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, row_bytes, static_cast<uint64_t>(n_expert * M), row_bytes,
+                   144, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st == GQ_OK)
+      st = make_tmap(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xg, static_cast<uint64_t>(K), static_cast<uint64_t>(P),
+                     static_cast<uint64_t>(K) * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st == GQ_OK) {
+      what = "MUL_MAT_ID gather launch";
+      e = launch_moe_gather_bf16(X, P, K, rt, xg, pdl, s);
+      if (e == cudaSuccess) {
+        what = "MUL_MAT_ID tensor-core launch";
+        e = launch_prefill_moe(&tmW, &tmX, n_expert, M, K, P, rt, Y, limit, pdl, s);
+      }
+    }
+  }
+  const cudaError_t f = scratch_free(scratch, s);
+  if (st != GQ_OK) return st;
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  return f == cudaSuccess ? GQ_OK : cuda_fail(f, "scratch free");
+}
+
 gq_status gq_mul_mat_q4_0_bf16x(const void* W, int64_t M, int64_t K, const uint16_t* X_bf16, int64_t N, float* Y,
                                 void* stream) {
   t_last_error.clear();
@@ -342,7 +424,9 @@ gq_status gq_sync_status(void* stream) {
   if (v) {
     const uint32_t zero = 0;
     cudaMemcpy(w, &zero, sizeof zero, cudaMemcpyHostToDevice);
-    return fail(GQ_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait gave up (device error bits 0x%x)", v);
+    if (v & DEVERR_TIMEOUT)
+      return fail(GQ_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait gave up (device error bits 0x%x)", v);
+    return fail(GQ_ERR_BAD_INDEX, "an expert id was outside [0, n_expert) (device error bits 0x%x)", v);
   }
   return GQ_OK;
 }
@@ -393,6 +477,10 @@ gq_status gq_set_option(gq_option opt, int64_t value) {
     case GQ_OPT_X_STATIC:
       set_decode_x_static(static_cast<int>(value));
       return GQ_OK;
+    case GQ_OPT_MOE_PATH:
+      if (value < 0 || value > 2) return fail(GQ_ERR_SHAPE, "MUL_MAT_ID path must be 0, 1 or 2");
+      g_moe_path = value;
+      return GQ_OK;
   }
   return fail(GQ_ERR_SHAPE, "unknown option %d", static_cast<int>(opt));
 }
@@ -411,6 +499,7 @@ int64_t gq_get_option(gq_option opt) {
     case GQ_OPT_PREFILL_SLOTS: return get_prefill_slots();
     case GQ_OPT_DECODE_EARLY_STAGES: return get_decode_early_stages();
     case GQ_OPT_X_STATIC: return get_decode_x_static();
+    case GQ_OPT_MOE_PATH: return g_moe_path.load();
   }
   return -1;
 }
@@ -427,6 +516,7 @@ const char* gq_status_string(gq_status s) {
     case GQ_ERR_ALLOC: return "GQ_ERR_ALLOC";
     case GQ_ERR_DEVICE_TIMEOUT: return "GQ_ERR_DEVICE_TIMEOUT";
     case GQ_ERR_UNSUPPORTED: return "GQ_ERR_UNSUPPORTED";
+    case GQ_ERR_BAD_INDEX: return "GQ_ERR_BAD_INDEX";
   }
   return "unknown gq_status";
 }

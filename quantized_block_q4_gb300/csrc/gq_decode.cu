@@ -133,11 +133,18 @@ constexpr int decode_min_blocks() {
   return (NT <= 2 && STAGES * KW * 16 * MT * 144 <= 80 * 1024) ? 2 : 1;
 }
 
-template <int NT, int MT, int KW, int STAGES, bool ONE>
+// MOE: MUL_MAT_ID over the decode groups of rt (expert e, up to N tokens
+// each).  N is then the group capacity, which fixes the shared-memory layout;
+// a group's own token count Nt <= N sets the work.  W rows of expert e start
+// at e * M; x and Y rows are the pairs perm[first + n].  The CTAs are shared
+// out evenly among the groups (each CTA taking every cpg-th tile of its
+// group), or, with more groups than CTAs, CTA b runs groups b, b + grid, ...
+template <int NT, int MT, int KW, int STAGES, bool ONE, bool MOE = false>
 __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, STAGES>()))
     k_decode_q4_0(const __grid_constant__ CUtensorMap tmW, const float* __restrict__ X, int N, int M, int K,
                   int KX, float* __restrict__ Y, uint64_t limit_ns, uint32_t* err, int early_stages,
-                  int x_static) {
+                  int x_static, const MoeRoute rt) {
+  static_assert(!(MOE && ONE), "MUL_MAT_ID uses the general token path");
   using Cfg = DecodeCfg<NT, MT, KW, STAGES>;
   constexpr int kBM = Cfg::kBM;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -158,6 +165,26 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
   const int ntiles = (M + kBM - 1) / kBM;
   const int nchunks = (K + KX - 1) / KX;
   const int stages_per_chunk = KX / Cfg::kStageK;
+  // Groups of this CTA: gk = 0 .. ngrp-1 is group g_first + gk * g_step, and
+  // within it tiles t_first, t_first + t_step, ...
+  int ngrp = 1, g_first = 0, g_step = 1, t_first = static_cast<int>(blockIdx.x), t_step = static_cast<int>(gridDim.x);
+  if (MOE) {
+    pdl_wait();  // the routing tables come from the kernel before
+    const int ng = rt.meta[1], grid = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+    if (ng <= grid) {
+      const int cpg = ng > 0 ? grid / ng : 1;
+      g_first = b / cpg;
+      ngrp = g_first < ng ? 1 : 0;
+      t_first = b % cpg;
+      t_step = cpg;
+    } else {
+      g_first = b;
+      g_step = grid;
+      ngrp = (ng - b + grid - 1) / grid;
+      t_first = 0;
+      t_step = 1;
+    }
+  }
 
   if (threadIdx.x < Cfg::kSlots) slot_count[threadIdx.x] = 0;
   if (threadIdx.x == 0) {
@@ -183,11 +210,13 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
       bool x_waited = early_stages == 0;
       uint32_t q = 0;
       bool ok = true;
+      for (int gk = 0; gk < ngrp && ok; ++gk)
       for (int c = 0; c < nchunks && ok; ++c) {
+        const int wrow0 = MOE ? rt.groups[3 * (g_first + gk * g_step)] * M : 0;
         const int kc0 = c * KX;
         const int kend = min(K, kc0 + KX);
         const int nst = min(stages_per_chunk, (kend - kc0 + Cfg::kStageK - 1) / Cfg::kStageK);
-        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        for (int tile = t_first; tile < ntiles && ok; tile += t_step) {
           for (int st = 0; st < nst; ++st, ++q) {
             const int slot = q % STAGES;
             const uint32_t ph = (q / STAGES) & 1;
@@ -208,8 +237,8 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
             mbar_arrive_expect_tx(full, nvalid * Cfg::kSubBytes);
             for (int j = 0; j < nvalid; ++j) {
               const int xb = ((k0 + j * kSubK) / kSubK) * kSubBytesRow;  // byte column in the row
-              tma_load_2d(smem_u32(ring + slot * Cfg::kStageBytes + j * Cfg::kSubBytes), &tmW, xb, tile * kBM,
-                          full);
+              tma_load_2d(smem_u32(ring + slot * Cfg::kStageBytes + j * Cfg::kSubBytes), &tmW, xb,
+                          wrow0 + tile * kBM, full);
             }
           }
         }
@@ -239,7 +268,17 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
   // not: x_static); Y may still be read by it, so Y is written after the wait.
   if (!x_static) pdl_wait();
 
+  for (int gk = 0; gk < ngrp; ++gk)
   for (int c = 0; c < nchunks; ++c) {
+    // Tokens of this group: Nt (<= N, the layout's width); token n's x and Y
+    // row is xrow(n).
+    int Nt = N, first = 0;
+    if (MOE) {
+      const int* grp = rt.groups + 3 * (g_first + gk * g_step);
+      first = grp[1];
+      Nt = grp[2];
+    }
+    auto xrow = [&](int n) -> size_t { return MOE ? static_cast<size_t>(__ldg(rt.perm + first + n)) : n; };
     const int kc0 = c * KX;
     const int kend = min(K, kc0 + KX);
     const int nst = min(stages_per_chunk, (kend - kc0 + Cfg::kStageK - 1) / Cfg::kStageK);
@@ -253,15 +292,15 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
     __syncwarp();  // this warp's previous chunk of fragments is no longer read
     {
       constexpr int kBoxBlocks = kSubK / kQK;  // 8
-      const int nent = nst * kBoxBlocks * N;   // (stage, block of the box, token) entries of this warp
+      const int nent = nst * kBoxBlocks * Nt;  // (stage, block of the box, token) entries of this warp
       for (int e = lane; e < nent; e += 32) {
-        const int st = e / (kBoxBlocks * N), rem = e % (kBoxBlocks * N);
-        const int bl = st * (Cfg::kStageK / kQK) + kw * kBoxBlocks + rem / N;  // block within the chunk
-        const int n = rem % N;
+        const int st = e / (kBoxBlocks * Nt), rem = e % (kBoxBlocks * Nt);
+        const int bl = st * (Cfg::kStageK / kQK) + kw * kBoxBlocks + rem / Nt;  // block within the chunk
+        const int n = rem % Nt;
         if (kc0 + bl * kQK >= kend) continue;
         float xv[32];
         const float4* xr =
-            reinterpret_cast<const float4*>(X + static_cast<size_t>(n) * K + static_cast<size_t>(kc0 + bl * kQK));
+            reinterpret_cast<const float4*>(X + xrow(n) * K + static_cast<size_t>(kc0 + bl * kQK));
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float4 v = __ldg(xr + i);
@@ -269,13 +308,13 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
         }
         uint4* dst = xs + (bl * N + n) * 4;
         cs[bl * csn + n] = ((kc0 / kQK + bl) & 1) ? stage_block<1>(xv, dst) : stage_block<0>(xv, dst);
-        if ((N & 1) && n == N - 1) cs[bl * csn + N] = 0.f;  // the padding column read by the last lane pair
+        if ((Nt & 1) && n == Nt - 1) cs[bl * csn + Nt] = 0.f;  // the padding column read by the last lane pair
       }
     }
     __syncwarp();
-    if (c == 0 && lane == 0) mbar_arrive(smem_u32(x_ready));
+    if (gk == 0 && c == 0 && lane == 0) mbar_arrive(smem_u32(x_ready));
 
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tile_iter) {
+    for (int tile = t_first; tile < ntiles; tile += t_step, ++tile_iter) {
       float acc[MT][NT][4];
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
@@ -327,9 +366,9 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
               } else {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                  xf[nt] = (nt * 8 + g < N) ? xsp[b * 4 * N + nt * 32] : make_uint4(0u, 0u, 0u, 0u);
-                  nb[nt] = (nt * 8 + 2 * t < N) ? *reinterpret_cast<const float2*>(csp + b * csn + nt * 8)
-                                                : make_float2(0.f, 0.f);
+                  xf[nt] = (nt * 8 + g < Nt) ? xsp[b * 4 * N + nt * 32] : make_uint4(0u, 0u, 0u, 0u);
+                  nb[nt] = (nt * 8 + 2 * t < Nt) ? *reinterpret_cast<const float2*>(csp + b * csn + nt * 8)
+                                                 : make_float2(0.f, 0.f);
                 }
               }
 #pragma unroll
@@ -366,7 +405,7 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
       // STAGES + 1 slots are never reused while still in use.
       const int aslot = tile_iter % Cfg::kSlots;
       float* as = acc_slots + aslot * slot_floats;
-      float* mine = as + kw * kBM * N;
+      float* mine = as + kw * kBM * Nt;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -374,7 +413,7 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int n = nt * 8 + 2 * t + (i & 1);
-            if (n < N) mine[n * kBM + mt * 16 + g + 8 * (i >> 1)] = acc[mt][nt][i];
+            if (n < Nt) mine[n * kBM + mt * 16 + g + 8 * (i >> 1)] = acc[mt][nt][i];
           }
       __syncwarp();
       int prev = 0;
@@ -397,19 +436,19 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
           for (int j = 0; j < kPer; ++j) {
             const int idx = lane + 32 * j;
             const int n = idx / kBM, row = tile * kBM + idx % kBM;
-            yold[j] = (idx < kBM * N && live && row < M) ? Y[static_cast<size_t>(n) * M + row] : 0.f;
+            yold[j] = (idx < kBM * Nt && live && row < M) ? Y[xrow(n) * M + row] : 0.f;
           }
         }
 #pragma unroll
         for (int j = 0; j < kPer; ++j) {
           const int idx = lane + 32 * j;
-          if (idx >= kBM * N) break;
+          if (idx >= kBM * Nt) break;
           const int n = idx / kBM, r = idx % kBM;
           const int row = tile * kBM + r;
           float v = 0.f;
 #pragma unroll
-          for (int w = 0; w < KW; ++w) v += *reinterpret_cast<volatile float*>(&as[(w * N + n) * kBM + r]);
-          if (live && row < M) Y[static_cast<size_t>(n) * M + row] = (c == 0) ? v : (yold[j] + v);
+          for (int w = 0; w < KW; ++w) v += *reinterpret_cast<volatile float*>(&as[(w * Nt + n) * kBM + r]);
+          if (live && row < M) Y[xrow(n) * M + row] = (c == 0) ? v : (yold[j] + v);
         }
         __syncwarp();
         if (lane == 0) {
@@ -426,10 +465,12 @@ int decode_early_stages() { return g_early_stages; }
 int g_x_static = 0;      // the caller promises X is not written by the kernel right before
 int decode_x_static() { return g_x_static; }
 
-template <int NT, int MT, int KW, int STAGES, bool ONE = false>
+template <int NT, int MT, int KW, int STAGES, bool ONE = false, bool MOE = false>
 cudaError_t launch_cfg(const CUtensorMap* tmW, const float* X, int N, int M, int K, float* Y, uint64_t limit_ns,
-                       int xs_budget, int early_w, int pdl, cudaStream_t s) {
-  const int early_stages = early_w ? std::max(1, std::min(STAGES, decode_early_stages())) : 0;
+                       int xs_budget, int early_w, int pdl, cudaStream_t s, const MoeRoute& rt = MoeRoute{},
+                       int64_t max_groups = 0) {
+  // MUL_MAT_ID needs the routing before it knows which weights to stream
+  const int early_stages = (early_w && !MOE) ? std::max(1, std::min(STAGES, decode_early_stages())) : 0;
   using Cfg = DecodeCfg<NT, MT, KW, STAGES>;
   // x chunk: a multiple of the stage width, as long as the budget allows
   int KX = (xs_budget / (2 * N)) / Cfg::kStageK * Cfg::kStageK;
@@ -437,7 +478,7 @@ cudaError_t launch_cfg(const CUtensorMap* tmW, const float* X, int N, int M, int
   const int Kpad = (K + Cfg::kStageK - 1) / Cfg::kStageK * Cfg::kStageK;
   if (KX > Kpad) KX = Kpad;
   const size_t smem = Cfg::smem_bytes(N, KX);
-  auto kern = k_decode_q4_0<NT, MT, KW, STAGES, ONE>;
+  auto kern = k_decode_q4_0<NT, MT, KW, STAGES, ONE, MOE>;
   static int configured_smem = 0;
   static int occ_cache_smem = -1, occ_cache = 1;
   if (static_cast<int>(smem) > configured_smem) {
@@ -458,7 +499,8 @@ cudaError_t launch_cfg(const CUtensorMap* tmW, const float* X, int N, int M, int
   // Small CTAs (two fit on an SM) run one per SM, so that the next launch's
   // CTA can share the SM and overlap this one.
   const int per_sm = (KW <= 4) ? 1 : occ_cache;
-  const int grid = std::min(ntiles, device_info().sm_count * per_sm);
+  const int64_t work = MOE ? ntiles * max_groups : ntiles;
+  const int grid = static_cast<int>(std::min<int64_t>(work, static_cast<int64_t>(device_info().sm_count) * per_sm));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(Cfg::kThreads);
@@ -470,7 +512,7 @@ cudaError_t launch_cfg(const CUtensorMap* tmW, const float* X, int N, int M, int
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, *tmW, X, N, M, K, KX, Y, limit_ns, device_error_word(), early_stages,
-                            decode_x_static());
+                            MOE ? 0 : decode_x_static(), rt);
 }
 
 // -------------------------------------------------------------------------
@@ -549,7 +591,36 @@ cudaError_t launch_decode(const CUtensorMap* tmW, const float* X, int64_t N, int
   }
   if (N <= 16) return launch_cfg<2, 2, 8, 2>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
   if (N <= 32) return launch_cfg<4, 1, 4, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 96 << 10, early_w, pdl, s);
-  return launch_cfg<8, 1, 4, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 48 << 10, early_w, pdl, s);
+  // N = 33..64: two k-warps, so that a stage's x (2 * 512 * N bytes) and the
+  // partial sums fit in shared memory next to the ring
+  return launch_cfg<8, 1, 2, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+}
+
+// MUL_MAT_ID group capacity: room for twice the mean tokens per used expert
+// (an expert with more tokens than that runs as several groups).
+int decode_moe_cap(int64_t P, int64_t E) {
+  const int64_t used = std::max<int64_t>(1, std::min(E, P));
+  const int64_t want = 2 * ((P + used - 1) / used);
+  return want <= 8 ? 8 : want <= 16 ? 16 : want <= 32 ? 32 : 64;
+}
+
+void decode_moe_w_box(int cap, uint32_t* box_x_bytes, uint32_t* box_rows) {
+  *box_x_bytes = kSubBytesRow;
+  *box_rows = cap <= 16 ? 32u : 16u;
+}
+
+cudaError_t launch_decode_moe(const CUtensorMap* tmW, const float* X, int cap, int64_t E, int64_t M, int64_t K,
+                              int64_t P, const MoeRoute& rt, float* Y, uint64_t wait_limit_ns, int pdl,
+                              cudaStream_t s) {
+  const int m = static_cast<int>(M), k = static_cast<int>(K);
+  const int64_t max_groups = std::min(E, P) + P / cap + 1;
+  if (cap == 8)
+    return launch_cfg<1, 2, 8, 3, false, true>(tmW, X, 8, m, k, Y, wait_limit_ns, 64 << 10, 0, pdl, s, rt, max_groups);
+  if (cap == 16)
+    return launch_cfg<2, 2, 8, 2, false, true>(tmW, X, 16, m, k, Y, wait_limit_ns, 64 << 10, 0, pdl, s, rt, max_groups);
+  if (cap == 32)
+    return launch_cfg<4, 1, 4, 4, false, true>(tmW, X, 32, m, k, Y, wait_limit_ns, 96 << 10, 0, pdl, s, rt, max_groups);
+  return launch_cfg<8, 1, 2, 4, false, true>(tmW, X, 64, m, k, Y, wait_limit_ns, 64 << 10, 0, pdl, s, rt, max_groups);
 }
 
 cudaError_t launch_generic(const uint8_t* W, int64_t M, int64_t K, const float* X, int64_t N, float* Y,

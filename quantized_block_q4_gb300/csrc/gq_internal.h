@@ -70,6 +70,38 @@ int get_prefill_bn_override();
 void prefill_boxes(int64_t N, uint32_t* w_box_x_bytes, uint32_t* w_box_rows, uint32_t* x_box_k,
                    uint32_t* x_box_rows);
 
+// ---- KR / KG: MUL_MAT_ID routing and activation gather (gq_moe.cu)
+// Routing tables in device memory, written by the routing kernel.
+struct MoeRoute {
+  int32_t* meta;        // [0] tensor-core work items, [1] decode groups, [2] routed pairs, [3] bad ids
+  int32_t* off;         // [E + 2]: expert e's pairs are perm[off[e] .. off[e+1]); bad ids from off[E]
+  int32_t* item_start;  // [E + 1]: first tensor-core work item (expert, row tile, token tile) of expert e
+  int32_t* groups;      // [3 * max groups]: decode group = (expert, first sorted position, tokens <= cap)
+  int32_t* perm;        // [P]: sorted position -> pair index t * S + s (stable within an expert)
+};
+size_t moe_route_ints(int64_t E, int64_t P, int cap);
+MoeRoute moe_route_layout(int32_t* base, int64_t E, int64_t P, int cap);
+bool moe_route_supported(int64_t E);
+cudaError_t launch_moe_route(const int32_t* ids, int64_t P, int64_t E, int64_t n_mtiles, int bn, int cap,
+                             const MoeRoute& rt, float* Y, int64_t M, cudaStream_t s);
+cudaError_t launch_moe_gather_bf16(const float* X, int64_t P, int64_t K, const MoeRoute& rt, uint16_t* Xg,
+                                   int pdl, cudaStream_t s);
+cudaError_t launch_generic_id(const uint8_t* W, int64_t E, int64_t M, int64_t K, const float* X,
+                              const int32_t* ids, int64_t P, float* Y, cudaStream_t s);
+// Tensor-core MUL_MAT_ID over the routed pairs (gq_prefill.cu): tmW covers the
+// E * M weight rows, tmX the gathered bf16 rows with 64-row boxes.
+constexpr int kMoeBN = 256;   // tokens per tensor-core work item
+cudaError_t launch_prefill_moe(const CUtensorMap* tmW, const CUtensorMap* tmX, int64_t E, int64_t M, int64_t K,
+                               int64_t P, const MoeRoute& rt, float* Y, uint64_t wait_limit_ns, int pdl,
+                               cudaStream_t s);
+// Decode MUL_MAT_ID over the decode groups (gq_decode.cu); returns the group
+// capacity the launch will use through decode_moe_cap first.
+int decode_moe_cap(int64_t P, int64_t E);
+void decode_moe_w_box(int cap, uint32_t* box_x_bytes, uint32_t* box_rows);
+cudaError_t launch_decode_moe(const CUtensorMap* tmW, const float* X, int cap, int64_t E, int64_t M, int64_t K,
+                              int64_t P, const MoeRoute& rt, float* Y, uint64_t wait_limit_ns, int pdl,
+                              cudaStream_t s);
+
 // ---- helpers of the C ABI (gq_api.cu) for entry points defined in other files
 gq_status api_fail(gq_status st, const char* msg);  // records the per-thread error text
 gq_status api_check_device();

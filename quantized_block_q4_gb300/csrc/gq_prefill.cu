@@ -192,6 +192,34 @@ __device__ __forceinline__ Seg seg_of(int g, int i, const PrefillWork& wk) {
   return sg;
 }
 
+// MUL_MAT_ID work item w (items run in (expert, 128-row tile, BN-token tile)
+// order, so the token tiles of one weight tile run side by side and share it
+// in L2): the expert is the last e with item_start[e] <= w.
+struct MoeItem {
+  int wrow;    // first W row among all experts' rows (TMA y)
+  int mrow0;   // first output row within the expert
+  int xrow;    // first gathered x row (sorted position) of the tile
+  int nvalid;  // tokens in the tile (1..BN)
+};
+
+__device__ __forceinline__ MoeItem moe_item(int w, const MoeRoute& rt, int E, int Mexp, int bn) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(rt.item_start + mid) <= w) lo = mid; else hi = mid - 1;
+  }
+  const int local = w - __ldg(rt.item_start + lo);
+  const int first = __ldg(rt.off + lo), cnt = __ldg(rt.off + lo + 1) - first;
+  const int ntn = (cnt + bn - 1) / bn;
+  const int im = local / ntn, j = local - im * ntn;
+  MoeItem it;
+  it.mrow0 = im * 128;
+  it.wrow = lo * Mexp + it.mrow0;
+  it.xrow = first + j * bn;
+  it.nvalid = min(bn, cnt - j * bn);
+  return it;
+}
+
 __device__ __forceinline__ uint32_t scale_pair(uint32_t qp, uint32_t dhi2, uint32_t dlo2) {
   return bfma2_u32(qp, dhi2, bmul2_u32(qp, dlo2));
 }
@@ -242,10 +270,16 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int slots, uint32_t i
   }
 }
 
-template <int BN, bool PAIR>
+// MOE: MUL_MAT_ID over routed pairs (1-CTA tiles only).  M is then the rows of
+// one expert, N is unused, the work items come from rt (item i of the launch
+// goes to CTA i % gridDim.x) and x rows are loaded in 64-row boxes, only as
+// many as the tile's tokens need.
+template <int BN, bool PAIR, bool MOE = false>
 __global__ void __launch_bounds__(PrefillCfg<BN, PAIR>::kThreads, 1)
     k_prefill_q4_0(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int N, int M,
-                   float* __restrict__ Y, const PrefillWork wk, uint64_t limit_ns, uint32_t* err) {
+                   float* __restrict__ Y, const PrefillWork wk, uint64_t limit_ns, uint32_t* err,
+                   const MoeRoute rt, int E) {
+  static_assert(!(MOE && PAIR), "MUL_MAT_ID uses the 1-CTA kernel");
   using C = PrefillCfg<BN, PAIR>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -266,7 +300,11 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR>::kThreads, 1)
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
   const bool leader = rank == 0;
   const int gi = static_cast<int>(blockIdx.x / C::kCtas);
-  const int nseg = seg_count(gi, wk);
+  if (MOE) pdl_wait();  // the routing tables and gathered x come from the kernels before
+  const int nseg = MOE ? (rt.meta[0] > gi ? (rt.meta[0] - gi + static_cast<int>(gridDim.x) - 1) /
+                                                 static_cast<int>(gridDim.x)
+                                           : 0)
+                       : seg_count(gi, wk);
   const int nr = wk.nr;
   // Barriers the leader's MMA thread waits on receive the arrivals of both CTAs.
   auto leader_bar = [&](uint64_t* bar) -> uint32_t { return PAIR ? mapa_shared(smem_u32(bar), 0) : smem_u32(bar); };
@@ -315,8 +353,16 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR>::kThreads, 1)
       uint32_t nraw = 0;
       bool ok = true;
       for (int i = 0; i < nseg && ok; ++i) {
-        const Seg sg = seg_of(gi, i, wk);
-        const int m0 = static_cast<int>(sg.t / wk.ntn) * (C::kBM * C::kCtas) + static_cast<int>(rank) * C::kBM;
+        Seg sg;
+        int m0;
+        if constexpr (MOE) {
+          m0 = moe_item(gi + i * static_cast<int>(gridDim.x), rt, E, M, BN).wrow;
+          sg.r0 = 0;
+          sg.r1 = nr;
+        } else {
+          sg = seg_of(gi, i, wk);
+          m0 = static_cast<int>(sg.t / wk.ntn) * (C::kBM * C::kCtas) + static_cast<int>(rank) * C::kBM;
+        }
         for (int r = sg.r0; r < sg.r1; ++r) {
           const uint32_t slot = nraw % C::RS;
           if (!mbar_wait_bounded(smem_u32(&raw_empty[slot]), ((nraw / C::RS) & 1) ^ 1, limit_ns, abort_flag, err)) {
@@ -337,8 +383,18 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR>::kThreads, 1)
       uint32_t nb = 0;
       bool ok = true;
       for (int i = 0; i < nseg && ok; ++i) {
-        const Seg sg = seg_of(gi, i, wk);
-        const int n0 = static_cast<int>(sg.t % wk.ntn) * BN + static_cast<int>(rank) * C::kXRows;
+        Seg sg;
+        int n0, nbox = 0;
+        if constexpr (MOE) {
+          const MoeItem it = moe_item(gi + i * static_cast<int>(gridDim.x), rt, E, M, BN);
+          sg.r0 = 0;
+          sg.r1 = nr;
+          n0 = it.xrow;
+          nbox = (it.nvalid + 63) / 64;  // 64-row boxes: rows past the tile's tokens are not loaded
+        } else {
+          sg = seg_of(gi, i, wk);
+          n0 = static_cast<int>(sg.t % wk.ntn) * BN + static_cast<int>(rank) * C::kXRows;
+        }
         for (int ks = 4 * sg.r0; ks < 4 * sg.r1; ++ks) {
           const uint32_t bs = nb % C::S;
           if (!mbar_wait_bounded(smem_u32(&empty[bs]), ((nb / C::S) & 1) ^ 1, limit_ns, abort_flag, err)) {
@@ -346,7 +402,11 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR>::kThreads, 1)
             break;
           }
           const uint32_t dst = sbase + C::kOffB + bs * C::kBBytes;
-          if (PAIR) {
+          if constexpr (MOE) {
+            mbar_arrive_expect_tx(smem_u32(&full[bs]), nbox * 64 * 128);
+            for (int b = 0; b < nbox; ++b)
+              tma_load_2d(dst + b * 64 * 128, &tmX, ks * C::kBK, n0 + b * 64, smem_u32(&full[bs]));
+          } else if (PAIR) {
             if (leader) mbar_arrive_expect_tx(smem_u32(&full[bs]), C::kCtas * C::kBBytes);
             tma_load_2d_pair(dst, &tmX, ks * C::kBK, n0, leader_bar(&full[bs]));
           } else {
@@ -362,11 +422,20 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR>::kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (the leader of a pair)
     if (leader && lane == 0) {
-      constexpr uint32_t idesc = umma_idesc_bf16_f32(C::kBM * C::kCtas, BN);
+      uint32_t idesc = umma_idesc_bf16_f32(C::kBM * C::kCtas, BN);
       uint32_t c = 0, seg = 0;
       bool ok = true;
       for (int i = 0; i < nseg && ok; ++i) {
-        const Seg sg = seg_of(gi, i, wk);
+        Seg sg;
+        if constexpr (MOE) {
+          // only the tile's tokens, rounded up to the MMA's N granularity of 16
+          const int nv = moe_item(gi + i * static_cast<int>(gridDim.x), rt, E, M, BN).nvalid;
+          idesc = umma_idesc_bf16_f32(C::kBM, static_cast<uint32_t>((nv + 15) / 16 * 16));
+          sg.r0 = 0;
+          sg.r1 = nr;
+        } else {
+          sg = seg_of(gi, i, wk);
+        }
         // the previous segment's epilogue must have read the accumulator
         if (seg > 0 && !mbar_wait_bounded(smem_u32(acc_empty), (seg - 1) & 1, limit_ns, abort_flag, err)) {
           ok = false;
@@ -425,7 +494,15 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR>::kThreads, 1)
     bool live = true;
     uint32_t cr = 0, c = 0, seg = 0;
     for (int i = 0; i < nseg; ++i) {
-      const Seg sg = seg_of(gi, i, wk);
+      Seg sg;
+      MoeItem it{};
+      if constexpr (MOE) {
+        it = moe_item(gi + i * static_cast<int>(gridDim.x), rt, E, M, BN);
+        sg.r0 = 0;
+        sg.r1 = nr;
+      } else {
+        sg = seg_of(gi, i, wk);
+      }
       for (int r = sg.r0; r < sg.r1; ++r, ++cr, c += 4) {
         const uint32_t rslot = cr % C::RS;
         const uint32_t as = (c + grp) % C::S;
@@ -471,6 +548,32 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR>::kThreads, 1)
       if (live) live = mbar_wait_bounded(smem_u32(acc_full), seg & 1, limit_ns, abort_flag, err);
       live = __all_sync(0xFFFFFFFFu, live);
       tc_fence_after();
+      if constexpr (MOE) {
+        // Column n of the tile is sorted position it.xrow + n; its Y row is
+        // the pair perm[it.xrow + n].  Lane j fetches the pair of column
+        // 32*cb + j and the warp shares them.
+        const int m = it.mrow0 + row;
+        if (live) {
+#pragma unroll 1
+          for (int cb = cb0; cb < cb1 && cb * 32 < it.nvalid; ++cb) {
+            uint32_t v32[32];
+            tmem_ld_32x32b_x32(lane_addr + cb * 32, v32);
+            const int nl = cb * 32 + lane;
+            const int my_pair = nl < it.nvalid ? __ldg(rt.perm + it.xrow + nl) : 0;
+            tmem_ld_wait();
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+              const int pr = __shfl_sync(0xFFFFFFFFu, my_pair, jj);
+              if (m < M && cb * 32 + jj < it.nvalid) Y[static_cast<size_t>(pr) * M + m] = __uint_as_float(v32[jj]);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) arrive_leader(acc_empty);
+        ++seg;
+        continue;
+      }
       const int m = static_cast<int>(sg.t / wk.ntn) * (C::kBM * C::kCtas) + static_cast<int>(rank) * C::kBM + row;
       const int n0 = static_cast<int>(sg.t % wk.ntn) * BN;
       if (sg.r0 == 0 && sg.r1 == nr) {
@@ -663,8 +766,8 @@ cudaError_t launch_prefill_cfg(const CUtensorMap* tmW, const CUtensorMap* tmX, i
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  cudaError_t e =
-      cudaLaunchKernelEx(&cfg, k_prefill_q4_0<BN, PAIR>, *tmW, *tmX, N, M, Y, wk, limit_ns, device_error_word());
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_prefill_q4_0<BN, PAIR>, *tmW, *tmX, N, M, Y, wk, limit_ns,
+                                     device_error_word(), MoeRoute{}, 0);
   if (scratch) {
     cudaError_t f = scratch_free(scratch, s);
     if (e == cudaSuccess) e = f;
@@ -702,6 +805,40 @@ int64_t get_prefill_streamk() { return g_streamk; }
 void set_prefill_slots(int64_t v) { g_slots = v; }
 int64_t get_prefill_slots() { return g_slots; }
 int get_prefill_pair_mode() { return g_pair_mode; }
+
+cudaError_t launch_prefill_moe(const CUtensorMap* tmW, const CUtensorMap* tmX, int64_t E, int64_t M, int64_t K,
+                               int64_t P, const MoeRoute& rt, float* Y, uint64_t wait_limit_ns, int pdl,
+                               cudaStream_t s) {
+  using C = PrefillCfg<kMoeBN, false>;
+  auto kern = k_prefill_q4_0<kMoeBN, false, true>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  // Work items: at most (row tiles) x (token tiles), where the token tiles of
+  // all experts number at most P / BN + min(E, P).
+  const int64_t n_mtiles = (M + C::kBM - 1) / C::kBM;
+  const int64_t max_items = n_mtiles * ((P + kMoeBN - 1) / kMoeBN + std::min(E, P));
+  int64_t G = device_info().sm_count;
+  if (g_slots > 0) G = g_slots;
+  G = std::max<int64_t>(1, std::min(G, max_items));
+  PrefillWork wk{};
+  wk.nr = static_cast<int>(K / C::kRawK);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(G));
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, *tmW, *tmX, 0, static_cast<int>(M), Y, wk, wait_limit_ns,
+                            device_error_word(), rt, static_cast<int>(E));
+}
 
 cudaError_t launch_prefill(const CUtensorMap* tmW, const CUtensorMap* tmX, int64_t N, int64_t M, int64_t K,
                            float* Y, uint64_t wait_limit_ns, bool allow_scratch, cudaStream_t s) {

@@ -13,6 +13,7 @@ namespace gq {
 // and clears it.  Nothing here traps.
 enum : uint32_t {
   DEVERR_TIMEOUT = 1u,  // a bounded wait gave up (mbarrier / TMA / MMA completion)
+  DEVERR_BAD_ID = 2u,   // MUL_MAT_ID: an expert id outside [0, n_expert)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -92,3 +92,22 @@ def blocks_from_parts(d_bits: np.ndarray, qs: np.ndarray) -> np.ndarray:
     out[:, :, 0:2] = d_bits.view(np.uint8).reshape(M, nb, 2)
     out[:, :, 2:] = qs
     return out.reshape(M, nb * BLOCK_BYTES)
+
+
+def expert_ids(T: int, S: int, E: int, seed: int, skew: float = 0.0) -> np.ndarray:
+    """int32 [T, S] expert ids: each token picks S distinct experts out of E
+    (S <= E), as a top-S router does.  skew = 0 draws them uniformly; skew > 0
+    weights expert e by 1 / (e + 1)**skew (Zipf-like: a few experts take most
+    tokens), sampled without replacement by Efraimidis-Spirakis keys u**(1/w)."""
+    if not 0 < S <= E:
+        raise ValueError("need 0 < S <= E")
+    rng = np.random.Generator(np.random.SFC64(seed ^ 0x1D5))
+    u = rng.random((T, E), dtype=np.float64)
+    w = 1.0 / np.power(np.arange(1, E + 1, dtype=np.float64), skew)
+    keys = np.power(u, 1.0 / w)
+    return np.argsort(-keys, axis=1, kind="stable")[:, :S].astype(np.int32)
+
+
+def moe_weights(E: int, M: int, K: int, seed: int) -> np.ndarray:
+    """E Q4_0 matrices of M rows each, one after the other: [E*M, K/32*18]."""
+    return np.concatenate([q4_0_weights(M, K, seed + 7919 * e) for e in range(E)], axis=0)

@@ -68,3 +68,18 @@ def test_argument_errors_before_any_device_work(lib):
     assert L.gq_dequant_q4_0(None, 4, 48, None, None) == lib.GQ_ERR_SHAPE
     assert L.gq_dequant_q4_0(None, 0, 64, None, None) == lib.GQ_OK
     assert L.gq_f32_to_bf16(None, None, -1, None) == lib.GQ_ERR_SHAPE
+    L2 = L.gq_mul_mat_id_q4_0
+    assert L2(None, 0, 4, 32, None, 2, None, 1, None, None) == lib.GQ_ERR_SHAPE          # n_expert < 1
+    assert L2(None, 2, 4, 33, None, 2, None, 1, None, None) == lib.GQ_ERR_SHAPE          # K % 32
+    assert L2(None, 2, 4, 32, None, -1, None, 1, None, None) == lib.GQ_ERR_SHAPE         # negative n_ids
+    assert L2(None, 2, 4, 32, None, 1 << 20, None, 1 << 12, None, None) == lib.GQ_ERR_SHAPE  # T*n_ids >= 2^31
+    assert L2(None, 2, 4, 32, None, 2, None, 0, None, None) == lib.GQ_OK                 # no tokens
+    assert L2(None, 2, 0, 32, None, 2, None, 3, None, None) == lib.GQ_OK                 # no rows
+    assert L2(None, 2, 4, 32, None, 2, None, 3, None, None) == lib.GQ_ERR_NULL
+    assert lib.gq_status_string(-8) == "GQ_ERR_BAD_INDEX"
+    old = lib.gq_get_option(lib.GQ_OPT_MOE_PATH)
+    with pytest.raises(lib.GQError):
+        lib.gq_set_option(lib.GQ_OPT_MOE_PATH, 3)
+    lib.gq_set_option(lib.GQ_OPT_MOE_PATH, 2)
+    assert lib.gq_get_option(lib.GQ_OPT_MOE_PATH) == 2
+    lib.gq_set_option(lib.GQ_OPT_MOE_PATH, old)
