@@ -304,6 +304,8 @@ def run_gpu(args, rank, world, dist):
     # ---- end to end through the public API with host buffers (decode, N = 1)
     e2e = run_e2e(gq, torch, dev, s, W, shapes, acts1, order, L, args)
     aux = run_aux(gq, torch, dev, s, peaks["hbm_gbs"]) if rank == 0 else {}
+    if rank == 0:
+        aux["mul_mat_id"] = run_moe_aux(gq, torch, dev, s, peaks)
     e2e["ms"] = max_over_ranks([e2e["ms"]], dist, dev)[0]
     e2e_value = world * wbytes / (e2e["ms"] * 1e-3) / 1e9
 
@@ -350,6 +352,7 @@ def run_gpu(args, rank, world, dist):
                 "path": "pinned host X -> device, gq_mul_mat_q4_0, Y -> pinned host, per matrix (decode sweep)"},
         "dequant": aux.get("dequant"),
         "quantize": aux.get("quantize"),
+        "mul_mat_id": aux.get("mul_mat_id"),
         "gpu_launches": K_ * (len(shapes) + len(shapes) + L * len(ks)),
         "clocks": clocks,
         "cpu_baseline": cpu,
@@ -394,6 +397,71 @@ def run_aux(gq, torch, dev, s, hbm_gbs):
         out[name] = {"kernel": kern, "shape": f"{M}x{K}", "us": round(t * 1e6, 2), "achieved": round(gbs, 1),
                      "unit": "GB/s", "peak": hbm_gbs, "frac": round(gbs / hbm_gbs, 4), "bound": "hbm",
                      "bytes": qbytes + fbytes, "bytes_note": "4*M*K fp32 + M*K/32*18 Q4_0, one read, one written"}
+    return out
+
+
+# MUL_MAT_ID workloads: experts the shape of the prefill matrix (14336 x 4096),
+# 8 experts, 2 used per token; 512 tokens (the probe batch) and 1 or 8 tokens.
+MOE_E, MOE_M, MOE_K, MOE_S = 8, 14336, 4096, 2
+MOE_SETS, MOE_REPS = 4, 8
+
+
+def moe_weights_dev(torch, dev, rows, K, seed):
+    """Seeded Q4_0 blocks generated on the device: qs uniform random bytes, d =
+    fp16 of U[0.005, 0.02] (the distribution synth.py uses)."""
+    g = torch.Generator(device=dev).manual_seed(seed)
+    nb = K // 32
+    blk = torch.randint(0, 256, (rows, nb, 18), dtype=torch.uint8, device=dev, generator=g)
+    d = (torch.rand((rows, nb), device=dev, generator=g, dtype=torch.float64) * 0.015 + 0.005).to(torch.float16)
+    blk[:, :, 0:2] = d.view(torch.uint8).view(rows, nb, 2)
+    return blk.view(rows, nb * 18)
+
+
+def run_moe_aux(gq, torch, dev, s, peaks):
+    """gq_mul_mat_id_q4_0 on MOE_SETS distinct expert sets (264 MB each), used in
+    turn so that every call streams its experts from DRAM; CUDA events on the
+    bench stream around MOE_REPS calls.  Each call = routing + (gather +
+    tensor-core | decode) kernels."""
+    E, M, K, S = MOE_E, MOE_M, MOE_K, MOE_S
+    Ws = [moe_weights_dev(torch, dev, E * M, K, 0x3E00 + i) for i in range(MOE_SETS)]
+    out = {}
+    for name, T in (("prefill", 512), ("decode", 1), ("decode_t8", 8)):
+        X = torch.randn(T, S, K, device=dev, generator=torch.Generator(device=dev).manual_seed(T))
+        ids = torch.from_numpy(synth.expert_ids(T, S, E, seed=0x1D00 + T)).to(dev)
+        Y = torch.empty(T, S, M, device=dev)
+        used = int(torch.unique(ids).numel())
+
+        def call(i):
+            gq.gq_mul_mat_id_q4_0(Ws[i % MOE_SETS], E, M, K, X, S, ids, T, Y, stream=s)
+
+        with torch.cuda.stream(s):
+            for i in range(MOE_SETS):
+                call(i)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for i in range(MOE_REPS):
+                call(i)
+            e1.record(s)
+        e1.synchronize()
+        gq.gq_sync_status(s)
+        t = e0.elapsed_time(e1) / MOE_REPS * 1e-3
+        P = T * S
+        wbytes = used * M * K // 32 * 18
+        entry = {"shape": f"{E} experts x {M}x{K}, T={T} tokens x {S} slots", "used_experts": used,
+                 "us": round(t * 1e6, 2)}
+        if name == "prefill":
+            tf = 2 * P * M * K / t / 1e12
+            entry.update({"path": "routing + bf16 gather + tcgen05 kernel", "achieved": round(tf, 2),
+                          "unit": "TFLOP/s", "peak": peaks["bf16_tflops"], "bound": "tensor",
+                          "frac": round(tf / peaks["bf16_tflops"], 4), "flops": 2 * P * M * K,
+                          "peak_kind": f"bf16 burst ({peaks['source']})"})
+        else:
+            b = wbytes + 4 * P * K + 4 * P * M
+            gbs = b / t / 1e9
+            entry.update({"path": "routing + decode kernel", "achieved": round(gbs, 1), "unit": "GB/s",
+                          "peak": peaks["hbm_gbs"], "bound": "hbm", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                          "bytes": b, "bytes_note": "used experts' Q4_0 weights + fp32 x and y"})
+        out[name] = entry
     return out
 
 
@@ -465,6 +533,8 @@ PROFILE_CASES = {
     "prefill_small": (4096, 4096, 512, "bf16"),
     "prefill_gate": (11008, 4096, 512, "bf16"),
     "prefill_down": (4096, 11008, 512, "bf16"),
+    "moe_prefill": (MOE_M, MOE_K, 512, "moe"),
+    "moe_decode": (MOE_M, MOE_K, 1, "moe"),
 }
 
 
@@ -476,6 +546,17 @@ def run_profile_case(name, pair=False):
     gq.gq_set_option(gq.GQ_OPT_WEIGHTS_STATIC, 1)
     gq.gq_set_option(gq.GQ_OPT_X_STATIC, 1)
     gq.gq_set_option(gq.GQ_OPT_PREFILL_PAIR, 1 if pair else 0)
+    if mode == "moe":  # MUL_MAT_ID: N tokens x MOE_S slots over MOE_E experts
+        W = moe_weights_dev(torch, "cuda", MOE_E * M, K, 1)
+        X = torch.randn(N, MOE_S, K, device="cuda")
+        ids = torch.from_numpy(synth.expert_ids(N, MOE_S, MOE_E, seed=3)).cuda()
+        Y = torch.empty(N, MOE_S, M, device="cuda")
+        for _ in range(2):
+            gq.gq_mul_mat_id_q4_0(W, MOE_E, M, K, X, MOE_S, ids, N, Y)
+        torch.cuda.synchronize()
+        gq.gq_sync_status()
+        print(f"profile case {name}: {MOE_E} experts {M}x{K}, {N} tokens x {MOE_S} ok")
+        return 0
     W = torch.from_numpy(synth.q4_0_weights(M, K, seed=1)).cuda()
     X = torch.from_numpy(synth.activations(N, K, seed=2)).cuda()
     Y = torch.empty(N, M, device="cuda")
