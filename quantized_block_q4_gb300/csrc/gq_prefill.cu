@@ -423,12 +423,6 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR>::kThreads, 1)
     // ------------------------------------------------------------ MMA issuer (the leader of a pair)
     if (leader && lane == 0) {
       uint32_t idesc = umma_idesc_bf16_f32(C::kBM * C::kCtas, BN);
-      static_assert(C::kBK == 64, "one asm block issues the four 16-k MMAs of a 64-k step");
-      // stage 0's A columns and B descriptor; stage st adds st * 32 columns and
-      // st * kBBytes bytes (the descriptor's address field is bytes / 16 and
-      // stays below 2^14 for any shared-memory address)
-      const uint32_t a_tmem0 = tmem_base + BN;
-      const uint64_t b_desc0 = umma_desc_sw128(sbase + C::kOffB);
       uint32_t c = 0, seg = 0;
       bool ok = true;
       for (int i = 0; i < nseg && ok; ++i) {
@@ -449,19 +443,22 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR>::kThreads, 1)
         }
         tc_fence_after();
         for (int ks = 4 * sg.r0; ks < 4 * sg.r1; ++ks, ++c) {
-          // Operands of this step first, then the wait, then nothing but the
-          // four MMAs and the commit: the issuing thread shares its scheduler
-          // with dequantising warps, so every instruction here costs.
           const uint32_t st = c % C::S;
-          const uint32_t a_tmem = a_tmem0 + st * C::kACols;
-          const uint64_t b_desc = b_desc0 + st * (C::kBBytes >> 4);
-          const uint32_t acc0 = ks != 4 * sg.r0;
           if (!mbar_wait_bounded(smem_u32(&full[st]), (c / C::S) & 1, limit_ns, abort_flag, err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          umma_bf16_ts_k64<C::kCtas>(tmem_base, a_tmem, b_desc, idesc, acc0);
+          const uint32_t a_tmem = tmem_base + BN + st * C::kACols;
+          const uint32_t b_addr = sbase + C::kOffB + st * C::kBBytes;
+#pragma unroll
+          for (int kk = 0; kk < C::kBK / 16; ++kk) {
+            const uint32_t acc = ks != 4 * sg.r0 || kk != 0;
+            if (PAIR)
+              umma_bf16_ts_pair(tmem_base, a_tmem + kk * 8, umma_desc_sw128(b_addr + kk * 32), idesc, acc);
+            else
+              umma_bf16_ts(tmem_base, a_tmem + kk * 8, umma_desc_sw128(b_addr + kk * 32), idesc, acc);
+          }
           if (PAIR)
             umma_commit_pair(smem_u32(&empty[st]), 3);
           else

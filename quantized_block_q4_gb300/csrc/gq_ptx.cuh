@@ -241,41 +241,6 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t tmem_d, uint32_t tmem_a, u
       : "memory");
 }
 
-// One 64-k step: four MMAs over consecutive 16-k slices, A from TMEM columns
-// a, a+8, a+16, a+24 and B from descriptors b, b+2, b+4, b+6 (32 bytes apart
-// in the 128-byte swizzled rows).  The first MMA accumulates iff acc0 != 0,
-// the others always.  One asm block, so the issuing thread spends as few
-// instructions as possible between the MMAs.
-template <int CTA_GROUP>
-__device__ __forceinline__ void umma_bf16_ts_k64(uint32_t tmem_d, uint32_t a, uint64_t b, uint32_t idesc,
-                                                 uint32_t acc0) {
-  static_assert(CTA_GROUP == 1 || CTA_GROUP == 2, "cta_group is 1 or 2");
-  if (CTA_GROUP == 1)
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t.reg .b32 a1, a2, a3;\n\t.reg .b64 b1, b2, b3;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, %3, %3;\n\t"
-        "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
-        "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, q;\n\t}" ::"r"(tmem_d),
-        "r"(a), "l"(b), "r"(idesc), "r"(acc0)
-        : "memory");
-  else
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t.reg .b32 a1, a2, a3;\n\t.reg .b64 b1, b2, b3;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, %3, %3;\n\t"
-        "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
-        "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], [a1], b1, %3, q;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], [a2], b2, %3, q;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], [a3], b3, %3, q;\n\t}" ::"r"(tmem_d),
-        "r"(a), "l"(b), "r"(idesc), "r"(acc0)
-        : "memory");
-}
-
 // Arrive once on an mbarrier when all prior tcgen05 ops of this thread finish.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
