@@ -69,6 +69,12 @@ class Oracle:
         lib.oracle_quantize_q4_0.restype = None
         lib.oracle_mul_mat_id_q4_0.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, vp, i32]
         lib.oracle_mul_mat_id_q4_0.restype = None
+        lib.oracle_type_nbytes.argtypes = [i32, i64, i64]
+        lib.oracle_type_nbytes.restype = sz
+        lib.oracle_dequant_typed.argtypes = [i32, vp, i64, i64, vp]
+        lib.oracle_dequant_typed.restype = None
+        lib.oracle_mul_mat_typed.argtypes = [i32, vp, i64, i64, vp, i64, vp, vp, i32]
+        lib.oracle_mul_mat_typed.restype = None
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = i32
         self.lib = lib
@@ -141,8 +147,37 @@ class Oracle:
                                         Y.ctypes.data, Sa.ctypes.data, int(nthreads))
         return Y, Sa
 
+    def type_nbytes(self, qtype: int, M: int, K: int) -> int:
+        return int(self.lib.oracle_type_nbytes(qtype, M, K))
+
+    def dequant_typed(self, qtype: int, W: np.ndarray, M: int, K: int) -> np.ndarray:
+        W = np.ascontiguousarray(W, dtype=np.uint8)
+        if W.size != self.type_nbytes(qtype, M, K):
+            raise ValueError("W has the wrong number of bytes")
+        out = np.empty((M, K), dtype=np.float32)
+        self.lib.oracle_dequant_typed(qtype, W.ctypes.data, M, K, out.ctypes.data)
+        return out
+
+    def mul_mat_typed(self, qtype: int, W: np.ndarray, M: int, K: int, X: np.ndarray, nthreads: int = 1):
+        """Returns (Y, S), both fp64 [N][M]."""
+        W = np.ascontiguousarray(W, dtype=np.uint8)
+        X = np.ascontiguousarray(X, dtype=np.float32)
+        if W.size != self.type_nbytes(qtype, M, K):
+            raise ValueError("W has the wrong number of bytes")
+        N = X.shape[0]
+        Y = np.empty((N, M), dtype=np.float64)
+        S = np.empty((N, M), dtype=np.float64)
+        self.lib.oracle_mul_mat_typed(qtype, W.ctypes.data, M, K, X.ctypes.data, N, Y.ctypes.data,
+                                      S.ctypes.data, int(nthreads))
+        return Y, S
+
     def max_threads(self) -> int:
         return int(self.lib.oracle_max_threads())
+
+
+# Block formats of the typed functions (the same numbering as the library's gq_type).
+TYPE_Q4_0, TYPE_Q4_1, TYPE_Q8_0 = 0, 1, 2
+BLOCK_BYTES = {TYPE_Q4_0: 18, TYPE_Q4_1: 20, TYPE_Q8_0: 34}
 
 
 def get() -> Oracle:

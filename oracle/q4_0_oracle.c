@@ -237,3 +237,101 @@ void oracle_mul_mat_id_q4_0(const uint8_t *W, int64_t n_expert, int64_t M, int64
                                 y, sa, nthreads);
         }
 }
+
+/*
+ * The other legacy formats ("Architecture and module overview", the
+ * quantisation-format section: 32 weights per block sharing one scale; Q4_1
+ * additionally stores a min offset; Q8_0 is the 8-bit member).  The pages do
+ * not print their structs; the readings (stated in the header) are:
+ *   Q4_1: fp16 d, fp16 m, uint8_t qs[16]  (20 bytes); w = d*q + m, q = 0..15,
+ *         low nibble of qs[j] = element j, high nibble = element j+16.
+ *   Q8_0: fp16 d, int8_t qs[32]           (34 bytes); w = d*q, q = -128..127,
+ *         qs[j] = element j.
+ * Both fp16 fields are little-endian.  In fp32: d*q is exact (at most 11 x 8
+ * significant bits); Q4_1 then adds m with one rounding.
+ */
+static int type_block_bytes(int type)
+{
+    switch (type) {
+    case ORACLE_TYPE_Q4_0: return 18;
+    case ORACLE_TYPE_Q4_1: return 20;
+    case ORACLE_TYPE_Q8_0: return 34;
+    default: return 0;
+    }
+}
+
+size_t oracle_type_nbytes(int type, int64_t M, int64_t K)
+{
+    return (size_t)M * (size_t)(K / QK) * (size_t)type_block_bytes(type);
+}
+
+static float le_half(const uint8_t *p)
+{
+    return (float)oracle_half_to_double((uint16_t)(p[0] | (p[1] << 8)));
+}
+
+static void dequant_row_typed(int type, const uint8_t *row, int64_t K, float *w)
+{
+    int64_t nb = K / QK;
+    int bb = type_block_bytes(type);
+    if (type == ORACLE_TYPE_Q4_0) {
+        dequant_row(row, K, w);
+        return;
+    }
+    for (int64_t b = 0; b < nb; ++b) {
+        const uint8_t *blk = row + b * bb;
+        float *wb = w + b * QK;
+        float d = le_half(blk);
+        if (type == ORACLE_TYPE_Q4_1) {
+            float m = le_half(blk + 2);
+            const uint8_t *qs = blk + 4;
+            for (int j = 0; j < 16; ++j) {
+                float lo = d * (float)(qs[j] & 0x0F);
+                float hi = d * (float)(qs[j] >> 4);
+                wb[j] = lo + m;
+                wb[j + 16] = hi + m;
+            }
+        } else {  /* Q8_0 */
+            const uint8_t *qs = blk + 2;
+            for (int j = 0; j < QK; ++j) {
+                int q = qs[j] < 128 ? (int)qs[j] : (int)qs[j] - 256;   /* two's complement */
+                wb[j] = d * (float)q;
+            }
+        }
+    }
+}
+
+void oracle_dequant_typed(int type, const uint8_t *W, int64_t M, int64_t K, float *out)
+{
+    size_t row_bytes = (size_t)(K / QK) * (size_t)type_block_bytes(type);
+    for (int64_t m = 0; m < M; ++m)
+        dequant_row_typed(type, W + (size_t)m * row_bytes, K, out + (size_t)m * (size_t)K);
+}
+
+void oracle_mul_mat_typed(int type, const uint8_t *W, int64_t M, int64_t K, const float *X, int64_t N,
+                          double *Y, double *S, int nthreads)
+{
+    size_t row_bytes = (size_t)(K / QK) * (size_t)type_block_bytes(type);
+    if (nthreads < 1)
+        nthreads = 1;
+    (void)nthreads;
+#ifdef _OPENMP
+#pragma omp parallel for num_threads(nthreads) schedule(dynamic, 4)
+#endif
+    for (int64_t m = 0; m < M; ++m) {
+        float *w = (float *)malloc((size_t)(K > 0 ? K : 1) * sizeof(float));
+        dequant_row_typed(type, W + (size_t)m * row_bytes, K, w);
+        for (int64_t n = 0; n < N; ++n) {
+            const float *x = X + (size_t)n * (size_t)K;
+            double acc = 0.0, acc_abs = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double p = (double)w[k] * (double)x[k];
+                acc += p;
+                acc_abs += fabs(p);
+            }
+            Y[(size_t)n * (size_t)M + (size_t)m] = acc;
+            S[(size_t)n * (size_t)M + (size_t)m] = acc_abs;
+        }
+        free(w);
+    }
+}

@@ -88,6 +88,20 @@ void oracle_mul_mat_id_q4_0(const uint8_t *W, int64_t n_expert, int64_t M, int64
                             const float *X, int64_t S, const int32_t *ids, int64_t T,
                             double *Y, double *S_abs, int nthreads);
 
+/*
+ * The other legacy formats of the quantisation-format section of
+ * "Architecture and module overview" (32 weights per block, one scale; Q4_1
+ * also a min offset; Q8_0 eight bits).  The pages do not print their structs;
+ * the reading: Q4_1 = fp16 d, fp16 m, qs[16] (20 bytes), w = d*q + m with q =
+ * 0..15 in the Q4_0 nibble order; Q8_0 = fp16 d, int8 qs[32] (34 bytes), w =
+ * d*q.  ORACLE_TYPE_Q4_0 is the Q4_0 functions above.
+ */
+enum { ORACLE_TYPE_Q4_0 = 0, ORACLE_TYPE_Q4_1 = 1, ORACLE_TYPE_Q8_0 = 2 };
+size_t oracle_type_nbytes(int type, int64_t M, int64_t K);
+void oracle_dequant_typed(int type, const uint8_t *W, int64_t M, int64_t K, float *out);
+void oracle_mul_mat_typed(int type, const uint8_t *W, int64_t M, int64_t K, const float *X, int64_t N,
+                          double *Y, double *S, int nthreads);
+
 /* Number of threads OpenMP would use by default (1 without OpenMP). */
 int oracle_max_threads(void);
 

@@ -111,3 +111,27 @@ def expert_ids(T: int, S: int, E: int, seed: int, skew: float = 0.0) -> np.ndarr
 def moe_weights(E: int, M: int, K: int, seed: int) -> np.ndarray:
     """E Q4_0 matrices of M rows each, one after the other: [E*M, K/32*18]."""
     return np.concatenate([q4_0_weights(M, K, seed + 7919 * e) for e in range(E)], axis=0)
+
+
+def typed_weights(qtype: int, M: int, K: int, seed: int) -> np.ndarray:
+    """Weights in one of the legacy block formats, as raw bytes [M, K/32*bytes]:
+    0 = Q4_0 (q4_0_weights), 1 = Q4_1 (fp16 d ~ U[0.005, 0.02], fp16 m ~
+    U[-0.16, 0], 16 random code bytes), 2 = Q8_0 (fp16 d ~ U[0.0003, 0.0012],
+    32 random int8 code bytes).  Scales are RNE fp16 of values drawn in fp64."""
+    if qtype == 0:
+        return q4_0_weights(M, K, seed)
+    if K % QK4_0:
+        raise ValueError("K must be a multiple of 32")
+    nb = K // QK4_0
+    if qtype == 1:
+        out = np.empty((M, nb, 20), dtype=np.uint8)
+        out[:, :, 4:] = random_bytes(seed, M * nb * 16).reshape(M, nb, 16)
+        out[:, :, 0:2] = random_scales(seed, M * nb).view(np.uint8).reshape(M, nb, 2)
+        out[:, :, 2:4] = random_scales(seed ^ 0x3117, M * nb, -0.16, 0.0).view(np.uint8).reshape(M, nb, 2)
+        return out.reshape(M, nb * 20)
+    if qtype == 2:
+        out = np.empty((M, nb, 34), dtype=np.uint8)
+        out[:, :, 2:] = random_bytes(seed, M * nb * 32).reshape(M, nb, 32)
+        out[:, :, 0:2] = random_scales(seed, M * nb, 0.0003, 0.0012).view(np.uint8).reshape(M, nb, 2)
+        return out.reshape(M, nb * 34)
+    raise ValueError("unknown block type")

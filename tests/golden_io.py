@@ -34,6 +34,27 @@ def read_blocks(name: str = "q4_0_blocks.txt"):
     return out
 
 
+def read_typed_blocks(name: str = "legacy_blocks.txt"):
+    """List of (type name, block name, raw bytes, 32 expected fp32 values)."""
+    out, cur, typ = [], {}, None
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, _, rest = line.partition(" ")
+            if key == "type":
+                typ = rest
+            elif key == "block":
+                cur = {"name": rest}
+            elif key == "bytes":
+                cur["bytes"] = np.frombuffer(bytes.fromhex(rest), dtype=np.uint8)
+            elif key == "values":
+                cur["values"] = np.array([_float(t) for t in rest.split()], dtype=np.float32)
+                out.append((typ, cur["name"], cur["bytes"], cur["values"]))
+    return out
+
+
 def read_mul_mat(name: str = "q4_0_mul_mat_small.txt"):
     rec = {"W": [], "X": [], "Y": [], "S": []}
     with open(os.path.join(GOLDEN, name)) as f:
