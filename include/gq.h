@@ -53,6 +53,17 @@ typedef enum {
                                   (reported by gq_sync_status) */
 } gq_status;
 
+/* Block formats of the typed entry points ("Architecture and module
+ * overview", quantisation-format section: the legacy formats, 32 weights per
+ * block with one scale; Q4_1 also stores a min offset; Q8_0 has 8-bit codes).
+ * The pages print only the Q4_0 struct; the layouts taken for the others:
+ *   GQ_TYPE_Q4_0  fp16 d, uint8_t qs[16]          18 bytes  w = d*(q - 8)
+ *   GQ_TYPE_Q4_1  fp16 d, fp16 m, uint8_t qs[16]  20 bytes  w = d*q + m
+ *   GQ_TYPE_Q8_0  fp16 d, int8_t qs[32]           34 bytes  w = d*q
+ * (fp16 little-endian; 4-bit codes: low nibble of qs[j] = element j, high
+ * nibble = element j+16; Q8_0: qs[j] = element j). */
+typedef enum { GQ_TYPE_Q4_0 = 0, GQ_TYPE_Q4_1 = 1, GQ_TYPE_Q8_0 = 2 } gq_type;
+
 /* Bytes of a Q4_0 matrix of M rows and K columns: M*(K/32)*18
  * ("Binding GGUF weights to the compute graph", section 2.3, ggml_nbytes note).
  * Returns 0 for K % 32 != 0 or negative sizes. */
@@ -76,6 +87,26 @@ gq_status gq_dequant_q4_0(const void *W, int64_t M, int64_t K, float *out, void 
  * Device pointers; W 4-byte aligned (16 bytes takes the vector path); errors:
  * K % 32 != 0 or negative sizes -> GQ_ERR_SHAPE, NULL -> GQ_ERR_NULL. */
 gq_status gq_quantize_q4_0(const float *W, int64_t M, int64_t K, void *out, void *stream);
+
+/* Bytes of an M x K matrix in block format `type`: M*(K/32)*block bytes; 0 for
+ * K % 32 != 0, negative sizes or an unknown type. */
+size_t gq_type_nbytes(gq_type type, int64_t M, int64_t K);
+
+/* Dequantise W (M x K in block format `type`) into out[M][K] fp32, bit-exact:
+ * d*q is exact in fp32 and Q4_1 adds m with one rounding (round to nearest
+ * even).  GQ_TYPE_Q4_0 is gq_dequant_q4_0.  Any alignment (16-byte aligned W
+ * and out take vector loads and stores); errors as gq_dequant_q4_0, plus
+ * GQ_ERR_SHAPE for an unknown type. */
+gq_status gq_dequant(gq_type type, const void *W, int64_t M, int64_t K, float *out, void *stream);
+
+/* MUL_MAT with W in block format `type`: Y[N][M] = X[N][K] * W^T, fp32 in and
+ * out.  GQ_TYPE_Q4_0 is gq_mul_mat_q4_0.  Q4_1 and Q8_0 run one kernel for
+ * every N: a warp per weight row decodes the blocks to fp32 in registers and
+ * accumulates in fp32, 4 tokens per pass over the row (W is streamed from
+ * DRAM once per pass and re-read from L2 after it).  Any alignment and K % 32
+ * == 0; M, N == 0 no-op, K == 0 zeros.  Accuracy as gq_mul_mat_q4_0. */
+gq_status gq_mul_mat(gq_type type, const void *W, int64_t M, int64_t K, const float *X, int64_t N, float *Y,
+                     void *stream);
 
 /* Y[N][M] = X[N][K] * W^T with W in Q4_0, fp32 in and out (see header).
  * Dispatch by N: N < 16 streams W through the decode kernel (fp16 x, exact

@@ -29,6 +29,9 @@ GQ_ERR_DEVICE_TIMEOUT = -6
 GQ_ERR_UNSUPPORTED = -7
 GQ_ERR_BAD_INDEX = -8
 
+GQ_TYPE_Q4_0, GQ_TYPE_Q4_1, GQ_TYPE_Q8_0 = 0, 1, 2
+TYPE_BLOCK_BYTES = {GQ_TYPE_Q4_0: 18, GQ_TYPE_Q4_1: 20, GQ_TYPE_Q8_0: 34}
+
 GQ_OPT_PREFILL_MIN_N = 0
 GQ_OPT_FORCE_GENERIC = 1
 GQ_OPT_WAIT_LIMIT_NS = 2
@@ -48,6 +51,9 @@ _i64, _sz, _vp, _i32 = ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.
 SIGNATURES = {
     "gq_q4_0_nbytes": (_sz, [_i64, _i64]),
     "gq_dequant_q4_0": (_i32, [_vp, _i64, _i64, _vp, _vp]),
+    "gq_type_nbytes": (_sz, [_i32, _i64, _i64]),
+    "gq_dequant": (_i32, [_i32, _vp, _i64, _i64, _vp, _vp]),
+    "gq_mul_mat": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "gq_quantize_q4_0": (_i32, [_vp, _i64, _i64, _vp, _vp]),
     "gq_mul_mat_q4_0": (_i32, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "gq_mul_mat_id_q4_0": (_i32, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp]),
@@ -119,6 +125,18 @@ def gq_q4_0_nbytes(M: int, K: int) -> int:
 
 def gq_dequant_q4_0(W, M: int, K: int, out, stream=None) -> None:
     _check(_lib.gq_dequant_q4_0(_ptr(W), M, K, _ptr(out), _stream(stream)))
+
+
+def gq_type_nbytes(qtype: int, M: int, K: int) -> int:
+    return int(_lib.gq_type_nbytes(qtype, M, K))
+
+
+def gq_dequant(qtype: int, W, M: int, K: int, out, stream=None) -> None:
+    _check(_lib.gq_dequant(qtype, _ptr(W), M, K, _ptr(out), _stream(stream)))
+
+
+def gq_mul_mat(qtype: int, W, M: int, K: int, X, N: int, Y, stream=None) -> None:
+    _check(_lib.gq_mul_mat(qtype, _ptr(W), M, K, _ptr(X), N, _ptr(Y), _stream(stream)))
 
 
 def gq_quantize_q4_0(W, M: int, K: int, out, stream=None) -> None:
@@ -231,4 +249,34 @@ def mul_mat_id_q4_0(W: torch.Tensor, n_expert: int, X: torch.Tensor, ids: torch.
     M = rows // n_expert
     Y = out if out is not None else torch.empty((T, S, M), dtype=torch.float32, device=X.device)
     gq_mul_mat_id_q4_0(W, n_expert, M, K, X, S, ids, T, Y, stream)
+    return Y
+
+
+def _rows_of(W: torch.Tensor, qtype: int, K: int) -> int:
+    if W.dtype != torch.uint8:
+        raise TypeError("W must be uint8 (raw blocks)")
+    if K % 32 or K <= 0:
+        raise ValueError("K must be a positive multiple of 32")
+    row = K // 32 * TYPE_BLOCK_BYTES[qtype]
+    if W.numel() % row:
+        raise ValueError("W size is not a whole number of rows")
+    return W.numel() // row
+
+
+def dequant(qtype: int, W: torch.Tensor, K: int, stream=None) -> torch.Tensor:
+    """W: uint8 rows of blocks of type qtype -> float32 [M, K] (bit-exact)."""
+    M = _rows_of(W, qtype, K)
+    out = torch.empty((M, K), dtype=torch.float32, device=W.device)
+    gq_dequant(qtype, W, M, K, out, stream)
+    return out
+
+
+def mul_mat(qtype: int, W: torch.Tensor, X: torch.Tensor, stream=None, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Y[N, M] = X[N, K] @ dequant(W)^T for W in block format qtype."""
+    if X.dtype != torch.float32 or X.dim() != 2:
+        raise TypeError("X must be float32 [N, K]")
+    N, K = X.shape
+    M = _rows_of(W, qtype, K)
+    Y = out if out is not None else torch.empty((N, M), dtype=torch.float32, device=X.device)
+    gq_mul_mat(qtype, W, M, K, X, N, Y, stream)
     return Y

@@ -247,6 +247,51 @@ gq_status gq_dequant_q4_0(const void* W, int64_t M, int64_t K, float* out, void*
   return e == cudaSuccess ? GQ_OK : cuda_fail(e, "dequant launch");
 }
 
+size_t gq_type_nbytes(gq_type type, int64_t M, int64_t K) {
+  const int bb = type_block_bytes(type);
+  if (bb == 0 || M < 0 || K < 0 || K % kQK) return 0;
+  return static_cast<size_t>(M) * static_cast<size_t>(K / kQK) * static_cast<size_t>(bb);
+}
+
+gq_status gq_dequant(gq_type type, const void* W, int64_t M, int64_t K, float* out, void* stream) {
+  if (type == GQ_TYPE_Q4_0) return gq_dequant_q4_0(W, M, K, out, stream);
+  t_last_error.clear();
+  if (type_block_bytes(type) == 0) return fail(GQ_ERR_SHAPE, "unknown block type %d", static_cast<int>(type));
+  if (M < 0 || K < 0) return fail(GQ_ERR_SHAPE, "negative size");
+  if (K % kQK) return fail(GQ_ERR_SHAPE, "K=%lld is not a multiple of 32", (long long)K);
+  if (M == 0 || K == 0) return GQ_OK;
+  if (!W || !out) return fail(GQ_ERR_NULL, "W and out must not be NULL");
+  if ((unsigned __int128)M * K * 4 > ((unsigned __int128)1 << 62)) return fail(GQ_ERR_SHAPE, "size overflows");
+  if (!aligned(out, 4)) return fail(GQ_ERR_ALIGN, "out must be 4-byte aligned");
+  gq_status st = check_device();
+  if (st != GQ_OK) return st;
+  cudaError_t e = launch_dequant_legacy(type, static_cast<const uint8_t*>(W), M * (K / kQK), out,
+                                        static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GQ_OK : cuda_fail(e, "dequant launch");
+}
+
+gq_status gq_mul_mat(gq_type type, const void* W, int64_t M, int64_t K, const float* X, int64_t N, float* Y,
+                     void* stream) {
+  if (type == GQ_TYPE_Q4_0) return gq_mul_mat_q4_0(W, M, K, X, N, Y, stream);
+  t_last_error.clear();
+  if (type_block_bytes(type) == 0) return fail(GQ_ERR_SHAPE, "unknown block type %d", static_cast<int>(type));
+  gq_status st = check_mm_shape(M, K, N);
+  if (st != GQ_OK) return st;
+  if (M == 0 || N == 0) return GQ_OK;
+  if (!Y) return fail(GQ_ERR_NULL, "Y must not be NULL");
+  st = check_device();
+  if (st != GQ_OK) return st;
+  auto s = static_cast<cudaStream_t>(stream);
+  if (K == 0) {
+    cudaError_t e = cudaMemsetAsync(Y, 0, static_cast<size_t>(N) * M * sizeof(float), s);
+    return e == cudaSuccess ? GQ_OK : cuda_fail(e, "memset");
+  }
+  if (!W || !X) return fail(GQ_ERR_NULL, "W and X must not be NULL");
+  if (!aligned(X, 4) || !aligned(Y, 4)) return fail(GQ_ERR_ALIGN, "X and Y must be 4-byte aligned");
+  cudaError_t e = launch_mul_mat_legacy(type, static_cast<const uint8_t*>(W), M, K, X, N, Y, s);
+  return e == cudaSuccess ? GQ_OK : cuda_fail(e, "mul_mat launch");
+}
+
 gq_status gq_quantize_q4_0(const float* W, int64_t M, int64_t K, void* out, void* stream) {
   t_last_error.clear();
   if (M < 0 || K < 0) return fail(GQ_ERR_SHAPE, "negative size");

@@ -102,6 +102,12 @@ cudaError_t launch_decode_moe(const CUtensorMap* tmW, const float* X, int cap, i
                               int64_t P, const MoeRoute& rt, float* Y, uint64_t wait_limit_ns, int pdl,
                               cudaStream_t s);
 
+// ---- KL: Q4_1 / Q8_0 dequantisation and MUL_MAT (gq_legacy.cu)
+int type_block_bytes(int type);  // 18 / 20 / 34, 0 for an unknown type
+cudaError_t launch_dequant_legacy(int type, const uint8_t* W, int64_t nblocks, float* out, cudaStream_t s);
+cudaError_t launch_mul_mat_legacy(int type, const uint8_t* W, int64_t M, int64_t K, const float* X, int64_t N,
+                                  float* Y, cudaStream_t s);
+
 // ---- helpers of the C ABI (gq_api.cu) for entry points defined in other files
 gq_status api_fail(gq_status st, const char* msg);  // records the per-thread error text
 gq_status api_check_device();
