@@ -306,6 +306,7 @@ def run_gpu(args, rank, world, dist):
     aux = run_aux(gq, torch, dev, s, peaks["hbm_gbs"]) if rank == 0 else {}
     if rank == 0:
         aux["mul_mat_id"] = run_moe_aux(gq, torch, dev, s, peaks)
+        aux["legacy_formats"] = run_legacy_aux(gq, torch, dev, s, peaks)
     e2e["ms"] = max_over_ranks([e2e["ms"]], dist, dev)[0]
     e2e_value = world * wbytes / (e2e["ms"] * 1e-3) / 1e9
 
@@ -353,6 +354,7 @@ def run_gpu(args, rank, world, dist):
         "dequant": aux.get("dequant"),
         "quantize": aux.get("quantize"),
         "mul_mat_id": aux.get("mul_mat_id"),
+        "legacy_formats": aux.get("legacy_formats"),
         "gpu_launches": K_ * (len(shapes) + len(shapes) + L * len(ks)),
         "clocks": clocks,
         "cpu_baseline": cpu,
@@ -462,6 +464,54 @@ def run_moe_aux(gq, torch, dev, s, peaks):
                           "peak": peaks["hbm_gbs"], "bound": "hbm", "frac": round(gbs / peaks["hbm_gbs"], 4),
                           "bytes": b, "bytes_note": "used experts' Q4_0 weights + fp32 x and y"})
         out[name] = entry
+    return out
+
+
+def run_legacy_aux(gq, torch, dev, s, peaks):
+    """Q4_1 and Q8_0 on the 14336 x 4096 matrix: dequant (GB/s), MUL_MAT at
+    N = 1 (weight GB/s) and N = 512 (TFLOP/s), CUDA events over repeated calls
+    on rotating weight copies (each copy streamed from DRAM)."""
+    M, K = MOE_M, MOE_K
+    out = {}
+    for name, qt in (("q4_1", gq.GQ_TYPE_Q4_1), ("q8_0", gq.GQ_TYPE_Q8_0)):
+        nbytes = gq.gq_type_nbytes(qt, M, K)
+        W0 = torch.from_numpy(synth.typed_weights(qt, M, K, seed=0x7E00 + qt)).to(dev)
+        Ws = [W0.clone() for _ in range(3)]
+        D = torch.empty(M, K, device=dev)
+        X1 = torch.randn(1, K, device=dev)
+        XP = torch.randn(512, K, device=dev)
+        Y1 = torch.empty(1, M, device=dev)
+        YP = torch.empty(512, M, device=dev)
+
+        def timed(fn, reps=6):
+            with torch.cuda.stream(s):
+                for i in range(3):
+                    fn(i)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(s)
+                for i in range(reps):
+                    fn(i)
+                e1.record(s)
+            e1.synchronize()
+            return e0.elapsed_time(e1) / reps * 1e-3
+
+        td = timed(lambda i: gq.gq_dequant(qt, Ws[i % 3], M, K, D, stream=s))
+        t1 = timed(lambda i: gq.gq_mul_mat(qt, Ws[i % 3], M, K, X1, 1, Y1, stream=s))
+        tp = timed(lambda i: gq.gq_mul_mat(qt, Ws[i % 3], M, K, XP, 512, YP, stream=s))
+        gq.gq_sync_status(s)
+        dq = (nbytes + 4 * M * K) / td / 1e9
+        g1 = (nbytes + 4 * K + 4 * M) / t1 / 1e9
+        tf = 2 * M * K * 512 / tp / 1e12
+        out[name] = {
+            "shape": f"{M}x{K}", "block_bytes": gq.TYPE_BLOCK_BYTES[qt],
+            "dequant": {"us": round(td * 1e6, 2), "achieved": round(dq, 1), "unit": "GB/s", "bound": "hbm",
+                        "frac": round(dq / peaks["hbm_gbs"], 4)},
+            "mul_mat_n1": {"us": round(t1 * 1e6, 2), "achieved": round(g1, 1), "unit": "GB/s", "bound": "hbm",
+                           "frac": round(g1 / peaks["hbm_gbs"], 4), "kernel": "k_mul_mat_legacy_bulk (scalar)"},
+            "mul_mat_n512": {"us": round(tp * 1e6, 2), "achieved": round(tf, 2), "unit": "TFLOP/s",
+                             "bound": "tensor", "frac": round(tf / peaks["bf16_tflops"], 4),
+                             "kernel": "k_f32_to_bf16 + k_prefill_q4_0<256, 0, 0, type>"},
+        }
     return out
 
 

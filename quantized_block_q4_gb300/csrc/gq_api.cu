@@ -197,19 +197,19 @@ static gq_status mul_mat_decode(const void* W, int64_t M, int64_t K, const float
 }
 
 static gq_status mul_mat_prefill_bf16(const void* W, int64_t M, int64_t K, const uint16_t* Xb, int64_t N, float* Y,
-                                      bool allow_scratch, cudaStream_t s) {
+                                      bool allow_scratch, cudaStream_t s, int type = GQ_TYPE_Q4_0) {
   CUtensorMap tmW, tmX;
-  uint32_t wbx, wby, xbk, xbr;
-  prefill_boxes(N, &wbx, &wby, &xbk, &xbr);
-  const uint64_t row_bytes = static_cast<uint64_t>(K / kQK) * kBlockBytes;
-  gq_status st = make_tmap(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, row_bytes, static_cast<uint64_t>(M), row_bytes,
-                           wbx, wby, CU_TENSOR_MAP_SWIZZLE_NONE);
+  uint32_t wbx, web, wby, xbk, xbr;
+  prefill_boxes(N, type, &wbx, &web, &wby, &xbk, &xbr);
+  const uint64_t row_bytes = static_cast<uint64_t>(K / kQK) * static_cast<uint64_t>(type_block_bytes(type));
+  gq_status st = make_tmap(&tmW, web == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, W,
+                           row_bytes / web, static_cast<uint64_t>(M), row_bytes, wbx, wby, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (st != GQ_OK) return st;
   st = make_tmap(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Xb, static_cast<uint64_t>(K), static_cast<uint64_t>(N),
                  static_cast<uint64_t>(K) * 2, xbk, xbr, CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != GQ_OK) return st;
-  cudaError_t e =
-      launch_prefill(&tmW, &tmX, N, M, K, Y, static_cast<uint64_t>(g_wait_limit_ns.load()), allow_scratch, s);
+  cudaError_t e = launch_prefill(&tmW, &tmX, N, M, K, Y, static_cast<uint64_t>(g_wait_limit_ns.load()), allow_scratch,
+                                 s, type);
   return e == cudaSuccess ? GQ_OK : cuda_fail(e, "prefill launch");
 }
 
@@ -288,8 +288,29 @@ gq_status gq_mul_mat(gq_type type, const void* W, int64_t M, int64_t K, const fl
   }
   if (!W || !X) return fail(GQ_ERR_NULL, "W and X must not be NULL");
   if (!aligned(X, 4) || !aligned(Y, 4)) return fail(GQ_ERR_ALIGN, "X and Y must be 4-byte aligned");
-  cudaError_t e = launch_mul_mat_legacy(type, static_cast<const uint8_t*>(W), M, K, X, N, Y, s);
-  return e == cudaSuccess ? GQ_OK : cuda_fail(e, "mul_mat launch");
+  // The scalar kernel is instruction-bound (no tensor cores): from two tokens
+  // on, the tensor-core kernel with this block format is faster.
+  const bool tc = N >= 2 && K % 256 == 0 && aligned(W, 16) && aligned(X, 16) && aligned(Y, 16) &&
+                  !g_force_generic.load();
+  if (!tc) {
+    cudaError_t e = launch_mul_mat_legacy(type, static_cast<const uint8_t*>(W), M, K, X, N, Y,
+                                          static_cast<uint64_t>(g_wait_limit_ns.load()), s);
+    return e == cudaSuccess ? GQ_OK : cuda_fail(e, "mul_mat launch");
+  }
+  // X -> bf16 scratch, then the tensor-core kernel with this block format
+  const size_t xbytes = static_cast<size_t>(N) * K * sizeof(uint16_t);
+  void* xb = nullptr;
+  cudaError_t e = scratch_alloc(&xb, xbytes, s);
+  if (e != cudaSuccess) return fail(GQ_ERR_ALLOC, "scratch allocation (%zu bytes): %s", xbytes, cudaGetErrorString(e));
+  e = launch_f32_to_bf16(X, static_cast<uint16_t*>(xb), N * K, s);
+  if (e != cudaSuccess) {
+    scratch_free(xb, s);
+    return cuda_fail(e, "f32->bf16 launch");
+  }
+  st = mul_mat_prefill_bf16(W, M, K, static_cast<const uint16_t*>(xb), N, Y, true, s, type);
+  e = scratch_free(xb, s);
+  if (st != GQ_OK) return st;
+  return e == cudaSuccess ? GQ_OK : cuda_fail(e, "scratch free");
 }
 
 gq_status gq_quantize_q4_0(const float* W, int64_t M, int64_t K, void* out, void* stream) {

@@ -57,8 +57,10 @@ cudaError_t launch_f32_to_bf16(const float* x, uint16_t* y, int64_t n, cudaStrea
 // ---- K3: prefill mul_mat on tcgen05 (gq_prefill.cu).  Needs K % 256 == 0.
 // allow_scratch: the launch may take stream-ordered scratch for the partial
 // sums of tiles split along k (else, or if that allocation fails, whole tiles).
+// type: block format of W (GQ_TYPE_*; Q4_1 and Q8_0 run the 1-CTA kernels).
 cudaError_t launch_prefill(const CUtensorMap* tmW, const CUtensorMap* tmX, int64_t N, int64_t M,
-                           int64_t K, float* Y, uint64_t wait_limit_ns, bool allow_scratch, cudaStream_t s);
+                           int64_t K, float* Y, uint64_t wait_limit_ns, bool allow_scratch, cudaStream_t s,
+                           int type = GQ_TYPE_Q4_0);
 void set_prefill_streamk(int64_t v);   // 0 whole tiles only, 1 by shape (default), n >= 2: every tile in n pieces
 int64_t get_prefill_streamk();
 void set_prefill_slots(int64_t v);     // 0: SM count; n: plan for n SMs (test aid)
@@ -67,8 +69,10 @@ void set_prefill_bn_override(int bn);  // 0 = by shape, else 128 or 256
 void set_prefill_pair_mode(int on);    // 1: 2-SM pair kernel for N > 128 (default 0)
 int get_prefill_pair_mode();
 int get_prefill_bn_override();
-void prefill_boxes(int64_t N, uint32_t* w_box_x_bytes, uint32_t* w_box_rows, uint32_t* x_box_k,
-                   uint32_t* x_box_rows);
+// TMA boxes of the prefill kernel: W rows of one 256-k chunk as w_box_x
+// elements of w_elem_bytes each (1, or 2 when the chunk is wider than 256 bytes).
+void prefill_boxes(int64_t N, int type, uint32_t* w_box_x, uint32_t* w_elem_bytes, uint32_t* w_box_rows,
+                   uint32_t* x_box_k, uint32_t* x_box_rows);
 
 // ---- KR / KG: MUL_MAT_ID routing and activation gather (gq_moe.cu)
 // Routing tables in device memory, written by the routing kernel.
@@ -106,7 +110,7 @@ cudaError_t launch_decode_moe(const CUtensorMap* tmW, const float* X, int cap, i
 int type_block_bytes(int type);  // 18 / 20 / 34, 0 for an unknown type
 cudaError_t launch_dequant_legacy(int type, const uint8_t* W, int64_t nblocks, float* out, cudaStream_t s);
 cudaError_t launch_mul_mat_legacy(int type, const uint8_t* W, int64_t M, int64_t K, const float* X, int64_t N,
-                                  float* Y, cudaStream_t s);
+                                  float* Y, uint64_t wait_limit_ns, cudaStream_t s);
 
 // ---- helpers of the C ABI (gq_api.cu) for entry points defined in other files
 gq_status api_fail(gq_status st, const char* msg);  // records the per-thread error text

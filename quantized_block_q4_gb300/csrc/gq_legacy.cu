@@ -13,15 +13,18 @@
 // bit-exact and MUL_MAT sees the same weights.
 //
 // MUL_MAT here is the decode-shaped kernel for these formats: one warp per
-// weight row, lanes taking consecutive blocks (a warp's loads of one step
-// cover 32 consecutive blocks), weights decoded to fp32 in registers and
-// dotted with x in fp32 for up to kTok tokens per pass; the lanes' partial
-// sums meet by shuffles.  W is read from DRAM once per pass; more tokens than
-// kTok re-read it from L2.
+// weight row, eight lanes per block, four blocks per step (coalesced W and x
+// loads), each lane keeping the W words of 8 steps in flight.  Per block part
+// and token a lane forms sum(q x) over its four exact
+// integer codes in fp32 and applies the scale, d*sum(q x) (+ m*sum(x) for
+// Q4_1): the same value as sum((d q + m) x) up to rounding order.  Up to kTok tokens per pass; the lanes' partial sums meet by
+// shuffles.  W is read from DRAM once per pass; more tokens than kTok re-read
+// it from L2.
 #include <algorithm>
 #include <cuda_fp16.h>
 
 #include "gq_internal.h"
+#include "gq_ptx.cuh"
 
 namespace gq {
 namespace {
@@ -105,43 +108,57 @@ __global__ void __launch_bounds__(kDqThreads) k_dequant_legacy(const uint8_t* __
 
 constexpr int kTok = 4;  // tokens per pass of the MUL_MAT kernel
 
-// One block's 32 weights, from global memory, into registers.
+// Integer codes to fp32 without the conversion unit: 0x4B000000 | u is the
+// float 2^23 + u exactly (u < 2^23), so subtracting 2^23 leaves u.
+__device__ __forceinline__ float u2f(uint32_t u) { return __int_as_float(0x4B000000 | u) - 8388608.0f; }
+
+// The raw words a lane needs for elements 4p..4p+3 (p = 0..7) of a block:
+// the scale word (d, and m for Q4_1) and the 4 code bytes.
 template <int T>
-__device__ __forceinline__ void load_block(const uint8_t* __restrict__ blk, float (&w)[32]) {
+__device__ __forceinline__ void load_part(const uint8_t* __restrict__ blk, int p, uint32_t& h, uint32_t& v) {
   if constexpr (T == GQ_TYPE_Q4_1) {
-    // 20-byte blocks of a 4-byte aligned row: five 32-bit loads
-    const uint32_t* p = reinterpret_cast<const uint32_t*>(blk);
-    const uint32_t h = __ldg(p);
-    const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(h & 0xFFFF)));
-    const float m = __half2float(__ushort_as_half(static_cast<uint16_t>(h >> 16)));
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t v = __ldg(p + 1 + i);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t byte = (v >> (8 * j)) & 0xFF;
-        w[4 * i + j] = __fadd_rn(__fmul_rn(d, static_cast<float>(byte & 0xF)), m);
-        w[16 + 4 * i + j] = __fadd_rn(__fmul_rn(d, static_cast<float>(byte >> 4)), m);
-      }
-    }
+    // 20-byte blocks of a 4-byte aligned row: the scale word and one code word
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(blk);
+    h = __ldg(w);
+    v = __ldg(w + 1 + (p & 3)) >> ((p & 4) ? 4 : 0);  // parts 4..7: high nibbles
   } else {
-    // 34-byte blocks are 2-byte aligned: seventeen 16-bit loads
-    const uint16_t* p = reinterpret_cast<const uint16_t*>(blk);
-    const float d = __half2float(__ushort_as_half(__ldg(p)));
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t v = __ldg(p + 1 + i);
-      w[2 * i] = __fmul_rn(d, static_cast<float>(static_cast<int8_t>(v & 0xFF)));
-      w[2 * i + 1] = __fmul_rn(d, static_cast<float>(static_cast<int8_t>(v >> 8)));
-    }
+    // 34-byte blocks are 2-byte aligned: the scale and two 16-bit code loads
+    const uint16_t* w = reinterpret_cast<const uint16_t*>(blk);
+    h = __ldg(w);
+    v = static_cast<uint32_t>(__ldg(w + 1 + 2 * p)) | (static_cast<uint32_t>(__ldg(w + 2 + 2 * p)) << 16);
   }
 }
 
+// Codes as fp32 (exact small integers: Q4_1 0..15, Q8_0 -128..127; a Q8_0
+// code c is (c ^ 0x80) - 128 with c ^ 0x80 in 0..255) and the scales.
+template <int T>
+__device__ __forceinline__ void decode_part(uint32_t h, uint32_t v, float (&q)[4], float& d, float& m) {
+  d = __half2float(__ushort_as_half(static_cast<uint16_t>(h & 0xFFFF)));
+  if constexpr (T == GQ_TYPE_Q4_1) {
+    m = __half2float(__ushort_as_half(static_cast<uint16_t>(h >> 16)));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) q[j] = u2f((v >> (8 * j)) & 0xF);
+  } else {
+    m = 0.f;
+    v ^= 0x80808080u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) q[j] = u2f((v >> (8 * j)) & 0xFF) - 128.0f;
+  }
+}
+
+constexpr int kSteps = 8;  // steps of four blocks whose W words a lane loads before using them
+
+// Eight lanes share a block (lane l takes elements 4*(l%8) .. +3 of block
+// 4*step + l/8), so a warp's x loads of one step are 512 contiguous bytes and
+// its W loads cover four consecutive blocks.  A lane first loads the W words
+// of kSteps steps (the kernel is bound by DRAM latency otherwise), then
+// computes them.
 template <int T>
 __global__ void __launch_bounds__(256) k_mul_mat_legacy(const uint8_t* __restrict__ W, int M, int K,
                                                         const float* __restrict__ X, int N, float* __restrict__ Y) {
   constexpr int kB = Fmt<T>::kBytes;
   const int lane = threadIdx.x & 31;
+  const int part = lane & 7, sub = lane >> 3;
   const int nb = K / kQK;
   const int64_t row_bytes = static_cast<int64_t>(nb) * kB;
   const int warps = gridDim.x * (blockDim.x >> 5);
@@ -150,21 +167,35 @@ __global__ void __launch_bounds__(256) k_mul_mat_legacy(const uint8_t* __restric
     for (int n0 = 0; n0 < N; n0 += kTok) {
       const int nt = N - n0 < kTok ? N - n0 : kTok;
       float acc[kTok] = {};
-      for (int b = lane; b < nb; b += 32) {
-        float w[32];
-        load_block<T>(row + static_cast<int64_t>(b) * kB, w);
+      for (int b0 = sub; b0 < nb; b0 += 4 * kSteps) {
+        uint32_t h[kSteps], v[kSteps];
+#pragma unroll
+        for (int i = 0; i < kSteps; ++i) {
+          h[i] = 0;
+          v[i] = 0;
+          if (b0 + 4 * i < nb) load_part<T>(row + static_cast<int64_t>(b0 + 4 * i) * kB, part, h[i], v[i]);
+        }
+        float q[kSteps][4], d[kSteps], mn[kSteps];
+#pragma unroll
+        for (int i = 0; i < kSteps; ++i) decode_part<T>(h[i], v[i], q[i], d[i], mn[i]);
 #pragma unroll
         for (int t = 0; t < kTok; ++t) {
           if (t < nt) {
-            const float4* xp = reinterpret_cast<const float4*>(X + static_cast<int64_t>(n0 + t) * K + b * kQK);
+            // this token's x for all kSteps steps first (independent loads), then the sums
+            const float4* xr = reinterpret_cast<const float4*>(X + static_cast<int64_t>(n0 + t) * K) + part;
+            float4 xv[kSteps];
+#pragma unroll
+            for (int i = 0; i < kSteps; ++i)
+              xv[i] = (b0 + 4 * i < nb) ? __ldg(xr + (b0 + 4 * i) * (kQK / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
             float a = acc[t];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 x = __ldg(xp + i);
-              a = fmaf(w[4 * i], x.x, a);
-              a = fmaf(w[4 * i + 1], x.y, a);
-              a = fmaf(w[4 * i + 2], x.z, a);
-              a = fmaf(w[4 * i + 3], x.w, a);
+            for (int i = 0; i < kSteps; ++i) {
+              float qx = q[i][0] * xv[i].x;
+              qx = fmaf(q[i][1], xv[i].y, qx);
+              qx = fmaf(q[i][2], xv[i].z, qx);
+              qx = fmaf(q[i][3], xv[i].w, qx);
+              a = fmaf(d[i], qx, a);
+              if (T == GQ_TYPE_Q4_1) a = fmaf(mn[i], (xv[i].x + xv[i].y) + (xv[i].z + xv[i].w), a);
             }
             acc[t] = a;
           }
@@ -176,6 +207,116 @@ __global__ void __launch_bounds__(256) k_mul_mat_legacy(const uint8_t* __restric
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
         if (lane == 0 && t < nt) Y[static_cast<int64_t>(n0 + t) * M + m] = a;
+      }
+    }
+  }
+}
+
+// The same computation with each warp's rows double-buffered in shared
+// memory: one lane copies the next whole row with a bulk copy while the warp
+// computes the current one, so every warp keeps a full row of W in flight.
+// Needs W 16-byte aligned and rows a multiple of 16 bytes.
+constexpr int kBulkMaxWarps = 8;
+
+template <int T>
+__global__ void __launch_bounds__(256) k_mul_mat_legacy_bulk(const uint8_t* __restrict__ W, int M, int K,
+                                                             const float* __restrict__ X, int N,
+                                                             float* __restrict__ Y, uint64_t limit_ns,
+                                                             uint32_t* err) {
+  constexpr int kB = Fmt<T>::kBytes;
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[kBulkMaxWarps][2];
+  __shared__ volatile int abort_flag;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int part = lane & 7, sub = lane >> 3;
+  const int nb = K / kQK;
+  const uint32_t rb = static_cast<uint32_t>(nb * kB);  // row bytes, a multiple of 16
+  uint8_t* buf[2] = {smem + (2 * warp) * rb, smem + (2 * warp + 1) * rb};
+  if (threadIdx.x == 0) abort_flag = 0;
+  if (lane == 0) {
+    mbar_init(smem_u32(&bars[warp][0]), 1);
+    mbar_init(smem_u32(&bars[warp][1]), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int gw = blockIdx.x * (blockDim.x >> 5) + warp, nw = gridDim.x * (blockDim.x >> 5);
+  if (gw < M && lane == 0) {
+    mbar_arrive_expect_tx(smem_u32(&bars[warp][0]), rb);
+    bulk_load(smem_u32(buf[0]), W + static_cast<int64_t>(gw) * rb, rb, smem_u32(&bars[warp][0]));
+  }
+  int issued = gw < M ? 1 : 0, i = 0;
+  bool live = true;
+  for (int m = gw; m < M && live; m += nw, ++i) {
+    const int j = i & 1;
+    if (m + nw < M && lane == 0) {  // the other buffer was last read before the previous __syncwarp
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(smem_u32(&bars[warp][j ^ 1]), rb);
+      bulk_load(smem_u32(buf[j ^ 1]), W + static_cast<int64_t>(m + nw) * rb, rb, smem_u32(&bars[warp][j ^ 1]));
+      ++issued;
+    }
+    live = mbar_wait_bounded(smem_u32(&bars[warp][j]), (i >> 1) & 1, limit_ns, &abort_flag, err);
+    live = __all_sync(0xFFFFFFFFu, live);
+    if (!live) break;
+    const uint8_t* row = buf[j];
+    for (int n0 = 0; n0 < N; n0 += kTok) {
+      const int nt = N - n0 < kTok ? N - n0 : kTok;
+      float acc[kTok] = {};
+      for (int b0 = sub; b0 < nb; b0 += 4 * kSteps) {
+        float q[kSteps][4], d[kSteps], mn[kSteps];
+#pragma unroll
+        for (int s2 = 0; s2 < kSteps; ++s2) {
+          uint32_t h = 0, v = 0;
+          const int b = b0 + 4 * s2;
+          if (b < nb) {
+            const uint8_t* blk = row + b * kB;
+            if constexpr (T == GQ_TYPE_Q4_1) {
+              h = *reinterpret_cast<const uint32_t*>(blk);
+              v = *reinterpret_cast<const uint32_t*>(blk + 4 + 4 * (part & 3)) >> ((part & 4) ? 4 : 0);
+            } else {
+              h = *reinterpret_cast<const uint16_t*>(blk);
+              v = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(blk + 2 + 4 * part)) |
+                  (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(blk + 4 + 4 * part)) << 16);
+            }
+          }
+          decode_part<T>(h, v, q[s2], d[s2], mn[s2]);
+        }
+#pragma unroll
+        for (int t = 0; t < kTok; ++t) {
+          if (t < nt) {
+            const float4* xr = reinterpret_cast<const float4*>(X + static_cast<int64_t>(n0 + t) * K) + part;
+            float4 xv[kSteps];
+#pragma unroll
+            for (int s2 = 0; s2 < kSteps; ++s2)
+              xv[s2] = (b0 + 4 * s2 < nb) ? __ldg(xr + (b0 + 4 * s2) * (kQK / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            float a = acc[t];
+#pragma unroll
+            for (int s2 = 0; s2 < kSteps; ++s2) {
+              float qx = q[s2][0] * xv[s2].x;
+              qx = fmaf(q[s2][1], xv[s2].y, qx);
+              qx = fmaf(q[s2][2], xv[s2].z, qx);
+              qx = fmaf(q[s2][3], xv[s2].w, qx);
+              a = fmaf(d[s2], qx, a);
+              if (T == GQ_TYPE_Q4_1) a = fmaf(mn[s2], (xv[s2].x + xv[s2].y) + (xv[s2].z + xv[s2].w), a);
+            }
+            acc[t] = a;
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kTok; ++t) {
+        float a = acc[t];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
+        if (lane == 0 && t < nt) Y[static_cast<int64_t>(n0 + t) * M + m] = a;
+      }
+    }
+    __syncwarp();  // every lane is done with buf[j] before it is refilled
+  }
+  // Leave no copy in flight: wait (bounded) for the last phase of each buffer.
+  if (lane == 0) {
+    for (int k = issued - 1; k >= 0 && k >= issued - 2; --k) {
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(smem_u32(&bars[warp][k & 1]), (k >> 1) & 1) && globaltimer_ns() - t0 < limit_ns) {
       }
     }
   }
@@ -219,7 +360,7 @@ cudaError_t launch_dequant_t(const uint8_t* W, int64_t nblocks, float* out, cuda
 
 template <int T>
 cudaError_t launch_mul_mat_t(const uint8_t* W, int64_t M, int64_t K, const float* X, int64_t N, float* Y,
-                             cudaStream_t s) {
+                             uint64_t limit_ns, cudaStream_t s) {
   const int64_t rows_per_cta = 8;  // 8 warps
   const int grid = static_cast<int>(
       std::min<int64_t>((M + rows_per_cta - 1) / rows_per_cta, static_cast<int64_t>(device_info().sm_count) * 16));
@@ -229,7 +370,30 @@ cudaError_t launch_mul_mat_t(const uint8_t* W, int64_t M, int64_t K, const float
   const uintptr_t wa = reinterpret_cast<uintptr_t>(W), xa = reinterpret_cast<uintptr_t>(X);
   const bool fast = ((wa | static_cast<uintptr_t>(row_bytes)) & (T == GQ_TYPE_Q4_1 ? 3 : 1)) == 0 && (xa & 15) == 0 &&
                     K % 4 == 0 && M < (int64_t(1) << 31) && K < (int64_t(1) << 31) && N < (int64_t(1) << 31);
-  if (fast)
+  const int rb = static_cast<int>(row_bytes);
+  int bulk_warps = 0;
+  // (one pass over the rows: with more tokens the plain kernel re-reads W from L2 faster)
+  if (fast && N <= kTok && (wa & 15) == 0 && row_bytes % 16 == 0 && row_bytes <= 96 * 1024) {
+    bulk_warps = std::min(kBulkMaxWarps, static_cast<int>((200 * 1024) / (2 * row_bytes)));
+  }
+  if (bulk_warps > 0) {
+    auto kern = k_mul_mat_legacy_bulk<T>;
+    const int smem = 2 * bulk_warps * rb;
+    static int configured = 0;
+    if (smem > configured) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      if (e != cudaSuccess) return e;
+      configured = 200 * 1024;
+    }
+    int occ = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32 * bulk_warps, smem);
+    if (e != cudaSuccess) return e;
+    const int64_t ctas = std::min<int64_t>((M + bulk_warps - 1) / bulk_warps,
+                                           static_cast<int64_t>(device_info().sm_count) * std::max(occ, 1));
+    kern<<<static_cast<unsigned>(ctas), 32 * bulk_warps, smem, s>>>(W, static_cast<int>(M), static_cast<int>(K), X,
+                                                                     static_cast<int>(N), Y, limit_ns,
+                                                                     device_error_word());
+  } else if (fast)
     k_mul_mat_legacy<T><<<grid > 0 ? grid : 1, 256, 0, s>>>(W, static_cast<int>(M), static_cast<int>(K), X,
                                                              static_cast<int>(N), Y);
   else
@@ -254,9 +418,9 @@ cudaError_t launch_dequant_legacy(int type, const uint8_t* W, int64_t nblocks, f
 }
 
 cudaError_t launch_mul_mat_legacy(int type, const uint8_t* W, int64_t M, int64_t K, const float* X, int64_t N,
-                                  float* Y, cudaStream_t s) {
-  if (type == GQ_TYPE_Q4_1) return launch_mul_mat_t<GQ_TYPE_Q4_1>(W, M, K, X, N, Y, s);
-  return launch_mul_mat_t<GQ_TYPE_Q8_0>(W, M, K, X, N, Y, s);
+                                  float* Y, uint64_t wait_limit_ns, cudaStream_t s) {
+  if (type == GQ_TYPE_Q4_1) return launch_mul_mat_t<GQ_TYPE_Q4_1>(W, M, K, X, N, Y, wait_limit_ns, s);
+  return launch_mul_mat_t<GQ_TYPE_Q8_0>(W, M, K, X, N, Y, wait_limit_ns, s);
 }
 
 }  // namespace gq

@@ -86,21 +86,34 @@ cudaError_t launch_f32_to_bf16(const float* x, uint16_t* y, int64_t n, cudaStrea
 
 namespace {
 
-template <int BN, bool PAIR>
+// F: block format of W (GQ_TYPE_*).  Q4_0 blocks are 18 bytes, Q4_1 20,
+// Q8_0 34; a raw stage holds 8 blocks (256 k) of each of the 128 rows.
+template <int F>
+constexpr int fmt_block_bytes() { return F == GQ_TYPE_Q4_0 ? 18 : (F == GQ_TYPE_Q4_1 ? 20 : 34); }
+
+template <int BN, bool PAIR, int F = GQ_TYPE_Q4_0>
 struct PrefillCfg {
   static constexpr int kBM = 128;       // W rows per CTA (a CTA pair covers 256)
   static constexpr int kBK = 64;        // k per MMA stage: one 128-byte row of bf16
   static constexpr int kRawK = 256;     // k per raw W stage (one work unit)
-  static constexpr int kRawRow = 144;   // bytes of 8 blocks
+  static constexpr int kBlk = fmt_block_bytes<F>();
+  static constexpr int kRawRow = 8 * kBlk;   // bytes of 8 blocks: 144, 160 or 272
+  // The TMA box is at most 256 elements wide: Q8_0's 272-byte rows are read
+  // as 136 16-bit elements.
+  static constexpr int kRawElem = kRawRow > 256 ? 2 : 1;
   static constexpr int kCtas = PAIR ? 2 : 1;
   static constexpr int kXRows = BN / kCtas;            // x rows (tokens) this CTA loads per stage
   static constexpr int kACols = kBK / 2;               // TMEM columns per A stage
   // One ring of S stages, each an A tile in TMEM (64 k of the 128 rows) and
   // an x tile in shared memory; the accumulator takes the first BN columns.
-  static constexpr int RS = 3, S = PAIR ? 8 : (BN == 256 ? 5 : 8);
+  // The larger raw stages of Q4_1 / Q8_0 leave room for fewer x stages.
+  static constexpr int RS = F == GQ_TYPE_Q8_0 ? 2 : 3;
+  static constexpr int S = PAIR ? 8 : (BN == 256 ? (F == GQ_TYPE_Q4_0 ? 5 : 4) : 8);
   static_assert(BN + S * kACols <= 512, "TMEM holds the accumulator and the A stages");
   static constexpr int kTmemCols = 512;
-  static constexpr int kRawBytes = kBM * kRawRow;  // 18432
+  static constexpr int kRawBytes = kBM * kRawRow;  // 18432 for Q4_0
+  // 16-byte words a dequantising thread loads to cover its two blocks
+  static constexpr int kWinWords = F == GQ_TYPE_Q8_0 ? 5 : 3;
   static constexpr int kBBytes = kXRows * 128;
   static constexpr int kOffB = 0;
   static constexpr int kOffRaw = kOffB + S * kBBytes;
@@ -114,6 +127,7 @@ struct PrefillCfg {
   static constexpr int kXWarp = 2 + kDeqWarps;  // warp 0 loads W, warp 1 issues MMAs, the last warp loads x
   static constexpr int kThreads = 32 * (3 + kDeqWarps);
   static constexpr int kSlotFloats = BN * kBM;         // one CTA's partial tile, [column][row]
+  static_assert(kSmem <= 216 * 1024, "shared memory budget (the Q4_0 BN = 256 ring uses 215 KB)");
 };
 
 // Work schedule of a launch over G work ranges (one CTA, or one CTA pair,
@@ -259,6 +273,73 @@ __device__ __forceinline__ void block_words(const uint32_t (&q)[4], uint32_t d_b
   word_to_bf16(q[3], dhi2, dlo2, o[6], o[7], o[14], o[15]);
 }
 
+// Q4_1 and Q8_0 steps: elements as fp32 (d*q exact; Q4_1 then adds m with
+// one rounding), rounded once more to bf16 in pairs (element 2i in the low
+// half of o[i], as for Q4_0).
+__device__ __forceinline__ float code_f(uint32_t u) { return __int_as_float(0x4B000000 | u) - 8388608.0f; }
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// One Q4_1 block: h = d | m << 16, c[4] = the 16 code bytes.
+__device__ __forceinline__ void q41_block(uint32_t h, const uint32_t (&c)[4], uint32_t* o) {
+  const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(h & 0xFFFF)));
+  const float m = __half2float(__ushort_as_half(static_cast<uint16_t>(h >> 16)));
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    float lo[4], hi[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      lo[j] = __fadd_rn(__fmul_rn(d, code_f((c[w] >> (8 * j)) & 0xF)), m);
+      hi[j] = __fadd_rn(__fmul_rn(d, code_f((c[w] >> (8 * j + 4)) & 0xF)), m);
+    }
+    o[2 * w] = pack_bf16(lo[0], lo[1]);
+    o[2 * w + 1] = pack_bf16(lo[2], lo[3]);
+    o[8 + 2 * w] = pack_bf16(hi[0], hi[1]);
+    o[8 + 2 * w + 1] = pack_bf16(hi[2], hi[3]);
+  }
+}
+
+// One Q8_0 block: d bits, c[8] = the 32 code bytes (two's complement; c ^
+// 0x80 is the code + 128).
+__device__ __forceinline__ void q80_block(uint32_t d_bits, const uint32_t (&c)[8], uint32_t* o) {
+  const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(d_bits)));
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const uint32_t u = c[w] ^ 0x80808080u;
+    float e[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) e[j] = __fmul_rn(d, code_f((u >> (8 * j)) & 0xFF) - 128.0f);
+    o[2 * w] = pack_bf16(e[0], e[1]);
+    o[2 * w + 1] = pack_bf16(e[2], e[3]);
+  }
+}
+
+// Group G's two blocks of a 256-k chunk row from the loaded window v (the
+// 16-byte words from byte (2*G*block bytes) & ~15 of the row).
+template <int F, int G>
+__device__ __forceinline__ void step_words_fmt(const uint32_t* v, uint32_t* o) {
+  if constexpr (F == GQ_TYPE_Q4_1) {
+    constexpr int w0 = (40 * G % 16) / 4;  // 0, 2, 0, 2
+    const uint32_t c0[4] = {v[w0 + 1], v[w0 + 2], v[w0 + 3], v[w0 + 4]};
+    const uint32_t c1[4] = {v[w0 + 6], v[w0 + 7], v[w0 + 8], v[w0 + 9]};
+    q41_block(v[w0], c0, o);
+    q41_block(v[w0 + 5], c1, o + 16);
+  } else {
+    // 68*G mod 16 = 4G: block 0 starts at word G, block 1 at byte 4G + 34
+    uint32_t c0[8], c1[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      c0[k] = prmt(v[G + k], v[G + k + 1], 0x5432u);  // bytes 4G + 2 + 4k ..
+      c1[k] = v[G + 9 + k];                            // bytes 4G + 36 + 4k ..
+    }
+    q80_block(v[G] & 0xFFFFu, c0, o);
+    q80_block(v[G + 8] >> 16, c1, o + 16);
+  }
+}
+
 // Bounded wait on the last phase issued into each slot of a ring (drain path).
 __device__ __forceinline__ void drain_ring(uint64_t* full, int slots, uint32_t issued, uint64_t limit_ns) {
   for (int s = 0; s < slots; ++s) {
@@ -274,13 +355,14 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int slots, uint32_t i
 // one expert, N is unused, the work items come from rt (item i of the launch
 // goes to CTA i % gridDim.x) and x rows are loaded in 64-row boxes, only as
 // many as the tile's tokens need.
-template <int BN, bool PAIR, bool MOE = false>
-__global__ void __launch_bounds__(PrefillCfg<BN, PAIR>::kThreads, 1)
+template <int BN, bool PAIR, bool MOE = false, int F = GQ_TYPE_Q4_0>
+__global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
     k_prefill_q4_0(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int N, int M,
                    float* __restrict__ Y, const PrefillWork wk, uint64_t limit_ns, uint32_t* err,
                    const MoeRoute rt, int E) {
   static_assert(!(MOE && PAIR), "MUL_MAT_ID uses the 1-CTA kernel");
-  using C = PrefillCfg<BN, PAIR>;
+  static_assert(!(MOE && F != GQ_TYPE_Q4_0), "MUL_MAT_ID takes Q4_0 weights");
+  using C = PrefillCfg<BN, PAIR, F>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -370,7 +452,8 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR>::kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(smem_u32(&raw_full[slot]), C::kRawBytes);
-          tma_load_2d(sbase + C::kOffRaw + slot * C::kRawBytes, &tmW, r * C::kRawRow, m0, smem_u32(&raw_full[slot]));
+          tma_load_2d(sbase + C::kOffRaw + slot * C::kRawBytes, &tmW, r * (C::kRawRow / C::kRawElem), m0,
+                      smem_u32(&raw_full[slot]));
           ++nraw;
         }
       }
@@ -488,9 +571,9 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR>::kThreads, 1)
     const bool e0 = warp == 2 && lane == 0;
     constexpr int kCbPerGrp = BN / 128;  // 32-column blocks of the accumulator per group
     const int cb0 = grp * kCbPerGrp, cb1 = cb0 + kCbPerGrp;
-    // This group's 36 bytes of a raw row start at byte 36*grp: read the three
-    // 16-byte words that cover them; word grp of those is the first one.
-    const int raw_off = row * C::kRawRow + (36 * grp & ~15);
+    // This group's two blocks of a raw row start at byte 2*grp*kBlk: read the
+    // 16-byte words that cover them (for Q4_0 the 36 bytes start at word grp).
+    const int raw_off = row * C::kRawRow + (2 * C::kBlk * grp & ~15);
     bool live = true;
     uint32_t cr = 0, c = 0, seg = 0;
     for (int i = 0; i < nseg; ++i) {
@@ -508,11 +591,11 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR>::kThreads, 1)
         const uint32_t as = (c + grp) % C::S;
         if (live) live = mbar_wait_bounded(smem_u32(&raw_full[rslot]), (cr / C::RS) & 1, limit_ns, abort_flag, err);
         live = __all_sync(0xFFFFFFFFu, live);
-        uint32_t v[12];
+        uint32_t v[4 * C::kWinWords];
         if (live) {
           const uint4* src = reinterpret_cast<const uint4*>(smem + C::kOffRaw + rslot * C::kRawBytes + raw_off);
 #pragma unroll
-          for (int i = 0; i < 3; ++i) {
+          for (int i = 0; i < C::kWinWords; ++i) {
             const uint4 x = src[i];
             v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
           }
@@ -522,7 +605,14 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR>::kThreads, 1)
         // Dequantise first, then wait for the A stage: only the store is left
         // between the stage becoming free and the MMA that reads it.
         uint32_t o[32];
-        {
+        if constexpr (F != GQ_TYPE_Q4_0) {
+          switch (grp) {  // warp-uniform
+            case 0: step_words_fmt<F, 0>(v, o); break;
+            case 1: step_words_fmt<F, 1>(v, o); break;
+            case 2: step_words_fmt<F, 2>(v, o); break;
+            default: step_words_fmt<F, 3>(v, o); break;
+          }
+        } else {
           uint32_t w[9];  // blocks 2*grp and 2*grp+1 of the row
 #pragma unroll
           for (int i = 0; i < 9; ++i)
@@ -715,14 +805,14 @@ void prefill_plan(int64_t T, int64_t nr, int64_t P, bool allow_split, PrefillWor
   wk->G = std::max(std::min(T, P), rem * s);
 }
 
-template <int BN, bool PAIR>
+template <int BN, bool PAIR, int F = GQ_TYPE_Q4_0>
 cudaError_t launch_prefill_cfg(const CUtensorMap* tmW, const CUtensorMap* tmX, int N, int M, int K, float* Y,
                                uint64_t limit_ns, bool allow_scratch, cudaStream_t s) {
-  using C = PrefillCfg<BN, PAIR>;
+  using C = PrefillCfg<BN, PAIR, F>;
+  auto kern = k_prefill_q4_0<BN, PAIR, false, F>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(k_prefill_q4_0<BN, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
@@ -766,8 +856,7 @@ cudaError_t launch_prefill_cfg(const CUtensorMap* tmW, const CUtensorMap* tmX, i
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  cudaError_t e = cudaLaunchKernelEx(&cfg, k_prefill_q4_0<BN, PAIR>, *tmW, *tmX, N, M, Y, wk, limit_ns,
-                                     device_error_word(), MoeRoute{}, 0);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, *tmW, *tmX, N, M, Y, wk, limit_ns, device_error_word(), MoeRoute{}, 0);
   if (scratch) {
     cudaError_t f = scratch_free(scratch, s);
     if (e == cudaSuccess) e = f;
@@ -791,12 +880,14 @@ bool use_pair(int64_t N) { return g_pair_mode && g_bn_override == 0 && N > 128; 
 void set_prefill_bn_override(int bn) { g_bn_override = bn; }
 int get_prefill_bn_override() { return g_bn_override; }
 
-void prefill_boxes(int64_t N, uint32_t* w_box_x_bytes, uint32_t* w_box_rows, uint32_t* x_box_k,
-                   uint32_t* x_box_rows) {
-  *w_box_x_bytes = 144;
+void prefill_boxes(int64_t N, int type, uint32_t* w_box_x, uint32_t* w_elem_bytes, uint32_t* w_box_rows,
+                   uint32_t* x_box_k, uint32_t* x_box_rows) {
+  const uint32_t raw_row = 8u * static_cast<uint32_t>(type_block_bytes(type));
+  *w_elem_bytes = raw_row > 256 ? 2u : 1u;
+  *w_box_x = raw_row / *w_elem_bytes;
   *w_box_rows = 128;
   *x_box_k = 64;
-  *x_box_rows = use_pair(N) ? 128u : static_cast<uint32_t>(prefill_bn(N));
+  *x_box_rows = (type == GQ_TYPE_Q4_0 && use_pair(N)) ? 128u : static_cast<uint32_t>(prefill_bn(N));
 }
 
 void set_prefill_pair_mode(int on) { g_pair_mode = on ? 1 : 0; }
@@ -841,8 +932,18 @@ cudaError_t launch_prefill_moe(const CUtensorMap* tmW, const CUtensorMap* tmX, i
 }
 
 cudaError_t launch_prefill(const CUtensorMap* tmW, const CUtensorMap* tmX, int64_t N, int64_t M, int64_t K,
-                           float* Y, uint64_t wait_limit_ns, bool allow_scratch, cudaStream_t s) {
+                           float* Y, uint64_t wait_limit_ns, bool allow_scratch, cudaStream_t s, int type) {
   const int n = static_cast<int>(N), m = static_cast<int>(M), k = static_cast<int>(K);
+  if (type == GQ_TYPE_Q4_1) {
+    if (prefill_bn(N) == 128)
+      return launch_prefill_cfg<128, false, GQ_TYPE_Q4_1>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, s);
+    return launch_prefill_cfg<256, false, GQ_TYPE_Q4_1>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, s);
+  }
+  if (type == GQ_TYPE_Q8_0) {
+    if (prefill_bn(N) == 128)
+      return launch_prefill_cfg<128, false, GQ_TYPE_Q8_0>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, s);
+    return launch_prefill_cfg<256, false, GQ_TYPE_Q8_0>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, s);
+  }
   if (use_pair(N)) return launch_prefill_cfg<256, true>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, s);
   if (prefill_bn(N) == 128) return launch_prefill_cfg<128, false>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, s);
   return launch_prefill_cfg<256, false>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, s);

@@ -72,9 +72,32 @@ def test_mul_mat_matches_oracle(qtype, M, K, N):
 
 
 @pytest.mark.parametrize("qtype", TYPES, ids=lambda t: NAMES[t])
-@pytest.mark.parametrize("M,K,N", [(11008, 4096, 1), (4096, 11008, 1), (11008, 4096, 8)])
+@pytest.mark.parametrize("M,K,N", [(11008, 4096, 1), (4096, 11008, 1), (11008, 4096, 8), (14336, 4096, 512),
+                                   (4096, 11008, 512), (32000, 4096, 16)])
 def test_mul_mat_full_size_sampled_rows(qtype, M, K, N):
     check(qtype, M, K, N, seed=13300 + N + qtype, sample=48)
+
+
+@pytest.mark.parametrize("qtype", TYPES, ids=lambda t: NAMES[t])
+@pytest.mark.parametrize("M,K,N", [(300, 512, 16), (129, 1024, 100), (1000, 2048, 257), (64, 256, 128), (700, 4096, 2),
+                                   (130, 768, 5)])
+def test_tensor_core_path_matches_oracle(qtype, M, K, N):
+    """N >= 16 with K % 256 == 0: the tcgen05 kernel with this block format
+    (several row tiles, ragged M and N, one and several 256-k chunks)."""
+    check(qtype, M, K, N, seed=13600 + M + N + qtype)
+
+
+@pytest.mark.parametrize("qtype", TYPES, ids=lambda t: NAMES[t])
+def test_tensor_core_and_scalar_paths_agree(qtype):
+    """The same N = 32 product through the tensor-core kernel and through the
+    scalar kernel (GQ_OPT_FORCE_GENERIC), both against the oracle."""
+    M, K, N = 500, 1024, 32
+    check(qtype, M, K, N, seed=13700 + qtype)
+    gq.gq_set_option(gq.GQ_OPT_FORCE_GENERIC, 1)
+    try:
+        check(qtype, M, K, N, seed=13700 + qtype)
+    finally:
+        gq.gq_set_option(gq.GQ_OPT_FORCE_GENERIC, 0)
 
 
 @pytest.mark.parametrize("qtype", TYPES, ids=lambda t: NAMES[t])
