@@ -560,8 +560,8 @@ def run_e2e(gq, torch, dev, s, W, shapes, acts1, order, L, args):
 # DRAM bytes (read + write) per launch, from one ncu capture per shape of the
 # sweep (profiles/dram_traffic_sweep_shapes.md); refresh when a kernel changes.
 MEASURED_TRAFFIC = {
-    "decode": {(4096, 4096): 9483520, (11008, 4096): 25412608, (4096, 11008): 25436672},
-    "prefill": {(4096, 4096): 13680384, (11008, 4096): 29956864, (4096, 11008): 36795136},
+    "decode": {(4096, 4096): 9483776, (11008, 4096): 25408768, (4096, 11008): 25436160},
+    "prefill": {(4096, 4096): 13681408, (11008, 4096): 29882880, (4096, 11008): 36805376},
 }
 
 
