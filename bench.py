@@ -307,6 +307,7 @@ def run_gpu(args, rank, world, dist):
     if rank == 0:
         aux["mul_mat_id"] = run_moe_aux(gq, torch, dev, s, peaks)
         aux["legacy_formats"] = run_legacy_aux(gq, torch, dev, s, peaks)
+        aux["prepared_layout"] = run_prepared_aux(gq, torch, dev, s, peaks)
     e2e["ms"] = max_over_ranks([e2e["ms"]], dist, dev)[0]
     e2e_value = world * wbytes / (e2e["ms"] * 1e-3) / 1e9
 
@@ -355,6 +356,7 @@ def run_gpu(args, rank, world, dist):
         "quantize": aux.get("quantize"),
         "mul_mat_id": aux.get("mul_mat_id"),
         "legacy_formats": aux.get("legacy_formats"),
+        "prepared_layout": aux.get("prepared_layout"),
         "gpu_launches": K_ * (len(shapes) + len(shapes) + L * len(ks)),
         "clocks": clocks,
         "cpu_baseline": cpu,
@@ -513,6 +515,48 @@ def run_legacy_aux(gq, torch, dev, s, peaks):
                              "kernel": "k_f32_to_bf16 + k_prefill_q4_0<256, 0, 0, type>"},
         }
     return out
+
+
+def run_prepared_aux(gq, torch, dev, s, peaks):
+    """The repacked layout on an 11008 x 2880 matrix (2880 = 11.25 x 256, a K
+    the packed fast paths do not take): gq_prepare_q4_0 (GB/s), then MUL_MAT on
+    the prepared weights at N = 1 (weight GB/s, rotating copies) and N = 512."""
+    M, K = 11008, 2880
+    W = torch.from_numpy(synth.q4_0_weights(M, K, seed=0x9E00)).to(dev)
+    pb = gq.gq_prepared_q4_0_nbytes(M, K)
+    Wps = [torch.empty(pb, dtype=torch.uint8, device=dev) for _ in range(8)]
+    X1 = torch.randn(1, K, device=dev)
+    XP = torch.randn(512, K, device=dev)
+    Y1 = torch.empty(1, M, device=dev)
+    YP = torch.empty(512, M, device=dev)
+
+    def timed(fn, reps=8):
+        with torch.cuda.stream(s):
+            for i in range(8):
+                fn(i)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for i in range(reps):
+                fn(i)
+            e1.record(s)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / reps * 1e-3
+
+    tpre = timed(lambda i: gq.gq_prepare_q4_0(W, M, K, 0, Wps[i % 8], stream=s))
+    t1 = timed(lambda i: gq.gq_mul_mat_q4_0_prepared(Wps[i % 8], M, K, X1, 1, Y1, stream=s))
+    tp = timed(lambda i: gq.gq_mul_mat_q4_0_prepared(Wps[i % 8], M, K, XP, 512, YP, stream=s))
+    gq.gq_sync_status(s)
+    wbytes = gq.gq_q4_0_nbytes(M, K)
+    return {
+        "shape": f"{M}x{K}",
+        "prepare": {"us": round(tpre * 1e6, 2), "achieved": round((wbytes + pb) / tpre / 1e9, 1), "unit": "GB/s",
+                    "bound": "hbm", "frac": round((wbytes + pb) / tpre / 1e9 / peaks["hbm_gbs"], 4)},
+        "mul_mat_n1": {"us": round(t1 * 1e6, 2), "achieved": round(wbytes / t1 / 1e9, 1), "unit": "GB/s",
+                       "bound": "hbm", "frac": round(wbytes / t1 / 1e9 / peaks["hbm_gbs"], 4)},
+        "mul_mat_n512": {"us": round(tp * 1e6, 2), "achieved": round(2 * M * K * 512 / tp / 1e12, 2),
+                         "unit": "TFLOP/s", "bound": "tensor",
+                         "frac": round(2 * M * K * 512 / tp / 1e12 / peaks["bf16_tflops"], 4)},
+    }
 
 
 def run_e2e(gq, torch, dev, s, W, shapes, acts1, order, L, args):

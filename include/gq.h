@@ -153,6 +153,30 @@ gq_status gq_mul_mat_q4_0(const void *W, int64_t M, int64_t K, const float *X, i
 gq_status gq_mul_mat_id_q4_0(const void *W, int64_t n_expert, int64_t M, int64_t K, const float *X,
                              int64_t n_ids, const int32_t *ids, int64_t T, float *Y, void *stream);
 
+/* The repack of Q4_0 weights for the fast kernels (the GPU analogue of the
+ * library's repacked layouts).  ggml rows may have a padded stride (nb[1],
+ * "ggml compute graph and memory allocator", the ggml_tensor section) and K
+ * need only be a multiple of 32; the TMA kernels want rows of a multiple of
+ * 256 weights.  gq_prepare_q4_0 copies each row of W (row_stride bytes apart;
+ * 0 = packed, K/32*18) into `out`, rows of ceil(K/256)*144 bytes, and fills
+ * each row up with zero blocks (d = +0, every code 8).  The blocks are copied
+ * unchanged: the prepared matrix holds the same weights.  out needs
+ * gq_prepared_q4_0_nbytes(M, K) bytes, 16-byte aligned; W any alignment.
+ * Errors: K % 32 != 0, negative sizes or row_stride shorter than a row ->
+ * GQ_ERR_SHAPE; NULL -> GQ_ERR_NULL; out unaligned -> GQ_ERR_ALIGN. */
+size_t gq_prepared_q4_0_nbytes(int64_t M, int64_t K);
+gq_status gq_prepare_q4_0(const void *W, int64_t M, int64_t K, int64_t row_stride, void *out, void *stream);
+
+/* MUL_MAT on prepared weights (gq_prepare_q4_0): the result of
+ * gq_mul_mat_q4_0 on the original W, through the fast kernels for any K % 32
+ * == 0 (the decode kernel below the tensor-core threshold, else X -> bf16 and
+ * the tcgen05 kernel; the zero blocks meet zero x).  K < 256 always takes the
+ * decode kernel, 64 tokens per launch: with so few terms the bf16 rounding of
+ * the tensor-core path does not average below the tolerance.  Wp, X, Y
+ * 16-byte aligned; scratch as gq_mul_mat_q4_0. */
+gq_status gq_mul_mat_q4_0_prepared(const void *Wp, int64_t M, int64_t K, const float *X, int64_t N, float *Y,
+                                   void *stream);
+
 /* MUL_MAT with activations the caller already holds in bf16: X_bf16[N][K]
  * (raw bfloat16 bits).  Runs the tensor-core kernel for every N >= 1.  Its
  * only allocation is the stream-ordered partial-sum scratch of split tiles

@@ -56,6 +56,9 @@ SIGNATURES = {
     "gq_mul_mat": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "gq_quantize_q4_0": (_i32, [_vp, _i64, _i64, _vp, _vp]),
     "gq_mul_mat_q4_0": (_i32, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
+    "gq_prepared_q4_0_nbytes": (_sz, [_i64, _i64]),
+    "gq_prepare_q4_0": (_i32, [_vp, _i64, _i64, _i64, _vp, _vp]),
+    "gq_mul_mat_q4_0_prepared": (_i32, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "gq_mul_mat_id_q4_0": (_i32, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp]),
     "gq_mul_mat_q4_0_bf16x": (_i32, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "gq_mul_mat_q4_0_noalloc": (_i32, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
@@ -145,6 +148,18 @@ def gq_quantize_q4_0(W, M: int, K: int, out, stream=None) -> None:
 
 def gq_mul_mat_q4_0(W, M: int, K: int, X, N: int, Y, stream=None) -> None:
     _check(_lib.gq_mul_mat_q4_0(_ptr(W), M, K, _ptr(X), N, _ptr(Y), _stream(stream)))
+
+
+def gq_prepared_q4_0_nbytes(M: int, K: int) -> int:
+    return int(_lib.gq_prepared_q4_0_nbytes(M, K))
+
+
+def gq_prepare_q4_0(W, M: int, K: int, row_stride: int, out, stream=None) -> None:
+    _check(_lib.gq_prepare_q4_0(_ptr(W), M, K, row_stride, _ptr(out), _stream(stream)))
+
+
+def gq_mul_mat_q4_0_prepared(Wp, M: int, K: int, X, N: int, Y, stream=None) -> None:
+    _check(_lib.gq_mul_mat_q4_0_prepared(_ptr(Wp), M, K, _ptr(X), N, _ptr(Y), _stream(stream)))
 
 
 def gq_mul_mat_id_q4_0(W, n_expert: int, M: int, K: int, X, n_ids: int, ids, T: int, Y, stream=None) -> None:
@@ -279,4 +294,25 @@ def mul_mat(qtype: int, W: torch.Tensor, X: torch.Tensor, stream=None, out: torc
     M = _rows_of(W, qtype, K)
     Y = out if out is not None else torch.empty((N, M), dtype=torch.float32, device=X.device)
     gq_mul_mat(qtype, W, M, K, X, N, Y, stream)
+    return Y
+
+
+def prepare_q4_0(W: torch.Tensor, K: int, row_stride: int = 0, M: int | None = None, stream=None) -> torch.Tensor:
+    """Q4_0 rows (packed, or row_stride bytes apart) -> the prepared layout
+    (uint8 [M, ceil(K/256)*144])."""
+    if W.dtype != torch.uint8:
+        raise TypeError("W must be uint8 (raw block_q4_0 bytes)")
+    if M is None:
+        M = _check_w(W, K) if row_stride == 0 else W.numel() // row_stride
+    out = torch.empty((M, gq_prepared_q4_0_nbytes(1, K)), dtype=torch.uint8, device=W.device)
+    gq_prepare_q4_0(W, M, K, row_stride, out, stream)
+    return out
+
+
+def mul_mat_q4_0_prepared(Wp: torch.Tensor, X: torch.Tensor, stream=None) -> torch.Tensor:
+    """Y[N, M] = X[N, K] @ dequant(W)^T with Wp = prepare_q4_0(W, K)."""
+    N, K = X.shape
+    M = Wp.shape[0]
+    Y = torch.empty((N, M), dtype=torch.float32, device=X.device)
+    gq_mul_mat_q4_0_prepared(Wp, M, K, X, N, Y, stream)
     return Y

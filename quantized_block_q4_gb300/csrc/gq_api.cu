@@ -181,13 +181,16 @@ cudaError_t scratch_free(void* p, cudaStream_t s) { return cudaFreeAsync(p, s); 
 
 using namespace gq;
 
+// W_row_bytes: the stride of W's rows (K/32*18, or the prepared layout's
+// ceil(K/256)*144, whose zero blocks pad each row to whole 256-k boxes).
 static gq_status mul_mat_decode(const void* W, int64_t M, int64_t K, const float* X, int64_t N, float* Y,
-                                cudaStream_t s) {
+                                cudaStream_t s, int64_t W_row_bytes = 0) {
   CUtensorMap tm;
   uint32_t bx = 0, by = 0;
   const int variant = static_cast<int>(g_decode_variant.load());
   decode_w_box(N, variant, &bx, &by);
-  const uint64_t row_bytes = static_cast<uint64_t>(K / kQK) * kBlockBytes;
+  const uint64_t row_bytes =
+      W_row_bytes > 0 ? static_cast<uint64_t>(W_row_bytes) : static_cast<uint64_t>(K / kQK) * kBlockBytes;
   gq_status st = make_tmap(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, row_bytes, static_cast<uint64_t>(M), row_bytes,
                            bx, by, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (st != GQ_OK) return st;
@@ -196,19 +199,22 @@ static gq_status mul_mat_decode(const void* W, int64_t M, int64_t K, const float
   return e == cudaSuccess ? GQ_OK : cuda_fail(e, "decode launch");
 }
 
+// Kw: the width of W's rows in weights (K, or K rounded up to 256 for the
+// prepared layout; x beyond K reads as zeros through the tensor map).
 static gq_status mul_mat_prefill_bf16(const void* W, int64_t M, int64_t K, const uint16_t* Xb, int64_t N, float* Y,
-                                      bool allow_scratch, cudaStream_t s, int type = GQ_TYPE_Q4_0) {
+                                      bool allow_scratch, cudaStream_t s, int type = GQ_TYPE_Q4_0, int64_t Kw = 0) {
   CUtensorMap tmW, tmX;
   uint32_t wbx, web, wby, xbk, xbr;
   prefill_boxes(N, type, &wbx, &web, &wby, &xbk, &xbr);
-  const uint64_t row_bytes = static_cast<uint64_t>(K / kQK) * static_cast<uint64_t>(type_block_bytes(type));
+  if (Kw <= 0) Kw = K;
+  const uint64_t row_bytes = static_cast<uint64_t>(Kw / kQK) * static_cast<uint64_t>(type_block_bytes(type));
   gq_status st = make_tmap(&tmW, web == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, W,
                            row_bytes / web, static_cast<uint64_t>(M), row_bytes, wbx, wby, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (st != GQ_OK) return st;
   st = make_tmap(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Xb, static_cast<uint64_t>(K), static_cast<uint64_t>(N),
                  static_cast<uint64_t>(K) * 2, xbk, xbr, CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != GQ_OK) return st;
-  cudaError_t e = launch_prefill(&tmW, &tmX, N, M, K, Y, static_cast<uint64_t>(g_wait_limit_ns.load()), allow_scratch,
+  cudaError_t e = launch_prefill(&tmW, &tmX, N, M, Kw, Y, static_cast<uint64_t>(g_wait_limit_ns.load()), allow_scratch,
                                  s, type);
   return e == cudaSuccess ? GQ_OK : cuda_fail(e, "prefill launch");
 }
@@ -443,6 +449,75 @@ gq_status gq_mul_mat_id_q4_0(const void* W, int64_t n_expert, int64_t M, int64_t
   if (st != GQ_OK) return st;
   if (e != cudaSuccess) return cuda_fail(e, what);
   return f == cudaSuccess ? GQ_OK : cuda_fail(f, "scratch free");
+}
+
+size_t gq_prepared_q4_0_nbytes(int64_t M, int64_t K) {
+  if (M < 0 || K < 0 || K % kQK) return 0;
+  return static_cast<size_t>(M) * static_cast<size_t>(prepared_row_bytes(K));
+}
+
+gq_status gq_prepare_q4_0(const void* W, int64_t M, int64_t K, int64_t row_stride, void* out, void* stream) {
+  t_last_error.clear();
+  if (M < 0 || K < 0) return fail(GQ_ERR_SHAPE, "negative size");
+  if (K % kQK) return fail(GQ_ERR_SHAPE, "K=%lld is not a multiple of 32", (long long)K);
+  const int64_t src_row = (K / kQK) * kBlockBytes;
+  if (row_stride == 0) row_stride = src_row;
+  if (row_stride < src_row)
+    return fail(GQ_ERR_SHAPE, "row_stride=%lld is shorter than a row (%lld bytes)", (long long)row_stride,
+                (long long)src_row);
+  if (M == 0 || K == 0) return GQ_OK;
+  if (!W || !out) return fail(GQ_ERR_NULL, "W and out must not be NULL");
+  if (!aligned(out, 16)) return fail(GQ_ERR_ALIGN, "out must be 16-byte aligned");
+  if ((unsigned __int128)M * row_stride > ((unsigned __int128)1 << 62)) return fail(GQ_ERR_SHAPE, "size overflows");
+  gq_status st = check_device();
+  if (st != GQ_OK) return st;
+  cudaError_t e = launch_prepare_q4_0(static_cast<const uint8_t*>(W), M, K, row_stride, static_cast<uint8_t*>(out),
+                                      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GQ_OK : cuda_fail(e, "prepare launch");
+}
+
+gq_status gq_mul_mat_q4_0_prepared(const void* Wp, int64_t M, int64_t K, const float* X, int64_t N, float* Y,
+                                   void* stream) {
+  t_last_error.clear();
+  gq_status st = check_mm_shape(M, K, N);
+  if (st != GQ_OK) return st;
+  if (M == 0 || N == 0) return GQ_OK;
+  if (!Y) return fail(GQ_ERR_NULL, "Y must not be NULL");
+  st = check_device();
+  if (st != GQ_OK) return st;
+  auto s = static_cast<cudaStream_t>(stream);
+  if (K == 0) {
+    cudaError_t e = cudaMemsetAsync(Y, 0, static_cast<size_t>(N) * M * sizeof(float), s);
+    return e == cudaSuccess ? GQ_OK : cuda_fail(e, "memset");
+  }
+  if (!Wp || !X) return fail(GQ_ERR_NULL, "Wp and X must not be NULL");
+  if (!aligned(Wp, 16) || !aligned(X, 16) || !aligned(Y, 16))
+    return fail(GQ_ERR_ALIGN, "Wp, X and Y must be 16-byte aligned");
+  const int64_t Kw = (K + 255) / 256 * 256;
+  if (N < g_prefill_min_n.load() && N <= 64) return mul_mat_decode(Wp, M, K, X, N, Y, s, prepared_row_bytes(K));
+  if (K < 256) {
+    // Fewer than 256 terms: bf16 operands (relative 2^-9 each) do not average
+    // below the 1e-3 * sum|w x| tolerance; the decode kernel (exact W, fp16 x)
+    // runs in chunks of 64 tokens instead.
+    for (int64_t n0 = 0; n0 < N; n0 += 64) {
+      st = mul_mat_decode(Wp, M, K, X + n0 * K, std::min<int64_t>(64, N - n0), Y + n0 * M, s, prepared_row_bytes(K));
+      if (st != GQ_OK) return st;
+    }
+    return GQ_OK;
+  }
+  const size_t xbytes = static_cast<size_t>(N) * K * sizeof(uint16_t);
+  void* xb = nullptr;
+  cudaError_t e = scratch_alloc(&xb, xbytes, s);
+  if (e != cudaSuccess) return fail(GQ_ERR_ALLOC, "scratch allocation (%zu bytes): %s", xbytes, cudaGetErrorString(e));
+  e = launch_f32_to_bf16(X, static_cast<uint16_t*>(xb), N * K, s);
+  if (e != cudaSuccess) {
+    scratch_free(xb, s);
+    return cuda_fail(e, "f32->bf16 launch");
+  }
+  st = mul_mat_prefill_bf16(Wp, M, K, static_cast<const uint16_t*>(xb), N, Y, true, s, GQ_TYPE_Q4_0, Kw);
+  e = scratch_free(xb, s);
+  if (st != GQ_OK) return st;
+  return e == cudaSuccess ? GQ_OK : cuda_fail(e, "scratch free");
 }
 
 gq_status gq_mul_mat_q4_0_bf16x(const void* W, int64_t M, int64_t K, const uint16_t* X_bf16, int64_t N, float* Y,

@@ -297,7 +297,16 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
         const int st = e / (kBoxBlocks * Nt), rem = e % (kBoxBlocks * Nt);
         const int bl = st * (Cfg::kStageK / kQK) + kw * kBoxBlocks + rem / Nt;  // block within the chunk
         const int n = rem % Nt;
-        if (kc0 + bl * kQK >= kend) continue;
+        if (kc0 + bl * kQK >= kend) {
+          // Past K inside the last 256-k box (rows padded to a multiple of 256
+          // weights with zero blocks): zero x, so that the zero blocks add
+          // exact zeros rather than whatever the slot held before.
+          uint4* dst = xs + (bl * N + n) * 4;
+          dst[0] = dst[1] = dst[2] = dst[3] = make_uint4(0u, 0u, 0u, 0u);
+          cs[bl * csn + n] = 0.f;
+          if ((Nt & 1) && n == Nt - 1) cs[bl * csn + Nt] = 0.f;
+          continue;
+        }
         float xv[32];
         const float4* xr =
             reinterpret_cast<const float4*>(X + xrow(n) * K + static_cast<size_t>(kc0 + bl * kQK));

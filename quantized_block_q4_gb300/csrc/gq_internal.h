@@ -112,6 +112,11 @@ cudaError_t launch_dequant_legacy(int type, const uint8_t* W, int64_t nblocks, f
 cudaError_t launch_mul_mat_legacy(int type, const uint8_t* W, int64_t M, int64_t K, const float* X, int64_t N,
                                   float* Y, uint64_t wait_limit_ns, cudaStream_t s);
 
+// ---- KP: Q4_0 repack into rows of a multiple of 256 weights (gq_prepare.cu)
+int64_t prepared_row_bytes(int64_t K);  // ceil(K / 256) * 144
+cudaError_t launch_prepare_q4_0(const uint8_t* W, int64_t M, int64_t K, int64_t row_stride, uint8_t* out,
+                                cudaStream_t s);
+
 // ---- helpers of the C ABI (gq_api.cu) for entry points defined in other files
 gq_status api_fail(gq_status st, const char* msg);  // records the per-thread error text
 gq_status api_check_device();
