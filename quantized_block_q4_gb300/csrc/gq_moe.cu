@@ -269,7 +269,9 @@ bool moe_route_supported(int64_t E) { return E >= 1 && route_warps(static_cast<i
 
 cudaError_t launch_moe_route(const int32_t* ids, int64_t P, int64_t E, int64_t n_mtiles, int bn, int cap,
                              const MoeRoute& rt, float* Y, int64_t M, cudaStream_t s) {
-  const int nw = route_warps(static_cast<int>(E));
+  // One warp per 64 pairs up to the shared-memory limit: a decode batch of a
+  // few pairs needs one warp and no cross-warp work.
+  const int nw = std::max(1, std::min(route_warps(static_cast<int>(E)), static_cast<int>((P + 63) / 64)));
   const size_t smem = (static_cast<size_t>(nw) + 1) * static_cast<size_t>(E + 1) * sizeof(int);
   static size_t configured = 48 * 1024;
   if (smem > configured) {
