@@ -351,7 +351,8 @@ def run_gpu(args, rank, world, dist):
                             "per_launch": "M*K*18/32 + 4*N*K + 4*N*M bytes; graph-replay time incl. launch gaps"},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
                 "d2h_bytes_per_step": e2e["d2h"],
-                "path": "pinned host X -> device, gq_mul_mat_q4_0, Y -> pinned host, per matrix (decode sweep)"},
+                "path": "per step: the step's activations pinned host -> device in one copy, the 224 "
+                        "gq_mul_mat_q4_0 calls, every Y -> pinned host in one copy (decode sweep)"},
         "dequant": aux.get("dequant"),
         "quantize": aux.get("quantize"),
         "mul_mat_id": aux.get("mul_mat_id"),
@@ -560,22 +561,32 @@ def run_prepared_aux(gq, torch, dev, s, peaks):
 
 
 def run_e2e(gq, torch, dev, s, W, shapes, acts1, order, L, args):
-    """Decode sweep through gq_mul_mat_q4_0 with host buffers: every step copies
-    each layer's activations from pinned host memory and every result back."""
-    hx = [[torch.from_numpy(a).pin_memory() for a in la] for la in acts1]
-    dx = [[torch.empty(a.shape, dtype=torch.float32, device=dev) for a in la] for la in acts1]
-    dy = [torch.empty(DECODE_N, M, device=dev) for M, _ in shapes]
-    hy = [torch.empty(DECODE_N, M).pin_memory() for M, _ in shapes]
+    """Decode sweep through gq_mul_mat_q4_0 with host buffers.  Every step
+    copies the step's inputs (all layers' activations, one pinned buffer) to
+    the device in one copy, runs the 224 calls, and copies the step's results
+    (every Y, one device buffer) back to pinned host memory in one copy, as a
+    decode step moves its inputs and outputs once."""
+    xs = [a for la in acts1 for a in la]
+    x_off = np.cumsum([0] + [a.size for a in xs])
+    hx = torch.from_numpy(np.concatenate([a.reshape(-1) for a in xs])).pin_memory()
+    dx = torch.empty(hx.numel(), dtype=torch.float32, device=dev)
+    y_sizes = [DECODE_N * M for M, _ in shapes]
+    y_off = np.cumsum([0] + y_sizes)
+    dy = torch.empty(int(y_off[-1]), device=dev)
+    hy = torch.empty(int(y_off[-1])).pin_memory()
+    nper = len(acts1[0])
+    xview = [[dx[int(x_off[l * nper + i]):int(x_off[l * nper + i + 1])].view(acts1[l][i].shape)
+              for i in range(nper)] for l in range(L)]
+    yview = [dy[int(y_off[i]):int(y_off[i + 1])] for i in range(len(shapes))]
 
     def one():
+        dx.copy_(hx, non_blocking=True)
         for layer in range(L):
-            for i in range(len(hx[layer])):
-                dx[layer][i].copy_(hx[layer][i], non_blocking=True)
             for j in range(len(order)):
                 i = layer * len(order) + j
                 M, K = shapes[i]
-                gq.gq_mul_mat_q4_0(W[i], M, K, dx[layer][order[j]], DECODE_N, dy[i], stream=s)
-                hy[i].copy_(dy[i], non_blocking=True)
+                gq.gq_mul_mat_q4_0(W[i], M, K, xview[layer][order[j]], DECODE_N, yview[i], stream=s)
+        hy.copy_(dy, non_blocking=True)
 
     with torch.cuda.stream(s):
         one()
@@ -596,9 +607,7 @@ def run_e2e(gq, torch, dev, s, W, shapes, acts1, order, L, args):
             g.replay()
         e1.record(s)
     e1.synchronize()
-    h2d = sum(t.numel() * 4 for la in hx for t in la)
-    d2h = sum(t.numel() * 4 for t in hy)
-    return {"ms": e0.elapsed_time(e1) / args.steps, "h2d": h2d, "d2h": d2h}
+    return {"ms": e0.elapsed_time(e1) / args.steps, "h2d": hx.numel() * 4, "d2h": hy.numel() * 4}
 
 
 # DRAM bytes (read + write) per launch, from one ncu capture per shape of the
