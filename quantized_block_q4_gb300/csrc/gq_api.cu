@@ -403,7 +403,7 @@ gq_status gq_mul_mat_id_q4_0(const void* W, int64_t n_expert, int64_t M, int64_t
   const int64_t used = std::min(n_expert, P);
   const int64_t path = g_moe_path.load();
   const bool tc = path == 2 || (path == 0 && P >= 16 * used);
-  const int cap = decode_moe_cap(P, n_expert);
+  const int cap = decode_moe_cap(P, n_expert, T);
   const int64_t n_mtiles = (M + 127) / 128;
   if (tc && n_mtiles * ((P + kMoeBN - 1) / kMoeBN + used) > lim)
     return fail(GQ_ERR_SHAPE, "too many tensor-core work items");
@@ -419,7 +419,7 @@ gq_status gq_mul_mat_id_q4_0(const void* W, int64_t n_expert, int64_t M, int64_t
   const int pdl = static_cast<int>(g_pdl.load());
   const uint64_t row_bytes = static_cast<uint64_t>(K / kQK) * kBlockBytes;
   const char* what = "MUL_MAT_ID routing launch";
-  e = launch_moe_route(ids, P, n_expert, n_mtiles, kMoeBN, cap, rt, Y, M, s);
+  e = launch_moe_route(ids, P, n_expert, n_mtiles, kMoeBN, cap, rt, Y, M, pdl, s);
   if (e == cudaSuccess && !tc) {
     CUtensorMap tm;
     uint32_t bx = 0, by = 0;

@@ -134,7 +134,8 @@ constexpr int decode_min_blocks() {
 }
 
 // MOE: MUL_MAT_ID over the decode groups of rt (expert e, up to N tokens
-// each).  N is then the group capacity, which fixes the shared-memory layout;
+// each; with ONE, one token).  N is then the group capacity, which fixes the
+// shared-memory layout;
 // a group's own token count Nt <= N sets the work.  W rows of expert e start
 // at e * M; x and Y rows are the pairs perm[first + n].  The CTAs are shared
 // out evenly among the groups (each CTA taking every cpg-th tile of its
@@ -144,7 +145,6 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
     k_decode_q4_0(const __grid_constant__ CUtensorMap tmW, const float* __restrict__ X, int N, int M, int K,
                   int KX, float* __restrict__ Y, uint64_t limit_ns, uint32_t* err, int early_stages,
                   int x_static, const MoeRoute rt) {
-  static_assert(!(MOE && ONE), "MUL_MAT_ID uses the general token path");
   using Cfg = DecodeCfg<NT, MT, KW, STAGES>;
   constexpr int kBM = Cfg::kBM;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -607,9 +607,12 @@ cudaError_t launch_decode(const CUtensorMap* tmW, const float* X, int64_t N, int
   return launch_cfg<8, 1, 2, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
 }
 
-// MUL_MAT_ID group capacity: room for twice the mean tokens per used expert
-// (an expert with more tokens than that runs as several groups).
-int decode_moe_cap(int64_t P, int64_t E) {
+// MUL_MAT_ID group capacity: one token for a single-token batch (its slots
+// pick distinct experts, so every group holds one token and the N = 1 kernel
+// runs), else room for twice the mean tokens per used expert (an expert with
+// more tokens than that runs as several groups).
+int decode_moe_cap(int64_t P, int64_t E, int64_t T) {
+  if (T == 1) return 1;
   const int64_t used = std::max<int64_t>(1, std::min(E, P));
   const int64_t want = 2 * ((P + used - 1) / used);
   return want <= 8 ? 8 : want <= 16 ? 16 : want <= 32 ? 32 : 64;
@@ -625,6 +628,8 @@ cudaError_t launch_decode_moe(const CUtensorMap* tmW, const float* X, int cap, i
                               cudaStream_t s) {
   const int m = static_cast<int>(M), k = static_cast<int>(K);
   const int64_t max_groups = std::min(E, P) + P / cap + 1;
+  if (cap == 1)
+    return launch_cfg<1, 2, 8, 3, true, true>(tmW, X, 1, m, k, Y, wait_limit_ns, 64 << 10, 0, pdl, s, rt, max_groups);
   if (cap == 8)
     return launch_cfg<1, 2, 8, 3, false, true>(tmW, X, 8, m, k, Y, wait_limit_ns, 64 << 10, 0, pdl, s, rt, max_groups);
   if (cap == 16)

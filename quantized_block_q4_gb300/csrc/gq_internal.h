@@ -87,7 +87,7 @@ size_t moe_route_ints(int64_t E, int64_t P, int cap);
 MoeRoute moe_route_layout(int32_t* base, int64_t E, int64_t P, int cap);
 bool moe_route_supported(int64_t E);
 cudaError_t launch_moe_route(const int32_t* ids, int64_t P, int64_t E, int64_t n_mtiles, int bn, int cap,
-                             const MoeRoute& rt, float* Y, int64_t M, cudaStream_t s);
+                             const MoeRoute& rt, float* Y, int64_t M, int pdl, cudaStream_t s);
 cudaError_t launch_moe_gather_bf16(const float* X, int64_t P, int64_t K, const MoeRoute& rt, uint16_t* Xg,
                                    int pdl, cudaStream_t s);
 cudaError_t launch_generic_id(const uint8_t* W, int64_t E, int64_t M, int64_t K, const float* X,
@@ -100,7 +100,7 @@ cudaError_t launch_prefill_moe(const CUtensorMap* tmW, const CUtensorMap* tmX, i
                                cudaStream_t s);
 // Decode MUL_MAT_ID over the decode groups (gq_decode.cu); returns the group
 // capacity the launch will use through decode_moe_cap first.
-int decode_moe_cap(int64_t P, int64_t E);
+int decode_moe_cap(int64_t P, int64_t E, int64_t T);
 void decode_moe_w_box(int cap, uint32_t* box_x_bytes, uint32_t* box_rows);
 cudaError_t launch_decode_moe(const CUtensorMap* tmW, const float* X, int cap, int64_t E, int64_t M, int64_t K,
                               int64_t P, const MoeRoute& rt, float* Y, uint64_t wait_limit_ns, int pdl,

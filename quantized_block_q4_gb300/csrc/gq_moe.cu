@@ -268,7 +268,7 @@ MoeRoute moe_route_layout(int32_t* base, int64_t E, int64_t P, int cap) {
 bool moe_route_supported(int64_t E) { return E >= 1 && route_warps(static_cast<int>(E)) >= 1; }
 
 cudaError_t launch_moe_route(const int32_t* ids, int64_t P, int64_t E, int64_t n_mtiles, int bn, int cap,
-                             const MoeRoute& rt, float* Y, int64_t M, cudaStream_t s) {
+                             const MoeRoute& rt, float* Y, int64_t M, int pdl, cudaStream_t s) {
   // One warp per 64 pairs up to the shared-memory limit: a decode batch of a
   // few pairs needs one warp and no cross-warp work.
   const int nw = std::max(1, std::min(route_warps(static_cast<int>(E)), static_cast<int>((P + 63) / 64)));
@@ -280,9 +280,20 @@ cudaError_t launch_moe_route(const int32_t* ids, int64_t P, int64_t E, int64_t n
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  k_moe_route<<<1, 32 * nw, smem, s>>>(ids, static_cast<int>(P), static_cast<int>(E), static_cast<int>(n_mtiles),
-                                        bn, cap, rt, Y, static_cast<int>(M), device_error_word());
-  return cudaGetLastError();
+  // With programmatic dependent launch the routing CTA starts while the
+  // previous kernel drains; it reads ids only after griddepcontrol.wait.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(32 * nw);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_moe_route, ids, static_cast<int>(P), static_cast<int>(E),
+                            static_cast<int>(n_mtiles), bn, cap, rt, Y, static_cast<int>(M), device_error_word());
 }
 
 cudaError_t launch_moe_gather_bf16(const float* X, int64_t P, int64_t K, const MoeRoute& rt, uint16_t* Xg,

@@ -186,3 +186,15 @@ def test_decode_full_size():
     """Decode-sized batch on full-size experts: 4 tokens x 2 slots."""
     E, M, K, T, S = 8, 14336, 4096, 4, 2
     check(E, M, K, T, S, seed=12900)
+
+
+@pytest.mark.parametrize("path", [DECODE, TC])
+def test_single_token_repeated_expert(path):
+    """One token whose slots name the same expert twice (and a third slot
+    another): the single-token decode path runs one group per slot."""
+    ids = np.array([[3, 3, 5]], dtype=np.int32)
+    check(8, 700, 1024, 1, 3, seed=12950, path=path, ids=ids)
+
+
+def test_single_token_many_slots():
+    check(64, 512, 2048, 1, 8, seed=12960, path=DECODE)
