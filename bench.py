@@ -510,7 +510,9 @@ def run_legacy_aux(gq, torch, dev, s, peaks):
             "dequant": {"us": round(td * 1e6, 2), "achieved": round(dq, 1), "unit": "GB/s", "bound": "hbm",
                         "frac": round(dq / peaks["hbm_gbs"], 4)},
             "mul_mat_n1": {"us": round(t1 * 1e6, 2), "achieved": round(g1, 1), "unit": "GB/s", "bound": "hbm",
-                           "frac": round(g1 / peaks["hbm_gbs"], 4), "kernel": "k_mul_mat_legacy_bulk (scalar)"},
+                           "frac": round(g1 / peaks["hbm_gbs"], 4),
+                           "kernel": ("k_decode_q4_0<1, 2, 8, 3, 1, 0, 1> (mma.sync decode, 20-byte blocks)"
+                                      if qt == gq.GQ_TYPE_Q4_1 else "k_mul_mat_legacy_bulk (scalar)")},
             "mul_mat_n512": {"us": round(tp * 1e6, 2), "achieved": round(tf, 2), "unit": "TFLOP/s",
                              "bound": "tensor", "frac": round(tf / peaks["bf16_tflops"], 4),
                              "kernel": "k_f32_to_bf16 + k_prefill_q4_0<256, 0, 0, type>"},

@@ -298,6 +298,18 @@ gq_status gq_mul_mat(gq_type type, const void* W, int64_t M, int64_t K, const fl
   // on, the tensor-core kernel with this block format is faster.
   const bool tc = N >= 2 && K % 256 == 0 && aligned(W, 16) && aligned(X, 16) && aligned(Y, 16) &&
                   !g_force_generic.load();
+  if (type == GQ_TYPE_Q4_1 && N == 1 && K % 256 == 0 && aligned(W, 16) && aligned(X, 16) && aligned(Y, 16) &&
+      !g_force_generic.load()) {
+    // the decode kernel on 20-byte blocks
+    CUtensorMap tm;
+    const uint64_t row_bytes = static_cast<uint64_t>(K / kQK) * 20;
+    st = make_tmap(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, row_bytes, static_cast<uint64_t>(M), row_bytes, 160, 32,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != GQ_OK) return st;
+    cudaError_t e = launch_decode_q41(&tm, X, M, K, Y, static_cast<uint64_t>(g_wait_limit_ns.load()),
+                                      static_cast<int>(g_early_w.load()), static_cast<int>(g_pdl.load()), s);
+    return e == cudaSuccess ? GQ_OK : cuda_fail(e, "decode launch");
+  }
   if (!tc) {
     cudaError_t e = launch_mul_mat_legacy(type, static_cast<const uint8_t*>(W), M, K, X, N, Y,
                                           static_cast<uint64_t>(g_wait_limit_ns.load()), s);

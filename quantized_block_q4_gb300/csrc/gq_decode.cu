@@ -41,14 +41,22 @@ namespace gq {
 namespace {
 
 constexpr int kSubK = 256;         // weights per row per TMA box
-constexpr int kSubBytesRow = 144;  // 8 blocks x 18 bytes
+constexpr int kSubBytesRow = 144;  // 8 blocks x 18 bytes (Q4_0)
+
+// Bytes of one row of a TMA box (8 blocks): Q4_0 144, Q4_1 160.
+template <int F>
+constexpr int sub_bytes_row() { return F == GQ_TYPE_Q4_1 ? 160 : kSubBytesRow; }
 
 // NT: n8 token tiles (N <= 8*NT); MT: m16 row tiles per warp (tile = 16*MT
-// rows); KW: consumer warps, each taking one 256-k box of every stage.
-template <int NT, int MT, int KW, int STAGES>
+// rows); KW: consumer warps, each taking one 256-k box of every stage; F: the
+// block format (Q4_0, or Q4_1 whose min offset needs a second per-block table
+// of x sums).
+template <int NT, int MT, int KW, int STAGES, int F = GQ_TYPE_Q4_0>
 struct DecodeCfg {
   static constexpr int kBM = 16 * MT;
-  static constexpr int kSubBytes = kBM * kSubBytesRow;
+  static constexpr int kRowBytes = sub_bytes_row<F>();
+  static constexpr int kTables = F == GQ_TYPE_Q4_1 ? 2 : 1;
+  static constexpr int kSubBytes = kBM * kRowBytes;
   static constexpr int kThreads = 32 * (KW + 1);
   static constexpr int kStageK = kSubK * KW;
   static constexpr int kStageBytes = kSubBytes * KW;
@@ -63,8 +71,8 @@ struct DecodeCfg {
     return static_cast<size_t>(KX / 32) * cs_stride(N) * sizeof(float);
   }
   static size_t smem_bytes(int N, int KX) {
-    return kRingBytes + xs_bytes(N, KX) + cs_bytes(N, KX) + (kSlots * slot_floats(N) + kSlots) * sizeof(float) +
-           (2 * STAGES + 1) * 8 + 16 + 128;
+    return kRingBytes + xs_bytes(N, KX) + kTables * cs_bytes(N, KX) +
+           (kSlots * slot_floats(N) + kSlots) * sizeof(float) + (2 * STAGES + 1) * 8 + 16 + 128;
   }
 };
 
@@ -126,6 +134,37 @@ __device__ __forceinline__ float stage_block(const float (&x)[32], uint4* dst) {
   return -bias;
 }
 
+// Q4_1 x staging: the natural k order (a lane owns code bytes 4t .. 4t+3 of
+// every block, like an odd Q4_0 block), codes biased by 1024 with no zero
+// point (A = 1024 + q for low nibbles, 1024 + 16q against x/16 for high
+// ones), so the bias is 1024 * (sum of the fp16 x and x/16 values).  Also the
+// block's sum of x as the MMA sees it (fp16 x, 16 * fp16(x/16)), which the
+// min offset multiplies.
+__device__ __forceinline__ float stage_block_q41(const float (&x)[32], uint4* dst, float* sx) {
+  float bias = 0.f, sum = 0.f;
+  __half xh[32];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    xh[j] = __float2half_rn(x[j]);
+    xh[16 + j] = __float2half_rn(x[16 + j] * 0.0625f);
+    bias += __half2float(xh[j]) + __half2float(xh[16 + j]);
+    sum = fmaf(16.f, __half2float(xh[16 + j]), sum + __half2float(xh[j]));
+  }
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const int c0 = 4 * t, c1 = 4 * t + 1, c2 = 4 * t + 2, c3 = 4 * t + 3;
+    __half2 h;
+    uint4 pk;
+    h = __halves2half2(xh[c0], xh[c2]); pk.x = *reinterpret_cast<uint32_t*>(&h);
+    h = __halves2half2(xh[c1], xh[c3]); pk.y = *reinterpret_cast<uint32_t*>(&h);
+    h = __halves2half2(xh[16 + c0], xh[16 + c2]); pk.z = *reinterpret_cast<uint32_t*>(&h);
+    h = __halves2half2(xh[16 + c1], xh[16 + c3]); pk.w = *reinterpret_cast<uint32_t*>(&h);
+    dst[t] = pk;
+  }
+  *sx = sum;
+  return -1024.f * bias;
+}
+
 // Two CTAs per SM only where the ring leaves room for a second one; otherwise
 // let the kernel use the registers of a single CTA.
 template <int NT, int MT, int KW, int STAGES>
@@ -140,19 +179,21 @@ constexpr int decode_min_blocks() {
 // at e * M; x and Y rows are the pairs perm[first + n].  The CTAs are shared
 // out evenly among the groups (each CTA taking every cpg-th tile of its
 // group), or, with more groups than CTAs, CTA b runs groups b, b + grid, ...
-template <int NT, int MT, int KW, int STAGES, bool ONE, bool MOE = false>
+template <int NT, int MT, int KW, int STAGES, bool ONE, bool MOE = false, int F = GQ_TYPE_Q4_0>
 __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, STAGES>()))
     k_decode_q4_0(const __grid_constant__ CUtensorMap tmW, const float* __restrict__ X, int N, int M, int K,
                   int KX, float* __restrict__ Y, uint64_t limit_ns, uint32_t* err, int early_stages,
                   int x_static, const MoeRoute rt) {
-  using Cfg = DecodeCfg<NT, MT, KW, STAGES>;
+  static_assert(F == GQ_TYPE_Q4_0 || (F == GQ_TYPE_Q4_1 && !MOE), "Q4_1 runs the plain MUL_MAT layout");
+  using Cfg = DecodeCfg<NT, MT, KW, STAGES, F>;
   constexpr int kBM = Cfg::kBM;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   uint8_t* ring = smem;
   uint4* xs = reinterpret_cast<uint4*>(smem + Cfg::kRingBytes);
   float* cs = reinterpret_cast<float*>(smem + Cfg::kRingBytes + Cfg::xs_bytes(N, KX));
-  float* acc_slots = cs + Cfg::cs_bytes(N, KX) / sizeof(float);  // [kSlots][KW][kBM][N]
+  float* sxs = cs + Cfg::cs_bytes(N, KX) / sizeof(float);  // Q4_1: per-block x sums, laid out like cs
+  float* acc_slots = cs + Cfg::kTables * Cfg::cs_bytes(N, KX) / sizeof(float);  // [kSlots][KW][kBM][N]
   const int csn = Cfg::cs_stride(N);
   const int slot_floats = static_cast<int>(Cfg::slot_floats(N));
   int* slot_count = reinterpret_cast<int*>(acc_slots + Cfg::kSlots * slot_floats);
@@ -236,7 +277,7 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
             const uint32_t full = smem_u32(&bars[slot]);
             mbar_arrive_expect_tx(full, nvalid * Cfg::kSubBytes);
             for (int j = 0; j < nvalid; ++j) {
-              const int xb = ((k0 + j * kSubK) / kSubK) * kSubBytesRow;  // byte column in the row
+              const int xb = ((k0 + j * kSubK) / kSubK) * Cfg::kRowBytes;  // byte column in the row
               tma_load_2d(smem_u32(ring + slot * Cfg::kStageBytes + j * Cfg::kSubBytes), &tmW, xb,
                           wrow0 + tile * kBM, full);
             }
@@ -305,6 +346,10 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
           dst[0] = dst[1] = dst[2] = dst[3] = make_uint4(0u, 0u, 0u, 0u);
           cs[bl * csn + n] = 0.f;
           if ((Nt & 1) && n == Nt - 1) cs[bl * csn + Nt] = 0.f;
+          if (F == GQ_TYPE_Q4_1) {
+            sxs[bl * csn + n] = 0.f;
+            if ((Nt & 1) && n == Nt - 1) sxs[bl * csn + Nt] = 0.f;
+          }
           continue;
         }
         float xv[32];
@@ -316,7 +361,12 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
           xv[4 * i] = v.x; xv[4 * i + 1] = v.y; xv[4 * i + 2] = v.z; xv[4 * i + 3] = v.w;
         }
         uint4* dst = xs + (bl * N + n) * 4;
-        cs[bl * csn + n] = ((kc0 / kQK + bl) & 1) ? stage_block<1>(xv, dst) : stage_block<0>(xv, dst);
+        if constexpr (F == GQ_TYPE_Q4_1) {
+          cs[bl * csn + n] = stage_block_q41(xv, dst, &sxs[bl * csn + n]);
+          if ((Nt & 1) && n == Nt - 1) sxs[bl * csn + Nt] = 0.f;
+        } else {
+          cs[bl * csn + n] = ((kc0 / kQK + bl) & 1) ? stage_block<1>(xv, dst) : stage_block<0>(xv, dst);
+        }
         if ((Nt & 1) && n == Nt - 1) cs[bl * csn + Nt] = 0.f;  // the padding column read by the last lane pair
       }
     }
@@ -337,47 +387,69 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
         if (live) live = mbar_wait_bounded(smem_u32(&bars[slot]), (q / STAGES) & 1, limit_ns, abort_flag, err);
         const int k0 = kc0 + st * Cfg::kStageK + kw * kSubK;
         if (live && k0 < kend) {
-          const uint8_t* sub = ring + slot * Cfg::kStageBytes + kw * Cfg::kSubBytes + g * kSubBytesRow;
+          const uint8_t* sub = ring + slot * Cfg::kStageBytes + kw * Cfg::kSubBytes + g * Cfg::kRowBytes;
           const int bl0 = (k0 - kc0) / kQK;
           const uint4* xsp = xs + (bl0 * N + g) * 4 + t;     // + block * 4N + nt * 32
           const float* csp = cs + bl0 * csn + 2 * t;         // + block * csn + nt * 8
           const uint4* xs1 = xs + bl0 * 4 + t;               // N = 1: token 0, slot t
           const float* cs1 = cs + bl0 * csn;                 // N = 1: token 0's bias
+          const float* sxp = sxs + bl0 * csn + 2 * t;        // Q4_1: x sums, like csp
+          const float* sx1 = sxs + bl0 * csn;                // Q4_1, N = 1
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
             uint32_t wd[MT][2][2];  // [m-tile][row g / g+8][even / odd block] code words
             float dd[MT][2][2];     // scales
+            float mm[MT][2][2];     // Q4_1 min offsets
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
               for (int r = 0; r < 2; ++r) {
-                const uint8_t* rb = sub + (mt * 16 + 8 * r) * kSubBytesRow + 36 * p;
-                const uint32_t Z = *reinterpret_cast<const uint32_t*>(rb);
-                const uint32_t U = *reinterpret_cast<const uint32_t*>(rb + 4 + 4 * t);
-                const uint32_t W4 = *reinterpret_cast<const uint32_t*>(rb + 16);
-                const uint32_t Y1 = *reinterpret_cast<const uint32_t*>(rb + 20 + 4 * t);
-                wd[mt][r][0] = prmt(Z, U, sel);
-                wd[mt][r][1] = Y1;
-                dd[mt][r][0] = half_lo(Z);
-                dd[mt][r][1] = half_hi(W4);
+                const uint8_t* rb = sub + (mt * 16 + 8 * r) * Cfg::kRowBytes;
+                if constexpr (F == GQ_TYPE_Q4_1) {
+                  // 20-byte blocks: word 0 = d | m << 16, words 1..4 the codes
+#pragma unroll
+                  for (int e = 0; e < 2; ++e) {
+                    const uint8_t* bb = rb + 20 * (2 * p + e);
+                    const uint32_t H = *reinterpret_cast<const uint32_t*>(bb);
+                    wd[mt][r][e] = *reinterpret_cast<const uint32_t*>(bb + 4 + 4 * t);
+                    dd[mt][r][e] = half_lo(H);
+                    mm[mt][r][e] = half_hi(H);
+                  }
+                } else {
+                  rb += 36 * p;
+                  const uint32_t Z = *reinterpret_cast<const uint32_t*>(rb);
+                  const uint32_t U = *reinterpret_cast<const uint32_t*>(rb + 4 + 4 * t);
+                  const uint32_t W4 = *reinterpret_cast<const uint32_t*>(rb + 16);
+                  const uint32_t Y1 = *reinterpret_cast<const uint32_t*>(rb + 20 + 4 * t);
+                  wd[mt][r][0] = prmt(Z, U, sel);
+                  wd[mt][r][1] = Y1;
+                  dd[mt][r][0] = half_lo(Z);
+                  dd[mt][r][1] = half_hi(W4);
+                  mm[mt][r][0] = mm[mt][r][1] = 0.f;
+                }
               }
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               const int b = 2 * p + e;
               uint4 xf[NT];
               float2 nb[NT];
+              float2 sxv[NT];  // Q4_1: the columns' x sums of this block
               if (ONE) {
                 // N = 1: every lane takes token 0's fragment (columns 1..7 then
                 // repeat column 0 and are never stored) and its bias.
                 xf[0] = xs1[b * 4];
                 const float bias = cs1[b * 2];  // stride of the bias table for N = 1
                 nb[0] = make_float2(bias, 0.f);
+                sxv[0] = make_float2(F == GQ_TYPE_Q4_1 ? sx1[b * 2] : 0.f, 0.f);
               } else {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                   xf[nt] = (nt * 8 + g < Nt) ? xsp[b * 4 * N + nt * 32] : make_uint4(0u, 0u, 0u, 0u);
                   nb[nt] = (nt * 8 + 2 * t < Nt) ? *reinterpret_cast<const float2*>(csp + b * csn + nt * 8)
                                                  : make_float2(0.f, 0.f);
+                  sxv[nt] = (F == GQ_TYPE_Q4_1 && nt * 8 + 2 * t < Nt)
+                                ? *reinterpret_cast<const float2*>(sxp + b * csn + nt * 8)
+                                : make_float2(0.f, 0.f);
                 }
               }
 #pragma unroll
@@ -391,11 +463,21 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
                   const float init[4] = {nb[nt].x, nb[nt].y, nb[nt].x, nb[nt].y};
                   mma_m16n8k16_f16(tsum, a_lo, xf[nt].x, xf[nt].y, init);
                   mma_m16n8k16_f16(tsum, a_hi, xf[nt].z, xf[nt].w, tsum);
-                  acc[mt][nt][0] = fmaf(dd[mt][0][e], tsum[0], acc[mt][nt][0]);
-                  acc[mt][nt][2] = fmaf(dd[mt][1][e], tsum[2], acc[mt][nt][2]);
-                  if (!ONE) {  // with N = 1 only column 0 (c0, c2) is ever stored
-                    acc[mt][nt][1] = fmaf(dd[mt][0][e], tsum[1], acc[mt][nt][1]);
-                    acc[mt][nt][3] = fmaf(dd[mt][1][e], tsum[3], acc[mt][nt][3]);
+                  if constexpr (F == GQ_TYPE_Q4_1) {
+                    // sum (d q + m) x = d * sum(q x) + m * sum(x)
+                    acc[mt][nt][0] = fmaf(mm[mt][0][e], sxv[nt].x, fmaf(dd[mt][0][e], tsum[0], acc[mt][nt][0]));
+                    acc[mt][nt][2] = fmaf(mm[mt][1][e], sxv[nt].x, fmaf(dd[mt][1][e], tsum[2], acc[mt][nt][2]));
+                    if (!ONE) {
+                      acc[mt][nt][1] = fmaf(mm[mt][0][e], sxv[nt].y, fmaf(dd[mt][0][e], tsum[1], acc[mt][nt][1]));
+                      acc[mt][nt][3] = fmaf(mm[mt][1][e], sxv[nt].y, fmaf(dd[mt][1][e], tsum[3], acc[mt][nt][3]));
+                    }
+                  } else {
+                    acc[mt][nt][0] = fmaf(dd[mt][0][e], tsum[0], acc[mt][nt][0]);
+                    acc[mt][nt][2] = fmaf(dd[mt][1][e], tsum[2], acc[mt][nt][2]);
+                    if (!ONE) {  // with N = 1 only column 0 (c0, c2) is ever stored
+                      acc[mt][nt][1] = fmaf(dd[mt][0][e], tsum[1], acc[mt][nt][1]);
+                      acc[mt][nt][3] = fmaf(dd[mt][1][e], tsum[3], acc[mt][nt][3]);
+                    }
                   }
                 }
               }
@@ -474,20 +556,20 @@ int decode_early_stages() { return g_early_stages; }
 int g_x_static = 0;      // the caller promises X is not written by the kernel right before
 int decode_x_static() { return g_x_static; }
 
-template <int NT, int MT, int KW, int STAGES, bool ONE = false, bool MOE = false>
+template <int NT, int MT, int KW, int STAGES, bool ONE = false, bool MOE = false, int F = GQ_TYPE_Q4_0>
 cudaError_t launch_cfg(const CUtensorMap* tmW, const float* X, int N, int M, int K, float* Y, uint64_t limit_ns,
                        int xs_budget, int early_w, int pdl, cudaStream_t s, const MoeRoute& rt = MoeRoute{},
                        int64_t max_groups = 0) {
   // MUL_MAT_ID needs the routing before it knows which weights to stream
   const int early_stages = (early_w && !MOE) ? std::max(1, std::min(STAGES, decode_early_stages())) : 0;
-  using Cfg = DecodeCfg<NT, MT, KW, STAGES>;
+  using Cfg = DecodeCfg<NT, MT, KW, STAGES, F>;
   // x chunk: a multiple of the stage width, as long as the budget allows
   int KX = (xs_budget / (2 * N)) / Cfg::kStageK * Cfg::kStageK;
   if (KX < Cfg::kStageK) KX = Cfg::kStageK;
   const int Kpad = (K + Cfg::kStageK - 1) / Cfg::kStageK * Cfg::kStageK;
   if (KX > Kpad) KX = Kpad;
   const size_t smem = Cfg::smem_bytes(N, KX);
-  auto kern = k_decode_q4_0<NT, MT, KW, STAGES, ONE, MOE>;
+  auto kern = k_decode_q4_0<NT, MT, KW, STAGES, ONE, MOE, F>;
   static int configured_smem = 0;
   static int occ_cache_smem = -1, occ_cache = 1;
   if (static_cast<int>(smem) > configured_smem) {
@@ -637,6 +719,18 @@ cudaError_t launch_decode_moe(const CUtensorMap* tmW, const float* X, int cap, i
   if (cap == 32)
     return launch_cfg<4, 1, 4, 4, false, true>(tmW, X, 32, m, k, Y, wait_limit_ns, 96 << 10, 0, pdl, s, rt, max_groups);
   return launch_cfg<8, 1, 2, 4, false, true>(tmW, X, 64, m, k, Y, wait_limit_ns, 64 << 10, 0, pdl, s, rt, max_groups);
+}
+
+// Q4_1 at N = 1: the decode kernel with 20-byte blocks (32-row tiles, 160-byte
+// box rows); the 4-warp co-resident CTA under the same promises as Q4_0.
+cudaError_t launch_decode_q41(const CUtensorMap* tmW, const float* X, int64_t M, int64_t K, float* Y,
+                              uint64_t wait_limit_ns, int early_w, int pdl, cudaStream_t s) {
+  const int m = static_cast<int>(M), k = static_cast<int>(K);
+  if (early_w && decode_x_static() && (m + 31) / 32 <= 4 * device_info().sm_count)
+    return launch_cfg<1, 2, 4, 3, true, false, GQ_TYPE_Q4_1>(tmW, X, 1, m, k, Y, wait_limit_ns, 64 << 10, early_w,
+                                                               pdl, s);
+  return launch_cfg<1, 2, 8, 3, true, false, GQ_TYPE_Q4_1>(tmW, X, 1, m, k, Y, wait_limit_ns, 64 << 10, early_w,
+                                                             pdl, s);
 }
 
 cudaError_t launch_generic(const uint8_t* W, int64_t M, int64_t K, const float* X, int64_t N, float* Y,

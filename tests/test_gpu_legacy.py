@@ -128,3 +128,25 @@ def test_typed_errors_and_q4_0_dispatch():
     b = gq.mul_mat_q4_0(dev(W), dev(X))
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("M,K", [(256, 1024), (1000, 4096), (33, 256), (4096, 11008)])
+def test_q4_1_decode_kernel_and_scalar_agree(M, K):
+    """Q4_1 at N = 1 through the mma.sync decode kernel (20-byte blocks) and
+    through the scalar kernel (GQ_OPT_FORCE_GENERIC), both against the oracle,
+    with and without the weights-static / x-static promises (which select the
+    4-warp CTA)."""
+    seed = 13800 + M + K
+    check(1, M, K, 1, seed, sample=None if M <= 1000 else 64)
+    for flag in (gq.GQ_OPT_WEIGHTS_STATIC, gq.GQ_OPT_X_STATIC):
+        gq.gq_set_option(flag, 1)
+    try:
+        check(1, M, K, 1, seed, sample=None if M <= 1000 else 64)
+    finally:
+        for flag in (gq.GQ_OPT_WEIGHTS_STATIC, gq.GQ_OPT_X_STATIC):
+            gq.gq_set_option(flag, 0)
+    gq.gq_set_option(gq.GQ_OPT_FORCE_GENERIC, 1)
+    try:
+        check(1, M, K, 1, seed, sample=None if M <= 1000 else 64)
+    finally:
+        gq.gq_set_option(gq.GQ_OPT_FORCE_GENERIC, 0)
