@@ -100,14 +100,15 @@ size_t gq_type_nbytes(gq_type type, int64_t M, int64_t K);
 gq_status gq_dequant(gq_type type, const void *W, int64_t M, int64_t K, float *out, void *stream);
 
 /* MUL_MAT with W in block format `type`: Y[N][M] = X[N][K] * W^T, fp32 in and
- * out.  GQ_TYPE_Q4_0 is gq_mul_mat_q4_0.  Q4_1 and Q8_0: for N >= 2 (with K %
- * 256 == 0 and W, X, Y 16-byte aligned) X is converted to bf16 and the tcgen05
- * kernel runs with this block format (N*K*2 bytes of stream-ordered scratch,
- * plus k-split scratch as in gq_mul_mat_q4_0); for N == 1 or other shapes a
- * warp per weight row decodes the blocks to fp32 codes in registers and
- * accumulates in fp32 (any alignment, K % 32 == 0).  GQ_OPT_FORCE_GENERIC
- * forces the latter.  M, N == 0 no-op, K == 0 zeros.  Accuracy as
- * gq_mul_mat_q4_0. */
+ * out.  GQ_TYPE_Q4_0 is gq_mul_mat_q4_0.  Q4_1 and Q8_0, with K % 256 == 0
+ * and W, X, Y 16-byte aligned: N >= GQ_OPT_PREFILL_MIN_N converts X to bf16
+ * and runs the tcgen05 kernel with this block format (N*K*2 bytes of
+ * stream-ordered scratch, plus k-split scratch as in gq_mul_mat_q4_0); a
+ * smaller N below 16 streams W through the decode kernel on this block format
+ * (fp16 x, exact integer codes, fp32 block scales and accumulation).  Other
+ * shapes: a warp per weight row decodes the blocks to fp32 codes in registers
+ * and accumulates in fp32 (any alignment, K % 32 == 0); GQ_OPT_FORCE_GENERIC
+ * forces it.  M, N == 0 no-op, K == 0 zeros.  Accuracy as gq_mul_mat_q4_0. */
 gq_status gq_mul_mat(gq_type type, const void *W, int64_t M, int64_t K, const float *X, int64_t N, float *Y,
                      void *stream);
 

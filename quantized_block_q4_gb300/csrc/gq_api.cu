@@ -294,20 +294,21 @@ gq_status gq_mul_mat(gq_type type, const void* W, int64_t M, int64_t K, const fl
   }
   if (!W || !X) return fail(GQ_ERR_NULL, "W and X must not be NULL");
   if (!aligned(X, 4) || !aligned(Y, 4)) return fail(GQ_ERR_ALIGN, "X and Y must be 4-byte aligned");
-  // The scalar kernel is instruction-bound (no tensor cores): from two tokens
-  // on, the tensor-core kernel with this block format is faster.
-  const bool tc = N >= 2 && K % 256 == 0 && aligned(W, 16) && aligned(X, 16) && aligned(Y, 16) &&
-                  !g_force_generic.load();
-  if (type == GQ_TYPE_Q4_1 && N == 1 && K % 256 == 0 && aligned(W, 16) && aligned(X, 16) && aligned(Y, 16) &&
-      !g_force_generic.load()) {
-    // the decode kernel on 20-byte blocks
+  // Fast paths as for Q4_0: the mma.sync decode kernel below the tensor-core
+  // threshold, the tcgen05 kernel from it on; the scalar kernel otherwise.
+  const bool fast = K % 256 == 0 && aligned(W, 16) && aligned(X, 16) && aligned(Y, 16) && !g_force_generic.load();
+  const bool tc = fast && N >= g_prefill_min_n.load();
+  if (fast && !tc && N < 16) {
+    // the decode kernel on 20- / 34-byte blocks (Q8_0's 272-byte box rows as 16-bit elements)
     CUtensorMap tm;
-    const uint64_t row_bytes = static_cast<uint64_t>(K / kQK) * 20;
-    st = make_tmap(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, row_bytes, static_cast<uint64_t>(M), row_bytes, 160, 32,
+    const uint64_t row_bytes = static_cast<uint64_t>(K / kQK) * static_cast<uint64_t>(type_block_bytes(type));
+    const bool wide = type == GQ_TYPE_Q8_0;
+    st = make_tmap(&tm, wide ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, W,
+                   row_bytes / (wide ? 2 : 1), static_cast<uint64_t>(M), row_bytes, wide ? 136 : 160, 32,
                    CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != GQ_OK) return st;
-    cudaError_t e = launch_decode_q41(&tm, X, M, K, Y, static_cast<uint64_t>(g_wait_limit_ns.load()),
-                                      static_cast<int>(g_early_w.load()), static_cast<int>(g_pdl.load()), s);
+    cudaError_t e = launch_decode_legacy(type, &tm, X, N, M, K, Y, static_cast<uint64_t>(g_wait_limit_ns.load()),
+                                         static_cast<int>(g_early_w.load()), static_cast<int>(g_pdl.load()), s);
     return e == cudaSuccess ? GQ_OK : cuda_fail(e, "decode launch");
   }
   if (!tc) {

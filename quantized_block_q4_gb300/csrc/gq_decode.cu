@@ -45,7 +45,7 @@ constexpr int kSubBytesRow = 144;  // 8 blocks x 18 bytes (Q4_0)
 
 // Bytes of one row of a TMA box (8 blocks): Q4_0 144, Q4_1 160.
 template <int F>
-constexpr int sub_bytes_row() { return F == GQ_TYPE_Q4_1 ? 160 : kSubBytesRow; }
+constexpr int sub_bytes_row() { return F == GQ_TYPE_Q4_1 ? 160 : (F == GQ_TYPE_Q8_0 ? 272 : kSubBytesRow); }
 
 // NT: n8 token tiles (N <= 8*NT); MT: m16 row tiles per warp (tile = 16*MT
 // rows); KW: consumer warps, each taking one 256-k box of every stage; F: the
@@ -55,6 +55,7 @@ template <int NT, int MT, int KW, int STAGES, int F = GQ_TYPE_Q4_0>
 struct DecodeCfg {
   static constexpr int kBM = 16 * MT;
   static constexpr int kRowBytes = sub_bytes_row<F>();
+  static constexpr int kElem = kRowBytes > 256 ? 2 : 1;  // TMA element bytes (a box is at most 256 wide)
   static constexpr int kTables = F == GQ_TYPE_Q4_1 ? 2 : 1;
   static constexpr int kSubBytes = kBM * kRowBytes;
   static constexpr int kThreads = 32 * (KW + 1);
@@ -165,11 +166,43 @@ __device__ __forceinline__ float stage_block_q41(const float (&x)[32], uint4* ds
   return -1024.f * bias;
 }
 
+// Q8_0 x staging: a lane owns elements 4t .. 4t+3 of each half of a block
+// (k 2t, 2t+1 <- 4t, 4t+1 and k 2t+8, 2t+9 <- 4t+2, 4t+3 in the MMA); the codes
+// enter as fp16 1024 + (c ^ 0x80) = 1152 + q, so the bias is 1152 * sum(x).
+__device__ __forceinline__ float stage_block_q80(const float (&x)[32], uint4* dst) {
+  float bias = 0.f;
+  __half xh[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    xh[j] = __float2half_rn(x[j]);
+    bias += __half2float(xh[j]);
+  }
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    __half2 h;
+    uint4 pk;
+    h = __halves2half2(xh[4 * t], xh[4 * t + 1]); pk.x = *reinterpret_cast<uint32_t*>(&h);
+    h = __halves2half2(xh[4 * t + 2], xh[4 * t + 3]); pk.y = *reinterpret_cast<uint32_t*>(&h);
+    h = __halves2half2(xh[16 + 4 * t], xh[16 + 4 * t + 1]); pk.z = *reinterpret_cast<uint32_t*>(&h);
+    h = __halves2half2(xh[16 + 4 * t + 2], xh[16 + 4 * t + 3]); pk.w = *reinterpret_cast<uint32_t*>(&h);
+    dst[t] = pk;
+  }
+  return -1152.f * bias;
+}
+
+// Four int8 codes (one word) -> two f16x2 registers of 1024 + (c ^ 0x80):
+// (c0, c1) and (c2, c3).
+__device__ __forceinline__ void q8_to_f16(uint32_t v, uint32_t& r01, uint32_t& r23) {
+  const uint32_t u = v ^ 0x80808080u;
+  r01 = prmt(u, 0x64646464u, 0x4140u);
+  r23 = prmt(u, 0x64646464u, 0x4342u);
+}
+
 // Two CTAs per SM only where the ring leaves room for a second one; otherwise
 // let the kernel use the registers of a single CTA.
-template <int NT, int MT, int KW, int STAGES>
+template <int NT, int MT, int KW, int STAGES, int F = GQ_TYPE_Q4_0>
 constexpr int decode_min_blocks() {
-  return (NT <= 2 && STAGES * KW * 16 * MT * 144 <= 80 * 1024) ? 2 : 1;
+  return (NT <= 2 && STAGES * KW * 16 * MT * sub_bytes_row<F>() <= 80 * 1024) ? 2 : 1;
 }
 
 // MOE: MUL_MAT_ID over the decode groups of rt (expert e, up to N tokens
@@ -180,11 +213,11 @@ constexpr int decode_min_blocks() {
 // out evenly among the groups (each CTA taking every cpg-th tile of its
 // group), or, with more groups than CTAs, CTA b runs groups b, b + grid, ...
 template <int NT, int MT, int KW, int STAGES, bool ONE, bool MOE = false, int F = GQ_TYPE_Q4_0>
-__global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, STAGES>()))
+__global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, STAGES, F>()))
     k_decode_q4_0(const __grid_constant__ CUtensorMap tmW, const float* __restrict__ X, int N, int M, int K,
                   int KX, float* __restrict__ Y, uint64_t limit_ns, uint32_t* err, int early_stages,
                   int x_static, const MoeRoute rt) {
-  static_assert(F == GQ_TYPE_Q4_0 || (F == GQ_TYPE_Q4_1 && !MOE), "Q4_1 runs the plain MUL_MAT layout");
+  static_assert(F == GQ_TYPE_Q4_0 || !MOE, "Q4_1 / Q8_0 run the plain MUL_MAT layout");
   using Cfg = DecodeCfg<NT, MT, KW, STAGES, F>;
   constexpr int kBM = Cfg::kBM;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -277,7 +310,7 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
             const uint32_t full = smem_u32(&bars[slot]);
             mbar_arrive_expect_tx(full, nvalid * Cfg::kSubBytes);
             for (int j = 0; j < nvalid; ++j) {
-              const int xb = ((k0 + j * kSubK) / kSubK) * Cfg::kRowBytes;  // byte column in the row
+              const int xb = ((k0 + j * kSubK) / kSubK) * (Cfg::kRowBytes / Cfg::kElem);  // element column
               tma_load_2d(smem_u32(ring + slot * Cfg::kStageBytes + j * Cfg::kSubBytes), &tmW, xb,
                           wrow0 + tile * kBM, full);
             }
@@ -364,6 +397,8 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
         if constexpr (F == GQ_TYPE_Q4_1) {
           cs[bl * csn + n] = stage_block_q41(xv, dst, &sxs[bl * csn + n]);
           if ((Nt & 1) && n == Nt - 1) sxs[bl * csn + Nt] = 0.f;
+        } else if constexpr (F == GQ_TYPE_Q8_0) {
+          cs[bl * csn + n] = stage_block_q80(xv, dst);
         } else {
           cs[bl * csn + n] = ((kc0 / kQK + bl) & 1) ? stage_block<1>(xv, dst) : stage_block<0>(xv, dst);
         }
@@ -398,6 +433,7 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
             uint32_t wd[MT][2][2];  // [m-tile][row g / g+8][even / odd block] code words
+            uint32_t wh[MT][2][2];  // Q8_0: the code word of the block's second half
             float dd[MT][2][2];     // scales
             float mm[MT][2][2];     // Q4_1 min offsets
 #pragma unroll
@@ -415,6 +451,21 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
                     dd[mt][r][e] = half_lo(H);
                     mm[mt][r][e] = half_hi(H);
                   }
+                } else if constexpr (F == GQ_TYPE_Q8_0) {
+                  // 34-byte blocks: the pair 2p, 2p+1 starts 4-byte aligned (68p).
+                  // Even block: d in the low half of word 0, code word k is the
+                  // high half of word k and the low half of word k+1.  Odd block
+                  // (byte 34): d in the high half of word 8, code word k is word
+                  // 9 + k.  A lane takes code words t and t + 4 of each block.
+                  const uint32_t* w = reinterpret_cast<const uint32_t*>(rb + 68 * p);
+                  const uint32_t w0 = w[0], w8 = w[8];
+                  wd[mt][r][0] = prmt(w[t], w[t + 1], 0x5432u);
+                  wh[mt][r][0] = prmt(w[t + 4], w[t + 5], 0x5432u);
+                  wd[mt][r][1] = w[9 + t];
+                  wh[mt][r][1] = w[13 + t];
+                  dd[mt][r][0] = half_lo(w0);
+                  dd[mt][r][1] = half_hi(w8);
+                  mm[mt][r][0] = mm[mt][r][1] = 0.f;
                 } else {
                   rb += 36 * p;
                   const uint32_t Z = *reinterpret_cast<const uint32_t*>(rb);
@@ -455,8 +506,15 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
 #pragma unroll
               for (int mt = 0; mt < MT; ++mt) {
                 uint32_t a_lo[4], a_hi[4];
-                codes_to_f16(wd[mt][0][e], a_lo[0], a_lo[2], a_hi[0], a_hi[2]);
-                codes_to_f16(wd[mt][1][e], a_lo[1], a_lo[3], a_hi[1], a_hi[3]);
+                if constexpr (F == GQ_TYPE_Q8_0) {
+                  q8_to_f16(wd[mt][0][e], a_lo[0], a_lo[2]);
+                  q8_to_f16(wd[mt][1][e], a_lo[1], a_lo[3]);
+                  q8_to_f16(wh[mt][0][e], a_hi[0], a_hi[2]);
+                  q8_to_f16(wh[mt][1][e], a_hi[1], a_hi[3]);
+                } else {
+                  codes_to_f16(wd[mt][0][e], a_lo[0], a_lo[2], a_hi[0], a_hi[2]);
+                  codes_to_f16(wd[mt][1][e], a_lo[1], a_lo[3], a_hi[1], a_hi[3]);
+                }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                   float tsum[4];
@@ -721,16 +779,40 @@ cudaError_t launch_decode_moe(const CUtensorMap* tmW, const float* X, int cap, i
   return launch_cfg<8, 1, 2, 4, false, true>(tmW, X, 64, m, k, Y, wait_limit_ns, 64 << 10, 0, pdl, s, rt, max_groups);
 }
 
-// Q4_1 at N = 1: the decode kernel with 20-byte blocks (32-row tiles, 160-byte
-// box rows); the 4-warp co-resident CTA under the same promises as Q4_0.
-cudaError_t launch_decode_q41(const CUtensorMap* tmW, const float* X, int64_t M, int64_t K, float* Y,
+// Q4_1 / Q8_0 at N = 1: the decode kernel with 20- or 34-byte blocks (32-row
+// tiles, 160- or 272-byte box rows); the 4-warp co-resident CTA under the same
+// promises as Q4_0.
+// Q8_0's stages are 1.9x Q4_0's: one stage fewer, so that the ring fits (the
+// 8-warp CTA) and two 4-warp CTAs still share an SM.
+template <int F>
+cudaError_t launch_decode_fmt(const CUtensorMap* tmW, const float* X, int64_t M, int64_t K, float* Y,
                               uint64_t wait_limit_ns, int early_w, int pdl, cudaStream_t s) {
+  constexpr int kSt = F == GQ_TYPE_Q8_0 ? 2 : 3;
   const int m = static_cast<int>(M), k = static_cast<int>(K);
   if (early_w && decode_x_static() && (m + 31) / 32 <= 4 * device_info().sm_count)
-    return launch_cfg<1, 2, 4, 3, true, false, GQ_TYPE_Q4_1>(tmW, X, 1, m, k, Y, wait_limit_ns, 64 << 10, early_w,
-                                                               pdl, s);
-  return launch_cfg<1, 2, 8, 3, true, false, GQ_TYPE_Q4_1>(tmW, X, 1, m, k, Y, wait_limit_ns, 64 << 10, early_w,
-                                                             pdl, s);
+    return launch_cfg<1, 2, 4, kSt, true, false, F>(tmW, X, 1, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+  return launch_cfg<1, 2, 8, kSt, true, false, F>(tmW, X, 1, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+}
+
+// 2..15 tokens: 32-row tiles and two stages (the larger blocks' rings and the
+// x fragments of up to 16 tokens must fit in shared memory beside each other).
+template <int F>
+cudaError_t launch_decode_fmt_n(const CUtensorMap* tmW, const float* X, int64_t N, int64_t M, int64_t K, float* Y,
+                                uint64_t wait_limit_ns, int early_w, int pdl, cudaStream_t s) {
+  constexpr int kKw = F == GQ_TYPE_Q8_0 ? 4 : 8;
+  const int n = static_cast<int>(N), m = static_cast<int>(M), k = static_cast<int>(K);
+  if (N <= 8)
+    return launch_cfg<1, 2, kKw, 2, false, false, F>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+  return launch_cfg<2, 2, kKw, 2, false, false, F>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+}
+
+cudaError_t launch_decode_legacy(int type, const CUtensorMap* tmW, const float* X, int64_t N, int64_t M, int64_t K,
+                                 float* Y, uint64_t wait_limit_ns, int early_w, int pdl, cudaStream_t s) {
+  if (type == GQ_TYPE_Q8_0)
+    return N == 1 ? launch_decode_fmt<GQ_TYPE_Q8_0>(tmW, X, M, K, Y, wait_limit_ns, early_w, pdl, s)
+                  : launch_decode_fmt_n<GQ_TYPE_Q8_0>(tmW, X, N, M, K, Y, wait_limit_ns, early_w, pdl, s);
+  return N == 1 ? launch_decode_fmt<GQ_TYPE_Q4_1>(tmW, X, M, K, Y, wait_limit_ns, early_w, pdl, s)
+                : launch_decode_fmt_n<GQ_TYPE_Q4_1>(tmW, X, N, M, K, Y, wait_limit_ns, early_w, pdl, s);
 }
 
 cudaError_t launch_generic(const uint8_t* W, int64_t M, int64_t K, const float* X, int64_t N, float* Y,

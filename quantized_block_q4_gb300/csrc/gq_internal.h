@@ -36,9 +36,10 @@ cudaError_t launch_dequant_bytes(const uint8_t* W, int64_t nblocks, float* out, 
 // W 16-byte aligned, N <= 64.
 cudaError_t launch_decode(const CUtensorMap* tmW, const float* X, int64_t N, int64_t M, int64_t K,
                           float* Y, uint64_t wait_limit_ns, int early_w, int variant, int pdl, cudaStream_t s);
-// Q4_1, N = 1: the decode kernel on 20-byte blocks; tmW boxes of 32 rows x 160 bytes.
-cudaError_t launch_decode_q41(const CUtensorMap* tmW, const float* X, int64_t M, int64_t K, float* Y,
-                              uint64_t wait_limit_ns, int early_w, int pdl, cudaStream_t s);
+// Q4_1 / Q8_0, N <= 15: the decode kernel on 20- / 34-byte blocks; tmW boxes of
+// 32 rows x 160 bytes (Q4_1, 8-bit elements) or 32 rows x 136 16-bit elements (Q8_0).
+cudaError_t launch_decode_legacy(int type, const CUtensorMap* tmW, const float* X, int64_t N, int64_t M, int64_t K,
+                                 float* Y, uint64_t wait_limit_ns, int early_w, int pdl, cudaStream_t s);
 // TMA box the decode kernel expects for W (rows of raw blocks viewed as bytes).
 void decode_w_box(int64_t N, int variant, uint32_t* box_x_bytes, uint32_t* box_rows);
 

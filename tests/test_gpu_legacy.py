@@ -130,23 +130,32 @@ def test_typed_errors_and_q4_0_dispatch():
     assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("qtype", TYPES, ids=lambda t: NAMES[t])
 @pytest.mark.parametrize("M,K", [(256, 1024), (1000, 4096), (33, 256), (4096, 11008)])
-def test_q4_1_decode_kernel_and_scalar_agree(M, K):
-    """Q4_1 at N = 1 through the mma.sync decode kernel (20-byte blocks) and
+def test_decode_kernel_and_scalar_agree(qtype, M, K):
+    """N = 1 through the mma.sync decode kernel (20- or 34-byte blocks) and
     through the scalar kernel (GQ_OPT_FORCE_GENERIC), both against the oracle,
     with and without the weights-static / x-static promises (which select the
     4-warp CTA)."""
-    seed = 13800 + M + K
-    check(1, M, K, 1, seed, sample=None if M <= 1000 else 64)
+    seed = 13800 + M + K + qtype
+    check(qtype, M, K, 1, seed, sample=None if M <= 1000 else 64)
     for flag in (gq.GQ_OPT_WEIGHTS_STATIC, gq.GQ_OPT_X_STATIC):
         gq.gq_set_option(flag, 1)
     try:
-        check(1, M, K, 1, seed, sample=None if M <= 1000 else 64)
+        check(qtype, M, K, 1, seed, sample=None if M <= 1000 else 64)
     finally:
         for flag in (gq.GQ_OPT_WEIGHTS_STATIC, gq.GQ_OPT_X_STATIC):
             gq.gq_set_option(flag, 0)
     gq.gq_set_option(gq.GQ_OPT_FORCE_GENERIC, 1)
     try:
-        check(1, M, K, 1, seed, sample=None if M <= 1000 else 64)
+        check(qtype, M, K, 1, seed, sample=None if M <= 1000 else 64)
     finally:
         gq.gq_set_option(gq.GQ_OPT_FORCE_GENERIC, 0)
+
+
+@pytest.mark.parametrize("qtype", TYPES, ids=lambda t: NAMES[t])
+@pytest.mark.parametrize("N", [2, 7, 9, 15])
+def test_small_batch_decode_kernel(qtype, N):
+    """2..15 tokens with K % 256 == 0: the mma.sync decode kernel (one or two
+    n8 token tiles), ragged rows, K over several x chunks."""
+    check(qtype, 1000, 8192, N, seed=13900 + N + qtype)
