@@ -218,9 +218,10 @@ typedef enum {
   GQ_OPT_FORCE_GENERIC = 1,  /* 1: every mul_mat takes the generic kernel (test aid) */
   GQ_OPT_WAIT_LIMIT_NS = 2,  /* bound on any in-kernel wait, nanoseconds (default 2e9) */
   GQ_OPT_WEIGHTS_STATIC = 3, /* 1: promise that no kernel launched right before a mul_mat on the same
-                                stream writes its W, so the decode kernel may start streaming W
-                                while that kernel finishes (weight-stationary inference); default 0 */
-  GQ_OPT_DECODE_VARIANT = 4, /* tuning: tile/warp layout of the N <= 8 decode kernel, 0..4 (default 0);
+                                stream writes its W, so the decode kernel (and the first chunks of the
+                                tensor-core kernel) may start streaming W while that kernel finishes
+                                (weight-stationary inference); default 0 */
+  GQ_OPT_DECODE_VARIANT = 4, /* tuning: tile/warp layout of the N <= 32 decode kernel, 0..4 (default 0);
                                 every variant computes the same result */
   GQ_OPT_PDL = 5,            /* 1 (default): launch kernels with programmatic dependent launch, so a
                                 kernel may start while the previous one on the stream drains; every

@@ -215,13 +215,14 @@ static gq_status mul_mat_prefill_bf16(const void* W, int64_t M, int64_t K, const
                  static_cast<uint64_t>(K) * 2, xbk, xbr, CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != GQ_OK) return st;
   cudaError_t e = launch_prefill(&tmW, &tmX, N, M, Kw, Y, static_cast<uint64_t>(g_wait_limit_ns.load()), allow_scratch,
-                                 s, type);
+                                 static_cast<int>(g_early_w.load()), static_cast<int>(g_pdl.load()), s, type);
   return e == cudaSuccess ? GQ_OK : cuda_fail(e, "prefill launch");
 }
 
 namespace gq {
 gq_status api_fail(gq_status st, const char* msg) { return fail(st, "%s", msg); }
 gq_status api_check_device() { return check_device(); }
+int api_pdl() { return static_cast<int>(g_pdl.load()); }
 gq_status api_check_mm_shape(int64_t M, int64_t K, int64_t N) { return check_mm_shape(M, K, N); }
 gq_status api_prefill_bf16(const void* W, int64_t M, int64_t K, const uint16_t* X_bf16, int64_t N, float* Y,
                            bool allow_scratch, cudaStream_t s) {
@@ -321,7 +322,7 @@ gq_status gq_mul_mat(gq_type type, const void* W, int64_t M, int64_t K, const fl
   void* xb = nullptr;
   cudaError_t e = scratch_alloc(&xb, xbytes, s);
   if (e != cudaSuccess) return fail(GQ_ERR_ALLOC, "scratch allocation (%zu bytes): %s", xbytes, cudaGetErrorString(e));
-  e = launch_f32_to_bf16(X, static_cast<uint16_t*>(xb), N * K, s);
+  e = launch_f32_to_bf16(X, static_cast<uint16_t*>(xb), N * K, s, static_cast<int>(g_pdl.load()));
   if (e != cudaSuccess) {
     scratch_free(xb, s);
     return cuda_fail(e, "f32->bf16 launch");
@@ -374,7 +375,7 @@ gq_status gq_mul_mat_q4_0(const void* W, int64_t M, int64_t K, const float* X, i
   void* xb = nullptr;
   cudaError_t e = scratch_alloc(&xb, xbytes, s);
   if (e != cudaSuccess) return fail(GQ_ERR_ALLOC, "scratch allocation (%zu bytes): %s", xbytes, cudaGetErrorString(e));
-  e = launch_f32_to_bf16(X, static_cast<uint16_t*>(xb), N * K, s);
+  e = launch_f32_to_bf16(X, static_cast<uint16_t*>(xb), N * K, s, static_cast<int>(g_pdl.load()));
   if (e != cudaSuccess) {
     scratch_free(xb, s);
     return cuda_fail(e, "f32->bf16 launch");
@@ -522,7 +523,7 @@ gq_status gq_mul_mat_q4_0_prepared(const void* Wp, int64_t M, int64_t K, const f
   void* xb = nullptr;
   cudaError_t e = scratch_alloc(&xb, xbytes, s);
   if (e != cudaSuccess) return fail(GQ_ERR_ALLOC, "scratch allocation (%zu bytes): %s", xbytes, cudaGetErrorString(e));
-  e = launch_f32_to_bf16(X, static_cast<uint16_t*>(xb), N * K, s);
+  e = launch_f32_to_bf16(X, static_cast<uint16_t*>(xb), N * K, s, static_cast<int>(g_pdl.load()));
   if (e != cudaSuccess) {
     scratch_free(xb, s);
     return cuda_fail(e, "f32->bf16 launch");
@@ -562,7 +563,7 @@ gq_status gq_f32_to_bf16(const float* x, uint16_t* y, int64_t n, void* stream) {
   if (!aligned(x, 4) || !aligned(y, 2)) return fail(GQ_ERR_ALIGN, "x must be 4-byte and y 2-byte aligned");
   gq_status st = check_device();
   if (st != GQ_OK) return st;
-  cudaError_t e = launch_f32_to_bf16(x, y, n, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_f32_to_bf16(x, y, n, static_cast<cudaStream_t>(stream), static_cast<int>(g_pdl.load()));
   return e == cudaSuccess ? GQ_OK : cuda_fail(e, "f32->bf16 launch");
 }
 

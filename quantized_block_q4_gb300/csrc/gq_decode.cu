@@ -198,11 +198,12 @@ __device__ __forceinline__ void q8_to_f16(uint32_t v, uint32_t& r01, uint32_t& r
   r23 = prmt(u, 0x64646464u, 0x4342u);
 }
 
-// Two CTAs per SM only where the ring leaves room for a second one; otherwise
-// let the kernel use the registers of a single CTA.
+// Two CTAs per SM only where the ring leaves room for a second one and x is
+// one token tile (more tokens' x fragments fill the rest of shared memory);
+// otherwise let the kernel use the registers of a single CTA.
 template <int NT, int MT, int KW, int STAGES, int F = GQ_TYPE_Q4_0>
 constexpr int decode_min_blocks() {
-  return (NT <= 2 && STAGES * KW * 16 * MT * sub_bytes_row<F>() <= 80 * 1024) ? 2 : 1;
+  return (NT == 1 && STAGES * KW * 16 * MT * sub_bytes_row<F>() <= 80 * 1024) ? 2 : 1;
 }
 
 // MOE: MUL_MAT_ID over the decode groups of rt (expert e, up to N tokens
@@ -704,7 +705,8 @@ __global__ void k_generic_q4_0(const uint8_t* __restrict__ W, int64_t M, int64_t
 int decode_rows_per_tile(int64_t N, int variant) {
   if (N == 1) return variant == 1 ? 16 : (variant == 2 ? 64 : 32);
   if (N <= 8) return (variant == 2) ? 16 : 32;
-  if (N <= 16) return 32;
+  if (N <= 16) return (variant == 1 || variant == 4) ? 16 : 32;
+  if (N <= 32) return variant == 2 ? 32 : 16;
   return 16;
 }
 
@@ -740,8 +742,19 @@ cudaError_t launch_decode(const CUtensorMap* tmW, const float* X, int64_t N, int
     if (variant == 2) return launch_cfg<1, 1, 8, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
     return launch_cfg<1, 2, 8, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
   }
-  if (N <= 16) return launch_cfg<2, 2, 8, 2>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
-  if (N <= 32) return launch_cfg<4, 1, 4, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 96 << 10, early_w, pdl, s);
+  if (N <= 16) {
+    if (variant == 1) return launch_cfg<2, 1, 8, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    if (variant == 2) return launch_cfg<2, 2, 4, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    if (variant == 3) return launch_cfg<2, 2, 4, 2>(tmW, X, n, m, k, Y, wait_limit_ns, 128 << 10, early_w, pdl, s);
+    if (variant == 4) return launch_cfg<2, 1, 4, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 128 << 10, early_w, pdl, s);
+    return launch_cfg<2, 2, 8, 2>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+  }
+  if (N <= 32) {
+    if (variant == 1) return launch_cfg<4, 1, 4, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 128 << 10, early_w, pdl, s);
+    if (variant == 2) return launch_cfg<4, 2, 4, 2>(tmW, X, n, m, k, Y, wait_limit_ns, 128 << 10, early_w, pdl, s);
+    if (variant == 3) return launch_cfg<4, 1, 8, 2>(tmW, X, n, m, k, Y, wait_limit_ns, 128 << 10, early_w, pdl, s);
+    return launch_cfg<4, 1, 4, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 96 << 10, early_w, pdl, s);
+  }
   // N = 33..64: two k-warps, so that a stage's x (2 * 512 * N bytes) and the
   // partial sums fit in shared memory next to the ring
   return launch_cfg<8, 1, 2, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);

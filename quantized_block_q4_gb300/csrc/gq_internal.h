@@ -56,15 +56,18 @@ int get_decode_x_static();
 cudaError_t launch_quantize(const float* W, int64_t M, int64_t K, uint8_t* out, cudaStream_t s);
 
 // ---- K0: fp32 -> bf16 (round to nearest even) (gq_prefill.cu)
-cudaError_t launch_f32_to_bf16(const float* x, uint16_t* y, int64_t n, cudaStream_t s);
+// pdl: launch with programmatic dependent launch (the kernel waits for the one before).
+cudaError_t launch_f32_to_bf16(const float* x, uint16_t* y, int64_t n, cudaStream_t s, int pdl);
 
 // ---- K3: prefill mul_mat on tcgen05 (gq_prefill.cu).  Needs K % 256 == 0.
 // allow_scratch: the launch may take stream-ordered scratch for the partial
 // sums of tiles split along k (else, or if that allocation fails, whole tiles).
 // type: block format of W (GQ_TYPE_*; Q4_1 and Q8_0 run the 1-CTA kernels).
+// pdl: launch with programmatic dependent launch (every role waits for the
+// kernel before; with early_w the first raw W chunks stream before that).
 cudaError_t launch_prefill(const CUtensorMap* tmW, const CUtensorMap* tmX, int64_t N, int64_t M,
-                           int64_t K, float* Y, uint64_t wait_limit_ns, bool allow_scratch, cudaStream_t s,
-                           int type = GQ_TYPE_Q4_0);
+                           int64_t K, float* Y, uint64_t wait_limit_ns, bool allow_scratch, int early_w, int pdl,
+                           cudaStream_t s, int type = GQ_TYPE_Q4_0);
 void set_prefill_streamk(int64_t v);   // 0 whole tiles only, 1 by shape (default), n >= 2: every tile in n pieces
 int64_t get_prefill_streamk();
 void set_prefill_slots(int64_t v);     // 0: SM count; n: plan for n SMs (test aid)
@@ -124,6 +127,7 @@ cudaError_t launch_prepare_q4_0(const uint8_t* W, int64_t M, int64_t K, int64_t 
 // ---- helpers of the C ABI (gq_api.cu) for entry points defined in other files
 gq_status api_fail(gq_status st, const char* msg);  // records the per-thread error text
 gq_status api_check_device();
+int api_pdl();  // GQ_OPT_PDL
 gq_status api_check_mm_shape(int64_t M, int64_t K, int64_t N);
 gq_status api_prefill_bf16(const void* W, int64_t M, int64_t K, const uint16_t* X_bf16, int64_t N, float* Y,
                            bool allow_scratch, cudaStream_t s);

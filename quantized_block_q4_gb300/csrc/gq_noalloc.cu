@@ -77,7 +77,7 @@ extern "C" gq_status gq_mul_mat_q4_0_noalloc(const void* W, int64_t M, int64_t K
   st = scratch_address(&xb);
   if (st != GQ_OK) return st;
   auto s = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = gq::launch_f32_to_bf16(X, xb, N * K, s);
+  const cudaError_t e = gq::launch_f32_to_bf16(X, xb, N * K, s, gq::api_pdl());
   if (e != cudaSuccess) return gq::api_fail(GQ_ERR_CUDA, "gq_mul_mat_q4_0_noalloc: conversion launch failed");
   return gq::api_prefill_bf16(W, M, K, xb, N, Y, false, s);
 }

@@ -43,8 +43,12 @@
 namespace gq {
 namespace {
 
-// 8 elements per thread per step: two float4 loads, one 16-byte store.
+// 8 elements per thread per step: two float4 loads, one 16-byte store.  Under
+// programmatic dependent launch it waits for the kernel before (which may
+// have written x, or may still read y) before touching memory.
 __global__ void k_f32_to_bf16(const float* __restrict__ x, uint16_t* __restrict__ y, int64_t n) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const bool vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15) == 0;
@@ -76,12 +80,20 @@ __global__ void k_f32_to_bf16(const float* __restrict__ x, uint16_t* __restrict_
 
 }  // namespace
 
-cudaError_t launch_f32_to_bf16(const float* x, uint16_t* y, int64_t n, cudaStream_t s) {
+cudaError_t launch_f32_to_bf16(const float* x, uint16_t* y, int64_t n, cudaStream_t s, int pdl) {
   const int64_t work = (n + 7) / 8;
   const int grid =
       static_cast<int>(std::min<int64_t>((work + 255) / 256, static_cast<int64_t>(device_info().sm_count) * 8));
-  k_f32_to_bf16<<<grid > 0 ? grid : 1, 256, 0, s>>>(x, y, n);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid > 0 ? grid : 1);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_f32_to_bf16, x, y, n);
 }
 
 namespace {
@@ -149,6 +161,7 @@ struct PrefillWork {
   float* ws;      // one partial-tile slot per piece and CTA (nullptr when R == 0)
   unsigned long long* count;  // per split tile and CTA of a pair: (epoch << 8) | pieces published
   unsigned long long epoch;   // this launch's tag (< 2^56): a counter with another tag reads as 0
+  int early_w;    // W is not written by the kernels before: its first chunks may stream before the PDL wait
 };
 
 // Arrival counters need no zeroing between launches: a counter whose tag is
@@ -382,7 +395,13 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
   const bool leader = rank == 0;
   const int gi = static_cast<int>(blockIdx.x / C::kCtas);
-  if (MOE) pdl_wait();  // the routing tables and gathered x come from the kernels before
+  // Programmatic dependent launch.  MUL_MAT_ID: the routing tables and the
+  // gathered x come from the kernels before, so every role waits first.
+  // MUL_MAT: each role waits for the kernel before (which may have written x
+  // or W, or may still read Y or this launch's scratch) before its first
+  // access to global memory, or its first bounded wait on a role that does;
+  // with early_w only the first raw W chunks stream before that.
+  if (MOE) pdl_wait();
   const int nseg = MOE ? (rt.meta[0] > gi ? (rt.meta[0] - gi + static_cast<int>(gridDim.x) - 1) /
                                                  static_cast<int>(gridDim.x)
                                            : 0)
@@ -427,13 +446,14 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
   if (PAIR) cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if (!MOE) pdl_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ W producer
     if (lane == 0) {
       tma_prefetch_desc(&tmW);
       uint32_t nraw = 0;
-      bool ok = true;
+      bool ok = true, waited = MOE;
       for (int i = 0; i < nseg && ok; ++i) {
         Seg sg;
         int m0;
@@ -446,6 +466,10 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
           m0 = static_cast<int>(sg.t / wk.ntn) * (C::kBM * C::kCtas) + static_cast<int>(rank) * C::kBM;
         }
         for (int r = sg.r0; r < sg.r1; ++r) {
+          if (!waited && (!wk.early_w || nraw >= static_cast<uint32_t>(C::RS))) {
+            pdl_wait();
+            waited = true;
+          }
           const uint32_t slot = nraw % C::RS;
           if (!mbar_wait_bounded(smem_u32(&raw_empty[slot]), ((nraw / C::RS) & 1) ^ 1, limit_ns, abort_flag, err)) {
             ok = false;
@@ -463,6 +487,7 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
     // ------------------------------------------------------------ x producer
     if (lane == 0) {
       tma_prefetch_desc(&tmX);
+      if (!MOE) pdl_wait();
       uint32_t nb = 0;
       bool ok = true;
       for (int i = 0; i < nseg && ok; ++i) {
@@ -505,6 +530,7 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (the leader of a pair)
     if (leader && lane == 0) {
+      if (!MOE) pdl_wait();
       uint32_t idesc = umma_idesc_bf16_f32(C::kBM * C::kCtas, BN);
       uint32_t c = 0, seg = 0;
       bool ok = true;
@@ -564,6 +590,7 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ dequant + epilogue
+    if (!MOE) pdl_wait();
     const int quad = warp & 3;           // TMEM lane quadrant this warp may access
     const int grp = (warp - 2) >> 2;     // 64-k step grp of every 256-k chunk; then columns grp/4 of the tile
     const int row = quad * 32 + lane;    // W row within this CTA's 128 == TMEM lane
@@ -807,7 +834,7 @@ void prefill_plan(int64_t T, int64_t nr, int64_t P, bool allow_split, PrefillWor
 
 template <int BN, bool PAIR, int F = GQ_TYPE_Q4_0>
 cudaError_t launch_prefill_cfg(const CUtensorMap* tmW, const CUtensorMap* tmX, int N, int M, int K, float* Y,
-                               uint64_t limit_ns, bool allow_scratch, cudaStream_t s) {
+                               uint64_t limit_ns, bool allow_scratch, int early_w, int pdl, cudaStream_t s) {
   using C = PrefillCfg<BN, PAIR, F>;
   auto kern = k_prefill_q4_0<BN, PAIR, false, F>;
   static bool configured = false;
@@ -823,6 +850,7 @@ cudaError_t launch_prefill_cfg(const CUtensorMap* tmW, const CUtensorMap* tmX, i
   PrefillWork wk{};
   wk.nr = static_cast<int>(nr);
   wk.ntn = static_cast<int>(ntn);
+  wk.early_w = pdl && early_w;
   prefill_plan(T, nr, device_info().sm_count / C::kCtas, allow_scratch, &wk);
   void* scratch = nullptr;
   if (wk.R > 0) {  // split tiles: partial-tile slots and arrival counters
@@ -847,15 +875,22 @@ cudaError_t launch_prefill_cfg(const CUtensorMap* tmW, const CUtensorMap* tmX, i
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  int na = 0;
   if (PAIR) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 2;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
   }
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, *tmW, *tmX, N, M, Y, wk, limit_ns, device_error_word(), MoeRoute{}, 0);
   if (scratch) {
     cudaError_t f = scratch_free(scratch, s);
@@ -932,21 +967,22 @@ cudaError_t launch_prefill_moe(const CUtensorMap* tmW, const CUtensorMap* tmX, i
 }
 
 cudaError_t launch_prefill(const CUtensorMap* tmW, const CUtensorMap* tmX, int64_t N, int64_t M, int64_t K,
-                           float* Y, uint64_t wait_limit_ns, bool allow_scratch, cudaStream_t s, int type) {
+                           float* Y, uint64_t wait_limit_ns, bool allow_scratch, int early_w, int pdl, cudaStream_t s,
+                           int type) {
   const int n = static_cast<int>(N), m = static_cast<int>(M), k = static_cast<int>(K);
   if (type == GQ_TYPE_Q4_1) {
     if (prefill_bn(N) == 128)
-      return launch_prefill_cfg<128, false, GQ_TYPE_Q4_1>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, s);
-    return launch_prefill_cfg<256, false, GQ_TYPE_Q4_1>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, s);
+      return launch_prefill_cfg<128, false, GQ_TYPE_Q4_1>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
+    return launch_prefill_cfg<256, false, GQ_TYPE_Q4_1>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
   }
   if (type == GQ_TYPE_Q8_0) {
     if (prefill_bn(N) == 128)
-      return launch_prefill_cfg<128, false, GQ_TYPE_Q8_0>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, s);
-    return launch_prefill_cfg<256, false, GQ_TYPE_Q8_0>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, s);
+      return launch_prefill_cfg<128, false, GQ_TYPE_Q8_0>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
+    return launch_prefill_cfg<256, false, GQ_TYPE_Q8_0>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
   }
-  if (use_pair(N)) return launch_prefill_cfg<256, true>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, s);
-  if (prefill_bn(N) == 128) return launch_prefill_cfg<128, false>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, s);
-  return launch_prefill_cfg<256, false>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, s);
+  if (use_pair(N)) return launch_prefill_cfg<256, true>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
+  if (prefill_bn(N) == 128) return launch_prefill_cfg<128, false>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
+  return launch_prefill_cfg<256, false>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
 }
 
 }  // namespace gq

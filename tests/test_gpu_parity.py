@@ -431,14 +431,97 @@ def test_back_to_back_dependent_calls():
 
 
 @pytest.mark.parametrize("variant", [0, 1, 2, 3, 4])
-@pytest.mark.parametrize("M,K,N", [(4096, 4096, 1), (300, 11008, 3), (33, 2304, 8)])
+@pytest.mark.parametrize("M,K,N", [(4096, 4096, 1), (300, 11008, 3), (33, 2304, 8), (1000, 4096, 12),
+                                   (530, 8192, 16)])
 def test_decode_variants(variant, M, K, N):
     old = gq.gq_get_option(gq.GQ_OPT_DECODE_VARIANT)
     gq.gq_set_option(gq.GQ_OPT_DECODE_VARIANT, variant)
     try:
-        check_mm(M, K, N, 7400 + M + N, f"variant {variant}")
+        _with_option(gq.GQ_OPT_PREFILL_MIN_N, 65, lambda: check_mm(M, K, N, 7400 + M + N, f"variant {variant}"))
     finally:
         gq.gq_set_option(gq.GQ_OPT_DECODE_VARIANT, old)
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+@pytest.mark.parametrize("M,K,N", [(700, 4096, 24), (260, 8192, 32)])
+def test_decode_variants_17_to_32_tokens(variant, M, K, N):
+    """17..32 tokens on the decode kernel (the tensor-core threshold raised):
+    four n8 token tiles, one or several x chunks."""
+    def run():
+        return _with_option(gq.GQ_OPT_PREFILL_MIN_N, 65, lambda: check_mm(M, K, N, 7450 + M + N, f"variant {variant}"))
+    _with_option(gq.GQ_OPT_DECODE_VARIANT, variant, run)
+
+
+@pytest.mark.parametrize("weights_static", [0, 1])
+def test_prefill_back_to_back_dependent_calls(weights_static):
+    """Tensor-core calls launched with programmatic dependent launch, each X
+    the previous call's Y: the conversion and the MUL_MAT must wait for the
+    kernel that produced their input (with WEIGHTS_STATIC only W streams
+    early)."""
+    K, N = 2048, 64
+    Ws = [synth.q4_0_weights(K, K, seed=7500 + i) for i in range(4)]
+    x0 = synth.activations(N, K, seed=7510)
+
+    def run():
+        xs = [dev(x0)]
+        for W in Ws:
+            xs.append(gq.mul_mat_q4_0(dev(W), xs[-1]))
+        torch.cuda.synchronize()
+        gq.gq_sync_status()
+        return xs
+    xs = _with_option(gq.GQ_OPT_WEIGHTS_STATIC, weights_static, run)
+    x = x0
+    for i, W in enumerate(Ws):
+        y_ref, s_ref = oracle_mul_mat(W, K, K, x)
+        got = xs[i + 1].cpu().numpy()
+        assert_mul_mat_close(got, y_ref, s_ref, f"prefill chain step {i}")
+        x = got.astype(np.float32)
+
+
+def test_prefill_quantize_then_mul_mat():
+    """W written on the device by the quantizer right before the tensor-core
+    MUL_MAT that reads it (WEIGHTS_STATIC off: W is read after the wait)."""
+    M, K, N = 900, 2048, 80
+    Wf = synth.activations(M, K, seed=7520)
+    X = synth.activations(N, K, seed=7521)
+    Wq = torch.empty(gq.gq_q4_0_nbytes(M, K), dtype=torch.uint8, device="cuda")
+    Wfd, Xd = dev(Wf), dev(X)
+    Y = torch.empty(N, M, device="cuda")
+    for _ in range(2):
+        gq.gq_quantize_q4_0(Wfd, M, K, Wq)
+        gq.gq_mul_mat_q4_0(Wq, M, K, Xd, N, Y)
+        Wfd.mul_(-1.0)  # the next round quantizes other values into the same W buffer
+    torch.cuda.synchronize()
+    gq.gq_sync_status()
+    Wq_ref = oracle.get().quantize(-Wf)  # the second round quantized the negated values
+    assert np.array_equal(Wq.cpu().numpy().reshape(Wq_ref.shape), Wq_ref)
+    y_ref, s_ref = oracle_mul_mat(Wq_ref, M, K, X)
+    assert_mul_mat_close(Y.cpu().numpy(), y_ref, s_ref, "quantize -> mul_mat")
+
+
+@pytest.mark.parametrize("streamk", [1, 3])
+def test_prefill_same_output_and_scratch_back_to_back(streamk):
+    """Consecutive tensor-core calls into one Y (and, split along k, through
+    reused scratch): the last call's result must be what remains."""
+    M, K, N = 640, 2048, 300
+    Ws = [synth.q4_0_weights(M, K, seed=7530 + i) for i in range(3)]
+    X = synth.activations(N, K, seed=7535)
+    Wd, Xd = [dev(w) for w in Ws], dev(X)
+    Y = torch.empty(N, M, device="cuda")
+    Ylast = torch.empty(N, M, device="cuda")
+
+    def run():
+        for _ in range(3):
+            for w in Wd:
+                gq.gq_mul_mat_q4_0(w, M, K, Xd, N, Y)
+            gq.gq_mul_mat_q4_0(Wd[1], M, K, Xd, N, Ylast)
+        torch.cuda.synchronize()
+        gq.gq_sync_status()
+    _with_option(gq.GQ_OPT_PREFILL_STREAMK, streamk, run)
+    y_ref, s_ref = oracle_mul_mat(Ws[2], M, K, X)
+    assert_mul_mat_close(Y.cpu().numpy(), y_ref, s_ref, "last writer wins")
+    y_ref, s_ref = oracle_mul_mat(Ws[1], M, K, X)
+    assert_mul_mat_close(Ylast.cpu().numpy(), y_ref, s_ref, "interleaved call")
 
 
 @pytest.mark.parametrize("M,K", [(4096, 4096), (11008, 4096), (4096, 11008)])
