@@ -17,7 +17,9 @@
 //    summed over the block, is precomputed per block and token and enters as
 //    the MMA's C input with a minus sign, so each block's MMA pair yields
 //    sum (q-8)*x directly.  The block scale d is then applied in fp32 to that
-//    partial, so W is never rounded; only x is (fp16, relative <= 2^-11).
+//    partial, so W is never rounded; only x is (fp16, relative <= 2^-11;
+//    a token with |x| >= 2^15 in a warp's blocks is staged times an exact
+//    power of two and the warp's partial sums are multiplied back).
 //  * The four bytes of codes a lane needs are read straight from the raw
 //    18-byte blocks: two blocks (36 bytes) form nine aligned 32-bit words, and
 //    one PRMT rebuilds the word that straddles the scale of the even block.
@@ -32,6 +34,7 @@
 //    streaming W before that wait (valid when the previous kernel does not
 //    write W, as in weight-stationary inference).
 #include <algorithm>
+#include <type_traits>
 #include <cuda_fp16.h>
 
 #include "gq_internal.h"
@@ -71,11 +74,26 @@ struct DecodeCfg {
   __host__ __device__ static size_t cs_bytes(int N, int KX) {
     return static_cast<size_t>(KX / 32) * cs_stride(N) * sizeof(float);
   }
+  // + per consumer warp and token the power-of-two factor its x was staged with
   static size_t smem_bytes(int N, int KX) {
     return kRingBytes + xs_bytes(N, KX) + kTables * cs_bytes(N, KX) +
-           (kSlots * slot_floats(N) + kSlots) * sizeof(float) + (2 * STAGES + 1) * 8 + 16 + 128;
+           (kSlots * slot_floats(N) + kSlots + static_cast<size_t>(KW) * N) * sizeof(float) + (2 * STAGES + 1) * 8 +
+           16 + 128;
   }
 };
+
+// x is staged as fp16.  A warp's chunk of a token whose largest |x| is m >=
+// 2^15 is staged as x * 2^-e, the smallest such factor that brings m below
+// 2^15 (and x/16 with it); 1 otherwise, and for non-finite m (which then
+// propagates as it would unscaled).
+constexpr float kXScaleFrom = 32768.f;
+__device__ __forceinline__ float x_scale_down(float m) {
+  if (!(m >= kXScaleFrom) || !isfinite(m)) return 1.f;
+  const int E = ((__float_as_int(m) >> 23) & 0xFF) - 127;  // m in [2^E, 2^(E+1)), E >= 15
+  return __int_as_float((127 - (E - 14)) << 23);            // m * 2^-(E-14) in [2^14, 2^15)
+}
+// 1/f for f a normal power of two, exactly (the exponent reflected about 0).
+__device__ __forceinline__ float pow2_inverse(float f) { return __int_as_float((254 << 23) - __float_as_int(f)); }
 
 // Bytes of the two 16-bit halves -> fp32 scale.
 __device__ __forceinline__ float half_lo(uint32_t w) {
@@ -206,6 +224,68 @@ constexpr int decode_min_blocks() {
   return (NT == 1 && STAGES * KW * 16 * MT * sub_bytes_row<F>() <= 80 * 1024) ? 2 : 1;
 }
 
+// Stage x for one (block, token) entry in the block format's fragment order:
+// the fragments, the negated bias (cs[n]) and, for Q4_1, the x sum (sx[n]);
+// the padding column of an odd token count is zeroed with the last token.
+template <int F>
+__device__ __forceinline__ void stage_entry(const float (&xv)[32], uint4* dst, float* cs, float* sx, int n, int Nt,
+                                            int parity) {
+  if constexpr (F == GQ_TYPE_Q4_1) {
+    cs[n] = stage_block_q41(xv, dst, &sx[n]);
+    if ((Nt & 1) && n == Nt - 1) sx[Nt] = 0.f;
+  } else if constexpr (F == GQ_TYPE_Q8_0) {
+    cs[n] = stage_block_q80(xv, dst);
+  } else {
+    cs[n] = parity ? stage_block<1>(xv, dst) : stage_block<0>(xv, dst);
+  }
+  if ((Nt & 1) && n == Nt - 1) cs[Nt] = 0.f;
+}
+
+// The x staging's rare path (out of line): per token, the largest |x| over
+// this warp's blocks of the chunk, its factor wsc[n] (x_scale_down), and the
+// chunk's entries staged again as x * wsc[n].  Blocks past K were zeroed by
+// the first pass.  perm: the token -> x row map of a MUL_MAT_ID group (or
+// nullptr: row n).
+template <int F, int kStageK>
+__device__ __noinline__ void stage_x_scaled(const float* __restrict__ X, int K, const int* perm, int kc0, int kend,
+                                            int nst, int N, int Nt, int kw, int lane, uint4* xs, float* cs,
+                                            float* sxs, int csn, float* wsc) {
+  constexpr int kBoxBlocks = kSubK / kQK;
+  auto xrow = [&](int n) -> size_t { return perm ? static_cast<size_t>(__ldg(perm + n)) : static_cast<size_t>(n); };
+  for (int n = lane; n < Nt; n += 32) {
+    float m = 0.f;
+    for (int st = 0; st < nst; ++st)
+      for (int i = 0; i < kBoxBlocks; ++i) {
+        const int bl = st * (kStageK / kQK) + kw * kBoxBlocks + i;
+        if (kc0 + bl * kQK >= kend) continue;
+        const float4* xr = reinterpret_cast<const float4*>(X + xrow(n) * K + static_cast<size_t>(kc0 + bl * kQK));
+        for (int j = 0; j < 8; ++j) {
+          const float4 v = __ldg(xr + j);
+          m = fmaxf(fmaxf(m, fmaxf(fabsf(v.x), fabsf(v.y))), fmaxf(fabsf(v.z), fabsf(v.w)));
+        }
+      }
+    wsc[n] = x_scale_down(m);
+  }
+  __syncwarp();
+  const int nent = nst * kBoxBlocks * Nt;
+  for (int e = lane; e < nent; e += 32) {
+    const int st = e / (kBoxBlocks * Nt), rem = e % (kBoxBlocks * Nt);
+    const int bl = st * (kStageK / kQK) + kw * kBoxBlocks + rem / Nt;
+    const int n = rem % Nt;
+    if (kc0 + bl * kQK >= kend) continue;
+    const float f = wsc[n];
+    float xv[32];
+    const float4* xr = reinterpret_cast<const float4*>(X + xrow(n) * K + static_cast<size_t>(kc0 + bl * kQK));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 v = __ldg(xr + i);
+      xv[4 * i] = v.x * f; xv[4 * i + 1] = v.y * f; xv[4 * i + 2] = v.z * f; xv[4 * i + 3] = v.w * f;
+    }
+    stage_entry<F>(xv, xs + (bl * N + n) * 4, cs + bl * csn, sxs + bl * csn, n, Nt, (kc0 / kQK + bl) & 1);
+  }
+  __syncwarp();
+}
+
 // MOE: MUL_MAT_ID over the decode groups of rt (expert e, up to N tokens
 // each; with ONE, one token).  N is then the group capacity, which fixes the
 // shared-memory layout;
@@ -231,8 +311,9 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
   const int csn = Cfg::cs_stride(N);
   const int slot_floats = static_cast<int>(Cfg::slot_floats(N));
   int* slot_count = reinterpret_cast<int*>(acc_slots + Cfg::kSlots * slot_floats);
+  float* xsc = reinterpret_cast<float*>(slot_count + Cfg::kSlots);  // [KW][N]: x staged as x * xsc
   uint64_t* bars = reinterpret_cast<uint64_t*>(
-      (reinterpret_cast<uintptr_t>(slot_count + Cfg::kSlots) + 7) & ~uintptr_t(7));
+      (reinterpret_cast<uintptr_t>(xsc + KW * N) + 7) & ~uintptr_t(7));
   uint64_t* x_ready = bars + 2 * STAGES;  // every consumer warp has staged the first chunk of x
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES + 1);
 
@@ -364,51 +445,56 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
     // Each warp stages only the blocks of its own k boxes (box kw of every
     // stage), which only it reads: no CTA-wide barrier, so a warp starts on
     // its W as soon as its own x has arrived.
+    // fp16 holds |x| < 65520.  A token whose x in this warp's blocks reaches
+    // 2^15 is staged again as x * 2^-e (exact), with 2^-e taking its largest
+    // |x| below 2^15, and the warp's partial sums for it are multiplied by 2^e
+    // (exact); every other token keeps the factor 1.
     __syncwarp();  // this warp's previous chunk of fragments is no longer read
-    {
-      constexpr int kBoxBlocks = kSubK / kQK;  // 8
-      const int nent = nst * kBoxBlocks * Nt;  // (stage, block of the box, token) entries of this warp
-      for (int e = lane; e < nent; e += 32) {
-        const int st = e / (kBoxBlocks * Nt), rem = e % (kBoxBlocks * Nt);
-        const int bl = st * (Cfg::kStageK / kQK) + kw * kBoxBlocks + rem / Nt;  // block within the chunk
-        const int n = rem % Nt;
-        if (kc0 + bl * kQK >= kend) {
-          // Past K inside the last 256-k box (rows padded to a multiple of 256
-          // weights with zero blocks): zero x, so that the zero blocks add
-          // exact zeros rather than whatever the slot held before.
-          uint4* dst = xs + (bl * N + n) * 4;
-          dst[0] = dst[1] = dst[2] = dst[3] = make_uint4(0u, 0u, 0u, 0u);
-          cs[bl * csn + n] = 0.f;
-          if ((Nt & 1) && n == Nt - 1) cs[bl * csn + Nt] = 0.f;
-          if (F == GQ_TYPE_Q4_1) {
-            sxs[bl * csn + n] = 0.f;
-            if ((Nt & 1) && n == Nt - 1) sxs[bl * csn + Nt] = 0.f;
-          }
-          continue;
-        }
-        float xv[32];
-        const float4* xr =
-            reinterpret_cast<const float4*>(X + xrow(n) * K + static_cast<size_t>(kc0 + bl * kQK));
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 v = __ldg(xr + i);
-          xv[4 * i] = v.x; xv[4 * i + 1] = v.y; xv[4 * i + 2] = v.z; xv[4 * i + 3] = v.w;
-        }
+    constexpr int kBoxBlocks = kSubK / kQK;  // 8
+    const int nent = nst * kBoxBlocks * Nt;  // (stage, block of the box, token) entries of this warp
+    float lmax = 0.f;                        // largest |x| this lane staged
+    for (int e = lane; e < nent; e += 32) {
+      const int st = e / (kBoxBlocks * Nt), rem = e % (kBoxBlocks * Nt);
+      const int bl = st * (Cfg::kStageK / kQK) + kw * kBoxBlocks + rem / Nt;  // block within the chunk
+      const int n = rem % Nt;
+      if (kc0 + bl * kQK >= kend) {
+        // Past K inside the last 256-k box (rows padded to a multiple of 256
+        // weights with zero blocks): zero x, so that the zero blocks add
+        // exact zeros rather than whatever the slot held before.
         uint4* dst = xs + (bl * N + n) * 4;
-        if constexpr (F == GQ_TYPE_Q4_1) {
-          cs[bl * csn + n] = stage_block_q41(xv, dst, &sxs[bl * csn + n]);
+        dst[0] = dst[1] = dst[2] = dst[3] = make_uint4(0u, 0u, 0u, 0u);
+        cs[bl * csn + n] = 0.f;
+        if ((Nt & 1) && n == Nt - 1) cs[bl * csn + Nt] = 0.f;
+        if (F == GQ_TYPE_Q4_1) {
+          sxs[bl * csn + n] = 0.f;
           if ((Nt & 1) && n == Nt - 1) sxs[bl * csn + Nt] = 0.f;
-        } else if constexpr (F == GQ_TYPE_Q8_0) {
-          cs[bl * csn + n] = stage_block_q80(xv, dst);
-        } else {
-          cs[bl * csn + n] = ((kc0 / kQK + bl) & 1) ? stage_block<1>(xv, dst) : stage_block<0>(xv, dst);
         }
-        if ((Nt & 1) && n == Nt - 1) cs[bl * csn + Nt] = 0.f;  // the padding column read by the last lane pair
+        continue;
       }
+      float xv[32];
+      const float4* xr =
+          reinterpret_cast<const float4*>(X + xrow(n) * K + static_cast<size_t>(kc0 + bl * kQK));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 v = __ldg(xr + i);
+        xv[4 * i] = v.x; xv[4 * i + 1] = v.y; xv[4 * i + 2] = v.z; xv[4 * i + 3] = v.w;
+        lmax = fmaxf(fmaxf(lmax, fmaxf(fabsf(v.x), fabsf(v.y))), fmaxf(fabsf(v.z), fabsf(v.w)));
+      }
+      stage_entry<F>(xv, xs + (bl * N + n) * 4, cs + bl * csn, sxs + bl * csn, n, Nt, (kc0 / kQK + bl) & 1);
     }
+    const bool xwide = __any_sync(0xFFFFFFFFu, lmax >= kXScaleFrom);
+    if (xwide)
+      stage_x_scaled<F, Cfg::kStageK>(X, K, MOE ? rt.perm + first : nullptr, kc0, kend, nst, N, Nt, kw, lane, xs,
+                                      cs, sxs, csn, xsc + kw * N);
     __syncwarp();
     if (gk == 0 && c == 0 && lane == 0) mbar_arrive(smem_u32(x_ready));
 
+    // The tiles of this chunk.  WIDE: this warp staged some token scaled by
+    // xsc (rare), so its partial sums are taken back by 1 / xsc at the
+    // hand-off; a separate copy of the loop, so that the usual one is not
+    // touched by it.
+    auto run_tiles = [&](auto wide_tag) {
+    constexpr bool WIDE = decltype(wide_tag)::value;
     for (int tile = t_first; tile < ntiles; tile += t_step, ++tile_iter) {
       float acc[MT][NT][4];
 #pragma unroll
@@ -434,7 +520,7 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
             uint32_t wd[MT][2][2];  // [m-tile][row g / g+8][even / odd block] code words
-            uint32_t wh[MT][2][2];  // Q8_0: the code word of the block's second half
+            [[maybe_unused]] uint32_t wh[MT][2][2];  // Q8_0: the code word of the block's second half
             float dd[MT][2][2];     // scales
             float mm[MT][2][2];     // Q4_1 min offsets
 #pragma unroll
@@ -563,7 +649,9 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int n = nt * 8 + 2 * t + (i & 1);
-            if (n < Nt) mine[n * kBM + mt * 16 + g + 8 * (i >> 1)] = acc[mt][nt][i];
+            if (n < Nt)
+              mine[n * kBM + mt * 16 + g + 8 * (i >> 1)] =
+                  WIDE ? acc[mt][nt][i] * pow2_inverse(xsc[kw * N + n]) : acc[mt][nt][i];
           }
       __syncwarp();
       int prev = 0;
@@ -607,6 +695,11 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
         }
       }
     }
+    };
+    if (xwide)
+      run_tiles(std::true_type{});
+    else
+      run_tiles(std::false_type{});
   }
 }
 

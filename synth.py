@@ -135,3 +135,18 @@ def typed_weights(qtype: int, M: int, K: int, seed: int) -> np.ndarray:
         out[:, :, 0:2] = random_scales(seed, M * nb, 0.0003, 0.0012).view(np.uint8).reshape(M, nb, 2)
         return out.reshape(M, nb * 34)
     raise ValueError("unknown block type")
+
+
+def wide_range_activations(N: int, K: int, seed: int, tokens, magnitudes=(1e5, 1e9)) -> np.ndarray:
+    """fp32 N(0, 1) activations whose listed tokens carry, in a quarter of their
+    32-element blocks (at least one), values scaled by 10^U[log10 lo, log10 hi]
+    (beyond the fp16 range): the wide-range stress input of the decode path."""
+    X = activations(N, K, seed)
+    rng = np.random.Generator(np.random.SFC64(seed + 1))
+    lo, hi = np.log10(magnitudes[0]), np.log10(magnitudes[1])
+    nb = K // QK4_0
+    for n in tokens:
+        blocks = rng.choice(nb, size=max(1, nb // 4), replace=False)
+        for b in blocks:
+            X[n, b * QK4_0:(b + 1) * QK4_0] *= np.float32(10.0 ** rng.uniform(lo, hi))
+    return X
