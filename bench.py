@@ -322,6 +322,7 @@ def run_gpu(args, rank, world, dist):
         aux["mul_mat_id"] = run_moe_aux(gq, torch, dev, s, peaks)
         aux["legacy_formats"] = run_legacy_aux(gq, torch, dev, s, peaks)
         aux["prepared_layout"] = run_prepared_aux(gq, torch, dev, s, peaks)
+        aux["library_reference"] = run_library_reference(gq, torch, dev, s, peaks)
     e2e["ms"] = max_over_ranks([e2e["ms"]], dist, dev)[0]
     e2e_value = world * wbytes / (e2e["ms"] * 1e-3) / 1e9
 
@@ -329,10 +330,13 @@ def run_gpu(args, rank, world, dist):
     if rank == 0 and not args.no_cpu_baseline:
         nthreads = os.cpu_count() or 1
         gbs, n, b, dt = oracle_decode_rate(host_w, acts1, args.cpu_budget, nthreads)
+        gbs1, n1, b1, dt1 = oracle_decode_rate(host_w, acts1, args.cpu_budget / 5, 1, max_passes=1)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": nthreads, "kind": "oracle",
                "sample": f"oracle MUL_MAT at N=1, {n} matrices taken in order from the same "
                          f"{len(host_w)}-matrix sweep, repeated ({b / 1e6:.0f} MB of weights, {dt:.1f} s), "
-                         f"fp64 sums"}
+                         f"fp64 sums",
+               "single_thread": {"value": round(gbs1, 4), "unit": "GB/s", "cores": 1,
+                                 "sample": f"the first {n1} matrices of the sweep ({b1 / 1e6:.0f} MB, {dt1:.1f} s)"}}
 
     if rank != 0:
         return 0
@@ -376,6 +380,7 @@ def run_gpu(args, rank, world, dist):
         "mul_mat_id": aux.get("mul_mat_id"),
         "legacy_formats": aux.get("legacy_formats"),
         "prepared_layout": aux.get("prepared_layout"),
+        "library_reference": aux.get("library_reference"),
         "gpu_launches": K_ * (len(shapes) + len(shapes) + L * len(ks)),
         "clocks": clocks,
         "cpu_baseline": cpu,
@@ -420,6 +425,61 @@ def run_aux(gq, torch, dev, s, hbm_gbs):
         out[name] = {"kernel": kern, "shape": f"{M}x{K}", "us": round(t * 1e6, 2), "achieved": round(gbs, 1),
                      "unit": "GB/s", "peak": hbm_gbs, "frac": round(gbs / hbm_gbs, 4), "bound": "hbm",
                      "bytes": qbytes + fbytes, "bytes_note": "4*M*K fp32 + M*K/32*18 Q4_0, one read, one written"}
+    return out
+
+
+def run_library_reference(gq, torch, dev, s, peaks):
+    """Library reference point, timed only (not part of any value): what a
+    caller without these kernels would do on the 14336 x 4096 matrix, namely
+    dequantise W to dense bf16 and multiply with torch.matmul (cuBLAS), either
+    once per call or once up front with the dense copy kept (4x the weight
+    bytes).  Against it: the Q4_0 MUL_MAT of this library on the same shapes."""
+    M, K = AUX_M, AUX_K
+    Wq = [torch.from_numpy(synth.q4_0_weights(M, K, seed=0x51B0 + i)).to(dev) for i in range(3)]
+    Wd = []
+    for w in Wq:
+        f = torch.empty(M, K, dtype=torch.float32, device=dev)
+        gq.gq_dequant_q4_0(w, M, K, f, stream=s)
+        Wd.append(f.to(torch.bfloat16))  # 117 MB each: three copies rotate past L2 at N = 1
+        del f
+    Ws = torch.empty(M, K, dtype=torch.float32, device=dev)
+    g = torch.Generator(device=dev).manual_seed(0x51B8)
+    X = {n: torch.randn(n, K, device=dev, generator=g) for n in (1, 512)}
+    Xb = {n: x.to(torch.bfloat16) for n, x in X.items()}
+    Y = {n: torch.empty(n, M, device=dev) for n in (1, 512)}
+    reps = 12
+
+    def timed(fn):
+        with torch.cuda.stream(s):
+            for i in range(3):
+                fn(i)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for i in range(reps):
+                fn(i)
+            e1.record(s)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / reps * 1e-3
+
+    def per_call(i, n):  # dequantise, convert, multiply: nothing cached
+        gq.gq_dequant_q4_0(Wq[i % 3], M, K, Ws, stream=s)
+        torch.matmul(Xb[n], Ws.to(torch.bfloat16).t())
+
+    out = {"note": "timed only; torch.matmul is cuBLAS bf16, fp32 accumulate; W dequantised by gq_dequant_q4_0"}
+    for n in (1, 512):
+        flops = 2.0 * M * K * n
+        t_dense = timed(lambda i: torch.matmul(Xb[n], Wd[i % 3].t()))
+        t_call = timed(lambda i: per_call(i, n))
+        t_ours = timed(lambda i: gq.gq_mul_mat_q4_0(Wq[i % 3], M, K, X[n], n, Y[n], stream=s))
+        out[f"n{n}"] = {
+            "dense_bf16_matmul_us": round(t_dense * 1e6, 2),
+            "dequant_then_matmul_us": round(t_call * 1e6, 2),
+            "gq_mul_mat_q4_0_us": round(t_ours * 1e6, 2),
+            "dense_bf16_matmul_tflops": round(flops / t_dense / 1e12, 1),
+            "gq_mul_mat_q4_0_tflops": round(flops / t_ours / 1e12, 1),
+            "weight_bytes": {"dense_bf16": 2 * M * K, "q4_0": M * K // 32 * 18},
+        }
+    gq.gq_sync_status(s)
     return out
 
 
