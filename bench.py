@@ -717,6 +717,9 @@ PROFILE_CASES = {
     "prefill_down": (4096, 11008, 512, "bf16"),
     "moe_prefill": (MOE_M, MOE_K, 512, "moe"),
     "moe_decode": (MOE_M, MOE_K, 1, "moe"),
+    "q4_1_decode": (14336, 4096, 1, "q4_1"),
+    "q8_0_decode": (14336, 4096, 1, "q8_0"),
+    "quantize": (14336, 4096, 0, "quantize"),
 }
 
 
@@ -738,6 +741,26 @@ def run_profile_case(name, pair=False):
         torch.cuda.synchronize()
         gq.gq_sync_status()
         print(f"profile case {name}: {MOE_E} experts {M}x{K}, {N} tokens x {MOE_S} ok")
+        return 0
+    if mode in ("q4_1", "q8_0"):  # the decode kernel on the other block formats
+        qt = gq.GQ_TYPE_Q4_1 if mode == "q4_1" else gq.GQ_TYPE_Q8_0
+        W = torch.from_numpy(synth.typed_weights(qt, M, K, seed=1)).cuda()
+        X = torch.from_numpy(synth.activations(N, K, seed=2)).cuda()
+        Y = torch.empty(N, M, device="cuda")
+        for _ in range(2):
+            gq.gq_mul_mat(qt, W, M, K, X, N, Y)
+        torch.cuda.synchronize()
+        gq.gq_sync_status()
+        print(f"profile case {name}: M={M} K={K} N={N} ok")
+        return 0
+    if mode == "quantize":  # fp32 -> Q4_0
+        Wf = torch.from_numpy(synth.activations(M, K, seed=3)).cuda() * 0.05
+        Q = torch.empty(M, K // 32 * 18, dtype=torch.uint8, device="cuda")
+        for _ in range(2):
+            gq.gq_quantize_q4_0(Wf, M, K, Q)
+        torch.cuda.synchronize()
+        gq.gq_sync_status()
+        print(f"profile case {name}: M={M} K={K} ok")
         return 0
     W = torch.from_numpy(synth.q4_0_weights(M, K, seed=1)).cuda()
     X = torch.from_numpy(synth.activations(N, K, seed=2)).cuda()
