@@ -75,6 +75,8 @@ class Oracle:
         lib.oracle_dequant_typed.restype = None
         lib.oracle_mul_mat_typed.argtypes = [i32, vp, i64, i64, vp, i64, vp, vp, i32]
         lib.oracle_mul_mat_typed.restype = None
+        lib.oracle_validate_typed.argtypes = [i32, vp, i64, i64, vp, vp]
+        lib.oracle_validate_typed.restype = None
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = i32
         self.lib = lib
@@ -170,6 +172,17 @@ class Oracle:
         self.lib.oracle_mul_mat_typed(qtype, W.ctypes.data, M, K, X.ctypes.data, N, Y.ctypes.data,
                                       S.ctypes.data, int(nthreads))
         return Y, S
+
+    def validate(self, qtype: int, W: np.ndarray, M: int, K: int):
+        """(count, first): blocks with a non-finite scale, and the first one's
+        flat index (row * K/32 + block), or None when there is none."""
+        W = np.ascontiguousarray(W, dtype=np.uint8)
+        if W.size != self.type_nbytes(qtype, M, K):
+            raise ValueError("W has the wrong number of bytes")
+        out = np.zeros(2, dtype=np.uint64)
+        self.lib.oracle_validate_typed(qtype, W.ctypes.data, M, K, out.ctypes.data, out[1:].ctypes.data)
+        count, first = int(out[0]), int(out[1])
+        return count, (None if first == 2**64 - 1 else first)
 
     def max_threads(self) -> int:
         return int(self.lib.oracle_max_threads())

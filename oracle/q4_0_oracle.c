@@ -308,6 +308,25 @@ void oracle_dequant_typed(int type, const uint8_t *W, int64_t M, int64_t K, floa
         dequant_row_typed(type, W + (size_t)m * row_bytes, K, out + (size_t)m * (size_t)K);
 }
 
+void oracle_validate_typed(int type, const uint8_t *W, int64_t M, int64_t K, uint64_t *count, uint64_t *first)
+{
+    int bb = type_block_bytes(type);
+    uint64_t nblocks = (uint64_t)M * (uint64_t)(K / QK);
+    *count = 0;
+    *first = UINT64_MAX;
+    for (uint64_t b = 0; b < nblocks; ++b) {
+        const uint8_t *blk = W + b * (uint64_t)bb;
+        int bad = !isfinite(oracle_half_to_double((uint16_t)(blk[0] | (blk[1] << 8))));
+        if (type == ORACLE_TYPE_Q4_1)
+            bad |= !isfinite(oracle_half_to_double((uint16_t)(blk[2] | (blk[3] << 8))));
+        if (bad) {
+            if (*count == 0)
+                *first = b;
+            ++*count;
+        }
+    }
+}
+
 void oracle_mul_mat_typed(int type, const uint8_t *W, int64_t M, int64_t K, const float *X, int64_t N,
                           double *Y, double *S, int nthreads)
 {

@@ -102,6 +102,17 @@ void oracle_dequant_typed(int type, const uint8_t *W, int64_t M, int64_t K, floa
 void oracle_mul_mat_typed(int type, const uint8_t *W, int64_t M, int64_t K, const float *X, int64_t N,
                           double *Y, double *S, int nthreads);
 
+/*
+ * Row-data validation ("Data structures and GGUF format", ggml_validate_row_data:
+ * a block's fp16 scale fields must be finite; every 4- or 8-bit code is a
+ * valid value).  Over the M x K weights in block format `type`: *count = the
+ * number of blocks with a NaN or infinite scale (d; for Q4_1 also m),
+ * *first = the smallest flat block index (row * K/32 + block) among them, or
+ * UINT64_MAX when there is none.  A scale is tested by decoding it with
+ * oracle_half_to_double and asking isfinite.
+ */
+void oracle_validate_typed(int type, const uint8_t *W, int64_t M, int64_t K, uint64_t *count, uint64_t *first);
+
 /* Number of threads OpenMP would use by default (1 without OpenMP). */
 int oracle_max_threads(void);
 
