@@ -99,6 +99,22 @@ size_t gq_type_nbytes(gq_type type, int64_t M, int64_t K);
  * GQ_ERR_SHAPE for an unknown type. */
 gq_status gq_dequant(gq_type type, const void *W, int64_t M, int64_t K, float *out, void *stream);
 
+/* Row-data validation ("Data structures and GGUF format",
+ * ggml_validate_row_data): scan W (M x K in block format `type`, rows
+ * contiguous) for blocks whose fp16 scale fields are NaN or infinite -- d in
+ * every format, and m in Q4_1; codes are always valid.  result: device
+ * pointer to two uint64 values, written on `stream`: result[0] = the number of
+ * such blocks, result[1] = the smallest flat block index (row * K/32 + block)
+ * among them, or UINT64_MAX when there is none.  Asynchronous: read result
+ * after the stream.  Any alignment of W; result 8-byte aligned.  M or K == 0:
+ * result (0, UINT64_MAX).  Errors: GQ_ERR_SHAPE (negative size, K % 32 != 0,
+ * unknown type), GQ_ERR_NULL (result NULL, or W NULL with M*K > 0),
+ * GQ_ERR_ALIGN (result not 8-byte aligned). */
+gq_status gq_validate(gq_type type, const void *W, int64_t M, int64_t K, uint64_t *result, void *stream);
+
+/* gq_validate for Q4_0 weights. */
+gq_status gq_validate_q4_0(const void *W, int64_t M, int64_t K, uint64_t *result, void *stream);
+
 /* MUL_MAT with W in block format `type`: Y[N][M] = X[N][K] * W^T, fp32 in and
  * out.  GQ_TYPE_Q4_0 is gq_mul_mat_q4_0.  Q4_1 and Q8_0, with K % 256 == 0
  * and W, X, Y 16-byte aligned: N >= GQ_OPT_PREFILL_MIN_N converts X to bf16

@@ -53,6 +53,8 @@ SIGNATURES = {
     "gq_dequant_q4_0": (_i32, [_vp, _i64, _i64, _vp, _vp]),
     "gq_type_nbytes": (_sz, [_i32, _i64, _i64]),
     "gq_dequant": (_i32, [_i32, _vp, _i64, _i64, _vp, _vp]),
+    "gq_validate": (_i32, [_i32, _vp, _i64, _i64, _vp, _vp]),
+    "gq_validate_q4_0": (_i32, [_vp, _i64, _i64, _vp, _vp]),
     "gq_mul_mat": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "gq_quantize_q4_0": (_i32, [_vp, _i64, _i64, _vp, _vp]),
     "gq_mul_mat_q4_0": (_i32, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
@@ -136,6 +138,14 @@ def gq_type_nbytes(qtype: int, M: int, K: int) -> int:
 
 def gq_dequant(qtype: int, W, M: int, K: int, out, stream=None) -> None:
     _check(_lib.gq_dequant(qtype, _ptr(W), M, K, _ptr(out), _stream(stream)))
+
+
+def gq_validate(qtype: int, W, M: int, K: int, result, stream=None) -> None:
+    _check(_lib.gq_validate(qtype, _ptr(W), M, K, _ptr(result), _stream(stream)))
+
+
+def gq_validate_q4_0(W, M: int, K: int, result, stream=None) -> None:
+    _check(_lib.gq_validate_q4_0(_ptr(W), M, K, _ptr(result), _stream(stream)))
 
 
 def gq_mul_mat(qtype: int, W, M: int, K: int, X, N: int, Y, stream=None) -> None:
@@ -284,6 +294,22 @@ def dequant(qtype: int, W: torch.Tensor, K: int, stream=None) -> torch.Tensor:
     out = torch.empty((M, K), dtype=torch.float32, device=W.device)
     gq_dequant(qtype, W, M, K, out, stream)
     return out
+
+
+def validate(qtype: int, W: torch.Tensor, K: int, M: int | None = None, stream=None):
+    """Blocks of W (block format qtype) with a NaN or infinite scale field:
+    (count, first flat block index or None).  Synchronises the stream."""
+    if W.dtype != torch.uint8:
+        raise TypeError("W must be uint8 (raw block bytes)")
+    if M is None:
+        M = _rows_of(W, qtype, K)
+    result = torch.empty(2, dtype=torch.int64, device=W.device)
+    gq_validate(qtype, W, M, K, result, stream)
+    if stream is not None:
+        stream.synchronize()
+    r = result.cpu().tolist()  # uint64 values read as int64: mask back to unsigned
+    count, first = int(r[0]), int(r[1]) & 0xFFFFFFFFFFFFFFFF
+    return count, (None if first == 0xFFFFFFFFFFFFFFFF else first)
 
 
 def mul_mat(qtype: int, W: torch.Tensor, X: torch.Tensor, stream=None, out: torch.Tensor | None = None) -> torch.Tensor:

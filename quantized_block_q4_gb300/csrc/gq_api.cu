@@ -277,6 +277,26 @@ gq_status gq_dequant(gq_type type, const void* W, int64_t M, int64_t K, float* o
   return e == cudaSuccess ? GQ_OK : cuda_fail(e, "dequant launch");
 }
 
+gq_status gq_validate(gq_type type, const void* W, int64_t M, int64_t K, uint64_t* result, void* stream) {
+  t_last_error.clear();
+  if (type_block_bytes(type) == 0) return fail(GQ_ERR_SHAPE, "unknown block type %d", static_cast<int>(type));
+  if (M < 0 || K < 0) return fail(GQ_ERR_SHAPE, "negative size");
+  if (K % kQK) return fail(GQ_ERR_SHAPE, "K=%lld is not a multiple of 32", (long long)K);
+  if (!result) return fail(GQ_ERR_NULL, "result must not be NULL");
+  if (!aligned(result, 8)) return fail(GQ_ERR_ALIGN, "result must be 8-byte aligned");
+  if (M > 0 && K > 0 && !W) return fail(GQ_ERR_NULL, "W must not be NULL");
+  if ((unsigned __int128)M * K > ((unsigned __int128)1 << 62)) return fail(GQ_ERR_SHAPE, "size overflows");
+  gq_status st = check_device();
+  if (st != GQ_OK) return st;
+  cudaError_t e = launch_validate(static_cast<const uint8_t*>(W), M * (K / kQK), type,
+                                  reinterpret_cast<unsigned long long*>(result), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GQ_OK : cuda_fail(e, "validate launch");
+}
+
+gq_status gq_validate_q4_0(const void* W, int64_t M, int64_t K, uint64_t* result, void* stream) {
+  return gq_validate(GQ_TYPE_Q4_0, W, M, K, result, stream);
+}
+
 gq_status gq_mul_mat(gq_type type, const void* W, int64_t M, int64_t K, const float* X, int64_t N, float* Y,
                      void* stream) {
   if (type == GQ_TYPE_Q4_0) return gq_mul_mat_q4_0(W, M, K, X, N, Y, stream);

@@ -116,6 +116,12 @@ cudaError_t launch_decode_moe(const CUtensorMap* tmW, const float* X, int cap, i
 // ---- KL: Q4_1 / Q8_0 dequantisation and MUL_MAT (gq_legacy.cu)
 int type_block_bytes(int type);  // 18 / 20 / 34, 0 for an unknown type
 cudaError_t launch_dequant_legacy(int type, const uint8_t* W, int64_t nblocks, float* out, cudaStream_t s);
+
+// ---- KV: row-data validation (gq_validate.cu).  result[0] = blocks with a
+// non-finite scale field, result[1] = the smallest such flat block index (or
+// all ones); both reset on the stream first.
+cudaError_t launch_validate(const uint8_t* W, int64_t nblocks, int type, unsigned long long* result,
+                            cudaStream_t s);
 cudaError_t launch_mul_mat_legacy(int type, const uint8_t* W, int64_t M, int64_t K, const float* X, int64_t N,
                                   float* Y, uint64_t wait_limit_ns, cudaStream_t s);
 

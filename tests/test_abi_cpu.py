@@ -76,6 +76,12 @@ def test_argument_errors_before_any_device_work(lib):
     assert L2(None, 2, 4, 32, None, 2, None, 0, None, None) == lib.GQ_OK                 # no tokens
     assert L2(None, 2, 0, 32, None, 2, None, 3, None, None) == lib.GQ_OK                 # no rows
     assert L2(None, 2, 4, 32, None, 2, None, 3, None, None) == lib.GQ_ERR_NULL
+    assert L.gq_validate(1, None, 4, 33, None, None) == lib.GQ_ERR_SHAPE                # K % 32
+    assert L.gq_validate(7, None, 4, 32, None, None) == lib.GQ_ERR_SHAPE                # unknown type
+    assert L.gq_validate(0, None, -1, 32, None, None) == lib.GQ_ERR_SHAPE               # negative rows
+    assert L.gq_validate(0, None, 4, 32, None, None) == lib.GQ_ERR_NULL                 # no result
+    assert L.gq_validate_q4_0(None, 4, 32, 8 * 1024 + 4, None) == lib.GQ_ERR_ALIGN      # result misaligned
+    assert L.gq_validate_q4_0(None, 4, 32, 8 * 1024, None) == lib.GQ_ERR_NULL           # W NULL, M*K > 0
     assert lib.gq_status_string(-8) == "GQ_ERR_BAD_INDEX"
     old = lib.gq_get_option(lib.GQ_OPT_MOE_PATH)
     with pytest.raises(lib.GQError):
