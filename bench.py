@@ -377,6 +377,7 @@ def run_gpu(args, rank, world, dist):
                         "gq_mul_mat_q4_0 calls, every Y -> pinned host in one copy (decode sweep)"},
         "dequant": aux.get("dequant"),
         "quantize": aux.get("quantize"),
+        "validate": aux.get("validate"),
         "mul_mat_id": aux.get("mul_mat_id"),
         "legacy_formats": aux.get("legacy_formats"),
         "prepared_layout": aux.get("prepared_layout"),
@@ -418,8 +419,21 @@ def run_aux(gq, torch, dev, s, hbm_gbs):
 
     tq = timed(lambda: gq.gq_quantize_q4_0(Wf, M, K, Q, stream=s))
     td = timed(lambda: gq.gq_dequant_q4_0(Q, M, K, D, stream=s))
+    R = torch.empty(2, dtype=torch.int64, device=dev)
+    Qs = [Q] + [Q.clone() for _ in range(5)]  # 6 x 33 MB: each call reads W from DRAM
+    calls = [0]
+
+    def validate():
+        gq.gq_validate_q4_0(Qs[calls[0] % len(Qs)], M, K, R, stream=s)
+        calls[0] += 1
+    tv = timed(validate)
     gq.gq_sync_status(s)
     out = {}
+    vgbs = qbytes / tv / 1e9
+    out["validate"] = {"kernel": "k_validate", "shape": f"{M}x{K}", "us": round(tv * 1e6, 2),
+                       "achieved": round(vgbs, 1), "unit": "GB/s", "peak": hbm_gbs, "frac": round(vgbs / hbm_gbs, 4),
+                       "bound": "hbm", "bytes": qbytes, "bytes_note": "M*K/32*18 Q4_0 read (every sector holds a scale)",
+                       "includes": "the one-thread reset of the result (overlapped under programmatic dependent launch)"}
     for name, t, kern in (("quantize", tq, "k_quantize_q4_0"), ("dequant", td, "k_dequant_vec")):
         gbs = (qbytes + fbytes) / t / 1e9
         out[name] = {"kernel": kern, "shape": f"{M}x{K}", "us": round(t * 1e6, 2), "achieved": round(gbs, 1),

@@ -289,7 +289,8 @@ gq_status gq_validate(gq_type type, const void* W, int64_t M, int64_t K, uint64_
   gq_status st = check_device();
   if (st != GQ_OK) return st;
   cudaError_t e = launch_validate(static_cast<const uint8_t*>(W), M * (K / kQK), type,
-                                  reinterpret_cast<unsigned long long*>(result), static_cast<cudaStream_t>(stream));
+                                  reinterpret_cast<unsigned long long*>(result), static_cast<int>(g_pdl.load()),
+                                  static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? GQ_OK : cuda_fail(e, "validate launch");
 }
 

@@ -119,8 +119,8 @@ cudaError_t launch_dequant_legacy(int type, const uint8_t* W, int64_t nblocks, f
 
 // ---- KV: row-data validation (gq_validate.cu).  result[0] = blocks with a
 // non-finite scale field, result[1] = the smallest such flat block index (or
-// all ones); both reset on the stream first.
-cudaError_t launch_validate(const uint8_t* W, int64_t nblocks, int type, unsigned long long* result,
+// all ones); both reset on the stream first (pdl: the scan overlaps the reset).
+cudaError_t launch_validate(const uint8_t* W, int64_t nblocks, int type, unsigned long long* result, int pdl,
                             cudaStream_t s);
 cudaError_t launch_mul_mat_legacy(int type, const uint8_t* W, int64_t M, int64_t K, const float* X, int64_t N,
                                   float* Y, uint64_t wait_limit_ns, cudaStream_t s);

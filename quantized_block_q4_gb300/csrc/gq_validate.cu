@@ -9,10 +9,13 @@
 // takes its smallest bad index with shuffles, and lane 0 folds them into the
 // caller's result with one 64-bit atomic add and one atomic min.  Every sector of W
 // holds a scale byte, so the pass streams the whole matrix: HBM-bound at the
-// weight bytes.
+// weight bytes.  A one-thread kernel resets the result first; under
+// programmatic dependent launch the scan starts while it runs and waits for
+// it only before its atomics.
 #include <algorithm>
 
 #include "gq_internal.h"
+#include "gq_ptx.cuh"
 
 namespace gq {
 namespace {
@@ -22,6 +25,15 @@ constexpr int kVThreads = 256;
 // An fp16 value is NaN or infinite exactly when its five exponent bits (bits
 // 10..14, i.e. bits 2..6 of the little-endian high byte) are all ones.
 __device__ __forceinline__ bool half_not_finite(uint32_t hi_byte) { return (hi_byte & 0x7Cu) == 0x7Cu; }
+
+// Waits for the kernel before (which may still read the previous result, and
+// which the scan must follow), then lets the scan start.
+__global__ void k_validate_init(unsigned long long* __restrict__ result) {
+  pdl_wait();
+  pdl_launch_dependents();
+  result[0] = 0ull;
+  result[1] = ~0ull;
+}
 
 __global__ void __launch_bounds__(kVThreads)
     k_validate(const uint8_t* __restrict__ W, uint64_t nblocks, int block_bytes, int check_min,
@@ -43,6 +55,7 @@ __global__ void __launch_bounds__(kVThreads)
     const unsigned long long f = __shfl_xor_sync(0xFFFFFFFFu, first, o);
     first = f < first ? f : first;
   }
+  pdl_wait();  // the reset of the result has landed
   if ((threadIdx.x & 31) == 0 && count) {
     atomicAdd(&result[0], count);
     atomicMin(&result[1], first);
@@ -51,16 +64,24 @@ __global__ void __launch_bounds__(kVThreads)
 
 }  // namespace
 
-cudaError_t launch_validate(const uint8_t* W, int64_t nblocks, int type, unsigned long long* result,
+cudaError_t launch_validate(const uint8_t* W, int64_t nblocks, int type, unsigned long long* result, int pdl,
                             cudaStream_t s) {
-  cudaError_t e = cudaMemsetAsync(result, 0, sizeof(unsigned long long), s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(result + 1, 0xFF, sizeof(unsigned long long), s);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(1);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_validate_init, result);
   if (e != cudaSuccess || nblocks == 0) return e;
   const int64_t want = (nblocks + kVThreads - 1) / kVThreads;
-  const int grid = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(device_info().sm_count) * 8));
-  k_validate<<<grid, kVThreads, 0, s>>>(W, static_cast<uint64_t>(nblocks), type_block_bytes(type),
-                                        type == GQ_TYPE_Q4_1 ? 1 : 0, result);
-  return cudaGetLastError();
+  cfg.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>(want, static_cast<int64_t>(device_info().sm_count) * 8)));
+  cfg.blockDim = dim3(kVThreads);
+  return cudaLaunchKernelEx(&cfg, k_validate, W, static_cast<uint64_t>(nblocks), type_block_bytes(type),
+                            type == GQ_TYPE_Q4_1 ? 1 : 0, result);
 }
 
 }  // namespace gq
