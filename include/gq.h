@@ -99,8 +99,9 @@ size_t gq_type_nbytes(gq_type type, int64_t M, int64_t K);
  * GQ_ERR_SHAPE for an unknown type. */
 gq_status gq_dequant(gq_type type, const void *W, int64_t M, int64_t K, float *out, void *stream);
 
-/* Row-data validation ("Data structures and GGUF format",
- * ggml_validate_row_data): scan W (M x K in block format `type`, rows
+/* Row-data validation ("GGUF loading, mmap and tensor placement", the
+ * section on --check-tensors: ggml_validate_row_data checks each row's scale
+ * factors and integers): scan W (M x K in block format `type`, rows
  * contiguous) for blocks whose fp16 scale fields are NaN or infinite -- d in
  * every format, and m in Q4_1; codes are always valid.  result: device
  * pointer to two uint64 values, written on `stream`: result[0] = the number of

@@ -103,9 +103,10 @@ void oracle_mul_mat_typed(int type, const uint8_t *W, int64_t M, int64_t K, cons
                           double *Y, double *S, int nthreads);
 
 /*
- * Row-data validation ("Data structures and GGUF format", ggml_validate_row_data:
- * a block's fp16 scale fields must be finite; every 4- or 8-bit code is a
- * valid value).  Over the M x K weights in block format `type`: *count = the
+ * Row-data validation ("GGUF loading, mmap and tensor placement", the section
+ * on --check-tensors and parallel validation: ggml_validate_row_data checks
+ * each row's scale factors and integers; the reading: a block's fp16 scale
+ * fields must be finite, and every 4- or 8-bit code is a valid integer).  Over the M x K weights in block format `type`: *count = the
  * number of blocks with a NaN or infinite scale (d; for Q4_1 also m),
  * *first = the smallest flat block index (row * K/32 + block) among them, or
  * UINT64_MAX when there is none.  A scale is tested by decoding it with

@@ -1,5 +1,7 @@
-// KV: row-data validation of block-quantised weights ("Data structures and
-// GGUF format", ggml_validate_row_data): a block is invalid when one of its
+// KV: row-data validation of block-quantised weights ("GGUF loading, mmap
+// and tensor placement", the section on --check-tensors and parallel
+// validation: ggml_validate_row_data checks each row's scale factors and
+// integers).  Reading: a block is invalid when one of its
 // fp16 scale fields is NaN or infinite (exponent bits all ones) -- d for
 // every format, and m for Q4_1; the 4- and 8-bit codes are always valid.
 //

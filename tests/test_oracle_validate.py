@@ -1,7 +1,8 @@
 """Pins of the oracle's row-data validation (CPU only).
 
 A block is invalid when one of its fp16 scale fields (d; for Q4_1 also m) is
-NaN or infinite ("Data structures and GGUF format", ggml_validate_row_data);
+NaN or infinite ("GGUF loading, mmap and tensor placement", the section on
+--check-tensors: ggml_validate_row_data checks each row's scales and integers);
 codes are never invalid.  Pinned against numpy's float16 classification of
 all 65,536 bit patterns (an independent decoder), hand-placed bad blocks at
 known positions, and the empty cases.
