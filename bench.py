@@ -555,7 +555,8 @@ def run_moe_aux(gq, torch, dev, s, peaks):
         else:
             b = wbytes + 4 * P * K + 4 * P * M
             gbs = b / t / 1e9
-            entry.update({"path": "routing + decode kernel", "achieved": round(gbs, 1), "unit": "GB/s",
+            path = "decode kernel reading the ids itself (no routing)" if T == 1 else "routing + decode kernel"
+            entry.update({"path": path, "achieved": round(gbs, 1), "unit": "GB/s",
                           "peak": peaks["hbm_gbs"], "bound": "hbm", "frac": round(gbs / peaks["hbm_gbs"], 4),
                           "bytes": b, "bytes_note": "used experts' Q4_0 weights + fp32 x and y"})
         out[name] = entry

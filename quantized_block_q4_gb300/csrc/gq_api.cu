@@ -443,6 +443,26 @@ gq_status gq_mul_mat_id_q4_0(const void* W, int64_t n_expert, int64_t M, int64_t
   if (tc && n_mtiles * ((P + kMoeBN - 1) / kMoeBN + used) > lim)
     return fail(GQ_ERR_SHAPE, "too many tensor-core work items");
 
+  const uint64_t limit = static_cast<uint64_t>(g_wait_limit_ns.load());
+  const int pdl = static_cast<int>(g_pdl.load());
+  const uint64_t row_bytes = static_cast<uint64_t>(K / kQK) * kBlockBytes;
+  if (!tc && cap == 1) {
+    // A single token: every slot is a one-token group of its own, so the
+    // decode kernel reads the ids itself -- no routing kernel, no scratch.
+    MoeRoute rt{};
+    rt.ids = ids;
+    rt.np = static_cast<int32_t>(P);
+    rt.ne = static_cast<int32_t>(n_expert);
+    CUtensorMap tm;
+    uint32_t bx = 0, by = 0;
+    decode_moe_w_box(cap, &bx, &by);
+    st = make_tmap(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, row_bytes, static_cast<uint64_t>(n_expert * M), row_bytes,
+                   bx, by, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != GQ_OK) return st;
+    const cudaError_t e = launch_decode_moe(&tm, X, cap, n_expert, M, K, P, rt, Y, limit, pdl, s);
+    return e == cudaSuccess ? GQ_OK : cuda_fail(e, "MUL_MAT_ID decode launch");
+  }
+
   const size_t route_bytes = (moe_route_ints(n_expert, P, cap) * sizeof(int32_t) + 255) / 256 * 256;
   const size_t xg_bytes = tc ? static_cast<size_t>(P) * K * sizeof(uint16_t) : 0;
   void* scratch = nullptr;
@@ -450,9 +470,6 @@ gq_status gq_mul_mat_id_q4_0(const void* W, int64_t n_expert, int64_t M, int64_t
   if (e != cudaSuccess)
     return fail(GQ_ERR_ALLOC, "scratch allocation (%zu bytes): %s", route_bytes + xg_bytes, cudaGetErrorString(e));
   const MoeRoute rt = moe_route_layout(static_cast<int32_t*>(scratch), n_expert, P, cap);
-  const uint64_t limit = static_cast<uint64_t>(g_wait_limit_ns.load());
-  const int pdl = static_cast<int>(g_pdl.load());
-  const uint64_t row_bytes = static_cast<uint64_t>(K / kQK) * kBlockBytes;
   const char* what = "MUL_MAT_ID routing launch";
   e = launch_moe_route(ids, P, n_expert, n_mtiles, kMoeBN, cap, rt, Y, M, pdl, s);
   if (e == cudaSuccess && !tc) {

@@ -244,14 +244,17 @@ __device__ __forceinline__ void stage_entry(const float (&xv)[32], uint4* dst, f
 // The x staging's rare path (out of line): per token, the largest |x| over
 // this warp's blocks of the chunk, its factor wsc[n] (x_scale_down), and the
 // chunk's entries staged again as x * wsc[n].  Blocks past K were zeroed by
-// the first pass.  perm: the token -> x row map of a MUL_MAT_ID group (or
-// nullptr: row n).
+// the first pass.  perm: the token -> x row map of a routed MUL_MAT_ID group
+// (or nullptr: row row0 + n).
 template <int F, int kStageK>
-__device__ __noinline__ void stage_x_scaled(const float* __restrict__ X, int K, const int* perm, int kc0, int kend,
+__device__ __noinline__ void stage_x_scaled(const float* __restrict__ X, int K, const int* perm, int row0, int kc0,
+                                            int kend,
                                             int nst, int N, int Nt, int kw, int lane, uint4* xs, float* cs,
                                             float* sxs, int csn, float* wsc) {
   constexpr int kBoxBlocks = kSubK / kQK;
-  auto xrow = [&](int n) -> size_t { return perm ? static_cast<size_t>(__ldg(perm + n)) : static_cast<size_t>(n); };
+  auto xrow = [&](int n) -> size_t {
+    return perm ? static_cast<size_t>(__ldg(perm + n)) : static_cast<size_t>(row0 + n);
+  };
   for (int n = lane; n < Nt; n += 32) {
     float m = 0.f;
     for (int st = 0; st < nst; ++st)
@@ -324,9 +327,14 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
   // Groups of this CTA: gk = 0 .. ngrp-1 is group g_first + gk * g_step, and
   // within it tiles t_first, t_first + t_step, ...
   int ngrp = 1, g_first = 0, g_step = 1, t_first = static_cast<int>(blockIdx.x), t_step = static_cast<int>(gridDim.x);
+  // Group g: its expert (direct groups -- single-token launches only: pair g
+  // alone, its id read here; an id outside [0, ne) marks the group bad).
+  const bool direct = MOE && ONE && rt.ids != nullptr;
+  auto grp_expert = [&](int g) -> int { return direct ? __ldg(rt.ids + g) : rt.groups[3 * g]; };
+  auto grp_bad = [&](int e) -> bool { return direct && (e < 0 || e >= rt.ne); };
   if (MOE) {
-    pdl_wait();  // the routing tables come from the kernel before
-    const int ng = rt.meta[1], grid = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+    pdl_wait();  // the routing tables (or the ids) come from the kernel before
+    const int ng = direct ? rt.np : rt.meta[1], grid = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
     if (ng <= grid) {
       const int cpg = ng > 0 ? grid / ng : 1;
       g_first = b / cpg;
@@ -368,7 +376,9 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
       bool ok = true;
       for (int gk = 0; gk < ngrp && ok; ++gk)
       for (int c = 0; c < nchunks && ok; ++c) {
-        const int wrow0 = MOE ? rt.groups[3 * (g_first + gk * g_step)] * M : 0;
+        const int ge = MOE ? grp_expert(g_first + gk * g_step) : 0;
+        if (MOE && grp_bad(ge)) continue;  // the consumers skip it too
+        const int wrow0 = ge * M;
         const int kc0 = c * KX;
         const int kend = min(K, kc0 + KX);
         const int nst = min(stages_per_chunk, (kend - kc0 + Cfg::kStageK - 1) / Cfg::kStageK);
@@ -430,11 +440,29 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
     // row is xrow(n).
     int Nt = N, first = 0;
     if (MOE) {
-      const int* grp = rt.groups + 3 * (g_first + gk * g_step);
-      first = grp[1];
-      Nt = grp[2];
+      const int g = g_first + gk * g_step;
+      if (direct) {
+        first = g;
+        Nt = 1;
+        if (grp_bad(grp_expert(g))) {
+          // A bad id: this CTA's rows of the pair's Y row become NaN.
+          if (c == 0 && kw == 0) {
+            for (int tile = t_first; tile < ntiles; tile += t_step)
+              for (int r = lane; r < kBM; r += 32)
+                if (tile * kBM + r < M) Y[static_cast<size_t>(g) * M + tile * kBM + r] = __int_as_float(0x7FC00000);
+            if (lane == 0) atomicOr(err, DEVERR_BAD_ID);
+          }
+          continue;
+        }
+      } else {
+        const int* grp = rt.groups + 3 * g;
+        first = grp[1];
+        Nt = grp[2];
+      }
     }
-    auto xrow = [&](int n) -> size_t { return MOE ? static_cast<size_t>(__ldg(rt.perm + first + n)) : n; };
+    auto xrow = [&](int n) -> size_t {
+      return MOE ? (direct ? static_cast<size_t>(first + n) : static_cast<size_t>(__ldg(rt.perm + first + n))) : n;
+    };
     const int kc0 = c * KX;
     const int kend = min(K, kc0 + KX);
     const int nst = min(stages_per_chunk, (kend - kc0 + Cfg::kStageK - 1) / Cfg::kStageK);
@@ -484,8 +512,8 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
     }
     const bool xwide = __any_sync(0xFFFFFFFFu, lmax >= kXScaleFrom);
     if (xwide)
-      stage_x_scaled<F, Cfg::kStageK>(X, K, MOE ? rt.perm + first : nullptr, kc0, kend, nst, N, Nt, kw, lane, xs,
-                                      cs, sxs, csn, xsc + kw * N);
+      stage_x_scaled<F, Cfg::kStageK>(X, K, (MOE && !direct) ? rt.perm + first : nullptr, MOE ? first : 0, kc0,
+                                      kend, nst, N, Nt, kw, lane, xs, cs, sxs, csn, xsc + kw * N);
     __syncwarp();
     if (gk == 0 && c == 0 && lane == 0) mbar_arrive(smem_u32(x_ready));
 

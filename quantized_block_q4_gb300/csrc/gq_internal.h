@@ -89,6 +89,11 @@ struct MoeRoute {
   int32_t* item_start;  // [E + 1]: first tensor-core work item (expert, row tile, token tile) of expert e
   int32_t* groups;      // [3 * max groups]: decode group = (expert, first sorted position, tokens <= cap)
   int32_t* perm;        // [P]: sorted position -> pair index t * S + s (stable within an expert)
+  // Direct decode groups (no routing tables; the decode kernel only): when
+  // ids is set, group g is pair g alone, with expert ids[g] (np groups of one
+  // token; an id outside [0, ne) gives a NaN row and DEVERR_BAD_ID).
+  const int32_t* ids;
+  int32_t np, ne;
 };
 size_t moe_route_ints(int64_t E, int64_t P, int cap);
 MoeRoute moe_route_layout(int32_t* base, int64_t E, int64_t P, int cap);

@@ -256,7 +256,7 @@ size_t moe_route_ints(int64_t E, int64_t P, int cap) {
 
 MoeRoute moe_route_layout(int32_t* base, int64_t E, int64_t P, int cap) {
   const int64_t max_groups = std::min(E, P) + P / std::max(cap, 1) + 1;
-  MoeRoute rt;
+  MoeRoute rt{};  // ids = nullptr: routed groups
   rt.meta = base;
   rt.off = rt.meta + 4;
   rt.item_start = rt.off + (E + 2);

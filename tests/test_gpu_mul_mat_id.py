@@ -198,3 +198,31 @@ def test_single_token_repeated_expert(path):
 
 def test_single_token_many_slots():
     check(64, 512, 2048, 1, 8, seed=12960, path=DECODE)
+
+
+def test_single_token_bad_ids_direct_groups():
+    """A single token reads its ids in the decode kernel itself (no routing
+    kernel): out-of-range slots give NaN rows and GQ_ERR_BAD_INDEX, the
+    others match the oracle."""
+    E, M, K, T, S = 8, 700, 1024, 1, 5
+    W = synth.moe_weights(E, M, K, 12970)
+    X = synth.activations(T * S, K, 12971).reshape(T, S, K)
+    ids = np.array([[3, E, -1, 5, 3]], dtype=np.int32)
+    with _path(DECODE):
+        y = gq.mul_mat_id_q4_0(dev(W), E, dev(X), dev(ids))
+        with pytest.raises(gq.GQError) as e:
+            gq.gq_sync_status()
+    assert e.value.status == gq.GQ_ERR_BAD_INDEX
+    gq.gq_sync_status()  # cleared
+    y = y.cpu().numpy()
+    y_ref, s_ref = oracle.get().mul_mat_id(W, E, M, K, X, ids, nthreads=cores())
+    bad = np.isnan(y_ref).all(axis=-1)
+    assert bad.sum() == 2 and bad[0, 1] and bad[0, 2]
+    assert np.isnan(y[bad]).all(), "rows of bad ids must be NaN"
+    assert_mul_mat_close(y[~bad], y_ref[~bad], s_ref[~bad], "single token, good slots")
+
+
+@pytest.mark.parametrize("path", [AUTO, DECODE])
+def test_single_token_full_size_experts(path):
+    """1 token x 2 slots on full-size experts (the single-token decode case)."""
+    check(8, 14336, 4096, 1, 2, seed=12980, path=path)
