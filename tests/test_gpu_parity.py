@@ -249,6 +249,12 @@ def test_prefill_n_tiles(N):
     check_mm(384, 1024, N, 5000 + N)
 
 
+@pytest.mark.parametrize("M,K,N", [(256, 1024, 2048), (130, 512, 4099)])
+def test_prefill_many_token_tiles(M, K, N):
+    """Long batches: 8 and 17 token tiles of 256 (the last one ragged) per row tile."""
+    check_mm(M, K, N, 5100 + N)
+
+
 @pytest.mark.parametrize("opt,val", [("GQ_OPT_PREFILL_PAIR", 1), ("GQ_OPT_PREFILL_TILE_N", 128)])
 @pytest.mark.parametrize("M,N", [(384, 129), (384, 300), (640, 513), (130, 257)])
 def test_prefill_kernel_options(opt, val, M, N):
