@@ -518,7 +518,8 @@ def run_moe_aux(gq, torch, dev, s, peaks):
     """gq_mul_mat_id_q4_0 on MOE_SETS distinct expert sets (264 MB each), used in
     turn so that every call streams its experts from DRAM; CUDA events on the
     bench stream around MOE_REPS calls.  Each call = routing + (gather +
-    tensor-core | decode) kernels."""
+    tensor-core | decode) kernels; a single token runs the decode kernel
+    alone, reading the ids itself."""
     E, M, K, S = MOE_E, MOE_M, MOE_K, MOE_S
     Ws = [moe_weights_dev(torch, dev, E * M, K, 0x3E00 + i) for i in range(MOE_SETS)]
     out = {}
