@@ -1,5 +1,5 @@
-// K2: decode / small-N MUL_MAT against Q4_0 weights, plus the generic
-// fallback kernel.
+// K2: decode / small-N MUL_MAT against Q4_0 (and Q4_1 / Q8_0) weights, plus
+// the generic fallback kernel.
 //
 // Y[n][m] = sum_k w[m][k] * X[n][k],  w = d*(q-8)  ("Binding GGUF weights to
 // the compute graph", section 2.3: blocks are dequantised inside MUL_MAT;
@@ -32,7 +32,12 @@
 //    the previous kernel on the stream drains; X is read and Y written only
 //    after griddepcontrol.wait.  With `early_w` set, the producer also starts
 //    streaming W before that wait (valid when the previous kernel does not
-//    write W, as in weight-stationary inference).
+//    write W, as in weight-stationary inference); with `x_static` X is read
+//    and the MMAs run before it too, and only the warp writing Y waits.
+//  * The same kernel serves Q4_1 and Q8_0 blocks (F: 20- and 34-byte blocks,
+//    their own code extraction and bias) and MUL_MAT_ID (MOE: groups of
+//    routed tokens of one expert; a single token's slots read their expert
+//    ids directly).
 #include <algorithm>
 #include <type_traits>
 #include <cuda_fp16.h>
