@@ -32,6 +32,10 @@
 // fma.rn.bf16x2(q', d_hi, q'*d_lo) rounds d*(q-8) once.
 // Every wait is bounded; a timeout sets the device error word, the roles
 // drain what they issued, TMEM is released and the CTA exits.
+// Launched with programmatic dependent launch (K0 too): the next launch's
+// CTAs take each SM as this one's CTA there leaves, and every role waits for
+// the kernel before ahead of its first global access (W may stream a few
+// chunks early when the caller promises the weights are not being written).
 #include <algorithm>
 #include <atomic>
 #include <random>
