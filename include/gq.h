@@ -26,9 +26,11 @@
  *  - M or N equal to 0 is a no-op that returns GQ_OK; K equal to 0 (an empty
  *    sum) writes zeros to Y.
  *  - Non-finite scales or activations propagate as IEEE arithmetic does; they
- *    are not validated.
- *  - No C++ exception crosses this interface.  Thread-safe for calls on
- *    different streams; gq_last_error() is per thread.
+ *    are not validated on the MUL_MAT path (gq_validate checks the scales).
+ *  - No C++ exception crosses this interface.  Calls on different streams may
+ *    run concurrently; gq_last_error() is per thread.  A process drives one
+ *    device: the kernels' shared-memory attributes are set once per process,
+ *    so a call on a second device can fail with GQ_ERR_CUDA.
  */
 #ifndef GQ_H
 #define GQ_H
