@@ -132,9 +132,12 @@ gq_status gq_mul_mat(gq_type type, const void *W, int64_t M, int64_t K, const fl
                      void *stream);
 
 /* Y[N][M] = X[N][K] * W^T with W in Q4_0, fp32 in and out (see header).
- * Dispatch by N: N < 16 streams W through the decode kernel (fp16 x, scaled
- * by an exact power of two where |x| reaches 2^15, so any finite x works; exact
- * integer codes, fp32 block scales and accumulation); N >= 16 converts X to
+ * Dispatch by N: N < 16 streams W through the decode kernel (fp16 x; where a
+ * token's largest |x| in a warp's chunk of K (256 to a few thousand elements)
+ * reaches 2^15 or stays below 2^-10 that chunk is staged times the exact power
+ * of two that brings it into [2^14, 2^15), so that the token's largest values
+ * keep fp16's 11 significant bits at any finite magnitude; exact integer
+ * codes, fp32 block scales and accumulation); N >= 16 converts X to
  * bf16 once and runs the tcgen05 tensor-core kernel on bf16 tiles of the
  * dequantised W with fp32 accumulation (GQ_OPT_PREFILL_MIN_N moves the
  * threshold).  Fast paths need K % 256 == 0 and W, X, Y 16-byte aligned; other

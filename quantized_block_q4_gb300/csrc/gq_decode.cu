@@ -18,8 +18,9 @@
 //    the MMA's C input with a minus sign, so each block's MMA pair yields
 //    sum (q-8)*x directly.  The block scale d is then applied in fp32 to that
 //    partial, so W is never rounded; only x is (fp16, relative <= 2^-11;
-//    a token with |x| >= 2^15 in a warp's blocks is staged times an exact
-//    power of two and the warp's partial sums are multiplied back).
+//    a token whose largest |x| in a warp's blocks reaches 2^15 or stays below
+//    2^-10 is staged times an exact power of two and the warp's partial sums
+//    are multiplied back).
 //  * The four bytes of codes a lane needs are read straight from the raw
 //    18-byte blocks: two blocks (36 bytes) form nine aligned 32-bit words, and
 //    one PRMT rebuilds the word that straddles the scale of the even block.
@@ -87,15 +88,21 @@ struct DecodeCfg {
   }
 };
 
-// x is staged as fp16.  A warp's chunk of a token whose largest |x| is m >=
-// 2^15 is staged as x * 2^-e, the smallest such factor that brings m below
-// 2^15 (and x/16 with it); 1 otherwise, and for non-finite m (which then
-// propagates as it would unscaled).
-constexpr float kXScaleFrom = 32768.f;
-__device__ __forceinline__ float x_scale_down(float m) {
-  if (!(m >= kXScaleFrom) || !isfinite(m)) return 1.f;
-  const int E = ((__float_as_int(m) >> 23) & 0xFF) - 127;  // m in [2^E, 2^(E+1)), E >= 15
-  return __int_as_float((127 - (E - 14)) << 23);            // m * 2^-(E-14) in [2^14, 2^15)
+// x is staged as fp16 (x for the low nibbles, x/16 for the high ones).  A
+// warp's chunk of a token whose largest |x| is m >= 2^15 would overflow fp16,
+// and one whose m is below 2^-10 would leave the normal fp16 range (m/16 <
+// 2^-14, where fp16 keeps fewer than 11 significant bits); such a chunk is
+// staged as x * 2^e with the power of two that brings m into [2^14, 2^15)
+// (clamped so that 2^e and 2^-e are normal fp32 numbers).  Any other chunk,
+// and one whose m is 0 or non-finite (which then propagates as it would
+// unscaled), keeps the factor 1.
+constexpr float kXScaleFrom = 32768.f;          // 2^15
+constexpr float kXScaleBelow = 0.0009765625f;   // 2^-10
+__device__ __forceinline__ float x_scale(float m) {
+  if (!(m >= kXScaleFrom || (m > 0.f && m < kXScaleBelow)) || !isfinite(m)) return 1.f;
+  const int E = ((__float_as_int(m) >> 23) & 0xFF) - 127;  // m in [2^E, 2^(E+1)) (subnormal m: E = -127)
+  const int e = max(-126, min(126, 14 - E));
+  return __int_as_float((e + 127) << 23);                   // m * 2^e in [2^14, 2^15)
 }
 // 1/f for f a normal power of two, exactly (the exponent reflected about 0).
 __device__ __forceinline__ float pow2_inverse(float f) { return __int_as_float((254 << 23) - __float_as_int(f)); }
@@ -247,7 +254,7 @@ __device__ __forceinline__ void stage_entry(const float (&xv)[32], uint4* dst, f
 }
 
 // The x staging's rare path (out of line): per token, the largest |x| over
-// this warp's blocks of the chunk, its factor wsc[n] (x_scale_down), and the
+// this warp's blocks of the chunk, its factor wsc[n] (x_scale), and the
 // chunk's entries staged again as x * wsc[n].  Blocks past K were zeroed by
 // the first pass.  perm: the token -> x row map of a routed MUL_MAT_ID group
 // (or nullptr: row row0 + n).
@@ -272,7 +279,7 @@ __device__ __noinline__ void stage_x_scaled(const float* __restrict__ X, int K, 
           m = fmaxf(fmaxf(m, fmaxf(fabsf(v.x), fabsf(v.y))), fmaxf(fabsf(v.z), fabsf(v.w)));
         }
       }
-    wsc[n] = x_scale_down(m);
+    wsc[n] = x_scale(m);
   }
   __syncwarp();
   const int nent = nst * kBoxBlocks * Nt;
@@ -478,14 +485,17 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
     // Each warp stages only the blocks of its own k boxes (box kw of every
     // stage), which only it reads: no CTA-wide barrier, so a warp starts on
     // its W as soon as its own x has arrived.
-    // fp16 holds |x| < 65520.  A token whose x in this warp's blocks reaches
-    // 2^15 is staged again as x * 2^-e (exact), with 2^-e taking its largest
-    // |x| below 2^15, and the warp's partial sums for it are multiplied by 2^e
-    // (exact); every other token keeps the factor 1.
+    // fp16 holds |x| < 65520 with 11 significant bits from 2^-14 on.  A token
+    // whose largest |x| in this warp's blocks reaches 2^15, or stays below
+    // 2^-10, is staged again as x * 2^e (exact; x_scale), and the warp's
+    // partial sums for it are multiplied by 2^-e (exact); every other token
+    // keeps the factor 1.  A lane notes the largest |x| it staged and whether
+    // some block it staged was small but not all zero.
     __syncwarp();  // this warp's previous chunk of fragments is no longer read
     constexpr int kBoxBlocks = kSubK / kQK;  // 8
     const int nent = nst * kBoxBlocks * Nt;  // (stage, block of the box, token) entries of this warp
     float lmax = 0.f;                        // largest |x| this lane staged
+    bool lsmall = false;                     // some staged block's largest |x| is in (0, 2^-10)
     for (int e = lane; e < nent; e += 32) {
       const int st = e / (kBoxBlocks * Nt), rem = e % (kBoxBlocks * Nt);
       const int bl = st * (Cfg::kStageK / kQK) + kw * kBoxBlocks + rem / Nt;  // block within the chunk
@@ -507,15 +517,18 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
       float xv[32];
       const float4* xr =
           reinterpret_cast<const float4*>(X + xrow(n) * K + static_cast<size_t>(kc0 + bl * kQK));
+      float em = 0.f;  // this block's largest |x|
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float4 v = __ldg(xr + i);
         xv[4 * i] = v.x; xv[4 * i + 1] = v.y; xv[4 * i + 2] = v.z; xv[4 * i + 3] = v.w;
-        lmax = fmaxf(fmaxf(lmax, fmaxf(fabsf(v.x), fabsf(v.y))), fmaxf(fabsf(v.z), fabsf(v.w)));
+        em = fmaxf(fmaxf(em, fmaxf(fabsf(v.x), fabsf(v.y))), fmaxf(fabsf(v.z), fabsf(v.w)));
       }
+      lmax = fmaxf(lmax, em);
+      lsmall |= em > 0.f && em < kXScaleBelow;
       stage_entry<F>(xv, xs + (bl * N + n) * 4, cs + bl * csn, sxs + bl * csn, n, Nt, (kc0 / kQK + bl) & 1);
     }
-    const bool xwide = __any_sync(0xFFFFFFFFu, lmax >= kXScaleFrom);
+    const bool xwide = __any_sync(0xFFFFFFFFu, lmax >= kXScaleFrom || lsmall);
     if (xwide)
       stage_x_scaled<F, Cfg::kStageK>(X, K, (MOE && !direct) ? rt.perm + first : nullptr, MOE ? first : 0, kc0,
                                       kend, nst, N, Nt, kw, lane, xs, cs, sxs, csn, xsc + kw * N);

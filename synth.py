@@ -58,18 +58,19 @@ def random_scales(seed: int, n: int, lo: float = 0.005, hi: float = 0.02) -> np.
     return u.astype("<f2")
 
 
-def q4_0_weights(M: int, K: int, seed: int) -> np.ndarray:
+def q4_0_weights(M: int, K: int, seed: int, d_range=(0.005, 0.02)) -> np.ndarray:
     """A Q4_0 weight matrix with M rows of K weights, as raw bytes.
 
     Shape ``[M, K/32*18]`` uint8: row m is K/32 consecutive 18-byte blocks, each
-    the little-endian fp16 scale followed by 16 bytes of packed codes.
+    the little-endian fp16 scale (RNE of U[d_range] drawn in fp64) followed by
+    16 bytes of packed codes.
     """
     if K % QK4_0:
         raise ValueError("K must be a multiple of 32")
     nb = K // QK4_0
     out = np.empty((M, nb, BLOCK_BYTES), dtype=np.uint8)
     out[:, :, 2:] = random_bytes(seed, M * nb * 16).reshape(M, nb, 16)
-    out[:, :, 0:2] = random_scales(seed, M * nb).view(np.uint8).reshape(M, nb, 2)
+    out[:, :, 0:2] = random_scales(seed, M * nb, *d_range).view(np.uint8).reshape(M, nb, 2)
     return out.reshape(M, nb * BLOCK_BYTES)
 
 
@@ -113,26 +114,27 @@ def moe_weights(E: int, M: int, K: int, seed: int) -> np.ndarray:
     return np.concatenate([q4_0_weights(M, K, seed + 7919 * e) for e in range(E)], axis=0)
 
 
-def typed_weights(qtype: int, M: int, K: int, seed: int) -> np.ndarray:
+def typed_weights(qtype: int, M: int, K: int, seed: int, d_scale: float = 1.0) -> np.ndarray:
     """Weights in one of the legacy block formats, as raw bytes [M, K/32*bytes]:
     0 = Q4_0 (q4_0_weights), 1 = Q4_1 (fp16 d ~ U[0.005, 0.02], fp16 m ~
     U[-0.16, 0], 16 random code bytes), 2 = Q8_0 (fp16 d ~ U[0.0003, 0.0012],
-    32 random int8 code bytes).  Scales are RNE fp16 of values drawn in fp64."""
+    32 random int8 code bytes).  Scales are RNE fp16 of values drawn in fp64;
+    d_scale multiplies the ranges of d and m (e.g. 100 for O(1) weights)."""
     if qtype == 0:
-        return q4_0_weights(M, K, seed)
+        return q4_0_weights(M, K, seed, (0.005 * d_scale, 0.02 * d_scale))
     if K % QK4_0:
         raise ValueError("K must be a multiple of 32")
     nb = K // QK4_0
     if qtype == 1:
         out = np.empty((M, nb, 20), dtype=np.uint8)
         out[:, :, 4:] = random_bytes(seed, M * nb * 16).reshape(M, nb, 16)
-        out[:, :, 0:2] = random_scales(seed, M * nb).view(np.uint8).reshape(M, nb, 2)
-        out[:, :, 2:4] = random_scales(seed ^ 0x3117, M * nb, -0.16, 0.0).view(np.uint8).reshape(M, nb, 2)
+        out[:, :, 0:2] = random_scales(seed, M * nb, 0.005 * d_scale, 0.02 * d_scale).view(np.uint8).reshape(M, nb, 2)
+        out[:, :, 2:4] = random_scales(seed ^ 0x3117, M * nb, -0.16 * d_scale, 0.0).view(np.uint8).reshape(M, nb, 2)
         return out.reshape(M, nb * 20)
     if qtype == 2:
         out = np.empty((M, nb, 34), dtype=np.uint8)
         out[:, :, 2:] = random_bytes(seed, M * nb * 32).reshape(M, nb, 32)
-        out[:, :, 0:2] = random_scales(seed, M * nb, 0.0003, 0.0012).view(np.uint8).reshape(M, nb, 2)
+        out[:, :, 0:2] = random_scales(seed, M * nb, 0.0003 * d_scale, 0.0012 * d_scale).view(np.uint8).reshape(M, nb, 2)
         return out.reshape(M, nb * 34)
     raise ValueError("unknown block type")
 
