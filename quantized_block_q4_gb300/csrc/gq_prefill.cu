@@ -126,6 +126,14 @@ struct PrefillCfg {
   static constexpr int RS = F == GQ_TYPE_Q8_0 ? 2 : 3;
   static constexpr int S = PAIR ? 8 : (BN == 256 ? (F == GQ_TYPE_Q4_0 ? 5 : 4) : 8);
   static_assert(BN + S * kACols <= 512, "TMEM holds the accumulator and the A stages");
+  // Step c of the ring goes to stage c mod S and is written by dequant group
+  // c mod 4, which waits on the stage's "empty" barrier by phase parity.  With
+  // S >= 4 that group's own previous step (c - 4) already needed the MMA of
+  // step c - 4 - S, and MMAs complete in order, so the barrier is at most one
+  // phase behind and the parity is unambiguous.  With fewer stages than
+  // groups it can be two phases behind: the wait passes early and the group
+  // overwrites an A stage that an MMA still reads.
+  static_assert(S >= 4, "an A/x stage ring shorter than the four dequant groups lets a parity wait pass early");
   static constexpr int kTmemCols = 512;
   static constexpr int kRawBytes = kBM * kRawRow;  // 18432 for Q4_0
   // 16-byte words a dequantising thread loads to cover its two blocks
