@@ -28,9 +28,9 @@
  *  - Non-finite scales or activations propagate as IEEE arithmetic does; they
  *    are not validated on the MUL_MAT path (gq_validate checks the scales).
  *  - No C++ exception crosses this interface.  Calls on different streams may
- *    run concurrently; gq_last_error() is per thread.  A process drives one
- *    device: the kernels' shared-memory attributes are set once per process,
- *    so a call on a second device can fail with GQ_ERR_CUDA.
+ *    run concurrently, and host threads may call in parallel, each on its own
+ *    current device: the library sets its kernels' launch attributes once per
+ *    (kernel, device) under a lock.  gq_last_error() is per thread.
  */
 #ifndef GQ_H
 #define GQ_H
@@ -218,10 +218,11 @@ gq_status gq_mul_mat_q4_0_bf16x(const void *W, int64_t M, int64_t K, const uint1
  * own the whole device, fixed arenas, allocation-free hot loops).
  *  - Needs K % 256 == 0 and N*K <= 6291456 (GQ_ERR_SHAPE otherwise), W 16-byte
  *    aligned, X and Y 4-byte aligned.
- *  - Every GPU that loads the library holds the 12 MiB array until the
- *    process exits.  The first call on a device looks up the array's device
- *    address (cudaGetSymbolAddress) with that device current; make that first
- *    call before any stream capture.
+ *  - The 12 MiB array is reserved on each device where the library's kernels
+ *    are first loaded and stays until that device's context is destroyed.
+ *    The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.  A device reset after it is not supported.
  *  - All calls share the array: calls whose GPU work overlaps race on it. */
 gq_status gq_mul_mat_q4_0_noalloc(const void *W, int64_t M, int64_t K, const float *X, int64_t N, float *Y,
                                   void *stream);
@@ -268,8 +269,14 @@ typedef enum {
                                 projections of one activation), so the kernel may read X and compute
                                 before that kernel finishes; Y is still written only after it.
                                 Default 0: X is read after the previous kernel completes */
-  GQ_OPT_MOE_PATH = 12        /* gq_mul_mat_id_q4_0 kernel: 0 (default) by tokens per used expert,
+  GQ_OPT_MOE_PATH = 12,       /* gq_mul_mat_id_q4_0 kernel: 0 (default) by tokens per used expert,
                                 1 decode kernel, 2 tensor-core kernel (fast-path shapes only) */
+  GQ_OPT_TEST_DROP_ARRIVE = 13 /* test aid for the timeout path, 0 (default) off: 1 = the decode kernel's
+                                W producer in CTA 0 never issues its second ring stage, 2 = the
+                                tensor-core kernel's W producer in CTA 0 never issues its second raw
+                                chunk.  The stage's consumers then wait out GQ_OPT_WAIT_LIMIT_NS, the
+                                kernel drains what it issued, releases tensor memory and returns, and
+                                gq_sync_status() reports GQ_ERR_DEVICE_TIMEOUT.  Nothing faults. */
 } gq_option;
 gq_status gq_set_option(gq_option opt, int64_t value);
 int64_t gq_get_option(gq_option opt);

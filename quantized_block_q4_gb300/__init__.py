@@ -45,6 +45,7 @@ GQ_OPT_PREFILL_SLOTS = 9
 GQ_OPT_DECODE_EARLY_STAGES = 10
 GQ_OPT_X_STATIC = 11
 GQ_OPT_MOE_PATH = 12
+GQ_OPT_TEST_DROP_ARRIVE = 13
 
 # Every symbol include/gq.h declares, with (restype, argtypes).
 _i64, _sz, _vp, _i32 = ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int

@@ -6,8 +6,10 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <string>
+#include <tuple>
 
 #include "gq.h"
 #include "gq_internal.h"
@@ -29,6 +31,7 @@ std::atomic<int64_t> g_early_w{0};
 std::atomic<int64_t> g_decode_variant{0};
 std::atomic<int64_t> g_pdl{1};
 std::atomic<int64_t> g_moe_path{0};
+std::atomic<int64_t> g_test_drop{0};
 
 gq_status fail(gq_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 gq_status fail(gq_status st, const char* fmt, ...) {
@@ -107,27 +110,34 @@ gq_status check_mm_shape(int64_t M, int64_t K, int64_t N) {
 }  // namespace
 
 uint32_t* device_error_word() {
-  static uint32_t* ptrs[kMaxDevices] = {};
+  static std::atomic<uint32_t*> ptrs[kMaxDevices] = {};
+  static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (!ptrs[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_dev_error) != cudaSuccess) return nullptr;
-    ptrs[dev] = static_cast<uint32_t*>(p);
+  uint32_t* p = ptrs[dev].load(std::memory_order_acquire);
+  if (!p) {
+    std::lock_guard<std::mutex> lk(mu);
+    p = ptrs[dev].load(std::memory_order_relaxed);
+    if (!p) {
+      void* a = nullptr;
+      if (cudaGetSymbolAddress(&a, g_dev_error) != cudaSuccess) return nullptr;
+      p = static_cast<uint32_t*>(a);
+      ptrs[dev].store(p, std::memory_order_release);
+    }
   }
-  return ptrs[dev];
+  return p;
 }
 
 const DeviceInfo& device_info() {
   static DeviceInfo infos[kMaxDevices];
+  static std::atomic<bool> ready[kMaxDevices] = {};
   static std::mutex mu;
-  static DeviceInfo none;
+  static const DeviceInfo none;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return none;
-  DeviceInfo& di = infos[dev];
-  if (di.device < 0) {
+  if (!ready[dev].load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lk(mu);
-    if (di.device < 0) {
+    if (!ready[dev].load(std::memory_order_relaxed)) {
       DeviceInfo d;
       int v = 0;
       cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
@@ -137,10 +147,50 @@ const DeviceInfo& device_info() {
       cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
       d.smem_optin = static_cast<size_t>(v);
       d.device = dev;
-      di = d;
+      infos[dev] = d;
+      ready[dev].store(true, std::memory_order_release);
     }
   }
-  return di;
+  return infos[dev];
+}
+
+namespace {
+std::mutex g_attr_mu;
+std::map<std::pair<const void*, int>, size_t> g_smem_set;                    // (kernel, device) -> bytes
+std::map<std::tuple<const void*, int, int, size_t>, int> g_occupancy;        // (kernel, device, threads, smem)
+}  // namespace
+
+cudaError_t kernel_smem(const void* kernel, size_t bytes, bool max_shared) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  size_t& have = g_smem_set[{kernel, dev}];
+  if (bytes <= have && (have > 0 || !max_shared)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e != cudaSuccess) return e;
+  if (max_shared) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
+  have = std::max(have, bytes);
+  return cudaSuccess;
+}
+
+cudaError_t kernel_occupancy(const void* kernel, int threads, size_t smem, int* blocks) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  auto it = g_occupancy.find({kernel, dev, threads, smem});
+  if (it == g_occupancy.end()) {
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, smem);
+    if (e != cudaSuccess) return e;
+    it = g_occupancy.emplace(std::make_tuple(kernel, dev, threads, smem), occ > 0 ? occ : 1).first;
+  }
+  *blocks = it->second;
+  return cudaSuccess;
 }
 
 // Stream-ordered scratch from a pool the library owns (one per device), which
@@ -221,6 +271,8 @@ static gq_status mul_mat_prefill_bf16(const void* W, int64_t M, int64_t K, const
 
 namespace gq {
 gq_status api_fail(gq_status st, const char* msg) { return fail(st, "%s", msg); }
+int test_drop() { return static_cast<int>(g_test_drop.load()); }
+void api_clear_error() { t_last_error.clear(); }
 gq_status api_check_device() { return check_device(); }
 int api_pdl() { return static_cast<int>(g_pdl.load()); }
 gq_status api_check_mm_shape(int64_t M, int64_t K, int64_t N) { return check_mm_shape(M, K, N); }
@@ -674,6 +726,10 @@ gq_status gq_set_option(gq_option opt, int64_t value) {
       if (value < 0 || value > 2) return fail(GQ_ERR_SHAPE, "MUL_MAT_ID path must be 0, 1 or 2");
       g_moe_path = value;
       return GQ_OK;
+    case GQ_OPT_TEST_DROP_ARRIVE:
+      if (value < 0 || value > 2) return fail(GQ_ERR_SHAPE, "test drop must be 0 (off), 1 (decode) or 2 (tensor core)");
+      g_test_drop = value;
+      return GQ_OK;
   }
   return fail(GQ_ERR_SHAPE, "unknown option %d", static_cast<int>(opt));
 }
@@ -693,6 +749,7 @@ int64_t gq_get_option(gq_option opt) {
     case GQ_OPT_DECODE_EARLY_STAGES: return get_decode_early_stages();
     case GQ_OPT_X_STATIC: return get_decode_x_static();
     case GQ_OPT_MOE_PATH: return g_moe_path.load();
+    case GQ_OPT_TEST_DROP_ARRIVE: return g_test_drop.load();
   }
   return -1;
 }

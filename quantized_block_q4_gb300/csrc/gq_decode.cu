@@ -312,7 +312,7 @@ template <int NT, int MT, int KW, int STAGES, bool ONE, bool MOE = false, int F 
 __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, STAGES, F>()))
     k_decode_q4_0(const __grid_constant__ CUtensorMap tmW, const float* __restrict__ X, int N, int M, int K,
                   int KX, float* __restrict__ Y, uint64_t limit_ns, uint32_t* err, int early_stages,
-                  int x_static, const MoeRoute rt) {
+                  int x_static, const MoeRoute rt, int drop) {
   static_assert(F == GQ_TYPE_Q4_0 || !MOE, "Q4_1 / Q8_0 run the plain MUL_MAT layout");
   using Cfg = DecodeCfg<NT, MT, KW, STAGES, F>;
   constexpr int kBM = Cfg::kBM;
@@ -409,6 +409,9 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
               ok = false;
               break;
             }
+            // test hook: stage 1 of CTA 0 is never issued, so its consumers'
+            // bounded wait runs out (GQ_OPT_TEST_DROP_ARRIVE)
+            if (drop && blockIdx.x == 0 && q == 1) continue;
             const int k0 = kc0 + st * Cfg::kStageK;
             const int nvalid = min(KW, (kend - k0 + kSubK - 1) / kSubK);
             const uint32_t full = smem_u32(&bars[slot]);
@@ -768,22 +771,11 @@ cudaError_t launch_cfg(const CUtensorMap* tmW, const float* X, int N, int M, int
   if (KX > Kpad) KX = Kpad;
   const size_t smem = Cfg::smem_bytes(N, KX);
   auto kern = k_decode_q4_0<NT, MT, KW, STAGES, ONE, MOE, F>;
-  static int configured_smem = 0;
-  static int occ_cache_smem = -1, occ_cache = 1;
-  if (static_cast<int>(smem) > configured_smem) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    configured_smem = static_cast<int>(smem);
-  }
-  if (occ_cache_smem != static_cast<int>(smem)) {
-    int occ = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, Cfg::kThreads, smem);
-    if (e != cudaSuccess) return e;
-    occ_cache = occ > 0 ? occ : 1;
-    occ_cache_smem = static_cast<int>(smem);
-  }
+  cudaError_t e = kernel_smem(reinterpret_cast<const void*>(kern), smem, true);
+  if (e != cudaSuccess) return e;
+  int occ_cache = 1;
+  e = kernel_occupancy(reinterpret_cast<const void*>(kern), Cfg::kThreads, smem, &occ_cache);
+  if (e != cudaSuccess) return e;
   const int ntiles = (M + Cfg::kBM - 1) / Cfg::kBM;
   // Small CTAs (two fit on an SM) run one per SM, so that the next launch's
   // CTA can share the SM and overlap this one.
@@ -801,7 +793,7 @@ cudaError_t launch_cfg(const CUtensorMap* tmW, const float* X, int N, int M, int
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, *tmW, X, N, M, K, KX, Y, limit_ns, device_error_word(), early_stages,
-                            MOE ? 0 : decode_x_static(), rt);
+                            MOE ? 0 : decode_x_static(), rt, test_drop() == 1 ? 1 : 0);
 }
 
 // -------------------------------------------------------------------------

@@ -24,6 +24,14 @@ struct DeviceInfo {
 };
 const DeviceInfo& device_info();  // current device, cached
 
+// Kernel launch attributes of the current device, set once per (kernel,
+// device) and cached; safe to call from several host threads at once.
+// Raise the kernel's dynamic shared-memory limit to at least `bytes` (and, with
+// max_shared, prefer all of the unified L1 / shared storage as shared memory).
+cudaError_t kernel_smem(const void* kernel, size_t bytes, bool max_shared);
+// Resident blocks per SM for `threads` threads and `smem` bytes (at least 1).
+cudaError_t kernel_occupancy(const void* kernel, int threads, size_t smem, int* blocks);
+
 // Stream-ordered scratch from the library's own per-device pool (gq_api.cu).
 cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t s);
 cudaError_t scratch_free(void* p, cudaStream_t s);
@@ -137,6 +145,10 @@ cudaError_t launch_prepare_q4_0(const uint8_t* W, int64_t M, int64_t K, int64_t 
 
 // ---- helpers of the C ABI (gq_api.cu) for entry points defined in other files
 gq_status api_fail(gq_status st, const char* msg);  // records the per-thread error text
+void api_clear_error();
+// GQ_OPT_TEST_DROP_ARRIVE: 1 = the decode kernel, 2 = the tensor-core kernel
+// leaves one W copy of CTA 0 unissued (its consumers' bounded wait runs out).
+int test_drop();                              // clears it (every entry point starts with this)
 gq_status api_check_device();
 int api_pdl();  // GQ_OPT_PDL
 gq_status api_check_mm_shape(int64_t M, int64_t K, int64_t N);

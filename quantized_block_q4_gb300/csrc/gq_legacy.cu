@@ -379,14 +379,10 @@ cudaError_t launch_mul_mat_t(const uint8_t* W, int64_t M, int64_t K, const float
   if (bulk_warps > 0) {
     auto kern = k_mul_mat_legacy_bulk<T>;
     const int smem = 2 * bulk_warps * rb;
-    static int configured = 0;
-    if (smem > configured) {
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-      if (e != cudaSuccess) return e;
-      configured = 200 * 1024;
-    }
+    cudaError_t e = kernel_smem(reinterpret_cast<const void*>(kern), 200 * 1024, false);
+    if (e != cudaSuccess) return e;
     int occ = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32 * bulk_warps, smem);
+    e = kernel_occupancy(reinterpret_cast<const void*>(kern), 32 * bulk_warps, smem, &occ);
     if (e != cudaSuccess) return e;
     const int64_t ctas = std::min<int64_t>((M + bulk_warps - 1) / bulk_warps,
                                            static_cast<int64_t>(device_info().sm_count) * std::max(occ, 1));

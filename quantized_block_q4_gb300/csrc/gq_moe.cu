@@ -273,12 +273,9 @@ cudaError_t launch_moe_route(const int32_t* ids, int64_t P, int64_t E, int64_t n
   // few pairs needs one warp and no cross-warp work.
   const int nw = std::max(1, std::min(route_warps(static_cast<int>(E)), static_cast<int>((P + 63) / 64)));
   const size_t smem = (static_cast<size_t>(nw) + 1) * static_cast<size_t>(E + 1) * sizeof(int);
-  static size_t configured = 48 * 1024;
-  if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_moe_route, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  if (smem > 48 * 1024) {
+    cudaError_t e = kernel_smem(reinterpret_cast<const void*>(k_moe_route), smem, false);
     if (e != cudaSuccess) return e;
-    configured = smem;
   }
   // With programmatic dependent launch the routing CTA starts while the
   // previous kernel drains; it reads ids only after griddepcontrol.wait.

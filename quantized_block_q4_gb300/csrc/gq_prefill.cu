@@ -174,6 +174,7 @@ struct PrefillWork {
   unsigned long long* count;  // per split tile and CTA of a pair: (epoch << 8) | pieces published
   unsigned long long epoch;   // this launch's tag (< 2^56): a counter with another tag reads as 0
   int early_w;    // W is not written by the kernels before: its first chunks may stream before the PDL wait
+  int drop;       // test hook (GQ_OPT_TEST_DROP_ARRIVE): raw chunk 1 of CTA 0 is never issued
 };
 
 // Arrival counters need no zeroing between launches: a counter whose tag is
@@ -486,6 +487,10 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
           if (!mbar_wait_bounded(smem_u32(&raw_empty[slot]), ((nraw / C::RS) & 1) ^ 1, limit_ns, abort_flag, err)) {
             ok = false;
             break;
+          }
+          if (wk.drop && blockIdx.x == 0 && nraw == 1) {  // test hook: the chunk's dequant warps wait it out
+            ++nraw;
+            continue;
           }
           mbar_arrive_expect_tx(smem_u32(&raw_full[slot]), C::kRawBytes);
           tma_load_2d(sbase + C::kOffRaw + slot * C::kRawBytes, &tmW, r * (C::kRawRow / C::kRawElem), m0,
@@ -849,11 +854,9 @@ cudaError_t launch_prefill_cfg(const CUtensorMap* tmW, const CUtensorMap* tmX, i
                                uint64_t limit_ns, bool allow_scratch, int early_w, int pdl, cudaStream_t s) {
   using C = PrefillCfg<BN, PAIR, F>;
   auto kern = k_prefill_q4_0<BN, PAIR, false, F>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  {
+    cudaError_t e = kernel_smem(reinterpret_cast<const void*>(kern), C::kSmem, false);
     if (e != cudaSuccess) return e;
-    configured = true;
   }
   const int64_t ntn = (N + BN - 1) / BN;
   const int64_t rows = C::kBM * C::kCtas;
@@ -863,6 +866,7 @@ cudaError_t launch_prefill_cfg(const CUtensorMap* tmW, const CUtensorMap* tmX, i
   wk.nr = static_cast<int>(nr);
   wk.ntn = static_cast<int>(ntn);
   wk.early_w = pdl && early_w;
+  wk.drop = test_drop() == 2 ? 1 : 0;
   prefill_plan(T, nr, device_info().sm_count / C::kCtas, allow_scratch, &wk);
   void* scratch = nullptr;
   if (wk.R > 0) {  // split tiles: partial-tile slots and arrival counters
@@ -949,11 +953,9 @@ cudaError_t launch_prefill_moe(const CUtensorMap* tmW, const CUtensorMap* tmX, i
                                cudaStream_t s) {
   using C = PrefillCfg<kMoeBN, false>;
   auto kern = k_prefill_q4_0<kMoeBN, false, true>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  {
+    cudaError_t e = kernel_smem(reinterpret_cast<const void*>(kern), C::kSmem, false);
     if (e != cudaSuccess) return e;
-    configured = true;
   }
   // Work items: at most (row tiles) x (token tiles), where the token tiles of
   // all experts number at most P / BN + min(E, P).

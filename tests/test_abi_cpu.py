@@ -89,3 +89,15 @@ def test_argument_errors_before_any_device_work(lib):
     lib.gq_set_option(lib.GQ_OPT_MOE_PATH, 2)
     assert lib.gq_get_option(lib.GQ_OPT_MOE_PATH) == 2
     lib.gq_set_option(lib.GQ_OPT_MOE_PATH, old)
+
+
+def test_timeout_test_hook_option(lib):
+    """GQ_OPT_TEST_DROP_ARRIVE: off by default, takes 0..2 only."""
+    assert lib.gq_get_option(lib.GQ_OPT_TEST_DROP_ARRIVE) == 0
+    with pytest.raises(lib.GQError):
+        lib.gq_set_option(lib.GQ_OPT_TEST_DROP_ARRIVE, 3)
+    with pytest.raises(lib.GQError):
+        lib.gq_set_option(lib.GQ_OPT_TEST_DROP_ARRIVE, -1)
+    for v in (1, 2, 0):
+        lib.gq_set_option(lib.GQ_OPT_TEST_DROP_ARRIVE, v)
+        assert lib.gq_get_option(lib.GQ_OPT_TEST_DROP_ARRIVE) == v
