@@ -8,13 +8,16 @@
 // bf16 copy in one fixed array compiled into the library:
 //
 //  * The array is a file-scope __device__ variable of kMaxElems bf16 values
-//    (12 MiB).  Every GPU that loads this library holds it until the process
-//    exits, whether or not this entry point is ever called.
+//    (12 MiB).  It is reserved on each device where the library's kernels are
+//    first loaded (lazily, on first use of the library on that device, under
+//    CUDA's default lazy module loading) and stays until that device's context
+//    is destroyed, whether or not this entry point is ever called.
 //  * Host code may not use the array's name as a device address (on the host it
 //    names a shadow variable).  The first call on a device, with that device
 //    current, asks the runtime for the real address with cudaGetSymbolAddress
 //    and caches it per device.  Make that first call before any stream capture
-//    begins.
+//    begins.  The cached address belongs to that context: resetting the device
+//    (cudaDeviceReset) after the first call is not supported.
 //  * All calls share the one array and it keeps whatever the last call wrote.
 //    Each call overwrites the N*K elements it later reads, so nothing needs to
 //    start at zero; calls whose work overlaps on the GPU (on different streams
@@ -59,6 +62,7 @@ gq_status scratch_address(uint16_t** out) {
 
 extern "C" gq_status gq_mul_mat_q4_0_noalloc(const void* W, int64_t M, int64_t K, const float* X, int64_t N,
                                              float* Y, void* stream) {
+  gq::api_clear_error();
   gq_status st = gq::api_check_mm_shape(M, K, N);
   if (st != GQ_OK) return st;
   if (M == 0 || N == 0) return GQ_OK;
