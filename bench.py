@@ -134,18 +134,29 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ CPU oracle leg
-def oracle_decode_rate(weights, acts, budget_s, nthreads, max_passes=64):
+def oracle_decode_rate(weights, acts, budget_s, nthreads, max_passes=64, gpu_out=None, check=None):
     """Oracle MUL_MAT at N=1 over the sweep's matrices, pass after pass, until
     budget_s elapses (at least one matrix, at most max_passes passes).
-    Returns (weight GB/s, matrices done, weight bytes done, seconds)."""
+    Returns (weight GB/s, matrices done, weight bytes done, seconds).  With
+    gpu_out (matrix index -> the GPU's y of that matrix) the first pass also
+    compares each result it computes with the GPU's, element by element, and
+    records the worst tolerance ratio in check (outside the timing)."""
     import oracle
     orc = oracle.get()
     order, _ = layer_inputs()
     done_bytes, done, t0 = 0, 0, time.perf_counter()
-    for _ in range(max_passes):
+    paused = 0.0
+    for p in range(max_passes):
         for idx, (M, K, W) in enumerate(weights):
             layer, j = divmod(idx, len(order))
-            orc.mul_mat(W, M, K, acts[layer][order[j]], nthreads=nthreads)
+            y_ref, s_ref = orc.mul_mat(W, M, K, acts[layer][order[j]], nthreads=nthreads)
+            if p == 0 and gpu_out is not None and idx in gpu_out:
+                tc = time.perf_counter()
+                _, worst = oracle.within_tolerance(gpu_out[idx], y_ref, s_ref)
+                check["decode_worst_ratio"] = max(check.get("decode_worst_ratio", 0.0), float(worst))
+                check["decode_matrices"] = check.get("decode_matrices", 0) + 1
+                check["decode_outputs"] = check.get("decode_outputs", 0) + int(y_ref.size)
+                paused += time.perf_counter() - tc
             done_bytes += W.nbytes
             done += 1
             if time.perf_counter() - t0 > budget_s:
@@ -153,8 +164,34 @@ def oracle_decode_rate(weights, acts, budget_s, nthreads, max_passes=64):
         else:
             continue
         break
-    dt = time.perf_counter() - t0
+    dt = time.perf_counter() - t0 - paused
     return done_bytes / dt / 1e9, done, done_bytes, dt
+
+
+def prefill_parity(weights, acts, order, pre_rows, nthreads, check):
+    """The oracle on the sampled rows of the prefill outputs (all 512 tokens),
+    compared element by element with the GPU's; returns the parity summary."""
+    import oracle
+    orc = oracle.get()
+    worst, n_out = 0.0, 0
+    for i, (rows, y_gpu) in pre_rows.items():
+        M, K, W = weights[i]
+        layer, j = divmod(i, len(order))
+        y_ref, s_ref = orc.mul_mat(np.ascontiguousarray(W[rows]), len(rows), K, acts[layer][order[j]],
+                                   nthreads=nthreads)
+        _, w = oracle.within_tolerance(y_gpu, y_ref, s_ref)
+        worst = max(worst, float(w))
+        n_out += int(y_ref.size)
+    check["prefill_worst_ratio"] = worst
+    check["prefill_outputs"] = n_out
+    d = check.get("decode_worst_ratio")
+    return {"parity_worst_ratio": round(max(worst, d if d is not None else 0.0), 4),
+            "tolerance": "|y - y_ref| <= 1e-3 * sum|w x| + 1e-5 (ratio < 1 passes)",
+            "decode": {"worst_ratio": round(d, 4) if d is not None else None,
+                       "matrices": check.get("decode_matrices", 0), "outputs": check.get("decode_outputs", 0),
+                       "what": "the last step's Y of every matrix the CPU leg's first pass computed"},
+            "prefill": {"worst_ratio": round(worst, 4), "outputs": n_out,
+                        "what": "32 sampled rows x 512 tokens of each matrix of the first and last layer"}}
 
 
 def run_reference(args, rank, world):
@@ -258,6 +295,17 @@ def run_gpu(args, rank, world, dist):
         with torch.cuda.graph(g_dec, stream=s):
             decode_pass()
     torch.cuda.synchronize(dev)
+    # the same sweep without the x-static promise: every launch reads its X
+    # only after the kernel before it has finished (a dependent chain)
+    gq.gq_set_option(gq.GQ_OPT_X_STATIC, 0)
+    g_dep = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        decode_pass()
+        torch.cuda.synchronize(dev)
+        with torch.cuda.graph(g_dep, stream=s):
+            decode_pass()
+    torch.cuda.synchronize(dev)
+    gq.gq_set_option(gq.GQ_OPT_X_STATIC, 1)
 
     def step(record):
         e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
@@ -299,13 +347,38 @@ def run_gpu(args, rank, world, dist):
         k3_ms += sum(a.elapsed_time(b) for a, b in ev_pairs)
     if dist is not None:
         dist.barrier()
+    # the dependent decode sweep, K steps, timed alone
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            g_dep.replay()
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        d0.record(s)
+        for _ in range(args.steps):
+            g_dep.replay()
+        d1.record(s)
+    d1.synchronize()
+    dep_ms = d0.elapsed_time(d1)
     clocks = clk.stop()
     gq.gq_sync_status(s)
+    # outputs of the last step, for the parity check of the CPU leg: every
+    # decode Y, and 32 sampled rows of each prefill Y of the first and last layer
+    with torch.cuda.stream(s):
+        g_dec.replay()
+        prefill_pass(False)
+    torch.cuda.synchronize(dev)
+    gq.gq_sync_status(s)
+    dec_out = {i: Y1[i].cpu().numpy() for i in range(len(shapes))}
+    rng = np.random.default_rng(0x51A7)
+    pre_rows = {}
+    for i in list(range(len(order))) + list(range(len(shapes) - len(order), len(shapes))):
+        M = shapes[i][0]
+        rows = np.sort(rng.choice(M, size=32, replace=False))
+        pre_rows[i] = (rows, YP[i][:, torch.from_numpy(rows).to(dev)].cpu().numpy())
 
     dec_ms = sum(a.elapsed_time(b) for a, b, _ in marks)
     pre_ms = sum(b.elapsed_time(c) for _, b, c in marks)
     step_ms = sum(a.elapsed_time(c) for a, _, c in marks)
-    dec_ms, pre_ms, step_ms, k3_ms = max_over_ranks([dec_ms, pre_ms, step_ms, k3_ms], dist, dev)
+    dec_ms, pre_ms, step_ms, k3_ms, dep_ms = max_over_ranks([dec_ms, pre_ms, step_ms, k3_ms, dep_ms], dist, dev)
 
     K_ = args.steps
     value = world * wbytes * K_ / (dec_ms * 1e-3) / 1e9
@@ -323,13 +396,18 @@ def run_gpu(args, rank, world, dist):
         aux["legacy_formats"] = run_legacy_aux(gq, torch, dev, s, peaks)
         aux["prepared_layout"] = run_prepared_aux(gq, torch, dev, s, peaks)
         aux["library_reference"] = run_library_reference(gq, torch, dev, s, peaks)
+    if rank == 0:
+        aux["per_config"] = run_per_config(gq, torch, dev, s, peaks)
     e2e["ms"] = max_over_ranks([e2e["ms"]], dist, dev)[0]
     e2e_value = world * wbytes / (e2e["ms"] * 1e-3) / 1e9
 
     cpu = None
+    parity = None
     if rank == 0 and not args.no_cpu_baseline:
         nthreads = os.cpu_count() or 1
-        gbs, n, b, dt = oracle_decode_rate(host_w, acts1, args.cpu_budget, nthreads)
+        check = {}
+        gbs, n, b, dt = oracle_decode_rate(host_w, acts1, args.cpu_budget, nthreads, gpu_out=dec_out, check=check)
+        parity = prefill_parity(host_w, actsP, order, pre_rows, nthreads, check)
         gbs1, n1, b1, dt1 = oracle_decode_rate(host_w, acts1, args.cpu_budget / 5, 1, max_passes=1)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": nthreads, "kind": "oracle",
                "sample": f"oracle MUL_MAT at N=1, {n} matrices taken in order from the same "
@@ -352,15 +430,24 @@ def run_gpu(args, rank, world, dist):
                    "weights_static": True, "x_static": True,
                    "parallelism": f"replicas x{world}"},
         "decode": {"value": round(value, 2), "unit": "GB/s", "ms": round(dec_ms / K_, 4),
-                   "avg_launch_us": round(dec_avg_us, 3)},
+                   "avg_launch_us": round(dec_avg_us, 3), "frac": round(value / peaks["hbm_gbs"], 4),
+                   "promises": "weights static and x static (each launch may read X and compute before the "
+                               "kernel before it ends; Y is written after it)"},
+        "decode_no_x_static": {"value": round(world * wbytes * K_ / (dep_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                               "ms": round(dep_ms / K_, 4),
+                               "frac": round(world * wbytes * K_ / (dep_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                               "promises": "weights static only: every launch reads X after the kernel before "
+                                           "it has finished, as in a chain where each input is the last output"},
         "prefill": {"value": round(prefill_tflops, 2), "unit": "TFLOP/s", "ms": round(pre_ms / K_, 4),
                     "includes": "fp32->bf16 activation conversion + tensor-core MUL_MAT",
                     "launch": "eager, programmatic dependent launch between consecutive kernels"},
         "roofline": {"kernel": "k_prefill_q4_0 (tcgen05 prefill)", "bound": "tensor",
-                     "achieved": round(k3_tflops, 2), "peak": sust, "unit": "TFLOP/s",
-                     "frac": round(k3_tflops / sust, 4), "traffic": sweep_traffic("prefill", shapes),
+                     "achieved": round(k3_tflops, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(k3_tflops / peaks["bf16_tflops"], 4), "traffic": sweep_traffic("prefill", shapes),
                      "traffic_unit": "bytes per launch (ncu, mean over the sweep's shapes)",
-                     "peak_kind": f"bf16 sustained ({peaks['source']})", "avg_launch_us": round(k3_avg_us, 3),
+                     "peak_kind": f"bf16 burst ({peaks['source']}): the timed region is under a second at "
+                                  f"full clock", "frac_of_sustained": round(k3_tflops / sust, 4),
+                     "avg_launch_us": round(k3_avg_us, 3),
                      "per_launch": "2*M*K*512 flops of the launch's matrix",
                      "timing": "event pair around each layer's 7 back-to-back launches (conversions outside), "
                                "over K further steps of the same sweep; avg = their time / 224"},
@@ -385,6 +472,9 @@ def run_gpu(args, rank, world, dist):
         "gpu_launches": K_ * (len(shapes) + len(shapes) + L * len(ks)),
         "clocks": clocks,
         "cpu_baseline": cpu,
+        "parity": parity,
+        "parity_worst_ratio": parity["parity_worst_ratio"] if parity else None,
+        "per_config": aux.get("per_config"),
         "wall_s": round(wall, 3), "setup_s": round(gen_s, 1),
     }
     print(json.dumps(line), flush=True)
@@ -392,6 +482,130 @@ def run_gpu(args, rank, world, dist):
 
 
 AUX_M, AUX_K, AUX_REPS = 14336, 4096, 10
+
+# (name, M, K, N list): the workloads besides the sweep, each timed on its own
+PER_CONFIG = [("small mat-vec", 256, 1024, [1]),
+              ("7B FFN gate/up mat-vec", 11008, 4096, [1]),
+              ("7B FFN down mat-vec", 4096, 11008, [1]),
+              ("7B attention projection, small batches", 4096, 4096, [1, 2, 4, 8, 16]),
+              ("32000-row output projection, small batches", 32000, 4096, [1, 2, 4, 8, 16]),
+              ("14336-row prefill, 512 tokens", 14336, 4096, [512])]
+
+
+def graph_time(torch, s, fn, reps, replays=5):
+    """Best of `replays` replays of a CUDA graph of `reps` calls fn(0..reps-1), per call, seconds."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        for i in range(reps):
+            fn(i)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            for i in range(reps):
+                fn(i)
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(replays):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            g.replay()
+            e1.record(s)
+        e1.synchronize()
+        best = min(best, e0.elapsed_time(e1) / reps * 1e-3)
+    return best
+
+
+def eager_time(torch, s, fn, reps, replays=5):
+    """Best of `replays` runs of `reps` back-to-back eager calls fn(0..reps-1), per call, seconds."""
+    best = float("inf")
+    with torch.cuda.stream(s):
+        for i in range(reps):
+            fn(i)
+    torch.cuda.synchronize()
+    for _ in range(replays):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            for i in range(reps):
+                fn(i)
+            e1.record(s)
+        e1.synchronize()
+        best = min(best, e0.elapsed_time(e1) / reps * 1e-3)
+    return best
+
+
+def graph_or_eager_time(gq, torch, s, fn, reps):
+    """graph_time, or eager_time where the calls cannot be captured (the
+    tensor-core path takes stream-ordered scratch); returns (seconds, how)."""
+    try:
+        return graph_time(torch, s, fn, reps), "graph"
+    except Exception as e:  # a refused capture is an API error, not a device fault
+        torch.cuda.synchronize()
+        gq.gq_last_error()
+        return eager_time(torch, s, fn, reps), f"eager ({type(e).__name__} on capture)"
+
+
+def run_per_config(gq, torch, dev, s, peaks):
+    """Every workload besides the sweep, device-timed: a CUDA graph of
+    back-to-back calls, each on its own weight copy (together more than 4x L2,
+    so every call streams its weights from DRAM; at most 200 calls), best of
+    5 replays.  Decode shapes
+    (N < 16) are timed with the x-static promise (as in the sweep) and
+    without it (each call reads X only after the kernel before it ends);
+    N >= 16 runs the bf16 conversion and the tensor-core kernel, config 4
+    also the tensor-core kernel alone on bf16 activations."""
+    hbm, tc = peaks["hbm_gbs"], peaks["bf16_tflops"]
+    out = []
+    old_x = gq.gq_get_option(gq.GQ_OPT_X_STATIC)
+    try:
+        for name, M, K, ns in PER_CONFIG:
+            nb = gq.gq_q4_0_nbytes(M, K)
+            # enough copies for 4x L2 per graph (capped at 200 calls: the
+            # 256 x 1024 matrix stays L2-resident, a latency figure)
+            copies = min(200, max(20, int(4 * 130e6 // nb) + 1))
+            W0 = torch.from_numpy(synth.q4_0_weights(M, K, seed=0x5C00 + M + K)).to(dev)
+            Ws = [W0] + [W0.clone() for _ in range(copies - 1)]
+            for n in ns:
+                X = torch.randn(n, K, device=dev, generator=torch.Generator(device=dev).manual_seed(n))
+                Y = torch.empty(n, M, device=dev)
+                alg = nb + 4 * n * K + 4 * n * M
+                e = {"workload": name, "shape": f"{M}x{K}", "n": n, "calls_per_graph": copies}
+
+                def call(i):
+                    gq.gq_mul_mat_q4_0(Ws[i % copies], M, K, X, n, Y, stream=s)
+                if n < gq.gq_get_option(gq.GQ_OPT_PREFILL_MIN_N):
+                    for xs, key in ((1, "x_static"), (0, "dependent")):
+                        gq.gq_set_option(gq.GQ_OPT_X_STATIC, xs)
+                        t = graph_time(torch, s, call, copies)
+                        gbs = alg / t / 1e9
+                        e[key] = {"us": round(t * 1e6, 2), "achieved": round(gbs, 1), "unit": "GB/s",
+                                  "frac": round(gbs / hbm, 4)}
+                    e.update({"bound": "hbm", "peak": hbm, "bytes": alg,
+                              "kernel": "k_decode_q4_0 (mma.sync decode)"})
+                else:
+                    t, how = graph_or_eager_time(gq, torch, s, call, copies)
+                    tf = 2 * M * K * n / t / 1e12
+                    e.update({"us": round(t * 1e6, 2), "achieved": round(tf, 2), "unit": "TFLOP/s", "timing": how,
+                              "frac": round(tf / tc, 4), "bound": "tensor", "peak": tc,
+                              "weight_gbs": round(nb / t / 1e9, 1),
+                              "kernel": "k_f32_to_bf16 + k_prefill_q4_0 (tcgen05)"})
+                    if n >= 512:
+                        Xb = X.to(torch.bfloat16).view(torch.int16)
+                        t3, how3 = graph_or_eager_time(gq, torch, s, lambda i: gq.gq_mul_mat_q4_0_bf16x(
+                            Ws[i % copies], M, K, Xb, n, Y, stream=s), copies)
+                        tf3 = 2 * M * K * n / t3 / 1e12
+                        e["tensor_core_kernel_only"] = {"us": round(t3 * 1e6, 2), "achieved": round(tf3, 2),
+                                                        "unit": "TFLOP/s", "frac": round(tf3 / tc, 4),
+                                                        "timing": how3}
+                out.append(e)
+            del Ws, W0
+    finally:
+        gq.gq_set_option(gq.GQ_OPT_X_STATIC, old_x)
+    gq.gq_sync_status(s)
+    return {"peak_kind": f"HBM copy / bf16 burst ({peaks['source']})",
+            "timing": "CUDA graph of back-to-back calls, one weight copy each (> 4x L2 together, "
+                      "except the 256 x 1024 matrix: 200 copies, L2-resident), best of 5 replays, "
+                      "with GQ_OPT_WEIGHTS_STATIC", "entries": out}
 
 
 def run_aux(gq, torch, dev, s, hbm_gbs):
