@@ -463,8 +463,12 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ W producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmW);
+    // The whole warp runs the loop (waits, bookkeeping) and one elected lane
+    // issues; a converged warp issues TMA and tcgen05 work faster than a lone
+    // lane of a diverged one.
+    {
+      const bool issuer = elect_one();
+      if (issuer) tma_prefetch_desc(&tmW);
       uint32_t nraw = 0;
       bool ok = true, waited = MOE;
       for (int i = 0; i < nseg && ok; ++i) {
@@ -484,7 +488,8 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
             waited = true;
           }
           const uint32_t slot = nraw % C::RS;
-          if (!mbar_wait_bounded(smem_u32(&raw_empty[slot]), ((nraw / C::RS) & 1) ^ 1, limit_ns, abort_flag, err)) {
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(&raw_empty[slot]), ((nraw / C::RS) & 1) ^ 1,
+                                                         limit_ns, abort_flag, err))) {
             ok = false;
             break;
           }
@@ -492,18 +497,22 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
             ++nraw;
             continue;
           }
-          mbar_arrive_expect_tx(smem_u32(&raw_full[slot]), C::kRawBytes);
-          tma_load_2d(sbase + C::kOffRaw + slot * C::kRawBytes, &tmW, r * (C::kRawRow / C::kRawElem), m0,
-                      smem_u32(&raw_full[slot]));
+          if (issuer) {
+            mbar_arrive_expect_tx(smem_u32(&raw_full[slot]), C::kRawBytes);
+            tma_load_2d(sbase + C::kOffRaw + slot * C::kRawBytes, &tmW, r * (C::kRawRow / C::kRawElem), m0,
+                        smem_u32(&raw_full[slot]));
+          }
+          __syncwarp();
           ++nraw;
         }
       }
-      if (!ok) drain_ring(raw_full, C::RS, nraw, limit_ns);
+      if (!ok && issuer) drain_ring(raw_full, C::RS, nraw, limit_ns);
     }
   } else if (warp == C::kXWarp) {
     // ------------------------------------------------------------ x producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmX);
+    {
+      const bool issuer = elect_one();
+      if (issuer) tma_prefetch_desc(&tmX);
       if (!MOE) pdl_wait();
       uint32_t nb = 0;
       bool ok = true;
@@ -522,31 +531,37 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
         }
         for (int ks = 4 * sg.r0; ks < 4 * sg.r1; ++ks) {
           const uint32_t bs = nb % C::S;
-          if (!mbar_wait_bounded(smem_u32(&empty[bs]), ((nb / C::S) & 1) ^ 1, limit_ns, abort_flag, err)) {
+          if (!__all_sync(0xFFFFFFFFu,
+                          mbar_wait_bounded(smem_u32(&empty[bs]), ((nb / C::S) & 1) ^ 1, limit_ns, abort_flag, err))) {
             ok = false;
             break;
           }
           const uint32_t dst = sbase + C::kOffB + bs * C::kBBytes;
-          if constexpr (MOE) {
-            mbar_arrive_expect_tx(smem_u32(&full[bs]), nbox * 64 * 128);
-            for (int b = 0; b < nbox; ++b)
-              tma_load_2d(dst + b * 64 * 128, &tmX, ks * C::kBK, n0 + b * 64, smem_u32(&full[bs]));
-          } else if (PAIR) {
-            if (leader) mbar_arrive_expect_tx(smem_u32(&full[bs]), C::kCtas * C::kBBytes);
-            tma_load_2d_pair(dst, &tmX, ks * C::kBK, n0, leader_bar(&full[bs]));
-          } else {
-            mbar_arrive_expect_tx(smem_u32(&full[bs]), C::kBBytes);
-            tma_load_2d(dst, &tmX, ks * C::kBK, n0, smem_u32(&full[bs]));
+          if (issuer) {
+            if constexpr (MOE) {
+              mbar_arrive_expect_tx(smem_u32(&full[bs]), nbox * 64 * 128);
+              for (int b = 0; b < nbox; ++b)
+                tma_load_2d(dst + b * 64 * 128, &tmX, ks * C::kBK, n0 + b * 64, smem_u32(&full[bs]));
+            } else if (PAIR) {
+              if (leader) mbar_arrive_expect_tx(smem_u32(&full[bs]), C::kCtas * C::kBBytes);
+              tma_load_2d_pair(dst, &tmX, ks * C::kBK, n0, leader_bar(&full[bs]));
+            } else {
+              mbar_arrive_expect_tx(smem_u32(&full[bs]), C::kBBytes);
+              tma_load_2d(dst, &tmX, ks * C::kBK, n0, smem_u32(&full[bs]));
+            }
           }
+          __syncwarp();
           ++nb;
         }
       }
       // (a pair's x copies complete on the leader's barriers: only the leader can drain them)
-      if (!ok && leader) drain_ring(full, C::S, nb, limit_ns);
+      if (!ok && leader && issuer) drain_ring(full, C::S, nb, limit_ns);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (the leader of a pair)
-    if (leader && lane == 0) {
+    // As for the W producer: the converged warp waits, one elected lane issues.
+    if (leader) {
+      const bool issuer = elect_one();
       if (!MOE) pdl_wait();
       uint32_t idesc = umma_idesc_bf16_f32(C::kBM * C::kCtas, BN);
       uint32_t c = 0, seg = 0;
@@ -563,38 +578,46 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
           sg = seg_of(gi, i, wk);
         }
         // the previous segment's epilogue must have read the accumulator
-        if (seg > 0 && !mbar_wait_bounded(smem_u32(acc_empty), (seg - 1) & 1, limit_ns, abort_flag, err)) {
+        if (seg > 0 && !__all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(acc_empty), (seg - 1) & 1, limit_ns,
+                                                                  abort_flag, err))) {
           ok = false;
           break;
         }
         tc_fence_after();
         for (int ks = 4 * sg.r0; ks < 4 * sg.r1; ++ks, ++c) {
           const uint32_t st = c % C::S;
-          if (!mbar_wait_bounded(smem_u32(&full[st]), (c / C::S) & 1, limit_ns, abort_flag, err)) {
+          if (!__all_sync(0xFFFFFFFFu,
+                          mbar_wait_bounded(smem_u32(&full[st]), (c / C::S) & 1, limit_ns, abort_flag, err))) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t a_tmem = tmem_base + BN + st * C::kACols;
           const uint32_t b_addr = sbase + C::kOffB + st * C::kBBytes;
+          if (issuer) {
 #pragma unroll
-          for (int kk = 0; kk < C::kBK / 16; ++kk) {
-            const uint32_t acc = ks != 4 * sg.r0 || kk != 0;
+            for (int kk = 0; kk < C::kBK / 16; ++kk) {
+              const uint32_t acc = ks != 4 * sg.r0 || kk != 0;
+              if (PAIR)
+                umma_bf16_ts_pair(tmem_base, a_tmem + kk * 8, umma_desc_sw128(b_addr + kk * 32), idesc, acc);
+              else
+                umma_bf16_ts(tmem_base, a_tmem + kk * 8, umma_desc_sw128(b_addr + kk * 32), idesc, acc);
+            }
             if (PAIR)
-              umma_bf16_ts_pair(tmem_base, a_tmem + kk * 8, umma_desc_sw128(b_addr + kk * 32), idesc, acc);
+              umma_commit_pair(smem_u32(&empty[st]), 3);
             else
-              umma_bf16_ts(tmem_base, a_tmem + kk * 8, umma_desc_sw128(b_addr + kk * 32), idesc, acc);
+              umma_commit(smem_u32(&empty[st]));
           }
-          if (PAIR)
-            umma_commit_pair(smem_u32(&empty[st]), 3);
-          else
-            umma_commit(smem_u32(&empty[st]));
+          __syncwarp();
         }
         // also on the error path: tracks every MMA issued so far
-        if (PAIR)
-          umma_commit_pair(smem_u32(acc_full), 3);
-        else
-          umma_commit(smem_u32(acc_full));
+        if (issuer) {
+          if (PAIR)
+            umma_commit_pair(smem_u32(acc_full), 3);
+          else
+            umma_commit(smem_u32(acc_full));
+        }
+        __syncwarp();
         ++seg;
       }
       // Do not leave while MMAs issued by this thread may still run: the last
