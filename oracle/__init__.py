@@ -175,7 +175,8 @@ class Oracle:
 
     def validate(self, qtype: int, W: np.ndarray, M: int, K: int):
         """(count, first): blocks with a non-finite scale, and the first one's
-        flat index (row * K/32 + block), or None when there is none."""
+        flat index (row * K/32 + block; super-blocks of 256 for Q4_K), or None
+        when there is none."""
         W = np.ascontiguousarray(W, dtype=np.uint8)
         if W.size != self.type_nbytes(qtype, M, K):
             raise ValueError("W has the wrong number of bytes")
@@ -189,8 +190,9 @@ class Oracle:
 
 
 # Block formats of the typed functions (the same numbering as the library's gq_type).
-TYPE_Q4_0, TYPE_Q4_1, TYPE_Q8_0 = 0, 1, 2
-BLOCK_BYTES = {TYPE_Q4_0: 18, TYPE_Q4_1: 20, TYPE_Q8_0: 34}
+TYPE_Q4_0, TYPE_Q4_1, TYPE_Q8_0, TYPE_Q4_K = 0, 1, 2, 3
+BLOCK_BYTES = {TYPE_Q4_0: 18, TYPE_Q4_1: 20, TYPE_Q8_0: 34, TYPE_Q4_K: 144}
+BLOCK_WEIGHTS = {TYPE_Q4_0: 32, TYPE_Q4_1: 32, TYPE_Q8_0: 32, TYPE_Q4_K: 256}
 
 
 def get() -> Oracle:

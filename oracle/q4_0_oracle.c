@@ -238,6 +238,12 @@ void oracle_mul_mat_id_q4_0(const uint8_t *W, int64_t n_expert, int64_t M, int64
         }
 }
 
+/* A little-endian binary16 field as fp32 (exact). */
+static float le_half_at(const uint8_t *p)
+{
+    return (float)oracle_half_to_double((uint16_t)(p[0] | (p[1] << 8)));
+}
+
 /*
  * The other legacy formats ("Architecture and module overview", the
  * quantisation-format section: 32 weights per block sharing one scale; Q4_1
@@ -256,18 +262,63 @@ static int type_block_bytes(int type)
     case ORACLE_TYPE_Q4_0: return 18;
     case ORACLE_TYPE_Q4_1: return 20;
     case ORACLE_TYPE_Q8_0: return 34;
+    case ORACLE_TYPE_Q4_K: return 144;
     default: return 0;
     }
 }
 
+/* Weights per block: 32 for the legacy formats, 256 for the k-quant. */
+static int type_block_weights(int type)
+{
+    return type == ORACLE_TYPE_Q4_K ? 256 : QK;
+}
+
 size_t oracle_type_nbytes(int type, int64_t M, int64_t K)
 {
-    return (size_t)M * (size_t)(K / QK) * (size_t)type_block_bytes(type);
+    int64_t bw = type_block_weights(type);
+    if (K % bw)
+        return 0;
+    return (size_t)M * (size_t)(K / bw) * (size_t)type_block_bytes(type);
+}
+
+/*
+ * Q4_K's sixteen 6-bit fields (the reading in the header): sc[j] and m[j] of
+ * sub-blocks j = 0..7 from the 12 bytes b[] that follow d and dmin.
+ */
+static void q4_k_fields(const uint8_t *b, int sc[8], int m[8])
+{
+    for (int j = 0; j < 4; ++j) {
+        sc[j] = b[j] & 0x3F;
+        m[j] = b[4 + j] & 0x3F;
+        sc[4 + j] = (b[8 + j] & 0x0F) | ((b[j] >> 6) << 4);
+        m[4 + j] = (b[8 + j] >> 4) | ((b[4 + j] >> 6) << 4);
+    }
+}
+
+/* One Q4_K super-block -> 256 fp32 weights, w = d*sc_j*q - dmin*m_j. */
+static void dequant_q4_k_block(const uint8_t *blk, float *w)
+{
+    float d = le_half_at(blk);
+    float dmin = le_half_at(blk + 2);
+    int sc[8], m[8];
+    q4_k_fields(blk + 4, sc, m);
+    const uint8_t *qs = blk + 16;
+    for (int c = 0; c < 4; ++c) {
+        int jl = 2 * c, jh = 2 * c + 1;                 /* sub-blocks of the low and high nibbles */
+        float dl = d * (float)sc[jl], ml = dmin * (float)m[jl];
+        float dh = d * (float)sc[jh], mh = dmin * (float)m[jh];
+        for (int l = 0; l < 32; ++l) {
+            int q_lo = qs[32 * c + l] & 0x0F;
+            int q_hi = qs[32 * c + l] >> 4;
+            w[64 * c + l] = dl * (float)q_lo - ml;
+            w[64 * c + 32 + l] = dh * (float)q_hi - mh;
+        }
+    }
 }
 
 static float le_half(const uint8_t *p)
 {
-    return (float)oracle_half_to_double((uint16_t)(p[0] | (p[1] << 8)));
+    return le_half_at(p);
 }
 
 static void dequant_row_typed(int type, const uint8_t *row, int64_t K, float *w)
@@ -276,6 +327,11 @@ static void dequant_row_typed(int type, const uint8_t *row, int64_t K, float *w)
     int bb = type_block_bytes(type);
     if (type == ORACLE_TYPE_Q4_0) {
         dequant_row(row, K, w);
+        return;
+    }
+    if (type == ORACLE_TYPE_Q4_K) {
+        for (int64_t b = 0; b < K / 256; ++b)
+            dequant_q4_k_block(row + b * bb, w + b * 256);
         return;
     }
     for (int64_t b = 0; b < nb; ++b) {
@@ -303,7 +359,9 @@ static void dequant_row_typed(int type, const uint8_t *row, int64_t K, float *w)
 
 void oracle_dequant_typed(int type, const uint8_t *W, int64_t M, int64_t K, float *out)
 {
-    size_t row_bytes = (size_t)(K / QK) * (size_t)type_block_bytes(type);
+    if (K % type_block_weights(type))
+        return;
+    size_t row_bytes = (size_t)(K / type_block_weights(type)) * (size_t)type_block_bytes(type);
     for (int64_t m = 0; m < M; ++m)
         dequant_row_typed(type, W + (size_t)m * row_bytes, K, out + (size_t)m * (size_t)K);
 }
@@ -311,13 +369,15 @@ void oracle_dequant_typed(int type, const uint8_t *W, int64_t M, int64_t K, floa
 void oracle_validate_typed(int type, const uint8_t *W, int64_t M, int64_t K, uint64_t *count, uint64_t *first)
 {
     int bb = type_block_bytes(type);
-    uint64_t nblocks = (uint64_t)M * (uint64_t)(K / QK);
     *count = 0;
     *first = UINT64_MAX;
+    if (K % type_block_weights(type))
+        return;
+    uint64_t nblocks = (uint64_t)M * (uint64_t)(K / type_block_weights(type));
     for (uint64_t b = 0; b < nblocks; ++b) {
         const uint8_t *blk = W + b * (uint64_t)bb;
         int bad = !isfinite(oracle_half_to_double((uint16_t)(blk[0] | (blk[1] << 8))));
-        if (type == ORACLE_TYPE_Q4_1)
+        if (type == ORACLE_TYPE_Q4_1 || type == ORACLE_TYPE_Q4_K)   /* m, or dmin */
             bad |= !isfinite(oracle_half_to_double((uint16_t)(blk[2] | (blk[3] << 8))));
         if (bad) {
             if (*count == 0)
@@ -330,7 +390,9 @@ void oracle_validate_typed(int type, const uint8_t *W, int64_t M, int64_t K, uin
 void oracle_mul_mat_typed(int type, const uint8_t *W, int64_t M, int64_t K, const float *X, int64_t N,
                           double *Y, double *S, int nthreads)
 {
-    size_t row_bytes = (size_t)(K / QK) * (size_t)type_block_bytes(type);
+    if (K % type_block_weights(type))
+        return;
+    size_t row_bytes = (size_t)(K / type_block_weights(type)) * (size_t)type_block_bytes(type);
     if (nthreads < 1)
         nthreads = 1;
     (void)nthreads;

@@ -96,7 +96,34 @@ void oracle_mul_mat_id_q4_0(const uint8_t *W, int64_t n_expert, int64_t M, int64
  * 0..15 in the Q4_0 nibble order; Q8_0 = fp16 d, int8 qs[32] (34 bytes), w =
  * d*q.  ORACLE_TYPE_Q4_0 is the Q4_0 functions above.
  */
-enum { ORACLE_TYPE_Q4_0 = 0, ORACLE_TYPE_Q4_1 = 1, ORACLE_TYPE_Q8_0 = 2 };
+enum { ORACLE_TYPE_Q4_0 = 0, ORACLE_TYPE_Q4_1 = 1, ORACLE_TYPE_Q8_0 = 2, ORACLE_TYPE_Q4_K = 3 };
+/*
+ * Q4_K, the 4-bit k-quant ("Architecture and module overview", the
+ * quantisation-format section and the error-model paragraph of the
+ * weight-loading section: k-quants group 256 weights per block and store the
+ * block's scales and mins hierarchically inside it, an upper level in 6 bits
+ * and a lower level in 4; "GGUF loading, mmap and tensor placement": a Q4_K
+ * tensor takes ne[0]/256 x block-size bytes).  The pages print no struct.
+ * The reading: the 6-bit level is a scale and a min per sub-block of 32
+ * weights, the 4-bit level is the weight codes, and the bytes are laid out as
+ * GGUF files carry them (the pages stress that the file's block layout is the
+ * memory layout the kernels consume), a 144-byte super-block of 256 weights:
+ *   bytes 0-1    fp16 d      (scale of the sub-block scales)
+ *   bytes 2-3    fp16 dmin   (scale of the sub-block mins)
+ *   bytes 4-15   sixteen 6-bit fields: sc_j and m_j of the 8 sub-blocks of
+ *                32 weights (byte b = bytes[4 + b]):
+ *                  b 0-3:  bits 0-5 = sc_b,     bits 6-7 = bits 4-5 of sc_{b+4}
+ *                  b 4-7:  bits 0-5 = m_{b-4},  bits 6-7 = bits 4-5 of m_b
+ *                  b 8-11: bits 0-3 = bits 0-3 of sc_{b-4}, bits 4-7 = bits 0-3 of m_{b-4}
+ *   bytes 16-143 qs[128]: weight 64c + l (c = 0..3, l = 0..31) is the low
+ *                nibble of qs[32c + l] (sub-block 2c); weight 64c + 32 + l is
+ *                its high nibble (sub-block 2c + 1).
+ * Weight i of sub-block j with code q: w = d*sc_j*q - dmin*m_j.  In fp32
+ * d*sc_j (at most 17 significant bits) times q (4 bits) and dmin*m_j are
+ * exact, so the fp32 weight is that value rounded once.  K must be a multiple
+ * of 256 (the typed functions return 0 bytes / do nothing otherwise), and the
+ * flat block index of validation counts super-blocks (row * K/256 + block).
+ */
 size_t oracle_type_nbytes(int type, int64_t M, int64_t K);
 void oracle_dequant_typed(int type, const uint8_t *W, int64_t M, int64_t K, float *out);
 void oracle_mul_mat_typed(int type, const uint8_t *W, int64_t M, int64_t K, const float *X, int64_t N,
@@ -106,9 +133,10 @@ void oracle_mul_mat_typed(int type, const uint8_t *W, int64_t M, int64_t K, cons
  * Row-data validation ("GGUF loading, mmap and tensor placement", the section
  * on --check-tensors and parallel validation: ggml_validate_row_data checks
  * each row's scale factors and integers; the reading: a block's fp16 scale
- * fields must be finite, and every 4- or 8-bit code is a valid integer).  Over the M x K weights in block format `type`: *count = the
- * number of blocks with a NaN or infinite scale (d; for Q4_1 also m),
- * *first = the smallest flat block index (row * K/32 + block) among them, or
+ * fields must be finite, and every 4-, 6- or 8-bit field is a valid integer).  Over the M x K weights in block format `type`: *count = the
+ * number of blocks with a NaN or infinite scale (d; for Q4_1 also m; for Q4_K also dmin),
+ * *first = the smallest flat block index (row * K/32 + block; row * K/256 +
+ * super-block for Q4_K) among them, or
  * UINT64_MAX when there is none.  A scale is tested by decoding it with
  * oracle_half_to_double and asking isfinite.
  */

@@ -114,14 +114,36 @@ def moe_weights(E: int, M: int, K: int, seed: int) -> np.ndarray:
     return np.concatenate([q4_0_weights(M, K, seed + 7919 * e) for e in range(E)], axis=0)
 
 
+def q4_k_weights(M: int, K: int, seed: int, d_scale: float = 1.0) -> np.ndarray:
+    """Q4_K weights as raw bytes [M, K/256*144]: per 256-weight super-block a
+    little-endian fp16 d ~ U[1e-4, 2e-4] and fp16 dmin ~ U[7.5e-4, 1.5e-3]
+    (RNE of fp64 draws, times d_scale), then 12 random bytes (every pattern
+    is a valid set of 6-bit sub-block scales and mins) and 128 random code
+    bytes.  With sub-block scales and mins uniform on 0..63, dmin ~ 7.5 d
+    centres the weights d*sc*q - dmin*m roughly on zero, as a quantiser that
+    fits each sub-block's range would."""
+    if K % 256:
+        raise ValueError("K must be a multiple of 256")
+    nb = K // 256
+    out = np.empty((M, nb, 144), dtype=np.uint8)
+    out[:, :, 4:] = random_bytes(seed, M * nb * 140).reshape(M, nb, 140)
+    out[:, :, 0:2] = random_scales(seed, M * nb, 1e-4 * d_scale, 2e-4 * d_scale).view(np.uint8).reshape(M, nb, 2)
+    out[:, :, 2:4] = random_scales(seed ^ 0x4D19, M * nb, 7.5e-4 * d_scale,
+                                   1.5e-3 * d_scale).view(np.uint8).reshape(M, nb, 2)
+    return out.reshape(M, nb * 144)
+
+
 def typed_weights(qtype: int, M: int, K: int, seed: int, d_scale: float = 1.0) -> np.ndarray:
-    """Weights in one of the legacy block formats, as raw bytes [M, K/32*bytes]:
+    """Weights in one of the block formats, as raw bytes [M, K/32*bytes]:
     0 = Q4_0 (q4_0_weights), 1 = Q4_1 (fp16 d ~ U[0.005, 0.02], fp16 m ~
     U[-0.16, 0], 16 random code bytes), 2 = Q8_0 (fp16 d ~ U[0.0003, 0.0012],
-    32 random int8 code bytes).  Scales are RNE fp16 of values drawn in fp64;
-    d_scale multiplies the ranges of d and m (e.g. 100 for O(1) weights)."""
+    32 random int8 code bytes), 3 = Q4_K (q4_k_weights: [M, K/256*144]).
+    Scales are RNE fp16 of values drawn in fp64; d_scale multiplies the ranges
+    of d and m (e.g. 100 for O(1) weights)."""
     if qtype == 0:
         return q4_0_weights(M, K, seed, (0.005 * d_scale, 0.02 * d_scale))
+    if qtype == 3:
+        return q4_k_weights(M, K, seed, d_scale)
     if K % QK4_0:
         raise ValueError("K must be a multiple of 32")
     nb = K // QK4_0

@@ -34,8 +34,18 @@ def read_blocks(name: str = "q4_0_blocks.txt"):
     return out
 
 
+def _values(rest: str) -> np.ndarray:
+    """Whitespace-separated values; "v*n" stands for n copies of v."""
+    vals = []
+    for tok in rest.split():
+        v, star, n = tok.partition("*")
+        vals.extend([_float(v)] * (int(n) if star else 1))
+    return np.array(vals, dtype=np.float32)
+
+
 def read_typed_blocks(name: str = "legacy_blocks.txt"):
-    """List of (type name, block name, raw bytes, 32 expected fp32 values)."""
+    """List of (type name, block name, raw bytes, expected fp32 values: 32 per
+    legacy block, 256 per Q4_K super-block)."""
     out, cur, typ = [], {}, None
     with open(os.path.join(GOLDEN, name)) as f:
         for line in f:
@@ -50,7 +60,7 @@ def read_typed_blocks(name: str = "legacy_blocks.txt"):
             elif key == "bytes":
                 cur["bytes"] = np.frombuffer(bytes.fromhex(rest), dtype=np.uint8)
             elif key == "values":
-                cur["values"] = np.array([_float(t) for t in rest.split()], dtype=np.float32)
+                cur["values"] = _values(rest)
                 out.append((typ, cur["name"], cur["bytes"], cur["values"]))
     return out
 
