@@ -57,14 +57,24 @@ typedef enum {
 
 /* Block formats of the typed entry points ("Architecture and module
  * overview", quantisation-format section: the legacy formats, 32 weights per
- * block with one scale; Q4_1 also stores a min offset; Q8_0 has 8-bit codes).
+ * block with one scale; Q4_1 also stores a min offset; Q8_0 has 8-bit codes;
+ * the k-quants, 256 weights per block with scales and mins stored
+ * hierarchically inside it, an upper level in 6 bits and a lower one in 4).
  * The pages print only the Q4_0 struct; the layouts taken for the others:
  *   GQ_TYPE_Q4_0  fp16 d, uint8_t qs[16]          18 bytes  w = d*(q - 8)
  *   GQ_TYPE_Q4_1  fp16 d, fp16 m, uint8_t qs[16]  20 bytes  w = d*q + m
  *   GQ_TYPE_Q8_0  fp16 d, int8_t qs[32]           34 bytes  w = d*q
- * (fp16 little-endian; 4-bit codes: low nibble of qs[j] = element j, high
- * nibble = element j+16; Q8_0: qs[j] = element j). */
-typedef enum { GQ_TYPE_Q4_0 = 0, GQ_TYPE_Q4_1 = 1, GQ_TYPE_Q8_0 = 2 } gq_type;
+ *   GQ_TYPE_Q4_K  fp16 d, fp16 dmin, uint8_t scales[12], uint8_t qs[128]
+ *                 144 bytes per 256 weights (the GGUF super-block)
+ *                 w = d*sc_j*q - dmin*m_j for sub-block j = 0..7 of 32 weights
+ * (fp16 little-endian; legacy 4-bit codes: low nibble of qs[j] = element j,
+ * high nibble = element j+16; Q8_0: qs[j] = element j.  Q4_K: weight 64c + l
+ * (l < 32) is the low nibble of qs[32c + l] in sub-block 2c, weight 64c+32+l
+ * its high nibble in sub-block 2c+1; the 6-bit sc_j, m_j: for j < 4 bits 0-5
+ * of scales[j] and scales[j+4]; for j >= 4 bits 0-3 from the low and high
+ * nibble of scales[j+4] and bits 4-5 from the top two bits of scales[j-4]
+ * and scales[j].)  Rows of Q4_K need K % 256 == 0. */
+typedef enum { GQ_TYPE_Q4_0 = 0, GQ_TYPE_Q4_1 = 1, GQ_TYPE_Q8_0 = 2, GQ_TYPE_Q4_K = 3 } gq_type;
 
 /* Bytes of a Q4_0 matrix of M rows and K columns: M*(K/32)*18
  * ("Binding GGUF weights to the compute graph", section 2.3, ggml_nbytes note).
@@ -90,28 +100,31 @@ gq_status gq_dequant_q4_0(const void *W, int64_t M, int64_t K, float *out, void 
  * K % 32 != 0 or negative sizes -> GQ_ERR_SHAPE, NULL -> GQ_ERR_NULL. */
 gq_status gq_quantize_q4_0(const float *W, int64_t M, int64_t K, void *out, void *stream);
 
-/* Bytes of an M x K matrix in block format `type`: M*(K/32)*block bytes; 0 for
- * K % 32 != 0, negative sizes or an unknown type. */
+/* Bytes of an M x K matrix in block format `type`: M*(K/32)*block bytes
+ * (Q4_K: M*(K/256)*144); 0 for K not a multiple of the block's weights,
+ * negative sizes or an unknown type. */
 size_t gq_type_nbytes(gq_type type, int64_t M, int64_t K);
 
 /* Dequantise W (M x K in block format `type`) into out[M][K] fp32, bit-exact:
  * d*q is exact in fp32 and Q4_1 adds m with one rounding (round to nearest
- * even).  GQ_TYPE_Q4_0 is gq_dequant_q4_0.  Any alignment (16-byte aligned W
- * and out take vector loads and stores); errors as gq_dequant_q4_0, plus
- * GQ_ERR_SHAPE for an unknown type. */
+ * even); Q4_K's d*sc_j*q and dmin*m_j are exact in fp32 and their difference
+ * is rounded once.  GQ_TYPE_Q4_0 is gq_dequant_q4_0.  Any alignment (16-byte
+ * aligned W and out take vector loads and stores); errors as gq_dequant_q4_0
+ * (Q4_K: K % 256 != 0 is GQ_ERR_SHAPE), plus GQ_ERR_SHAPE for an unknown type. */
 gq_status gq_dequant(gq_type type, const void *W, int64_t M, int64_t K, float *out, void *stream);
 
 /* Row-data validation ("GGUF loading, mmap and tensor placement", the
  * section on --check-tensors: ggml_validate_row_data checks each row's scale
  * factors and integers): scan W (M x K in block format `type`, rows
  * contiguous) for blocks whose fp16 scale fields are NaN or infinite -- d in
- * every format, and m in Q4_1; codes are always valid.  result: device
- * pointer to two uint64 values, written on `stream`: result[0] = the number of
- * such blocks, result[1] = the smallest flat block index (row * K/32 + block)
- * among them, or UINT64_MAX when there is none.  Asynchronous: read result
+ * every format, m in Q4_1, dmin in Q4_K; codes and 6-bit fields are always
+ * valid.  result: device pointer to two uint64 values, written on `stream`:
+ * result[0] = the number of such blocks, result[1] = the smallest flat block
+ * index (row * K/32 + block; for Q4_K row * K/256 + super-block) among them,
+ * or UINT64_MAX when there is none.  Asynchronous: read result
  * after the stream.  Any alignment of W; result 8-byte aligned.  M or K == 0:
  * result (0, UINT64_MAX).  Errors: GQ_ERR_SHAPE (negative size, K % 32 != 0,
- * unknown type), GQ_ERR_NULL (result NULL, or W NULL with M*K > 0),
+ * unknown type, Q4_K with K % 256 != 0), GQ_ERR_NULL (result NULL, or W NULL with M*K > 0),
  * GQ_ERR_ALIGN (result not 8-byte aligned). */
 gq_status gq_validate(gq_type type, const void *W, int64_t M, int64_t K, uint64_t *result, void *stream);
 
@@ -119,13 +132,16 @@ gq_status gq_validate(gq_type type, const void *W, int64_t M, int64_t K, uint64_
 gq_status gq_validate_q4_0(const void *W, int64_t M, int64_t K, uint64_t *result, void *stream);
 
 /* MUL_MAT with W in block format `type`: Y[N][M] = X[N][K] * W^T, fp32 in and
- * out.  GQ_TYPE_Q4_0 is gq_mul_mat_q4_0.  Q4_1 and Q8_0, with K % 256 == 0
+ * out.  GQ_TYPE_Q4_0 is gq_mul_mat_q4_0.  Q4_1, Q8_0 and Q4_K (whose K must be
+ * a multiple of 256: GQ_ERR_SHAPE otherwise), with K % 256 == 0
  * and W, X, Y 16-byte aligned: N >= GQ_OPT_PREFILL_MIN_N converts X to bf16
  * and runs the tcgen05 kernel with this block format (N*K*2 bytes of
  * stream-ordered scratch, plus k-split scratch as in gq_mul_mat_q4_0); a
  * smaller N below 16 streams W through the decode kernel on this block format
- * (fp16 x, exact integer codes, fp32 block scales and accumulation).  Other
- * shapes: a warp per weight row decodes the blocks to fp32 codes in registers
+ * (fp16 x, exact integer codes, fp32 block scales and accumulation; Q4_K:
+ * per 32-weight sub-block the scale d*sc_j and the min dmin*m_j in fp32; the
+ * tensor-core path rounds each fp32 weight to bf16).  Other
+ * shapes: a warp per weight row decodes the blocks to fp32 in registers
  * and accumulates in fp32 (any alignment, K % 32 == 0); GQ_OPT_FORCE_GENERIC
  * forces it.  M, N == 0 no-op, K == 0 zeros.  Accuracy as gq_mul_mat_q4_0. */
 gq_status gq_mul_mat(gq_type type, const void *W, int64_t M, int64_t K, const float *X, int64_t N, float *Y,

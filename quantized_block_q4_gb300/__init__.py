@@ -29,8 +29,9 @@ GQ_ERR_DEVICE_TIMEOUT = -6
 GQ_ERR_UNSUPPORTED = -7
 GQ_ERR_BAD_INDEX = -8
 
-GQ_TYPE_Q4_0, GQ_TYPE_Q4_1, GQ_TYPE_Q8_0 = 0, 1, 2
-TYPE_BLOCK_BYTES = {GQ_TYPE_Q4_0: 18, GQ_TYPE_Q4_1: 20, GQ_TYPE_Q8_0: 34}
+GQ_TYPE_Q4_0, GQ_TYPE_Q4_1, GQ_TYPE_Q8_0, GQ_TYPE_Q4_K = 0, 1, 2, 3
+TYPE_BLOCK_BYTES = {GQ_TYPE_Q4_0: 18, GQ_TYPE_Q4_1: 20, GQ_TYPE_Q8_0: 34, GQ_TYPE_Q4_K: 144}
+TYPE_BLOCK_WEIGHTS = {GQ_TYPE_Q4_0: 32, GQ_TYPE_Q4_1: 32, GQ_TYPE_Q8_0: 32, GQ_TYPE_Q4_K: 256}
 
 GQ_OPT_PREFILL_MIN_N = 0
 GQ_OPT_FORCE_GENERIC = 1
@@ -281,9 +282,10 @@ def mul_mat_id_q4_0(W: torch.Tensor, n_expert: int, X: torch.Tensor, ids: torch.
 def _rows_of(W: torch.Tensor, qtype: int, K: int) -> int:
     if W.dtype != torch.uint8:
         raise TypeError("W must be uint8 (raw blocks)")
-    if K % 32 or K <= 0:
-        raise ValueError("K must be a positive multiple of 32")
-    row = K // 32 * TYPE_BLOCK_BYTES[qtype]
+    bw = TYPE_BLOCK_WEIGHTS[qtype]
+    if K % bw or K <= 0:
+        raise ValueError(f"K must be a positive multiple of {bw}")
+    row = K // bw * TYPE_BLOCK_BYTES[qtype]
     if W.numel() % row:
         raise ValueError("W size is not a whole number of rows")
     return W.numel() // row

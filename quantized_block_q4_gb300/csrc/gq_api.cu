@@ -257,7 +257,7 @@ static gq_status mul_mat_prefill_bf16(const void* W, int64_t M, int64_t K, const
   uint32_t wbx, web, wby, xbk, xbr;
   prefill_boxes(N, type, &wbx, &web, &wby, &xbk, &xbr);
   if (Kw <= 0) Kw = K;
-  const uint64_t row_bytes = static_cast<uint64_t>(Kw / kQK) * static_cast<uint64_t>(type_block_bytes(type));
+  const uint64_t row_bytes = type_row_bytes(type, Kw);
   gq_status st = make_tmap(&tmW, web == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, W,
                            row_bytes / web, static_cast<uint64_t>(M), row_bytes, wbx, wby, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (st != GQ_OK) return st;
@@ -307,9 +307,8 @@ gq_status gq_dequant_q4_0(const void* W, int64_t M, int64_t K, float* out, void*
 }
 
 size_t gq_type_nbytes(gq_type type, int64_t M, int64_t K) {
-  const int bb = type_block_bytes(type);
-  if (bb == 0 || M < 0 || K < 0 || K % kQK) return 0;
-  return static_cast<size_t>(M) * static_cast<size_t>(K / kQK) * static_cast<size_t>(bb);
+  if (type_block_bytes(type) == 0 || M < 0 || K < 0 || K % type_block_weights(type)) return 0;
+  return static_cast<size_t>(M) * static_cast<size_t>(type_row_bytes(type, K));
 }
 
 gq_status gq_dequant(gq_type type, const void* W, int64_t M, int64_t K, float* out, void* stream) {
@@ -317,15 +316,19 @@ gq_status gq_dequant(gq_type type, const void* W, int64_t M, int64_t K, float* o
   t_last_error.clear();
   if (type_block_bytes(type) == 0) return fail(GQ_ERR_SHAPE, "unknown block type %d", static_cast<int>(type));
   if (M < 0 || K < 0) return fail(GQ_ERR_SHAPE, "negative size");
-  if (K % kQK) return fail(GQ_ERR_SHAPE, "K=%lld is not a multiple of 32", (long long)K);
+  const int bw = type_block_weights(type);
+  if (K % bw) return fail(GQ_ERR_SHAPE, "K=%lld is not a multiple of %d", (long long)K, bw);
   if (M == 0 || K == 0) return GQ_OK;
   if (!W || !out) return fail(GQ_ERR_NULL, "W and out must not be NULL");
   if ((unsigned __int128)M * K * 4 > ((unsigned __int128)1 << 62)) return fail(GQ_ERR_SHAPE, "size overflows");
   if (!aligned(out, 4)) return fail(GQ_ERR_ALIGN, "out must be 4-byte aligned");
   gq_status st = check_device();
   if (st != GQ_OK) return st;
-  cudaError_t e = launch_dequant_legacy(type, static_cast<const uint8_t*>(W), M * (K / kQK), out,
-                                        static_cast<cudaStream_t>(stream));
+  cudaError_t e = type == GQ_TYPE_Q4_K
+                      ? launch_dequant_q4_k(static_cast<const uint8_t*>(W), M * (K / bw), out,
+                                            static_cast<cudaStream_t>(stream))
+                      : launch_dequant_legacy(type, static_cast<const uint8_t*>(W), M * (K / kQK), out,
+                                              static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? GQ_OK : cuda_fail(e, "dequant launch");
 }
 
@@ -333,14 +336,15 @@ gq_status gq_validate(gq_type type, const void* W, int64_t M, int64_t K, uint64_
   t_last_error.clear();
   if (type_block_bytes(type) == 0) return fail(GQ_ERR_SHAPE, "unknown block type %d", static_cast<int>(type));
   if (M < 0 || K < 0) return fail(GQ_ERR_SHAPE, "negative size");
-  if (K % kQK) return fail(GQ_ERR_SHAPE, "K=%lld is not a multiple of 32", (long long)K);
+  const int bw = type_block_weights(type);
+  if (K % bw) return fail(GQ_ERR_SHAPE, "K=%lld is not a multiple of %d", (long long)K, bw);
   if (!result) return fail(GQ_ERR_NULL, "result must not be NULL");
   if (!aligned(result, 8)) return fail(GQ_ERR_ALIGN, "result must be 8-byte aligned");
   if (M > 0 && K > 0 && !W) return fail(GQ_ERR_NULL, "W must not be NULL");
   if ((unsigned __int128)M * K > ((unsigned __int128)1 << 62)) return fail(GQ_ERR_SHAPE, "size overflows");
   gq_status st = check_device();
   if (st != GQ_OK) return st;
-  cudaError_t e = launch_validate(static_cast<const uint8_t*>(W), M * (K / kQK), type,
+  cudaError_t e = launch_validate(static_cast<const uint8_t*>(W), M * (K / bw), type,
                                   reinterpret_cast<unsigned long long*>(result), static_cast<int>(g_pdl.load()),
                                   static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? GQ_OK : cuda_fail(e, "validate launch");
@@ -357,6 +361,8 @@ gq_status gq_mul_mat(gq_type type, const void* W, int64_t M, int64_t K, const fl
   if (type_block_bytes(type) == 0) return fail(GQ_ERR_SHAPE, "unknown block type %d", static_cast<int>(type));
   gq_status st = check_mm_shape(M, K, N);
   if (st != GQ_OK) return st;
+  if (K % type_block_weights(type))
+    return fail(GQ_ERR_SHAPE, "K=%lld is not a multiple of %d", (long long)K, type_block_weights(type));
   if (M == 0 || N == 0) return GQ_OK;
   if (!Y) return fail(GQ_ERR_NULL, "Y must not be NULL");
   st = check_device();
@@ -373,12 +379,14 @@ gq_status gq_mul_mat(gq_type type, const void* W, int64_t M, int64_t K, const fl
   const bool fast = K % 256 == 0 && aligned(W, 16) && aligned(X, 16) && aligned(Y, 16) && !g_force_generic.load();
   const bool tc = fast && N >= g_prefill_min_n.load();
   if (fast && !tc && N < 16) {
-    // the decode kernel on 20- / 34-byte blocks (Q8_0's 272-byte box rows as 16-bit elements)
+    // the decode kernel on this block format: a box row is 256 k of a weight
+    // row (Q4_1 160 bytes, Q4_K 144; Q8_0's 272 bytes as 16-bit elements)
     CUtensorMap tm;
-    const uint64_t row_bytes = static_cast<uint64_t>(K / kQK) * static_cast<uint64_t>(type_block_bytes(type));
-    const bool wide = type == GQ_TYPE_Q8_0;
+    const uint64_t row_bytes = type_row_bytes(type, K);
+    const uint32_t box_bytes = static_cast<uint32_t>(type_row_bytes(type, 256));
+    const bool wide = box_bytes > 256;
     st = make_tmap(&tm, wide ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, W,
-                   row_bytes / (wide ? 2 : 1), static_cast<uint64_t>(M), row_bytes, wide ? 136 : 160, 32,
+                   row_bytes / (wide ? 2 : 1), static_cast<uint64_t>(M), row_bytes, box_bytes / (wide ? 2 : 1), 32,
                    CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != GQ_OK) return st;
     cudaError_t e = launch_decode_legacy(type, &tm, X, N, M, K, Y, static_cast<uint64_t>(g_wait_limit_ns.load()),
@@ -386,8 +394,10 @@ gq_status gq_mul_mat(gq_type type, const void* W, int64_t M, int64_t K, const fl
     return e == cudaSuccess ? GQ_OK : cuda_fail(e, "decode launch");
   }
   if (!tc) {
-    cudaError_t e = launch_mul_mat_legacy(type, static_cast<const uint8_t*>(W), M, K, X, N, Y,
-                                          static_cast<uint64_t>(g_wait_limit_ns.load()), s);
+    cudaError_t e = type == GQ_TYPE_Q4_K
+                        ? launch_mul_mat_q4_k(static_cast<const uint8_t*>(W), M, K, X, N, Y, s)
+                        : launch_mul_mat_legacy(type, static_cast<const uint8_t*>(W), M, K, X, N, Y,
+                                                static_cast<uint64_t>(g_wait_limit_ns.load()), s);
     return e == cudaSuccess ? GQ_OK : cuda_fail(e, "mul_mat launch");
   }
   // X -> bf16 scratch, then the tensor-core kernel with this block format

@@ -36,7 +36,10 @@
 //    write W, as in weight-stationary inference); with `x_static` X is read
 //    and the MMAs run before it too, and only the warp writing Y waits.
 //  * The same kernel serves Q4_1 and Q8_0 blocks (F: 20- and 34-byte blocks,
-//    their own code extraction and bias) and MUL_MAT_ID (MOE: groups of
+//    their own code extraction and bias), Q4_K super-blocks (one 144-byte
+//    super-block per box row; each 32-weight sub-block is a staging block of
+//    its own with its scale d*sc_j and min dmin*m_j, its codes the low
+//    (even sub-block) or high (odd) nibbles of 32 code bytes) and MUL_MAT_ID (MOE: groups of
 //    routed tokens of one expert; a single token's slots read their expert
 //    ids directly).
 #include <algorithm>
@@ -45,6 +48,7 @@
 
 #include "gq_internal.h"
 #include "gq_ptx.cuh"
+#include "gq_q4k.cuh"
 
 namespace gq {
 namespace {
@@ -52,7 +56,8 @@ namespace {
 constexpr int kSubK = 256;         // weights per row per TMA box
 constexpr int kSubBytesRow = 144;  // 8 blocks x 18 bytes (Q4_0)
 
-// Bytes of one row of a TMA box (8 blocks): Q4_0 144, Q4_1 160.
+// Bytes of one row of a TMA box (256 weights): Q4_0 144, Q4_1 160, Q8_0 272,
+// Q4_K 144 (one super-block).
 template <int F>
 constexpr int sub_bytes_row() { return F == GQ_TYPE_Q4_1 ? 160 : (F == GQ_TYPE_Q8_0 ? 272 : kSubBytesRow); }
 
@@ -65,7 +70,8 @@ struct DecodeCfg {
   static constexpr int kBM = 16 * MT;
   static constexpr int kRowBytes = sub_bytes_row<F>();
   static constexpr int kElem = kRowBytes > 256 ? 2 : 1;  // TMA element bytes (a box is at most 256 wide)
-  static constexpr int kTables = F == GQ_TYPE_Q4_1 ? 2 : 1;
+  // Q4_1 and Q4_K also keep per-block x sums for their min offsets
+  static constexpr int kTables = (F == GQ_TYPE_Q4_1 || F == GQ_TYPE_Q4_K) ? 2 : 1;
   static constexpr int kSubBytes = kBM * kRowBytes;
   static constexpr int kThreads = 32 * (KW + 1);
   static constexpr int kStageK = kSubK * KW;
@@ -196,6 +202,46 @@ __device__ __forceinline__ float stage_block_q41(const float (&x)[32], uint4* ds
   return -1024.f * bias;
 }
 
+// Q4_K x staging of one 32-weight sub-block (natural k order, like Q4_1).  Its
+// codes are the low nibbles (even sub-block: A = 1024 + q against fp16 x) or
+// the high nibbles (odd: A = 1024 + 16q against fp16 x/16) of 32 code bytes,
+// bytes 0-15 feeding the first MMA (fragment halves x, y) and bytes 16-31 the
+// second (z, w).  The bias is 1024 * (sum of the staged values); the x sum the
+// sub-block's min multiplies is the staged sum (times 16 when odd).
+__device__ __forceinline__ float stage_block_q4k(const float (&x)[32], uint4* dst, float* sx, int odd) {
+  const float f = odd ? 0.0625f : 1.f;
+  float staged = 0.f;
+  __half xh[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    xh[j] = __float2half_rn(x[j] * f);
+    staged += __half2float(xh[j]);
+  }
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const int c0 = 4 * t, c1 = 4 * t + 1, c2 = 4 * t + 2, c3 = 4 * t + 3;
+    __half2 h;
+    uint4 pk;
+    h = __halves2half2(xh[c0], xh[c2]); pk.x = *reinterpret_cast<uint32_t*>(&h);
+    h = __halves2half2(xh[c1], xh[c3]); pk.y = *reinterpret_cast<uint32_t*>(&h);
+    h = __halves2half2(xh[16 + c0], xh[16 + c2]); pk.z = *reinterpret_cast<uint32_t*>(&h);
+    h = __halves2half2(xh[16 + c1], xh[16 + c3]); pk.w = *reinterpret_cast<uint32_t*>(&h);
+    dst[t] = pk;
+  }
+  *sx = odd ? 16.f * staged : staged;
+  return -1024.f * staged;
+}
+
+// Half of the biased codes of a word of 4 code bytes (c0..c3): the low
+// nibbles as fp16 1024 + q, or the high nibbles as 1024 + 16q, in the pairs
+// (c0, c2) and (c1, c3).
+__device__ __forceinline__ void codes_half_f16(uint32_t v, int hi, uint32_t& r02, uint32_t& r13) {
+  const uint32_t kMagic = 0x64006400u;
+  const uint32_t mask = hi ? 0x00F000F0u : 0x000F000Fu;
+  r02 = lop3_and_or(v, mask, kMagic);
+  r13 = lop3_and_or(v >> 8, mask, kMagic);
+}
+
 // Q8_0 x staging: a lane owns elements 4t .. 4t+3 of each half of a block
 // (k 2t, 2t+1 <- 4t, 4t+1 and k 2t+8, 2t+9 <- 4t+2, 4t+3 in the MMA); the codes
 // enter as fp16 1024 + (c ^ 0x80) = 1152 + q, so the bias is 1152 * sum(x).
@@ -237,13 +283,16 @@ constexpr int decode_min_blocks() {
 }
 
 // Stage x for one (block, token) entry in the block format's fragment order:
-// the fragments, the negated bias (cs[n]) and, for Q4_1, the x sum (sx[n]);
+// the fragments, the negated bias (cs[n]) and, for Q4_1 / Q4_K, the x sum (sx[n]);
 // the padding column of an odd token count is zeroed with the last token.
 template <int F>
 __device__ __forceinline__ void stage_entry(const float (&xv)[32], uint4* dst, float* cs, float* sx, int n, int Nt,
                                             int parity) {
   if constexpr (F == GQ_TYPE_Q4_1) {
     cs[n] = stage_block_q41(xv, dst, &sx[n]);
+    if ((Nt & 1) && n == Nt - 1) sx[Nt] = 0.f;
+  } else if constexpr (F == GQ_TYPE_Q4_K) {
+    cs[n] = stage_block_q4k(xv, dst, &sx[n], parity);  // parity: odd sub-block of its super-block
     if ((Nt & 1) && n == Nt - 1) sx[Nt] = 0.f;
   } else if constexpr (F == GQ_TYPE_Q8_0) {
     cs[n] = stage_block_q80(xv, dst);
@@ -313,7 +362,7 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
     k_decode_q4_0(const __grid_constant__ CUtensorMap tmW, const float* __restrict__ X, int N, int M, int K,
                   int KX, float* __restrict__ Y, uint64_t limit_ns, uint32_t* err, int early_stages,
                   int x_static, const MoeRoute rt, int drop) {
-  static_assert(F == GQ_TYPE_Q4_0 || !MOE, "Q4_1 / Q8_0 run the plain MUL_MAT layout");
+  static_assert(F == GQ_TYPE_Q4_0 || !MOE, "Q4_1 / Q8_0 / Q4_K run the plain MUL_MAT layout");
   using Cfg = DecodeCfg<NT, MT, KW, STAGES, F>;
   constexpr int kBM = Cfg::kBM;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -377,8 +426,11 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
 
   if (warp == KW) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmW);
+    // The whole warp runs the loop and one elected lane issues: a converged
+    // warp issues TMA faster than a lone lane of a diverged one.
+    {
+      const bool issuer = elect_one();
+      if (issuer) tma_prefetch_desc(&tmW);
       // With early_stages > 0 the first stages of W stream before the previous
       // kernel finishes; the rest waits until x is staged, so that the x loads
       // right after the dependency do not queue behind a ring full of W.
@@ -400,12 +452,13 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
             const uint32_t ph = (q / STAGES) & 1;
             if (!x_waited && q >= static_cast<uint32_t>(early_stages)) {
               x_waited = true;
-              if (!mbar_wait_bounded(smem_u32(x_ready), 0, limit_ns, abort_flag, err)) {
+              if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(x_ready), 0, limit_ns, abort_flag, err))) {
                 ok = false;
                 break;
               }
             }
-            if (!mbar_wait_bounded(smem_u32(&bars[STAGES + slot]), ph ^ 1, limit_ns, abort_flag, err)) {
+            if (!__all_sync(0xFFFFFFFFu,
+                            mbar_wait_bounded(smem_u32(&bars[STAGES + slot]), ph ^ 1, limit_ns, abort_flag, err))) {
               ok = false;
               break;
             }
@@ -415,16 +468,19 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
             const int k0 = kc0 + st * Cfg::kStageK;
             const int nvalid = min(KW, (kend - k0 + kSubK - 1) / kSubK);
             const uint32_t full = smem_u32(&bars[slot]);
-            mbar_arrive_expect_tx(full, nvalid * Cfg::kSubBytes);
-            for (int j = 0; j < nvalid; ++j) {
-              const int xb = ((k0 + j * kSubK) / kSubK) * (Cfg::kRowBytes / Cfg::kElem);  // element column
-              tma_load_2d(smem_u32(ring + slot * Cfg::kStageBytes + j * Cfg::kSubBytes), &tmW, xb,
-                          wrow0 + tile * kBM, full);
+            if (issuer) {
+              mbar_arrive_expect_tx(full, nvalid * Cfg::kSubBytes);
+              for (int j = 0; j < nvalid; ++j) {
+                const int xb = ((k0 + j * kSubK) / kSubK) * (Cfg::kRowBytes / Cfg::kElem);  // element column
+                tma_load_2d(smem_u32(ring + slot * Cfg::kStageBytes + j * Cfg::kSubBytes), &tmW, xb,
+                            wrow0 + tile * kBM, full);
+              }
             }
+            __syncwarp();
           }
         }
       }
-      if (!ok) {
+      if (!ok && issuer) {
         // Let copies already issued land before the CTA can exit.
         for (uint32_t i = 0; i < STAGES && i < q; ++i) {
           const uint32_t qq = q - 1 - i;
@@ -511,7 +567,7 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
         dst[0] = dst[1] = dst[2] = dst[3] = make_uint4(0u, 0u, 0u, 0u);
         cs[bl * csn + n] = 0.f;
         if ((Nt & 1) && n == Nt - 1) cs[bl * csn + Nt] = 0.f;
-        if (F == GQ_TYPE_Q4_1) {
+        if (Cfg::kTables == 2) {
           sxs[bl * csn + n] = 0.f;
           if ((Nt & 1) && n == Nt - 1) sxs[bl * csn + Nt] = 0.f;
         }
@@ -564,20 +620,48 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
           const float* csp = cs + bl0 * csn + 2 * t;         // + block * csn + nt * 8
           const uint4* xs1 = xs + bl0 * 4 + t;               // N = 1: token 0, slot t
           const float* cs1 = cs + bl0 * csn;                 // N = 1: token 0's bias
-          const float* sxp = sxs + bl0 * csn + 2 * t;        // Q4_1: x sums, like csp
-          const float* sx1 = sxs + bl0 * csn;                // Q4_1, N = 1
+          const float* sxp = sxs + bl0 * csn + 2 * t;        // Q4_1 / Q4_K: x sums, like csp
+          const float* sx1 = sxs + bl0 * csn;                // Q4_1 / Q4_K, N = 1
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
             uint32_t wd[MT][2][2];  // [m-tile][row g / g+8][even / odd block] code words
             [[maybe_unused]] uint32_t wh[MT][2][2];  // Q8_0: the code word of the block's second half
             float dd[MT][2][2];     // scales
-            float mm[MT][2][2];     // Q4_1 min offsets
+            float mm[MT][2][2];     // Q4_1 / Q4_K min offsets
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
               for (int r = 0; r < 2; ++r) {
                 const uint8_t* rb = sub + (mt * 16 + 8 * r) * Cfg::kRowBytes;
-                if constexpr (F == GQ_TYPE_Q4_1) {
+                if constexpr (F == GQ_TYPE_Q4_K) {
+                  // One 144-byte super-block per box row: sub-blocks 2p (low
+                  // nibbles) and 2p+1 (high nibbles) of code bytes 32p .. 32p+31;
+                  // a lane takes code words t and t + 4 of them.  w = d*sc*q -
+                  // dmin*m: scale d*sc (exact in fp32), min offset -dmin*m.
+                  const uint32_t* hw = reinterpret_cast<const uint32_t*>(rb);
+                  const uint32_t H = hw[0], F0 = hw[1], F1 = hw[2], F2 = hw[3];
+                  wd[mt][r][0] = wd[mt][r][1] = hw[4 + 8 * p + t];
+                  wh[mt][r][0] = wh[mt][r][1] = hw[8 + 8 * p + t];
+                  const float d = half_lo(H), dmin = half_hi(H);
+                  uint32_t sc0, m0, sc1, m1;
+                  if (p == 0) {
+                    q4k_scale_min<0>(F0, F1, F2, sc0, m0);
+                    q4k_scale_min<1>(F0, F1, F2, sc1, m1);
+                  } else if (p == 1) {
+                    q4k_scale_min<2>(F0, F1, F2, sc0, m0);
+                    q4k_scale_min<3>(F0, F1, F2, sc1, m1);
+                  } else if (p == 2) {
+                    q4k_scale_min<4>(F0, F1, F2, sc0, m0);
+                    q4k_scale_min<5>(F0, F1, F2, sc1, m1);
+                  } else {
+                    q4k_scale_min<6>(F0, F1, F2, sc0, m0);
+                    q4k_scale_min<7>(F0, F1, F2, sc1, m1);
+                  }
+                  dd[mt][r][0] = d * static_cast<float>(sc0);
+                  dd[mt][r][1] = d * static_cast<float>(sc1);
+                  mm[mt][r][0] = -(dmin * static_cast<float>(m0));
+                  mm[mt][r][1] = -(dmin * static_cast<float>(m1));
+                } else if constexpr (F == GQ_TYPE_Q4_1) {
                   // 20-byte blocks: word 0 = d | m << 16, words 1..4 the codes
 #pragma unroll
                   for (int e = 0; e < 2; ++e) {
@@ -620,21 +704,21 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
               const int b = 2 * p + e;
               uint4 xf[NT];
               float2 nb[NT];
-              float2 sxv[NT];  // Q4_1: the columns' x sums of this block
+              float2 sxv[NT];  // Q4_1 / Q4_K: the columns' x sums of this block
               if (ONE) {
                 // N = 1: every lane takes token 0's fragment (columns 1..7 then
                 // repeat column 0 and are never stored) and its bias.
                 xf[0] = xs1[b * 4];
                 const float bias = cs1[b * 2];  // stride of the bias table for N = 1
                 nb[0] = make_float2(bias, 0.f);
-                sxv[0] = make_float2(F == GQ_TYPE_Q4_1 ? sx1[b * 2] : 0.f, 0.f);
+                sxv[0] = make_float2(Cfg::kTables == 2 ? sx1[b * 2] : 0.f, 0.f);
               } else {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                   xf[nt] = (nt * 8 + g < Nt) ? xsp[b * 4 * N + nt * 32] : make_uint4(0u, 0u, 0u, 0u);
                   nb[nt] = (nt * 8 + 2 * t < Nt) ? *reinterpret_cast<const float2*>(csp + b * csn + nt * 8)
                                                  : make_float2(0.f, 0.f);
-                  sxv[nt] = (F == GQ_TYPE_Q4_1 && nt * 8 + 2 * t < Nt)
+                  sxv[nt] = (Cfg::kTables == 2 && nt * 8 + 2 * t < Nt)
                                 ? *reinterpret_cast<const float2*>(sxp + b * csn + nt * 8)
                                 : make_float2(0.f, 0.f);
                 }
@@ -642,7 +726,13 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
 #pragma unroll
               for (int mt = 0; mt < MT; ++mt) {
                 uint32_t a_lo[4], a_hi[4];
-                if constexpr (F == GQ_TYPE_Q8_0) {
+                if constexpr (F == GQ_TYPE_Q4_K) {
+                  // sub-block 2p + e: code bytes 0-15 (word wd) then 16-31 (word wh)
+                  codes_half_f16(wd[mt][0][e], e, a_lo[0], a_lo[2]);
+                  codes_half_f16(wd[mt][1][e], e, a_lo[1], a_lo[3]);
+                  codes_half_f16(wh[mt][0][e], e, a_hi[0], a_hi[2]);
+                  codes_half_f16(wh[mt][1][e], e, a_hi[1], a_hi[3]);
+                } else if constexpr (F == GQ_TYPE_Q8_0) {
                   q8_to_f16(wd[mt][0][e], a_lo[0], a_lo[2]);
                   q8_to_f16(wd[mt][1][e], a_lo[1], a_lo[3]);
                   q8_to_f16(wh[mt][0][e], a_hi[0], a_hi[2]);
@@ -657,7 +747,7 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
                   const float init[4] = {nb[nt].x, nb[nt].y, nb[nt].x, nb[nt].y};
                   mma_m16n8k16_f16(tsum, a_lo, xf[nt].x, xf[nt].y, init);
                   mma_m16n8k16_f16(tsum, a_hi, xf[nt].z, xf[nt].w, tsum);
-                  if constexpr (F == GQ_TYPE_Q4_1) {
+                  if constexpr (Cfg::kTables == 2) {
                     // sum (d q + m) x = d * sum(q x) + m * sum(x)
                     acc[mt][nt][0] = fmaf(mm[mt][0][e], sxv[nt].x, fmaf(dd[mt][0][e], tsum[0], acc[mt][nt][0]));
                     acc[mt][nt][2] = fmaf(mm[mt][1][e], sxv[nt].x, fmaf(dd[mt][1][e], tsum[2], acc[mt][nt][2]));
@@ -952,6 +1042,9 @@ cudaError_t launch_decode_fmt_n(const CUtensorMap* tmW, const float* X, int64_t 
 
 cudaError_t launch_decode_legacy(int type, const CUtensorMap* tmW, const float* X, int64_t N, int64_t M, int64_t K,
                                  float* Y, uint64_t wait_limit_ns, int early_w, int pdl, cudaStream_t s) {
+  if (type == GQ_TYPE_Q4_K)
+    return N == 1 ? launch_decode_fmt<GQ_TYPE_Q4_K>(tmW, X, M, K, Y, wait_limit_ns, early_w, pdl, s)
+                  : launch_decode_fmt_n<GQ_TYPE_Q4_K>(tmW, X, N, M, K, Y, wait_limit_ns, early_w, pdl, s);
   if (type == GQ_TYPE_Q8_0)
     return N == 1 ? launch_decode_fmt<GQ_TYPE_Q8_0>(tmW, X, M, K, Y, wait_limit_ns, early_w, pdl, s)
                   : launch_decode_fmt_n<GQ_TYPE_Q8_0>(tmW, X, N, M, K, Y, wait_limit_ns, early_w, pdl, s);

@@ -127,7 +127,9 @@ cudaError_t launch_decode_moe(const CUtensorMap* tmW, const float* X, int cap, i
                               cudaStream_t s);
 
 // ---- KL: Q4_1 / Q8_0 dequantisation and MUL_MAT (gq_legacy.cu)
-int type_block_bytes(int type);  // 18 / 20 / 34, 0 for an unknown type
+int type_block_bytes(int type);    // bytes per block: 18 / 20 / 34 / 144 (Q4_K), 0 for an unknown type
+int type_block_weights(int type);  // weights per block: 32, or 256 for Q4_K
+uint64_t type_row_bytes(int type, int64_t K);  // bytes of a row of K weights; 0 unless K % block weights == 0
 cudaError_t launch_dequant_legacy(int type, const uint8_t* W, int64_t nblocks, float* out, cudaStream_t s);
 
 // ---- KV: row-data validation (gq_validate.cu).  result[0] = blocks with a
@@ -137,6 +139,11 @@ cudaError_t launch_validate(const uint8_t* W, int64_t nblocks, int type, unsigne
                             cudaStream_t s);
 cudaError_t launch_mul_mat_legacy(int type, const uint8_t* W, int64_t M, int64_t K, const float* X, int64_t N,
                                   float* Y, uint64_t wait_limit_ns, cudaStream_t s);
+
+// ---- KK: Q4_K dequantisation (bit-exact) and the any-alignment MUL_MAT (gq_kquant.cu)
+cudaError_t launch_dequant_q4_k(const uint8_t* W, int64_t nsuper, float* out, cudaStream_t s);
+cudaError_t launch_mul_mat_q4_k(const uint8_t* W, int64_t M, int64_t K, const float* X, int64_t N, float* Y,
+                                cudaStream_t s);
 
 // ---- KP: Q4_0 repack into rows of a multiple of 256 weights (gq_prepare.cu)
 int64_t prepared_row_bytes(int64_t K);  // ceil(K / 256) * 144

@@ -404,8 +404,17 @@ int type_block_bytes(int type) {
     case GQ_TYPE_Q4_0: return kBlockBytes;
     case GQ_TYPE_Q4_1: return Fmt<GQ_TYPE_Q4_1>::kBytes;
     case GQ_TYPE_Q8_0: return Fmt<GQ_TYPE_Q8_0>::kBytes;
+    case GQ_TYPE_Q4_K: return 144;
   }
   return 0;
+}
+
+int type_block_weights(int type) { return type == GQ_TYPE_Q4_K ? 256 : kQK; }
+
+uint64_t type_row_bytes(int type, int64_t K) {
+  const int bw = type_block_weights(type);
+  if (K < 0 || K % bw) return 0;
+  return static_cast<uint64_t>(K / bw) * static_cast<uint64_t>(type_block_bytes(type));
 }
 
 cudaError_t launch_dequant_legacy(int type, const uint8_t* W, int64_t nblocks, float* out, cudaStream_t s) {

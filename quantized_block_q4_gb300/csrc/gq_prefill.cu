@@ -43,6 +43,7 @@
 
 #include "gq_internal.h"
 #include "gq_ptx.cuh"
+#include "gq_q4k.cuh"
 
 namespace gq {
 namespace {
@@ -103,9 +104,12 @@ cudaError_t launch_f32_to_bf16(const float* x, uint16_t* y, int64_t n, cudaStrea
 namespace {
 
 // F: block format of W (GQ_TYPE_*).  Q4_0 blocks are 18 bytes, Q4_1 20,
-// Q8_0 34; a raw stage holds 8 blocks (256 k) of each of the 128 rows.
+// Q8_0 34; a raw stage holds 8 blocks (256 k) of each of the 128 rows.  A Q4_K
+// super-block is itself 256 k in 144 bytes (18 bytes per 32 weights).
 template <int F>
-constexpr int fmt_block_bytes() { return F == GQ_TYPE_Q4_0 ? 18 : (F == GQ_TYPE_Q4_1 ? 20 : 34); }
+constexpr int fmt_block_bytes() {
+  return (F == GQ_TYPE_Q4_0 || F == GQ_TYPE_Q4_K) ? 18 : (F == GQ_TYPE_Q4_1 ? 20 : 34);
+}
 
 template <int BN, bool PAIR, int F = GQ_TYPE_Q4_0>
 struct PrefillCfg {
@@ -124,7 +128,7 @@ struct PrefillCfg {
   // an x tile in shared memory; the accumulator takes the first BN columns.
   // The larger raw stages of Q4_1 / Q8_0 leave room for fewer x stages.
   static constexpr int RS = F == GQ_TYPE_Q8_0 ? 2 : 3;
-  static constexpr int S = PAIR ? 8 : (BN == 256 ? (F == GQ_TYPE_Q4_0 ? 5 : 4) : 8);
+  static constexpr int S = PAIR ? 8 : (BN == 256 ? (kRawRow == 144 ? 5 : 4) : 8);
   static_assert(BN + S * kACols <= 512, "TMEM holds the accumulator and the A stages");
   // Step c of the ring goes to stage c mod S and is written by dequant group
   // c mod 4, which waits on the stage's "empty" barrier by phase parity.  With
@@ -136,7 +140,8 @@ struct PrefillCfg {
   static_assert(S >= 4, "an A/x stage ring shorter than the four dequant groups lets a parity wait pass early");
   static constexpr int kTmemCols = 512;
   static constexpr int kRawBytes = kBM * kRawRow;  // 18432 for Q4_0
-  // 16-byte words a dequantising thread loads to cover its two blocks
+  // 16-byte words a dequantising thread loads to cover its two blocks (Q4_K:
+  // the super-block's 16-byte header and the 32 code bytes of its step)
   static constexpr int kWinWords = F == GQ_TYPE_Q8_0 ? 5 : 3;
   static constexpr int kBBytes = kXRows * 128;
   static constexpr int kOffB = 0;
@@ -343,11 +348,44 @@ __device__ __forceinline__ void q80_block(uint32_t d_bits, const uint32_t (&c)[8
   }
 }
 
+// Q4_K step G of a super-block row: sub-blocks 2G (the low nibbles of code
+// bytes 32G .. 32G+31, k 0..31 of the step) and 2G+1 (their high nibbles, k
+// 32..63).  v[0..3]: the header (d | dmin << 16 and the field words F0, F1,
+// F2); v[4..11]: the 32 code bytes.  Elements in fp32 (d*sc*q exact, the min
+// subtracted with one rounding), then rounded to bf16 in pairs.
+template <int G>
+__device__ __forceinline__ void q4k_step_words(const uint32_t* v, uint32_t* o) {
+  const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(v[0] & 0xFFFF)));
+  const float dmin = __half2float(__ushort_as_half(static_cast<uint16_t>(v[0] >> 16)));
+  uint32_t sc0, m0, sc1, m1;
+  q4k_scale_min<2 * G>(v[1], v[2], v[3], sc0, m0);
+  q4k_scale_min<2 * G + 1>(v[1], v[2], v[3], sc1, m1);
+  const float d0 = d * static_cast<float>(sc0), mn0 = dmin * static_cast<float>(m0);
+  const float d1 = d * static_cast<float>(sc1), mn1 = dmin * static_cast<float>(m1);
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const uint32_t c = v[4 + w];  // code bytes 4w .. 4w+3
+    float lo[4], hi[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      lo[j] = __fmaf_rn(d0, code_f((c >> (8 * j)) & 0xF), -mn0);
+      hi[j] = __fmaf_rn(d1, code_f((c >> (8 * j + 4)) & 0xF), -mn1);
+    }
+    o[2 * w] = pack_bf16(lo[0], lo[1]);
+    o[2 * w + 1] = pack_bf16(lo[2], lo[3]);
+    o[16 + 2 * w] = pack_bf16(hi[0], hi[1]);
+    o[16 + 2 * w + 1] = pack_bf16(hi[2], hi[3]);
+  }
+}
+
 // Group G's two blocks of a 256-k chunk row from the loaded window v (the
-// 16-byte words from byte (2*G*block bytes) & ~15 of the row).
+// 16-byte words from byte (2*G*block bytes) & ~15 of the row; for Q4_K the
+// header and the step's code bytes).
 template <int F, int G>
 __device__ __forceinline__ void step_words_fmt(const uint32_t* v, uint32_t* o) {
-  if constexpr (F == GQ_TYPE_Q4_1) {
+  if constexpr (F == GQ_TYPE_Q4_K) {
+    q4k_step_words<G>(v, o);
+  } else if constexpr (F == GQ_TYPE_Q4_1) {
     constexpr int w0 = (40 * G % 16) / 4;  // 0, 2, 0, 2
     const uint32_t c0[4] = {v[w0 + 1], v[w0 + 2], v[w0 + 3], v[w0 + 4]};
     const uint32_t c1[4] = {v[w0 + 6], v[w0 + 7], v[w0 + 8], v[w0 + 9]};
@@ -640,7 +678,8 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
     const int cb0 = grp * kCbPerGrp, cb1 = cb0 + kCbPerGrp;
     // This group's two blocks of a raw row start at byte 2*grp*kBlk: read the
     // 16-byte words that cover them (for Q4_0 the 36 bytes start at word grp).
-    const int raw_off = row * C::kRawRow + (2 * C::kBlk * grp & ~15);
+    // Q4_K: the row's 16-byte header, then the step's 32 code bytes at 16 + 32*grp.
+    const int raw_off = F == GQ_TYPE_Q4_K ? row * C::kRawRow : row * C::kRawRow + (2 * C::kBlk * grp & ~15);
     bool live = true;
     uint32_t cr = 0, c = 0, seg = 0;
     for (int i = 0; i < nseg; ++i) {
@@ -663,7 +702,8 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
           const uint4* src = reinterpret_cast<const uint4*>(smem + C::kOffRaw + rslot * C::kRawBytes + raw_off);
 #pragma unroll
           for (int i = 0; i < C::kWinWords; ++i) {
-            const uint4 x = src[i];
+            // Q4_K: word 0 is the header, words 1-2 the code bytes at 16 + 32*grp
+            const uint4 x = src[(F == GQ_TYPE_Q4_K && i > 0) ? i + 2 * grp : i];
             v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
           }
         }
@@ -956,7 +996,7 @@ int get_prefill_bn_override() { return g_bn_override; }
 
 void prefill_boxes(int64_t N, int type, uint32_t* w_box_x, uint32_t* w_elem_bytes, uint32_t* w_box_rows,
                    uint32_t* x_box_k, uint32_t* x_box_rows) {
-  const uint32_t raw_row = 8u * static_cast<uint32_t>(type_block_bytes(type));
+  const uint32_t raw_row = static_cast<uint32_t>(type_row_bytes(type, 256));  // 256 k of a row
   *w_elem_bytes = raw_row > 256 ? 2u : 1u;
   *w_box_x = raw_row / *w_elem_bytes;
   *w_box_rows = 128;
@@ -1016,6 +1056,11 @@ cudaError_t launch_prefill(const CUtensorMap* tmW, const CUtensorMap* tmX, int64
     if (prefill_bn(N) == 128)
       return launch_prefill_cfg<128, false, GQ_TYPE_Q8_0>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
     return launch_prefill_cfg<256, false, GQ_TYPE_Q8_0>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
+  }
+  if (type == GQ_TYPE_Q4_K) {
+    if (prefill_bn(N) == 128)
+      return launch_prefill_cfg<128, false, GQ_TYPE_Q4_K>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
+    return launch_prefill_cfg<256, false, GQ_TYPE_Q4_K>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
   }
   if (use_pair(N)) return launch_prefill_cfg<256, true>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
   if (prefill_bn(N) == 128) return launch_prefill_cfg<128, false>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
