@@ -393,7 +393,7 @@ def run_gpu(args, rank, world, dist):
     aux = run_aux(gq, torch, dev, s, peaks["hbm_gbs"]) if rank == 0 else {}
     if rank == 0:
         aux["mul_mat_id"] = run_moe_aux(gq, torch, dev, s, peaks)
-        aux["legacy_formats"] = run_legacy_aux(gq, torch, dev, s, peaks)
+        aux["block_formats"] = run_formats_aux(gq, torch, dev, s, peaks)
         aux["prepared_layout"] = run_prepared_aux(gq, torch, dev, s, peaks)
         aux["library_reference"] = run_library_reference(gq, torch, dev, s, peaks)
     if rank == 0:
@@ -466,7 +466,7 @@ def run_gpu(args, rank, world, dist):
         "quantize": aux.get("quantize"),
         "validate": aux.get("validate"),
         "mul_mat_id": aux.get("mul_mat_id"),
-        "legacy_formats": aux.get("legacy_formats"),
+        "block_formats": aux.get("block_formats"),
         "prepared_layout": aux.get("prepared_layout"),
         "library_reference": aux.get("library_reference"),
         "gpu_launches": K_ * (len(shapes) + len(shapes) + L * len(ks)),
@@ -778,16 +778,17 @@ def run_moe_aux(gq, torch, dev, s, peaks):
     return out
 
 
-def run_legacy_aux(gq, torch, dev, s, peaks):
-    """Q4_1 and Q8_0 on the 14336 x 4096 matrix: dequant (GB/s), MUL_MAT at
-    N = 1 (weight GB/s) and N = 512 (TFLOP/s), CUDA events over repeated calls
-    on rotating weight copies (each copy streamed from DRAM)."""
+def run_formats_aux(gq, torch, dev, s, peaks):
+    """Q4_1, Q8_0 and Q4_K on the 14336 x 4096 matrix: dequant (GB/s), MUL_MAT
+    at N = 1 (weight GB/s) and N = 512 (TFLOP/s), CUDA events over repeated
+    calls on 8 rotating weight copies (264 MB and more together, so each call
+    streams its copy from DRAM)."""
     M, K = MOE_M, MOE_K
     out = {}
-    for name, qt in (("q4_1", gq.GQ_TYPE_Q4_1), ("q8_0", gq.GQ_TYPE_Q8_0)):
+    for name, qt in (("q4_1", gq.GQ_TYPE_Q4_1), ("q8_0", gq.GQ_TYPE_Q8_0), ("q4_k", gq.GQ_TYPE_Q4_K)):
         nbytes = gq.gq_type_nbytes(qt, M, K)
         W0 = torch.from_numpy(synth.typed_weights(qt, M, K, seed=0x7E00 + qt)).to(dev)
-        Ws = [W0.clone() for _ in range(3)]
+        Ws = [W0.clone() for _ in range(8)]
         D = torch.empty(M, K, device=dev)
         X1 = torch.randn(1, K, device=dev)
         XP = torch.randn(512, K, device=dev)
@@ -806,20 +807,22 @@ def run_legacy_aux(gq, torch, dev, s, peaks):
             e1.synchronize()
             return e0.elapsed_time(e1) / reps * 1e-3
 
-        td = timed(lambda i: gq.gq_dequant(qt, Ws[i % 3], M, K, D, stream=s))
-        t1 = timed(lambda i: gq.gq_mul_mat(qt, Ws[i % 3], M, K, X1, 1, Y1, stream=s))
-        tp = timed(lambda i: gq.gq_mul_mat(qt, Ws[i % 3], M, K, XP, 512, YP, stream=s))
+        td = timed(lambda i: gq.gq_dequant(qt, Ws[i % 8], M, K, D, stream=s))
+        t1 = timed(lambda i: gq.gq_mul_mat(qt, Ws[i % 8], M, K, X1, 1, Y1, stream=s), reps=16)
+        tp = timed(lambda i: gq.gq_mul_mat(qt, Ws[i % 8], M, K, XP, 512, YP, stream=s))
         gq.gq_sync_status(s)
         dq = (nbytes + 4 * M * K) / td / 1e9
         g1 = (nbytes + 4 * K + 4 * M) / t1 / 1e9
         tf = 2 * M * K * 512 / tp / 1e12
         out[name] = {
             "shape": f"{M}x{K}", "block_bytes": gq.TYPE_BLOCK_BYTES[qt],
+            "block_weights": gq.TYPE_BLOCK_WEIGHTS[qt],
             "dequant": {"us": round(td * 1e6, 2), "achieved": round(dq, 1), "unit": "GB/s", "bound": "hbm",
                         "frac": round(dq / peaks["hbm_gbs"], 4)},
             "mul_mat_n1": {"us": round(t1 * 1e6, 2), "achieved": round(g1, 1), "unit": "GB/s", "bound": "hbm",
                            "frac": round(g1 / peaks["hbm_gbs"], 4),
-                           "kernel": "k_decode_q4_0<..., type> (mma.sync decode on this block format)"},
+                           "kernel": "k_decode_q4_0<..., type> (mma.sync decode on this block format)",
+                           "timing": "eager back-to-back calls (launch gaps included)"},
             "mul_mat_n512": {"us": round(tp * 1e6, 2), "achieved": round(tf, 2), "unit": "TFLOP/s",
                              "bound": "tensor", "frac": round(tf / peaks["bf16_tflops"], 4),
                              "kernel": "k_f32_to_bf16 + k_prefill_q4_0<256, 0, 0, type>"},
@@ -949,6 +952,9 @@ PROFILE_CASES = {
     "moe_decode": (MOE_M, MOE_K, 1, "moe"),
     "q4_1_decode": (14336, 4096, 1, "q4_1"),
     "q8_0_decode": (14336, 4096, 1, "q8_0"),
+    "q4_k_decode": (14336, 4096, 1, "q4_k"),
+    "q4_k_prefill": (14336, 4096, 512, "q4_k"),
+    "q4_k_dequant": (14336, 4096, 0, "q4_k"),
     "quantize": (14336, 4096, 0, "quantize"),
 }
 
@@ -972,13 +978,17 @@ def run_profile_case(name, pair=False):
         gq.gq_sync_status()
         print(f"profile case {name}: {MOE_E} experts {M}x{K}, {N} tokens x {MOE_S} ok")
         return 0
-    if mode in ("q4_1", "q8_0"):  # the decode kernel on the other block formats
-        qt = gq.GQ_TYPE_Q4_1 if mode == "q4_1" else gq.GQ_TYPE_Q8_0
+    if mode in ("q4_1", "q8_0", "q4_k"):  # the other block formats (N = 0: dequantisation)
+        qt = {"q4_1": gq.GQ_TYPE_Q4_1, "q8_0": gq.GQ_TYPE_Q8_0, "q4_k": gq.GQ_TYPE_Q4_K}[mode]
         W = torch.from_numpy(synth.typed_weights(qt, M, K, seed=1)).cuda()
-        X = torch.from_numpy(synth.activations(N, K, seed=2)).cuda()
-        Y = torch.empty(N, M, device="cuda")
+        X = torch.from_numpy(synth.activations(max(N, 1), K, seed=2)).cuda()
+        Y = torch.empty(max(N, 1), M, device="cuda")
+        D = torch.empty(M, K, device="cuda") if N == 0 else None
         for _ in range(2):
-            gq.gq_mul_mat(qt, W, M, K, X, N, Y)
+            if N == 0:
+                gq.gq_dequant(qt, W, M, K, D)
+            else:
+                gq.gq_mul_mat(qt, W, M, K, X, N, Y)
         torch.cuda.synchronize()
         gq.gq_sync_status()
         print(f"profile case {name}: M={M} K={K} N={N} ok")
