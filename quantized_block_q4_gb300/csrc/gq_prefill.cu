@@ -880,36 +880,57 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
 int64_t g_streamk = 1;  // 0: never split tiles; 1: split the last partial wave when it pays; n >= 2: split every tile in n
 int64_t g_slots = 0;    // 0: work ranges up to the SM count (pairs: half); n > 0: at most n ranges (test aid)
 
-constexpr int64_t kFixupUnits = 6;
 // Launch tags for the arrival counters: unique per launch in this process; the
 // start is random so that scratch memory left by another process's launches
 // cannot carry a matching tag either.
-std::atomic<unsigned long long> g_epoch{(static_cast<unsigned long long>(std::random_device{}()) << 24) + 1};  // time of a split tile's publish / reduce, in 256-k chunks
+std::atomic<unsigned long long> g_epoch{(static_cast<unsigned long long>(std::random_device{}()) << 24) + 1};
+
+// Cost model of a launch, in hundredths of the time one CTA takes for a
+// 256-k chunk of a 128 x 256 tile, fitted to this kernel's measured times on
+// the GB300 (graphs of calls on weights streamed from DRAM, 4096 to 14336
+// rows, K 4096 and 11008, N 512; each estimate within 2 %):
+//   a chunk of a 128 x 128 tile                 97  (half the MMA work; the per-step cost stays)
+//   a CTA's start and its last epilogue        570 (BN 256) / 430 (BN 128)
+//   each further tile's epilogue               520 (BN 256) / 260 (BN 128)
+//   a split tile's publish and reduce          830 + 150 per piece beyond two
+struct PlanCost {
+  int64_t chunk, start, epilogue;
+};
+constexpr PlanCost plan_cost(int bn) { return bn == 128 ? PlanCost{97, 430, 260} : PlanCost{100, 570, 520}; }
+constexpr int64_t split_fixup_cost(int64_t s) { return 830 + 150 * (s - 2); }
 
 // Schedule of T tiles of nr chunks on P ranges (PrefillWork): w = T / P whole
 // tiles per range, and the rem = T % P left over either as one more whole
-// tile for rem ranges or, when it is faster, split s = P / rem ways along k.
-void prefill_plan(int64_t T, int64_t nr, int64_t P, bool allow_split, PrefillWork* wk) {
+// tile for rem ranges or, when the cost model says it is faster, split
+// s = P / rem ways along k.  Returns the estimated cost.
+int64_t prefill_plan(int64_t T, int64_t nr, int64_t P, bool allow_split, int bn, PrefillWork* wk) {
   if (g_slots > 0) P = g_slots;
   P = std::max<int64_t>(P, 1);
+  const PlanCost c = plan_cost(bn);
   wk->T = T;
   wk->R = 0;
   wk->s = 1;
   wk->G = std::min(T, P);
-  if (!allow_split || g_streamk == 0 || nr < 2) return;
-  if (g_streamk >= 2) {  // every tile in pieces
+  const int64_t w = T / P, rem = T - w * P;
+  const int64_t waves = w + (rem ? 1 : 0);
+  const int64_t whole = waves * nr * c.chunk + c.start + (waves > 0 ? waves - 1 : 0) * c.epilogue;
+  if (!allow_split || g_streamk == 0 || nr < 2) return whole;
+  if (g_streamk >= 2) {  // every tile in pieces (test aid)
     wk->s = static_cast<int>(std::min(g_streamk, nr));
     wk->R = static_cast<int>(T);
     wk->G = T * wk->s;
-    return;
+    return whole;
   }
-  const int64_t w = T / P, rem = T - w * P;
-  if (rem == 0) return;
+  if (rem == 0) return whole;
   const int64_t s = std::min(P / rem, nr / 2);
-  if (s < 2 || w * nr + (nr + s - 1) / s + kFixupUnits >= (w + 1) * nr) return;
+  if (s < 2) return whole;
+  const int64_t split =
+      w * nr * c.chunk + (nr + s - 1) / s * c.chunk + c.start + w * c.epilogue + split_fixup_cost(s);
+  if (split >= whole) return whole;
   wk->R = static_cast<int>(rem);
   wk->s = static_cast<int>(s);
   wk->G = std::max(std::min(T, P), rem * s);
+  return split;
 }
 
 template <int BN, bool PAIR, int F = GQ_TYPE_Q4_0>
@@ -930,7 +951,7 @@ cudaError_t launch_prefill_cfg(const CUtensorMap* tmW, const CUtensorMap* tmX, i
   wk.ntn = static_cast<int>(ntn);
   wk.early_w = pdl && early_w;
   wk.drop = test_drop() == 2 ? 1 : 0;
-  prefill_plan(T, nr, device_info().sm_count / C::kCtas, allow_scratch, &wk);
+  prefill_plan(T, nr, device_info().sm_count / C::kCtas, allow_scratch, BN, &wk);
   void* scratch = nullptr;
   if (wk.R > 0) {  // split tiles: partial-tile slots and arrival counters
     const size_t ws_bytes =
@@ -980,9 +1001,18 @@ cudaError_t launch_prefill_cfg(const CUtensorMap* tmW, const CUtensorMap* tmX, i
 
 int g_bn_override = 0;  // 0: choose by shape; 128 or 256: force the tile width (tuning)
 
-int prefill_bn(int64_t N) {
+// Tile width: 128 tokens up to N = 128; beyond, whichever of 128 and 256 the
+// cost model above rates faster for this shape (e.g. 4096 x 4096 x 512: 64
+// tiles of 256 tokens leave 88 of 152 SMs idle or split tiles, 128 tiles of
+// 128 tokens do not).
+int prefill_bn(int64_t N, int64_t M, int64_t K, bool allow_split) {
   if (g_bn_override) return g_bn_override;
-  return N <= 128 ? 128 : 256;
+  if (N <= 128) return 128;
+  const int64_t P = device_info().sm_count, rows = (M + 127) / 128, nr = K / 256;
+  PrefillWork w128{}, w256{};
+  const int64_t c128 = prefill_plan(rows * ((N + 127) / 128), nr, P, allow_split, 128, &w128);
+  const int64_t c256 = prefill_plan(rows * ((N + 255) / 256), nr, P, allow_split, 256, &w256);
+  return c128 < c256 ? 128 : 256;
 }
 
 // 0 (default): 1-CTA kernel with 128 x prefill_bn tiles; 1: 2-SM pair kernel (256 x 256 tiles).
@@ -994,14 +1024,15 @@ bool use_pair(int64_t N) { return g_pair_mode && g_bn_override == 0 && N > 128; 
 void set_prefill_bn_override(int bn) { g_bn_override = bn; }
 int get_prefill_bn_override() { return g_bn_override; }
 
-void prefill_boxes(int64_t N, int type, uint32_t* w_box_x, uint32_t* w_elem_bytes, uint32_t* w_box_rows,
-                   uint32_t* x_box_k, uint32_t* x_box_rows) {
+void prefill_boxes(int64_t N, int64_t M, int64_t K, bool allow_split, int type, uint32_t* w_box_x,
+                   uint32_t* w_elem_bytes, uint32_t* w_box_rows, uint32_t* x_box_k, uint32_t* x_box_rows) {
   const uint32_t raw_row = static_cast<uint32_t>(type_row_bytes(type, 256));  // 256 k of a row
   *w_elem_bytes = raw_row > 256 ? 2u : 1u;
   *w_box_x = raw_row / *w_elem_bytes;
   *w_box_rows = 128;
   *x_box_k = 64;
-  *x_box_rows = (type == GQ_TYPE_Q4_0 && use_pair(N)) ? 128u : static_cast<uint32_t>(prefill_bn(N));
+  *x_box_rows = (type == GQ_TYPE_Q4_0 && use_pair(N)) ? 128u
+                                                        : static_cast<uint32_t>(prefill_bn(N, M, K, allow_split));
 }
 
 void set_prefill_pair_mode(int on) { g_pair_mode = on ? 1 : 0; }
@@ -1048,22 +1079,22 @@ cudaError_t launch_prefill(const CUtensorMap* tmW, const CUtensorMap* tmX, int64
                            int type) {
   const int n = static_cast<int>(N), m = static_cast<int>(M), k = static_cast<int>(K);
   if (type == GQ_TYPE_Q4_1) {
-    if (prefill_bn(N) == 128)
+    if (prefill_bn(N, M, K, allow_scratch) == 128)
       return launch_prefill_cfg<128, false, GQ_TYPE_Q4_1>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
     return launch_prefill_cfg<256, false, GQ_TYPE_Q4_1>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
   }
   if (type == GQ_TYPE_Q8_0) {
-    if (prefill_bn(N) == 128)
+    if (prefill_bn(N, M, K, allow_scratch) == 128)
       return launch_prefill_cfg<128, false, GQ_TYPE_Q8_0>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
     return launch_prefill_cfg<256, false, GQ_TYPE_Q8_0>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
   }
   if (type == GQ_TYPE_Q4_K) {
-    if (prefill_bn(N) == 128)
+    if (prefill_bn(N, M, K, allow_scratch) == 128)
       return launch_prefill_cfg<128, false, GQ_TYPE_Q4_K>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
     return launch_prefill_cfg<256, false, GQ_TYPE_Q4_K>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
   }
   if (use_pair(N)) return launch_prefill_cfg<256, true>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
-  if (prefill_bn(N) == 128) return launch_prefill_cfg<128, false>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
+  if (prefill_bn(N, M, K, allow_scratch) == 128) return launch_prefill_cfg<128, false>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
   return launch_prefill_cfg<256, false>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
 }
 

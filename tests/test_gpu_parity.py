@@ -330,17 +330,21 @@ def test_prefill_whole_tiles_only_matches_oracle():
     _with_option(gq.GQ_OPT_PREFILL_STREAMK, 0, lambda: check_mm(640, 2048, 513, 5400, "whole tiles"))
 
 
+@pytest.mark.parametrize("tile_n", [0, 128, 256])
 @pytest.mark.parametrize("M,K", [(4096, 4096), (4096, 11008), (11008, 4096)])
-def test_prefill_full_size_split_sampled_rows(M, K):
-    """Full-size shapes whose last wave of tiles is split along k by default.
+def test_prefill_full_size_split_sampled_rows(M, K, tile_n):
+    """The sweep's N = 512 shapes under the planner's own choice (tile_n = 0:
+    4096 x 4096 in 128-token tiles, 11008 x 4096 in two waves of whole tiles,
+    4096 x 11008 split in two along k) and with each tile width forced (at 256
+    tokens 4096 x 4096 has 64 tiles, which the planner may split along k).
     Sampled rows against the oracle."""
     N = 512
     W = synth.q4_0_weights(M, K, seed=synth.seed_for(5, M + K))
     X = synth.activations(N, K, seed=synth.seed_for(5, M + K + 1))
-    y = run_mm(W, X, M, K)
+    y = _with_option(gq.GQ_OPT_PREFILL_TILE_N, tile_n, lambda: run_mm(W, X, M, K))
     rows = sampled_rows(M, 128, 43)
     y_ref, s_ref = oracle_mul_mat(W.reshape(M, -1)[rows], len(rows), K, X)
-    assert_mul_mat_close(y[:, rows], y_ref, s_ref, f"split {M}x{K}")
+    assert_mul_mat_close(y[:, rows], y_ref, s_ref, f"{M}x{K} tile_n={tile_n}")
 
 
 def test_f32_to_bf16_matches_torch_rounding():
