@@ -73,8 +73,45 @@ __device__ __forceinline__ void q4k_part(const uint8_t* __restrict__ blk, int i,
 
 constexpr int kDqThreads = 256;
 
-// One thread per 8 weights: 32 threads per super-block, consecutive threads
-// writing consecutive 32-byte runs of the output.
+// Weights 4q .. 4q+3 of a 16-byte aligned super-block (q = 0..63): chunk c =
+// q / 16, sub-block 2c (q % 16 < 8, low nibbles) or 2c + 1 (high nibbles),
+// code bytes 32c + 4 (q % 8) .. + 3.
+__device__ __forceinline__ float4 q4k_quad(const uint8_t* __restrict__ blk, uint4 h, int q) {
+  const int c = q >> 4, hi = (q >> 3) & 1;
+  const uint32_t codes = __ldg(reinterpret_cast<const uint32_t*>(blk + 16 + 32 * c + 4 * (q & 7)));
+  uint32_t sc, mn;
+  q4k_scale_min_rt(h.y, h.z, h.w, 2 * c + hi, sc, mn);
+  const float d1 = half_bits(h.x) * static_cast<float>(sc);       // exact
+  const float m1 = half_bits(h.x >> 16) * static_cast<float>(mn);  // exact
+  const uint32_t v = hi ? codes >> 4 : codes;
+  float4 r;
+  r.x = __fmaf_rn(d1, static_cast<float>(v & 15), -m1);  // d1*q exact: one rounding
+  r.y = __fmaf_rn(d1, static_cast<float>((v >> 8) & 15), -m1);
+  r.z = __fmaf_rn(d1, static_cast<float>((v >> 16) & 15), -m1);
+  r.w = __fmaf_rn(d1, static_cast<float>((v >> 24) & 15), -m1);
+  return r;
+}
+
+// 16-byte aligned W and out: a warp per super-block and step, lane i writing
+// weights 4i .. 4i+3 and 128 + 4i .. 128 + 4i + 3, so that each float4 store
+// instruction covers 512 contiguous bytes (whole sectors).
+__global__ void __launch_bounds__(kDqThreads) k_dequant_q4_k_vec(const uint8_t* __restrict__ W, int64_t nsuper,
+                                                                 float* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (kDqThreads / 32);
+  for (int64_t sb = static_cast<int64_t>(blockIdx.x) * (kDqThreads / 32) + (threadIdx.x >> 5); sb < nsuper;
+       sb += warps) {
+    const uint8_t* blk = W + sb * kSuperBytes;
+    const uint4 h = __ldg(reinterpret_cast<const uint4*>(blk));  // d | dmin << 16, then the field words
+    const float4 a = q4k_quad(blk, h, lane);
+    const float4 b = q4k_quad(blk, h, 32 + lane);
+    float4* dst = reinterpret_cast<float4*>(out + sb * kSuperWeights);
+    dst[lane] = a;
+    dst[32 + lane] = b;
+  }
+}
+
+// Any alignment: one thread per 8 weights, 32 threads per super-block.
 template <bool ALIGNED, bool VEC_OUT>
 __global__ void __launch_bounds__(kDqThreads) k_dequant_q4_k(const uint8_t* __restrict__ W, int64_t nsuper,
                                                              float* __restrict__ out) {
@@ -154,9 +191,11 @@ cudaError_t launch_dequant_q4_k(const uint8_t* W, int64_t nsuper, float* out, cu
   const int grid = static_cast<int>(std::max<int64_t>(
       1, std::min<int64_t>(want, static_cast<int64_t>(device_info().sm_count) * 8)));
   const bool a = (reinterpret_cast<uintptr_t>(W) & 15) == 0, v = (reinterpret_cast<uintptr_t>(out) & 15) == 0;
-  if (a && v)
-    k_dequant_q4_k<true, true><<<grid, kDqThreads, 0, s>>>(W, nsuper, out);
-  else if (a)
+  if (a && v) {
+    const int vgrid = static_cast<int>(std::max<int64_t>(
+        1, std::min<int64_t>((nsuper + 7) / 8, static_cast<int64_t>(device_info().sm_count) * 8)));
+    k_dequant_q4_k_vec<<<vgrid, kDqThreads, 0, s>>>(W, nsuper, out);
+  } else if (a)
     k_dequant_q4_k<true, false><<<grid, kDqThreads, 0, s>>>(W, nsuper, out);
   else if (v)
     k_dequant_q4_k<false, true><<<grid, kDqThreads, 0, s>>>(W, nsuper, out);
