@@ -270,8 +270,11 @@ def run_gpu(args, rank, world, dist):
     # one event pair per layer around its run of tensor-core launches
     ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
 
-    def prefill_pass(record):
-        # activation conversion for each layer's inputs, then the tensor-core MUL_MATs
+    def prefill_pass(record, promise=True):
+        # activation conversion for each layer's inputs, then the tensor-core
+        # MUL_MATs: the first without the x-static promise (its X was converted
+        # right before), which orders the conversions before everything after
+        # it; the other six with it (their X was written before that call)
         for layer in range(L):
             for i, x in enumerate(XP[layer]):
                 gq.gq_f32_to_bf16(x, XPb[layer][i], x.numel(), stream=s)
@@ -280,7 +283,9 @@ def run_gpu(args, rank, world, dist):
             for j in range(len(order)):
                 i = layer * len(order) + j
                 M, K = shapes[i]
+                gq.gq_set_option(gq.GQ_OPT_X_STATIC, 1 if promise and j > 0 else 0)
                 gq.gq_mul_mat_q4_0_bf16x(W[i], M, K, XPb[layer][order[j]], PREFILL_N, YP[i], stream=s)
+            gq.gq_set_option(gq.GQ_OPT_X_STATIC, 1)
             if record:
                 ev_pairs[layer][1].record(s)
 
@@ -347,6 +352,16 @@ def run_gpu(args, rank, world, dist):
         k3_ms += sum(a.elapsed_time(b) for a, b in ev_pairs)
     if dist is not None:
         dist.barrier()
+    # the prefill pass with no x-static promise at all, K passes, timed alone
+    with torch.cuda.stream(s):
+        prefill_pass(False, promise=False)
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        p0.record(s)
+        for _ in range(args.steps):
+            prefill_pass(False, promise=False)
+        p1.record(s)
+    p1.synchronize()
+    pre_dep_ms = p0.elapsed_time(p1)
     # the dependent decode sweep, K steps, timed alone
     with torch.cuda.stream(s):
         for _ in range(3):
@@ -378,7 +393,8 @@ def run_gpu(args, rank, world, dist):
     dec_ms = sum(a.elapsed_time(b) for a, b, _ in marks)
     pre_ms = sum(b.elapsed_time(c) for _, b, c in marks)
     step_ms = sum(a.elapsed_time(c) for a, _, c in marks)
-    dec_ms, pre_ms, step_ms, k3_ms, dep_ms = max_over_ranks([dec_ms, pre_ms, step_ms, k3_ms, dep_ms], dist, dev)
+    dec_ms, pre_ms, step_ms, k3_ms, dep_ms, pre_dep_ms = max_over_ranks(
+        [dec_ms, pre_ms, step_ms, k3_ms, dep_ms, pre_dep_ms], dist, dev)
 
     K_ = args.steps
     value = world * wbytes * K_ / (dec_ms * 1e-3) / 1e9
@@ -440,7 +456,12 @@ def run_gpu(args, rank, world, dist):
                                            "it has finished, as in a chain where each input is the last output"},
         "prefill": {"value": round(prefill_tflops, 2), "unit": "TFLOP/s", "ms": round(pre_ms / K_, 4),
                     "includes": "fp32->bf16 activation conversion + tensor-core MUL_MAT",
-                    "launch": "eager, programmatic dependent launch between consecutive kernels"},
+                    "launch": "eager, programmatic dependent launch between consecutive kernels; per layer "
+                              "the first MUL_MAT without the x-static promise, the other six with it"},
+        "prefill_no_x_static": {"value": round(world * flops_p * K_ / (pre_dep_ms * 1e-3) / 1e12, 2),
+                                "unit": "TFLOP/s", "ms": round(pre_dep_ms / K_, 4),
+                                "promises": "weights static only: every MUL_MAT reads X after the kernel "
+                                            "before it has finished"},
         "roofline": {"kernel": "k_prefill_q4_0 (tcgen05 prefill)", "bound": "tensor",
                      "achieved": round(k3_tflops, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": round(k3_tflops / peaks["bf16_tflops"], 4), "traffic": sweep_traffic("prefill", shapes),

@@ -221,7 +221,9 @@ gq_status gq_mul_mat_q4_0_prepared(const void *Wp, int64_t M, int64_t K, const f
  * (raw bfloat16 bits).  Runs the tensor-core kernel for every N >= 1.  Its
  * only allocation is the stream-ordered partial-sum scratch of split tiles
  * (see gq_mul_mat_q4_0); if that allocation fails it runs one CTA per tile
- * instead.  Needs K % 256 == 0, W and X_bf16 16-byte aligned. */
+ * instead.  Needs K % 256 == 0, W and X_bf16 16-byte aligned.  Honours
+ * GQ_OPT_X_STATIC for X_bf16 (the call then streams W and runs its MMAs while
+ * the kernels ahead of it finish). */
 gq_status gq_mul_mat_q4_0_bf16x(const void *W, int64_t M, int64_t K, const uint16_t *X_bf16, int64_t N,
                                 float *Y, void *stream);
 
@@ -265,7 +267,8 @@ typedef enum {
                                 every variant computes the same result */
   GQ_OPT_PDL = 5,            /* 1 (default): launch kernels with programmatic dependent launch, so a
                                 kernel may start while the previous one on the stream drains; every
-                                read of X and write of Y still waits for that previous kernel */
+                                write of Y waits for that previous kernel, and so does every read of X
+                                unless GQ_OPT_X_STATIC promises otherwise */
   GQ_OPT_PREFILL_TILE_N = 6, /* tuning: token-tile width of the 1-CTA tensor-core kernel, 0 = by shape
                                 (default), 128 or 256; a non-zero value also selects the 1-CTA kernel */
   GQ_OPT_PREFILL_PAIR = 7,   /* 1: N > 128 runs the 2-SM kernel (CTA pairs, 256 x 256 tiles);
@@ -280,11 +283,16 @@ typedef enum {
   GQ_OPT_DECODE_EARLY_STAGES = 10, /* with GQ_OPT_WEIGHTS_STATIC: how many ring stages of W the decode
                                 kernel streams before the previous kernel finishes (1..64, capped by the
                                 ring, default 2); later stages wait until x is staged */
-  GQ_OPT_X_STATIC = 11,       /* 1: promise that the kernel launched right before a decode mul_mat
-                                (N below the tensor-core threshold) on the same stream does not write its X (e.g. several
-                                projections of one activation), so the kernel may read X and compute
-                                before that kernel finishes; Y is still written only after it.
-                                Default 0: X is read after the previous kernel completes */
+  GQ_OPT_X_STATIC = 11,       /* 1: promise that X was completely written before the most recent call
+                                on this stream made without the promise (e.g. several projections of
+                                one activation: the first call without it, the others with it; or
+                                activations copied in before a run of calls).  The decode kernel (N
+                                below the tensor-core threshold) and gq_mul_mat_q4_0_bf16x then read X
+                                and compute while the kernels ahead of them on the stream finish; Y
+                                (and the tensor-core kernel's k-split scratch) are written only after
+                                them.  A call without the promise reads X only after every kernel
+                                ahead of it has finished, and lets later launches start only then, so
+                                it orders everything after it.  Default 0 */
   GQ_OPT_MOE_PATH = 12,       /* gq_mul_mat_id_q4_0 kernel: 0 (default) by tokens per used expert,
                                 1 decode kernel, 2 tensor-core kernel (fast-path shapes only) */
   GQ_OPT_TEST_DROP_ARRIVE = 13 /* test aid for the timeout path, 0 (default) off: 1 = the decode kernel's

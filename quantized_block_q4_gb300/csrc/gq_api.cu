@@ -251,8 +251,11 @@ static gq_status mul_mat_decode(const void* W, int64_t M, int64_t K, const float
 
 // Kw: the width of W's rows in weights (K, or K rounded up to 256 for the
 // prepared layout; x beyond K reads as zeros through the tensor map).
+// x_static: the caller's promise (GQ_OPT_X_STATIC) about Xb; only for the
+// entry point whose Xb is the caller's (the other paths convert X right before).
 static gq_status mul_mat_prefill_bf16(const void* W, int64_t M, int64_t K, const uint16_t* Xb, int64_t N, float* Y,
-                                      bool allow_scratch, cudaStream_t s, int type = GQ_TYPE_Q4_0, int64_t Kw = 0) {
+                                      bool allow_scratch, cudaStream_t s, int type = GQ_TYPE_Q4_0, int64_t Kw = 0,
+                                      bool x_static = false) {
   CUtensorMap tmW, tmX;
   uint32_t wbx, web, wby, xbk, xbr;
   if (Kw <= 0) Kw = K;
@@ -265,7 +268,8 @@ static gq_status mul_mat_prefill_bf16(const void* W, int64_t M, int64_t K, const
                  static_cast<uint64_t>(K) * 2, xbk, xbr, CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != GQ_OK) return st;
   cudaError_t e = launch_prefill(&tmW, &tmX, N, M, Kw, Y, static_cast<uint64_t>(g_wait_limit_ns.load()), allow_scratch,
-                                 static_cast<int>(g_early_w.load()), static_cast<int>(g_pdl.load()), s, type);
+                                 static_cast<int>(g_early_w.load()), x_static ? 1 : 0, static_cast<int>(g_pdl.load()),
+                                 s, type);
   return e == cudaSuccess ? GQ_OK : cuda_fail(e, "prefill launch");
 }
 
@@ -652,7 +656,7 @@ gq_status gq_mul_mat_q4_0_bf16x(const void* W, int64_t M, int64_t K, const uint1
   if (K % 256) return fail(GQ_ERR_SHAPE, "the bf16-activation path needs K %% 256 == 0 (K=%lld)", (long long)K);
   if (!aligned(W, 16) || !aligned(X_bf16, 16) || !aligned(Y, 16))
     return fail(GQ_ERR_ALIGN, "W, X_bf16 and Y must be 16-byte aligned");
-  return mul_mat_prefill_bf16(W, M, K, X_bf16, N, Y, true, s);
+  return mul_mat_prefill_bf16(W, M, K, X_bf16, N, Y, true, s, GQ_TYPE_Q4_0, 0, get_decode_x_static() != 0);
 }
 
 gq_status gq_f32_to_bf16(const float* x, uint16_t* y, int64_t n, void* stream) {

@@ -421,7 +421,12 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
     *abort_flag = 0;
     fence_mbar_init();
   }
-  pdl_launch_dependents();
+  // The next kernel on the stream may launch once every CTA has signalled.
+  // A kernel that reads X only after the kernel before it (no x_static, or
+  // MUL_MAT_ID, which waited above) signals after that wait, so that a later
+  // x-static launch cannot start before the kernels ahead of this one are
+  // done; an x-static kernel signals at once.
+  if (MOE || x_static) pdl_launch_dependents();
   __syncthreads();
 
   if (warp == KW) {
@@ -503,7 +508,10 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
   bool live = true;  // false once a bounded wait gave up; the loops still run to keep barriers matched
   // X may come from the previous kernel (unless the caller promised it does
   // not: x_static); Y may still be read by it, so Y is written after the wait.
-  if (!x_static) pdl_wait();
+  if (!x_static) {
+    pdl_wait();
+    if (!MOE) pdl_launch_dependents();
+  }
 
   for (int gk = 0; gk < ngrp; ++gk)
   for (int c = 0; c < nchunks; ++c) {

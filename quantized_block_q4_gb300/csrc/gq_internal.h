@@ -57,7 +57,7 @@ cudaError_t launch_generic(const uint8_t* W, int64_t M, int64_t K, const float* 
 
 void set_decode_early_stages(int n);  // W stages streamed before the dependency (with WEIGHTS_STATIC)
 int get_decode_early_stages();
-void set_decode_x_static(int on);      // X is not written by the kernel right before (decode reads it early)
+void set_decode_x_static(int on);      // GQ_OPT_X_STATIC: X is not written by kernels that may still run (read early)
 int get_decode_x_static();
 
 // ---- KQ: fp32 -> Q4_0 blocks (gq_quantize.cu).  K % 32 == 0, W 4-byte aligned.
@@ -72,10 +72,11 @@ cudaError_t launch_f32_to_bf16(const float* x, uint16_t* y, int64_t n, cudaStrea
 // sums of tiles split along k (else, or if that allocation fails, whole tiles).
 // type: block format of W (GQ_TYPE_*; Q4_1 and Q8_0 run the 1-CTA kernels).
 // pdl: launch with programmatic dependent launch (every role waits for the
-// kernel before; with early_w the first raw W chunks stream before that).
+// kernel before; with early_w the first raw W chunks stream before that; with
+// x_static only Y and the k-split scratch wait for it).
 cudaError_t launch_prefill(const CUtensorMap* tmW, const CUtensorMap* tmX, int64_t N, int64_t M,
-                           int64_t K, float* Y, uint64_t wait_limit_ns, bool allow_scratch, int early_w, int pdl,
-                           cudaStream_t s, int type = GQ_TYPE_Q4_0);
+                           int64_t K, float* Y, uint64_t wait_limit_ns, bool allow_scratch, int early_w,
+                           int x_static, int pdl, cudaStream_t s, int type = GQ_TYPE_Q4_0);
 void set_prefill_streamk(int64_t v);   // 0 whole tiles only, 1 by shape (default), n >= 2: every tile in n pieces
 int64_t get_prefill_streamk();
 void set_prefill_slots(int64_t v);     // 0: SM count; n: plan for n SMs (test aid)

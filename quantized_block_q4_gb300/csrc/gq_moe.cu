@@ -41,8 +41,8 @@ __global__ void k_moe_route(const int32_t* __restrict__ ids, int P, int E, int n
   const int EB = E + 1;           // bucket E collects the ids outside [0, E)
   int* hist = sh;                 // [nw][EB]: pass-1 counts, then each warp's next sorted position
   int* cnt = sh + nw * EB;        // [EB]: pairs per bucket
-  pdl_launch_dependents();
   pdl_wait();  // ids may come from the previous kernel
+  pdl_launch_dependents();  // after the wait: a later launch cannot overtake the kernels ahead of this one
 
   for (int i = threadIdx.x; i < nw * EB; i += blockDim.x) hist[i] = 0;
   __syncthreads();
@@ -176,8 +176,8 @@ __global__ void k_moe_route(const int32_t* __restrict__ ids, int P, int E, int n
 // X, Xg 16-byte aligned: 8 elements per thread step.
 __global__ void k_moe_gather_bf16(const float* __restrict__ X, int64_t K, const MoeRoute rt,
                                   uint16_t* __restrict__ Xg) {
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int routed = rt.meta[2];
   const int64_t k8 = K / 8;
   for (int pos = blockIdx.x; pos < routed; pos += gridDim.x) {

@@ -179,6 +179,7 @@ struct PrefillWork {
   unsigned long long* count;  // per split tile and CTA of a pair: (epoch << 8) | pieces published
   unsigned long long epoch;   // this launch's tag (< 2^56): a counter with another tag reads as 0
   int early_w;    // W is not written by the kernels before: its first chunks may stream before the PDL wait
+  int x_static;   // X is not written by the kernels that may still run: only Y (and scratch) wait for the kernel before
   int drop;       // test hook (GQ_OPT_TEST_DROP_ARRIVE): raw chunk 1 of CTA 0 is never issued
 };
 
@@ -497,7 +498,11 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
   if (PAIR) cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  if (!MOE) pdl_launch_dependents();
+  // The next kernel may launch once every CTA has signalled: at once with
+  // x_static, else after this CTA's x producer has waited for the kernel
+  // before, so that a later x-static launch cannot start before the kernels
+  // ahead of this one are done.
+  if (!MOE && wk.x_static) pdl_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ W producer
@@ -508,7 +513,8 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
       const bool issuer = elect_one();
       if (issuer) tma_prefetch_desc(&tmW);
       uint32_t nraw = 0;
-      bool ok = true, waited = MOE;
+      // static W under an x-static launch: nothing of this producer waits for the kernel before
+      bool ok = true, waited = MOE || (wk.early_w && wk.x_static);
       for (int i = 0; i < nseg && ok; ++i) {
         Seg sg;
         int m0;
@@ -551,7 +557,10 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
     {
       const bool issuer = elect_one();
       if (issuer) tma_prefetch_desc(&tmX);
-      if (!MOE) pdl_wait();
+      if (!MOE && !wk.x_static) {
+        pdl_wait();
+        pdl_launch_dependents();
+      }
       uint32_t nb = 0;
       bool ok = true;
       for (int i = 0; i < nseg && ok; ++i) {
@@ -600,7 +609,7 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
     // As for the W producer: the converged warp waits, one elected lane issues.
     if (leader) {
       const bool issuer = elect_one();
-      if (!MOE) pdl_wait();
+      if (!MOE && !wk.x_static) pdl_wait();
       uint32_t idesc = umma_idesc_bf16_f32(C::kBM * C::kCtas, BN);
       uint32_t c = 0, seg = 0;
       bool ok = true;
@@ -668,7 +677,9 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ dequant + epilogue
-    if (!MOE) pdl_wait();
+    // With x_static nothing before the first epilogue touches global memory
+    // that the kernel before may still use: Y and the k-split scratch wait there.
+    if (!MOE && !wk.x_static) pdl_wait();
     const int quad = warp & 3;           // TMEM lane quadrant this warp may access
     const int grp = (warp - 2) >> 2;     // 64-k step grp of every 256-k chunk; then columns grp/4 of the tile
     const int row = quad * 32 + lane;    // W row within this CTA's 128 == TMEM lane
@@ -742,6 +753,7 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
       }
 
       // ---- epilogue of this segment: this group's quarter of the accumulator columns
+      if (!MOE && wk.x_static && seg == 0) pdl_wait();
       if (live) live = mbar_wait_bounded(smem_u32(acc_full), seg & 1, limit_ns, abort_flag, err);
       live = __all_sync(0xFFFFFFFFu, live);
       tc_fence_after();
@@ -935,7 +947,8 @@ int64_t prefill_plan(int64_t T, int64_t nr, int64_t P, bool allow_split, int bn,
 
 template <int BN, bool PAIR, int F = GQ_TYPE_Q4_0>
 cudaError_t launch_prefill_cfg(const CUtensorMap* tmW, const CUtensorMap* tmX, int N, int M, int K, float* Y,
-                               uint64_t limit_ns, bool allow_scratch, int early_w, int pdl, cudaStream_t s) {
+                               uint64_t limit_ns, bool allow_scratch, int early_w, int x_static, int pdl,
+                               cudaStream_t s) {
   using C = PrefillCfg<BN, PAIR, F>;
   auto kern = k_prefill_q4_0<BN, PAIR, false, F>;
   {
@@ -950,6 +963,7 @@ cudaError_t launch_prefill_cfg(const CUtensorMap* tmW, const CUtensorMap* tmX, i
   wk.nr = static_cast<int>(nr);
   wk.ntn = static_cast<int>(ntn);
   wk.early_w = pdl && early_w;
+  wk.x_static = pdl && x_static;
   wk.drop = test_drop() == 2 ? 1 : 0;
   prefill_plan(T, nr, device_info().sm_count / C::kCtas, allow_scratch, BN, &wk);
   void* scratch = nullptr;
@@ -1075,27 +1089,27 @@ cudaError_t launch_prefill_moe(const CUtensorMap* tmW, const CUtensorMap* tmX, i
 }
 
 cudaError_t launch_prefill(const CUtensorMap* tmW, const CUtensorMap* tmX, int64_t N, int64_t M, int64_t K,
-                           float* Y, uint64_t wait_limit_ns, bool allow_scratch, int early_w, int pdl, cudaStream_t s,
-                           int type) {
+                           float* Y, uint64_t wait_limit_ns, bool allow_scratch, int early_w, int x_static, int pdl,
+                           cudaStream_t s, int type) {
   const int n = static_cast<int>(N), m = static_cast<int>(M), k = static_cast<int>(K);
   if (type == GQ_TYPE_Q4_1) {
     if (prefill_bn(N, M, K, allow_scratch) == 128)
-      return launch_prefill_cfg<128, false, GQ_TYPE_Q4_1>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
-    return launch_prefill_cfg<256, false, GQ_TYPE_Q4_1>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
+      return launch_prefill_cfg<128, false, GQ_TYPE_Q4_1>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
+    return launch_prefill_cfg<256, false, GQ_TYPE_Q4_1>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
   }
   if (type == GQ_TYPE_Q8_0) {
     if (prefill_bn(N, M, K, allow_scratch) == 128)
-      return launch_prefill_cfg<128, false, GQ_TYPE_Q8_0>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
-    return launch_prefill_cfg<256, false, GQ_TYPE_Q8_0>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
+      return launch_prefill_cfg<128, false, GQ_TYPE_Q8_0>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
+    return launch_prefill_cfg<256, false, GQ_TYPE_Q8_0>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
   }
   if (type == GQ_TYPE_Q4_K) {
     if (prefill_bn(N, M, K, allow_scratch) == 128)
-      return launch_prefill_cfg<128, false, GQ_TYPE_Q4_K>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
-    return launch_prefill_cfg<256, false, GQ_TYPE_Q4_K>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
+      return launch_prefill_cfg<128, false, GQ_TYPE_Q4_K>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
+    return launch_prefill_cfg<256, false, GQ_TYPE_Q4_K>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
   }
-  if (use_pair(N)) return launch_prefill_cfg<256, true>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
-  if (prefill_bn(N, M, K, allow_scratch) == 128) return launch_prefill_cfg<128, false>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
-  return launch_prefill_cfg<256, false>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, pdl, s);
+  if (use_pair(N)) return launch_prefill_cfg<256, true>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
+  if (prefill_bn(N, M, K, allow_scratch) == 128) return launch_prefill_cfg<128, false>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
+  return launch_prefill_cfg<256, false>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
 }
 
 }  // namespace gq

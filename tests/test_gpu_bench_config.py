@@ -7,7 +7,8 @@ bench.py runs each layer of the 7B-like sweep as:
     launch, so consecutive launches overlap;
   * prefill: eagerly, the layer's four activations converted to bf16
     (gq_f32_to_bf16), then the seven tensor-core MUL_MATs on them
-    (gq_mul_mat_q4_0_bf16x) at N = 512.
+    (gq_mul_mat_q4_0_bf16x) at N = 512, the first without the x-static
+    promise and the other six with it.
 These tests build one layer from the bench's own input recipe, run it the same
 way, and compare with the oracle: every decode output over two graph replays,
 and sampled rows (all 512 tokens) of every prefill output.
@@ -95,10 +96,13 @@ def test_prefill_layer_eager_bf16_chain():
 
     def run():
         with torch.cuda.stream(s):
-            for i, x in enumerate(X):
-                gq.gq_f32_to_bf16(x, Xb[i], x.numel(), stream=s)
-            for j, (M, K, _) in enumerate(host_w):
-                gq.gq_mul_mat_q4_0_bf16x(W[j], M, K, Xb[order[j]], N, Y[j], stream=s)
+            for _ in range(2):  # twice: the second layer's conversions overwrite X while the first's calls may run
+                for i, x in enumerate(X):
+                    gq.gq_f32_to_bf16(x, Xb[i], x.numel(), stream=s)
+                for j, (M, K, _) in enumerate(host_w):
+                    # as the bench: the first call without the x-static promise, the others with it
+                    gq.gq_set_option(gq.GQ_OPT_X_STATIC, 1 if j > 0 else 0)
+                    gq.gq_mul_mat_q4_0_bf16x(W[j], M, K, Xb[order[j]], N, Y[j], stream=s)
         torch.cuda.synchronize()
         gq.gq_sync_status(s)
         return [y.cpu().numpy() for y in Y]

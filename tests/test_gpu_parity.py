@@ -556,6 +556,84 @@ def test_x_static_back_to_back_independent_calls(M, K):
         assert_mul_mat_close(Ys[i].cpu().numpy(), y_ref, s_ref, f"x-static call {i}")
 
 
+def _chain_rounds(project, make_x, rounds=4):
+    """A writer kernel produces X, then three projections of it: the first
+    call without GQ_OPT_X_STATIC, the next two with it (the pattern the
+    promise allows).  Each round writes another X, so a projection that read
+    X before its writer finished would carry the previous round's values.
+    Returns the last round's X (host) and three outputs."""
+    out = None
+    for r in range(rounds):
+        x = make_x(r)
+        ys = []
+        for i in range(3):
+            gq.gq_set_option(gq.GQ_OPT_X_STATIC, 0 if i == 0 else 1)
+            ys.append(project(i, x))
+        gq.gq_set_option(gq.GQ_OPT_X_STATIC, 0)
+        out = (x, ys)
+    torch.cuda.synchronize()
+    gq.gq_sync_status()
+    return out
+
+
+def test_x_static_chain_after_a_writer_decode():
+    """Decode: X of the projections is the Y of the MUL_MAT right before them."""
+    M0 = K = 4096
+    W0 = synth.q4_0_weights(M0, 2048, seed=7900)
+    Ws = [synth.q4_0_weights(4096, K, seed=7901 + i) for i in range(3)]
+    W0d, Wd = dev(W0), [dev(w) for w in Ws]
+    X0s = [dev(synth.activations(1, 2048, seed=7910 + r)) for r in range(4)]
+    Y1 = torch.empty(1, K, device="cuda")
+    Ys = [torch.empty(1, 4096, device="cuda") for _ in range(3)]
+
+    def make_x(r):
+        gq.gq_mul_mat_q4_0(W0d, M0, 2048, X0s[r], 1, Y1)  # the writer of X (no promise)
+        return Y1
+
+    def project(i, x):
+        gq.gq_mul_mat_q4_0(Wd[i], 4096, K, x, 1, Ys[i])
+        return Ys[i]
+    old = gq.gq_get_option(gq.GQ_OPT_X_STATIC)
+    try:
+        x, ys = _with_option(gq.GQ_OPT_WEIGHTS_STATIC, 1, lambda: _chain_rounds(project, make_x))
+    finally:
+        gq.gq_set_option(gq.GQ_OPT_X_STATIC, old)
+    xh = x.cpu().numpy()
+    for i in range(3):
+        y_ref, s_ref = oracle_mul_mat(Ws[i], 4096, K, xh)
+        assert_mul_mat_close(ys[i].cpu().numpy(), y_ref, s_ref, f"decode projection {i} of the last round")
+
+
+@pytest.mark.parametrize("M,K,N", [(4096, 4096, 512), (11008, 4096, 300), (640, 2048, 64)])
+def test_x_static_chain_after_a_writer_tensor_core(M, K, N):
+    """gq_mul_mat_q4_0_bf16x: X_bf16 is written by the activation conversion
+    right before the first projection; the other two carry the promise and
+    may start their MMAs while the kernels ahead of them finish."""
+    Ws = [synth.q4_0_weights(M, K, seed=7920 + i) for i in range(3)]
+    Wd = [dev(w) for w in Ws]
+    Xfs = [dev(synth.activations(N, K, seed=7930 + r)) for r in range(4)]
+    Xb = torch.empty(N, K, dtype=torch.int16, device="cuda")
+    Ys = [torch.empty(N, M, device="cuda") for _ in range(3)]
+
+    def make_x(r):
+        gq.gq_f32_to_bf16(Xfs[r], Xb, N * K)  # the writer of X
+        return Xb
+
+    def project(i, x):
+        gq.gq_mul_mat_q4_0_bf16x(Wd[i], M, K, x, N, Ys[i])
+        return Ys[i]
+    old = gq.gq_get_option(gq.GQ_OPT_X_STATIC)
+    try:
+        x, ys = _with_option(gq.GQ_OPT_WEIGHTS_STATIC, 1, lambda: _chain_rounds(project, make_x))
+    finally:
+        gq.gq_set_option(gq.GQ_OPT_X_STATIC, old)
+    xh = (x.cpu().numpy().astype(np.int32).astype(np.uint32) << 16).view(np.float32)  # bf16 bits -> fp32
+    rows = sampled_rows(M, 96, 79)
+    for i in range(3):
+        y_ref, s_ref = oracle_mul_mat(Ws[i].reshape(M, -1)[rows], len(rows), K, xh)
+        assert_mul_mat_close(ys[i].cpu().numpy()[:, rows], y_ref, s_ref, f"tensor-core projection {i}")
+
+
 @pytest.mark.parametrize("stages", [1, 2, 3, 8])
 def test_decode_early_stages_option(stages):
     def run():
