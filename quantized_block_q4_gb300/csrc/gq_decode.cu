@@ -969,6 +969,12 @@ cudaError_t launch_decode(const CUtensorMap* tmW, const float* X, int64_t N, int
   }
   if (N <= 8) {
     if (variant == 2) return launch_cfg<1, 1, 8, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    // The co-resident 4-warp CTA, as for N = 1, where it measured faster when
+    // repeated: up to 4 tokens and one 32-row tile per SM (4096 x 4096: 2
+    // tokens 4.95 -> 3.82 us, 4 tokens 6.23 -> 4.86 us); with 8 tokens, or
+    // 11008 rows and 2 tokens, the 8-warp CTA was faster.
+    if (variant == 0 && N <= 4 && early_w && decode_x_static() && (m + 31) / 32 <= device_info().sm_count)
+      return launch_cfg<1, 2, 4, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
     return launch_cfg<1, 2, 8, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
   }
   if (N <= 16) {

@@ -534,6 +534,28 @@ def test_prefill_same_output_and_scratch_back_to_back(streamk):
     assert_mul_mat_close(Ylast.cpu().numpy(), y_ref, s_ref, "interleaved call")
 
 
+@pytest.mark.parametrize("N", [2, 3, 4])
+@pytest.mark.parametrize("M,K", [(4096, 4096), (1000, 2048), (4096, 11008)])
+def test_small_batch_co_resident_cta(M, K, N):
+    """2-4 tokens under both promises on matrices of at most one 32-row tile
+    per SM: the 4-warp CTA (two launches share an SM), back to back."""
+    Ws = [synth.q4_0_weights(M, K, seed=8100 + i + N) for i in range(2)]
+    Xs = [synth.activations(N, K, seed=8110 + i + N) for i in range(2)]
+    Wd, Xd = [dev(w) for w in Ws], [dev(x) for x in Xs]
+    Ys = [torch.empty(N, M, device="cuda") for _ in range(2)]
+
+    def run():
+        for _ in range(3):
+            for w, x, y in zip(Wd, Xd, Ys):
+                gq.gq_mul_mat_q4_0(w, M, K, x, N, y)
+        torch.cuda.synchronize()
+        gq.gq_sync_status()
+    _with_option(gq.GQ_OPT_X_STATIC, 1, lambda: _with_option(gq.GQ_OPT_WEIGHTS_STATIC, 1, run))
+    for i in range(2):
+        y_ref, s_ref = oracle_mul_mat(Ws[i], M, K, Xs[i])
+        assert_mul_mat_close(Ys[i].cpu().numpy(), y_ref, s_ref, f"{N} tokens, call {i}")
+
+
 @pytest.mark.parametrize("M,K", [(4096, 4096), (11008, 4096), (4096, 11008)])
 def test_x_static_back_to_back_independent_calls(M, K):
     """X_STATIC + WEIGHTS_STATIC: calls whose X no preceding kernel writes may

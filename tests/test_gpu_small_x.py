@@ -70,14 +70,15 @@ def test_q4_0_decode_small_x(variant, N, scale):
                 {gq.GQ_OPT_DECODE_VARIANT: variant})
 
 
+@pytest.mark.parametrize("N", [1, 3])
 @pytest.mark.parametrize("static", [0, 1])
 @pytest.mark.parametrize("shape", [(11008, 4096), (4096, 11008)])
-def test_q4_0_decode_small_x_sweep_shapes(shape, static):
-    """The sweep's N = 1 shapes, with and without the static promises (the
-    4-warp and 8-warp CTA layouts)."""
+def test_q4_0_decode_small_x_sweep_shapes(shape, static, N):
+    """The sweep's shapes at 1 and 3 tokens, with and without the static
+    promises (the 4-warp and 8-warp CTA layouts)."""
     M, K = shape
     opts = {gq.GQ_OPT_X_STATIC: static, gq.GQ_OPT_WEIGHTS_STATIC: static}
-    _check_q4_0(M, K, 1, 1e-6, 16100 + M + static, f"small x {M}x{K} static={static}", opts)
+    _check_q4_0(M, K, N, 1e-6, 16100 + M + static + N, f"small x {M}x{K} N={N} static={static}", opts)
 
 
 @pytest.mark.parametrize("qtype", [1, 2], ids=["q4_1", "q8_0"])
