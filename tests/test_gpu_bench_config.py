@@ -5,8 +5,8 @@ bench.py runs each layer of the 7B-like sweep as:
     11008 x 4096; down 4096 x 11008) captured in one CUDA graph, with
     GQ_OPT_WEIGHTS_STATIC and GQ_OPT_X_STATIC set and programmatic dependent
     launch, so consecutive launches overlap;
-  * prefill: eagerly, the layer's four activations converted to bf16
-    (gq_f32_to_bf16), then the seven tensor-core MUL_MATs on them
+  * prefill: eagerly, the layer's four activations (one buffer) converted
+    to bf16 by one gq_f32_to_bf16 call, then the seven tensor-core MUL_MATs on them
     (gq_mul_mat_q4_0_bf16x) at N = 512, the first without the x-static
     promise and the other six with it.
 These tests build one layer from the bench's own input recipe, run it the same
@@ -89,16 +89,20 @@ def test_prefill_layer_eager_bf16_chain():
     N = bench.PREFILL_N
     order, host_w, acts = _layer(N, 1)
     W = [torch.from_numpy(w).cuda() for _, _, w in host_w]
-    X = [torch.from_numpy(a).cuda() for a in acts]
-    Xb = [torch.empty(x.shape, dtype=torch.int16, device="cuda") for x in X]
+    # the layer's activations in one buffer, converted by one call, as the bench does
+    Xflat = torch.from_numpy(np.concatenate([a.ravel() for a in acts])).cuda()
+    Xbflat = torch.empty(Xflat.numel(), dtype=torch.int16, device="cuda")
+    Xb, off = [], 0
+    for a in acts:
+        Xb.append(Xbflat[off:off + a.size].view(a.shape))
+        off += a.size
     Y = [torch.full((N, M), float("nan"), device="cuda") for M, _, _ in host_w]
     s = torch.cuda.Stream()
 
     def run():
         with torch.cuda.stream(s):
-            for _ in range(2):  # twice: the second layer's conversions overwrite X while the first's calls may run
-                for i, x in enumerate(X):
-                    gq.gq_f32_to_bf16(x, Xb[i], x.numel(), stream=s)
+            for _ in range(2):  # twice: the second layer's conversion overwrites X while the first's calls may run
+                gq.gq_f32_to_bf16(Xflat, Xbflat, Xflat.numel(), stream=s)
                 for j, (M, K, _) in enumerate(host_w):
                     # as the bench: the first call without the x-static promise, the others with it
                     gq.gq_set_option(gq.GQ_OPT_X_STATIC, 1 if j > 0 else 0)
