@@ -190,9 +190,9 @@ class Oracle:
 
 
 # Block formats of the typed functions (the same numbering as the library's gq_type).
-TYPE_Q4_0, TYPE_Q4_1, TYPE_Q8_0, TYPE_Q4_K = 0, 1, 2, 3
-BLOCK_BYTES = {TYPE_Q4_0: 18, TYPE_Q4_1: 20, TYPE_Q8_0: 34, TYPE_Q4_K: 144}
-BLOCK_WEIGHTS = {TYPE_Q4_0: 32, TYPE_Q4_1: 32, TYPE_Q8_0: 32, TYPE_Q4_K: 256}
+TYPE_Q4_0, TYPE_Q4_1, TYPE_Q8_0, TYPE_Q4_K, TYPE_Q5_0, TYPE_Q5_1 = 0, 1, 2, 3, 4, 5
+BLOCK_BYTES = {TYPE_Q4_0: 18, TYPE_Q4_1: 20, TYPE_Q8_0: 34, TYPE_Q4_K: 144, TYPE_Q5_0: 22, TYPE_Q5_1: 24}
+BLOCK_WEIGHTS = {TYPE_Q4_0: 32, TYPE_Q4_1: 32, TYPE_Q8_0: 32, TYPE_Q4_K: 256, TYPE_Q5_0: 32, TYPE_Q5_1: 32}
 
 
 def get() -> Oracle:

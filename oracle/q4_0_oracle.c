@@ -263,6 +263,8 @@ static int type_block_bytes(int type)
     case ORACLE_TYPE_Q4_1: return 20;
     case ORACLE_TYPE_Q8_0: return 34;
     case ORACLE_TYPE_Q4_K: return 144;
+    case ORACLE_TYPE_Q5_0: return 22;
+    case ORACLE_TYPE_Q5_1: return 24;
     default: return 0;
     }
 }
@@ -292,6 +294,30 @@ static void q4_k_fields(const uint8_t *b, int sc[8], int m[8])
         m[j] = b[4 + j] & 0x3F;
         sc[4 + j] = (b[8 + j] & 0x0F) | ((b[j] >> 6) << 4);
         m[4 + j] = (b[8 + j] >> 4) | ((b[4 + j] >> 6) << 4);
+    }
+}
+
+/*
+ * One Q5_0 / Q5_1 block -> 32 fp32 weights (the reading in the header): the
+ * 5-bit code of element e is its nibble plus 16 times bit e of qh.
+ */
+static void dequant_q5_block(int type, const uint8_t *blk, float *w)
+{
+    float d = le_half_at(blk);
+    int off = type == ORACLE_TYPE_Q5_1 ? 4 : 2;             /* qh follows d (and m) */
+    uint32_t qh = (uint32_t)blk[off] | ((uint32_t)blk[off + 1] << 8) |
+                  ((uint32_t)blk[off + 2] << 16) | ((uint32_t)blk[off + 3] << 24);
+    const uint8_t *qs = blk + off + 4;
+    for (int e = 0; e < QK; ++e) {
+        int nib = e < 16 ? (qs[e] & 0x0F) : (qs[e - 16] >> 4);
+        int q = nib | (int)(((qh >> e) & 1u) << 4);
+        if (type == ORACLE_TYPE_Q5_0) {
+            w[e] = d * (float)(q - 16);
+        } else {
+            float m = le_half_at(blk + 2);
+            float dq = d * (float)q;
+            w[e] = dq + m;
+        }
     }
 }
 
@@ -332,6 +358,11 @@ static void dequant_row_typed(int type, const uint8_t *row, int64_t K, float *w)
     if (type == ORACLE_TYPE_Q4_K) {
         for (int64_t b = 0; b < K / 256; ++b)
             dequant_q4_k_block(row + b * bb, w + b * 256);
+        return;
+    }
+    if (type == ORACLE_TYPE_Q5_0 || type == ORACLE_TYPE_Q5_1) {
+        for (int64_t b = 0; b < nb; ++b)
+            dequant_q5_block(type, row + b * bb, w + b * QK);
         return;
     }
     for (int64_t b = 0; b < nb; ++b) {
@@ -377,7 +408,7 @@ void oracle_validate_typed(int type, const uint8_t *W, int64_t M, int64_t K, uin
     for (uint64_t b = 0; b < nblocks; ++b) {
         const uint8_t *blk = W + b * (uint64_t)bb;
         int bad = !isfinite(oracle_half_to_double((uint16_t)(blk[0] | (blk[1] << 8))));
-        if (type == ORACLE_TYPE_Q4_1 || type == ORACLE_TYPE_Q4_K)   /* m, or dmin */
+        if (type == ORACLE_TYPE_Q4_1 || type == ORACLE_TYPE_Q4_K || type == ORACLE_TYPE_Q5_1)   /* m, or dmin */
             bad |= !isfinite(oracle_half_to_double((uint16_t)(blk[2] | (blk[3] << 8))));
         if (bad) {
             if (*count == 0)

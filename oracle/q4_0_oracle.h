@@ -96,7 +96,21 @@ void oracle_mul_mat_id_q4_0(const uint8_t *W, int64_t n_expert, int64_t M, int64
  * 0..15 in the Q4_0 nibble order; Q8_0 = fp16 d, int8 qs[32] (34 bytes), w =
  * d*q.  ORACLE_TYPE_Q4_0 is the Q4_0 functions above.
  */
-enum { ORACLE_TYPE_Q4_0 = 0, ORACLE_TYPE_Q4_1 = 1, ORACLE_TYPE_Q8_0 = 2, ORACLE_TYPE_Q4_K = 3 };
+enum { ORACLE_TYPE_Q4_0 = 0, ORACLE_TYPE_Q4_1 = 1, ORACLE_TYPE_Q8_0 = 2, ORACLE_TYPE_Q4_K = 3,
+       ORACLE_TYPE_Q5_0 = 4, ORACLE_TYPE_Q5_1 = 5 };
+/*
+ * Q5_0 and Q5_1, the 5-bit legacy formats named beside Q4_0 / Q4_1 in the
+ * quantisation-format section (32 weights per block, one scale; the _1 form
+ * also a min).  The pages print neither struct.  The reading, the layout
+ * GGUF files carry:
+ *   Q5_0: fp16 d, uint8_t qh[4], uint8_t qs[16]            (22 bytes), w = d*(q - 16)
+ *   Q5_1: fp16 d, fp16 m, uint8_t qh[4], uint8_t qs[16]    (24 bytes), w = d*q + m
+ * with the 5-bit code q of element e (0..31) = its nibble (low nibble of
+ * qs[e] for e < 16, high nibble of qs[e-16] for e >= 16, as in Q4_0) plus 16
+ * times bit e of the little-endian 32-bit word qh.  In fp32, d*(q-16) is exact
+ * (11 x 5 significant bits); Q5_1's d*q is exact and m is added with one
+ * rounding.
+ */
 /*
  * Q4_K, the 4-bit k-quant ("Architecture and module overview", the
  * quantisation-format section and the error-model paragraph of the
@@ -134,7 +148,7 @@ void oracle_mul_mat_typed(int type, const uint8_t *W, int64_t M, int64_t K, cons
  * on --check-tensors and parallel validation: ggml_validate_row_data checks
  * each row's scale factors and integers; the reading: a block's fp16 scale
  * fields must be finite, and every 4-, 6- or 8-bit field is a valid integer).  Over the M x K weights in block format `type`: *count = the
- * number of blocks with a NaN or infinite scale (d; for Q4_1 also m; for Q4_K also dmin),
+ * number of blocks with a NaN or infinite scale (d; for Q4_1 and Q5_1 also m; for Q4_K also dmin),
  * *first = the smallest flat block index (row * K/32 + block; row * K/256 +
  * super-block for Q4_K) among them, or
  * UINT64_MAX when there is none.  A scale is tested by decoding it with

@@ -137,13 +137,29 @@ def typed_weights(qtype: int, M: int, K: int, seed: int, d_scale: float = 1.0) -
     """Weights in one of the block formats, as raw bytes [M, K/32*bytes]:
     0 = Q4_0 (q4_0_weights), 1 = Q4_1 (fp16 d ~ U[0.005, 0.02], fp16 m ~
     U[-0.16, 0], 16 random code bytes), 2 = Q8_0 (fp16 d ~ U[0.0003, 0.0012],
-    32 random int8 code bytes), 3 = Q4_K (q4_k_weights: [M, K/256*144]).
+    32 random int8 code bytes), 3 = Q4_K (q4_k_weights: [M, K/256*144]), 4 / 5 =
+    Q5_0 / Q5_1 (fp16 d ~ U[0.0025, 0.01], Q5_1 also m ~ U[-0.16, 0], 20 random
+    bytes of high bits and codes).
     Scales are RNE fp16 of values drawn in fp64; d_scale multiplies the ranges
     of d and m (e.g. 100 for O(1) weights)."""
     if qtype == 0:
         return q4_0_weights(M, K, seed, (0.005 * d_scale, 0.02 * d_scale))
     if qtype == 3:
         return q4_k_weights(M, K, seed, d_scale)
+    if qtype in (4, 5):
+        # Q5_0 / Q5_1: fp16 d ~ U[0.0025, 0.01] (half Q4_0's range: codes span 32
+        # levels), Q5_1 also fp16 m ~ U[-0.16, 0]; 4 random high-bit bytes and 16
+        # random code bytes
+        if K % QK4_0:
+            raise ValueError("K must be a multiple of 32")
+        nb = K // QK4_0
+        bb = 22 if qtype == 4 else 24
+        out = np.empty((M, nb, bb), dtype=np.uint8)
+        out[:, :, bb - 20:] = random_bytes(seed, M * nb * 20).reshape(M, nb, 20)
+        out[:, :, 0:2] = random_scales(seed, M * nb, 0.0025 * d_scale, 0.01 * d_scale).view(np.uint8).reshape(M, nb, 2)
+        if qtype == 5:
+            out[:, :, 2:4] = random_scales(seed ^ 0x3117, M * nb, -0.16 * d_scale, 0.0).view(np.uint8).reshape(M, nb, 2)
+        return out.reshape(M, nb * bb)
     if K % QK4_0:
         raise ValueError("K must be a multiple of 32")
     nb = K // QK4_0
