@@ -189,8 +189,8 @@ Q4K_MUTATIONS = {
     "codes_interleaved": [("w[64 * c + 32 + l] = dh * (float)q_hi - mh;", "w[64 * c + 32 + (l ^ 1)] = dh * (float)q_hi - mh;")],
     "block_bytes_128": [("    case ORACLE_TYPE_Q4_K: return 144;", "    case ORACLE_TYPE_Q4_K: return 128;")],
     "zero_point_8": [("w[64 * c + l] = dl * (float)q_lo - ml;", "w[64 * c + l] = dl * (float)(q_lo - 8) - ml;")],
-    "validate_ignores_dmin": [("if (type == ORACLE_TYPE_Q4_1 || type == ORACLE_TYPE_Q4_K)   /* m, or dmin */",
-                               "if (type == ORACLE_TYPE_Q4_1)   /* m, or dmin */")],
+    "validate_ignores_dmin": [("if (type == ORACLE_TYPE_Q4_1 || type == ORACLE_TYPE_Q4_K || type == ORACLE_TYPE_Q5_1)",
+                               "if (type == ORACLE_TYPE_Q4_1 || type == ORACLE_TYPE_Q5_1)")],
 }
 
 

@@ -106,8 +106,8 @@ def test_pin(pin):
 MUTATIONS = {
     "nan_not_detected": [("int bad = !isfinite(oracle_half_to_double((uint16_t)(blk[0] | (blk[1] << 8))));",
                           "int bad = isinf(oracle_half_to_double((uint16_t)(blk[0] | (blk[1] << 8))));")],
-    "q4_1_min_ignored": [("if (type == ORACLE_TYPE_Q4_1 || type == ORACLE_TYPE_Q4_K)   /* m, or dmin */\n            bad |=",
-                          "if (type == ORACLE_TYPE_Q4_K)\n            bad |=")],
+    "q4_1_min_ignored": [("if (type == ORACLE_TYPE_Q4_1 || type == ORACLE_TYPE_Q4_K || type == ORACLE_TYPE_Q5_1)   /* m, or dmin */\n            bad |=",
+                          "if (type == ORACLE_TYPE_Q4_K || type == ORACLE_TYPE_Q5_1)\n            bad |=")],
     "first_is_the_last": [("if (*count == 0)\n                *first = b;", "*first = b;")],
     "q4_0_block_stride": [("const uint8_t *blk = W + b * (uint64_t)bb;", "const uint8_t *blk = W + b * 18u;")],
     "scale_big_endian": [("int bad = !isfinite(oracle_half_to_double((uint16_t)(blk[0] | (blk[1] << 8))));",
