@@ -816,13 +816,14 @@ def run_moe_aux(gq, torch, dev, s, peaks):
 
 
 def run_formats_aux(gq, torch, dev, s, peaks):
-    """Q4_1, Q8_0 and Q4_K on the 14336 x 4096 matrix: dequant (GB/s), MUL_MAT
+    """Q4_1, Q8_0, Q4_K, Q5_0 and Q5_1 on the 14336 x 4096 matrix: dequant (GB/s), MUL_MAT
     at N = 1 (weight GB/s) and N = 512 (TFLOP/s), CUDA events over repeated
     calls on 8 rotating weight copies (264 MB and more together, so each call
     streams its copy from DRAM)."""
     M, K = MOE_M, MOE_K
     out = {}
-    for name, qt in (("q4_1", gq.GQ_TYPE_Q4_1), ("q8_0", gq.GQ_TYPE_Q8_0), ("q4_k", gq.GQ_TYPE_Q4_K)):
+    for name, qt in (("q4_1", gq.GQ_TYPE_Q4_1), ("q8_0", gq.GQ_TYPE_Q8_0), ("q4_k", gq.GQ_TYPE_Q4_K),
+                     ("q5_0", gq.GQ_TYPE_Q5_0), ("q5_1", gq.GQ_TYPE_Q5_1)):
         nbytes = gq.gq_type_nbytes(qt, M, K)
         W0 = torch.from_numpy(synth.typed_weights(qt, M, K, seed=0x7E00 + qt)).to(dev)
         Ws = [W0.clone() for _ in range(8)]
@@ -858,7 +859,9 @@ def run_formats_aux(gq, torch, dev, s, peaks):
                         "frac": round(dq / peaks["hbm_gbs"], 4)},
             "mul_mat_n1": {"us": round(t1 * 1e6, 2), "achieved": round(g1, 1), "unit": "GB/s", "bound": "hbm",
                            "frac": round(g1 / peaks["hbm_gbs"], 4),
-                           "kernel": "k_decode_q4_0<..., type> (mma.sync decode on this block format)",
+                           "kernel": ("k_mul_mat_legacy_bulk<type> (scalar: no mma.sync decode for 5-bit codes)"
+                                      if name.startswith("q5") else
+                                      "k_decode_q4_0<..., type> (mma.sync decode on this block format)"),
                            "timing": "eager back-to-back calls (launch gaps included)"},
             "mul_mat_n512": {"us": round(tp * 1e6, 2), "achieved": round(tf, 2), "unit": "TFLOP/s",
                              "bound": "tensor", "frac": round(tf / peaks["bf16_tflops"], 4),

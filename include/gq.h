@@ -64,17 +64,28 @@ typedef enum {
  *   GQ_TYPE_Q4_0  fp16 d, uint8_t qs[16]          18 bytes  w = d*(q - 8)
  *   GQ_TYPE_Q4_1  fp16 d, fp16 m, uint8_t qs[16]  20 bytes  w = d*q + m
  *   GQ_TYPE_Q8_0  fp16 d, int8_t qs[32]           34 bytes  w = d*q
+ *   GQ_TYPE_Q5_0  fp16 d, uint8_t qh[4], uint8_t qs[16]          22 bytes  w = d*(q - 16)
+ *   GQ_TYPE_Q5_1  fp16 d, fp16 m, uint8_t qh[4], uint8_t qs[16]  24 bytes  w = d*q + m
  *   GQ_TYPE_Q4_K  fp16 d, fp16 dmin, uint8_t scales[12], uint8_t qs[128]
  *                 144 bytes per 256 weights (the GGUF super-block)
  *                 w = d*sc_j*q - dmin*m_j for sub-block j = 0..7 of 32 weights
  * (fp16 little-endian; legacy 4-bit codes: low nibble of qs[j] = element j,
- * high nibble = element j+16; Q8_0: qs[j] = element j.  Q4_K: weight 64c + l
+ * high nibble = element j+16; Q8_0: qs[j] = element j; Q5_0 / Q5_1: the 5-bit
+ * q of element e is its nibble in the Q4_0 order plus 16 times bit e of qh
+ * read as a little-endian 32-bit word.  Q4_K: weight 64c + l
  * (l < 32) is the low nibble of qs[32c + l] in sub-block 2c, weight 64c+32+l
  * its high nibble in sub-block 2c+1; the 6-bit sc_j, m_j: for j < 4 bits 0-5
  * of scales[j] and scales[j+4]; for j >= 4 bits 0-3 from the low and high
  * nibble of scales[j+4] and bits 4-5 from the top two bits of scales[j-4]
  * and scales[j].)  Rows of Q4_K need K % 256 == 0. */
-typedef enum { GQ_TYPE_Q4_0 = 0, GQ_TYPE_Q4_1 = 1, GQ_TYPE_Q8_0 = 2, GQ_TYPE_Q4_K = 3 } gq_type;
+typedef enum {
+  GQ_TYPE_Q4_0 = 0,
+  GQ_TYPE_Q4_1 = 1,
+  GQ_TYPE_Q8_0 = 2,
+  GQ_TYPE_Q4_K = 3,
+  GQ_TYPE_Q5_0 = 4,
+  GQ_TYPE_Q5_1 = 5
+} gq_type;
 
 /* Bytes of a Q4_0 matrix of M rows and K columns: M*(K/32)*18
  * ("Binding GGUF weights to the compute graph", section 2.3, ggml_nbytes note).

@@ -29,9 +29,11 @@ GQ_ERR_DEVICE_TIMEOUT = -6
 GQ_ERR_UNSUPPORTED = -7
 GQ_ERR_BAD_INDEX = -8
 
-GQ_TYPE_Q4_0, GQ_TYPE_Q4_1, GQ_TYPE_Q8_0, GQ_TYPE_Q4_K = 0, 1, 2, 3
-TYPE_BLOCK_BYTES = {GQ_TYPE_Q4_0: 18, GQ_TYPE_Q4_1: 20, GQ_TYPE_Q8_0: 34, GQ_TYPE_Q4_K: 144}
-TYPE_BLOCK_WEIGHTS = {GQ_TYPE_Q4_0: 32, GQ_TYPE_Q4_1: 32, GQ_TYPE_Q8_0: 32, GQ_TYPE_Q4_K: 256}
+GQ_TYPE_Q4_0, GQ_TYPE_Q4_1, GQ_TYPE_Q8_0, GQ_TYPE_Q4_K, GQ_TYPE_Q5_0, GQ_TYPE_Q5_1 = 0, 1, 2, 3, 4, 5
+TYPE_BLOCK_BYTES = {GQ_TYPE_Q4_0: 18, GQ_TYPE_Q4_1: 20, GQ_TYPE_Q8_0: 34, GQ_TYPE_Q4_K: 144, GQ_TYPE_Q5_0: 22,
+                    GQ_TYPE_Q5_1: 24}
+TYPE_BLOCK_WEIGHTS = {GQ_TYPE_Q4_0: 32, GQ_TYPE_Q4_1: 32, GQ_TYPE_Q8_0: 32, GQ_TYPE_Q4_K: 256, GQ_TYPE_Q5_0: 32,
+                      GQ_TYPE_Q5_1: 32}
 
 GQ_OPT_PREFILL_MIN_N = 0
 GQ_OPT_FORCE_GENERIC = 1

@@ -1,5 +1,5 @@
-// KL: the other legacy block formats, Q4_1 and Q8_0: dequantisation (bit-
-// exact) and MUL_MAT.
+// KL: the other legacy block formats, Q4_1, Q8_0, Q5_0 and Q5_1:
+// dequantisation (bit-exact) and MUL_MAT.
 //
 // "Architecture and module overview", quantisation-format section: the legacy
 // formats keep one scale per block of 32 weights, Q4_1 additionally a min
@@ -8,8 +8,12 @@
 //   Q4_1: ggml_half d, ggml_half m, uint8_t qs[16]  (20 bytes), w = d*q + m,
 //         q = 0..15, low nibble of qs[j] = element j, high nibble = j+16;
 //   Q8_0: ggml_half d, int8_t qs[32]                (34 bytes), w = d*q.
-// In fp32 d*q is exact (at most 11 x 8 significant bits); Q4_1 adds m with
-// one rounding.  Both kernels evaluate exactly that, so dequantisation is
+//   Q5_0: ggml_half d, uint8_t qh[4], uint8_t qs[16]           (22 bytes), w = d*(q - 16),
+//   Q5_1: ggml_half d, ggml_half m, uint8_t qh[4], uint8_t qs[16] (24 bytes), w = d*q + m,
+//         the 5-bit q of element e = its Q4_0-order nibble + 16 * bit e of
+//         the little-endian word qh.
+// In fp32 d*q is exact (at most 11 x 8 significant bits); Q4_1 and Q5_1 add m
+// with one rounding.  Both kernels evaluate exactly that, so dequantisation is
 // bit-exact and MUL_MAT sees the same weights.
 //
 // MUL_MAT here is the decode-shaped kernel for these formats: one warp per
@@ -39,15 +43,44 @@ template <>
 struct Fmt<GQ_TYPE_Q8_0> {
   static constexpr int kBytes = 34;
 };
+template <>
+struct Fmt<GQ_TYPE_Q5_0> {
+  static constexpr int kBytes = 22;
+};
+template <>
+struct Fmt<GQ_TYPE_Q5_1> {
+  static constexpr int kBytes = 24;
+};
+
+// Formats with a min offset m (the fp16 field after d) and 5-bit formats.
+template <int T>
+constexpr bool has_min() { return T == GQ_TYPE_Q4_1 || T == GQ_TYPE_Q5_1; }
+template <int T>
+constexpr bool five_bit() { return T == GQ_TYPE_Q5_0 || T == GQ_TYPE_Q5_1; }
+// Byte offsets of Q5's high-bit word and codes within a block.
+template <int T>
+constexpr int q5_qh_off() { return T == GQ_TYPE_Q5_1 ? 4 : 2; }
 
 __device__ __forceinline__ float half_at(const uint8_t* p) {
   return __half2float(__ushort_as_half(static_cast<uint16_t>(p[0] | (p[1] << 8))));
 }
 
+// The little-endian high-bit word of a Q5 block (byte loads: any alignment).
+template <int T>
+__device__ __forceinline__ uint32_t q5_high_bits(const uint8_t* blk) {
+  const uint8_t* p = blk + q5_qh_off<T>();
+  return p[0] | (p[1] << 8) | (p[2] << 16) | (static_cast<uint32_t>(p[3]) << 24);
+}
+
 // Element e (0..31) of a block held in shared or global memory.
 template <int T>
 __device__ __forceinline__ float weight(const uint8_t* blk, int e, float d, float m) {
-  if constexpr (T == GQ_TYPE_Q4_1) {
+  if constexpr (five_bit<T>()) {
+    const uint32_t byte = blk[q5_qh_off<T>() + 4 + (e & 15)];
+    const uint32_t q = (e < 16 ? (byte & 0xF) : (byte >> 4)) | (((q5_high_bits<T>(blk) >> e) & 1u) << 4);
+    if constexpr (T == GQ_TYPE_Q5_0) return __fmul_rn(d, static_cast<float>(static_cast<int>(q) - 16));
+    else return __fadd_rn(__fmul_rn(d, static_cast<float>(q)), m);
+  } else if constexpr (T == GQ_TYPE_Q4_1) {
     const uint32_t byte = blk[4 + (e & 15)];
     const uint32_t q = e < 16 ? (byte & 0xF) : (byte >> 4);
     return __fadd_rn(__fmul_rn(d, static_cast<float>(q)), m);
@@ -90,7 +123,7 @@ __global__ void __launch_bounds__(kDqThreads) k_dequant_legacy(const uint8_t* __
       const int b = o >> 3, part = o & 7;
       const uint8_t* blk = tile + b * kB;
       const float d = half_at(blk);
-      const float m = T == GQ_TYPE_Q4_1 ? half_at(blk + 2) : 0.f;
+      const float m = has_min<T>() ? half_at(blk + 2) : 0.f;
       float4 v;
       v.x = weight<T>(blk, 4 * part, d, m);
       v.y = weight<T>(blk, 4 * part + 1, d, m);
@@ -114,9 +147,28 @@ __device__ __forceinline__ float u2f(uint32_t u) { return __int_as_float(0x4B000
 
 // The raw words a lane needs for elements 4p..4p+3 (p = 0..7) of a block:
 // the scale word (d, and m for Q4_1) and the 4 code bytes.
+// Q5 part p (elements 4p..4p+3): their 4 nibbles in bits 0-3 of each byte of
+// the result, and their 4 high bits (bits 4p..4p+3 of qh) in bit 4 of each byte.
+__device__ __forceinline__ uint32_t q5_part_codes(uint32_t codes, uint32_t qh, int p) {
+  const uint32_t nib = ((p & 4) ? codes >> 4 : codes) & 0x0F0F0F0Fu;
+  const uint32_t hb = (qh >> (4 * p)) & 0xFu;  // bit i: element 4p + i
+  const uint32_t spread = (hb & 1u) | ((hb & 2u) << 7) | ((hb & 4u) << 14) | ((hb & 8u) << 21);
+  return nib | (spread << 4);
+}
+
 template <int T>
 __device__ __forceinline__ void load_part(const uint8_t* __restrict__ blk, int p, uint32_t& h, uint32_t& v) {
-  if constexpr (T == GQ_TYPE_Q4_1) {
+  if constexpr (five_bit<T>()) {
+    // 22- / 24-byte blocks of a 2-byte aligned row: 16-bit loads
+    const uint16_t* w = reinterpret_cast<const uint16_t*>(blk);
+    constexpr int qo = q5_qh_off<T>() / 2;  // qh at halfword qo, codes at qo + 2
+    h = has_min<T>() ? (static_cast<uint32_t>(__ldg(w)) | (static_cast<uint32_t>(__ldg(w + 1)) << 16))
+                     : static_cast<uint32_t>(__ldg(w));
+    const uint32_t qh = static_cast<uint32_t>(__ldg(w + qo)) | (static_cast<uint32_t>(__ldg(w + qo + 1)) << 16);
+    const int c = qo + 2 + 2 * (p & 3);
+    const uint32_t codes = static_cast<uint32_t>(__ldg(w + c)) | (static_cast<uint32_t>(__ldg(w + c + 1)) << 16);
+    v = q5_part_codes(codes, qh, p);
+  } else if constexpr (T == GQ_TYPE_Q4_1) {
     // 20-byte blocks of a 4-byte aligned row: the scale word and one code word
     const uint32_t* w = reinterpret_cast<const uint32_t*>(blk);
     h = __ldg(w);
@@ -134,7 +186,11 @@ __device__ __forceinline__ void load_part(const uint8_t* __restrict__ blk, int p
 template <int T>
 __device__ __forceinline__ void decode_part(uint32_t h, uint32_t v, float (&q)[4], float& d, float& m) {
   d = __half2float(__ushort_as_half(static_cast<uint16_t>(h & 0xFFFF)));
-  if constexpr (T == GQ_TYPE_Q4_1) {
+  if constexpr (five_bit<T>()) {
+    m = has_min<T>() ? __half2float(__ushort_as_half(static_cast<uint16_t>(h >> 16))) : 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) q[j] = u2f((v >> (8 * j)) & 0x1F) - (T == GQ_TYPE_Q5_0 ? 16.0f : 0.0f);
+  } else if constexpr (T == GQ_TYPE_Q4_1) {
     m = __half2float(__ushort_as_half(static_cast<uint16_t>(h >> 16)));
 #pragma unroll
     for (int j = 0; j < 4; ++j) q[j] = u2f((v >> (8 * j)) & 0xF);
@@ -195,7 +251,7 @@ __global__ void __launch_bounds__(256) k_mul_mat_legacy(const uint8_t* __restric
               qx = fmaf(q[i][2], xv[i].z, qx);
               qx = fmaf(q[i][3], xv[i].w, qx);
               a = fmaf(d[i], qx, a);
-              if (T == GQ_TYPE_Q4_1) a = fmaf(mn[i], (xv[i].x + xv[i].y) + (xv[i].z + xv[i].w), a);
+              if (has_min<T>()) a = fmaf(mn[i], (xv[i].x + xv[i].y) + (xv[i].z + xv[i].w), a);
             }
             acc[t] = a;
           }
@@ -269,7 +325,14 @@ __global__ void __launch_bounds__(256) k_mul_mat_legacy_bulk(const uint8_t* __re
           const int b = b0 + 4 * s2;
           if (b < nb) {
             const uint8_t* blk = row + b * kB;
-            if constexpr (T == GQ_TYPE_Q4_1) {
+            if constexpr (five_bit<T>()) {
+              const uint16_t* w16 = reinterpret_cast<const uint16_t*>(blk);
+              constexpr int qo = q5_qh_off<T>() / 2;
+              h = has_min<T>() ? (static_cast<uint32_t>(w16[0]) | (static_cast<uint32_t>(w16[1]) << 16)) : w16[0];
+              const uint32_t qh = static_cast<uint32_t>(w16[qo]) | (static_cast<uint32_t>(w16[qo + 1]) << 16);
+              const int c = qo + 2 + 2 * (part & 3);
+              v = q5_part_codes(static_cast<uint32_t>(w16[c]) | (static_cast<uint32_t>(w16[c + 1]) << 16), qh, part);
+            } else if constexpr (T == GQ_TYPE_Q4_1) {
               h = *reinterpret_cast<const uint32_t*>(blk);
               v = *reinterpret_cast<const uint32_t*>(blk + 4 + 4 * (part & 3)) >> ((part & 4) ? 4 : 0);
             } else {
@@ -296,7 +359,7 @@ __global__ void __launch_bounds__(256) k_mul_mat_legacy_bulk(const uint8_t* __re
               qx = fmaf(q[s2][2], xv[s2].z, qx);
               qx = fmaf(q[s2][3], xv[s2].w, qx);
               a = fmaf(d[s2], qx, a);
-              if (T == GQ_TYPE_Q4_1) a = fmaf(mn[s2], (xv[s2].x + xv[s2].y) + (xv[s2].z + xv[s2].w), a);
+              if (has_min<T>()) a = fmaf(mn[s2], (xv[s2].x + xv[s2].y) + (xv[s2].z + xv[s2].w), a);
             }
             acc[t] = a;
           }
@@ -338,7 +401,7 @@ __global__ void k_mul_mat_legacy_bytes(const uint8_t* __restrict__ W, int64_t M,
       for (int64_t b = lane; b < nb; b += 32) {
         const uint8_t* blk = row + b * kB;
         const float d = half_at(blk);
-        const float mn = T == GQ_TYPE_Q4_1 ? half_at(blk + 2) : 0.f;
+        const float mn = has_min<T>() ? half_at(blk + 2) : 0.f;
         for (int e = 0; e < kQK; ++e) acc = fmaf(weight<T>(blk, e, d, mn), x[b * kQK + e], acc);
       }
 #pragma unroll
@@ -405,6 +468,8 @@ int type_block_bytes(int type) {
     case GQ_TYPE_Q4_1: return Fmt<GQ_TYPE_Q4_1>::kBytes;
     case GQ_TYPE_Q8_0: return Fmt<GQ_TYPE_Q8_0>::kBytes;
     case GQ_TYPE_Q4_K: return 144;
+    case GQ_TYPE_Q5_0: return Fmt<GQ_TYPE_Q5_0>::kBytes;
+    case GQ_TYPE_Q5_1: return Fmt<GQ_TYPE_Q5_1>::kBytes;
   }
   return 0;
 }
@@ -419,12 +484,16 @@ uint64_t type_row_bytes(int type, int64_t K) {
 
 cudaError_t launch_dequant_legacy(int type, const uint8_t* W, int64_t nblocks, float* out, cudaStream_t s) {
   if (type == GQ_TYPE_Q4_1) return launch_dequant_t<GQ_TYPE_Q4_1>(W, nblocks, out, s);
+  if (type == GQ_TYPE_Q5_0) return launch_dequant_t<GQ_TYPE_Q5_0>(W, nblocks, out, s);
+  if (type == GQ_TYPE_Q5_1) return launch_dequant_t<GQ_TYPE_Q5_1>(W, nblocks, out, s);
   return launch_dequant_t<GQ_TYPE_Q8_0>(W, nblocks, out, s);
 }
 
 cudaError_t launch_mul_mat_legacy(int type, const uint8_t* W, int64_t M, int64_t K, const float* X, int64_t N,
                                   float* Y, uint64_t wait_limit_ns, cudaStream_t s) {
   if (type == GQ_TYPE_Q4_1) return launch_mul_mat_t<GQ_TYPE_Q4_1>(W, M, K, X, N, Y, wait_limit_ns, s);
+  if (type == GQ_TYPE_Q5_0) return launch_mul_mat_t<GQ_TYPE_Q5_0>(W, M, K, X, N, Y, wait_limit_ns, s);
+  if (type == GQ_TYPE_Q5_1) return launch_mul_mat_t<GQ_TYPE_Q5_1>(W, M, K, X, N, Y, wait_limit_ns, s);
   return launch_mul_mat_t<GQ_TYPE_Q8_0>(W, M, K, X, N, Y, wait_limit_ns, s);
 }
 

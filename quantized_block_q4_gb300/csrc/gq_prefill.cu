@@ -108,7 +108,11 @@ namespace {
 // super-block is itself 256 k in 144 bytes (18 bytes per 32 weights).
 template <int F>
 constexpr int fmt_block_bytes() {
-  return (F == GQ_TYPE_Q4_0 || F == GQ_TYPE_Q4_K) ? 18 : (F == GQ_TYPE_Q4_1 ? 20 : 34);
+  return (F == GQ_TYPE_Q4_0 || F == GQ_TYPE_Q4_K) ? 18
+         : F == GQ_TYPE_Q4_1                      ? 20
+         : F == GQ_TYPE_Q5_0                      ? 22
+         : F == GQ_TYPE_Q5_1                      ? 24
+                                                  : 34;
 }
 
 template <int BN, bool PAIR, int F = GQ_TYPE_Q4_0>
@@ -141,8 +145,9 @@ struct PrefillCfg {
   static constexpr int kTmemCols = 512;
   static constexpr int kRawBytes = kBM * kRawRow;  // 18432 for Q4_0
   // 16-byte words a dequantising thread loads to cover its two blocks (Q4_K:
-  // the super-block's 16-byte header and the 32 code bytes of its step)
-  static constexpr int kWinWords = F == GQ_TYPE_Q8_0 ? 5 : 3;
+  // the super-block's 16-byte header and the 32 code bytes of its step; Q5_0:
+  // 44 bytes from an offset of up to 12 into the first word)
+  static constexpr int kWinWords = F == GQ_TYPE_Q8_0 ? 5 : (F == GQ_TYPE_Q5_0 ? 4 : 3);
   static constexpr int kBBytes = kXRows * 128;
   static constexpr int kOffB = 0;
   static constexpr int kOffRaw = kOffB + S * kBBytes;
@@ -379,6 +384,39 @@ __device__ __forceinline__ void q4k_step_words(const uint32_t* v, uint32_t* o) {
   }
 }
 
+// The 32-bit little-endian value at byte offset B (a constant) of the window v.
+template <int B>
+__device__ __forceinline__ uint32_t win_word(const uint32_t* v) {
+  if constexpr (B % 4 == 0) return v[B / 4];
+  else return __funnelshift_r(v[B / 4], v[B / 4 + 1], 8 * (B % 4));
+}
+
+// One Q5_0 / Q5_1 block at byte offset B of the window: 32 elements w =
+// d*(q - 16) (exact in fp32) or d*q + m (one rounding), rounded to bf16 in
+// pairs (o[i] = elements 2i, 2i+1).
+template <int F, int B>
+__device__ __forceinline__ void q5_block_words(const uint32_t* v, uint32_t* o) {
+  constexpr int qo = F == GQ_TYPE_Q5_1 ? 4 : 2;  // high-bit word, then 16 code bytes
+  const uint32_t h = win_word<B>(v);
+  const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(h & 0xFFFF)));
+  const float m = F == GQ_TYPE_Q5_1 ? __half2float(__ushort_as_half(static_cast<uint16_t>(h >> 16))) : 0.f;
+  const uint32_t qh = win_word<B + qo>(v);
+  const uint32_t c[4] = {win_word<B + qo + 4>(v), win_word<B + qo + 8>(v), win_word<B + qo + 12>(v),
+                         win_word<B + qo + 16>(v)};
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {  // element e = 2i, 2i+1
+    float e2[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int e = 2 * i + j;
+      const uint32_t byte = (c[(e & 15) >> 2] >> (8 * (e & 3))) & 0xFF;
+      const uint32_t q = (e < 16 ? (byte & 0xF) : (byte >> 4)) | (((qh >> e) & 1u) << 4);
+      e2[j] = F == GQ_TYPE_Q5_0 ? __fmul_rn(d, code_f(q) - 16.0f) : __fadd_rn(__fmul_rn(d, code_f(q)), m);
+    }
+    o[i] = pack_bf16(e2[0], e2[1]);
+  }
+}
+
 // Group G's two blocks of a 256-k chunk row from the loaded window v (the
 // 16-byte words from byte (2*G*block bytes) & ~15 of the row; for Q4_K the
 // header and the step's code bytes).
@@ -386,6 +424,11 @@ template <int F, int G>
 __device__ __forceinline__ void step_words_fmt(const uint32_t* v, uint32_t* o) {
   if constexpr (F == GQ_TYPE_Q4_K) {
     q4k_step_words<G>(v, o);
+  } else if constexpr (F == GQ_TYPE_Q5_0 || F == GQ_TYPE_Q5_1) {
+    constexpr int bb = F == GQ_TYPE_Q5_0 ? 22 : 24;
+    constexpr int b0 = (2 * G * bb) % 16;  // the group's first block within the window
+    q5_block_words<F, b0>(v, o);
+    q5_block_words<F, b0 + bb>(v, o + 16);
   } else if constexpr (F == GQ_TYPE_Q4_1) {
     constexpr int w0 = (40 * G % 16) / 4;  // 0, 2, 0, 2
     const uint32_t c0[4] = {v[w0 + 1], v[w0 + 2], v[w0 + 3], v[w0 + 4]};
@@ -711,9 +754,16 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
         uint32_t v[4 * C::kWinWords];
         if (live) {
           const uint4* src = reinterpret_cast<const uint4*>(smem + C::kOffRaw + rslot * C::kRawBytes + raw_off);
+          const int win0 = F == GQ_TYPE_Q4_K ? 0 : (2 * C::kBlk * grp & ~15);  // window start within the row
 #pragma unroll
           for (int i = 0; i < C::kWinWords; ++i) {
-            // Q4_K: word 0 is the header, words 1-2 the code bytes at 16 + 32*grp
+            // Q4_K: word 0 is the header, words 1-2 the code bytes at 16 + 32*grp.
+            // A word that would start past the row (Q5_0's last group needs 3 of
+            // its 4) is not loaded: it holds no byte of the group's blocks.
+            if (F != GQ_TYPE_Q4_K && win0 + 16 * i >= C::kRawRow) {
+              v[4 * i] = v[4 * i + 1] = v[4 * i + 2] = v[4 * i + 3] = 0u;
+              continue;
+            }
             const uint4 x = src[(F == GQ_TYPE_Q4_K && i > 0) ? i + 2 * grp : i];
             v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
           }
@@ -1101,6 +1151,16 @@ cudaError_t launch_prefill(const CUtensorMap* tmW, const CUtensorMap* tmX, int64
     if (prefill_bn(N, M, K, allow_scratch) == 128)
       return launch_prefill_cfg<128, false, GQ_TYPE_Q8_0>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
     return launch_prefill_cfg<256, false, GQ_TYPE_Q8_0>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
+  }
+  if (type == GQ_TYPE_Q5_0) {
+    if (prefill_bn(N, M, K, allow_scratch) == 128)
+      return launch_prefill_cfg<128, false, GQ_TYPE_Q5_0>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
+    return launch_prefill_cfg<256, false, GQ_TYPE_Q5_0>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
+  }
+  if (type == GQ_TYPE_Q5_1) {
+    if (prefill_bn(N, M, K, allow_scratch) == 128)
+      return launch_prefill_cfg<128, false, GQ_TYPE_Q5_1>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
+    return launch_prefill_cfg<256, false, GQ_TYPE_Q5_1>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
   }
   if (type == GQ_TYPE_Q4_K) {
     if (prefill_bn(N, M, K, allow_scratch) == 128)

@@ -3,8 +3,8 @@
 // validation: ggml_validate_row_data checks each row's scale factors and
 // integers).  Reading: a block is invalid when one of its
 // fp16 scale fields is NaN or infinite (exponent bits all ones) -- d for
-// every format, m for Q4_1 and dmin for Q4_K; the 4-, 6- and 8-bit fields are
-// always valid.  A Q4_K block is a 256-weight super-block.
+// every format, m for Q4_1 and Q5_1 and dmin for Q4_K; the 4-, 5-, 6- and 8-bit
+// fields are always valid.  A Q4_K block is a 256-weight super-block.
 //
 // One pass over the flat block array (rows are contiguous, so row boundaries
 // do not matter): each thread tests the blocks it strides over with byte
@@ -83,9 +83,9 @@ cudaError_t launch_validate(const uint8_t* W, int64_t nblocks, int type, unsigne
   const int64_t want = (nblocks + kVThreads - 1) / kVThreads;
   cfg.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>(want, static_cast<int64_t>(device_info().sm_count) * 8)));
   cfg.blockDim = dim3(kVThreads);
-  // Q4_1's min offset and Q4_K's dmin sit in bytes 2-3, as the second fp16 field
+  // Q4_1's and Q5_1's min offset and Q4_K's dmin sit in bytes 2-3, as the second fp16 field
   return cudaLaunchKernelEx(&cfg, k_validate, W, static_cast<uint64_t>(nblocks), type_block_bytes(type),
-                            (type == GQ_TYPE_Q4_1 || type == GQ_TYPE_Q4_K) ? 1 : 0, result);
+                            (type == GQ_TYPE_Q4_1 || type == GQ_TYPE_Q4_K || type == GQ_TYPE_Q5_1) ? 1 : 0, result);
 }
 
 }  // namespace gq
