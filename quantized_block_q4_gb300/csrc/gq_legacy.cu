@@ -152,7 +152,9 @@ __device__ __forceinline__ float u2f(uint32_t u) { return __int_as_float(0x4B000
 __device__ __forceinline__ uint32_t q5_part_codes(uint32_t codes, uint32_t qh, int p) {
   const uint32_t nib = ((p & 4) ? codes >> 4 : codes) & 0x0F0F0F0Fu;
   const uint32_t hb = (qh >> (4 * p)) & 0xFu;  // bit i: element 4p + i
-  const uint32_t spread = (hb & 1u) | ((hb & 2u) << 7) | ((hb & 4u) << 14) | ((hb & 8u) << 21);
+  // bit i to bit 8i: the products hb_i * 2^(7j) land on distinct bits, so the
+  // multiply carries nothing into the mask
+  const uint32_t spread = (hb * 0x00204081u) & 0x01010101u;
   return nib | (spread << 4);
 }
 

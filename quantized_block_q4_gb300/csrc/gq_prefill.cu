@@ -310,15 +310,21 @@ __device__ __forceinline__ void block_words(const uint32_t (&q)[4], uint32_t d_b
   word_to_bf16(q[3], dhi2, dlo2, o[6], o[7], o[14], o[15]);
 }
 
-// Q4_1 and Q8_0 steps: elements as fp32 (d*q exact; Q4_1 then adds m with
-// one rounding), rounded once more to bf16 in pairs (element 2i in the low
-// half of o[i], as for Q4_0).
-__device__ __forceinline__ float code_f(uint32_t u) { return __int_as_float(0x4B000000 | u) - 8388608.0f; }
+// Byte j (a constant) of q as an exact fp32 integer: one byte permute builds
+// the float 2^23 + byte, one subtraction removes 2^23.
+template <int J>
+__device__ __forceinline__ float byte_f(uint32_t q) {
+  return __uint_as_float(prmt(q, 0x4B000000u, 0x7650u | J)) - 8388608.0f;
+}
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
 }
+
+// Q4_1 and Q8_0 steps: elements as fp32 (d*q exact; Q4_1 then adds m with
+// one rounding), rounded once more to bf16 in pairs (element 2i in the low
+// half of o[i], as for Q4_0).
 
 // One Q4_1 block: h = d | m << 16, c[4] = the 16 code bytes.
 __device__ __forceinline__ void q41_block(uint32_t h, const uint32_t (&c)[4], uint32_t* o) {
@@ -327,11 +333,12 @@ __device__ __forceinline__ void q41_block(uint32_t h, const uint32_t (&c)[4], ui
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
     float lo[4], hi[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      lo[j] = __fadd_rn(__fmul_rn(d, code_f((c[w] >> (8 * j)) & 0xF)), m);
-      hi[j] = __fadd_rn(__fmul_rn(d, code_f((c[w] >> (8 * j + 4)) & 0xF)), m);
-    }
+    const uint32_t ql = c[w] & 0x0F0F0F0Fu, qhi = (c[w] >> 4) & 0x0F0F0F0Fu;
+    // d*q is exact, so one fused multiply-add rounds d*q + m once
+    lo[0] = __fmaf_rn(d, byte_f<0>(ql), m); hi[0] = __fmaf_rn(d, byte_f<0>(qhi), m);
+    lo[1] = __fmaf_rn(d, byte_f<1>(ql), m); hi[1] = __fmaf_rn(d, byte_f<1>(qhi), m);
+    lo[2] = __fmaf_rn(d, byte_f<2>(ql), m); hi[2] = __fmaf_rn(d, byte_f<2>(qhi), m);
+    lo[3] = __fmaf_rn(d, byte_f<3>(ql), m); hi[3] = __fmaf_rn(d, byte_f<3>(qhi), m);
     o[2 * w] = pack_bf16(lo[0], lo[1]);
     o[2 * w + 1] = pack_bf16(lo[2], lo[3]);
     o[8 + 2 * w] = pack_bf16(hi[0], hi[1]);
@@ -343,12 +350,16 @@ __device__ __forceinline__ void q41_block(uint32_t h, const uint32_t (&c)[4], ui
 // 0x80 is the code + 128).
 __device__ __forceinline__ void q80_block(uint32_t d_bits, const uint32_t (&c)[8], uint32_t* o) {
   const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(d_bits)));
+  const float off = -128.0f * d;  // exact
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
-    const uint32_t u = c[w] ^ 0x80808080u;
+    const uint32_t u = c[w] ^ 0x80808080u;  // code + 128 in each byte
     float e[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) e[j] = __fmul_rn(d, code_f((u >> (8 * j)) & 0xFF) - 128.0f);
+    // d*(u - 128) = d*u - 128d, every term exact: one fused multiply-add
+    e[0] = __fmaf_rn(d, byte_f<0>(u), off);
+    e[1] = __fmaf_rn(d, byte_f<1>(u), off);
+    e[2] = __fmaf_rn(d, byte_f<2>(u), off);
+    e[3] = __fmaf_rn(d, byte_f<3>(u), off);
     o[2 * w] = pack_bf16(e[0], e[1]);
     o[2 * w + 1] = pack_bf16(e[2], e[3]);
   }
@@ -371,12 +382,12 @@ __device__ __forceinline__ void q4k_step_words(const uint32_t* v, uint32_t* o) {
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
     const uint32_t c = v[4 + w];  // code bytes 4w .. 4w+3
+    const uint32_t ql = c & 0x0F0F0F0Fu, qhi = (c >> 4) & 0x0F0F0F0Fu;
     float lo[4], hi[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      lo[j] = __fmaf_rn(d0, code_f((c >> (8 * j)) & 0xF), -mn0);
-      hi[j] = __fmaf_rn(d1, code_f((c >> (8 * j + 4)) & 0xF), -mn1);
-    }
+    lo[0] = __fmaf_rn(d0, byte_f<0>(ql), -mn0); hi[0] = __fmaf_rn(d1, byte_f<0>(qhi), -mn1);
+    lo[1] = __fmaf_rn(d0, byte_f<1>(ql), -mn0); hi[1] = __fmaf_rn(d1, byte_f<1>(qhi), -mn1);
+    lo[2] = __fmaf_rn(d0, byte_f<2>(ql), -mn0); hi[2] = __fmaf_rn(d1, byte_f<2>(qhi), -mn1);
+    lo[3] = __fmaf_rn(d0, byte_f<3>(ql), -mn0); hi[3] = __fmaf_rn(d1, byte_f<3>(qhi), -mn1);
     o[2 * w] = pack_bf16(lo[0], lo[1]);
     o[2 * w + 1] = pack_bf16(lo[2], lo[3]);
     o[16 + 2 * w] = pack_bf16(hi[0], hi[1]);
@@ -391,29 +402,35 @@ __device__ __forceinline__ uint32_t win_word(const uint32_t* v) {
   else return __funnelshift_r(v[B / 4], v[B / 4 + 1], 8 * (B % 4));
 }
 
+// Bits 0-3 of b to bit 0 of bytes 0-3 (the four products b_i * 2^(7j) land
+// on distinct bits, so the multiply carries nothing into the mask).
+__device__ __forceinline__ uint32_t spread4(uint32_t b) { return (b * 0x00204081u) & 0x01010101u; }
+
 // One Q5_0 / Q5_1 block at byte offset B of the window: 32 elements w =
-// d*(q - 16) (exact in fp32) or d*q + m (one rounding), rounded to bf16 in
-// pairs (o[i] = elements 2i, 2i+1).
+// d*(q - 16) (exact in fp32: d*q and 16d are) or d*q + m (d*q exact, one
+// rounding), rounded to bf16 in pairs (o[i] = elements 2i, 2i+1).  Per code
+// word: four 5-bit codes (nibbles with their high bits at bit 4 of each byte),
+// each byte made an fp32 2^23 + q by one byte permute.
 template <int F, int B>
 __device__ __forceinline__ void q5_block_words(const uint32_t* v, uint32_t* o) {
   constexpr int qo = F == GQ_TYPE_Q5_1 ? 4 : 2;  // high-bit word, then 16 code bytes
   const uint32_t h = win_word<B>(v);
   const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(h & 0xFFFF)));
-  const float m = F == GQ_TYPE_Q5_1 ? __half2float(__ushort_as_half(static_cast<uint16_t>(h >> 16))) : 0.f;
+  const float add = F == GQ_TYPE_Q5_1 ? __half2float(__ushort_as_half(static_cast<uint16_t>(h >> 16))) : -16.0f * d;
   const uint32_t qh = win_word<B + qo>(v);
-  const uint32_t c[4] = {win_word<B + qo + 4>(v), win_word<B + qo + 8>(v), win_word<B + qo + 12>(v),
-                         win_word<B + qo + 16>(v)};
+  const uint32_t cw[4] = {win_word<B + qo + 4>(v), win_word<B + qo + 8>(v), win_word<B + qo + 12>(v),
+                          win_word<B + qo + 16>(v)};
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {  // element e = 2i, 2i+1
-    float e2[2];
+  for (int w = 0; w < 4; ++w) {
+    const uint32_t c = cw[w];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int e = 2 * i + j;
-      const uint32_t byte = (c[(e & 15) >> 2] >> (8 * (e & 3))) & 0xFF;
-      const uint32_t q = (e < 16 ? (byte & 0xF) : (byte >> 4)) | (((qh >> e) & 1u) << 4);
-      e2[j] = F == GQ_TYPE_Q5_0 ? __fmul_rn(d, code_f(q) - 16.0f) : __fadd_rn(__fmul_rn(d, code_f(q)), m);
+    for (int half = 0; half < 2; ++half) {  // low nibbles: elements 4w.., high nibbles: 16 + 4w..
+      const uint32_t q = ((half ? c >> 4 : c) & 0x0F0F0F0Fu) | (spread4((qh >> (16 * half + 4 * w)) & 0xFu) << 4);
+      const float e[4] = {__fmaf_rn(d, byte_f<0>(q), add), __fmaf_rn(d, byte_f<1>(q), add),
+                          __fmaf_rn(d, byte_f<2>(q), add), __fmaf_rn(d, byte_f<3>(q), add)};
+      o[8 * half + 2 * w] = pack_bf16(e[0], e[1]);
+      o[8 * half + 2 * w + 1] = pack_bf16(e[2], e[3]);
     }
-    o[i] = pack_bf16(e2[0], e2[1]);
   }
 }
 
