@@ -859,9 +859,7 @@ def run_formats_aux(gq, torch, dev, s, peaks):
                         "frac": round(dq / peaks["hbm_gbs"], 4)},
             "mul_mat_n1": {"us": round(t1 * 1e6, 2), "achieved": round(g1, 1), "unit": "GB/s", "bound": "hbm",
                            "frac": round(g1 / peaks["hbm_gbs"], 4),
-                           "kernel": ("k_mul_mat_legacy_bulk<type> (scalar: no mma.sync decode for 5-bit codes)"
-                                      if name.startswith("q5") else
-                                      "k_decode_q4_0<..., type> (mma.sync decode on this block format)"),
+                           "kernel": "k_decode_q4_0<..., type> (mma.sync decode on this block format)",
                            "timing": "eager back-to-back calls (launch gaps included)"},
             "mul_mat_n512": {"us": round(tp * 1e6, 2), "achieved": round(tf, 2), "unit": "TFLOP/s",
                              "bound": "tensor", "frac": round(tf / peaks["bf16_tflops"], 4),

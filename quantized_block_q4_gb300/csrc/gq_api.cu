@@ -382,9 +382,7 @@ gq_status gq_mul_mat(gq_type type, const void* W, int64_t M, int64_t K, const fl
   // threshold, the tcgen05 kernel from it on; the scalar kernel otherwise.
   const bool fast = K % 256 == 0 && aligned(W, 16) && aligned(X, 16) && aligned(Y, 16) && !g_force_generic.load();
   const bool tc = fast && N >= g_prefill_min_n.load();
-  // (the decode kernel has no Q5 code extraction: Q5 takes the scalar kernel below 16 tokens)
-  const bool five_bit = type == GQ_TYPE_Q5_0 || type == GQ_TYPE_Q5_1;
-  if (fast && !tc && N < 16 && !five_bit) {
+  if (fast && !tc && N < 16) {
     // the decode kernel on this block format: a box row is 256 k of a weight
     // row (Q4_1 160 bytes, Q4_K 144; Q8_0's 272 bytes as 16-bit elements)
     CUtensorMap tm;

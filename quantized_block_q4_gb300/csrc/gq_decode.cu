@@ -57,9 +57,15 @@ constexpr int kSubK = 256;         // weights per row per TMA box
 constexpr int kSubBytesRow = 144;  // 8 blocks x 18 bytes (Q4_0)
 
 // Bytes of one row of a TMA box (256 weights): Q4_0 144, Q4_1 160, Q8_0 272,
-// Q4_K 144 (one super-block).
+// Q4_K 144 (one super-block), Q5_0 176, Q5_1 192.
 template <int F>
-constexpr int sub_bytes_row() { return F == GQ_TYPE_Q4_1 ? 160 : (F == GQ_TYPE_Q8_0 ? 272 : kSubBytesRow); }
+constexpr int sub_bytes_row() {
+  return F == GQ_TYPE_Q4_1   ? 160
+         : F == GQ_TYPE_Q8_0 ? 272
+         : F == GQ_TYPE_Q5_0 ? 176
+         : F == GQ_TYPE_Q5_1 ? 192
+                             : kSubBytesRow;
+}
 
 // NT: n8 token tiles (N <= 8*NT); MT: m16 row tiles per warp (tile = 16*MT
 // rows); KW: consumer warps, each taking one 256-k box of every stage; F: the
@@ -70,8 +76,8 @@ struct DecodeCfg {
   static constexpr int kBM = 16 * MT;
   static constexpr int kRowBytes = sub_bytes_row<F>();
   static constexpr int kElem = kRowBytes > 256 ? 2 : 1;  // TMA element bytes (a box is at most 256 wide)
-  // Q4_1 and Q4_K also keep per-block x sums for their min offsets
-  static constexpr int kTables = (F == GQ_TYPE_Q4_1 || F == GQ_TYPE_Q4_K) ? 2 : 1;
+  // Q4_1, Q4_K and Q5_1 also keep per-block x sums for their min offsets
+  static constexpr int kTables = (F == GQ_TYPE_Q4_1 || F == GQ_TYPE_Q4_K || F == GQ_TYPE_Q5_1) ? 2 : 1;
   static constexpr int kSubBytes = kBM * kRowBytes;
   static constexpr int kThreads = 32 * (KW + 1);
   static constexpr int kStageK = kSubK * KW;
@@ -232,6 +238,60 @@ __device__ __forceinline__ float stage_block_q4k(const float (&x)[32], uint4* ds
   return -1024.f * staged;
 }
 
+// Q5_0 / Q5_1 x staging: the natural k order (a lane owns code bytes 4t ..
+// 4t+3, as for Q4_1) with 5-bit codes: A = 1024 + q against fp16 x (low
+// nibbles) and 1024 + 16q against fp16 x/16 (high nibbles).  Q5_0's zero point
+// 16 joins the bias: 1040 * sum(x) + 1280 * sum(x/16); Q5_1 keeps 1024 times
+// the staged sums and, for its min, the x sum as the MMA sees it.
+template <int F>
+__device__ __forceinline__ float stage_block_q5(const float (&x)[32], uint4* dst, float* sx) {
+  float lo = 0.f, hi = 0.f;
+  __half xh[32];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    xh[j] = __float2half_rn(x[j]);
+    xh[16 + j] = __float2half_rn(x[16 + j] * 0.0625f);
+    lo += __half2float(xh[j]);
+    hi += __half2float(xh[16 + j]);
+  }
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const int c0 = 4 * t, c1 = 4 * t + 1, c2 = 4 * t + 2, c3 = 4 * t + 3;
+    __half2 h;
+    uint4 pk;
+    h = __halves2half2(xh[c0], xh[c2]); pk.x = *reinterpret_cast<uint32_t*>(&h);
+    h = __halves2half2(xh[c1], xh[c3]); pk.y = *reinterpret_cast<uint32_t*>(&h);
+    h = __halves2half2(xh[16 + c0], xh[16 + c2]); pk.z = *reinterpret_cast<uint32_t*>(&h);
+    h = __halves2half2(xh[16 + c1], xh[16 + c3]); pk.w = *reinterpret_cast<uint32_t*>(&h);
+    dst[t] = pk;
+  }
+  if constexpr (F == GQ_TYPE_Q5_1) {
+    *sx = fmaf(16.f, hi, lo);
+    return -1024.f * (lo + hi);
+  } else {
+    return -(1040.f * lo + 1280.f * hi);
+  }
+}
+
+// Bits 0-3 of b to bit 0 of bytes 0-3 (the four products b_i * 2^(7j) land on
+// distinct bits, so the multiply carries nothing into the mask).
+__device__ __forceinline__ uint32_t spread4(uint32_t b) { return (b * 0x00204081u) & 0x01010101u; }
+
+// A code word of a Q5 block (bytes c0..c3 = elements 4t..4t+3 low, 16+4t..
+// high) with the block's high-bit word qh -> the four f16x2 A registers of
+// biased 5-bit codes: lo02 / lo13 = 1024 + q of (c0, c2) / (c1, c3) low
+// nibbles, hi02 / hi13 = 1024 + 16q of the high ones.
+__device__ __forceinline__ void q5_codes_to_f16(uint32_t v, uint32_t qh, int t, uint32_t& lo02, uint32_t& lo13,
+                                                uint32_t& hi02, uint32_t& hi13) {
+  const uint32_t kMagic = 0x64006400u;
+  const uint32_t q5lo = (v & 0x0F0F0F0Fu) | (spread4((qh >> (4 * t)) & 0xFu) << 4);
+  const uint32_t q5hi = ((v >> 4) & 0x0F0F0F0Fu) | (spread4((qh >> (16 + 4 * t)) & 0xFu) << 4);
+  lo02 = lop3_and_or(q5lo, 0x001F001Fu, kMagic);
+  lo13 = lop3_and_or(q5lo >> 8, 0x001F001Fu, kMagic);
+  hi02 = lop3_and_or(q5hi << 4, 0x01F001F0u, kMagic);
+  hi13 = lop3_and_or(q5hi >> 4, 0x01F001F0u, kMagic);
+}
+
 // Half of the biased codes of a word of 4 code bytes (c0..c3): the low
 // nibbles as fp16 1024 + q, or the high nibbles as 1024 + 16q, in the pairs
 // (c0, c2) and (c1, c3).
@@ -294,6 +354,9 @@ __device__ __forceinline__ void stage_entry(const float (&xv)[32], uint4* dst, f
   } else if constexpr (F == GQ_TYPE_Q4_K) {
     cs[n] = stage_block_q4k(xv, dst, &sx[n], parity);  // parity: odd sub-block of its super-block
     if ((Nt & 1) && n == Nt - 1) sx[Nt] = 0.f;
+  } else if constexpr (F == GQ_TYPE_Q5_0 || F == GQ_TYPE_Q5_1) {
+    cs[n] = stage_block_q5<F>(xv, dst, &sx[n]);
+    if (F == GQ_TYPE_Q5_1 && (Nt & 1) && n == Nt - 1) sx[Nt] = 0.f;
   } else if constexpr (F == GQ_TYPE_Q8_0) {
     cs[n] = stage_block_q80(xv, dst);
   } else {
@@ -362,7 +425,7 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
     k_decode_q4_0(const __grid_constant__ CUtensorMap tmW, const float* __restrict__ X, int N, int M, int K,
                   int KX, float* __restrict__ Y, uint64_t limit_ns, uint32_t* err, int early_stages,
                   int x_static, const MoeRoute rt, int drop) {
-  static_assert(F == GQ_TYPE_Q4_0 || !MOE, "Q4_1 / Q8_0 / Q4_K run the plain MUL_MAT layout");
+  static_assert(F == GQ_TYPE_Q4_0 || !MOE, "the other block formats run the plain MUL_MAT layout");
   using Cfg = DecodeCfg<NT, MT, KW, STAGES, F>;
   constexpr int kBM = Cfg::kBM;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -641,7 +704,33 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
 #pragma unroll
               for (int r = 0; r < 2; ++r) {
                 const uint8_t* rb = sub + (mt * 16 + 8 * r) * Cfg::kRowBytes;
-                if constexpr (F == GQ_TYPE_Q4_K) {
+                if constexpr (F == GQ_TYPE_Q5_0) {
+                  // 22-byte blocks: the pair 2p, 2p+1 starts 4-byte aligned (44p).
+                  // Even block: d in the low half of word 0, qh in bytes 2-5,
+                  // code word t in bytes 6+4t..9+4t (straddling words); odd
+                  // block (byte 22): d in the high half of word 5, qh word 6,
+                  // code word t = word 7 + t.
+                  const uint32_t* w = reinterpret_cast<const uint32_t*>(rb + 44 * p);
+                  const uint32_t w0 = w[0];
+                  wd[mt][r][0] = prmt(w[1 + t], w[2 + t], 0x5432u);
+                  wh[mt][r][0] = prmt(w0, w[1], 0x5432u);
+                  wd[mt][r][1] = w[7 + t];
+                  wh[mt][r][1] = w[6];
+                  dd[mt][r][0] = half_lo(w0);
+                  dd[mt][r][1] = half_hi(w[5]);
+                  mm[mt][r][0] = mm[mt][r][1] = 0.f;
+                } else if constexpr (F == GQ_TYPE_Q5_1) {
+                  // 24-byte blocks, all fields word-aligned: d | m << 16, qh, 4 code words.
+                  const uint32_t* w = reinterpret_cast<const uint32_t*>(rb + 48 * p);
+#pragma unroll
+                  for (int e = 0; e < 2; ++e) {
+                    const uint32_t H = w[6 * e];
+                    wh[mt][r][e] = w[6 * e + 1];
+                    wd[mt][r][e] = w[6 * e + 2 + t];
+                    dd[mt][r][e] = half_lo(H);
+                    mm[mt][r][e] = half_hi(H);
+                  }
+                } else if constexpr (F == GQ_TYPE_Q4_K) {
                   // One 144-byte super-block per box row: sub-blocks 2p (low
                   // nibbles) and 2p+1 (high nibbles) of code bytes 32p .. 32p+31;
                   // a lane takes code words t and t + 4 of them.  w = d*sc*q -
@@ -734,7 +823,10 @@ __global__ void __launch_bounds__(32 * (KW + 1), (decode_min_blocks<NT, MT, KW, 
 #pragma unroll
               for (int mt = 0; mt < MT; ++mt) {
                 uint32_t a_lo[4], a_hi[4];
-                if constexpr (F == GQ_TYPE_Q4_K) {
+                if constexpr (F == GQ_TYPE_Q5_0 || F == GQ_TYPE_Q5_1) {
+                  q5_codes_to_f16(wd[mt][0][e], wh[mt][0][e], t, a_lo[0], a_lo[2], a_hi[0], a_hi[2]);
+                  q5_codes_to_f16(wd[mt][1][e], wh[mt][1][e], t, a_lo[1], a_lo[3], a_hi[1], a_hi[3]);
+                } else if constexpr (F == GQ_TYPE_Q4_K) {
                   // sub-block 2p + e: code bytes 0-15 (word wd) then 16-31 (word wh)
                   codes_half_f16(wd[mt][0][e], e, a_lo[0], a_lo[2]);
                   codes_half_f16(wd[mt][1][e], e, a_lo[1], a_lo[3]);
@@ -1059,6 +1151,12 @@ cudaError_t launch_decode_legacy(int type, const CUtensorMap* tmW, const float* 
   if (type == GQ_TYPE_Q4_K)
     return N == 1 ? launch_decode_fmt<GQ_TYPE_Q4_K>(tmW, X, M, K, Y, wait_limit_ns, early_w, pdl, s)
                   : launch_decode_fmt_n<GQ_TYPE_Q4_K>(tmW, X, N, M, K, Y, wait_limit_ns, early_w, pdl, s);
+  if (type == GQ_TYPE_Q5_0)
+    return N == 1 ? launch_decode_fmt<GQ_TYPE_Q5_0>(tmW, X, M, K, Y, wait_limit_ns, early_w, pdl, s)
+                  : launch_decode_fmt_n<GQ_TYPE_Q5_0>(tmW, X, N, M, K, Y, wait_limit_ns, early_w, pdl, s);
+  if (type == GQ_TYPE_Q5_1)
+    return N == 1 ? launch_decode_fmt<GQ_TYPE_Q5_1>(tmW, X, M, K, Y, wait_limit_ns, early_w, pdl, s)
+                  : launch_decode_fmt_n<GQ_TYPE_Q5_1>(tmW, X, N, M, K, Y, wait_limit_ns, early_w, pdl, s);
   if (type == GQ_TYPE_Q8_0)
     return N == 1 ? launch_decode_fmt<GQ_TYPE_Q8_0>(tmW, X, M, K, Y, wait_limit_ns, early_w, pdl, s)
                   : launch_decode_fmt_n<GQ_TYPE_Q8_0>(tmW, X, N, M, K, Y, wait_limit_ns, early_w, pdl, s);

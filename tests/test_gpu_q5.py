@@ -1,9 +1,10 @@
 """Q5_0 and Q5_1 on the GPU against the oracle: dequantisation bit for bit,
 MUL_MAT within |y - y_ref| <= 1e-3 * sum_k |w_k x_k| + 1e-5 (fp64 oracle) on
-the tensor-core kernel (N >= 16, K % 256 == 0, aligned) and the scalar kernel
-(every other case: fewer tokens, other K, unaligned, forced); validation of
-d (and Q5_1's m).  Inputs: synth.typed_weights (fp16 d ~ U[0.0025, 0.01], Q5_1
-m ~ U[-0.16, 0], random high-bit and code bytes) and N(0, 1) activations."""
+the mma.sync decode kernel (N < 16) and the tensor-core kernel (N >= 16), both
+for K % 256 == 0 and aligned pointers, and the scalar kernel (other K,
+unaligned, forced); validation of d (and Q5_1's m).  Inputs:
+synth.typed_weights (fp16 d ~ U[0.0025, 0.01], Q5_1 m ~ U[-0.16, 0], random
+high-bit and code bytes) and N(0, 1) activations."""
 import numpy as np
 import pytest
 
@@ -81,12 +82,46 @@ def check(qtype, M, K, N, seed, sample=None):
 
 
 @pytest.mark.parametrize("qtype", TYPES, ids=lambda t: NAMES[t])
-@pytest.mark.parametrize("M,K,N", [(256, 1024, 1), (300, 512, 3), (129, 96, 4), (77, 288, 5), (1000, 8192, 8),
-                                   (33, 1024, 15), (1, 32, 1), (64, 288, 40)])
+@pytest.mark.parametrize("M,K,N", [(129, 96, 4), (77, 288, 5), (1, 32, 1), (64, 288, 40), (300, 800, 3)])
 def test_scalar_kernel_matches_oracle(qtype, M, K, N):
-    """Fewer than 16 tokens, or K % 256 != 0: the scalar kernel (row-bulk copies
-    for aligned rows of a multiple of 16 bytes, else plain loads)."""
+    """K % 256 != 0: the scalar kernel (row-bulk copies for aligned rows of a
+    multiple of 16 bytes, else plain loads)."""
     check(qtype, M, K, N, seed=19300 + M + K + N + qtype)
+
+
+@pytest.mark.parametrize("qtype", TYPES, ids=lambda t: NAMES[t])
+@pytest.mark.parametrize("M,K,N", [(256, 1024, 1), (300, 512, 3), (1000, 8192, 8), (33, 1024, 15), (500, 4096, 9),
+                                   (700, 256, 1), (4096, 4096, 2)])
+def test_decode_kernel_matches_oracle(qtype, M, K, N):
+    """1-15 tokens with K % 256 == 0: the mma.sync decode kernel on 22- / 24-byte
+    blocks (one and two token tiles, ragged rows, several x chunks)."""
+    check(qtype, M, K, N, seed=19350 + M + K + N + qtype)
+
+
+@pytest.mark.parametrize("static", [0, 1])
+@pytest.mark.parametrize("qtype", TYPES, ids=lambda t: NAMES[t])
+@pytest.mark.parametrize("M,K", [(11008, 4096), (4096, 11008), (32000, 4096)])
+def test_decode_sweep_shapes(qtype, M, K, static):
+    """N = 1 on the sweep's shapes with and without the static promises (the
+    co-resident 4-warp CTA and the 8-warp CTA)."""
+    def run():
+        return check(qtype, M, K, 1, seed=19370 + M + static + qtype, sample=96)
+    _with_option(gq.GQ_OPT_WEIGHTS_STATIC, static, lambda: _with_option(gq.GQ_OPT_X_STATIC, static, run))
+
+
+@pytest.mark.parametrize("qtype", TYPES, ids=lambda t: NAMES[t])
+@pytest.mark.parametrize("N,x_scale", [(1, 1e-6), (5, 1e-6), (1, 1e5), (12, 1e5)])
+def test_decode_small_and_large_x(qtype, N, x_scale):
+    """Activations far below 1 (1e-6 N(0,1), O(1) weights) and beyond fp16's
+    range (1e5 N(0,1)): the decode kernel's power-of-two staging."""
+    M, K = 600, 4096
+    W = synth.typed_weights(qtype, M, K, seed=19380 + N + qtype, d_scale=100.0 if x_scale < 1 else 1.0)
+    X = synth.activations(N, K, seed=19381 + N) * np.float32(x_scale)
+    y = gq.mul_mat(qtype, dev(W), dev(X)).cpu().numpy()
+    gq.gq_sync_status()
+    y_ref, s_ref = oracle.get().mul_mat_typed(qtype, W, M, K, X, nthreads=cores())
+    assert np.isfinite(y).all()
+    assert_mul_mat_close(y, y_ref, s_ref, f"{NAMES[qtype]} x scale {x_scale} N={N}")
 
 
 @pytest.mark.parametrize("qtype", TYPES, ids=lambda t: NAMES[t])
@@ -106,10 +141,13 @@ def test_full_size_sampled_rows(qtype, M, K, N):
 
 
 @pytest.mark.parametrize("qtype", TYPES, ids=lambda t: NAMES[t])
-def test_tensor_core_and_scalar_paths_agree(qtype):
-    M, K, N = 500, 1024, 32
-    check(qtype, M, K, N, seed=19600 + qtype)
-    _with_option(gq.GQ_OPT_FORCE_GENERIC, 1, lambda: check(qtype, M, K, N, seed=19600 + qtype))
+@pytest.mark.parametrize("N", [32, 4])
+def test_fast_and_scalar_paths_agree(qtype, N):
+    """N = 32 (tensor core) and N = 4 (decode kernel), each also through the
+    scalar kernel (GQ_OPT_FORCE_GENERIC), all against the oracle."""
+    M, K = 500, 1024
+    check(qtype, M, K, N, seed=19600 + qtype + N)
+    _with_option(gq.GQ_OPT_FORCE_GENERIC, 1, lambda: check(qtype, M, K, N, seed=19600 + qtype + N))
 
 
 @pytest.mark.parametrize("qtype", TYPES, ids=lambda t: NAMES[t])
