@@ -963,10 +963,9 @@ def run_e2e(gq, torch, dev, s, W, shapes, acts1, order, L, args):
 # DRAM bytes (read + write) per launch, from one ncu capture per shape of the
 # sweep (profiles/dram_traffic_sweep_shapes.md); refresh when a kernel changes.
 MEASURED_TRAFFIC = {
-    "decode": {(4096, 4096): 9512704, (11008, 4096): 25438208, (4096, 11008): 25465856},
-    "prefill": {(4096, 4096): 13681408, (11008, 4096): 29616896, (4096, 11008): 36786688},
+    "decode": {(4096, 4096): 9512704, (11008, 4096): 25442048, (4096, 11008): 25465344},
+    "prefill": {(4096, 4096): 13681920, (11008, 4096): 29615360, (4096, 11008): 36794880},
 }
-
 
 def sweep_traffic(kind, shapes):
     """Mean measured DRAM bytes per launch over the sweep's launches, or None."""
