@@ -524,8 +524,8 @@ PER_CONFIG = [("small mat-vec", 256, 1024, [1]),
               ("14336-row prefill, 512 tokens", 14336, 4096, [512])]
 
 
-def graph_time(torch, s, fn, reps, replays=5):
-    """Best of `replays` replays of a CUDA graph of `reps` calls fn(0..reps-1), per call, seconds."""
+def graph_time(torch, s, fn, reps, replays=10):
+    """Median of `replays` replays of a CUDA graph of `reps` calls fn(0..reps-1), per call, seconds."""
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(s):
         for i in range(reps):
@@ -535,7 +535,7 @@ def graph_time(torch, s, fn, reps, replays=5):
             for i in range(reps):
                 fn(i)
     torch.cuda.synchronize()
-    best = float("inf")
+    times = []
     for _ in range(replays):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(s):
@@ -543,13 +543,13 @@ def graph_time(torch, s, fn, reps, replays=5):
             g.replay()
             e1.record(s)
         e1.synchronize()
-        best = min(best, e0.elapsed_time(e1) / reps * 1e-3)
-    return best
+        times.append(e0.elapsed_time(e1) / reps * 1e-3)
+    return statistics.median(times)
 
 
-def eager_time(torch, s, fn, reps, replays=5):
-    """Best of `replays` runs of `reps` back-to-back eager calls fn(0..reps-1), per call, seconds."""
-    best = float("inf")
+def eager_time(torch, s, fn, reps, replays=10):
+    """Median of `replays` runs of `reps` back-to-back eager calls fn(0..reps-1), per call, seconds."""
+    times = []
     with torch.cuda.stream(s):
         for i in range(reps):
             fn(i)
@@ -562,8 +562,8 @@ def eager_time(torch, s, fn, reps, replays=5):
                 fn(i)
             e1.record(s)
         e1.synchronize()
-        best = min(best, e0.elapsed_time(e1) / reps * 1e-3)
-    return best
+        times.append(e0.elapsed_time(e1) / reps * 1e-3)
+    return statistics.median(times)
 
 
 def graph_or_eager_time(gq, torch, s, fn, reps):
@@ -578,10 +578,10 @@ def graph_or_eager_time(gq, torch, s, fn, reps):
 
 
 def run_per_config(gq, torch, dev, s, peaks):
-    """Every workload besides the sweep, device-timed: a CUDA graph of
-    back-to-back calls, each on its own weight copy (together more than 4x L2,
-    so every call streams its weights from DRAM; at most 200 calls), best of
-    5 replays.  Decode shapes
+    """Every workload besides the sweep, device-timed: a CUDA graph of 50 to
+    200 back-to-back calls, each on its own weight copy (together more than
+    4x L2, so every call streams its weights from DRAM), median of 10
+    replays.  Decode shapes
     (N < 16) are timed with the x-static promise (as in the sweep) and
     without it (each call reads X only after the kernel before it ends);
     N >= 16 runs the bf16 conversion and the tensor-core kernel (the promise
@@ -594,9 +594,9 @@ def run_per_config(gq, torch, dev, s, peaks):
     try:
         for name, M, K, ns in PER_CONFIG:
             nb = gq.gq_q4_0_nbytes(M, K)
-            # enough copies for 4x L2 per graph (capped at 200 calls: the
-            # 256 x 1024 matrix stays L2-resident, a latency figure)
-            copies = min(200, max(20, int(4 * 130e6 // nb) + 1))
+            # at least 50 calls per graph, on enough copies for 4x L2 (capped
+            # at 200: the 256 x 1024 matrix stays L2-resident, a latency figure)
+            copies = min(200, max(50, int(4 * 130e6 // nb) + 1))
             W0 = torch.from_numpy(synth.q4_0_weights(M, K, seed=0x5C00 + M + K)).to(dev)
             Ws = [W0] + [W0.clone() for _ in range(copies - 1)]
             for n in ns:
@@ -640,8 +640,8 @@ def run_per_config(gq, torch, dev, s, peaks):
         gq.gq_set_option(gq.GQ_OPT_X_STATIC, old_x)
     gq.gq_sync_status(s)
     return {"peak_kind": f"HBM copy / bf16 burst ({peaks['source']})",
-            "timing": "CUDA graph of back-to-back calls, one weight copy each (> 4x L2 together, "
-                      "except the 256 x 1024 matrix: 200 copies, L2-resident), best of 5 replays, "
+            "timing": "CUDA graph of 50-200 back-to-back calls, one weight copy each (> 4x L2 together, "
+                      "except the 256 x 1024 matrix: 200 copies, L2-resident), median of 10 replays, "
                       "with GQ_OPT_WEIGHTS_STATIC", "entries": out}
 
 
