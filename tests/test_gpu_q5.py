@@ -178,3 +178,28 @@ def test_validate(qtype):
     want = (2, 13) if qtype == 5 else (1, 13)
     assert gq.validate(qtype, dev(Wf), K) == want
     assert oracle.get().validate(qtype, Wf, M, K) == want
+
+
+@pytest.mark.parametrize("qtype", [3, 4, 5], ids=["q4_k", "q5_0", "q5_1"])
+def test_empty_sizes(qtype):
+    """M, N == 0: nothing happens; K == 0: Y is zeros (the empty sum); validation
+    of an empty matrix reports nothing."""
+    L = gq._lib
+    Y = torch.full((3, 5), float("nan"), device="cuda")
+    X = torch.zeros(3, 256, device="cuda")
+    W = torch.zeros(5 * gq.TYPE_BLOCK_BYTES[qtype] * (256 // gq.TYPE_BLOCK_WEIGHTS[qtype]), dtype=torch.uint8,
+                    device="cuda")
+    assert L.gq_mul_mat(qtype, W.data_ptr(), 0, 256, X.data_ptr(), 3, Y.data_ptr(), None) == gq.GQ_OK
+    assert L.gq_mul_mat(qtype, W.data_ptr(), 5, 256, X.data_ptr(), 0, Y.data_ptr(), None) == gq.GQ_OK
+    torch.cuda.synchronize()
+    assert torch.isnan(Y).all()
+    assert L.gq_mul_mat(qtype, W.data_ptr(), 5, 0, X.data_ptr(), 3, Y.data_ptr(), None) == gq.GQ_OK
+    torch.cuda.synchronize()
+    assert (Y == 0).all()
+    out = torch.empty(1, device="cuda")
+    assert L.gq_dequant(qtype, W.data_ptr(), 0, 256, out.data_ptr(), None) == gq.GQ_OK
+    r = torch.full((2,), 7, dtype=torch.int64, device="cuda")
+    assert L.gq_validate(qtype, W.data_ptr(), 0, 256, r.data_ptr(), None) == gq.GQ_OK
+    torch.cuda.synchronize()
+    assert r.cpu().tolist() == [0, -1]  # count 0, first = UINT64_MAX read as int64
+    assert L.gq_type_nbytes(qtype, 0, 256) == 0
