@@ -244,7 +244,7 @@ static gq_status mul_mat_decode(const void* W, int64_t M, int64_t K, const float
   gq_status st = make_tmap(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, row_bytes, static_cast<uint64_t>(M), row_bytes,
                            bx, by, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (st != GQ_OK) return st;
-  cudaError_t e = launch_decode(&tm, X, N, M, K, Y, static_cast<uint64_t>(g_wait_limit_ns.load()),
+  cudaError_t e = launch_decode(&tm, DecodeBox{bx, by}, X, N, M, K, Y, static_cast<uint64_t>(g_wait_limit_ns.load()),
                                 static_cast<int>(g_early_w.load()), variant, static_cast<int>(g_pdl.load()), s);
   return e == cudaSuccess ? GQ_OK : cuda_fail(e, "decode launch");
 }
@@ -393,7 +393,7 @@ gq_status gq_mul_mat(gq_type type, const void* W, int64_t M, int64_t K, const fl
                    row_bytes / (wide ? 2 : 1), static_cast<uint64_t>(M), row_bytes, box_bytes / (wide ? 2 : 1), 32,
                    CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != GQ_OK) return st;
-    cudaError_t e = launch_decode_legacy(type, &tm, X, N, M, K, Y, static_cast<uint64_t>(g_wait_limit_ns.load()),
+    cudaError_t e = launch_decode_legacy(type, &tm, DecodeBox{box_bytes, 32}, X, N, M, K, Y, static_cast<uint64_t>(g_wait_limit_ns.load()),
                                          static_cast<int>(g_early_w.load()), static_cast<int>(g_pdl.load()), s);
     return e == cudaSuccess ? GQ_OK : cuda_fail(e, "decode launch");
   }
@@ -525,7 +525,7 @@ gq_status gq_mul_mat_id_q4_0(const void* W, int64_t n_expert, int64_t M, int64_t
     st = make_tmap(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, row_bytes, static_cast<uint64_t>(n_expert * M), row_bytes,
                    bx, by, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != GQ_OK) return st;
-    const cudaError_t e = launch_decode_moe(&tm, X, cap, n_expert, M, K, P, rt, Y, limit, pdl, s);
+    const cudaError_t e = launch_decode_moe(&tm, DecodeBox{bx, by}, X, cap, n_expert, M, K, P, rt, Y, limit, pdl, s);
     return e == cudaSuccess ? GQ_OK : cuda_fail(e, "MUL_MAT_ID decode launch");
   }
 
@@ -545,7 +545,7 @@ gq_status gq_mul_mat_id_q4_0(const void* W, int64_t n_expert, int64_t M, int64_t
     st = make_tmap(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, row_bytes, static_cast<uint64_t>(n_expert * M), row_bytes,
                    bx, by, CU_TENSOR_MAP_SWIZZLE_NONE);
     what = "MUL_MAT_ID decode launch";
-    if (st == GQ_OK) e = launch_decode_moe(&tm, X, cap, n_expert, M, K, P, rt, Y, limit, pdl, s);
+    if (st == GQ_OK) e = launch_decode_moe(&tm, DecodeBox{bx, by}, X, cap, n_expert, M, K, P, rt, Y, limit, pdl, s);
   } else if (e == cudaSuccess) {
     uint16_t* xg = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(scratch) + route_bytes);
     CUtensorMap tmW, tmX;

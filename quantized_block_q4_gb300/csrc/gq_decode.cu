@@ -948,12 +948,16 @@ int g_x_static = 0;      // the caller promises X is not written by the kernel r
 int decode_x_static() { return g_x_static; }
 
 template <int NT, int MT, int KW, int STAGES, bool ONE = false, bool MOE = false, int F = GQ_TYPE_Q4_0>
-cudaError_t launch_cfg(const CUtensorMap* tmW, const float* X, int N, int M, int K, float* Y, uint64_t limit_ns,
-                       int xs_budget, int early_w, int pdl, cudaStream_t s, const MoeRoute& rt = MoeRoute{},
-                       int64_t max_groups = 0) {
+cudaError_t launch_cfg(const CUtensorMap* tmW, const DecodeBox& box, const float* X, int N, int M, int K, float* Y,
+                       uint64_t limit_ns, int xs_budget, int early_w, int pdl, cudaStream_t s,
+                       const MoeRoute& rt = MoeRoute{}, int64_t max_groups = 0) {
   // MUL_MAT_ID needs the routing before it knows which weights to stream
   const int early_stages = (early_w && !MOE) ? std::max(1, std::min(STAGES, decode_early_stages())) : 0;
   using Cfg = DecodeCfg<NT, MT, KW, STAGES, F>;
+  // Every box lands in a ring slot of kBM rows x kRowBytes: a tensor map
+  // encoded with another box would overrun the slots, so it is refused.
+  if (box.rows != static_cast<uint32_t>(Cfg::kBM) || box.row_bytes != static_cast<uint32_t>(Cfg::kRowBytes))
+    return cudaErrorInvalidValue;
   // x chunk: a multiple of the stage width, as long as the budget allows
   int KX = (xs_budget / (2 * N)) / Cfg::kStageK * Cfg::kStageK;
   if (KX < Cfg::kStageK) KX = Cfg::kStageK;
@@ -1041,14 +1045,14 @@ void set_decode_x_static(int on) { g_x_static = on ? 1 : 0; }
 int get_decode_x_static() { return g_x_static; }
 int get_decode_early_stages() { return g_early_stages; }
 
-cudaError_t launch_decode(const CUtensorMap* tmW, const float* X, int64_t N, int64_t M, int64_t K, float* Y,
+cudaError_t launch_decode(const CUtensorMap* tmW, const DecodeBox& box, const float* X, int64_t N, int64_t M, int64_t K, float* Y,
                           uint64_t wait_limit_ns, int early_w, int variant, int pdl, cudaStream_t s) {
   const int n = static_cast<int>(N), m = static_cast<int>(M), k = static_cast<int>(K);
   if (N == 1) {
-    if (variant == 1) return launch_cfg<1, 1, 16, 4, true>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
-    if (variant == 2) return launch_cfg<1, 4, 8, 2, true>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
-    if (variant == 3) return launch_cfg<1, 2, 8, 2, true>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
-    if (variant == 4) return launch_cfg<1, 2, 4, 3, true>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    if (variant == 1) return launch_cfg<1, 1, 16, 4, true>(tmW, box, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    if (variant == 2) return launch_cfg<1, 4, 8, 2, true>(tmW, box, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    if (variant == 3) return launch_cfg<1, 2, 8, 2, true>(tmW, box, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    if (variant == 4) return launch_cfg<1, 2, 4, 3, true>(tmW, box, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
     // By default, when consecutive launches may overlap (X and W not written by
     // the previous kernel), the small 4-warp CTA lets the next launch's CTA
     // share the SM.  Measured over the 7B-like layer sequence this beats the
@@ -1056,35 +1060,35 @@ cudaError_t launch_decode(const CUtensorMap* tmW, const float* X, int64_t N, int
     // alone run faster on the 8-warp CTA; from 4 tiles per SM on (e.g. the
     // 32000-row output projection) the 8-warp CTA stays.
     if (variant == 0 && early_w && decode_x_static() && (m + 31) / 32 <= 4 * device_info().sm_count)
-      return launch_cfg<1, 2, 4, 3, true>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
-    return launch_cfg<1, 2, 8, 3, true>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+      return launch_cfg<1, 2, 4, 3, true>(tmW, box, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    return launch_cfg<1, 2, 8, 3, true>(tmW, box, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
   }
   if (N <= 8) {
-    if (variant == 2) return launch_cfg<1, 1, 8, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    if (variant == 2) return launch_cfg<1, 1, 8, 4>(tmW, box, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
     // The co-resident 4-warp CTA, as for N = 1, where it measured faster when
     // repeated: up to 4 tokens and one 32-row tile per SM (4096 x 4096: 2
     // tokens 4.95 -> 3.82 us, 4 tokens 6.23 -> 4.86 us); with 8 tokens, or
     // 11008 rows and 2 tokens, the 8-warp CTA was faster.
     if (variant == 0 && N <= 4 && early_w && decode_x_static() && (m + 31) / 32 <= device_info().sm_count)
-      return launch_cfg<1, 2, 4, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
-    return launch_cfg<1, 2, 8, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+      return launch_cfg<1, 2, 4, 3>(tmW, box, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    return launch_cfg<1, 2, 8, 3>(tmW, box, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
   }
   if (N <= 16) {
-    if (variant == 1) return launch_cfg<2, 1, 8, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
-    if (variant == 2) return launch_cfg<2, 2, 4, 3>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
-    if (variant == 3) return launch_cfg<2, 2, 4, 2>(tmW, X, n, m, k, Y, wait_limit_ns, 128 << 10, early_w, pdl, s);
-    if (variant == 4) return launch_cfg<2, 1, 4, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 128 << 10, early_w, pdl, s);
-    return launch_cfg<2, 2, 8, 2>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    if (variant == 1) return launch_cfg<2, 1, 8, 3>(tmW, box, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    if (variant == 2) return launch_cfg<2, 2, 4, 3>(tmW, box, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    if (variant == 3) return launch_cfg<2, 2, 4, 2>(tmW, box, X, n, m, k, Y, wait_limit_ns, 128 << 10, early_w, pdl, s);
+    if (variant == 4) return launch_cfg<2, 1, 4, 4>(tmW, box, X, n, m, k, Y, wait_limit_ns, 128 << 10, early_w, pdl, s);
+    return launch_cfg<2, 2, 8, 2>(tmW, box, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
   }
   if (N <= 32) {
-    if (variant == 1) return launch_cfg<4, 1, 4, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 128 << 10, early_w, pdl, s);
-    if (variant == 2) return launch_cfg<4, 2, 4, 2>(tmW, X, n, m, k, Y, wait_limit_ns, 128 << 10, early_w, pdl, s);
-    if (variant == 3) return launch_cfg<4, 1, 8, 2>(tmW, X, n, m, k, Y, wait_limit_ns, 128 << 10, early_w, pdl, s);
-    return launch_cfg<4, 1, 4, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 96 << 10, early_w, pdl, s);
+    if (variant == 1) return launch_cfg<4, 1, 4, 4>(tmW, box, X, n, m, k, Y, wait_limit_ns, 128 << 10, early_w, pdl, s);
+    if (variant == 2) return launch_cfg<4, 2, 4, 2>(tmW, box, X, n, m, k, Y, wait_limit_ns, 128 << 10, early_w, pdl, s);
+    if (variant == 3) return launch_cfg<4, 1, 8, 2>(tmW, box, X, n, m, k, Y, wait_limit_ns, 128 << 10, early_w, pdl, s);
+    return launch_cfg<4, 1, 4, 4>(tmW, box, X, n, m, k, Y, wait_limit_ns, 96 << 10, early_w, pdl, s);
   }
   // N = 33..64: two k-warps, so that a stage's x (2 * 512 * N bytes) and the
   // partial sums fit in shared memory next to the ring
-  return launch_cfg<8, 1, 2, 4>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+  return launch_cfg<8, 1, 2, 4>(tmW, box, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
 }
 
 // MUL_MAT_ID group capacity: one token for a single-token batch (its slots
@@ -1103,20 +1107,20 @@ void decode_moe_w_box(int cap, uint32_t* box_x_bytes, uint32_t* box_rows) {
   *box_rows = cap <= 16 ? 32u : 16u;
 }
 
-cudaError_t launch_decode_moe(const CUtensorMap* tmW, const float* X, int cap, int64_t E, int64_t M, int64_t K,
+cudaError_t launch_decode_moe(const CUtensorMap* tmW, const DecodeBox& box, const float* X, int cap, int64_t E, int64_t M, int64_t K,
                               int64_t P, const MoeRoute& rt, float* Y, uint64_t wait_limit_ns, int pdl,
                               cudaStream_t s) {
   const int m = static_cast<int>(M), k = static_cast<int>(K);
   const int64_t max_groups = std::min(E, P) + P / cap + 1;
   if (cap == 1)
-    return launch_cfg<1, 2, 8, 3, true, true>(tmW, X, 1, m, k, Y, wait_limit_ns, 64 << 10, 0, pdl, s, rt, max_groups);
+    return launch_cfg<1, 2, 8, 3, true, true>(tmW, box, X, 1, m, k, Y, wait_limit_ns, 64 << 10, 0, pdl, s, rt, max_groups);
   if (cap == 8)
-    return launch_cfg<1, 2, 8, 3, false, true>(tmW, X, 8, m, k, Y, wait_limit_ns, 64 << 10, 0, pdl, s, rt, max_groups);
+    return launch_cfg<1, 2, 8, 3, false, true>(tmW, box, X, 8, m, k, Y, wait_limit_ns, 64 << 10, 0, pdl, s, rt, max_groups);
   if (cap == 16)
-    return launch_cfg<2, 2, 8, 2, false, true>(tmW, X, 16, m, k, Y, wait_limit_ns, 64 << 10, 0, pdl, s, rt, max_groups);
+    return launch_cfg<2, 2, 8, 2, false, true>(tmW, box, X, 16, m, k, Y, wait_limit_ns, 64 << 10, 0, pdl, s, rt, max_groups);
   if (cap == 32)
-    return launch_cfg<4, 1, 4, 4, false, true>(tmW, X, 32, m, k, Y, wait_limit_ns, 96 << 10, 0, pdl, s, rt, max_groups);
-  return launch_cfg<8, 1, 2, 4, false, true>(tmW, X, 64, m, k, Y, wait_limit_ns, 64 << 10, 0, pdl, s, rt, max_groups);
+    return launch_cfg<4, 1, 4, 4, false, true>(tmW, box, X, 32, m, k, Y, wait_limit_ns, 96 << 10, 0, pdl, s, rt, max_groups);
+  return launch_cfg<8, 1, 2, 4, false, true>(tmW, box, X, 64, m, k, Y, wait_limit_ns, 64 << 10, 0, pdl, s, rt, max_groups);
 }
 
 // Q4_1 / Q8_0 at N = 1: the decode kernel with 20- or 34-byte blocks (32-row
@@ -1125,43 +1129,43 @@ cudaError_t launch_decode_moe(const CUtensorMap* tmW, const float* X, int cap, i
 // Q8_0's stages are 1.9x Q4_0's: one stage fewer, so that the ring fits (the
 // 8-warp CTA) and two 4-warp CTAs still share an SM.
 template <int F>
-cudaError_t launch_decode_fmt(const CUtensorMap* tmW, const float* X, int64_t M, int64_t K, float* Y,
+cudaError_t launch_decode_fmt(const CUtensorMap* tmW, const DecodeBox& box, const float* X, int64_t M, int64_t K, float* Y,
                               uint64_t wait_limit_ns, int early_w, int pdl, cudaStream_t s) {
   constexpr int kSt = F == GQ_TYPE_Q8_0 ? 2 : 3;
   const int m = static_cast<int>(M), k = static_cast<int>(K);
   if (early_w && decode_x_static() && (m + 31) / 32 <= 4 * device_info().sm_count)
-    return launch_cfg<1, 2, 4, kSt, true, false, F>(tmW, X, 1, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
-  return launch_cfg<1, 2, 8, kSt, true, false, F>(tmW, X, 1, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    return launch_cfg<1, 2, 4, kSt, true, false, F>(tmW, box, X, 1, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+  return launch_cfg<1, 2, 8, kSt, true, false, F>(tmW, box, X, 1, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
 }
 
 // 2..15 tokens: 32-row tiles and two stages (the larger blocks' rings and the
 // x fragments of up to 16 tokens must fit in shared memory beside each other).
 template <int F>
-cudaError_t launch_decode_fmt_n(const CUtensorMap* tmW, const float* X, int64_t N, int64_t M, int64_t K, float* Y,
+cudaError_t launch_decode_fmt_n(const CUtensorMap* tmW, const DecodeBox& box, const float* X, int64_t N, int64_t M, int64_t K, float* Y,
                                 uint64_t wait_limit_ns, int early_w, int pdl, cudaStream_t s) {
   constexpr int kKw = F == GQ_TYPE_Q8_0 ? 4 : 8;
   const int n = static_cast<int>(N), m = static_cast<int>(M), k = static_cast<int>(K);
   if (N <= 8)
-    return launch_cfg<1, 2, kKw, 2, false, false, F>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
-  return launch_cfg<2, 2, kKw, 2, false, false, F>(tmW, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+    return launch_cfg<1, 2, kKw, 2, false, false, F>(tmW, box, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
+  return launch_cfg<2, 2, kKw, 2, false, false, F>(tmW, box, X, n, m, k, Y, wait_limit_ns, 64 << 10, early_w, pdl, s);
 }
 
-cudaError_t launch_decode_legacy(int type, const CUtensorMap* tmW, const float* X, int64_t N, int64_t M, int64_t K,
+cudaError_t launch_decode_legacy(int type, const CUtensorMap* tmW, const DecodeBox& box, const float* X, int64_t N, int64_t M, int64_t K,
                                  float* Y, uint64_t wait_limit_ns, int early_w, int pdl, cudaStream_t s) {
   if (type == GQ_TYPE_Q4_K)
-    return N == 1 ? launch_decode_fmt<GQ_TYPE_Q4_K>(tmW, X, M, K, Y, wait_limit_ns, early_w, pdl, s)
-                  : launch_decode_fmt_n<GQ_TYPE_Q4_K>(tmW, X, N, M, K, Y, wait_limit_ns, early_w, pdl, s);
+    return N == 1 ? launch_decode_fmt<GQ_TYPE_Q4_K>(tmW, box, X, M, K, Y, wait_limit_ns, early_w, pdl, s)
+                  : launch_decode_fmt_n<GQ_TYPE_Q4_K>(tmW, box, X, N, M, K, Y, wait_limit_ns, early_w, pdl, s);
   if (type == GQ_TYPE_Q5_0)
-    return N == 1 ? launch_decode_fmt<GQ_TYPE_Q5_0>(tmW, X, M, K, Y, wait_limit_ns, early_w, pdl, s)
-                  : launch_decode_fmt_n<GQ_TYPE_Q5_0>(tmW, X, N, M, K, Y, wait_limit_ns, early_w, pdl, s);
+    return N == 1 ? launch_decode_fmt<GQ_TYPE_Q5_0>(tmW, box, X, M, K, Y, wait_limit_ns, early_w, pdl, s)
+                  : launch_decode_fmt_n<GQ_TYPE_Q5_0>(tmW, box, X, N, M, K, Y, wait_limit_ns, early_w, pdl, s);
   if (type == GQ_TYPE_Q5_1)
-    return N == 1 ? launch_decode_fmt<GQ_TYPE_Q5_1>(tmW, X, M, K, Y, wait_limit_ns, early_w, pdl, s)
-                  : launch_decode_fmt_n<GQ_TYPE_Q5_1>(tmW, X, N, M, K, Y, wait_limit_ns, early_w, pdl, s);
+    return N == 1 ? launch_decode_fmt<GQ_TYPE_Q5_1>(tmW, box, X, M, K, Y, wait_limit_ns, early_w, pdl, s)
+                  : launch_decode_fmt_n<GQ_TYPE_Q5_1>(tmW, box, X, N, M, K, Y, wait_limit_ns, early_w, pdl, s);
   if (type == GQ_TYPE_Q8_0)
-    return N == 1 ? launch_decode_fmt<GQ_TYPE_Q8_0>(tmW, X, M, K, Y, wait_limit_ns, early_w, pdl, s)
-                  : launch_decode_fmt_n<GQ_TYPE_Q8_0>(tmW, X, N, M, K, Y, wait_limit_ns, early_w, pdl, s);
-  return N == 1 ? launch_decode_fmt<GQ_TYPE_Q4_1>(tmW, X, M, K, Y, wait_limit_ns, early_w, pdl, s)
-                : launch_decode_fmt_n<GQ_TYPE_Q4_1>(tmW, X, N, M, K, Y, wait_limit_ns, early_w, pdl, s);
+    return N == 1 ? launch_decode_fmt<GQ_TYPE_Q8_0>(tmW, box, X, M, K, Y, wait_limit_ns, early_w, pdl, s)
+                  : launch_decode_fmt_n<GQ_TYPE_Q8_0>(tmW, box, X, N, M, K, Y, wait_limit_ns, early_w, pdl, s);
+  return N == 1 ? launch_decode_fmt<GQ_TYPE_Q4_1>(tmW, box, X, M, K, Y, wait_limit_ns, early_w, pdl, s)
+                : launch_decode_fmt_n<GQ_TYPE_Q4_1>(tmW, box, X, N, M, K, Y, wait_limit_ns, early_w, pdl, s);
 }
 
 cudaError_t launch_generic(const uint8_t* W, int64_t M, int64_t K, const float* X, int64_t N, float* Y,

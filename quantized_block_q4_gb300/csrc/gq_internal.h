@@ -42,11 +42,19 @@ cudaError_t launch_dequant_bytes(const uint8_t* W, int64_t nblocks, float* out, 
 
 // ---- K2: decode / small-N mul_mat (gq_decode.cu).  Needs K % 256 == 0,
 // W 16-byte aligned, N <= 64.
-cudaError_t launch_decode(const CUtensorMap* tmW, const float* X, int64_t N, int64_t M, int64_t K,
+// The W box a decode tensor map was encoded with (rows, and bytes of a box
+// row); the launch is refused (cudaErrorInvalidValue) unless it is the box the
+// chosen tile layout expects (decode_w_box / decode_moe_w_box, or 32 rows of
+// 256 weights for the other block formats).
+struct DecodeBox {
+  uint32_t row_bytes = 0;
+  uint32_t rows = 0;
+};
+cudaError_t launch_decode(const CUtensorMap* tmW, const DecodeBox& box, const float* X, int64_t N, int64_t M, int64_t K,
                           float* Y, uint64_t wait_limit_ns, int early_w, int variant, int pdl, cudaStream_t s);
 // Q4_1 / Q8_0, N <= 15: the decode kernel on 20- / 34-byte blocks; tmW boxes of
 // 32 rows x 160 bytes (Q4_1, 8-bit elements) or 32 rows x 136 16-bit elements (Q8_0).
-cudaError_t launch_decode_legacy(int type, const CUtensorMap* tmW, const float* X, int64_t N, int64_t M, int64_t K,
+cudaError_t launch_decode_legacy(int type, const CUtensorMap* tmW, const DecodeBox& box, const float* X, int64_t N, int64_t M, int64_t K,
                                  float* Y, uint64_t wait_limit_ns, int early_w, int pdl, cudaStream_t s);
 // TMA box the decode kernel expects for W (rows of raw blocks viewed as bytes).
 void decode_w_box(int64_t N, int variant, uint32_t* box_x_bytes, uint32_t* box_rows);
@@ -125,7 +133,7 @@ cudaError_t launch_prefill_moe(const CUtensorMap* tmW, const CUtensorMap* tmX, i
 // capacity the launch will use through decode_moe_cap first.
 int decode_moe_cap(int64_t P, int64_t E, int64_t T);
 void decode_moe_w_box(int cap, uint32_t* box_x_bytes, uint32_t* box_rows);
-cudaError_t launch_decode_moe(const CUtensorMap* tmW, const float* X, int cap, int64_t E, int64_t M, int64_t K,
+cudaError_t launch_decode_moe(const CUtensorMap* tmW, const DecodeBox& box, const float* X, int cap, int64_t E, int64_t M, int64_t K,
                               int64_t P, const MoeRoute& rt, float* Y, uint64_t wait_limit_ns, int pdl,
                               cudaStream_t s);
 
