@@ -981,6 +981,7 @@ PROFILE_CASES = {
     "decode_down": (4096, 11008, 1, "f32"),
     "decode_small": (4096, 4096, 1, "f32"),
     "decode_big": (32000, 4096, 1, "f32"),
+    "decode_big_n8": (32000, 4096, 8, "f32"),
     "prefill": (14336, 4096, 512, "bf16"),
     "prefill_small": (4096, 4096, 512, "bf16"),
     "prefill_gate": (11008, 4096, 512, "bf16"),
