@@ -852,10 +852,13 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
       }
       const int m = static_cast<int>(sg.t / wk.ntn) * (C::kBM * C::kCtas) + static_cast<int>(rank) * C::kBM + row;
       const int n0 = static_cast<int>(sg.t % wk.ntn) * BN;
+      // Columns n0 + ncols .. n0 + BN - 1 are past N (their x rows were zero
+      // fill): neither stored, published nor reduced.
+      const int ncols = min(BN, N - n0);
       if (sg.r0 == 0 && sg.r1 == nr) {
         if (live) {
 #pragma unroll 1
-          for (int cb = cb0; cb < cb1; ++cb) {
+          for (int cb = cb0; cb < cb1 && cb * 32 < ncols; ++cb) {
             uint32_t v32[32];
             tmem_ld_32x32b_x32(lane_addr + cb * 32, v32);
             tmem_ld_wait();
@@ -884,7 +887,7 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
           if (live) {  // publish this split's partial tile
             float* p = wk.ws + (static_cast<int64_t>(gi) * C::kCtas + rank) * C::kSlotFloats + row;
 #pragma unroll 1
-            for (int cb = cb0; cb < cb1; ++cb) {
+            for (int cb = cb0; cb < cb1 && cb * 32 < ncols; ++cb) {
               uint32_t v32[32];
               tmem_ld_32x32b_x32(lane_addr + cb * 32, v32);
               tmem_ld_wait();
@@ -905,7 +908,7 @@ __global__ void __launch_bounds__(PrefillCfg<BN, PAIR, F>::kThreads, 1)
         if (last && live) {
           __threadfence();
 #pragma unroll 1
-          for (int hb = 2 * cb0; hb < 2 * cb1; ++hb) {  // 16-column halves of this group's blocks
+          for (int hb = 2 * cb0; hb < 2 * cb1 && hb * 16 < ncols; ++hb) {  // 16-column halves of this group's blocks
             float acc[16];
 #pragma unroll 1
             for (int g = ga; g < ga + nsplit; ++g) {

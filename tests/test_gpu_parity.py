@@ -281,10 +281,13 @@ def _with_option(code, val, fn):
 # summed in k order by whichever piece arrives last).  T = ceil(M/128) *
 # ceil(N/BN) tiles of K/256 chunks; n is capped at the chunk count.
 #   384x1024 (4 chunks), N=300: 2, 3, 4 and 7 (-> 4) pieces; N=100: the 128-wide tile;
-#   640x2048 (8 chunks), N=513: 3 and 8 pieces; 130 rows: ragged last row block.
+#   640x2048 (8 chunks), N=513: 3 and 8 pieces; 130 rows: ragged last row block;
+#   N = 16, 17, 40: a 128-wide tile with 16, 17 or 40 valid columns (only those
+#   are published and reduced).
 @pytest.mark.parametrize("M,K,N,n", [(384, 1024, 300, 2), (384, 1024, 300, 3), (384, 1024, 300, 4),
                                      (384, 1024, 300, 7), (384, 1024, 100, 2), (640, 2048, 513, 3),
-                                     (640, 2048, 513, 8), (130, 1024, 257, 3)])
+                                     (640, 2048, 513, 8), (130, 1024, 257, 3), (384, 1024, 16, 4),
+                                     (384, 1024, 17, 3), (640, 2048, 40, 2)])
 def test_prefill_split_every_tile(M, K, N, n):
     _with_option(gq.GQ_OPT_PREFILL_STREAMK, n, lambda: check_mm(M, K, N, 5200 + M + N + n, f"k-split n={n}"))
 
@@ -345,6 +348,19 @@ def test_prefill_full_size_split_sampled_rows(M, K, tile_n):
     rows = sampled_rows(M, 128, 43)
     y_ref, s_ref = oracle_mul_mat(W.reshape(M, -1)[rows], len(rows), K, X)
     assert_mul_mat_close(y[:, rows], y_ref, s_ref, f"{M}x{K} tile_n={tile_n}")
+
+
+@pytest.mark.parametrize("M,K,N", [(4096, 4096, 16), (4096, 11008, 24), (32000, 4096, 16)])
+def test_prefill_small_batch_full_size_sampled_rows(M, K, N):
+    """The small-batch shapes on the tensor-core kernel under the planner's
+    choice (4096 x 4096 at 16 tokens: 32 tiles split in 4 along k; 32000 x
+    4096: two waves of whole tiles).  Sampled rows against the oracle."""
+    W = synth.q4_0_weights(M, K, seed=synth.seed_for(3, M + K + N))
+    X = synth.activations(N, K, seed=synth.seed_for(3, M + K + N + 1))
+    y = run_mm(W, X, M, K)
+    rows = sampled_rows(M, 128, 47)
+    y_ref, s_ref = oracle_mul_mat(W.reshape(M, -1)[rows], len(rows), K, X)
+    assert_mul_mat_close(y[:, rows], y_ref, s_ref, f"{M}x{K} N={N}")
 
 
 def test_f32_to_bf16_matches_torch_rounding():
