@@ -259,7 +259,7 @@ static gq_status mul_mat_prefill_bf16(const void* W, int64_t M, int64_t K, const
   CUtensorMap tmW, tmX;
   uint32_t wbx, web, wby, xbk, xbr;
   if (Kw <= 0) Kw = K;
-  prefill_boxes(N, M, Kw, allow_scratch, type, &wbx, &web, &wby, &xbk, &xbr);
+  prefill_boxes(N, M, Kw, allow_scratch, x_static && g_pdl.load() != 0, type, &wbx, &web, &wby, &xbk, &xbr);
   const uint64_t row_bytes = type_row_bytes(type, Kw);
   gq_status st = make_tmap(&tmW, web == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, W,
                            row_bytes / web, static_cast<uint64_t>(M), row_bytes, wbx, wby, CU_TENSOR_MAP_SWIZZLE_NONE);

@@ -95,9 +95,11 @@ int get_prefill_pair_mode();
 int get_prefill_bn_override();
 // TMA boxes of the prefill kernel: W rows of one 256-k chunk as w_box_x
 // elements of w_elem_bytes each (1, or 2 when the chunk is wider than 256 bytes).
-// The tile width depends on the shape and on whether tiles may be split
-// (allow_split), so the same arguments must reach launch_prefill.
-void prefill_boxes(int64_t N, int64_t M, int64_t K, bool allow_split, int type, uint32_t* w_box_x,
+// The tile width depends on the shape, on whether tiles may be split
+// (allow_split) and on whether the launch overlaps its neighbours on the
+// stream (overlap: pdl and x_static), so the same arguments must reach
+// launch_prefill.
+void prefill_boxes(int64_t N, int64_t M, int64_t K, bool allow_split, bool overlap, int type, uint32_t* w_box_x,
                    uint32_t* w_elem_bytes, uint32_t* w_box_rows, uint32_t* x_box_k, uint32_t* x_box_rows);
 
 // ---- KR / KG: MUL_MAT_ID routing and activation gather (gq_moe.cu)

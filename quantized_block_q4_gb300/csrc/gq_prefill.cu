@@ -985,7 +985,12 @@ constexpr int64_t split_fixup_cost(int64_t s) { return 830 + 150 * (s - 2); }
 // tiles per range, and the rem = T % P left over either as one more whole
 // tile for rem ranges or, when the cost model says it is faster, split
 // s = P / rem ways along k.  Returns the estimated cost.
-int64_t prefill_plan(int64_t T, int64_t nr, int64_t P, bool allow_split, int bn, PrefillWork* wk) {
+// overlap: the launch runs its main loop beside the launches before and after
+// it on the stream (the x-static promise under programmatic dependent launch),
+// and they take the SMs it leaves idle.  Its own span then matters less than
+// the SM time it uses, which a split only adds to (the hand-off), so its
+// tiles stay whole.
+int64_t prefill_plan(int64_t T, int64_t nr, int64_t P, bool allow_split, int bn, PrefillWork* wk, bool overlap) {
   if (g_slots > 0) P = g_slots;
   P = std::max<int64_t>(P, 1);
   const PlanCost c = plan_cost(bn);
@@ -1003,7 +1008,7 @@ int64_t prefill_plan(int64_t T, int64_t nr, int64_t P, bool allow_split, int bn,
     wk->G = T * wk->s;
     return whole;
   }
-  if (rem == 0) return whole;
+  if (rem == 0 || overlap) return whole;
   const int64_t s = std::min(P / rem, nr / 2);
   if (s < 2) return whole;
   const int64_t split =
@@ -1035,7 +1040,7 @@ cudaError_t launch_prefill_cfg(const CUtensorMap* tmW, const CUtensorMap* tmX, i
   wk.early_w = pdl && early_w;
   wk.x_static = pdl && x_static;
   wk.drop = test_drop() == 2 ? 1 : 0;
-  prefill_plan(T, nr, device_info().sm_count / C::kCtas, allow_scratch, BN, &wk);
+  prefill_plan(T, nr, device_info().sm_count / C::kCtas, allow_scratch, BN, &wk, wk.x_static != 0);
   void* scratch = nullptr;
   if (wk.R > 0) {  // split tiles: partial-tile slots and arrival counters
     const size_t ws_bytes =
@@ -1088,14 +1093,17 @@ int g_bn_override = 0;  // 0: choose by shape; 128 or 256: force the tile width 
 // Tile width: 128 tokens up to N = 128; beyond, whichever of 128 and 256 the
 // cost model above rates faster for this shape (e.g. 4096 x 4096 x 512: 64
 // tiles of 256 tokens leave 88 of 152 SMs idle or split tiles, 128 tiles of
-// 128 tokens do not).
-int prefill_bn(int64_t N, int64_t M, int64_t K, bool allow_split) {
+// 128 tokens do not).  Under overlap (see prefill_plan) the SMs a launch
+// leaves idle go to its neighbours, and 256-token tiles take the least SM
+// time (a 64-k step costs about as much at either width).
+int prefill_bn(int64_t N, int64_t M, int64_t K, bool allow_split, bool overlap) {
   if (g_bn_override) return g_bn_override;
   if (N <= 128) return 128;
+  if (overlap) return 256;
   const int64_t P = device_info().sm_count, rows = (M + 127) / 128, nr = K / 256;
   PrefillWork w128{}, w256{};
-  const int64_t c128 = prefill_plan(rows * ((N + 127) / 128), nr, P, allow_split, 128, &w128);
-  const int64_t c256 = prefill_plan(rows * ((N + 255) / 256), nr, P, allow_split, 256, &w256);
+  const int64_t c128 = prefill_plan(rows * ((N + 127) / 128), nr, P, allow_split, 128, &w128, false);
+  const int64_t c256 = prefill_plan(rows * ((N + 255) / 256), nr, P, allow_split, 256, &w256, false);
   return c128 < c256 ? 128 : 256;
 }
 
@@ -1108,7 +1116,7 @@ bool use_pair(int64_t N) { return g_pair_mode && g_bn_override == 0 && N > 128; 
 void set_prefill_bn_override(int bn) { g_bn_override = bn; }
 int get_prefill_bn_override() { return g_bn_override; }
 
-void prefill_boxes(int64_t N, int64_t M, int64_t K, bool allow_split, int type, uint32_t* w_box_x,
+void prefill_boxes(int64_t N, int64_t M, int64_t K, bool allow_split, bool overlap, int type, uint32_t* w_box_x,
                    uint32_t* w_elem_bytes, uint32_t* w_box_rows, uint32_t* x_box_k, uint32_t* x_box_rows) {
   const uint32_t raw_row = static_cast<uint32_t>(type_row_bytes(type, 256));  // 256 k of a row
   *w_elem_bytes = raw_row > 256 ? 2u : 1u;
@@ -1116,7 +1124,7 @@ void prefill_boxes(int64_t N, int64_t M, int64_t K, bool allow_split, int type, 
   *w_box_rows = 128;
   *x_box_k = 64;
   *x_box_rows = (type == GQ_TYPE_Q4_0 && use_pair(N)) ? 128u
-                                                        : static_cast<uint32_t>(prefill_bn(N, M, K, allow_split));
+                                                        : static_cast<uint32_t>(prefill_bn(N, M, K, allow_split, overlap));
 }
 
 void set_prefill_pair_mode(int on) { g_pair_mode = on ? 1 : 0; }
@@ -1162,33 +1170,34 @@ cudaError_t launch_prefill(const CUtensorMap* tmW, const CUtensorMap* tmX, int64
                            float* Y, uint64_t wait_limit_ns, bool allow_scratch, int early_w, int x_static, int pdl,
                            cudaStream_t s, int type) {
   const int n = static_cast<int>(N), m = static_cast<int>(M), k = static_cast<int>(K);
+  const bool overlap = pdl && x_static;
   if (type == GQ_TYPE_Q4_1) {
-    if (prefill_bn(N, M, K, allow_scratch) == 128)
+    if (prefill_bn(N, M, K, allow_scratch, overlap) == 128)
       return launch_prefill_cfg<128, false, GQ_TYPE_Q4_1>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
     return launch_prefill_cfg<256, false, GQ_TYPE_Q4_1>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
   }
   if (type == GQ_TYPE_Q8_0) {
-    if (prefill_bn(N, M, K, allow_scratch) == 128)
+    if (prefill_bn(N, M, K, allow_scratch, overlap) == 128)
       return launch_prefill_cfg<128, false, GQ_TYPE_Q8_0>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
     return launch_prefill_cfg<256, false, GQ_TYPE_Q8_0>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
   }
   if (type == GQ_TYPE_Q5_0) {
-    if (prefill_bn(N, M, K, allow_scratch) == 128)
+    if (prefill_bn(N, M, K, allow_scratch, overlap) == 128)
       return launch_prefill_cfg<128, false, GQ_TYPE_Q5_0>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
     return launch_prefill_cfg<256, false, GQ_TYPE_Q5_0>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
   }
   if (type == GQ_TYPE_Q5_1) {
-    if (prefill_bn(N, M, K, allow_scratch) == 128)
+    if (prefill_bn(N, M, K, allow_scratch, overlap) == 128)
       return launch_prefill_cfg<128, false, GQ_TYPE_Q5_1>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
     return launch_prefill_cfg<256, false, GQ_TYPE_Q5_1>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
   }
   if (type == GQ_TYPE_Q4_K) {
-    if (prefill_bn(N, M, K, allow_scratch) == 128)
+    if (prefill_bn(N, M, K, allow_scratch, overlap) == 128)
       return launch_prefill_cfg<128, false, GQ_TYPE_Q4_K>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
     return launch_prefill_cfg<256, false, GQ_TYPE_Q4_K>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
   }
   if (use_pair(N)) return launch_prefill_cfg<256, true>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
-  if (prefill_bn(N, M, K, allow_scratch) == 128) return launch_prefill_cfg<128, false>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
+  if (prefill_bn(N, M, K, allow_scratch, overlap) == 128) return launch_prefill_cfg<128, false>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
   return launch_prefill_cfg<256, false>(tmW, tmX, n, m, k, Y, wait_limit_ns, allow_scratch, early_w, x_static, pdl, s);
 }
 
