@@ -10,8 +10,9 @@
 //   fp32 division rounded to nearest even, q = 8 when d == 0 or the quotient is
 //   NaN.  The low nibble of qs[j] is element j, the high nibble element j+16.
 // One thread per block (the fp32 rows are contiguous and K % 32 == 0, so block
-// b starts at float 32*b); a warp stages its 32 packed blocks (576 bytes) in
-// shared memory and writes them out with coalesced 16-byte stores.  HBM-bound:
+// b starts at float 32*b); a warp reads its 32 blocks (4 KB) with coalesced
+// 16-byte loads through shared memory, and stages its 32 packed blocks (576
+// bytes) there to write them out with coalesced 16-byte stores.  HBM-bound:
 // 128 bytes read and 18 written per block.
 #include <algorithm>
 #include <cuda_fp16.h>
@@ -23,42 +24,55 @@ namespace {
 
 constexpr int kQThreads = 256;
 
+// The exact quotient's code, for the rare element whose w * RN(1/d) lies next
+// to a half-integer (out of line, so that the usual loop stays short).
+__device__ __noinline__ uint32_t code_by_division(float w, float d) {
+  const int qi = __float2int_rn(__fdiv_rn(w, d)) + 8;  // a NaN quotient converts to 0: code 8
+  return static_cast<uint32_t>(min(max(qi, 0), 15));
+}
+
 __device__ __forceinline__ void quantize_one(const float (&w)[32], uint8_t* dst) {
-  float amax = 0.f, m = 0.f;
+  // m: the first weight of largest magnitude (NaNs never win the comparison)
+  float amax = 0.f;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const float a = fabsf(w[j]);
-    if (a > amax) {
-      amax = a;
-      m = w[j];
-    }
-  }
+  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(w[j]));
+  float m = 0.f;
+#pragma unroll
+  for (int j = 31; j >= 0; --j) m = fabsf(w[j]) == amax ? w[j] : m;
   const uint16_t d_bits = amax > 0.f ? __half_as_ushort(__float2half_rn(m / -8.0f)) : static_cast<uint16_t>(0);
   const float d = __half2float(__ushort_as_half(d_bits));
-  // rint(w / d) with the IEEE quotient: w * RN(1/d) is within 2 ulps of the
-  // rounded quotient (|w / d| <= 8.01), so the two can round to different
-  // integers only next to a half-integer; there the division itself decides.
-  const float r = __frcp_rn(d);
-  uint32_t q[32];
+  uint32_t packed[4] = {0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u};  // d == 0: every code 8
+  if (d != 0.f) {
+    // rint(w / d) with the IEEE quotient: w * RN(1/d) is within 2 ulps of the
+    // rounded quotient (|w / d| <= 8.01), so the two can round to different
+    // integers only next to a half-integer; there the division itself decides.
+    // A NaN quotient (w NaN, or w and d infinite) converts to 0: code 8.
+    const float r = __frcp_rn(d);
+    uint32_t q[32];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    if (d == 0.f) {
-      q[j] = 8;
-    } else {
-      float u = w[j] * r;
-      float h = rintf(u);
-      if (fabsf(u - h) > 0.5f - 1e-4f) h = rintf(__fdiv_rn(w[j], d));
-      const float t = h + 8.0f;
-      q[j] = (t != t) ? 8u : (t < 0.f ? 0u : (t > 15.f ? 15u : static_cast<uint32_t>(t)));
+    for (int j = 0; j < 32; ++j) {
+      const float u = w[j] * r;
+      const float h = rintf(u);
+      if (fabsf(u - h) > 0.5f - 1e-4f) {
+        q[j] = code_by_division(w[j], d);
+      } else {
+        const int qi = static_cast<int>(h) + 8;
+        q[j] = static_cast<uint32_t>(min(max(qi, 0), 15));
+      }
     }
+    // byte b of the codes: element b in the low nibble, element b + 16 in the high one
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      packed[i] = (q[4 * i] | (q[4 * i + 16] << 4)) | ((q[4 * i + 1] | (q[4 * i + 17] << 4)) << 8) |
+                  ((q[4 * i + 2] | (q[4 * i + 18] << 4)) << 16) | ((q[4 * i + 3] | (q[4 * i + 19] << 4)) << 24);
   }
   // 18 bytes at an even offset: nine 16-bit stores
   uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);
   d16[0] = d_bits;
 #pragma unroll
-  for (int j = 0; j < 16; j += 2) {
-    const uint32_t b0 = q[j] | (q[j + 16] << 4), b1 = q[j + 1] | (q[j + 17] << 4);
-    d16[1 + j / 2] = static_cast<uint16_t>(b0 | (b1 << 8));
+  for (int i = 0; i < 4; ++i) {
+    d16[1 + 2 * i] = static_cast<uint16_t>(packed[i]);
+    d16[2 + 2 * i] = static_cast<uint16_t>(packed[i] >> 16);
   }
 }
 
@@ -66,10 +80,30 @@ __global__ void __launch_bounds__(kQThreads)
     k_quantize_q4_0(const float* __restrict__ W, int64_t nblocks, uint8_t* __restrict__ out, int vec_in,
                     int vec_out) {
   __shared__ __align__(16) uint8_t stage[kQThreads / 32][32 * 18];
+  // A warp's 32 blocks of fp32 weights, read with coalesced 16-byte loads;
+  // rows padded to 36 floats, so that both the row-major writes and each
+  // lane's reads of its own block are free of bank conflicts.
+  __shared__ __align__(16) float xin[kQThreads / 32][32 * 36];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t b0 = (static_cast<int64_t>(blockIdx.x) * kQThreads) + warp * 32;  // first block of this warp
   const int64_t b = b0 + lane;
-  if (b < nblocks) {
+  if (vec_in && b0 + 32 <= nblocks) {
+    const float4* src4 = reinterpret_cast<const float4*>(W + b0 * 32);  // 1024 contiguous floats
+    float* xs = xin[warp];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int f = 4 * (32 * i + lane);  // first float of this load within the warp's blocks
+      *reinterpret_cast<float4*>(xs + (f >> 5) * 36 + (f & 31)) = __ldg(src4 + 32 * i + lane);
+    }
+    __syncwarp();
+    float w[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 v = *reinterpret_cast<const float4*>(xs + lane * 36 + 4 * i);
+      w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+    }
+    quantize_one(w, &stage[warp][lane * 18]);
+  } else if (b < nblocks) {
     float w[32];
     const float* src = W + b * 32;
     if (vec_in) {
