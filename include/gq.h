@@ -213,8 +213,9 @@ gq_status gq_mul_mat_id_q4_0(const void *W, int64_t n_expert, int64_t M, int64_t
  * each row up with zero blocks (d = +0, every code 8).  The blocks are copied
  * unchanged: the prepared matrix holds the same weights.  out needs
  * gq_prepared_q4_0_nbytes(M, K) bytes, 16-byte aligned; W any alignment.
- * Errors: K % 32 != 0, negative sizes or row_stride shorter than a row ->
- * GQ_ERR_SHAPE; NULL -> GQ_ERR_NULL; out unaligned -> GQ_ERR_ALIGN. */
+ * Errors: K % 32 != 0, negative sizes, row_stride shorter than a row or a
+ * prepared row above 2^31 bytes -> GQ_ERR_SHAPE; NULL -> GQ_ERR_NULL; out
+ * unaligned -> GQ_ERR_ALIGN. */
 size_t gq_prepared_q4_0_nbytes(int64_t M, int64_t K);
 gq_status gq_prepare_q4_0(const void *W, int64_t M, int64_t K, int64_t row_stride, void *out, void *stream);
 

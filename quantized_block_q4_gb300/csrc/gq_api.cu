@@ -587,6 +587,8 @@ gq_status gq_prepare_q4_0(const void* W, int64_t M, int64_t K, int64_t row_strid
   if (!W || !out) return fail(GQ_ERR_NULL, "W and out must not be NULL");
   if (!aligned(out, 16)) return fail(GQ_ERR_ALIGN, "out must be 16-byte aligned");
   if ((unsigned __int128)M * row_stride > ((unsigned __int128)1 << 62)) return fail(GQ_ERR_SHAPE, "size overflows");
+  if (prepared_row_bytes(K) > INT32_MAX)
+    return fail(GQ_ERR_SHAPE, "K=%lld: a prepared row would exceed 2^31 bytes", (long long)K);
   gq_status st = check_device();
   if (st != GQ_OK) return st;
   cudaError_t e = launch_prepare_q4_0(static_cast<const uint8_t*>(W), M, K, row_stride, static_cast<uint8_t*>(out),
