@@ -68,6 +68,10 @@ def test_quantize_special_blocks():
     W[0, 192:224] = 1.0                              # all equal: d = -1/8, every code 0
     W[0, 224:256] = np.arange(32) - 16.0
     check(W, "special blocks")
+    # the same blocks in whole warps of 32 blocks (the coalesced-load path),
+    # one row of 64 blocks and four rows of 16
+    check(np.tile(W, (1, 8)), "special blocks, whole warps")
+    check(np.tile(W, (4, 2)), "special blocks, four rows")
 
 
 def test_quantize_unaligned_pointers():
