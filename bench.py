@@ -623,17 +623,20 @@ def run_per_config(gq, torch, dev, s, peaks):
                               "frac": round(tf / tc, 4), "bound": "tensor", "peak": tc,
                               "weight_gbs": round(nb / t / 1e9, 1),
                               "kernel": "k_f32_to_bf16 + k_prefill_q4_0 (tcgen05)"})
-                    if n >= 512:
-                        Xb = X.to(torch.bfloat16).view(torch.int16)
-                        e["tensor_core_kernel_only"] = {}
-                        for xs, key in ((1, "x_static"), (0, "dependent")):
-                            gq.gq_set_option(gq.GQ_OPT_X_STATIC, xs)
-                            t3, how3 = graph_or_eager_time(gq, torch, s, lambda i: gq.gq_mul_mat_q4_0_bf16x(
-                                Ws[i % copies], M, K, Xb, n, Y, stream=s), copies)
-                            tf3 = 2 * M * K * n / t3 / 1e12
-                            e["tensor_core_kernel_only"][key] = {"us": round(t3 * 1e6, 2), "achieved": round(tf3, 2),
-                                                                 "unit": "TFLOP/s", "frac": round(tf3 / tc, 4),
-                                                                 "timing": how3}
+                    # the tensor-core kernel alone (bf16 X given), with and
+                    # without the x-static promise
+                    Xb = X.to(torch.bfloat16).view(torch.int16)
+                    e["tensor_core_kernel_only"] = {}
+                    for xs, key in ((1, "x_static"), (0, "dependent")):
+                        gq.gq_set_option(gq.GQ_OPT_X_STATIC, xs)
+                        t3, how3 = graph_or_eager_time(gq, torch, s, lambda i: gq.gq_mul_mat_q4_0_bf16x(
+                            Ws[i % copies], M, K, Xb, n, Y, stream=s), copies)
+                        tf3 = 2 * M * K * n / t3 / 1e12
+                        e["tensor_core_kernel_only"][key] = {"us": round(t3 * 1e6, 2), "achieved": round(tf3, 2),
+                                                             "unit": "TFLOP/s", "frac": round(tf3 / tc, 4),
+                                                             "weight_gbs": round(nb / t3 / 1e9, 1),
+                                                             "weight_frac_of_hbm": round(nb / t3 / 1e9 / hbm, 4),
+                                                             "timing": how3}
                 out.append(e)
             del Ws, W0
     finally:
