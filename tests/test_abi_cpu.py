@@ -82,6 +82,11 @@ def test_argument_errors_before_any_device_work(lib):
     assert L.gq_validate(0, None, 4, 32, None, None) == lib.GQ_ERR_NULL                 # no result
     assert L.gq_validate_q4_0(None, 4, 32, 8 * 1024 + 4, None) == lib.GQ_ERR_ALIGN      # result misaligned
     assert L.gq_validate_q4_0(None, 4, 32, 8 * 1024, None) == lib.GQ_ERR_NULL           # W NULL, M*K > 0
+    # the repack: a prepared row of K = 2^32 weights would exceed 2^31 bytes (no
+    # device access: the pointers are never dereferenced)
+    assert L.gq_prepare_q4_0(256, 1, 1 << 32, 0, 256, None) == lib.GQ_ERR_SHAPE
+    assert "2^31" in lib.gq_last_error()
+    assert L.gq_prepare_q4_0(None, 4, 48, 0, None, None) == lib.GQ_ERR_SHAPE              # K % 32
     assert lib.gq_status_string(-8) == "GQ_ERR_BAD_INDEX"
     old = lib.gq_get_option(lib.GQ_OPT_MOE_PATH)
     with pytest.raises(lib.GQError):
