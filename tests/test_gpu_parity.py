@@ -642,11 +642,14 @@ def test_x_static_chain_after_a_writer_decode():
         assert_mul_mat_close(ys[i].cpu().numpy(), y_ref, s_ref, f"decode projection {i} of the last round")
 
 
-@pytest.mark.parametrize("M,K,N", [(4096, 4096, 512), (11008, 4096, 300), (640, 2048, 64)])
+@pytest.mark.parametrize("M,K,N", [(4096, 4096, 512), (11008, 4096, 300), (640, 2048, 64), (4096, 4096, 16),
+                                   (4096, 11008, 512)])
 def test_x_static_chain_after_a_writer_tensor_core(M, K, N):
     """gq_mul_mat_q4_0_bf16x: X_bf16 is written by the activation conversion
     right before the first projection; the other two carry the promise and
-    may start their MMAs while the kernels ahead of them finish."""
+    may start their MMAs while the kernels ahead of them finish (and run whole
+    256-token tiles, or whole 128-token tiles at 16 tokens, where the first
+    call's plan splits them along k)."""
     Ws = [synth.q4_0_weights(M, K, seed=7920 + i) for i in range(3)]
     Wd = [dev(w) for w in Ws]
     Xfs = [dev(synth.activations(N, K, seed=7930 + r)) for r in range(4)]
